@@ -1,0 +1,201 @@
+"""fp64 CPU oracle for the SDPA backward (test infrastructure).
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` import this package. The GPU library never does, and this package
+imports nothing from it: the two share no code.
+
+The arithmetic lives in ``sdpa_oracle.c`` (plain definitions in double
+precision, see its header for the page sections it follows). This module only
+marshals numpy float64 arrays into it through ctypes.
+
+Layout of every tensor: contiguous (B, H, S, D); LSE and delta are (B, H, S).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import numpy as np
+
+from . import build as _build
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+class _Cfg(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int),
+        ("Sq", ctypes.c_int), ("Skv", ctypes.c_int), ("Dqk", ctypes.c_int), ("Dv", ctypes.c_int),
+        ("scale", ctypes.c_double),
+        ("causal", ctypes.c_int), ("bottom_right", ctypes.c_int),
+        ("window_left", ctypes.c_int), ("window_right", ctypes.c_int),
+        ("seq_q_lens", ctypes.POINTER(ctypes.c_int32)),
+        ("seq_kv_lens", ctypes.POINTER(ctypes.c_int32)),
+    ]
+
+
+@dataclass
+class Problem:
+    """Shape and mask of one attention problem (mirrors the C struct)."""
+    B: int
+    Hq: int
+    Hkv: int
+    Sq: int
+    Skv: int
+    Dqk: int
+    Dv: int
+    scale: Optional[float] = None   # None -> 1/sqrt(Dqk)
+    causal: bool = False
+    bottom_right: bool = False
+    window_left: int = -1
+    window_right: int = -1
+    seq_q_lens: Optional[np.ndarray] = None
+    seq_kv_lens: Optional[np.ndarray] = None
+
+    @property
+    def resolved_scale(self) -> float:
+        return 1.0 / math.sqrt(self.Dqk) if self.scale is None else float(self.scale)
+
+    def _struct(self):
+        keep = []
+
+        def lens(a):
+            if a is None:
+                return ctypes.POINTER(ctypes.c_int32)()
+            arr = np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+            keep.append(arr)
+            return arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+        s = _Cfg(self.B, self.Hq, self.Hkv, self.Sq, self.Skv, self.Dqk, self.Dv,
+                 self.resolved_scale, int(self.causal), int(self.bottom_right),
+                 int(self.window_left), int(self.window_right),
+                 lens(self.seq_q_lens), lens(self.seq_kv_lens))
+        return s, keep
+
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = _build.library_path()
+        if not os.path.exists(path) or _build.is_stale():
+            _build.build()
+        lib = ctypes.CDLL(path)
+        P = ctypes.POINTER(ctypes.c_double)
+        C = ctypes.POINTER(_Cfg)
+        I64 = ctypes.POINTER(ctypes.c_int64)
+        lib.oracle_forward.argtypes = [C, P, P, P, P, P]
+        lib.oracle_delta.argtypes = [C, P, P, P]
+        lib.oracle_backward.argtypes = [C, P, P, P, P, P, P, P, P, P]
+        lib.oracle_backward_sampled.argtypes = [C, P, P, P, P, P, P, ctypes.c_long, I64, P,
+                                                ctypes.c_long, I64, P, P]
+        lib.oracle_count_visible.argtypes = [C]
+        lib.oracle_count_visible.restype = ctypes.c_longlong
+        lib.oracle_max_threads.restype = ctypes.c_int
+        lib.oracle_set_threads.argtypes = [ctypes.c_int]
+        _lib = lib
+    return _lib
+
+
+def _f64(a, shape=None):
+    arr = np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+    if shape is not None and tuple(arr.shape) != tuple(shape):
+        raise ValueError(f"expected shape {tuple(shape)}, got {tuple(arr.shape)}")
+    return arr
+
+
+def _p(a):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _check_heads(p: Problem):
+    if p.Hkv <= 0 or p.Hq % p.Hkv != 0:
+        raise ValueError("H_kv must divide H_q")
+
+
+def forward(p: Problem, q, k, v):
+    """Returns (O, LSE) in float64; LSE is the natural-log row log-sum-exp."""
+    _check_heads(p)
+    lib = _load()
+    q = _f64(q, (p.B, p.Hq, p.Sq, p.Dqk))
+    k = _f64(k, (p.B, p.Hkv, p.Skv, p.Dqk))
+    v = _f64(v, (p.B, p.Hkv, p.Skv, p.Dv))
+    o = np.zeros((p.B, p.Hq, p.Sq, p.Dv))
+    lse = np.zeros((p.B, p.Hq, p.Sq))
+    s, keep = p._struct()
+    lib.oracle_forward(ctypes.byref(s), _p(q), _p(k), _p(v), _p(o), _p(lse))
+    return o, lse
+
+
+def delta(p: Problem, o, do):
+    """delta = rowsum(O * dO), shape (B, Hq, Sq)."""
+    lib = _load()
+    o = _f64(o, (p.B, p.Hq, p.Sq, p.Dv))
+    do = _f64(do, (p.B, p.Hq, p.Sq, p.Dv))
+    out = np.zeros((p.B, p.Hq, p.Sq))
+    s, keep = p._struct()
+    lib.oracle_delta(ctypes.byref(s), _p(o), _p(do), _p(out))
+    return out
+
+
+def backward(p: Problem, q, k, v, o, do, lse):
+    """Returns (dQ, dK, dV) in float64 from the given forward tensors."""
+    _check_heads(p)
+    lib = _load()
+    q = _f64(q, (p.B, p.Hq, p.Sq, p.Dqk))
+    k = _f64(k, (p.B, p.Hkv, p.Skv, p.Dqk))
+    v = _f64(v, (p.B, p.Hkv, p.Skv, p.Dv))
+    o = _f64(o, (p.B, p.Hq, p.Sq, p.Dv))
+    do = _f64(do, (p.B, p.Hq, p.Sq, p.Dv))
+    lse = _f64(lse, (p.B, p.Hq, p.Sq))
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    s, keep = p._struct()
+    lib.oracle_backward(ctypes.byref(s), _p(q), _p(k), _p(v), _p(o), _p(do), _p(lse),
+                        _p(dq), _p(dk), _p(dv))
+    return dq, dk, dv
+
+
+def backward_sampled(p: Problem, q, k, v, o, do, lse, q_rows, kv_rows):
+    """dQ at the flat query rows ``q_rows`` ((b*Hq + h)*Sq + q) and dK/dV at the
+    flat key rows ``kv_rows`` ((b*Hkv + hk)*Skv + k). Returns three 2-D arrays."""
+    _check_heads(p)
+    lib = _load()
+    q = _f64(q, (p.B, p.Hq, p.Sq, p.Dqk))
+    k = _f64(k, (p.B, p.Hkv, p.Skv, p.Dqk))
+    v = _f64(v, (p.B, p.Hkv, p.Skv, p.Dv))
+    o = _f64(o, (p.B, p.Hq, p.Sq, p.Dv))
+    do = _f64(do, (p.B, p.Hq, p.Sq, p.Dv))
+    lse = _f64(lse, (p.B, p.Hq, p.Sq))
+    qi = np.ascontiguousarray(np.asarray(q_rows, dtype=np.int64))
+    ki = np.ascontiguousarray(np.asarray(kv_rows, dtype=np.int64))
+    dq = np.zeros((len(qi), p.Dqk))
+    dk = np.zeros((len(ki), p.Dqk))
+    dv = np.zeros((len(ki), p.Dv))
+    s, keep = p._struct()
+    I64 = ctypes.POINTER(ctypes.c_int64)
+    lib.oracle_backward_sampled(ctypes.byref(s), _p(q), _p(k), _p(v), _p(o), _p(do), _p(lse),
+                                len(qi), qi.ctypes.data_as(I64), _p(dq),
+                                len(ki), ki.ctypes.data_as(I64), _p(dk), _p(dv))
+    return dq, dk, dv
+
+
+def count_visible(p: Problem) -> int:
+    """Visible (q, k) pairs summed over batches and query heads."""
+    lib = _load()
+    s, keep = p._struct()
+    return int(lib.oracle_count_visible(ctypes.byref(s)))
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def set_threads(n: int) -> None:
+    _load().oracle_set_threads(int(n))

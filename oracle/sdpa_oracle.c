@@ -1,0 +1,258 @@
+/*
+ * sdpa_oracle.c -- plain, slow, fp64 CPU reference for scaled-dot-product
+ * attention: the forward (O, LSE) and the backward (dQ, dK, dV).
+ *
+ * TEST INFRASTRUCTURE. Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg load this library. The GPU library shares no
+ * code, header, table or helper with it, and neither side includes the other.
+ *
+ * Source of the arithmetic ("SDPA Backward (SM120)" page of the cuDNN
+ * frontend docs):
+ *   - API Usage: tensors are logical (B, H, S, D); `stats` is the natural-log
+ *     forward LSE; scale defaults to 1/sqrt(D); K/V carry H_kv heads and
+ *     H_kv divides H_q (GQA/MQA).
+ *   - Main-kernel pipeline: P replayed from LSE, dP = dO V^T,
+ *     delta = rowsum(O * dO), dS = P * (dP - delta), dV = P^T dO,
+ *     dQ = scale * dS K, dK = scale * dS^T Q.
+ *   - GQA/MQA group reduction: the KV head of query head h is h / group and
+ *     dK/dV of a KV head sum over the query heads of its group.
+ *   - Causal, sliding-window, and padding masks: diag = 0 (top-left) or
+ *     L_kv - L_q (bottom-right, anchored at the actual lengths); causal keeps
+ *     k <= q + diag + R; a left window masks k < q + diag - W; keys at or past
+ *     seq_kv_lens[b] and queries at or past seq_q_lens[b] are masked; a row
+ *     with no visible key has LSE = -inf and gets P = 0 (not NaN).
+ *
+ * Every quantity is computed straight from its definition, one output row at
+ * a time, in double precision. There is no tiling, fusion or reordering.
+ * Rows are independent, so OpenMP splits the row loops across threads; each
+ * output element is written by exactly one thread.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+typedef struct {
+    int B, Hq, Hkv, Sq, Skv, Dqk, Dv;
+    double scale;         /* applied to Q.K; the caller resolves the default */
+    int causal;           /* 1: keep k <= q + diag + max(R, 0)               */
+    int bottom_right;     /* 1: diag = L_kv - L_q, else diag = 0             */
+    int window_left;      /* W >= 0: mask k < q + diag - W; < 0: no window   */
+    int window_right;     /* R: widens the causal diagonal; < 0 means 0      */
+    const int32_t *seq_q_lens;   /* (B,) or NULL: every row is S_q long     */
+    const int32_t *seq_kv_lens;  /* (B,) or NULL: every row is S_kv long    */
+} oracle_cfg;
+
+/* ---- the mask predicate ("Causal, sliding-window, and padding masks") ---- */
+
+static void lengths(const oracle_cfg *c, int b, int *Lq, int *Lk) {
+    *Lq = c->seq_q_lens ? c->seq_q_lens[b] : c->Sq;
+    *Lk = c->seq_kv_lens ? c->seq_kv_lens[b] : c->Skv;
+    if (*Lq > c->Sq) *Lq = c->Sq;
+    if (*Lk > c->Skv) *Lk = c->Skv;
+    if (*Lq < 0) *Lq = 0;
+    if (*Lk < 0) *Lk = 0;
+}
+
+static int visible(const oracle_cfg *c, int Lq, int Lk, long q, long k) {
+    long diag = c->bottom_right ? (long)Lk - (long)Lq : 0;
+    if (q >= Lq || k >= Lk) return 0;
+    if (c->causal) {
+        long R = c->window_right > 0 ? c->window_right : 0;
+        if (k > q + diag + R) return 0;
+    }
+    if (c->window_left >= 0 && k < q + diag - c->window_left) return 0;
+    return 1;
+}
+
+/* ---- index helpers: contiguous (B, H, S, D) ---- */
+
+static inline const double *row_of(const double *t, long bh, long s, long S, long D) {
+    return t + (bh * S + s) * D;
+}
+
+static double dot(const double *a, const double *b, int n) {
+    double acc = 0.0;
+    for (int i = 0; i < n; ++i) acc += a[i] * b[i];
+    return acc;
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void oracle_set_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+/* Number of visible (q, k) pairs summed over batches and query heads. */
+long long oracle_count_visible(const oracle_cfg *c) {
+    long long total = 0;
+    for (int b = 0; b < c->B; ++b) {
+        int Lq, Lk;
+        lengths(c, b, &Lq, &Lk);
+        long long per_head = 0;
+        for (long q = 0; q < c->Sq; ++q)
+            for (long k = 0; k < c->Skv; ++k) per_head += visible(c, Lq, Lk, q, k);
+        total += per_head * c->Hq;
+    }
+    return total;
+}
+
+/* Forward: LSE_q = log sum_{visible k} exp(s_qk), s_qk = scale * Q_q . K_k;
+ * O_q = sum_k exp(s_qk - LSE_q) V_k. An empty row gives LSE = -inf, O = 0. */
+void oracle_forward(const oracle_cfg *c, const double *Q, const double *K, const double *V,
+                    double *O, double *LSE) {
+    const int G = c->Hq / c->Hkv;
+    const long rows = (long)c->B * c->Hq * c->Sq;
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(c->Skv > 0 ? c->Skv : 1));
+#pragma omp for schedule(dynamic, 16)
+        for (long r = 0; r < rows; ++r) {
+            long q = r % c->Sq, bh = r / c->Sq;
+            int b = (int)(bh / c->Hq), h = (int)(bh % c->Hq);
+            long bhk = (long)b * c->Hkv + h / G;
+            int Lq, Lk;
+            lengths(c, b, &Lq, &Lk);
+            const double *qr = row_of(Q, bh, q, c->Sq, c->Dqk);
+            double *orow = O + r * c->Dv;
+            double m = -INFINITY;
+            for (long k = 0; k < c->Skv; ++k) {
+                if (!visible(c, Lq, Lk, q, k)) continue;
+                s[k] = c->scale * dot(qr, row_of(K, bhk, k, c->Skv, c->Dqk), c->Dqk);
+                if (s[k] > m) m = s[k];
+            }
+            for (int d = 0; d < c->Dv; ++d) orow[d] = 0.0;
+            if (m == -INFINITY) { LSE[r] = -INFINITY; continue; }
+            double l = 0.0;
+            for (long k = 0; k < c->Skv; ++k)
+                if (visible(c, Lq, Lk, q, k)) l += exp(s[k] - m);
+            double lse = m + log(l);
+            LSE[r] = lse;
+            for (long k = 0; k < c->Skv; ++k) {
+                if (!visible(c, Lq, Lk, q, k)) continue;
+                double p = exp(s[k] - lse);
+                const double *vr = row_of(V, bhk, k, c->Skv, c->Dv);
+                for (int d = 0; d < c->Dv; ++d) orow[d] += p * vr[d];
+            }
+        }
+        free(s);
+    }
+}
+
+/* delta_q = sum_d dO[q, d] * O[q, d] ("dot" step of the kernel chain). */
+void oracle_delta(const oracle_cfg *c, const double *O, const double *dO, double *delta) {
+    const long rows = (long)c->B * c->Hq * c->Sq;
+#pragma omp parallel for schedule(static)
+    for (long r = 0; r < rows; ++r) delta[r] = dot(O + r * c->Dv, dO + r * c->Dv, c->Dv);
+}
+
+/* P_qk replayed from the given LSE; zero when masked or when LSE = -inf. */
+static double prob(const oracle_cfg *c, double s, double lse) {
+    (void)c;
+    if (lse == -INFINITY) return 0.0;
+    return exp(s - lse);
+}
+
+/* dQ row (b, h, q): scale * sum_k dS_qk K_k with dS_qk = P_qk (dP_qk - delta_q). */
+static void dq_row(const oracle_cfg *c, const double *Q, const double *K, const double *V,
+                   const double *dO, const double *LSE, const double *delta, long bh, long q,
+                   double *out) {
+    const int G = c->Hq / c->Hkv;
+    int b = (int)(bh / c->Hq), h = (int)(bh % c->Hq);
+    long bhk = (long)b * c->Hkv + h / G;
+    int Lq, Lk;
+    lengths(c, b, &Lq, &Lk);
+    const double *qr = row_of(Q, bh, q, c->Sq, c->Dqk);
+    const double *dor = row_of(dO, bh, q, c->Sq, c->Dv);
+    double lse = LSE[bh * c->Sq + q], D = delta[bh * c->Sq + q];
+    for (int d = 0; d < c->Dqk; ++d) out[d] = 0.0;
+    for (long k = 0; k < c->Skv; ++k) {
+        if (!visible(c, Lq, Lk, q, k)) continue;
+        const double *kr = row_of(K, bhk, k, c->Skv, c->Dqk);
+        double p = prob(c, c->scale * dot(qr, kr, c->Dqk), lse);
+        double dp = dot(dor, row_of(V, bhk, k, c->Skv, c->Dv), c->Dv);
+        double ds = p * (dp - D);
+        for (int d = 0; d < c->Dqk; ++d) out[d] += ds * kr[d];
+    }
+    for (int d = 0; d < c->Dqk; ++d) out[d] *= c->scale;
+}
+
+/* dK, dV row (b, hk, k): sums over every query head of the KV head's group and
+ * every visible query: dK_k = scale * sum dS_qk Q_q, dV_k = sum P_qk dO_q. */
+static void dkv_row(const oracle_cfg *c, const double *Q, const double *K, const double *V,
+                    const double *dO, const double *LSE, const double *delta, long bhk, long k,
+                    double *dk_out, double *dv_out) {
+    const int G = c->Hq / c->Hkv;
+    int b = (int)(bhk / c->Hkv), hk = (int)(bhk % c->Hkv);
+    int Lq, Lk;
+    lengths(c, b, &Lq, &Lk);
+    const double *kr = row_of(K, bhk, k, c->Skv, c->Dqk);
+    const double *vr = row_of(V, bhk, k, c->Skv, c->Dv);
+    for (int d = 0; d < c->Dqk; ++d) dk_out[d] = 0.0;
+    for (int d = 0; d < c->Dv; ++d) dv_out[d] = 0.0;
+    for (int j = 0; j < G; ++j) {
+        long bh = (long)b * c->Hq + (long)hk * G + j;
+        for (long q = 0; q < c->Sq; ++q) {
+            if (!visible(c, Lq, Lk, q, k)) continue;
+            const double *qr = row_of(Q, bh, q, c->Sq, c->Dqk);
+            const double *dor = row_of(dO, bh, q, c->Sq, c->Dv);
+            double p = prob(c, c->scale * dot(qr, kr, c->Dqk), LSE[bh * c->Sq + q]);
+            double dp = dot(dor, vr, c->Dv);
+            double ds = p * (dp - delta[bh * c->Sq + q]);
+            for (int d = 0; d < c->Dqk; ++d) dk_out[d] += ds * qr[d];
+            for (int d = 0; d < c->Dv; ++d) dv_out[d] += p * dor[d];
+        }
+    }
+    for (int d = 0; d < c->Dqk; ++d) dk_out[d] *= c->scale;
+}
+
+/* Full backward: every dQ row and every dK/dV row. */
+void oracle_backward(const oracle_cfg *c, const double *Q, const double *K, const double *V,
+                     const double *O, const double *dO, const double *LSE, double *dQ,
+                     double *dK, double *dV) {
+    const long qrows = (long)c->B * c->Hq * c->Sq;
+    const long krows = (long)c->B * c->Hkv * c->Skv;
+    double *delta = (double *)malloc(sizeof(double) * (size_t)(qrows > 0 ? qrows : 1));
+    oracle_delta(c, O, dO, delta);
+#pragma omp parallel for schedule(dynamic, 8)
+    for (long r = 0; r < qrows; ++r)
+        dq_row(c, Q, K, V, dO, LSE, delta, r / c->Sq, r % c->Sq, dQ + r * c->Dqk);
+#pragma omp parallel for schedule(dynamic, 8)
+    for (long r = 0; r < krows; ++r)
+        dkv_row(c, Q, K, V, dO, LSE, delta, r / c->Skv, r % c->Skv, dK + r * c->Dqk,
+                dV + r * c->Dv);
+    free(delta);
+}
+
+/* Sampled backward: dQ at the flat query-row indices q_idx ((b*Hq + h)*Sq + q)
+ * and dK/dV at the flat key-row indices k_idx ((b*Hkv + hk)*Skv + k). */
+void oracle_backward_sampled(const oracle_cfg *c, const double *Q, const double *K,
+                             const double *V, const double *O, const double *dO,
+                             const double *LSE, long n_q, const int64_t *q_idx, double *dQ_rows,
+                             long n_k, const int64_t *k_idx, double *dK_rows, double *dV_rows) {
+    const long qrows = (long)c->B * c->Hq * c->Sq;
+    double *delta = (double *)malloc(sizeof(double) * (size_t)(qrows > 0 ? qrows : 1));
+    oracle_delta(c, O, dO, delta);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long i = 0; i < n_q; ++i)
+        dq_row(c, Q, K, V, dO, LSE, delta, q_idx[i] / c->Sq, q_idx[i] % c->Sq,
+               dQ_rows + i * c->Dqk);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long i = 0; i < n_k; ++i)
+        dkv_row(c, Q, K, V, dO, LSE, delta, k_idx[i] / c->Skv, k_idx[i] % c->Skv,
+                dK_rows + i * c->Dqk, dV_rows + i * c->Dv);
+    free(delta);
+}

@@ -1,0 +1,309 @@
+"""Pins for the fp64 oracle, independent of the oracle itself.
+
+Each check below fixes the oracle to something it does not compute the same
+way: central finite differences of its own forward, algebraic invariants,
+closed forms worked by hand, brute-force counts against closed forms, and a
+float64 autograd run of torch's scaled_dot_product_attention (a library
+special case). A dropped delta term, a wrong sign, a transposed operand or an
+off-by-one in a mask edge each fails at least one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import Problem
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def _rand(rng, *shape):
+    return rng.standard_normal(shape)
+
+
+def _inputs(p: Problem, seed=0, qscale=1.0):
+    rng = np.random.default_rng(seed)
+    q = _rand(rng, p.B, p.Hq, p.Sq, p.Dqk) * qscale
+    k = _rand(rng, p.B, p.Hkv, p.Skv, p.Dqk)
+    v = _rand(rng, p.B, p.Hkv, p.Skv, p.Dv)
+    do = _rand(rng, p.B, p.Hq, p.Sq, p.Dv)
+    return q, k, v, do
+
+
+# Tiny problems spanning every mask kind, GQA/MQA, S_q != S_kv and D_qk != D_v.
+FD_CASES = {
+    "dense": Problem(1, 2, 2, 5, 7, 4, 3),
+    "causal_tl": Problem(1, 2, 1, 6, 6, 4, 4, causal=True),
+    "causal_br_long_q": Problem(1, 2, 2, 7, 4, 3, 5, causal=True, bottom_right=True),
+    "causal_br_long_kv": Problem(1, 2, 2, 4, 9, 5, 3, causal=True, bottom_right=True),
+    "causal_band_r2": Problem(1, 2, 2, 6, 8, 4, 4, causal=True, window_right=2),
+    "window_causal": Problem(1, 2, 2, 8, 8, 4, 3, causal=True, window_left=2),
+    "window_only": Problem(1, 2, 2, 7, 9, 3, 3, window_left=3, bottom_right=True),
+    "padded": Problem(2, 2, 2, 6, 7, 4, 4, causal=True, bottom_right=True,
+                      seq_q_lens=np.array([4, 6]), seq_kv_lens=np.array([5, 3])),
+    "gqa": Problem(1, 4, 2, 5, 6, 4, 4, causal=True),
+    "mqa_scale": Problem(1, 3, 1, 5, 5, 6, 4, scale=0.37),
+}
+
+
+def _loss(oracle_mod, p, q, k, v, do):
+    o, _ = oracle_mod.forward(p, q, k, v)
+    return float(np.sum(o * do))
+
+
+@pytest.mark.parametrize("name", sorted(FD_CASES))
+def test_backward_matches_central_differences(oracle_mod, name):
+    """dL/dQ, dL/dK, dL/dV of L = sum(O * dO) by central differences of the forward."""
+    p = FD_CASES[name]
+    q, k, v, do = _inputs(p, seed=sum(map(ord, name)))
+    o, lse = oracle_mod.forward(p, q, k, v)
+    dq, dk, dv = oracle_mod.backward(p, q, k, v, o, do, lse)
+    h = 1e-6
+    for tensor, grad, which in ((q, dq, "q"), (k, dk, "k"), (v, dv, "v")):
+        fd = np.zeros_like(tensor)
+        it = np.nditer(tensor, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            args = {"q": q, "k": k, "v": v}
+            plus = tensor.copy()
+            plus[idx] += h
+            minus = tensor.copy()
+            minus[idx] -= h
+            args[which] = plus
+            lp = _loss(oracle_mod, p, args["q"], args["k"], args["v"], do)
+            args[which] = minus
+            lm = _loss(oracle_mod, p, args["q"], args["k"], args["v"], do)
+            fd[idx] = (lp - lm) / (2 * h)
+        scale = max(1.0, float(np.abs(fd).max()))
+        np.testing.assert_allclose(grad, fd, rtol=0, atol=2e-7 * scale, err_msg=f"d{which}")
+
+
+@pytest.mark.parametrize("name", ["dense", "causal_br_long_q", "padded", "gqa", "window_causal"])
+def test_row_sum_invariants(oracle_mod, name):
+    """With exact O: each row of dS sums to 0, so sum_k dK_k = 0 per (b, kv head);
+    and sum_k dV_k equals the sum of dO over the group's non-empty query rows."""
+    p = FD_CASES[name]
+    q, k, v, do = _inputs(p, seed=3)
+    o, lse = oracle_mod.forward(p, q, k, v)
+    dq, dk, dv = oracle_mod.backward(p, q, k, v, o, do, lse)
+    G = p.Hq // p.Hkv
+    nonempty = np.isfinite(lse)
+    for b in range(p.B):
+        for hk in range(p.Hkv):
+            np.testing.assert_allclose(dk[b, hk].sum(0), 0.0, atol=1e-12)
+            heads = range(hk * G, hk * G + G)
+            expect = sum(do[b, h][nonempty[b, h]].sum(0) for h in heads)
+            np.testing.assert_allclose(dv[b, hk].sum(0), expect, atol=1e-12)
+
+
+def test_dq_invariant_under_key_shift(oracle_mod):
+    """Adding one vector c to every key row shifts each score row by a constant,
+    so P is unchanged and (rows of dS summing to 0) dQ is unchanged."""
+    p = Problem(1, 2, 2, 6, 9, 5, 4, causal=True, bottom_right=True)
+    q, k, v, do = _inputs(p, seed=7)
+    c = np.random.default_rng(1).standard_normal(p.Dqk)
+    res = []
+    for kk in (k, k + c):
+        o, lse = oracle_mod.forward(p, q, kk, v)
+        res.append(oracle_mod.backward(p, q, kk, v, o, do, lse))
+    np.testing.assert_allclose(res[0][0], res[1][0], atol=1e-11)
+    np.testing.assert_allclose(res[0][2], res[1][2], atol=1e-11)
+
+
+def test_gqa_equals_replicated_mha(oracle_mod):
+    """GQA with H_kv heads == MHA with each KV head repeated G times (query head h
+    reads KV head h // G); dK/dV of a KV head == the sum over its group."""
+    G, Hkv = 3, 2
+    pg = Problem(2, G * Hkv, Hkv, 6, 7, 4, 5, causal=True, bottom_right=True)
+    pm = Problem(2, G * Hkv, G * Hkv, 6, 7, 4, 5, causal=True, bottom_right=True)
+    q, k, v, do = _inputs(pg, seed=11)
+    kr, vr = np.repeat(k, G, axis=1), np.repeat(v, G, axis=1)
+    og, lg = oracle_mod.forward(pg, q, k, v)
+    om, lm = oracle_mod.forward(pm, q, kr, vr)
+    np.testing.assert_allclose(og, om, atol=1e-13)
+    np.testing.assert_allclose(lg, lm, atol=1e-13)
+    dqg, dkg, dvg = oracle_mod.backward(pg, q, k, v, og, do, lg)
+    dqm, dkm, dvm = oracle_mod.backward(pm, q, kr, vr, om, do, lm)
+    np.testing.assert_allclose(dqg, dqm, atol=1e-13)
+    np.testing.assert_allclose(dkg, dkm.reshape(2, Hkv, G, 7, 4).sum(2), atol=1e-12)
+    np.testing.assert_allclose(dvg, dvm.reshape(2, Hkv, G, 7, 5).sum(2), atol=1e-12)
+
+
+def test_fully_masked_rows_give_exact_zeros(oracle_mod):
+    """Padded query rows and rows left empty by a bottom-right diagonal have
+    LSE = -inf, O = 0 and exactly zero dQ; padded key rows get exactly zero dK/dV."""
+    p = Problem(2, 2, 1, 8, 5, 4, 4, causal=True, bottom_right=True,
+                seq_q_lens=np.array([8, 3]), seq_kv_lens=np.array([5, 2]))
+    q, k, v, do = _inputs(p, seed=5)
+    o, lse = oracle_mod.forward(p, q, k, v)
+    dq, dk, dv = oracle_mod.backward(p, q, k, v, o, do, lse)
+    # b=0: L_q=8, L_kv=5, diag=-3 -> rows q<3 see no key. b=1: L_q=3, L_kv=2, diag=-1.
+    for b, (lq, lk, empty) in enumerate([(8, 5, [0, 1, 2]), (3, 2, [0])]):
+        dead_q = sorted(set(empty) | set(range(lq, 8)))
+        assert np.all(np.isneginf(lse[b][:, dead_q]))
+        assert np.all(o[b][:, dead_q] == 0.0)
+        assert np.all(dq[b][:, dead_q] == 0.0)
+        live = [i for i in range(8) if i not in dead_q]
+        assert np.all(np.isfinite(lse[b][:, live]))
+        assert np.all(dk[b][:, lk:] == 0.0) and np.all(dv[b][:, lk:] == 0.0)
+
+
+def test_single_visible_key_closed_form(oracle_mod):
+    """With one key, P = 1 and dS = 0: dQ = dK = 0 and dV = sum_q dO_q; O = V."""
+    p = Problem(1, 2, 1, 5, 1, 4, 3)
+    q, k, v, do = _inputs(p, seed=2)
+    o, lse = oracle_mod.forward(p, q, k, v)
+    np.testing.assert_allclose(o, np.broadcast_to(v[:, :1], o.shape), atol=1e-15)
+    dq, dk, dv = oracle_mod.backward(p, q, k, v, o, do, lse)
+    assert np.abs(dq).max() < 1e-15 and np.abs(dk).max() < 1e-15
+    np.testing.assert_allclose(dv[0, 0, 0], do[0].sum(axis=(0, 1)), atol=1e-13)
+
+
+def test_zero_query_gives_uniform_attention(oracle_mod):
+    """Q = 0 makes every visible score 0, so O_q is the mean of the visible V rows
+    and LSE_q = log(number of visible keys)."""
+    p = Problem(1, 1, 1, 4, 6, 3, 2, causal=True, bottom_right=True)
+    _, k, v, _ = _inputs(p, seed=4)
+    q = np.zeros((1, 1, 4, 3))
+    o, lse = oracle_mod.forward(p, q, k, v)
+    for i in range(4):
+        n = i + 3  # diag = 2: row i sees keys 0..i+2
+        np.testing.assert_allclose(o[0, 0, i], v[0, 0, :n].mean(0), atol=1e-15)
+        assert abs(lse[0, 0, i] - math.log(n)) < 1e-15
+
+
+def test_two_keys_worked_by_hand(oracle_mod):
+    g = json.load(open(os.path.join(HERE, "golden", "two_keys_by_hand.json")))
+    p = Problem(1, 1, 1, 1, 2, 1, 1, scale=1.0)
+    i = g["inputs"]
+    q = np.array(i["q"]).reshape(1, 1, 1, 1)
+    k = np.array(i["k"]).reshape(1, 1, 2, 1)
+    v = np.array(i["v"]).reshape(1, 1, 2, 1)
+    do = np.array(i["do"]).reshape(1, 1, 1, 1)
+    o, lse = oracle_mod.forward(p, q, k, v)
+    e = g["expected"]
+    assert abs(lse.item() - e["lse"]) < 1e-14 and abs(o.item() - e["o"]) < 1e-14
+    dq, dk, dv = oracle_mod.backward(p, q, k, v, o, do, lse)
+    assert abs(dq.item() - e["dq"]) < 1e-14
+    np.testing.assert_allclose(dk.ravel(), e["dk"], atol=1e-14)
+    np.testing.assert_allclose(dv.ravel(), e["dv"], atol=1e-14)
+
+
+def _pairs_causal_window(L, W):
+    """Visible pairs of one head, square causal top-left with left window W, length L:
+    row q sees min(q + 1, W + 1) keys."""
+    if L <= W + 1:
+        return L * (L + 1) // 2
+    return (W + 1) * (W + 2) // 2 + (L - W - 1) * (W + 1)
+
+
+def test_visible_counts_match_closed_forms(oracle_mod):
+    # Square top-left causal: S(S+1)/2 per head.
+    p = Problem(2, 3, 3, 37, 37, 8, 8, causal=True)
+    assert oracle_mod.count_visible(p) == 2 * 3 * 37 * 38 // 2
+    # Bottom-right causal, S_q < S_kv: row q sees q + (S_kv - S_q) + 1 keys.
+    p = Problem(1, 2, 1, 5, 12, 8, 8, causal=True, bottom_right=True)
+    assert oracle_mod.count_visible(p) == 2 * sum(q + 7 + 1 for q in range(5))
+    # Right band R = 3 on a square causal mask: row q sees min(q + 4, S) keys.
+    p = Problem(1, 1, 1, 10, 10, 8, 8, causal=True, window_right=3)
+    assert oracle_mod.count_visible(p) == sum(min(q + 4, 10) for q in range(10))
+    # Causal + left window W with padding: closed form per batch length.
+    lens = np.array([40, 200, 65, 129])
+    p = Problem(4, 2, 2, 200, 200, 8, 8, causal=True, window_left=64,
+                seq_q_lens=lens, seq_kv_lens=lens)
+    assert oracle_mod.count_visible(p) == 2 * sum(_pairs_causal_window(int(L), 64) for L in lens)
+    # Window with W = 1 and top-left causal: every row but the first sees 2 keys.
+    p = Problem(1, 1, 1, 9, 9, 8, 8, causal=True, window_left=1)
+    assert oracle_mod.count_visible(p) == 2 * 9 - 1
+    # Non-causal left window only (keys to the right stay visible).
+    p = Problem(1, 1, 1, 6, 6, 8, 8, window_left=2)
+    assert oracle_mod.count_visible(p) == sum(6 - max(0, q - 2) for q in range(6))
+
+
+def _torch_mask(p: Problem):
+    """Boolean (B, 1, Sq, Skv) mask from tril/triu bands of torch (not the oracle's predicate)."""
+    masks = []
+    for b in range(p.B):
+        Lq = p.Sq if p.seq_q_lens is None else int(p.seq_q_lens[b])
+        Lk = p.Skv if p.seq_kv_lens is None else int(p.seq_kv_lens[b])
+        diag = (Lk - Lq) if p.bottom_right else 0
+        m = torch.ones(p.Sq, p.Skv, dtype=torch.bool)
+        if p.causal:
+            m &= torch.ones(p.Sq, p.Skv, dtype=torch.bool).tril(diag + max(p.window_right, 0))
+        if p.window_left >= 0:
+            m &= torch.ones(p.Sq, p.Skv, dtype=torch.bool).triu(diag - p.window_left)
+        m[Lq:, :] = False
+        m[:, Lk:] = False
+        masks.append(m)
+    return torch.stack(masks)[:, None]
+
+
+@pytest.mark.parametrize("name", ["dense", "causal_tl", "causal_br_long_kv", "window_causal",
+                                  "window_only", "padded", "gqa", "mqa_scale", "causal_band_r2"])
+def test_matches_torch_sdpa_float64(oracle_mod, name):
+    """Forward and backward against torch SDPA in float64 with autograd, on rows
+    that see at least one key (torch returns NaN on empty rows)."""
+    p = FD_CASES[name]
+    q, k, v, do = _inputs(p, seed=9)
+    o, lse = oracle_mod.forward(p, q, k, v)
+    dq, dk, dv = oracle_mod.backward(p, q, k, v, o, do, lse)
+    G = p.Hq // p.Hkv
+    tq = torch.tensor(q, requires_grad=True)
+    tk = torch.tensor(k, requires_grad=True)
+    tv = torch.tensor(v, requires_grad=True)
+    mask = _torch_mask(p)
+    rows = mask.any(-1)  # (B, 1, Sq)
+    out = torch.nn.functional.scaled_dot_product_attention(
+        tq, tk.repeat_interleave(G, 1), tv.repeat_interleave(G, 1), attn_mask=mask,
+        scale=p.resolved_scale)
+    live = rows.expand(-1, p.Hq, -1)
+    tdo = torch.tensor(do) * live[..., None]
+    out = torch.where(live[..., None], out, torch.zeros_like(out))
+    (out * tdo).sum().backward()
+    np.testing.assert_allclose(o, out.detach().numpy(), atol=1e-12)
+    scores = (tq.detach() @ tk.detach().repeat_interleave(G, 1).transpose(-1, -2)) * p.resolved_scale
+    tl = torch.logsumexp(scores.masked_fill(~mask, float("-inf")), -1)
+    np.testing.assert_allclose(lse[live.numpy()], tl[live].numpy(), atol=1e-12)
+    # The oracle's dO on empty rows does not matter (P = 0 there); zero it to compare.
+    do_live = do * live[..., None].numpy()
+    dq2, dk2, dv2 = oracle_mod.backward(p, q, k, v, o, do_live, lse)
+    np.testing.assert_allclose(dq2, tq.grad.numpy(), atol=1e-11)
+    np.testing.assert_allclose(dk2, tk.grad.numpy(), atol=1e-11)
+    np.testing.assert_allclose(dv2, tv.grad.numpy(), atol=1e-11)
+    np.testing.assert_allclose(dq, dq2, atol=1e-12)  # dO on empty rows has no effect
+
+
+def test_sampled_rows_equal_full_backward(oracle_mod):
+    p = FD_CASES["padded"]
+    q, k, v, do = _inputs(p, seed=13)
+    o, lse = oracle_mod.forward(p, q, k, v)
+    dq, dk, dv = oracle_mod.backward(p, q, k, v, o, do, lse)
+    qi = np.array([0, 5, 7, 13, 23])
+    ki = np.array([1, 6, 9, 27])
+    sq, sk, sv = oracle_mod.backward_sampled(p, q, k, v, o, do, lse, qi, ki)
+    np.testing.assert_array_equal(sq, dq.reshape(-1, p.Dqk)[qi])
+    np.testing.assert_array_equal(sk, dk.reshape(-1, p.Dqk)[ki])
+    np.testing.assert_array_equal(sv, dv.reshape(-1, p.Dv)[ki])
+
+
+def test_negative_infinite_lse_gives_zero_probability(oracle_mod):
+    """A row whose given LSE is -inf replays P = 0 (not NaN/inf) even when keys are
+    visible: its dQ is exactly 0 and it adds nothing to dK/dV (same result as
+    zeroing that row's dO)."""
+    p = Problem(1, 2, 1, 5, 6, 4, 4, causal=True, bottom_right=True)
+    q, k, v, do = _inputs(p, seed=21)
+    o, lse = oracle_mod.forward(p, q, k, v)
+    lse_cut = lse.copy()
+    lse_cut[0, 1, 3] = -np.inf
+    dq, dk, dv = oracle_mod.backward(p, q, k, v, o, do, lse_cut)
+    assert np.all(np.isfinite(dq)) and np.all(np.isfinite(dk)) and np.all(np.isfinite(dv))
+    assert np.all(dq[0, 1, 3] == 0.0)
+    do_cut = do.copy()
+    do_cut[0, 1, 3] = 0.0
+    _, dk_ref, dv_ref = oracle_mod.backward(p, q, k, v, o, do_cut, lse)
+    # with dO zeroed the row still has P != 0 but dP = 0 and delta = 0, so dS = 0 and P*dO = 0
+    np.testing.assert_allclose(dk, dk_ref, atol=1e-13)
+    np.testing.assert_allclose(dv, dv_ref, atol=1e-13)
