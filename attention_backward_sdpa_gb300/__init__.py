@@ -1,0 +1,173 @@
+"""GB300 (sm_103a) scaled-dot-product-attention backward.
+
+A thin ctypes binding over ``libsdpa_bwd.so`` (C ABI in ``include/sdpa_bwd.h``).
+Every step of the backward runs in the library's CUDA kernels; this module
+only checks tensor properties and passes pointers, sizes and the current CUDA
+stream. PyTorch is used for device memory and streams.
+
+There is no fallback: if the library cannot be loaded, or the device is not
+an sm_103 GPU, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Tuple
+
+import torch
+
+from . import _build
+
+__all__ = ["sdpa_bwd", "workspace_size", "check_device_status", "profile_enable", "profile_read",
+           "library_path", "load", "SdpaError", "KERNEL_NAMES"]
+
+KERNEL_NAMES = ("preprocess", "main", "gqa_reduce", "dq_convert")
+
+_STATUS = {0: "SDPA_OK", 1: "SDPA_ERR_INVALID", 2: "SDPA_ERR_UNSUPPORTED", 3: "SDPA_ERR_ALIGN",
+           4: "SDPA_ERR_WORKSPACE", 5: "SDPA_ERR_CUDA", 6: "SDPA_ERR_TIMEOUT"}
+
+
+class SdpaError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {_STATUS.get(code, code)} ({_lib_status_string(code)})")
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False):
+    """Loads libsdpa_bwd.so (optionally building it first) and declares its ABI."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if build_if_missing and (not os.path.exists(path) or _build.is_stale()):
+        _build.build()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `python -m attention_backward_sdpa_gb300._build`"
+                           " (or __graft_entry__.build())")
+    lib = ctypes.CDLL(path)
+    vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.sdpa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, ctypes.c_float,
+                             i, i, i, i, i, vp, vp, vp, sz, vp]
+    lib.sdpa_bwd.restype = i
+    lib.sdpa_bwd_workspace_size.argtypes = [i, i, i, i, i, i, i, i]
+    lib.sdpa_bwd_workspace_size.restype = sz
+    lib.sdpa_status_string.argtypes = [i]
+    lib.sdpa_status_string.restype = ctypes.c_char_p
+    lib.sdpa_bwd_check_device_status.argtypes = [vp]
+    lib.sdpa_bwd_check_device_status.restype = i
+    lib.sdpa_bwd_profile_enable.argtypes = [i]
+    lib.sdpa_bwd_profile_enable.restype = i
+    lib.sdpa_bwd_profile_read.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int), i]
+    lib.sdpa_bwd_profile_read.restype = i
+    lib.sdpa_bwd_version.restype = i
+    _lib = lib
+    return lib
+
+
+def _lib_status_string(code: int) -> str:
+    try:
+        return load().sdpa_status_string(code).decode()
+    except Exception:  # pragma: no cover - only used while formatting an error
+        return "?"
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream]):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def workspace_size(B, Hq, Hkv, Sq, Skv, Dqk, Dv, deterministic=False) -> int:
+    return int(load().sdpa_bwd_workspace_size(B, Hq, Hkv, Sq, Skv, Dqk, Dv, int(deterministic)))
+
+
+def _check_bf16(name, t, shape):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def sdpa_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, do: torch.Tensor,
+             lse: torch.Tensor, *, scale: Optional[float] = None, causal: bool = False,
+             bottom_right: bool = False, window_left: int = -1, window_right: int = -1,
+             deterministic: bool = False, seq_q_lens: Optional[torch.Tensor] = None,
+             seq_kv_lens: Optional[torch.Tensor] = None, dq: Optional[torch.Tensor] = None,
+             dk: Optional[torch.Tensor] = None, dv: Optional[torch.Tensor] = None,
+             workspace: Optional[torch.Tensor] = None,
+             stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """dQ, dK, dV of scaled-dot-product attention (see include/sdpa_bwd.h).
+
+    q (B,Hq,Sq,Dqk), k (B,Hkv,Skv,Dqk), v (B,Hkv,Skv,Dv), o/do (B,Hq,Sq,Dv): bf16 CUDA,
+    contiguous. lse (B,Hq,Sq) fp32 natural-log forward statistic. Lengths: int32 (B,) CUDA.
+    Outputs are allocated when not given. Runs on ``stream`` (default: current stream).
+    """
+    lib = load()
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be (B, H, S, D)")
+    B, Hq, Sq, Dqk = q.shape
+    Hkv, Skv = k.shape[1], k.shape[2]
+    Dv = v.shape[3]
+    _check_bf16("q", q, (B, Hq, Sq, Dqk))
+    _check_bf16("k", k, (B, Hkv, Skv, Dqk))
+    _check_bf16("v", v, (B, Hkv, Skv, Dv))
+    _check_bf16("o", o, (B, Hq, Sq, Dv))
+    _check_bf16("do", do, (B, Hq, Sq, Dv))
+    if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous() \
+            or lse.numel() != B * Hq * Sq:
+        raise ValueError("lse must be a contiguous fp32 CUDA tensor with B*Hq*Sq elements")
+    for name, lens in (("seq_q_lens", seq_q_lens), ("seq_kv_lens", seq_kv_lens)):
+        if lens is not None and (lens.dtype != torch.int32 or not lens.is_cuda or lens.numel() != B
+                                 or not lens.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor of B elements")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check_bf16("dq", dq, q.shape)
+    _check_bf16("dk", dk, k.shape)
+    _check_bf16("dv", dv, v.shape)
+    ws_bytes = 0
+    if workspace is not None:
+        if not workspace.is_cuda or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    sc = 0.0 if scale is None else float(scale)
+    rc = lib.sdpa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
+                      _ptr(dv), B, Hq, Hkv, Sq, Skv, Dqk, Dv, sc, int(causal), int(bottom_right),
+                      int(window_left), int(window_right), int(deterministic), _ptr(seq_q_lens),
+                      _ptr(seq_kv_lens), _ptr(workspace), ws_bytes, _stream_handle(stream))
+    if rc != 0:
+        raise SdpaError(rc, "sdpa_bwd")
+    return dq, dk, dv
+
+
+def check_device_status(stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Synchronizes the stream and raises if a kernel reported a timed-out wait."""
+    rc = load().sdpa_bwd_check_device_status(_stream_handle(stream))
+    if rc != 0:
+        raise SdpaError(rc, "device status")
+
+
+def profile_enable(on: bool = True) -> None:
+    load().sdpa_bwd_profile_enable(int(on))
+
+
+def profile_read():
+    """{kernel name: (total ms, launches)} accumulated since profile_enable()."""
+    ms = (ctypes.c_float * 4)()
+    n = (ctypes.c_int * 4)()
+    load().sdpa_bwd_profile_read(ms, n, 4)
+    return {name: (float(ms[i]), int(n[i])) for i, name in enumerate(KERNEL_NAMES)}

@@ -1,0 +1,103 @@
+// common.cuh -- parameters and workspace geometry shared by the SDPA backward
+// kernels and their host launcher.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <utility>
+
+namespace sdpa {
+
+// Tile sizes of the KV-stationary main kernel: one CTA owns BN keys of one
+// query head and walks the query tiles of BM rows.
+constexpr int BM = 128;
+constexpr int BN = 128;
+
+// Row statistics staged per query tile: BM values of LSE * log2(e) (+inf for
+// masked or empty rows) followed by BM values of delta.
+constexpr int QSTAT_FLOATS = 2 * BM;
+
+// Device status bits (OR-ed into the per-device status word).
+constexpr int STATUS_TIMEOUT = 1;
+constexpr int STATUS_SMEM_ALIGN = 2;
+
+struct ChainParams {
+  int B, Hq, Hkv, Sq, Skv, Dqk, Dv;
+  int G;            // Hq / Hkv
+  int n_qt, n_kt;   // ceil(Sq / BM), ceil(Skv / BN)
+  float scale;      // softmax scale
+  float scale_log2; // scale * log2(e)
+  int causal, bottom_right, window_left, window_right, deterministic;
+  const int32_t* seq_q_lens;   // (B,) or null
+  const int32_t* seq_kv_lens;  // (B,) or null
+
+  // inputs
+  const __nv_bfloat16* o;
+  const __nv_bfloat16* d_o;
+  const float* lse;
+  // outputs
+  __nv_bfloat16* dq;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+
+  // workspace regions
+  float* qstat;         // [B*Hq][n_qt][QSTAT_FLOATS]
+  float* dq_accum;      // [B*Hq][n_qt][Dqk/4][BM][4]
+  int* counters;        // [B*Hq][n_qt] turn counters (deterministic mode)
+  int* ticket;          // work-unit ticket
+  __nv_bfloat16* dk_ws; // GQA: [B][Hq][Skv][Dqk] partials, else null
+  __nv_bfloat16* dv_ws; // GQA: [B][Hq][Skv][Dv]
+  int n_counters;       // B*Hq*n_qt + 1 (counters plus ticket)
+
+  int* status;          // per-device status word
+};
+
+// TMA tensor maps of the main kernel (K and V with H_kv heads, Q and dO with H_q).
+struct MainMaps {
+  CUtensorMap q, k, v, d_o;
+};
+
+// Host launchers, one per kernel, defined beside their kernels. `pdl` launches
+// with programmatic stream serialization (the kernel waits on its predecessor
+// with griddepcontrol.wait before touching dependent data).
+cudaError_t launch_preprocess(const ChainParams& p, int grid, cudaStream_t s);
+cudaError_t launch_main(const MainMaps& maps, const ChainParams& p, cudaStream_t s);
+cudaError_t launch_gqa_reduce(const ChainParams& p, int grid, cudaStream_t s);
+cudaError_t launch_dq_convert(const ChainParams& p, int grid, cudaStream_t s);
+cudaError_t main_kernel_setup();  // per device: opt in to the main kernel's shared memory
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t stream, bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+__host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// floor(a / b) for b > 0 and any sign of a.
+__host__ __device__ inline long long floor_div(long long a, long long b) {
+  return a >= 0 ? a / b : -((-a + b - 1) / b);
+}
+
+// Valid lengths of batch row b (the full S when no length array is given).
+__device__ inline void batch_lengths(const ChainParams& p, int b, int& Lq, int& Lk) {
+  Lq = p.seq_q_lens ? min(max(p.seq_q_lens[b], 0), p.Sq) : p.Sq;
+  Lk = p.seq_kv_lens ? min(max(p.seq_kv_lens[b], 0), p.Skv) : p.Skv;
+}
+
+}  // namespace sdpa

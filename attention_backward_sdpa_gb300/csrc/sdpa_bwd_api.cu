@@ -1,0 +1,322 @@
+// sdpa_bwd_api.cu -- host side of libsdpa_bwd.so: the C ABI declared in
+// include/sdpa_bwd.h.
+//
+// One call validates its arguments, carves the workspace, encodes the four TMA
+// tensor maps and enqueues the kernel chain on the caller's stream
+// (cuDNN frontend docs, "SDPA Backward (SM120)", section "The kernel chain"):
+//   preprocess -> main -> [gqa_reduce when H_kv < H_q] -> dq_convert
+// Every launch after the first uses programmatic dependent launch, so each
+// kernel's prologue overlaps its predecessor's tail; each kernel waits for its
+// predecessor's completion (griddepcontrol.wait) before touching its outputs.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/sdpa_bwd.h"
+#include "common.cuh"
+#include "tmap.h"
+
+namespace sdpa {
+
+// Per-device status word written by kernels that give up on a bounded wait.
+__device__ int g_device_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int* g_status_ptr[kMaxDevices] = {};
+bool g_device_checked[kMaxDevices] = {};
+bool g_device_ok[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+
+// Profiling state.
+bool g_profile = false;
+float g_prof_ms[4] = {};
+int g_prof_n[4] = {};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct Carve {
+  size_t qstat, dq_accum, counters, dk_ws, dv_ws, total;
+};
+
+Carve carve(int B, int Hq, int Hkv, int Sq, int Skv, int Dqk, int Dv) {
+  const size_t n_qt = (size_t)ceil_div(Sq, BM);
+  const size_t bh = (size_t)B * Hq;
+  Carve c{};
+  size_t off = 0;
+  c.qstat = off;
+  off = align256(off + bh * n_qt * QSTAT_FLOATS * sizeof(float));
+  c.dq_accum = off;
+  off = align256(off + bh * n_qt * BM * (size_t)Dqk * sizeof(float));
+  c.counters = off;
+  off = align256(off + (bh * n_qt + 1) * sizeof(int));
+  if (Hkv < Hq) {
+    c.dk_ws = off;
+    off = align256(off + bh * (size_t)Skv * Dqk * 2);
+    c.dv_ws = off;
+    off = align256(off + bh * (size_t)Skv * Dv * 2);
+  } else {
+    c.dk_ws = c.dv_ws = SIZE_MAX;
+  }
+  c.total = off;
+  return c;
+}
+
+bool dims_supported(int Dqk, int Dv) { return (Dqk == 64 && Dv == 64) || (Dqk == 128 && Dv == 128); }
+
+int basic_checks(int B, int Hq, int Hkv, int Sq, int Skv, int Dqk, int Dv) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Skv < 0 || Dqk <= 0 || Dv <= 0)
+    return SDPA_ERR_INVALID;
+  if (Hq % Hkv != 0) return SDPA_ERR_INVALID;
+  if (!dims_supported(Dqk, Dv)) return SDPA_ERR_UNSUPPORTED;
+  // TMA coordinates and the flattened (batch, head) axis are 32-bit.
+  if ((long long)B * Hq >= (1ll << 31) || (long long)B * Hq * ceil_div(Skv, BN) >= (1ll << 31))
+    return SDPA_ERR_INVALID;
+  return SDPA_OK;
+}
+
+// Sets up per-device state once: device capability check and the status word.
+int device_state(int dev, int** status_out, int* sms_out) {
+  if (dev < 0 || dev >= kMaxDevices) return SDPA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_device_checked[dev]) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return SDPA_ERR_CUDA;
+    g_device_ok[dev] = (prop.major == 10 && prop.minor == 3);
+    g_num_sms[dev] = prop.multiProcessorCount;
+    if (g_device_ok[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return SDPA_ERR_CUDA;
+      g_status_ptr[dev] = static_cast<int*>(p);
+      if (main_kernel_setup() != cudaSuccess) return SDPA_ERR_CUDA;
+    }
+    g_device_checked[dev] = true;
+  }
+  if (!g_device_ok[dev]) return SDPA_ERR_UNSUPPORTED;
+  *status_out = g_status_ptr[dev];
+  *sms_out = g_num_sms[dev];
+  return SDPA_OK;
+}
+
+bool make_bhsd_map(CUtensorMap* m, const void* base, int D, int S, long long BH) {
+  const uint64_t dims[3] = {(uint64_t)D, (uint64_t)S, (uint64_t)BH};
+  const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)S * D * 2};
+  const uint32_t box[3] = {64, (uint32_t)BM, 1};
+  return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Records one event pair per launch while profiling is on; the pairs are
+// resolved once at the end of the call, so no synchronization sits between
+// launches (a busy stream keeps host launch latency out of the intervals).
+struct ProfEvents {
+  cudaEvent_t ev[4][2] = {};
+  bool used[4] = {};
+  cudaStream_t s;
+  explicit ProfEvents(cudaStream_t s_) : s(s_) {}
+  void begin(int slot) {
+    if (!g_profile) return;
+    cudaEventCreate(&ev[slot][0]);
+    cudaEventCreate(&ev[slot][1]);
+    cudaEventRecord(ev[slot][0], s);
+    used[slot] = true;
+  }
+  void end(int slot) {
+    if (g_profile && used[slot]) cudaEventRecord(ev[slot][1], s);
+  }
+  ~ProfEvents() {
+    for (int i = 0; i < 4; ++i) {
+      if (!used[i]) continue;
+      cudaEventSynchronize(ev[i][1]);
+      float ms = 0.f;
+      if (cudaEventElapsedTime(&ms, ev[i][0], ev[i][1]) == cudaSuccess) {
+        std::lock_guard<std::mutex> lock(g_mu);
+        g_prof_ms[i] += ms;
+        g_prof_n[i] += 1;
+      }
+      cudaEventDestroy(ev[i][0]);
+      cudaEventDestroy(ev[i][1]);
+    }
+  }
+};
+
+}  // namespace
+}  // namespace sdpa
+
+using namespace sdpa;
+
+extern "C" {
+
+int sdpa_bwd_version(void) { return 100; }
+
+const char* sdpa_status_string(int status) {
+  switch (status) {
+    case SDPA_OK: return "ok";
+    case SDPA_ERR_INVALID: return "invalid argument";
+    case SDPA_ERR_UNSUPPORTED: return "unsupported configuration or device";
+    case SDPA_ERR_ALIGN: return "tensor pointer not 16-byte aligned";
+    case SDPA_ERR_WORKSPACE: return "workspace too small";
+    case SDPA_ERR_CUDA: return "CUDA runtime error";
+    case SDPA_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+size_t sdpa_bwd_workspace_size(int B, int H_q, int H_kv, int S_q, int S_kv, int D_qk, int D_v,
+                               int deterministic) {
+  (void)deterministic;
+  if (basic_checks(B, H_q, H_kv, S_q, S_kv, D_qk, D_v) != SDPA_OK) return 0;
+  if (S_q == 0 || S_kv == 0) return 0;
+  return carve(B, H_q, H_kv, S_q, S_kv, D_qk, D_v).total;
+}
+
+int sdpa_bwd_profile_enable(int on) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_profile = on != 0;
+  for (int i = 0; i < 4; ++i) {
+    g_prof_ms[i] = 0.f;
+    g_prof_n[i] = 0;
+  }
+  return SDPA_OK;
+}
+
+int sdpa_bwd_profile_read(float* ms, int* launches, int n) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  for (int i = 0; i < n && i < 4; ++i) {
+    if (ms) ms[i] = g_prof_ms[i];
+    if (launches) launches[i] = g_prof_n[i];
+  }
+  return 4;
+}
+
+int sdpa_bwd_check_device_status(void* stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SDPA_ERR_CUDA;
+  int* status = nullptr;
+  int sms = 0;
+  int rc = device_state(dev, &status, &sms);
+  if (rc != SDPA_OK) return rc;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SDPA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return SDPA_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    cudaMemcpy(status, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    return SDPA_ERR_TIMEOUT;
+  }
+  return SDPA_OK;
+}
+
+int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const void* d_o,
+             const float* lse, void* dq, void* dk, void* dv, int B, int H_q, int H_kv, int S_q,
+             int S_kv, int D_qk, int D_v, float scale, int causal, int bottom_right,
+             int window_left, int window_right, int deterministic, const int32_t* seq_q_lens,
+             const int32_t* seq_kv_lens, void* workspace, size_t workspace_bytes, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  int rc = basic_checks(B, H_q, H_kv, S_q, S_kv, D_qk, D_v);
+  if (rc != SDPA_OK) return rc;
+  if (!q || !k || !v || !o || !d_o || !lse || !dq || !dk || !dv) return SDPA_ERR_INVALID;
+  for (const void* ptr : {q, k, v, o, d_o, (const void*)dq, (const void*)dk, (const void*)dv})
+    if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return SDPA_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(lse) % 4 != 0) return SDPA_ERR_ALIGN;
+  if (window_right >= 0 && !causal) return SDPA_ERR_UNSUPPORTED;
+  if (!(scale > 0.f) || !std::isfinite(scale)) scale = 1.0f / std::sqrt((float)D_qk);
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SDPA_ERR_CUDA;
+  int* status = nullptr;
+  int sms = 0;
+  rc = device_state(dev, &status, &sms);
+  if (rc != SDPA_OK) return rc;
+
+  const size_t dq_bytes = (size_t)B * H_q * S_q * D_qk * 2;
+  const size_t dk_bytes = (size_t)B * H_kv * S_kv * D_qk * 2;
+  const size_t dv_bytes = (size_t)B * H_kv * S_kv * D_v * 2;
+  if (S_q == 0 || S_kv == 0) {  // no (query, key) pair: every gradient is zero
+    if (cudaMemsetAsync(dq, 0, dq_bytes, stream) != cudaSuccess ||
+        cudaMemsetAsync(dk, 0, dk_bytes, stream) != cudaSuccess ||
+        cudaMemsetAsync(dv, 0, dv_bytes, stream) != cudaSuccess)
+      return SDPA_ERR_CUDA;
+    return SDPA_OK;
+  }
+
+  const Carve cv = carve(B, H_q, H_kv, S_q, S_kv, D_qk, D_v);
+  bool own_ws = false;
+  if (workspace == nullptr) {
+    if (cudaMallocAsync(&workspace, cv.total, stream) != cudaSuccess) return SDPA_ERR_CUDA;
+    own_ws = true;
+  } else {
+    if (workspace_bytes < cv.total) return SDPA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return SDPA_ERR_ALIGN;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+
+  ChainParams p{};
+  p.B = B; p.Hq = H_q; p.Hkv = H_kv; p.Sq = S_q; p.Skv = S_kv; p.Dqk = D_qk; p.Dv = D_v;
+  p.G = H_q / H_kv;
+  p.n_qt = ceil_div(S_q, BM);
+  p.n_kt = ceil_div(S_kv, BN);
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.causal = causal ? 1 : 0;
+  p.bottom_right = bottom_right ? 1 : 0;
+  p.window_left = window_left < 0 ? -1 : window_left;
+  p.window_right = (causal && window_right > 0) ? window_right : -1;
+  p.deterministic = deterministic ? 1 : 0;
+  p.seq_q_lens = seq_q_lens;
+  p.seq_kv_lens = seq_kv_lens;
+  p.o = static_cast<const __nv_bfloat16*>(o);
+  p.d_o = static_cast<const __nv_bfloat16*>(d_o);
+  p.lse = lse;
+  p.dq = static_cast<__nv_bfloat16*>(dq);
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.qstat = reinterpret_cast<float*>(ws + cv.qstat);
+  p.dq_accum = reinterpret_cast<float*>(ws + cv.dq_accum);
+  p.counters = reinterpret_cast<int*>(ws + cv.counters);
+  p.n_counters = B * H_q * p.n_qt + 1;
+  p.ticket = p.counters + (p.n_counters - 1);
+  p.dk_ws = H_kv < H_q ? reinterpret_cast<__nv_bfloat16*>(ws + cv.dk_ws) : nullptr;
+  p.dv_ws = H_kv < H_q ? reinterpret_cast<__nv_bfloat16*>(ws + cv.dv_ws) : nullptr;
+  p.status = status;
+
+  MainMaps maps;
+  const long long BHq = (long long)B * H_q, BHkv = (long long)B * H_kv;
+  if (!make_bhsd_map(&maps.q, q, D_qk, S_q, BHq) || !make_bhsd_map(&maps.k, k, D_qk, S_kv, BHkv) ||
+      !make_bhsd_map(&maps.v, v, D_v, S_kv, BHkv) || !make_bhsd_map(&maps.d_o, d_o, D_v, S_q, BHq)) {
+    if (own_ws) cudaFreeAsync(workspace, stream);
+    return SDPA_ERR_CUDA;
+  }
+
+  cudaError_t e = cudaSuccess;
+  const int aux_grid = sms * 4;
+  ProfEvents prof(stream);
+  prof.begin(0);
+  e = launch_preprocess(p, aux_grid, stream);
+  prof.end(0);
+  if (e == cudaSuccess) {
+    prof.begin(1);
+    e = launch_main(maps, p, stream);
+    prof.end(1);
+  }
+  if (e == cudaSuccess && H_kv < H_q) {
+    prof.begin(2);
+    e = launch_gqa_reduce(p, aux_grid, stream);
+    prof.end(2);
+  }
+  if (e == cudaSuccess) {
+    prof.begin(3);
+    e = launch_dq_convert(p, aux_grid, stream);
+    prof.end(3);
+  }
+  if (own_ws) cudaFreeAsync(workspace, stream);
+  return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+}
+
+}  // extern "C"

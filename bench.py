@@ -1,0 +1,418 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 SDPA backward: TFLOP/s and fraction of dense bf16 peak.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl gb300|reference]
+
+One step = one full backward (preprocess -> main -> [GQA reduce] -> dQ convert)
+over one batch of the workload, inputs resident in HBM. Each step is timed
+with CUDA events on the launching stream; a 256 MiB buffer is written between
+steps so that every step starts with a cold L2 (the flush is outside the event
+pair). FLOPs are algorithmic: 2 * (3*D_qk + 2*D_v) per visible (query, key)
+pair (= 10 * D per pair when D_qk = D_v), counted exactly from the mask.
+
+Inputs: Q, K, V, dO are seeded draws (workloads.py); O and LSE are the fp64
+oracle forward of those draws, computed in the CPU-baseline leg on rank 0
+(which also times the oracle backward on a bounded sample of the workload)
+and broadcast to the other ranks. The timed GPU path never calls the oracle.
+
+Multi-GPU: the op does not shard across GPUs in this library; N ranks run N
+independent replicas of the workload (weak scaling) and the step time is the
+max over ranks. `--impl reference` times the fp64 oracle on the host cores
+(the only reference this op has) on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "SDPA backward TFLOP/s (bf16, 1xGB300) and fraction of dense tensor peak"
+DEFAULT_WORKLOAD = "causal_mha"
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ---------------------------------------------------------------- FLOP counting
+def visible_pairs(w: workloads.Workload, lens) -> int:
+    """Visible (query, key) pairs summed over batch rows and query heads: per query
+    q the visible keys form the interval [q+diag-W, q+diag+R] clipped to [0, L_kv)."""
+    total = 0
+    for b in range(w.B):
+        Lq = w.Sq if lens is None else min(int(lens[b]), w.Sq)
+        Lk = w.Skv if lens is None else min(int(lens[b]), w.Skv)
+        if Lq <= 0 or Lk <= 0:
+            continue
+        diag = (Lk - Lq) if w.bottom_right else 0
+        q = np.arange(Lq, dtype=np.int64)
+        lo = np.zeros(Lq, dtype=np.int64)
+        hi = np.full(Lq, Lk - 1, dtype=np.int64)
+        if w.causal:
+            hi = np.minimum(hi, q + diag + max(w.window_right, 0))
+        if w.window_left >= 0:
+            lo = np.maximum(lo, q + diag - w.window_left)
+        total += int(np.clip(hi - lo + 1, 0, None).sum()) * w.Hq
+    return total
+
+
+def flops_per_pair(w: workloads.Workload) -> int:
+    return 2 * (3 * w.Dqk + 2 * w.Dv)
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the GPU works."""
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, index: int, interval_ms: int = 50):
+        self.index, self.interval = index, interval_ms
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread:
+                self.thread.join(timeout=2)
+
+    def summary(self):
+        rows = []
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[2], parts[3:]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- distributed
+def init_dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def broadcast_tensor(t: torch.Tensor, world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.broadcast(t, src=0)
+    return t
+
+
+# ---------------------------------------------------------------- CPU baseline (oracle)
+def _problem(w, lens):
+    import oracle
+    return oracle.Problem(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.Dqk, w.Dv, scale=w.resolved_scale,
+                          causal=w.causal,
+                          bottom_right=w.bottom_right, window_left=w.window_left,
+                          window_right=w.window_right,
+                          seq_q_lens=None if lens is None else lens.numpy(),
+                          seq_kv_lens=None if lens is None else lens.numpy())
+
+
+def oracle_forward_inputs(w, t):
+    """O (bf16) and LSE (fp32) of the workload from the fp64 oracle forward."""
+    import oracle
+    p = _problem(w, t["seq_q_lens"])
+    o64, lse64 = oracle.forward(p, t["q"].double().numpy(), t["k"].double().numpy(),
+                                t["v"].double().numpy())
+    return torch.from_numpy(o64).to(torch.bfloat16), torch.from_numpy(lse64).float()
+
+
+def _head_slice(w, t, o, lse, G_groups):
+    """The first G_groups KV heads with their query heads (the sample unit)."""
+    G = w.Hq // w.Hkv
+    hq = G_groups * G
+    return {k: v[:, :hq].contiguous() if k in ("q", "do") else v[:, :G_groups].contiguous()
+            for k, v in (("q", t["q"]), ("do", t["do"]), ("k", t["k"]), ("v", t["v"]))}, \
+        o[:, :hq].contiguous(), lse[:, :hq].contiguous(), hq
+
+
+def oracle_backward_sample(w, t, o, lse, groups):
+    """Runs the oracle backward on the first `groups` KV-head groups of every batch
+    row; returns (seconds, algorithmic FLOPs of the sample)."""
+    import oracle
+    sl, os_, ls, hq = _head_slice(w, t, o, lse, groups)
+    ws = w.with_(Hq=hq, Hkv=groups)
+    p = _problem(ws, t["seq_q_lens"])
+    args = [sl["q"].double().numpy(), sl["k"].double().numpy(), sl["v"].double().numpy(),
+            os_.double().numpy(), sl["do"].double().numpy(), ls.double().numpy()]
+    t0 = time.perf_counter()
+    oracle.backward(p, *args)
+    dt = time.perf_counter() - t0
+    return dt, visible_pairs(ws, t["seq_q_lens"]) * flops_per_pair(ws)
+
+
+def cpu_baseline_leg(w, t, target_s=12.0):
+    import oracle
+    t0 = time.perf_counter()
+    o, lse = oracle_forward_inputs(w, t)
+    fwd_s = time.perf_counter() - t0
+    dt1, f1 = oracle_backward_sample(w, t, o, lse, 1)
+    groups = max(1, min(w.Hkv, int(target_s / max(dt1, 1e-3))))
+    if groups > 1:
+        dt, fl = oracle_backward_sample(w, t, o, lse, groups)
+    else:
+        dt, fl = dt1, f1
+    cb = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+          "kind": "oracle",
+          "sample": f"fp64 oracle backward of {groups} of {w.Hkv} KV-head groups x B={w.B} "
+                    f"({fl / 1e9:.2f} GFLOP algorithmic in {dt:.2f} s); oracle forward for the "
+                    f"O/LSE inputs took {fwd_s:.1f} s"}
+    return o, lse, cb
+
+
+# ---------------------------------------------------------------- GPU leg
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d.get("bf16_tflops"), d.get("hbm_gbs"), "measured"
+    return 1900.0, 6800.0, "fallback"
+
+
+def run_gpu(args, w, t, o, lse, rank, world, device):
+    import attention_backward_sdpa_gb300 as pkg
+    pkg.load()
+    lens = t["seq_q_lens"]
+    d = {k: t[k].to(device) for k in ("q", "k", "v", "do")}
+    d["o"], d["lse"] = o.to(device), lse.to(device)
+    lq = None if lens is None else lens.to(device)
+    lk = None if t["seq_kv_lens"] is None else t["seq_kv_lens"].to(device)
+    dq, dk, dv = torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"])
+    ws = torch.empty(max(pkg.workspace_size(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.Dqk, w.Dv,
+                                            w.deterministic), 256), dtype=torch.uint8, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    kw = dict(scale=w.resolved_scale, causal=w.causal, bottom_right=w.bottom_right,
+              window_left=w.window_left, window_right=w.window_right,
+              deterministic=w.deterministic, seq_q_lens=lq, seq_kv_lens=lk, dq=dq, dk=dk, dv=dv,
+              workspace=ws)
+
+    def step():
+        pkg.sdpa_bwd(d["q"], d["k"], d["v"], d["o"], d["do"], d["lse"], **kw)
+
+    def timed_loop(n, profile=False):
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        if profile:
+            pkg.profile_enable(True)
+        for i in range(n):
+            flush.fill_(i & 0xFF)
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(device)
+        prof = pkg.profile_read() if profile else None
+        if profile:
+            pkg.profile_enable(False)
+        return sum(s.elapsed_time(e) for s, e in zip(starts, ends)), prof
+
+    flops = visible_pairs(w, None if lens is None else lens.numpy()) * flops_per_pair(w)
+    with ClockSampler(device.index if device.index is not None else 0) as clocks:
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize(device)
+        pkg.check_device_status()
+        barrier(world)
+        torch.cuda.synchronize(device)
+        total_ms, _ = timed_loop(args.steps)
+        torch.cuda.synchronize(device)
+        barrier(world)
+        pkg.check_device_status()
+        # Per-kernel durations from the library's own events on the launch stream
+        # (a second pass: the events between launches disable the PDL overlap).
+        _, prof = timed_loop(args.steps, profile=True)
+        # End to end through the public API with host buffers: pinned host -> device
+        # copies of the inputs and a device -> host read of dQ/dK/dV every step.
+        host_in = {k: v.cpu().pin_memory() for k, v in d.items()}
+        host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (dq, dk, dv)]
+        h2d = sum(x.numel() * x.element_size() for x in host_in.values())
+        d2h = sum(x.numel() * x.element_size() for x in host_out)
+        e2e_steps = max(3, min(args.steps, 50))
+        torch.cuda.synchronize(device)
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            for k, v in host_in.items():
+                d[k].copy_(v, non_blocking=True)
+            step()
+            for h, x in zip(host_out, (dq, dk, dv)):
+                h.copy_(x, non_blocking=True)
+            torch.cuda.synchronize(device)
+        e2e_s = (time.perf_counter() - t0) / e2e_steps
+    pkg.check_device_status()
+    ms_step = max_over_ranks(total_ms / args.steps, world, device)
+    e2e_s = max_over_ranks(e2e_s, world, device)
+    peak_tf, peak_hbm, peak_kind = peaks()
+    main_ms = prof["main"][0] / max(prof["main"][1], 1)
+    achieved = flops / (main_ms * 1e-3) / 1e12
+    value = world * flops / (ms_step * 1e-3) / 1e12
+    kernel_ms = {k: round(v[0] / max(v[1], 1), 5) for k, v in prof.items() if v[1]}
+    return {
+        "value": value, "ms_per_step": ms_step, "flops": flops,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": achieved / peak_tf, "traffic": None,
+                     "kernel": "sdpa_bwd_main", "peak_kind": f"{peak_kind} bf16 burst"},
+        "kernel_ms": kernel_ms,
+        "e2e": {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "clocks": clocks.summary(),
+        "gpu_launches": (4 if w.Hkv < w.Hq else 3) * args.steps,
+    }
+
+
+def run_reference(args, w, rank, world):
+    """The fp64 oracle on the host cores, bounded samples of the workload per step."""
+    if rank != 0:
+        return
+    import oracle
+    t = workloads.generate(w)
+    o, lse = oracle_forward_inputs(w, t)
+    times, fl = [], 0
+    for i in range(args.warmup + args.steps):
+        dt, fl = oracle_backward_sample(w, t, o, lse, 1)
+        if i >= args.warmup:
+            times.append(dt)
+    dt = sum(times) / len(times)
+    v = fl / dt / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H_q": w.Hq, "H_kv": w.Hkv, "S_q": w.Sq,
+                       "S_kv": w.Skv, "D_qk": w.Dqk, "D_v": w.Dv, "causal": w.causal,
+                       "bottom_right": w.bottom_right, "window_left": w.window_left,
+                       "deterministic": w.deterministic,
+                       "sample": "first KV-head group of every batch row per step"},
+            "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+                             "kind": "oracle",
+                             "sample": f"fp64 oracle backward of 1 of {w.Hkv} KV-head groups "
+                                       f"x B={w.B} per step ({fl / 1e9:.2f} GFLOP)"},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip timing the oracle backward (O/LSE still come from the oracle forward)")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)
+    args.steps = max(args.steps, 1)
+    rank, world, local = init_dist()
+    w = workloads.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return 0
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    t = workloads.generate(w)
+    o = torch.empty((w.B, w.Hq, w.Sq, w.Dv), dtype=torch.bfloat16)
+    lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32)
+    cb = None
+    if rank == 0:
+        if args.no_cpu_baseline:
+            o, lse = oracle_forward_inputs(w, t)
+        else:
+            o, lse, cb = cpu_baseline_leg(w, t)
+    if world > 1:
+        o_d, l_d = o.to(device), lse.to(device)
+        broadcast_tensor(o_d, world)
+        broadcast_tensor(l_d, world)
+        o, lse = o_d.cpu(), l_d.cpu()
+    r = run_gpu(args, w, t, o, lse, rank, world, device)
+    if rank == 0:
+        line = {"metric": METRIC, "value": r["value"], "unit": "TFLOP/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic",
+                "config": {"workload": w.name, "B": w.B, "H_q": w.Hq, "H_kv": w.Hkv, "S_q": w.Sq,
+                           "S_kv": w.Skv, "D_qk": w.Dqk, "D_v": w.Dv, "causal": w.causal,
+                           "bottom_right": w.bottom_right, "window_left": w.window_left,
+                           "deterministic": w.deterministic, "seed": w.seed,
+                           "gflop_per_step": r["flops"] / 1e9,
+                           "l2": "256 MiB buffer written between timed steps",
+                           "parallelism": f"replicas{world}" if world > 1 else "single"},
+                "roofline": r["roofline"], "cpu_baseline": cb, "e2e": r["e2e"],
+                "gpu_launches": r["gpu_launches"], "kernel_ms": r["kernel_ms"],
+                "clocks": r["clocks"]}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

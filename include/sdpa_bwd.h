@@ -1,0 +1,134 @@
+/*
+ * sdpa_bwd.h -- C ABI of the GB300 (sm_103a) scaled-dot-product-attention
+ * backward library, libsdpa_bwd.so.
+ *
+ * Operation (cuDNN frontend docs, "SDPA Backward (SM120)": Overview, API
+ * Usage, and "Main-kernel pipeline: KV-stationary, five chained GEMMs"):
+ * given the forward activations Q, K, V, the forward output O, the loss
+ * gradient dO and the natural-log forward row statistic LSE, compute
+ *     P     = exp(scale * Q K^T - LSE)       (masked entries and LSE = -inf rows: 0)
+ *     delta = rowsum(dO * O)
+ *     dP    = dO V^T
+ *     dS    = P * (dP - delta)
+ *     dV    = P^T dO,   dQ = scale * dS K,   dK = scale * dS^T Q
+ * with the causal / sliding-window / padding masks of the page's "Causal,
+ * sliding-window, and padding masks" section and GQA/MQA (section "GQA/MQA
+ * group reduction": query head h reads KV head h / (H_q / H_kv); dK and dV of
+ * a KV head sum over its group of query heads, in ascending head order).
+ *
+ * Conventions shared by every entry point:
+ *   - Tensors are dense, contiguous, row-major (B, H, S, D) bf16 device
+ *     buffers, D innermost; every tensor pointer must be 16-byte aligned.
+ *     Q, O, dO, dQ have H_q heads; K, V, dK, dV have H_kv heads.
+ *     Q, K, dQ, dK have D_qk columns; V, O, dO, dV have D_v columns.
+ *   - lse is fp32 (B, H_q, S_q), natural log; -inf marks a row with no key.
+ *   - The caller owns every buffer. The library writes only dq, dk, dv and the
+ *     workspace; every element of dq, dk, dv is overwritten (masked or padded
+ *     rows get exact zeros), so outputs need no clearing.
+ *   - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and is asynchronous with respect to the host.
+ *   - Functions return an sdpa_status code and never abort the process. Errors
+ *     found while validating arguments are returned before anything is
+ *     launched. Errors that kernels detect while running (a bounded wait that
+ *     ran out) are recorded in a per-device status word that
+ *     sdpa_bwd_check_device_status() reads.
+ */
+#ifndef SDPA_BWD_H_
+#define SDPA_BWD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SDPA_OK = 0,
+  SDPA_ERR_INVALID = 1,     /* null pointer, bad size, H_kv not dividing H_q        */
+  SDPA_ERR_UNSUPPORTED = 2, /* head dims / mask combination / device not served     */
+  SDPA_ERR_ALIGN = 3,       /* a tensor pointer is not 16-byte aligned              */
+  SDPA_ERR_WORKSPACE = 4,   /* workspace smaller than sdpa_bwd_workspace_size()     */
+  SDPA_ERR_CUDA = 5,        /* a CUDA runtime call failed                           */
+  SDPA_ERR_TIMEOUT = 6      /* a device-side bounded wait ran out (reported later)  */
+} sdpa_status;
+
+/*
+ * Bytes of device workspace sdpa_bwd() needs for this problem (0 when none).
+ * The workspace holds, each region 256-byte aligned: per-query-tile fp32 row
+ * statistics (LSE * log2(e) and delta), the fp32 dQ accumulator, the
+ * deterministic-mode turn counters and a work ticket, and, when H_kv < H_q,
+ * the per-query-head bf16 dK/dV partials of the GQA reduction.
+ * Returns 0 for arguments sdpa_bwd() would reject.
+ */
+size_t sdpa_bwd_workspace_size(int B, int H_q, int H_kv, int S_q, int S_kv, int D_qk, int D_v,
+                               int deterministic);
+
+/*
+ * SDPA backward. Arguments:
+ *   q, k, v, o, d_o   device bf16 inputs, layouts above.
+ *   lse               device fp32 (B, H_q, S_q) natural-log LSE of the forward.
+ *   dq, dk, dv        device bf16 outputs (same shapes as q, k, v).
+ *   B, H_q, H_kv      batch and head counts; H_kv must divide H_q.
+ *   S_q, S_kv         sequence lengths (>= 0; a zero length gives zero gradients).
+ *   D_qk, D_v         head dims; served: (64, 64) and (128, 128).
+ *   scale             softmax scale applied to Q K^T; <= 0 or NaN selects 1/sqrt(D_qk).
+ *   causal            1: keep key k for query q only if k <= q + diag + max(window_right, 0).
+ *   bottom_right      1: diag = L_kv - L_q (the actual lengths of the batch row);
+ *                     0: diag = 0. Applies to the causal and the window masks.
+ *   window_left       W >= 0: mask keys k < q + diag - W; < 0: no left window.
+ *   window_right      R >= 0 widens the causal diagonal by R keys; requires causal.
+ *                     < 0: no widening.
+ *   deterministic     1: dQ is reduced across KV tiles in a fixed (ascending KV
+ *                     tile) order, so repeated calls give bitwise-identical
+ *                     dQ; dK and dV are bitwise reproducible in both modes.
+ *   seq_q_lens,       device int32 (B,) per-batch valid lengths, or NULL for
+ *   seq_kv_lens       "the full S". Queries at or past seq_q_lens[b] and keys
+ *                     at or past seq_kv_lens[b] are masked; their gradient
+ *                     rows are exact zeros.
+ *   workspace         device buffer of >= sdpa_bwd_workspace_size() bytes,
+ *                     256-byte aligned, used only for the duration of the call
+ *                     on `stream`; NULL makes the library take one from the
+ *                     stream-ordered allocator (cudaMallocAsync) and release
+ *                     it after the last kernel.
+ *   workspace_bytes   size of `workspace` (ignored when it is NULL).
+ *   stream            cudaStream_t on which every kernel is enqueued.
+ * Returns SDPA_OK once every kernel is enqueued, else an error code (nothing
+ * enqueued). Calls that share a workspace must not overlap on the device.
+ */
+int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const void* d_o,
+             const float* lse, void* dq, void* dk, void* dv, int B, int H_q, int H_kv, int S_q,
+             int S_kv, int D_qk, int D_v, float scale, int causal, int bottom_right,
+             int window_left, int window_right, int deterministic, const int32_t* seq_q_lens,
+             const int32_t* seq_kv_lens, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* sdpa_status_string(int status);
+
+/*
+ * Synchronizes `stream`, then reads and clears the current device's status
+ * word. Returns SDPA_OK, SDPA_ERR_TIMEOUT if any kernel gave up on a bounded
+ * wait since the last check (its results are then invalid), or SDPA_ERR_CUDA
+ * if the synchronization itself failed.
+ */
+int sdpa_bwd_check_device_status(void* stream);
+
+/*
+ * Per-kernel timing for benchmarks. While enabled, sdpa_bwd() records CUDA
+ * events around each launch and synchronizes the stream before returning, so
+ * it is for measurement only. sdpa_bwd_profile_read() fills up to n entries of
+ * ms[] (total milliseconds) and launches[] (count) per kernel in the order
+ * preprocess, main, gqa_reduce, dq_convert, and returns the number of kernels.
+ * Enabling resets the totals.
+ */
+int sdpa_bwd_profile_enable(int on);
+int sdpa_bwd_profile_read(float* ms, int* launches, int n);
+
+/* Library ABI version (major * 100 + minor). */
+int sdpa_bwd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDPA_BWD_H_ */

@@ -1,0 +1,118 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function the
+header declares, sizes its workspace as documented, and rejects bad arguments
+with the documented status codes before launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sdpa_bwd.h")
+
+OK, INVALID, UNSUPPORTED, ALIGN, WORKSPACE, CUDA, TIMEOUT = range(7)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import attention_backward_sdpa_gb300 as pkg
+    return pkg.load(build_if_missing=True)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w]+\s*\*?\s*(sdpa_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for expected in ("sdpa_bwd", "sdpa_bwd_workspace_size", "sdpa_status_string",
+                     "sdpa_bwd_check_device_status", "sdpa_bwd_profile_enable",
+                     "sdpa_bwd_profile_read", "sdpa_bwd_version"):
+        assert expected in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in sdpa_bwd.h but not exported"
+
+
+def test_version_and_status_strings(lib):
+    assert lib.sdpa_bwd_version() == 100
+    assert lib.sdpa_status_string(OK) == b"ok"
+    for code in range(1, 7):
+        assert lib.sdpa_status_string(code) not in (b"ok", b"unknown status")
+    assert lib.sdpa_status_string(99) == b"unknown status"
+
+
+def _a256(x):
+    return (x + 255) // 256 * 256
+
+
+def expected_workspace(B, Hq, Hkv, Sq, Skv, Dqk, Dv):
+    """Documented layout: per-query-tile row statistics (2 x 128 fp32), the fp32 dQ
+    accumulator over whole 128-row tiles, one int per query tile plus a ticket, and
+    for GQA the bf16 dK/dV partials with H_q heads; every region 256-byte aligned."""
+    n_qt = -(-Sq // 128)
+    total = _a256(B * Hq * n_qt * 256 * 4)
+    total += _a256(B * Hq * n_qt * 128 * Dqk * 4)
+    total += _a256((B * Hq * n_qt + 1) * 4)
+    if Hkv < Hq:
+        total += _a256(B * Hq * Skv * Dqk * 2) + _a256(B * Hq * Skv * Dv * 2)
+    return total
+
+
+@pytest.mark.parametrize("shape", [(1, 2, 2, 128, 128, 64, 64), (2, 16, 16, 2048, 2048, 128, 128),
+                                   (1, 32, 8, 4096, 4096, 128, 128), (3, 4, 1, 300, 177, 128, 128),
+                                   (1, 1, 1, 1, 1, 64, 64)])
+def test_workspace_size_matches_layout(lib, shape):
+    for det in (0, 1):
+        assert lib.sdpa_bwd_workspace_size(*shape, det) == expected_workspace(*shape)
+
+
+def test_workspace_size_rejects(lib):
+    assert lib.sdpa_bwd_workspace_size(1, 3, 2, 128, 128, 128, 128, 0) == 0  # Hkv does not divide
+    assert lib.sdpa_bwd_workspace_size(1, 2, 2, 128, 128, 96, 96, 0) == 0    # head dim not served
+    assert lib.sdpa_bwd_workspace_size(0, 2, 2, 128, 128, 128, 128, 0) == 0
+    assert lib.sdpa_bwd_workspace_size(1, 2, 2, 0, 128, 128, 128, 0) == 0    # nothing to stage
+
+
+FAKE = 0x10000  # never dereferenced: every call below fails validation first
+
+
+def call(lib, ptrs=None, B=1, Hq=2, Hkv=2, Sq=128, Skv=128, Dqk=128, Dv=128, scale=0.0, causal=0,
+         br=0, wl=-1, wr=-1, det=0, ws=None, ws_bytes=0):
+    ptrs = ptrs or [FAKE] * 9
+    vp = [ctypes.c_void_p(p) if p is not None else None for p in ptrs]
+    return lib.sdpa_bwd(*vp, B, Hq, Hkv, Sq, Skv, Dqk, Dv, ctypes.c_float(scale), causal, br, wl,
+                        wr, det, None, None, ws, ws_bytes, None)
+
+
+def test_argument_validation(lib):
+    assert call(lib, Hq=3, Hkv=2) == INVALID
+    assert call(lib, B=0) == INVALID
+    assert call(lib, Sq=-1) == INVALID
+    assert call(lib, Dqk=96, Dv=96) == UNSUPPORTED
+    assert call(lib, Dqk=128, Dv=64) == UNSUPPORTED
+    for i in range(9):
+        ptrs = [FAKE] * 9
+        ptrs[i] = None
+        assert call(lib, ptrs) == INVALID
+    for i in (0, 1, 2, 3, 4, 6, 7, 8):  # bf16 tensors need 16-byte alignment
+        ptrs = [FAKE] * 9
+        ptrs[i] = FAKE + 8
+        assert call(lib, ptrs) == ALIGN
+    ptrs = [FAKE] * 9
+    ptrs[5] = FAKE + 2  # lse needs 4-byte alignment
+    assert call(lib, ptrs) == ALIGN
+    assert call(lib, wr=3, causal=0) == UNSUPPORTED  # a right band only widens a causal mask
+
+
+def test_python_binding_rejects_cpu_tensors():
+    import torch
+    import attention_backward_sdpa_gb300 as pkg
+    x = torch.zeros(1, 2, 128, 128, dtype=torch.bfloat16)
+    lse = torch.zeros(1, 2, 128)
+    with pytest.raises(ValueError):
+        pkg.sdpa_bwd(x, x, x, x, x, lse)

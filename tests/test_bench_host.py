@@ -1,0 +1,59 @@
+"""Host-side logic of bench.py that needs no GPU: the algorithmic FLOP count
+(visible pairs) against the oracle's brute-force count, and the multi-rank
+timing reduction / input broadcast over world_size-2 gloo ranks."""
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+import workloads
+from harness import problem_of
+
+W = workloads.Workload
+
+
+@pytest.mark.parametrize("w,lens", [
+    (W("a", 2, 4, 2, 300, 300, 64, 64, causal=True), None),
+    (W("b", 1, 2, 2, 200, 333, 64, 64, causal=True, bottom_right=True), None),
+    (W("c", 1, 2, 2, 333, 200, 64, 64, causal=True, bottom_right=True), None),
+    (W("d", 3, 2, 2, 300, 300, 64, 64, causal=True, window_left=64), np.array([1, 130, 300])),
+    (W("e", 1, 2, 2, 260, 260, 64, 64, causal=True, window_right=50), None),
+    (W("f", 1, 2, 2, 300, 280, 64, 64, window_left=150, bottom_right=True), None),
+    (W("g", 2, 2, 2, 100, 100, 64, 64), np.array([0, 77])),
+])
+def test_visible_pairs_matches_oracle(oracle_mod, w, lens):
+    p = problem_of(w, None if lens is None else torch.from_numpy(lens))
+    assert bench.visible_pairs(w, lens) == oracle_mod.count_visible(p)
+
+
+def test_headline_flops_formula():
+    # D_qk = D_v = D: 2*(3D+2D) = 10*D per visible pair.
+    w = workloads.WORKLOADS["causal_mha"]
+    assert bench.flops_per_pair(w) == 10 * 128
+    assert bench.visible_pairs(w, None) == 2 * 16 * 2048 * 2049 // 2
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    m = bench.max_over_ranks(1.5 + rank, world)
+    t = torch.full((3,), float(rank))
+    bench.broadcast_tensor(t, world)
+    bench.barrier(world)
+    out[rank] = (m, t.tolist())
+    dist.destroy_process_group()
+
+
+def test_two_rank_reduction_and_broadcast():
+    port = 29500 + os.getpid() % 1000
+    with mp.Manager() as mgr:
+        out = mgr.dict()
+        mp.spawn(_worker, args=(2, port, out), nprocs=2, join=True)
+        res = dict(out)
+    assert res[0][0] == res[1][0] == 2.5          # max over ranks
+    assert res[0][1] == res[1][1] == [0.0, 0.0, 0.0]  # rank 0's tensor on every rank

@@ -1,0 +1,190 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Small cases compare every element of dQ/dK/dV; they span several 128-row tiles
+with ragged tails and cover each mask kind, GQA/MQA, both causal alignments,
+S_q != S_kv, padding (including empty batch rows) and the deterministic relay.
+The five benchmark workloads run at full size and are compared on sampled rows
+that the oracle computes one by one. Outputs are NaN-poisoned before every call,
+so an element the library fails to write fails the test.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from harness import (assert_close, errors, gpu_backward, make_case, oracle_backward,
+                     oracle_sampled, to_device)
+
+pytestmark = pytest.mark.gpu
+
+W = workloads.Workload
+
+
+def _full_compare(w):
+    case = make_case(w)
+    dq, dk, dv = gpu_backward(case)
+    ref = oracle_backward(case)
+    res = {}
+    for name, g, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        res[name] = assert_close(name, g.double().cpu().numpy(), r)
+    return case, (dq, dk, dv), ref
+
+
+SMALL = {
+    "tiny_dense": workloads.WORKLOADS["tiny_dense"],
+    "tiny_causal": workloads.WORKLOADS["tiny_dense"].with_(causal=True),
+    "d128_causal_ragged": W("d128_causal_ragged", 1, 2, 2, 300, 300, 128, 128, causal=True, seed=10),
+    "d128_dense_ragged": W("d128_dense_ragged", 2, 2, 2, 190, 250, 128, 128, seed=11),
+    "br_causal_long_kv": W("br_causal_long_kv", 1, 2, 2, 200, 333, 128, 128, causal=True,
+                           bottom_right=True, seed=12),
+    "br_causal_long_q": W("br_causal_long_q", 1, 2, 2, 333, 200, 128, 128, causal=True,
+                          bottom_right=True, seed=13),
+    "tl_causal_long_q": W("tl_causal_long_q", 1, 2, 2, 333, 200, 64, 64, causal=True, seed=14),
+    "window_causal": W("window_causal", 1, 2, 2, 400, 400, 128, 128, causal=True, window_left=100,
+                       seed=15),
+    "window_only": W("window_only", 1, 2, 2, 300, 280, 128, 128, window_left=150,
+                     bottom_right=True, seed=16),
+    "causal_band_right": W("causal_band_right", 1, 2, 2, 260, 260, 128, 128, causal=True,
+                           window_right=50, seed=17),
+    "gqa": W("gqa", 2, 4, 2, 256, 256, 128, 128, causal=True, seed=18),
+    "mqa_d64": W("mqa_d64", 1, 3, 1, 200, 170, 64, 64, causal=True, bottom_right=True, seed=19),
+    "padded_window": W("padded_window", 3, 2, 2, 300, 300, 128, 128, causal=True,
+                       window_left=64, padded=(1, 300), seed=20),
+    "custom_scale": W("custom_scale", 1, 2, 2, 150, 150, 128, 128, causal=True, scale=0.05,
+                      seed=21),
+    "single_query": W("single_query", 1, 2, 2, 1, 300, 128, 128, causal=True, bottom_right=True,
+                      seed=22),
+    "single_key": W("single_key", 1, 2, 2, 130, 1, 64, 64, seed=23),
+    "gqa_det": W("gqa_det", 1, 4, 2, 520, 520, 128, 128, causal=True, deterministic=True, seed=24),
+    "window_det": W("window_det", 2, 2, 1, 600, 600, 128, 128, causal=True, window_left=200,
+                    deterministic=True, seed=25),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_small_full_parity(name):
+    _full_compare(SMALL[name])
+
+
+def test_padded_rows_are_exact_zeros():
+    w = SMALL["padded_window"]
+    case, (dq, dk, dv), _ = _full_compare(w)
+    lens = case["seq_q_lens"].tolist()
+    for b, L in enumerate(lens):
+        assert torch.all(dq[b, :, L:] == 0)
+        assert torch.all(dk[b, :, L:] == 0) and torch.all(dv[b, :, L:] == 0)
+
+
+def test_zero_length_batch_row():
+    w = W("zero_len", 2, 2, 2, 200, 200, 128, 128, causal=True, seed=26)
+    case = make_case(w)
+    lens = torch.tensor([0, 150], dtype=torch.int32)
+    case["seq_q_lens"] = lens
+    case["seq_kv_lens"] = lens.clone()
+    case["problem"].seq_q_lens = lens.numpy()
+    case["problem"].seq_kv_lens = lens.numpy()
+    # O/LSE consistent with the lengths
+    import oracle
+    from harness import f64
+    o64, lse64 = oracle.forward(case["problem"], f64(case["q"]), f64(case["k"]), f64(case["v"]))
+    case["o"] = torch.from_numpy(o64).to(torch.bfloat16)
+    case["lse"] = torch.from_numpy(lse64).float()
+    dq, dk, dv = gpu_backward(case)
+    ref = oracle_backward(case)
+    for name, g, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        assert_close(name, g.double().cpu().numpy(), r)
+    assert torch.all(dq[0] == 0) and torch.all(dk[0] == 0) and torch.all(dv[0] == 0)
+
+
+def test_adversarial_key_growth_masked():
+    """Keys scaled by growth**(key // 128) make the probability mass jump between
+    key tiles; a masked entry leaking into a gradient shows as ref == 0, gpu != 0.
+    (Where the oracle's zero comes from cancellation, e.g. a row that sees one key
+    has dS = P*(dP - delta) = 0 exactly in fp64, the fp32 GPU result is ~1e-8, so
+    the check is relative to the tensor's scale: a leaked probability is O(1).)"""
+    w = W("growth", 1, 2, 2, 384, 384, 128, 128, causal=True, window_left=150, seed=27)
+    case = make_case(w)
+    growth = torch.tensor(1.5) ** (torch.arange(384) // 128).float()
+    case["k"] = (case["k"].float() * growth[None, None, :, None]).to(torch.bfloat16)
+    import oracle
+    from harness import f64
+    o64, lse64 = oracle.forward(case["problem"], f64(case["q"]), f64(case["k"]), f64(case["v"]))
+    case["o"] = torch.from_numpy(o64).to(torch.bfloat16)
+    case["lse"] = torch.from_numpy(lse64).float()
+    dq, dk, dv = gpu_backward(case)
+    ref = oracle_backward(case)
+    for name, g, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        g = g.double().cpu().numpy()
+        assert_close(name, g, r)
+        leak = np.abs(g[r == 0]).max(initial=0.0)
+        assert leak <= 1e-5 * np.abs(r).max(), f"{name}: {leak:.3e} where the oracle is exactly zero"
+
+
+def test_deterministic_bitwise_small():
+    w = SMALL["window_det"]
+    case = make_case(w)
+    d = to_device(case)
+    first = gpu_backward(case, d)
+    for _ in range(5):
+        again = gpu_backward(case, d)
+        for a, b in zip(first, again):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+# ---------------------------------------------------------------- full-size workloads
+_CASES = {}
+
+
+def _case(name):
+    if name not in _CASES:
+        _CASES[name] = make_case(workloads.WORKLOADS[name])
+    return _CASES[name]
+
+
+def _sample_rows(w, lens, rng, n_rand=24):
+    """Flat query rows and key rows to check: tile edges, ends, padding, random."""
+    q_rows, kv_rows = [], []
+    edges = [0, 1, 127, 128, 129, 255, 256, w.Sq // 2, w.Sq - 129, w.Sq - 128, w.Sq - 1]
+    for b in range(w.B):
+        L = w.Sq if lens is None else int(lens[b])
+        pick = set(e for e in edges if 0 <= e < w.Sq)
+        pick |= {max(L - 1, 0), min(L, w.Sq - 1)}
+        for h in (0, w.Hq - 1):
+            q_rows += [(b * w.Hq + h) * w.Sq + q for q in sorted(pick)]
+        for hk in (0, w.Hkv - 1):
+            kv_rows += [(b * w.Hkv + hk) * w.Skv + k for k in sorted(pick) if k < w.Skv]
+    q_rows += list(rng.integers(0, w.B * w.Hq * w.Sq, n_rand))
+    kv_rows += list(rng.integers(0, w.B * w.Hkv * w.Skv, n_rand))
+    return np.unique(np.array(q_rows)), np.unique(np.array(kv_rows))
+
+
+@pytest.mark.parametrize("name", ["tiny_dense", "causal_mha", "causal_gqa_det", "swa_causal_padded"])
+def test_workload_sampled_parity(name):
+    case = _case(name)
+    w = case["workload"]
+    dq, dk, dv = gpu_backward(case)
+    lens = None if case["seq_q_lens"] is None else case["seq_q_lens"].numpy()
+    q_rows, kv_rows = _sample_rows(w, lens, np.random.default_rng(w.seed))
+    rq, rk, rv = oracle_sampled(case, q_rows, kv_rows)
+    gq = dq.reshape(-1, w.Dqk)[torch.from_numpy(q_rows).cuda()].double().cpu().numpy()
+    gk = dk.reshape(-1, w.Dqk)[torch.from_numpy(kv_rows).cuda()].double().cpu().numpy()
+    gv = dv.reshape(-1, w.Dv)[torch.from_numpy(kv_rows).cuda()].double().cpu().numpy()
+    assert_close("dq", gq, rq)
+    assert_close("dk", gk, rk)
+    assert_close("dv", gv, rv)
+    for g in (dq, dk, dv):
+        assert torch.isfinite(g).all()
+    if lens is not None:
+        for b, L in enumerate(lens):
+            assert torch.all(dq[b, :, L:] == 0) and torch.all(dk[b, :, L:] == 0)
+            assert torch.all(dv[b, :, L:] == 0)
+
+
+def test_workload_deterministic_bitwise_10_runs():
+    case = _case("causal_gqa_det")
+    d = to_device(case)
+    first = gpu_backward(case, d)
+    for _ in range(9):
+        again = gpu_backward(case, d, poison=True)
+        for a, b in zip(first, again):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
