@@ -124,6 +124,33 @@ int sdpa_bwd_check_device_status(void* stream);
 int sdpa_bwd_profile_enable(int on);
 int sdpa_bwd_profile_read(float* ms, int* launches, int n);
 
+/*
+ * Allocation-free SDPA backward. The SDPA backward pages have no counterpart
+ * to this entry point; it exists for callers that cannot allocate device
+ * memory where they run the backward (plugins or foreign-function hooks of a
+ * framework that already owns the whole device memory pool, where cudaMalloc
+ * fails or fragments the pool, and latency-critical code that cannot accept
+ * cudaMalloc's implicit synchronization).
+ *
+ * Same arguments and results as sdpa_bwd() without the workspace: the caller
+ * still provides every input and output, and the chain's scratch memory comes
+ * from a 16 MiB device array compiled into the library (held on every GPU that
+ * loads the library until the process exits). It calls no allocator.
+ *   - Problems whose sdpa_bwd_workspace_size() exceeds 16 MiB (16777216 bytes)
+ *     return SDPA_ERR_WORKSPACE before anything is launched.
+ *   - All calls on a device share that array and it keeps what the last call
+ *     left; the kernels re-clear what must start at zero on every call, but
+ *     calls whose work overlaps on the device race on the array.
+ *   - The first call on each device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ */
+int sdpa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                     const void* d_o, const float* lse, void* dq, void* dk, void* dv, int B,
+                     int H_q, int H_kv, int S_q, int S_kv, int D_qk, int D_v, float scale,
+                     int causal, int bottom_right, int window_left, int window_right,
+                     int deterministic, const int32_t* seq_q_lens, const int32_t* seq_kv_lens,
+                     void* stream);
+
 /* Library ABI version (major * 100 + minor). */
 int sdpa_bwd_version(void);
 
