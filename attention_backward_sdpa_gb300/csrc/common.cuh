@@ -12,13 +12,13 @@
 namespace sdpa {
 
 // Tile sizes of the KV-stationary main kernel: one CTA owns BN keys of one
-// query head and walks the query tiles of BM rows.
-constexpr int BM = 128;
+// query head and walks the query tiles of BQ rows.
 constexpr int BN = 128;
+constexpr int BQ = 64;
 
-// Row statistics staged per query tile: BM values of LSE * log2(e) (+inf for
-// masked or empty rows) followed by BM values of delta.
-constexpr int QSTAT_FLOATS = 2 * BM;
+// Row statistics staged per query tile: BQ values of LSE * log2(e) (+inf for
+// masked or empty rows) followed by BQ values of delta.
+constexpr int QSTAT_FLOATS = 2 * BQ;
 
 // Device status bits (OR-ed into the per-device status word).
 constexpr int STATUS_TIMEOUT = 1;
@@ -27,7 +27,7 @@ constexpr int STATUS_SMEM_ALIGN = 2;
 struct ChainParams {
   int B, Hq, Hkv, Sq, Skv, Dqk, Dv;
   int G;            // Hq / Hkv
-  int n_qt, n_kt;   // ceil(Sq / BM), ceil(Skv / BN)
+  int n_qt, n_kt;   // ceil(Sq / BQ), ceil(Skv / BN)
   float scale;      // softmax scale
   float scale_log2; // scale * log2(e)
   int causal, bottom_right, window_left, window_right, deterministic;
@@ -45,7 +45,7 @@ struct ChainParams {
 
   // workspace regions
   float* qstat;         // [B*Hq][n_qt][QSTAT_FLOATS]
-  float* dq_accum;      // [B*Hq][n_qt][Dqk/4][BM][4]
+  float* dq_accum;      // [B*Hq][n_qt*BQ][Dqk] row-major, rows padded to whole tiles
   int* counters;        // [B*Hq][n_qt] turn counters (deterministic mode)
   int* ticket;          // work-unit ticket
   __nv_bfloat16* dk_ws; // GQA: [B][Hq][Skv][Dqk] partials, else null

@@ -16,7 +16,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/sdpa_bwd.h"
+#include "sdpa_bwd.h"
 #include "common.cuh"
 #include "tmap.h"
 
@@ -46,14 +46,14 @@ struct Carve {
 };
 
 Carve carve(int B, int Hq, int Hkv, int Sq, int Skv, int Dqk, int Dv) {
-  const size_t n_qt = (size_t)ceil_div(Sq, BM);
+  const size_t n_qt = (size_t)ceil_div(Sq, BQ);
   const size_t bh = (size_t)B * Hq;
   Carve c{};
   size_t off = 0;
   c.qstat = off;
   off = align256(off + bh * n_qt * QSTAT_FLOATS * sizeof(float));
   c.dq_accum = off;
-  off = align256(off + bh * n_qt * BM * (size_t)Dqk * sizeof(float));
+  off = align256(off + bh * n_qt * BQ * (size_t)Dqk * sizeof(float));
   c.counters = off;
   off = align256(off + (bh * n_qt + 1) * sizeof(int));
   if (Hkv < Hq) {
@@ -104,10 +104,12 @@ int device_state(int dev, int** status_out, int* sms_out) {
   return SDPA_OK;
 }
 
-bool make_bhsd_map(CUtensorMap* m, const void* base, int D, int S, long long BH) {
+// 3-D map {D, S, B*H} of a contiguous (B, H, S, D) bf16 tensor; boxes of 64
+// columns (128 bytes, the swizzle span) by `rows` sequence positions.
+bool make_bhsd_map(CUtensorMap* m, const void* base, int D, int S, long long BH, int rows) {
   const uint64_t dims[3] = {(uint64_t)D, (uint64_t)S, (uint64_t)BH};
   const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)S * D * 2};
-  const uint32_t box[3] = {64, (uint32_t)BM, 1};
+  const uint32_t box[3] = {64, (uint32_t)rows, 1};
   return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box,
                    CU_TENSOR_MAP_SWIZZLE_128B);
 }
@@ -260,7 +262,7 @@ int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const v
   ChainParams p{};
   p.B = B; p.Hq = H_q; p.Hkv = H_kv; p.Sq = S_q; p.Skv = S_kv; p.Dqk = D_qk; p.Dv = D_v;
   p.G = H_q / H_kv;
-  p.n_qt = ceil_div(S_q, BM);
+  p.n_qt = ceil_div(S_q, BQ);
   p.n_kt = ceil_div(S_kv, BN);
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
@@ -288,8 +290,10 @@ int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const v
 
   MainMaps maps;
   const long long BHq = (long long)B * H_q, BHkv = (long long)B * H_kv;
-  if (!make_bhsd_map(&maps.q, q, D_qk, S_q, BHq) || !make_bhsd_map(&maps.k, k, D_qk, S_kv, BHkv) ||
-      !make_bhsd_map(&maps.v, v, D_v, S_kv, BHkv) || !make_bhsd_map(&maps.d_o, d_o, D_v, S_q, BHq)) {
+  if (!make_bhsd_map(&maps.q, q, D_qk, S_q, BHq, BQ) ||
+      !make_bhsd_map(&maps.k, k, D_qk, S_kv, BHkv, BN) ||
+      !make_bhsd_map(&maps.v, v, D_v, S_kv, BHkv, BN) ||
+      !make_bhsd_map(&maps.d_o, d_o, D_v, S_q, BHq, BQ)) {
     if (own_ws) cudaFreeAsync(workspace, stream);
     return SDPA_ERR_CUDA;
   }

@@ -4,8 +4,8 @@
 //               LSE * log2(e) (+inf for masked rows and LSE = -inf), staged
 //               per query tile; clears the fp32 dQ accumulator and the
 //               deterministic-mode counters. ("The kernel chain": dot.)
-//   dq_convert  dQ = bf16(scale * dq_accum), undoing the accumulator's
-//               tile order. ("The kernel chain": cvt.)
+//   dq_convert  dQ = bf16(scale * dq_accum), dropping the accumulator's
+//               padding rows. ("The kernel chain": cvt.)
 //   gqa_reduce  dK/dV of each KV head = fp32 sum of its group's per-query-head
 //               partials in ascending head order, rounded to bf16.
 //               ("GQA/MQA group reduction".)
@@ -43,17 +43,17 @@ __global__ void __launch_bounds__(256) sdpa_bwd_preprocess(const ChainParams p) 
   const int lane = threadIdx.x & 31;
   const unsigned group_mask = (TPR == 32 ? 0xFFFFFFFFu : ((1u << TPR) - 1u) << (lane / TPR * TPR));
   const int sub = threadIdx.x % TPR;
-  const long long rows = (long long)p.B * p.Hq * p.n_qt * BM;
+  const long long rows = (long long)p.B * p.Hq * p.n_qt * BQ;
   const long long nthreads = (long long)gridDim.x * blockDim.x;
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
 
   for (long long r = tid / TPR; r < rows; r += nthreads / TPR) {
-    const int qi = (int)(r % BM);
-    const long long t = r / BM;
+    const int qi = (int)(r % BQ);
+    const long long t = r / BQ;
     const int qt = (int)(t % p.n_qt);
     const long long bh = t / p.n_qt;
     const int b = (int)(bh / p.Hq);
-    const int q = qt * BM + qi;
+    const int q = qt * BQ + qi;
     int Lq, Lk;
     batch_lengths(p, b, Lq, Lk);
     float dot = 0.f;
@@ -76,52 +76,41 @@ __global__ void __launch_bounds__(256) sdpa_bwd_preprocess(const ChainParams p) 
       }
       float* qs = p.qstat + t * QSTAT_FLOATS;
       qs[qi] = lse2;
-      qs[BM + qi] = delta;
+      qs[BQ + qi] = delta;
     }
   }
 
   // Clear the dQ accumulator and the counters (+ ticket).
   float4* acc = reinterpret_cast<float4*>(p.dq_accum);
-  const long long n4 = (long long)p.B * p.Hq * p.n_qt * BM * p.Dqk / 4;
+  const long long n4 = (long long)p.B * p.Hq * p.n_qt * BQ * p.Dqk / 4;
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
   for (long long i = tid; i < n4; i += nthreads) acc[i] = z;
   for (long long i = tid; i < p.n_counters; i += nthreads) p.counters[i] = 0;
 }
 
 // ---------------------------------------------------------------- dq convert
-// dq_accum tile layout: [Dqk/4 column quads][BM rows][4] per (b, h, q tile).
+// dq_accum: [B*Hq][n_qt*BQ][Dqk] fp32, row-major; rows past S_q are padding.
 template <int DQK>
 __global__ void __launch_bounds__(256) sdpa_bwd_dq_convert(const ChainParams p) {
   pdl_wait_prior_grid();
-  __shared__ __align__(16) float tile[32][DQK + 4];
-  const long long n_slices = (long long)p.B * p.Hq * p.n_qt * (BM / 32);
-  for (long long slice = blockIdx.x; slice < n_slices; slice += gridDim.x) {
-    const int s32 = (int)(slice % (BM / 32));
-    const long long tq = slice / (BM / 32);  // (b*Hq + h)*n_qt + qt
-    const int qt = (int)(tq % p.n_qt);
-    const long long bh = tq / p.n_qt;
-    const int q_base = qt * BM + s32 * 32;
-    if (q_base >= p.Sq) continue;  // uniform across the block
-    const float* src = p.dq_accum + tq * (long long)BM * DQK;
-    for (int i = threadIdx.x; i < 32 * (DQK / 4); i += blockDim.x) {
-      const int c = i / 32, r = i % 32;
-      const float4 v = *reinterpret_cast<const float4*>(src + ((long long)c * BM + s32 * 32 + r) * 4);
-      *reinterpret_cast<float4*>(&tile[r][4 * c]) = v;
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < 32 * (DQK / 8); i += blockDim.x) {
-      const int r = i / (DQK / 8), c8 = i % (DQK / 8);
-      const int q = q_base + r;
-      if (q < p.Sq) {
-        uint4 out;
-        out.x = pack_bf16x2(tile[r][c8 * 8 + 0] * p.scale, tile[r][c8 * 8 + 1] * p.scale);
-        out.y = pack_bf16x2(tile[r][c8 * 8 + 2] * p.scale, tile[r][c8 * 8 + 3] * p.scale);
-        out.z = pack_bf16x2(tile[r][c8 * 8 + 4] * p.scale, tile[r][c8 * 8 + 5] * p.scale);
-        out.w = pack_bf16x2(tile[r][c8 * 8 + 6] * p.scale, tile[r][c8 * 8 + 7] * p.scale);
-        *reinterpret_cast<uint4*>(p.dq + (bh * p.Sq + q) * (long long)DQK + c8 * 8) = out;
-      }
-    }
-    __syncthreads();
+  constexpr int PER_ROW = DQK / 8;
+  const long long total = (long long)p.B * p.Hq * p.Sq * PER_ROW;
+  const long long nthreads = (long long)gridDim.x * blockDim.x;
+  const long long rows_pad = (long long)p.n_qt * BQ;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += nthreads) {
+    const int c8 = (int)(i % PER_ROW);
+    const long long r = i / PER_ROW;  // (b*Hq + h)*Sq + q
+    const long long bh = r / p.Sq;
+    const int q = (int)(r % p.Sq);
+    const float* src = p.dq_accum + (bh * rows_pad + q) * DQK + c8 * 8;
+    const float4 a = *reinterpret_cast<const float4*>(src);
+    const float4 c = *reinterpret_cast<const float4*>(src + 4);
+    uint4 out;
+    out.x = pack_bf16x2(a.x * p.scale, a.y * p.scale);
+    out.y = pack_bf16x2(a.z * p.scale, a.w * p.scale);
+    out.z = pack_bf16x2(c.x * p.scale, c.y * p.scale);
+    out.w = pack_bf16x2(c.z * p.scale, c.w * p.scale);
+    *reinterpret_cast<uint4*>(p.dq + r * DQK + c8 * 8) = out;
   }
 }
 

@@ -28,7 +28,7 @@
 #include <cstdint>
 #include <mutex>
 
-#include "../../include/sdpa_bwd.h"
+#include "sdpa_bwd.h"
 
 namespace {
 

@@ -51,12 +51,13 @@ def _a256(x):
 
 
 def expected_workspace(B, Hq, Hkv, Sq, Skv, Dqk, Dv):
-    """Documented layout: per-query-tile row statistics (2 x 128 fp32), the fp32 dQ
-    accumulator over whole 128-row tiles, one int per query tile plus a ticket, and
-    for GQA the bf16 dK/dV partials with H_q heads; every region 256-byte aligned."""
-    n_qt = -(-Sq // 128)
-    total = _a256(B * Hq * n_qt * 256 * 4)
-    total += _a256(B * Hq * n_qt * 128 * Dqk * 4)
+    """Documented layout: per-query-tile row statistics (2 x 64 fp32 per 64-row tile),
+    the fp32 dQ accumulator over whole 64-row tiles, one int per query tile plus a
+    ticket, and for GQA the bf16 dK/dV partials with H_q heads; every region
+    256-byte aligned."""
+    n_qt = -(-Sq // 64)
+    total = _a256(B * Hq * n_qt * 128 * 4)
+    total += _a256(B * Hq * n_qt * 64 * Dqk * 4)
     total += _a256((B * Hq * n_qt + 1) * 4)
     if Hkv < Hq:
         total += _a256(B * Hq * Skv * Dqk * 2) + _a256(B * Hq * Skv * Dv * 2)
