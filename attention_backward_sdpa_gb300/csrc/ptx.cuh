@@ -275,6 +275,15 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// True on exactly one (the same) lane of a converged warp.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t e;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(e));
+  return e != 0;
+}
+
 // Per-warp register budget changes (executed by every warp of a warpgroup).
 template <uint32_t N>
 __device__ __forceinline__ void regs_increase() {

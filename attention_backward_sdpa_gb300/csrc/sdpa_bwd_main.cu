@@ -18,18 +18,18 @@
 // Schedule. Two query tiles are in flight: tensor memory holds two slots, each
 // with S^T and dP^T (dQ^T reuses the dP^T columns once dS is formed). Compute
 // warpgroup 0 owns the even tiles (slot 0), warpgroup 1 the odd ones (slot 1).
-// The MMA thread issues G1/G2 of tile t and then G3/G4/G5 of tile t-1, so the
-// tensor core works on one tile while a warpgroup replays the softmax of the
-// other. A third warpgroup moves each dQ^T tile from tensor memory to shared
-// memory and hands it to the TMA engine as one bulk reduction (in deterministic
-// mode after waiting its turn on the query tile's counter).
+// One MMA warp issues G1/G2 of tile t while the other issues G3/G4/G5 of tile
+// t-1, so the tensor core works on one tile while a warpgroup replays the
+// softmax of the other. A third warpgroup moves each dQ^T tile from tensor
+// memory to shared memory and hands it to the TMA engine as one bulk reduction
+// (in deterministic mode after waiting its turn on the query tile's counter).
 //
 // Warps: 0-3 slot-0 compute, 4-7 slot-1 compute, 8-11 dQ, 12 TMA producer,
-// 13 MMA issuer and tensor-memory owner, 14-15 idle (they complete the fourth
-// warpgroup so that register budgets can be moved between warpgroups: launched
-// with 128 registers per thread, the compute warpgroups grow to 168 while the dQ
-// warpgroup shrinks to 104 and the producer/MMA warpgroup to 72; 128 threads x
-// (168 + 168 + 104 + 72) = 65536 = 512 threads x 128).
+// 13 score-GEMM issuer and tensor-memory owner, 14 gradient-GEMM issuer, 15 idle
+// (it completes the fourth warpgroup so that register budgets can be moved
+// between warpgroups: launched with 128 registers per thread, the compute
+// warpgroups grow to 160 while the dQ and control warpgroups shrink to 96;
+// 128 threads x (160 + 160 + 96 + 96) = 65536 = 512 threads x 128).
 //
 // Shared memory (128-byte swizzle, every tile 1024-byte aligned):
 //   K, V        [D/64 blocks][128 key rows][128 B]
@@ -50,7 +50,7 @@
 namespace sdpa {
 
 constexpr int MAIN_THREADS = 512;
-constexpr uint32_t REGS_COMPUTE = 168, REGS_DQ = 104, REGS_CTRL = 72;
+constexpr uint32_t REGS_COMPUTE = 160, REGS_DQ = 96, REGS_CTRL = 96;
 static_assert(128 * (2 * REGS_COMPUTE + REGS_DQ + REGS_CTRL) <= MAIN_THREADS * 128,
               "register split exceeds the launch budget");
 constexpr int NSTAGE = 3;
@@ -217,10 +217,14 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
                   p.qstat + ((long long)bh * p.n_qt + qt) * QSTAT_FLOATS, QSTAT_FLOATS * 4, full);
       }
     }
-    } else if (warp == 13) {
-    // ------------------------------------------------------------ MMA issuer
-    pdl_wait_prior_grid();
-    if (lane == 0 && n > 0) {
+    } else if (warp == 13 || warp == 14) {
+      // ---------------------------------------------------------- MMA issuers
+      // A tcgen05.mma costs its issuing thread on the order of 100 cycles, more
+      // than a 64-column MMA takes on the tensor core, so two warps issue: warp
+      // 13 the score GEMMs G1/G2 of every tile, warp 14 the gradient GEMMs
+      // G3/G4/G5. Each warp stays converged and issues from one elected lane;
+      // mbarriers carry every dependency between the two streams.
+      pdl_wait_prior_grid();
       constexpr uint32_t ID_G12 = idesc_bf16_f32(128, BQ, false, false);  // S^T, dP^T
       constexpr uint32_t ID_G34 = idesc_bf16_f32(128, D, false, true);    // dV, dK
       constexpr uint32_t ID_G5 = idesc_bf16_f32(128, BQ, true, true);     // dQ^T (rows >= D unused)
@@ -228,9 +232,9 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
       constexpr uint64_t T_MN_Q = sdesc_sw128_template(L::BLK_Q, 1024);    // MN-major, 64-row tiles
       constexpr uint64_t T_MN_KV = sdesc_sw128_template(L::BLK_KV, 1024);  // MN-major, 128-row tiles
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
-      bool ok = mbar_wait(&bars[BAR_KV], 0, abort_flag, WAIT_LIMIT_NS);
-      for (int t = 0; t <= n && ok; ++t) {
-        if (t < n) {
+      bool ok = n > 0 && mbar_wait(&bars[BAR_KV], 0, abort_flag, WAIT_LIMIT_NS);
+      if (warp == 13) {
+        for (int t = 0; t < n && ok; ++t) {
           const int s = t & 1, st = t % NSTAGE, j = t >> 1;
           const uint32_t aQ = smem_u32(sQ + st * L::TILE_Q);
           const uint32_t aDO = smem_u32(sDO + st * L::TILE_Q);
@@ -238,61 +242,81 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
           // The slot's S^T columns hold P^T of tile t-2 until its G3 completes.
           if (ok && t >= 2) ok = mbar_wait(&bars[BAR_SFREE + s], (j - 1) & 1, abort_flag, WAIT_LIMIT_NS);
           if (!ok) break;
+          __syncwarp();
           tc_fence_after();
-          // G1: S^T[key, q] = sum_d K[key, d] Q[q, d]   (both K-major)
+          if (elect_one()) {
+            // G1: S^T[key, q] = sum_d K[key, d] Q[q, d]   (both K-major)
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t kk = (k >> 2) * L::BLK_KV + (k & 3) * 32;
-            const uint32_t kq = (k >> 2) * L::BLK_Q + (k & 3) * 32;
-            mma_ss(tmem + L::col_s(s), sdesc_at(T_KMAJ, aK + kk), sdesc_at(T_KMAJ, aQ + kq), ID_G12,
-                   k > 0);
+            for (int k = 0; k < D / 16; ++k) {
+              const uint32_t kk = (k >> 2) * L::BLK_KV + (k & 3) * 32;
+              const uint32_t kq = (k >> 2) * L::BLK_Q + (k & 3) * 32;
+              mma_ss(tmem + L::col_s(s), sdesc_at(T_KMAJ, aK + kk), sdesc_at(T_KMAJ, aQ + kq), ID_G12,
+                     k > 0);
+            }
+            mma_commit(&bars[BAR_SFULL + s]);
           }
-          mma_commit(&bars[BAR_SFULL + s]);
+          __syncwarp();
           // The slot's dP^T columns hold dQ^T of tile t-2 until it is read out.
           if (t >= 2 && !mbar_wait(&bars[BAR_DQEMPTY + s], (j - 1) & 1, abort_flag, WAIT_LIMIT_NS)) break;
+          __syncwarp();
           tc_fence_after();
-          // G2: dP^T[key, q] = sum_d V[key, d] dO[q, d]
+          if (elect_one()) {
+            // G2: dP^T[key, q] = sum_d V[key, d] dO[q, d]
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t kk = (k >> 2) * L::BLK_KV + (k & 3) * 32;
-            const uint32_t kq = (k >> 2) * L::BLK_Q + (k & 3) * 32;
-            mma_ss(tmem + L::col_dp(s), sdesc_at(T_KMAJ, aV + kk), sdesc_at(T_KMAJ, aDO + kq), ID_G12,
-                   k > 0);
+            for (int k = 0; k < D / 16; ++k) {
+              const uint32_t kk = (k >> 2) * L::BLK_KV + (k & 3) * 32;
+              const uint32_t kq = (k >> 2) * L::BLK_Q + (k & 3) * 32;
+              mma_ss(tmem + L::col_dp(s), sdesc_at(T_KMAJ, aV + kk), sdesc_at(T_KMAJ, aDO + kq), ID_G12,
+                     k > 0);
+            }
+            mma_commit(&bars[BAR_DPFULL + s]);
           }
-          mma_commit(&bars[BAR_DPFULL + s]);
+          __syncwarp();
         }
-        if (t >= 1) {
-          const int u = t - 1, su = u & 1, stu = u % NSTAGE, ju = u >> 1;
+      } else {
+        for (int u = 0; u < n && ok; ++u) {
+          const int su = u & 1, stu = u % NSTAGE, ju = u >> 1;
           const uint32_t aQ = smem_u32(sQ + stu * L::TILE_Q);
           const uint32_t aDO = smem_u32(sDO + stu * L::TILE_Q);
           const uint32_t aDS = smem_u32(sDS + su * L::TILE_DS);
           if (!mbar_wait(&bars[BAR_PREADY + su], ju & 1, abort_flag, WAIT_LIMIT_NS)) break;
+          __syncwarp();
           tc_fence_after();
-          // G3: dV[key, d] += sum_q P^T[key, q] dO[q, d]; P^T pairs in columns [0,32) of the slot.
+          if (elect_one()) {
+            // G3: dV[key, d] += sum_q P^T[key, q] dO[q, d]; P^T pairs in columns [0,32) of the slot.
 #pragma unroll
-          for (int k = 0; k < BQ / 16; ++k)
-            mma_ts(tmem + L::COL_DV, tmem + L::col_s(su) + 8 * k, sdesc_at(T_MN_Q, aDO + k * 2048),
-                   ID_G34, (u > 0 || k > 0));
-          mma_commit(&bars[BAR_SFREE + su]);
+            for (int k = 0; k < BQ / 16; ++k)
+              mma_ts(tmem + L::COL_DV, tmem + L::col_s(su) + 8 * k, sdesc_at(T_MN_Q, aDO + k * 2048),
+                     ID_G34, (u > 0 || k > 0));
+            mma_commit(&bars[BAR_SFREE + su]);
+          }
+          __syncwarp();
           if (!mbar_wait(&bars[BAR_DSREADY + su], ju & 1, abort_flag, WAIT_LIMIT_NS)) break;
+          __syncwarp();
           tc_fence_after();
-          // G4: dK[key, d] += sum_q dS^T[key, q] Q[q, d]   (dS^T K-major, Q MN-major)
+          if (elect_one()) {
+            // G4: dK[key, d] += sum_q dS^T[key, q] Q[q, d]   (dS^T K-major, Q MN-major)
 #pragma unroll
-          for (int k = 0; k < BQ / 16; ++k)
-            mma_ss(tmem + L::COL_DK, sdesc_at(T_KMAJ, aDS + k * 32), sdesc_at(T_MN_Q, aQ + k * 2048),
-                   ID_G34, (u > 0 || k > 0));
-          if (u + NSTAGE < n) mma_commit(&bars[BAR_QEMPTY + stu]);  // stage refilled for u+3
-          // G5: dQ^T[d, q] = sum_key K[key, d] dS^T[key, q]   (both MN-major)
+            for (int k = 0; k < BQ / 16; ++k)
+              mma_ss(tmem + L::COL_DK, sdesc_at(T_KMAJ, aDS + k * 32), sdesc_at(T_MN_Q, aQ + k * 2048),
+                     ID_G34, (u > 0 || k > 0));
+            // Stage u is refilled for tile u+3 once G4 is done (G1/G2 of tile u
+            // completed before P_READY / DS_READY could arrive).
+            if (u + NSTAGE < n) mma_commit(&bars[BAR_QEMPTY + stu]);
+            // G5: dQ^T[d, q] = sum_key K[key, d] dS^T[key, q]   (both MN-major)
 #pragma unroll
-          for (int k = 0; k < BN / 16; ++k)
-            mma_ss(tmem + L::col_dp(su), sdesc_at(T_MN_KV, aK + k * 2048),
-                   sdesc_at(T_MN_KV, aDS + k * 2048), ID_G5, k > 0);
-          mma_commit(&bars[BAR_DQFULL + su]);
+            for (int k = 0; k < BN / 16; ++k)
+              mma_ss(tmem + L::col_dp(su), sdesc_at(T_MN_KV, aK + k * 2048),
+                     sdesc_at(T_MN_KV, aDS + k * 2048), ID_G5, k > 0);
+            mma_commit(&bars[BAR_DQFULL + su]);
+          }
+          __syncwarp();
         }
+        // After the last tile (also releases the epilogue on abort).
+        if (n > 0 && elect_one()) mma_commit(&bars[BAR_MMADONE]);
+        __syncwarp();
       }
-      mma_commit(&bars[BAR_MMADONE]);  // after the last tile (also releases the epilogue on abort)
-    }
-    }  // warps 14-15: idle members of the control warpgroup
+    }  // warp 15: idle member of the control warpgroup
   } else if (warp >= 8) {
     // ------------------------------------------------------------ dQ warpgroup
     regs_decrease<REGS_DQ>();
