@@ -22,7 +22,7 @@ from . import _build
 __all__ = ["sdpa_bwd", "workspace_size", "check_device_status", "profile_enable", "profile_read",
            "library_path", "load", "SdpaError", "KERNEL_NAMES"]
 
-KERNEL_NAMES = ("preprocess", "main", "gqa_reduce", "dq_convert")
+KERNEL_NAMES = ("preprocess", "main", "gqa_reduce", "dq")
 
 _STATUS = {0: "SDPA_OK", 1: "SDPA_ERR_INVALID", 2: "SDPA_ERR_UNSUPPORTED", 3: "SDPA_ERR_ALIGN",
            4: "SDPA_ERR_WORKSPACE", 5: "SDPA_ERR_CUDA", 6: "SDPA_ERR_TIMEOUT"}

@@ -52,8 +52,41 @@ struct ChainParams {
   __nv_bfloat16* dv_ws; // GQA: [B][Hq][Skv][Dv]
   int n_counters;       // B*Hq*n_qt + 1 (counters plus ticket)
 
+  // Deterministic two-kernel route: the main kernel stores each bf16 dS^T tile
+  // (its swizzled shared-memory image, DS_TILE_BYTES) at
+  // ds_ws + ((bh * n_kt + kt) * n_qt + qt) * DS_TILE_BYTES, and the dQ kernel
+  // reads them back in ascending key-tile order. zero_tile is DS_TILE_BYTES of
+  // zeros standing in for tiles the main kernel never visits.
+  int ds_route;
+  uint8_t* ds_ws;
+  uint8_t* zero_tile;
+
   int* status;          // per-device status word
 };
+
+constexpr int DS_TILE_BYTES = BN * BQ * 2;  // one dS^T tile: 128 keys x 64 queries, bf16
+
+// Query tiles [qt_lo, qt_hi] (of BQ rows) that key tile kt visits for batch row
+// b: loop bounds of "Causal, sliding-window, and padding masks". Empty when
+// qt_lo > qt_hi. Shared by the main kernel and the dQ kernel so that both walk
+// exactly the same (key tile, query tile) pairs.
+__host__ __device__ inline void visited_query_tiles(int kt, int Lq, int Lk, int causal,
+                                                    int bottom_right, int window_left,
+                                                    int window_right, int& qt_lo, int& qt_hi) {
+  qt_lo = 0;
+  qt_hi = -1;
+  const int k0 = kt * BN;
+  if (k0 >= Lk || Lq <= 0) return;
+  const long long diag = bottom_right ? (long long)Lk - Lq : 0;
+  const long long Rp = window_right > 0 ? window_right : 0;
+  const long long k_last = (k0 + BN - 1 < Lk - 1) ? k0 + BN - 1 : Lk - 1;
+  long long q_min = 0, q_max = Lq - 1;
+  if (causal) q_min = (k0 - diag - Rp > 0) ? k0 - diag - Rp : 0;
+  if (window_left >= 0 && k_last - diag + window_left < q_max) q_max = k_last - diag + window_left;
+  if (q_min > q_max) return;
+  qt_lo = (int)(q_min / BQ);
+  qt_hi = (int)(q_max / BQ);
+}
 
 // TMA tensor maps of the main kernel (K and V with H_kv heads, Q and dO with H_q).
 struct MainMaps {
@@ -67,6 +100,8 @@ cudaError_t launch_preprocess(const ChainParams& p, int grid, cudaStream_t s);
 cudaError_t launch_main(const MainMaps& maps, const ChainParams& p, cudaStream_t s);
 cudaError_t launch_gqa_reduce(const ChainParams& p, int grid, cudaStream_t s);
 cudaError_t launch_dq_convert(const ChainParams& p, int grid, cudaStream_t s);
+cudaError_t launch_dq_from_ds(const CUtensorMap& k_map, const ChainParams& p, cudaStream_t s);
+cudaError_t dq_kernel_setup();  // per device: opt in to the dQ kernel's shared memory
 cudaError_t main_kernel_setup();  // per device: opt in to the main kernel's shared memory
 
 template <typename... KArgs, typename... Args>

@@ -106,6 +106,13 @@ __device__ __forceinline__ void bulk_reduce_add_f32(float* dst, const void* src,
       "r"(smem_u32(src)), "r"(bytes)
       : "memory");
 }
+// Bulk copy shared -> global (both 16-byte aligned, bytes % 16 == 0).
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                   reinterpret_cast<uint64_t>(dst)),
+               "r"(smem_u32(src)), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -116,6 +123,10 @@ __device__ __forceinline__ void bulk_wait_group_read0() {
 // Waits until every committed bulk group has completed (global writes done).
 __device__ __forceinline__ void bulk_wait_group0() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Waits until all but the most recent committed bulk group have completed.
+__device__ __forceinline__ void bulk_wait_group1() {
+  asm volatile("cp.async.bulk.wait_group 1;" ::: "memory");
 }
 // Orders generic-proxy and async-proxy accesses to global memory.
 __device__ __forceinline__ void fence_proxy_async_global() {

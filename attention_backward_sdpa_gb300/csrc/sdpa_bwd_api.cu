@@ -41,19 +41,32 @@ int g_prof_n[4] = {};
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Deterministic two-kernel route (dS stored, dQ from a Q-stationary kernel):
+// taken for D_qk = 128 as on the pages (the relay serves the other head dims).
+bool use_ds_route(int deterministic, int Dqk) { return deterministic && Dqk == 128; }
+
 struct Carve {
-  size_t qstat, dq_accum, counters, dk_ws, dv_ws, total;
+  size_t qstat, dq_accum, ds_ws, zero_tile, counters, dk_ws, dv_ws, total;
 };
 
-Carve carve(int B, int Hq, int Hkv, int Sq, int Skv, int Dqk, int Dv) {
-  const size_t n_qt = (size_t)ceil_div(Sq, BQ);
+Carve carve(int B, int Hq, int Hkv, int Sq, int Skv, int Dqk, int Dv, bool ds_route) {
+  const size_t n_qt = (size_t)ceil_div(Sq, BQ), n_kt = (size_t)ceil_div(Skv, BN);
   const size_t bh = (size_t)B * Hq;
   Carve c{};
   size_t off = 0;
   c.qstat = off;
   off = align256(off + bh * n_qt * QSTAT_FLOATS * sizeof(float));
-  c.dq_accum = off;
-  off = align256(off + bh * n_qt * BQ * (size_t)Dqk * sizeof(float));
+  if (ds_route) {
+    c.dq_accum = SIZE_MAX;
+    c.ds_ws = off;
+    off = align256(off + bh * n_kt * n_qt * (size_t)DS_TILE_BYTES);
+    c.zero_tile = off;
+    off = align256(off + DS_TILE_BYTES);
+  } else {
+    c.ds_ws = c.zero_tile = SIZE_MAX;
+    c.dq_accum = off;
+    off = align256(off + bh * n_qt * BQ * (size_t)Dqk * sizeof(float));
+  }
   c.counters = off;
   off = align256(off + (bh * n_qt + 1) * sizeof(int));
   if (Hkv < Hq) {
@@ -94,7 +107,8 @@ int device_state(int dev, int** status_out, int* sms_out) {
       void* p = nullptr;
       if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return SDPA_ERR_CUDA;
       g_status_ptr[dev] = static_cast<int*>(p);
-      if (main_kernel_setup() != cudaSuccess) return SDPA_ERR_CUDA;
+      if (main_kernel_setup() != cudaSuccess || dq_kernel_setup() != cudaSuccess)
+        return SDPA_ERR_CUDA;
     }
     g_device_checked[dev] = true;
   }
@@ -172,10 +186,9 @@ const char* sdpa_status_string(int status) {
 
 size_t sdpa_bwd_workspace_size(int B, int H_q, int H_kv, int S_q, int S_kv, int D_qk, int D_v,
                                int deterministic) {
-  (void)deterministic;
   if (basic_checks(B, H_q, H_kv, S_q, S_kv, D_qk, D_v) != SDPA_OK) return 0;
   if (S_q == 0 || S_kv == 0) return 0;
-  return carve(B, H_q, H_kv, S_q, S_kv, D_qk, D_v).total;
+  return carve(B, H_q, H_kv, S_q, S_kv, D_qk, D_v, use_ds_route(deterministic, D_qk)).total;
 }
 
 int sdpa_bwd_profile_enable(int on) {
@@ -248,7 +261,8 @@ int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const v
     return SDPA_OK;
   }
 
-  const Carve cv = carve(B, H_q, H_kv, S_q, S_kv, D_qk, D_v);
+  const bool ds_route = use_ds_route(deterministic, D_qk);
+  const Carve cv = carve(B, H_q, H_kv, S_q, S_kv, D_qk, D_v, ds_route);
   bool own_ws = false;
   if (workspace == nullptr) {
     if (cudaMallocAsync(&workspace, cv.total, stream) != cudaSuccess) return SDPA_ERR_CUDA;
@@ -270,7 +284,10 @@ int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const v
   p.bottom_right = bottom_right ? 1 : 0;
   p.window_left = window_left < 0 ? -1 : window_left;
   p.window_right = (causal && window_right > 0) ? window_right : -1;
-  p.deterministic = deterministic ? 1 : 0;
+  // The two-kernel route is deterministic by construction (no cross-CTA
+  // reduction); `deterministic` inside the kernels selects the ordered relay.
+  p.deterministic = (deterministic && !ds_route) ? 1 : 0;
+  p.ds_route = ds_route ? 1 : 0;
   p.seq_q_lens = seq_q_lens;
   p.seq_kv_lens = seq_kv_lens;
   p.o = static_cast<const __nv_bfloat16*>(o);
@@ -280,7 +297,9 @@ int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const v
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
   p.qstat = reinterpret_cast<float*>(ws + cv.qstat);
-  p.dq_accum = reinterpret_cast<float*>(ws + cv.dq_accum);
+  p.dq_accum = ds_route ? nullptr : reinterpret_cast<float*>(ws + cv.dq_accum);
+  p.ds_ws = ds_route ? ws + cv.ds_ws : nullptr;
+  p.zero_tile = ds_route ? ws + cv.zero_tile : nullptr;
   p.counters = reinterpret_cast<int*>(ws + cv.counters);
   p.n_counters = B * H_q * p.n_qt + 1;
   p.ticket = p.counters + (p.n_counters - 1);
@@ -316,7 +335,7 @@ int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const v
   }
   if (e == cudaSuccess) {
     prof.begin(3);
-    e = launch_dq_convert(p, aux_grid, stream);
+    e = ds_route ? launch_dq_from_ds(maps.k, p, stream) : launch_dq_convert(p, aux_grid, stream);
     prof.end(3);
   }
   if (own_ws) cudaFreeAsync(workspace, stream);

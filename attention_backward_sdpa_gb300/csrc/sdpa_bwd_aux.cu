@@ -80,11 +80,18 @@ __global__ void __launch_bounds__(256) sdpa_bwd_preprocess(const ChainParams p) 
     }
   }
 
-  // Clear the dQ accumulator and the counters (+ ticket).
-  float4* acc = reinterpret_cast<float4*>(p.dq_accum);
-  const long long n4 = (long long)p.B * p.Hq * p.n_qt * BQ * p.Dqk / 4;
+  // Clear the dQ accumulator (dQ-reduction route), the stand-in zero dS tile
+  // (two-kernel route), and the counters (+ ticket).
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (long long i = tid; i < n4; i += nthreads) acc[i] = z;
+  if (p.dq_accum) {
+    float4* acc = reinterpret_cast<float4*>(p.dq_accum);
+    const long long n4 = (long long)p.B * p.Hq * p.n_qt * BQ * p.Dqk / 4;
+    for (long long i = tid; i < n4; i += nthreads) acc[i] = z;
+  }
+  if (p.zero_tile) {
+    float4* zt = reinterpret_cast<float4*>(p.zero_tile);
+    for (long long i = tid; i < DS_TILE_BYTES / 16; i += nthreads) zt[i] = z;
+  }
   for (long long i = tid; i < p.n_counters; i += nthreads) p.counters[i] = 0;
 }
 

@@ -1,0 +1,209 @@
+// sdpa_bwd_dq.cu -- deterministic dQ from stored dS tiles (the "two-kernel
+// split" of the cuDNN frontend page "SDPA Backward (SM120)", section
+// "Determinism": the main kernel streams dS to a workspace and a Q-stationary
+// kernel computes dQ = scale * dS K over an ascending key walk).
+//
+// One CTA owns 128 query rows (two 64-row query tiles) of one (batch, query
+// head). It walks, in ascending order, every 128-key tile that the main kernel
+// visited for either of its query tiles (the same loop bounds), and for each
+// loads the key tile K (TMA) and the two stored dS^T tiles (bulk copies of the
+// main kernel's swizzled shared-memory images; a tile the main kernel did not
+// visit is replaced by zeros). Per key tile it issues
+//     dQ[q, d] += sum_key dS[q, key] K[key, d]
+// as eight tcgen05.mma (M = 128 queries, N = D, K = 16 keys; both operands
+// MN-major), accumulating in tensor memory. The fixed walk order makes dQ
+// bitwise reproducible; there are no atomics and no fp32 accumulator in memory.
+//
+// Warps: 0-3 epilogue (tensor memory -> scale -> bf16 -> dQ), 4 loads, 5 MMA.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace sdpa {
+
+constexpr int DQ_THREADS = 192;
+constexpr uint64_t DQ_WAIT_LIMIT_NS = 4000000000ull;
+
+template <int D>
+struct DqLayout {
+  static constexpr int NSTAGE = (D <= 128) ? 3 : 2;
+  static constexpr int TILE_K = BN * D * 2;             // [D/64 blocks][128 keys][128 B]
+  static constexpr int TILE_DS = 2 * DS_TILE_BYTES;     // two dS^T tiles: [2][128 keys][64 q]
+  static constexpr int STAGE = TILE_K + TILE_DS;
+  static constexpr int OFF_BAR = NSTAGE * STAGE;
+  static constexpr int BYTES = OFF_BAR + (2 * NSTAGE + 1) * 8 + 64;
+  static constexpr uint32_t TMEM_COLS = D <= 128 ? 128 : 256;
+  static_assert(BYTES <= 232448, "shared memory budget");
+};
+
+template <int D>
+__global__ void __launch_bounds__(DQ_THREADS, 1)
+    sdpa_bwd_dq_from_ds(const __grid_constant__ CUtensorMap k_map, const ChainParams p) {
+  using L = DqLayout<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (tid == 0) atomicOr(p.status, STATUS_SMEM_ALIGN);
+    return;
+  }
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+  uint64_t* empty = full + L::NSTAGE;
+  uint64_t* done = empty + L::NSTAGE;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int n_qp = ceil_div(p.n_qt, 2);
+  const int qp = blockIdx.x % n_qp;
+  const int bh = blockIdx.x / n_qp;
+  const int b = bh / p.Hq, h = bh % p.Hq, hk = h / p.G;
+  const int qt0 = 2 * qp, qt1 = 2 * qp + 1;  // qt1 may be past the last tile
+  int Lq, Lk;
+  batch_lengths(p, b, Lq, Lk);
+
+  // Key tiles visited for either query tile, ascending: a contiguous range.
+  int kv_first = p.n_kt, kv_last = -1;
+  for (int kt = 0; kt < p.n_kt; ++kt) {
+    int lo, hi;
+    visited_query_tiles(kt, Lq, Lk, p.causal, p.bottom_right, p.window_left, p.window_right, lo, hi);
+    const bool any = (lo <= qt0 && qt0 <= hi) || (qt1 < p.n_qt && lo <= qt1 && qt1 <= hi);
+    if (any) {
+      kv_first = min(kv_first, kt);
+      kv_last = kt;
+    }
+  }
+  const int n = kv_last - kv_first + 1;  // may be <= 0
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    for (int i = 0; i < L::NSTAGE; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(tmem_slot, L::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_wait_prior_grid();  // the dS tiles come from the main kernel
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ loads
+    if (lane == 0 && n > 0) {
+      prefetch_tmap(&k_map);
+      for (int i = 0; i < n; ++i) {
+        const int st = i % L::NSTAGE;
+        const int kt = kv_first + i;
+        if (i >= L::NSTAGE &&
+            !mbar_wait(&empty[st], ((i / L::NSTAGE) - 1) & 1, abort_flag, DQ_WAIT_LIMIT_NS))
+          break;
+        uint8_t* stage = smem + st * L::STAGE;
+        mbar_arrive_expect_tx(&full[st], L::STAGE);
+        for (int blk = 0; blk < D / 64; ++blk)
+          tma_load_3d(stage + blk * (BN * 128), &k_map, &full[st], blk * 64, kt * BN, b * p.Hkv + hk);
+        int lo, hi;
+        visited_query_tiles(kt, Lq, Lk, p.causal, p.bottom_right, p.window_left, p.window_right, lo, hi);
+        for (int half = 0; half < 2; ++half) {
+          const int qt = qt0 + half;
+          const bool stored = qt < p.n_qt && lo <= qt && qt <= hi;
+          const uint8_t* src =
+              stored ? p.ds_ws + (((long long)bh * p.n_kt + kt) * p.n_qt + qt) * (long long)DS_TILE_BYTES
+                     : p.zero_tile;
+          bulk_load(stage + L::TILE_K + half * DS_TILE_BYTES, src, DS_TILE_BYTES, &full[st]);
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA
+    constexpr uint32_t ID = idesc_bf16_f32(128, D, true, true);
+    constexpr uint64_t T_MN = sdesc_sw128_template(BN * 128, 1024);  // 16 KB block stride
+    bool ok = true;
+    for (int i = 0; i < n && ok; ++i) {
+      const int st = i % L::NSTAGE;
+      ok = mbar_wait(&full[st], (i / L::NSTAGE) & 1, abort_flag, DQ_WAIT_LIMIT_NS);
+      __syncwarp();
+      if (!ok) break;
+      tc_fence_after();
+      if (elect_one()) {
+        const uint32_t aK = smem_u32(smem + st * L::STAGE);
+        const uint32_t aS = aK + L::TILE_K;
+        // A = dS as (M = 128 queries, K = keys): the stored dS^T tiles are
+        // [key][query] with queries contiguous, i.e. MN-major, the two 64-query
+        // tiles 16 KB apart. B = K as (N = d, K = keys): MN-major as well.
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k)
+          mma_ss(tmem, sdesc_at(T_MN, aS + k * 2048), sdesc_at(T_MN, aK + k * 2048), ID,
+                 (i > 0 || k > 0));
+        mma_commit(&empty[st]);
+        if (i == n - 1) mma_commit(done);
+      }
+      __syncwarp();
+    }
+    if (!ok && elect_one()) mma_commit(done);  // release the epilogue after an abort
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int row = warp * 32 + lane;          // query within the 128-row tile
+    const int q = qt0 * BQ + row;
+    const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+    bool have = n > 0;
+    if (have) {
+      have = mbar_wait(done, 0, abort_flag, DQ_WAIT_LIMIT_NS);
+      __syncwarp();
+      tc_fence_after();
+    }
+    const bool warp_ok = __all_sync(0xffffffffu, have);
+    __nv_bfloat16* out = p.dq + ((long long)bh * p.Sq + q) * D;
+#pragma unroll
+    for (int c32 = 0; c32 < D / 32; ++c32) {
+      uint32_t r[32];
+      if (warp_ok) {
+        tmem_ld32(t_lane + c32 * 32, r);
+        tmem_ld_wait(r);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = 0u;
+      }
+      if (q < p.Sq) {
+#pragma unroll
+        for (int v8 = 0; v8 < 4; ++v8) {
+          uint4 o;
+          o.x = pack_bf16x2(__uint_as_float(r[v8 * 8 + 0]) * p.scale, __uint_as_float(r[v8 * 8 + 1]) * p.scale);
+          o.y = pack_bf16x2(__uint_as_float(r[v8 * 8 + 2]) * p.scale, __uint_as_float(r[v8 * 8 + 3]) * p.scale);
+          o.z = pack_bf16x2(__uint_as_float(r[v8 * 8 + 4]) * p.scale, __uint_as_float(r[v8 * 8 + 5]) * p.scale);
+          o.w = pack_bf16x2(__uint_as_float(r[v8 * 8 + 6]) * p.scale, __uint_as_float(r[v8 * 8 + 7]) * p.scale);
+          *reinterpret_cast<uint4*>(out + c32 * 32 + v8 * 8) = o;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && tid == 0) atomicOr(p.status, STATUS_TIMEOUT);
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::TMEM_COLS);
+  }
+}
+
+cudaError_t dq_kernel_setup() {
+  return cudaFuncSetAttribute(sdpa_bwd_dq_from_ds<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              DqLayout<128>::BYTES);
+}
+
+// One CTA per (batch, query head, 128-row query tile).
+cudaError_t launch_dq_from_ds(const CUtensorMap& k_map, const ChainParams& p, cudaStream_t s) {
+  const dim3 grid((unsigned)(ceil_div(p.n_qt, 2) * p.B * p.Hq));
+  return launch_kernel(sdpa_bwd_dq_from_ds<128>, grid, dim3(DQ_THREADS), DqLayout<128>::BYTES, s,
+                       true, k_map, p);
+}
+
+}  // namespace sdpa

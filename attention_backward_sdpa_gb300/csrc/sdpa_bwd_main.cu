@@ -70,7 +70,8 @@ enum : int {
   BAR_STAGEREADY = 21,  // 128 arrivals
   BAR_STAGEFREE = 22,
   BAR_MMADONE = 23,     // every MMA of the CTA has completed (epilogue may read dK/dV)
-  NUM_BARS = 24
+  BAR_DSCOPIED = 24,    // + slot: the slot's dS^T tile has been read out to global (dS route)
+  NUM_BARS = 26
 };
 
 template <int D>
@@ -103,7 +104,9 @@ struct MainLayout {
 
 __device__ __forceinline__ void set_status(int* status, int bit) { atomicOr(status, bit); }
 
-template <int D>
+// DS_OUT selects the deterministic two-kernel route: instead of G5 and the dQ
+// reduction, every dS^T tile is stored to the workspace for the dQ kernel.
+template <int D, bool DS_OUT>
 __global__ void __launch_bounds__(MAIN_THREADS, 1)
     sdpa_bwd_main(const __grid_constant__ MainMaps maps, const ChainParams p) {
   using L = MainLayout<D>;
@@ -177,17 +180,9 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
   const int diag = p.bottom_right ? Lk - Lq : 0;
   const int Rp = p.window_right > 0 ? p.window_right : 0;
   const bool has_window = p.window_left >= 0;
-  int qt_lo = 0, qt_hi = -1;
-  if (k0 < Lk && Lq > 0) {
-    const int k_last = min(k0 + BN - 1, Lk - 1);
-    long long q_min = 0, q_max = Lq - 1;
-    if (p.causal) q_min = max(0ll, (long long)k0 - diag - Rp);
-    if (has_window) q_max = min(q_max, (long long)k_last - diag + p.window_left);
-    if (q_min <= q_max) {
-      qt_lo = (int)(q_min / BQ);
-      qt_hi = (int)(q_max / BQ);
-    }
-  }
+  int qt_lo, qt_hi;
+  visited_query_tiles(kt, Lq, Lk, p.causal, p.bottom_right, p.window_left, p.window_right, qt_lo,
+                      qt_hi);
   const int n = qt_hi - qt_lo + 1;  // query tiles this CTA visits (may be 0)
 
   if (warp >= 12) {
@@ -257,7 +252,9 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
           }
           __syncwarp();
           // The slot's dP^T columns hold dQ^T of tile t-2 until it is read out.
-          if (t >= 2 && !mbar_wait(&bars[BAR_DQEMPTY + s], (j - 1) & 1, abort_flag, WAIT_LIMIT_NS)) break;
+          if (!DS_OUT && t >= 2 &&
+              !mbar_wait(&bars[BAR_DQEMPTY + s], (j - 1) & 1, abort_flag, WAIT_LIMIT_NS))
+            break;
           __syncwarp();
           tc_fence_after();
           if (elect_one()) {
@@ -303,11 +300,14 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
             // Stage u is refilled for tile u+3 once G4 is done (G1/G2 of tile u
             // completed before P_READY / DS_READY could arrive).
             if (u + NSTAGE < n) mma_commit(&bars[BAR_QEMPTY + stu]);
-            // G5: dQ^T[d, q] = sum_key K[key, d] dS^T[key, q]   (both MN-major)
+            if (!DS_OUT) {
+              // G5: dQ^T[d, q] = sum_key K[key, d] dS^T[key, q]   (both MN-major)
 #pragma unroll
-            for (int k = 0; k < BN / 16; ++k)
-              mma_ss(tmem + L::col_dp(su), sdesc_at(T_MN_KV, aK + k * 2048),
-                     sdesc_at(T_MN_KV, aDS + k * 2048), ID_G5, k > 0);
+              for (int k = 0; k < BN / 16; ++k)
+                mma_ss(tmem + L::col_dp(su), sdesc_at(T_MN_KV, aK + k * 2048),
+                       sdesc_at(T_MN_KV, aDS + k * 2048), ID_G5, k > 0);
+            }
+            // dQ^T ready (dQ route) / the slot's dS^T buffer no longer read by MMAs.
             mma_commit(&bars[BAR_DQFULL + su]);
           }
           __syncwarp();
@@ -326,8 +326,10 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
     const bool has_rows = quarter * 32 < D;            // warp-uniform
     const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
     const bool leader = (warp == 8 && lane == 0);
+    int* pending_counter = nullptr;  // deterministic mode: turn not yet released
+    int pending_turn = 0;
     bool ok = true;
-    for (int t = 0; t < n && ok; ++t) {
+    for (int t = 0; t < (DS_OUT ? 0 : n) && ok; ++t) {
       const int s = t & 1, j = t >> 1;
       const int qt = qt_hi - t;
       if (!mbar_wait(&bars[BAR_DQFULL + s], j & 1, abort_flag, WAIT_LIMIT_NS)) { ok = false; break; }
@@ -356,7 +358,12 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
         mbar_wait(&bars[BAR_STAGEREADY], t & 1, abort_flag, WAIT_LIMIT_NS);
         float* dst = p.dq_accum + ((long long)bh * p.n_qt + qt) * (long long)BQ * D;
         if (p.deterministic) {
-          // Ordered relay: key tiles add into this query tile in ascending order.
+          // Ordered relay: key tiles add into this query tile in ascending
+          // order. This tile's turn is released once its reduction has
+          // completed, which is checked after the next tile's reduction has been
+          // issued (wait_group 1), so the completion latency overlaps the next
+          // tile instead of stalling this warpgroup. A key tile only ever waits
+          // on lower key tiles, so the delayed release only skews the chain.
           const int kv_lo = has_window ? (int)max(0ll, floor_div((long long)qt * BQ + diag -
                                                                      p.window_left, BN))
                                        : 0;
@@ -364,7 +371,7 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
           int* counter = p.counters + (long long)bh * p.n_qt + qt;
           const uint64_t t0 = globaltimer_ns();
           while (ld_acquire_gpu(counter) != turn) {
-            __nanosleep(64);
+            __nanosleep(32);
             if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
               set_status(p.status, STATUS_TIMEOUT);
               break;
@@ -373,18 +380,30 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
           fence_proxy_async_global();
           bulk_reduce_add_f32(dst, sDQ, L::TILE_DQ);
           bulk_commit_group();
-          bulk_wait_group0();
-          fence_proxy_async_global();
-          st_release_gpu(counter, turn + 1);
+          bulk_wait_group_read0();
+          mbar_arrive(&bars[BAR_STAGEFREE]);
+          if (pending_counter != nullptr) {  // previous tile: complete -> release its turn
+            bulk_wait_group1();
+            fence_proxy_async_global();
+            st_release_gpu(pending_counter, pending_turn + 1);
+          }
+          pending_counter = counter;
+          pending_turn = turn;
         } else {
           bulk_reduce_add_f32(dst, sDQ, L::TILE_DQ);
           bulk_commit_group();
           bulk_wait_group_read0();
+          mbar_arrive(&bars[BAR_STAGEFREE]);
         }
-        mbar_arrive(&bars[BAR_STAGEFREE]);
       }
     }
-    if (leader) bulk_wait_group0();
+    if (leader) {
+      bulk_wait_group0();
+      if (pending_counter != nullptr) {
+        fence_proxy_async_global();
+        st_release_gpu(pending_counter, pending_turn + 1);
+      }
+    }
   } else {
     // ------------------------------------------------------------ compute warpgroups
     regs_increase<REGS_COMPUTE>();
@@ -445,8 +464,11 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
 
       // ---- dS^T = P^T * (dP^T - delta) -> shared memory (K-major, swizzled)
       if (!mbar_wait(&bars[BAR_DPFULL + slot], j & 1, abort_flag, WAIT_LIMIT_NS)) { ok = false; break; }
-      // This slot's dS^T buffer is read by G4/G5 of tile t-2 until they complete.
+      // This slot's dS^T buffer is read by G4/G5 of tile t-2 until they complete
+      // (and, on the dS route, by the bulk store of tile t-2).
       if (j >= 1 && !mbar_wait(&bars[BAR_DQFULL + slot], (j - 1) & 1, abort_flag, WAIT_LIMIT_NS)) { ok = false; break; }
+      if (DS_OUT && j >= 1 &&
+          !mbar_wait(&bars[BAR_DSCOPIED + slot], (j - 1) & 1, abort_flag, WAIT_LIMIT_NS)) { ok = false; break; }
       __syncwarp();
       tc_fence_after();
 #pragma unroll
@@ -471,7 +493,18 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bars[BAR_DSREADY + slot]);
+      if (DS_OUT && row == 0) {
+        // Once the whole warpgroup has written the tile, one thread stores it.
+        if (mbar_wait(&bars[BAR_DSREADY + slot], j & 1, abort_flag, WAIT_LIMIT_NS)) {
+          uint8_t* dst = p.ds_ws + (((long long)bh * p.n_kt + kt) * p.n_qt + qt) * (long long)DS_TILE_BYTES;
+          bulk_store(dst, sDS + slot * L::TILE_DS, DS_TILE_BYTES);
+          bulk_commit_group();
+          bulk_wait_group_read0();
+        }
+        mbar_arrive(&bars[BAR_DSCOPIED + slot]);
+      }
     }
+    if (DS_OUT && row == 0) bulk_wait_group0();  // stores complete before the kernel ends
 
     // ---- epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK, one key
     // row per thread. Every lane runs the (warp-collective) tensor-memory loads;
@@ -521,22 +554,28 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
   }
 }
 
+template <int D, bool DS_OUT>
+static cudaError_t set_main_smem() {
+  return cudaFuncSetAttribute(sdpa_bwd_main<D, DS_OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              MainLayout<D>::BYTES);
+}
+
 cudaError_t main_kernel_setup() {
-  cudaError_t e = cudaFuncSetAttribute(sdpa_bwd_main<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       MainLayout<64>::BYTES);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(sdpa_bwd_main<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              MainLayout<128>::BYTES);
+  cudaError_t e = set_main_smem<64, false>();
+  if (e == cudaSuccess) e = set_main_smem<128, false>();
+  if (e == cudaSuccess) e = set_main_smem<128, true>();
+  return e;
 }
 
 // One CTA per (key tile, batch, query head) work unit.
 cudaError_t launch_main(const MainMaps& maps, const ChainParams& p, cudaStream_t s) {
   const dim3 grid((unsigned)(p.n_kt * p.B * p.Hq));
+  const dim3 block(MAIN_THREADS);
   if (p.Dqk == 64)
-    return launch_kernel(sdpa_bwd_main<64>, grid, dim3(MAIN_THREADS), MainLayout<64>::BYTES, s, true,
-                         maps, p);
-  return launch_kernel(sdpa_bwd_main<128>, grid, dim3(MAIN_THREADS), MainLayout<128>::BYTES, s,
-                       true, maps, p);
+    return launch_kernel(sdpa_bwd_main<64, false>, grid, block, MainLayout<64>::BYTES, s, true, maps, p);
+  if (p.ds_route)
+    return launch_kernel(sdpa_bwd_main<128, true>, grid, block, MainLayout<128>::BYTES, s, true, maps, p);
+  return launch_kernel(sdpa_bwd_main<128, false>, grid, block, MainLayout<128>::BYTES, s, true, maps, p);
 }
 
 }  // namespace sdpa

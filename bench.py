@@ -72,6 +72,15 @@ def flops_per_pair(w: workloads.Workload) -> int:
     return 2 * (3 * w.Dqk + 2 * w.Dv)
 
 
+def main_kernel_flops_per_pair(w: workloads.Workload) -> int:
+    """FLOPs the main kernel itself performs per visible pair: all five GEMMs, or
+    four on the deterministic two-kernel route, where dQ = dS K runs in the
+    separate dQ kernel (the library takes that route for D_qk = 128)."""
+    if w.deterministic and w.Dqk == 128:
+        return 2 * (2 * w.Dqk + 2 * w.Dv)
+    return flops_per_pair(w)
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons while the GPU works."""
@@ -274,7 +283,9 @@ def run_gpu(args, w, t, o, lse, rank, world, device):
             pkg.profile_enable(False)
         return sum(s.elapsed_time(e) for s, e in zip(starts, ends)), prof
 
-    flops = visible_pairs(w, None if lens is None else lens.numpy()) * flops_per_pair(w)
+    pairs = visible_pairs(w, None if lens is None else lens.numpy())
+    flops = pairs * flops_per_pair(w)
+    main_flops = pairs * main_kernel_flops_per_pair(w)
     with ClockSampler(device.index if device.index is not None else 0) as clocks:
         for _ in range(args.warmup):
             step()
@@ -311,14 +322,15 @@ def run_gpu(args, w, t, o, lse, rank, world, device):
     e2e_s = max_over_ranks(e2e_s, world, device)
     peak_tf, peak_hbm, peak_kind = peaks()
     main_ms = prof["main"][0] / max(prof["main"][1], 1)
-    achieved = flops / (main_ms * 1e-3) / 1e12
+    achieved = main_flops / (main_ms * 1e-3) / 1e12
     value = world * flops / (ms_step * 1e-3) / 1e12
     kernel_ms = {k: round(v[0] / max(v[1], 1), 5) for k, v in prof.items() if v[1]}
     return {
         "value": value, "ms_per_step": ms_step, "flops": flops,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
                      "frac": achieved / peak_tf, "traffic": None,
-                     "kernel": "sdpa_bwd_main", "peak_kind": f"{peak_kind} bf16 burst"},
+                     "kernel": "sdpa_bwd_main", "peak_kind": f"{peak_kind} bf16 burst",
+                     "kernel_gflop": main_flops / 1e9},
         "kernel_ms": kernel_ms,
         "e2e": {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

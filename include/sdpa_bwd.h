@@ -56,9 +56,10 @@ typedef enum {
 /*
  * Bytes of device workspace sdpa_bwd() needs for this problem (0 when none).
  * The workspace holds, each region 256-byte aligned: per-query-tile fp32 row
- * statistics (LSE * log2(e) and delta), the fp32 dQ accumulator, the
- * deterministic-mode turn counters and a work ticket, and, when H_kv < H_q,
- * the per-query-head bf16 dK/dV partials of the GQA reduction.
+ * statistics (LSE * log2(e) and delta); the fp32 dQ accumulator, or on the
+ * deterministic two-kernel route the bf16 dS tiles; the deterministic-mode turn
+ * counters and a work ticket; and, when H_kv < H_q, the per-query-head bf16
+ * dK/dV partials of the GQA reduction.
  * Returns 0 for arguments sdpa_bwd() would reject.
  */
 size_t sdpa_bwd_workspace_size(int B, int H_q, int H_kv, int S_q, int S_kv, int D_qk, int D_v,
@@ -79,9 +80,13 @@ size_t sdpa_bwd_workspace_size(int B, int H_q, int H_kv, int S_q, int S_kv, int 
  *   window_left       W >= 0: mask keys k < q + diag - W; < 0: no left window.
  *   window_right      R >= 0 widens the causal diagonal by R keys; requires causal.
  *                     < 0: no widening.
- *   deterministic     1: dQ is reduced across KV tiles in a fixed (ascending KV
- *                     tile) order, so repeated calls give bitwise-identical
- *                     dQ; dK and dV are bitwise reproducible in both modes.
+ *   deterministic     1: repeated calls give bitwise-identical dQ. For D_qk =
+ *                     128 the main kernel stores dS and a second kernel forms
+ *                     dQ = scale * dS K over an ascending key walk (larger
+ *                     workspace: 2 bytes per (query, key) position); otherwise
+ *                     the dQ partials of the KV tiles are added in ascending
+ *                     KV-tile order. dK and dV are bitwise reproducible in
+ *                     both modes.
  *   seq_q_lens,       device int32 (B,) per-batch valid lengths, or NULL for
  *   seq_kv_lens       "the full S". Queries at or past seq_q_lens[b] and keys
  *                     at or past seq_kv_lens[b] are masked; their gradient
@@ -118,7 +123,9 @@ int sdpa_bwd_check_device_status(void* stream);
  * events around each launch and synchronizes the stream before returning, so
  * it is for measurement only. sdpa_bwd_profile_read() fills up to n entries of
  * ms[] (total milliseconds) and launches[] (count) per kernel in the order
- * preprocess, main, gqa_reduce, dq_convert, and returns the number of kernels.
+ * preprocess, main, gqa_reduce, dq (the dQ convert, or on the deterministic
+ * two-kernel route the dQ = scale * dS K kernel), and returns the number of
+ * kernels.
  * Enabling resets the totals.
  */
 int sdpa_bwd_profile_enable(int on);

@@ -50,14 +50,18 @@ def _a256(x):
     return (x + 255) // 256 * 256
 
 
-def expected_workspace(B, Hq, Hkv, Sq, Skv, Dqk, Dv):
-    """Documented layout: per-query-tile row statistics (2 x 64 fp32 per 64-row tile),
-    the fp32 dQ accumulator over whole 64-row tiles, one int per query tile plus a
-    ticket, and for GQA the bf16 dK/dV partials with H_q heads; every region
-    256-byte aligned."""
-    n_qt = -(-Sq // 64)
+def expected_workspace(B, Hq, Hkv, Sq, Skv, Dqk, Dv, det=0):
+    """Documented layout: per-query-tile row statistics (2 x 64 fp32 per 64-row tile);
+    then either the fp32 dQ accumulator over whole 64-row tiles, or (deterministic,
+    D_qk = 128: two-kernel route) one 16 KiB bf16 dS^T tile per (128-key tile,
+    64-query tile) plus one zero tile; one int per query tile plus a ticket; and for
+    GQA the bf16 dK/dV partials with H_q heads. Every region 256-byte aligned."""
+    n_qt, n_kt = -(-Sq // 64), -(-Skv // 128)
     total = _a256(B * Hq * n_qt * 128 * 4)
-    total += _a256(B * Hq * n_qt * 64 * Dqk * 4)
+    if det and Dqk == 128:
+        total += _a256(B * Hq * n_kt * n_qt * 16384) + _a256(16384)
+    else:
+        total += _a256(B * Hq * n_qt * 64 * Dqk * 4)
     total += _a256((B * Hq * n_qt + 1) * 4)
     if Hkv < Hq:
         total += _a256(B * Hq * Skv * Dqk * 2) + _a256(B * Hq * Skv * Dv * 2)
@@ -69,7 +73,7 @@ def expected_workspace(B, Hq, Hkv, Sq, Skv, Dqk, Dv):
                                    (1, 1, 1, 1, 1, 64, 64)])
 def test_workspace_size_matches_layout(lib, shape):
     for det in (0, 1):
-        assert lib.sdpa_bwd_workspace_size(*shape, det) == expected_workspace(*shape)
+        assert lib.sdpa_bwd_workspace_size(*shape, det) == expected_workspace(*shape, det=det)
 
 
 def test_workspace_size_rejects(lib):
