@@ -102,6 +102,8 @@ cudaError_t launch_gqa_reduce(const ChainParams& p, int grid, cudaStream_t s);
 cudaError_t launch_dq_convert(const ChainParams& p, int grid, cudaStream_t s);
 cudaError_t launch_dq_from_ds(const CUtensorMap& k_map, const ChainParams& p, cudaStream_t s);
 cudaError_t dq_kernel_setup();  // per device: opt in to the dQ kernel's shared memory
+cudaError_t launch_main_ds(const MainMaps& maps, const ChainParams& p, cudaStream_t s);
+cudaError_t main_ds_kernel_setup();
 cudaError_t main_kernel_setup();  // per device: opt in to the main kernel's shared memory
 
 template <typename... KArgs, typename... Args>

@@ -41,9 +41,11 @@ int g_prof_n[4] = {};
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Deterministic two-kernel route (dS stored, dQ from a Q-stationary kernel):
-// taken for D_qk = 128 as on the pages (the relay serves the other head dims).
-bool use_ds_route(int deterministic, int Dqk) { return deterministic && Dqk == 128; }
+// Two-kernel route (dS stored, dQ from a Q-stationary kernel): the
+// deterministic route for D_qk = 128 as on the pages (the relay serves
+// D_qk = 64), and the only route for D_qk = 192, whose dK accumulator leaves no
+// tensor memory for dQ in the main kernel.
+bool use_ds_route(int deterministic, int Dqk) { return Dqk == 192 || (deterministic && Dqk == 128); }
 
 struct Carve {
   size_t qstat, dq_accum, ds_ws, zero_tile, counters, dk_ws, dv_ws, total;
@@ -81,7 +83,9 @@ Carve carve(int B, int Hq, int Hkv, int Sq, int Skv, int Dqk, int Dv, bool ds_ro
   return c;
 }
 
-bool dims_supported(int Dqk, int Dv) { return (Dqk == 64 && Dv == 64) || (Dqk == 128 && Dv == 128); }
+bool dims_supported(int Dqk, int Dv) {
+  return (Dqk == 64 && Dv == 64) || (Dqk == 128 && Dv == 128) || (Dqk == 192 && Dv == 128);
+}
 
 int basic_checks(int B, int Hq, int Hkv, int Sq, int Skv, int Dqk, int Dv) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Skv < 0 || Dqk <= 0 || Dv <= 0)
@@ -107,7 +111,8 @@ int device_state(int dev, int** status_out, int* sms_out) {
       void* p = nullptr;
       if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return SDPA_ERR_CUDA;
       g_status_ptr[dev] = static_cast<int*>(p);
-      if (main_kernel_setup() != cudaSuccess || dq_kernel_setup() != cudaSuccess)
+      if (main_kernel_setup() != cudaSuccess || main_ds_kernel_setup() != cudaSuccess ||
+          dq_kernel_setup() != cudaSuccess)
         return SDPA_ERR_CUDA;
     }
     g_device_checked[dev] = true;
@@ -325,7 +330,7 @@ int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const v
   prof.end(0);
   if (e == cudaSuccess) {
     prof.begin(1);
-    e = launch_main(maps, p, stream);
+    e = D_qk == 192 ? launch_main_ds(maps, p, stream) : launch_main(maps, p, stream);
     prof.end(1);
   }
   if (e == cudaSuccess && H_kv < H_q) {

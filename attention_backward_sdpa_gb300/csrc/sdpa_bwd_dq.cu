@@ -195,13 +195,20 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
 }
 
 cudaError_t dq_kernel_setup() {
-  return cudaFuncSetAttribute(sdpa_bwd_dq_from_ds<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              DqLayout<128>::BYTES);
+  cudaError_t e = cudaFuncSetAttribute(sdpa_bwd_dq_from_ds<128>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       DqLayout<128>::BYTES);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(sdpa_bwd_dq_from_ds<192>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              DqLayout<192>::BYTES);
 }
 
 // One CTA per (batch, query head, 128-row query tile).
 cudaError_t launch_dq_from_ds(const CUtensorMap& k_map, const ChainParams& p, cudaStream_t s) {
   const dim3 grid((unsigned)(ceil_div(p.n_qt, 2) * p.B * p.Hq));
+  if (p.Dqk == 192)
+    return launch_kernel(sdpa_bwd_dq_from_ds<192>, grid, dim3(DQ_THREADS), DqLayout<192>::BYTES, s,
+                         true, k_map, p);
   return launch_kernel(sdpa_bwd_dq_from_ds<128>, grid, dim3(DQ_THREADS), DqLayout<128>::BYTES, s,
                        true, k_map, p);
 }

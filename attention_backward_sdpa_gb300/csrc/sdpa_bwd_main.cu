@@ -251,7 +251,11 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
             mma_commit(&bars[BAR_SFULL + s]);
           }
           __syncwarp();
-          // The slot's dP^T columns hold dQ^T of tile t-2 until it is read out.
+          // The slot's dP^T columns are read by the compute warpgroup of tile t-2
+          // until it has formed dS (DS_READY), and on the dQ-reduction route
+          // then hold dQ^T of tile t-2 until the dQ warpgroup has read it out.
+          if (t >= 2 && !mbar_wait(&bars[BAR_DSREADY + s], (j - 1) & 1, abort_flag, WAIT_LIMIT_NS))
+            break;
           if (!DS_OUT && t >= 2 &&
               !mbar_wait(&bars[BAR_DQEMPTY + s], (j - 1) & 1, abort_flag, WAIT_LIMIT_NS))
             break;

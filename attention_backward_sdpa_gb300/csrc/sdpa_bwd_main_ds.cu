@@ -1,0 +1,430 @@
+// sdpa_bwd_main_ds.cu -- SDPA backward main kernel for head dims whose dK
+// accumulator leaves no tensor memory for dQ (MLA: D_qk = 192, D_v = 128).
+//
+// Same computation as sdpa_bwd_main.cu (cuDNN frontend docs, "SDPA Backward
+// (SM120)", "Main-kernel pipeline: KV-stationary, five chained GEMMs"; D_qk
+// sizes Q/K/dQ/dK and D_v sizes V/O/dO/dV as in "Head-size support and tile
+// configs"), with dQ always on the two-kernel route of the "Determinism"
+// section: every bf16 dS^T tile is stored and sdpa_bwd_dq.cu forms
+// dQ = scale * dS K. Per 64-row query tile t:
+//   G1  S^T  = K Q^T       -> slot columns [0,64)
+//       P^T  = exp2(...)    -> bf16 into slot columns [64,96)
+//   G2  dP^T = V dO^T      -> slot columns [0,64), once S^T has been read
+//       dS^T = P^T (dP^T - delta) -> shared memory -> workspace (bulk store)
+//   G3  dV  += P^T dO       (A = P^T from tensor memory)
+//   G4  dK  += dS^T Q
+// Tensor memory (512 columns): two 96-column slots at 96s, dV at [192,192+D_v),
+// dK at [192+D_v, 192+D_v+D_qk): 2*96 + 128 + 192 = 512 for MLA.
+//
+// Warps: 0-3 even tiles (slot 0), 4-7 odd tiles (slot 1), 8 TMA producer,
+// 9 G1/G2 issuer and tensor-memory owner, 10 G3/G4 issuer, 11 idle.
+// Shared memory: K [D_qk/64][128][128 B], V [D_v/64][128][128 B], Q and dO
+// stage rings ([D/64][64][128 B]), dS^T x2 [128 keys][64 q], row statistics.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace sdpa {
+
+namespace ds_kernel {
+
+constexpr int THREADS = 384;
+constexpr uint64_t WAIT_LIMIT_NS = 4000000000ull;
+
+enum : int {
+  BAR_KV = 0,
+  BAR_QFULL = 1,     // + stage (up to 3)
+  BAR_QEMPTY = 4,    // + stage
+  BAR_SFULL = 7,     // + slot: S^T in tensor memory
+  BAR_PREADY = 9,    // + slot, 128 arrivals: S^T read, P^T written
+  BAR_DPFULL = 11,   // + slot: dP^T in tensor memory
+  BAR_SFREE = 13,    // + slot: G3 done reading P^T
+  BAR_DSREADY = 15,  // + slot, 128 arrivals: dP^T read, dS^T in shared memory
+  BAR_DSFREE = 17,   // + slot: G4 done reading dS^T
+  BAR_DSCOPIED = 19, // + slot: dS^T stored to the workspace
+  BAR_MMADONE = 21,
+  NUM_BARS = 22
+};
+
+template <int DQK, int DV>
+struct Layout {
+  static constexpr int BLK_KV = BN * 128;
+  static constexpr int BLK_Q = BQ * 128;
+  static constexpr int TILE_K = BN * DQK * 2;
+  static constexpr int TILE_V = BN * DV * 2;
+  static constexpr int TILE_Q = BQ * DQK * 2;
+  static constexpr int TILE_DO = BQ * DV * 2;
+  static constexpr int TILE_DS = BN * BQ * 2;
+  static constexpr int FIXED = TILE_K + TILE_V + 2 * TILE_DS;
+  static constexpr int PER_STAGE = TILE_Q + TILE_DO + QSTAT_FLOATS * 4;
+  static constexpr int NSTAGE = (FIXED + 3 * PER_STAGE + NUM_BARS * 8 + 64 <= 232448) ? 3 : 2;
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + TILE_K;
+  static constexpr int OFF_DS = OFF_V + TILE_V;
+  static constexpr int OFF_Q = OFF_DS + 2 * TILE_DS;
+  static constexpr int OFF_DO = OFF_Q + NSTAGE * TILE_Q;
+  static constexpr int OFF_QS = OFF_DO + NSTAGE * TILE_DO;
+  static constexpr int OFF_BAR = OFF_QS + NSTAGE * QSTAT_FLOATS * 4;
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int BYTES = OFF_MISC + 64;
+  static constexpr uint32_t COL_DV = 192, COL_DK = 192 + DV;
+  __host__ __device__ static constexpr uint32_t col_s(int slot) { return 96u * slot; }
+  __host__ __device__ static constexpr uint32_t col_p(int slot) { return 96u * slot + 64u; }
+  static_assert(COL_DK + DQK <= 512, "tensor memory budget");
+  static_assert(BYTES <= 232448, "shared memory budget");
+  static_assert(BYTES > 116 * 1024, "one CTA per SM");
+  static_assert(TILE_Q % 1024 == 0 && TILE_DO % 1024 == 0 && TILE_K % 1024 == 0, "alignment");
+};
+
+}  // namespace ds_kernel
+
+template <int DQK, int DV>
+__global__ void __launch_bounds__(ds_kernel::THREADS, 1)
+    sdpa_bwd_main_ds(const __grid_constant__ MainMaps maps, const ChainParams p) {
+  using namespace ds_kernel;
+  using L = Layout<DQK, DV>;
+  constexpr int NST = L::NSTAGE;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (tid == 0) atomicOr(p.status, STATUS_SMEM_ALIGN);
+    return;
+  }
+  uint8_t* sK = smem + L::OFF_K;
+  uint8_t* sV = smem + L::OFF_V;
+  uint8_t* sQ = smem + L::OFF_Q;
+  uint8_t* sDO = smem + L::OFF_DO;
+  uint8_t* sDS = smem + L::OFF_DS;
+  float* sQS = reinterpret_cast<float*>(smem + L::OFF_QS);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    for (int i = 0; i < NUM_BARS; ++i) {
+      const bool threads128 = (i == BAR_PREADY || i == BAR_PREADY + 1 || i == BAR_DSREADY ||
+                               i == BAR_DSREADY + 1);
+      mbar_init(&bars[i], threads128 ? 128 : 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 8 && lane == 0) {
+    prefetch_tmap(&maps.q);
+    prefetch_tmap(&maps.k);
+    prefetch_tmap(&maps.v);
+    prefetch_tmap(&maps.d_o);
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int BH = p.B * p.Hq;
+  const int kt = blockIdx.x / BH;   // key tile major: the longest units first under causal masks
+  const int bh = blockIdx.x % BH;
+  const int b = bh / p.Hq, h = bh % p.Hq, hk = h / p.G;
+  const int k0 = kt * BN;
+  int Lq, Lk;
+  batch_lengths(p, b, Lq, Lk);
+  const int diag = p.bottom_right ? Lk - Lq : 0;
+  const int Rp = p.window_right > 0 ? p.window_right : 0;
+  const bool has_window = p.window_left >= 0;
+  int qt_lo, qt_hi;
+  visited_query_tiles(kt, Lq, Lk, p.causal, p.bottom_right, p.window_left, p.window_right, qt_lo,
+                      qt_hi);
+  const int n = qt_hi - qt_lo + 1;
+
+  constexpr uint32_t ID_G1 = idesc_bf16_f32(128, BQ, false, false);
+  constexpr uint32_t ID_G2 = idesc_bf16_f32(128, BQ, false, false);
+  constexpr uint32_t ID_G3 = idesc_bf16_f32(128, DV, false, true);
+  constexpr uint32_t ID_G4 = idesc_bf16_f32(128, DQK, false, true);
+  constexpr uint64_t T_KMAJ = sdesc_sw128_template(16, 1024);
+  constexpr uint64_t T_MN_Q = sdesc_sw128_template(L::BLK_Q, 1024);
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && n > 0) {
+      mbar_arrive_expect_tx(&bars[BAR_KV], L::TILE_K + L::TILE_V);
+      for (int blk = 0; blk < DQK / 64; ++blk)
+        tma_load_3d(sK + blk * L::BLK_KV, &maps.k, &bars[BAR_KV], blk * 64, k0, b * p.Hkv + hk);
+      for (int blk = 0; blk < DV / 64; ++blk)
+        tma_load_3d(sV + blk * L::BLK_KV, &maps.v, &bars[BAR_KV], blk * 64, k0, b * p.Hkv + hk);
+      pdl_wait_prior_grid();
+      for (int t = 0; t < n; ++t) {
+        const int st = t % NST;
+        if (t >= NST &&
+            !mbar_wait(&bars[BAR_QEMPTY + st], ((t / NST) - 1) & 1, abort_flag, WAIT_LIMIT_NS))
+          break;
+        const int qt = qt_hi - t;
+        uint64_t* full = &bars[BAR_QFULL + st];
+        mbar_arrive_expect_tx(full, L::TILE_Q + L::TILE_DO + QSTAT_FLOATS * 4);
+        for (int blk = 0; blk < DQK / 64; ++blk)
+          tma_load_3d(sQ + st * L::TILE_Q + blk * L::BLK_Q, &maps.q, full, blk * 64, qt * BQ, bh);
+        for (int blk = 0; blk < DV / 64; ++blk)
+          tma_load_3d(sDO + st * L::TILE_DO + blk * L::BLK_Q, &maps.d_o, full, blk * 64, qt * BQ, bh);
+        bulk_load(sQS + st * QSTAT_FLOATS, p.qstat + ((long long)bh * p.n_qt + qt) * QSTAT_FLOATS,
+                  QSTAT_FLOATS * 4, full);
+      }
+    }
+  } else if (warp == 9 || warp == 10) {
+    // ------------------------------------------------------------ MMA issuers
+    pdl_wait_prior_grid();
+    const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
+    bool ok = n > 0 && mbar_wait(&bars[BAR_KV], 0, abort_flag, WAIT_LIMIT_NS);
+    if (warp == 9) {
+      // G1 of tile t+1 is issued before G2 of tile t waits for the softmax of t.
+      auto issue_g1 = [&](int t) -> bool {
+        const int s = t & 1, st = t % NST, j = t >> 1;
+        if (!mbar_wait(&bars[BAR_QFULL + st], (t / NST) & 1, abort_flag, WAIT_LIMIT_NS)) return false;
+        // Slot columns [0,64) hold dP^T of tile t-2 until its dS has been formed.
+        if (t >= 2 && !mbar_wait(&bars[BAR_DSREADY + s], (j - 1) & 1, abort_flag, WAIT_LIMIT_NS))
+          return false;
+        __syncwarp();
+        tc_fence_after();
+        if (elect_one()) {
+          const uint32_t aQ = smem_u32(sQ + st * L::TILE_Q);
+#pragma unroll
+          for (int k = 0; k < DQK / 16; ++k) {
+            const uint32_t kk = (k >> 2) * L::BLK_KV + (k & 3) * 32;
+            const uint32_t kq = (k >> 2) * L::BLK_Q + (k & 3) * 32;
+            mma_ss(tmem + L::col_s(s), sdesc_at(T_KMAJ, aK + kk), sdesc_at(T_KMAJ, aQ + kq), ID_G1,
+                   k > 0);
+          }
+          mma_commit(&bars[BAR_SFULL + s]);
+        }
+        __syncwarp();
+        return true;
+      };
+      if (ok) ok = issue_g1(0);
+      for (int t = 0; t < n && ok; ++t) {
+        if (t + 1 < n && !issue_g1(t + 1)) break;
+        const int s = t & 1, st = t % NST, j = t >> 1;
+        // dP^T overwrites S^T once the warpgroup has read it (P_READY).
+        if (!mbar_wait(&bars[BAR_PREADY + s], j & 1, abort_flag, WAIT_LIMIT_NS)) break;
+        __syncwarp();
+        tc_fence_after();
+        if (elect_one()) {
+          const uint32_t aDO = smem_u32(sDO + st * L::TILE_DO);
+#pragma unroll
+          for (int k = 0; k < DV / 16; ++k) {
+            const uint32_t kk = (k >> 2) * L::BLK_KV + (k & 3) * 32;
+            const uint32_t kq = (k >> 2) * L::BLK_Q + (k & 3) * 32;
+            mma_ss(tmem + L::col_s(s), sdesc_at(T_KMAJ, aV + kk), sdesc_at(T_KMAJ, aDO + kq), ID_G2,
+                   k > 0);
+          }
+          mma_commit(&bars[BAR_DPFULL + s]);
+        }
+        __syncwarp();
+      }
+    } else {
+      for (int u = 0; u < n && ok; ++u) {
+        const int su = u & 1, stu = u % NST, ju = u >> 1;
+        if (!mbar_wait(&bars[BAR_PREADY + su], ju & 1, abort_flag, WAIT_LIMIT_NS)) break;
+        __syncwarp();
+        tc_fence_after();
+        if (elect_one()) {
+          // G3: dV[key, d] += sum_q P^T[key, q] dO[q, d]
+          const uint32_t aDO = smem_u32(sDO + stu * L::TILE_DO);
+#pragma unroll
+          for (int k = 0; k < BQ / 16; ++k)
+            mma_ts(tmem + L::COL_DV, tmem + L::col_p(su) + 8 * k, sdesc_at(T_MN_Q, aDO + k * 2048),
+                   ID_G3, (u > 0 || k > 0));
+          mma_commit(&bars[BAR_SFREE + su]);
+        }
+        __syncwarp();
+        if (!mbar_wait(&bars[BAR_DSREADY + su], ju & 1, abort_flag, WAIT_LIMIT_NS)) break;
+        __syncwarp();
+        tc_fence_after();
+        if (elect_one()) {
+          // G4: dK[key, d] += sum_q dS^T[key, q] Q[q, d]
+          const uint32_t aQ = smem_u32(sQ + stu * L::TILE_Q);
+          const uint32_t aDS = smem_u32(sDS + su * L::TILE_DS);
+#pragma unroll
+          for (int k = 0; k < BQ / 16; ++k)
+            mma_ss(tmem + L::COL_DK, sdesc_at(T_KMAJ, aDS + k * 32), sdesc_at(T_MN_Q, aQ + k * 2048),
+                   ID_G4, (u > 0 || k > 0));
+          if (u + NST < n) mma_commit(&bars[BAR_QEMPTY + stu]);
+          mma_commit(&bars[BAR_DSFREE + su]);
+        }
+        __syncwarp();
+      }
+      if (n > 0 && elect_one()) mma_commit(&bars[BAR_MMADONE]);
+      __syncwarp();
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ compute warpgroups
+    pdl_wait_prior_grid();
+    const int slot = warp >> 2;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+    const int k = k0 + row;
+    const bool row_dead = k >= Lk;
+    const long long q_lo_vis = p.causal ? (long long)k - diag - Rp : -(1ll << 40);
+    const long long q_hi_vis = has_window ? (long long)k - diag + p.window_left : (1ll << 40);
+    uint8_t* ds_row = sDS + slot * L::TILE_DS + row * 128;
+    float P[BQ];
+    bool ok = true;
+    for (int t = slot; t < n && ok; t += 2) {
+      const int j = t >> 1, st = t % NST;
+      const int qt = qt_hi - t, q0 = qt * BQ;
+      const float* qs = sQS + st * QSTAT_FLOATS;
+      const bool need_mask = (k0 + BN > Lk) ||
+                             (p.causal && (long long)q0 < (long long)(k0 + BN - 1) - diag - Rp) ||
+                             (has_window && (long long)(q0 + BQ - 1) > (long long)k0 - diag + p.window_left);
+      if (!mbar_wait(&bars[BAR_QFULL + st], (t / NST) & 1, abort_flag, WAIT_LIMIT_NS) ||
+          !mbar_wait(&bars[BAR_SFULL + slot], j & 1, abort_flag, WAIT_LIMIT_NS)) { ok = false; break; }
+      __syncwarp();
+      tc_fence_after();
+      {
+        uint32_t ra[32], rb[32];
+        tmem_ld32(t_lane + L::col_s(slot), ra);
+        tmem_ld32(t_lane + L::col_s(slot) + 32, rb);
+        tmem_ld_wait(ra);
+        tmem_ld_wait(rb);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          P[i] = ex2_approx(fmaf(__uint_as_float(ra[i]), p.scale_log2, -qs[i]));
+          P[32 + i] = ex2_approx(fmaf(__uint_as_float(rb[i]), p.scale_log2, -qs[32 + i]));
+        }
+      }
+      if (need_mask) {
+#pragma unroll
+        for (int i = 0; i < BQ; ++i) {
+          const long long q = q0 + i;
+          if (row_dead || q < q_lo_vis || q > q_hi_vis) P[i] = 0.f;
+        }
+      }
+      // P^T columns of this slot are read by G3 of tile t-2 until it completes.
+      if (j >= 1 && !mbar_wait(&bars[BAR_SFREE + slot], (j - 1) & 1, abort_flag, WAIT_LIMIT_NS)) { ok = false; break; }
+      __syncwarp();
+#pragma unroll
+      for (int c16 = 0; c16 < 2; ++c16) {
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(P[c16 * 32 + 2 * i], P[c16 * 32 + 2 * i + 1]);
+        tmem_st16(t_lane + L::col_p(slot) + c16 * 16, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars[BAR_PREADY + slot]);  // S^T read and P^T written
+
+      if (!mbar_wait(&bars[BAR_DPFULL + slot], j & 1, abort_flag, WAIT_LIMIT_NS)) { ok = false; break; }
+      // The dS^T buffer is read by G4 and by the bulk store of tile t-2.
+      if (j >= 1 && (!mbar_wait(&bars[BAR_DSFREE + slot], (j - 1) & 1, abort_flag, WAIT_LIMIT_NS) ||
+                     !mbar_wait(&bars[BAR_DSCOPIED + slot], (j - 1) & 1, abort_flag, WAIT_LIMIT_NS))) {
+        ok = false;
+        break;
+      }
+      __syncwarp();
+      tc_fence_after();
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t r[32];
+        tmem_ld32(t_lane + L::col_s(slot) + half * 32, r);
+        tmem_ld_wait(r);
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t w[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int c = half * 32 + ch * 8 + 2 * i;
+            const float d0 = P[c] * (__uint_as_float(r[ch * 8 + 2 * i]) - qs[BQ + c]);
+            const float d1 = P[c + 1] * (__uint_as_float(r[ch * 8 + 2 * i + 1]) - qs[BQ + c + 1]);
+            w[i] = pack_bf16x2(d0, d1);
+          }
+          const int chunk = half * 4 + ch;
+          *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars[BAR_DSREADY + slot]);  // dP^T read, dS^T in shared memory
+      if (row == 0) {
+        if (mbar_wait(&bars[BAR_DSREADY + slot], j & 1, abort_flag, WAIT_LIMIT_NS)) {
+          uint8_t* dst = p.ds_ws + (((long long)bh * p.n_kt + kt) * p.n_qt + qt) * (long long)DS_TILE_BYTES;
+          bulk_store(dst, sDS + slot * L::TILE_DS, DS_TILE_BYTES);
+          bulk_commit_group();
+          bulk_wait_group_read0();
+        }
+        mbar_arrive(&bars[BAR_DSCOPIED + slot]);
+      }
+    }
+    if (row == 0) bulk_wait_group0();
+
+    // ---- epilogue: warpgroup 0 writes dV (D_v columns), warpgroup 1 scale * dK (D_qk).
+    if (n > 0 && ok) {
+      ok = mbar_wait(&bars[BAR_MMADONE], 0, abort_flag, WAIT_LIMIT_NS);
+      __syncwarp();
+      tc_fence_after();
+    }
+    const bool warp_ok = __all_sync(0xffffffffu, ok);
+    const bool store_row = k < p.Skv;
+    const int D = slot ? DQK : DV;
+    const uint32_t col0 = slot ? L::COL_DK : L::COL_DV;
+    const float mult = slot ? p.scale : 1.f;
+    __nv_bfloat16* base = slot ? (p.dk_ws ? p.dk_ws : p.dk) : (p.dv_ws ? p.dv_ws : p.dv);
+    const long long head = p.dk_ws ? (long long)bh : (long long)b * p.Hkv + hk;
+    __nv_bfloat16* out = base + (head * p.Skv + k) * (long long)D;
+    for (int c32 = 0; c32 < D / 32; ++c32) {
+      uint32_t r[32];
+      if (n > 0 && warp_ok) {
+        tmem_ld32(t_lane + col0 + c32 * 32, r);
+        tmem_ld_wait(r);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = 0u;
+      }
+      if (store_row) {
+#pragma unroll
+        for (int v8 = 0; v8 < 4; ++v8) {
+          uint4 o;
+          o.x = pack_bf16x2(__uint_as_float(r[v8 * 8 + 0]) * mult, __uint_as_float(r[v8 * 8 + 1]) * mult);
+          o.y = pack_bf16x2(__uint_as_float(r[v8 * 8 + 2]) * mult, __uint_as_float(r[v8 * 8 + 3]) * mult);
+          o.z = pack_bf16x2(__uint_as_float(r[v8 * 8 + 4]) * mult, __uint_as_float(r[v8 * 8 + 5]) * mult);
+          o.w = pack_bf16x2(__uint_as_float(r[v8 * 8 + 6]) * mult, __uint_as_float(r[v8 * 8 + 7]) * mult);
+          *reinterpret_cast<uint4*>(out + c32 * 32 + v8 * 8) = o;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && tid == 0) atomicOr(p.status, STATUS_TIMEOUT);
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int DQK, int DV>
+static cudaError_t set_ds_smem() {
+  return cudaFuncSetAttribute(sdpa_bwd_main_ds<DQK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              ds_kernel::Layout<DQK, DV>::BYTES);
+}
+
+cudaError_t main_ds_kernel_setup() {
+  cudaError_t e = set_ds_smem<192, 128>();
+  if (e == cudaSuccess) e = set_ds_smem<128, 128>();
+  return e;
+}
+
+cudaError_t launch_main_ds(const MainMaps& maps, const ChainParams& p, cudaStream_t s) {
+  const dim3 grid((unsigned)(p.n_kt * p.B * p.Hq));
+  const dim3 block(ds_kernel::THREADS);
+  if (p.Dqk == 192)
+    return launch_kernel(sdpa_bwd_main_ds<192, 128>, grid, block, ds_kernel::Layout<192, 128>::BYTES,
+                         s, true, maps, p);
+  return launch_kernel(sdpa_bwd_main_ds<128, 128>, grid, block, ds_kernel::Layout<128, 128>::BYTES, s,
+                       true, maps, p);
+}
+
+}  // namespace sdpa

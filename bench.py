@@ -74,9 +74,10 @@ def flops_per_pair(w: workloads.Workload) -> int:
 
 def main_kernel_flops_per_pair(w: workloads.Workload) -> int:
     """FLOPs the main kernel itself performs per visible pair: all five GEMMs, or
-    four on the deterministic two-kernel route, where dQ = dS K runs in the
-    separate dQ kernel (the library takes that route for D_qk = 128)."""
-    if w.deterministic and w.Dqk == 128:
+    four on the two-kernel route, where dQ = dS K runs in the separate dQ kernel
+    (the library takes that route for D_qk = 192, and for D_qk = 128 when
+    deterministic)."""
+    if w.Dqk == 192 or (w.deterministic and w.Dqk == 128):
         return 2 * (2 * w.Dqk + 2 * w.Dv)
     return flops_per_pair(w)
 

@@ -72,7 +72,7 @@ size_t sdpa_bwd_workspace_size(int B, int H_q, int H_kv, int S_q, int S_kv, int 
  *   dq, dk, dv        device bf16 outputs (same shapes as q, k, v).
  *   B, H_q, H_kv      batch and head counts; H_kv must divide H_q.
  *   S_q, S_kv         sequence lengths (>= 0; a zero length gives zero gradients).
- *   D_qk, D_v         head dims; served: (64, 64) and (128, 128).
+ *   D_qk, D_v         head dims; served: (64, 64), (128, 128) and (192, 128).
  *   scale             softmax scale applied to Q K^T; <= 0 or NaN selects 1/sqrt(D_qk).
  *   causal            1: keep key k for query q only if k <= q + diag + max(window_right, 0).
  *   bottom_right      1: diag = L_kv - L_q (the actual lengths of the batch row);
@@ -83,10 +83,11 @@ size_t sdpa_bwd_workspace_size(int B, int H_q, int H_kv, int S_q, int S_kv, int 
  *   deterministic     1: repeated calls give bitwise-identical dQ. For D_qk =
  *                     128 the main kernel stores dS and a second kernel forms
  *                     dQ = scale * dS K over an ascending key walk (larger
- *                     workspace: 2 bytes per (query, key) position); otherwise
- *                     the dQ partials of the KV tiles are added in ascending
- *                     KV-tile order. dK and dV are bitwise reproducible in
- *                     both modes.
+ *                     workspace: 2 bytes per (query, key) position); for
+ *                     D_qk = 64 the dQ partials of the KV tiles are added in
+ *                     ascending KV-tile order. D_qk = 192 always takes the
+ *                     stored-dS route, so its dQ is reproducible in both
+ *                     modes. dK and dV are bitwise reproducible in both modes.
  *   seq_q_lens,       device int32 (B,) per-batch valid lengths, or NULL for
  *   seq_kv_lens       "the full S". Queries at or past seq_q_lens[b] and keys
  *                     at or past seq_kv_lens[b] are masked; their gradient

@@ -58,7 +58,7 @@ def expected_workspace(B, Hq, Hkv, Sq, Skv, Dqk, Dv, det=0):
     GQA the bf16 dK/dV partials with H_q heads. Every region 256-byte aligned."""
     n_qt, n_kt = -(-Sq // 64), -(-Skv // 128)
     total = _a256(B * Hq * n_qt * 128 * 4)
-    if det and Dqk == 128:
+    if (det and Dqk == 128) or Dqk == 192:
         total += _a256(B * Hq * n_kt * n_qt * 16384) + _a256(16384)
     else:
         total += _a256(B * Hq * n_qt * 64 * Dqk * 4)
@@ -70,7 +70,8 @@ def expected_workspace(B, Hq, Hkv, Sq, Skv, Dqk, Dv, det=0):
 
 @pytest.mark.parametrize("shape", [(1, 2, 2, 128, 128, 64, 64), (2, 16, 16, 2048, 2048, 128, 128),
                                    (1, 32, 8, 4096, 4096, 128, 128), (3, 4, 1, 300, 177, 128, 128),
-                                   (1, 1, 1, 1, 1, 64, 64)])
+                                   (1, 1, 1, 1, 1, 64, 64), (1, 16, 16, 4096, 4096, 192, 128),
+                                   (2, 4, 2, 300, 177, 192, 128)])
 def test_workspace_size_matches_layout(lib, shape):
     for det in (0, 1):
         assert lib.sdpa_bwd_workspace_size(*shape, det) == expected_workspace(*shape, det=det)
@@ -100,6 +101,7 @@ def test_argument_validation(lib):
     assert call(lib, Sq=-1) == INVALID
     assert call(lib, Dqk=96, Dv=96) == UNSUPPORTED
     assert call(lib, Dqk=128, Dv=64) == UNSUPPORTED
+    assert call(lib, Dqk=192, Dv=192) == UNSUPPORTED
     for i in range(9):
         ptrs = [FAKE] * 9
         ptrs[i] = None

@@ -58,6 +58,13 @@ SMALL = {
     "gqa_det": W("gqa_det", 1, 4, 2, 520, 520, 128, 128, causal=True, deterministic=True, seed=24),
     "window_det": W("window_det", 2, 2, 1, 600, 600, 128, 128, causal=True, window_left=200,
                     deterministic=True, seed=25),
+    "mla_br_causal_ragged": W("mla_br_causal_ragged", 1, 2, 2, 300, 333, 192, 128, causal=True,
+                              bottom_right=True, seed=28),
+    "mla_dense": W("mla_dense", 2, 2, 2, 190, 250, 192, 128, seed=29),
+    "mla_gqa_window": W("mla_gqa_window", 1, 4, 2, 400, 400, 192, 128, causal=True,
+                        window_left=100, seed=30),
+    "mla_padded_det": W("mla_padded_det", 2, 2, 2, 300, 300, 192, 128, causal=True,
+                        padded=(50, 300), deterministic=True, seed=31),
 }
 
 
@@ -158,7 +165,7 @@ def _sample_rows(w, lens, rng, n_rand=24):
     return np.unique(np.array(q_rows)), np.unique(np.array(kv_rows))
 
 
-@pytest.mark.parametrize("name", ["tiny_dense", "causal_mha", "causal_gqa_det", "swa_causal_padded"])
+@pytest.mark.parametrize("name", workloads.ORDER)
 def test_workload_sampled_parity(name):
     case = _case(name)
     w = case["workload"]
