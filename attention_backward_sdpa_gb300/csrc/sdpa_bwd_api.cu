@@ -92,8 +92,12 @@ int basic_checks(int B, int Hq, int Hkv, int Sq, int Skv, int Dqk, int Dv) {
     return SDPA_ERR_INVALID;
   if (Hq % Hkv != 0) return SDPA_ERR_INVALID;
   if (!dims_supported(Dqk, Dv)) return SDPA_ERR_UNSUPPORTED;
-  // TMA coordinates and the flattened (batch, head) axis are 32-bit.
-  if ((long long)B * Hq >= (1ll << 31) || (long long)B * Hq * ceil_div(Skv, BN) >= (1ll << 31))
+  // TMA coordinates, the flattened (batch, head) axis and the element index of
+  // every tensor are 32-bit.
+  const long long limit = 1ll << 31;
+  if ((long long)B * Hq * Sq * (Dqk > Dv ? Dqk : Dv) >= limit ||
+      (long long)B * Hkv * Skv * (Dqk > Dv ? Dqk : Dv) >= limit ||
+      (long long)B * Hq * ceil_div(Skv, BN) >= limit)
     return SDPA_ERR_INVALID;
   return SDPA_OK;
 }

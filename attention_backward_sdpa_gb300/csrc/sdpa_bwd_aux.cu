@@ -31,6 +31,10 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
 }
 
 // ---------------------------------------------------------------- preprocess
+// One 64-row query tile per CTA pass: TPR = DV/8 lanes per row (8 bf16 each),
+// 256 / TPR rows per pass, all loads of a tile issued before any reduction.
+// Index arithmetic is done once per tile in 32 bits (the host rejects tensors
+// of 2^31 elements or more).
 template <int DV>
 __global__ void __launch_bounds__(256) sdpa_bwd_preprocess(const ChainParams p) {
   // The main kernel may start its prologue (barrier setup, TMEM allocation,
@@ -38,50 +42,65 @@ __global__ void __launch_bounds__(256) sdpa_bwd_preprocess(const ChainParams p) 
   // anything written here.
   pdl_launch_dependents();
 
-  constexpr int TPR = DV / 8;  // threads per query row, 8 bf16 each
+  constexpr int TPR = DV / 8;              // lanes per query row
+  constexpr int RPP = 256 / TPR;           // rows per pass
+  constexpr int PASSES = BQ / RPP;         // passes per 64-row tile
   constexpr float LOG2E = 1.4426950408889634f;
   const int lane = threadIdx.x & 31;
   const unsigned group_mask = (TPR == 32 ? 0xFFFFFFFFu : ((1u << TPR) - 1u) << (lane / TPR * TPR));
   const int sub = threadIdx.x % TPR;
-  const long long rows = (long long)p.B * p.Hq * p.n_qt * BQ;
-  const long long nthreads = (long long)gridDim.x * blockDim.x;
-  const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int rsub = threadIdx.x / TPR;
+  const unsigned n_tiles = (unsigned)p.B * p.Hq * p.n_qt;
 
-  for (long long r = tid / TPR; r < rows; r += nthreads / TPR) {
-    const int qi = (int)(r % BQ);
-    const long long t = r / BQ;
-    const int qt = (int)(t % p.n_qt);
-    const long long bh = t / p.n_qt;
-    const int b = (int)(bh / p.Hq);
-    const int q = qt * BQ + qi;
+  for (unsigned t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+    const unsigned bh = t / (unsigned)p.n_qt;
+    const int qt = (int)(t - bh * (unsigned)p.n_qt);
     int Lq, Lk;
-    batch_lengths(p, b, Lq, Lk);
-    float dot = 0.f;
-    if (q < Lq) {
-      const long long off = (bh * p.Sq + q) * (long long)DV + sub * 8;
+    batch_lengths(p, (int)(bh / (unsigned)p.Hq), Lq, Lk);
+    const __nv_bfloat16* o_base = p.o + (long long)bh * p.Sq * DV + sub * 8;
+    const __nv_bfloat16* do_base = p.d_o + (long long)bh * p.Sq * DV + sub * 8;
+    uint4 vo[PASSES], vd[PASSES];
+#pragma unroll
+    for (int u = 0; u < PASSES; ++u) {
+      const int q = qt * BQ + u * RPP + rsub;
+      if (q < Lq) {
+        vo[u] = *reinterpret_cast<const uint4*>(o_base + (long long)q * DV);
+        vd[u] = *reinterpret_cast<const uint4*>(do_base + (long long)q * DV);
+      } else {
+        vo[u] = make_uint4(0, 0, 0, 0);
+        vd[u] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    float* qs = p.qstat + (long long)t * QSTAT_FLOATS;
+#pragma unroll
+    for (int u = 0; u < PASSES; ++u) {
+      const int qi = u * RPP + rsub;
+      const int q = qt * BQ + qi;
       float fo[8], fd[8];
-      unpack8(*reinterpret_cast<const uint4*>(p.o + off), fo);
-      unpack8(*reinterpret_cast<const uint4*>(p.d_o + off), fd);
+      unpack8(vo[u], fo);
+      unpack8(vd[u], fd);
+      float dot = 0.f;
 #pragma unroll
       for (int i = 0; i < 8; ++i) dot = fmaf(fo[i], fd[i], dot);
-    }
 #pragma unroll
-    for (int s = TPR / 2; s > 0; s >>= 1) dot += __shfl_xor_sync(group_mask, dot, s, TPR);
-    if (sub == 0) {
-      float lse2 = INFINITY, delta = 0.f;
-      if (q < Lq) {
-        const float l = p.lse[bh * p.Sq + q];
-        lse2 = (l == -INFINITY) ? INFINITY : l * LOG2E;
-        delta = dot;
+      for (int sft = TPR / 2; sft > 0; sft >>= 1) dot += __shfl_xor_sync(group_mask, dot, sft, TPR);
+      if (sub == 0) {
+        float lse2 = INFINITY, delta = 0.f;
+        if (q < Lq) {
+          const float l = p.lse[(long long)bh * p.Sq + q];
+          lse2 = (l == -INFINITY) ? INFINITY : l * LOG2E;
+          delta = dot;
+        }
+        qs[qi] = lse2;
+        qs[BQ + qi] = delta;
       }
-      float* qs = p.qstat + t * QSTAT_FLOATS;
-      qs[qi] = lse2;
-      qs[BQ + qi] = delta;
     }
   }
 
   // Clear the dQ accumulator (dQ-reduction route), the stand-in zero dS tile
   // (two-kernel route), and the counters (+ ticket).
+  const long long nthreads = (long long)gridDim.x * blockDim.x;
+  const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
   if (p.dq_accum) {
     float4* acc = reinterpret_cast<float4*>(p.dq_accum);
@@ -97,53 +116,76 @@ __global__ void __launch_bounds__(256) sdpa_bwd_preprocess(const ChainParams p) 
 
 // ---------------------------------------------------------------- dq convert
 // dq_accum: [B*Hq][n_qt*BQ][Dqk] fp32, row-major; rows past S_q are padding.
+// Thread item i = (row, 8-column chunk) of dQ; 32-bit index arithmetic.
 template <int DQK>
 __global__ void __launch_bounds__(256) sdpa_bwd_dq_convert(const ChainParams p) {
   pdl_wait_prior_grid();
-  constexpr int PER_ROW = DQK / 8;
-  const long long total = (long long)p.B * p.Hq * p.Sq * PER_ROW;
-  const long long nthreads = (long long)gridDim.x * blockDim.x;
-  const long long rows_pad = (long long)p.n_qt * BQ;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += nthreads) {
-    const int c8 = (int)(i % PER_ROW);
-    const long long r = i / PER_ROW;  // (b*Hq + h)*Sq + q
-    const long long bh = r / p.Sq;
-    const int q = (int)(r % p.Sq);
-    const float* src = p.dq_accum + (bh * rows_pad + q) * DQK + c8 * 8;
-    const float4 a = *reinterpret_cast<const float4*>(src);
-    const float4 c = *reinterpret_cast<const float4*>(src + 4);
-    uint4 out;
-    out.x = pack_bf16x2(a.x * p.scale, a.y * p.scale);
-    out.y = pack_bf16x2(a.z * p.scale, a.w * p.scale);
-    out.z = pack_bf16x2(c.x * p.scale, c.y * p.scale);
-    out.w = pack_bf16x2(c.z * p.scale, c.w * p.scale);
-    *reinterpret_cast<uint4*>(p.dq + r * DQK + c8 * 8) = out;
+  constexpr unsigned PER_ROW = DQK / 8;
+  const unsigned total = (unsigned)p.B * p.Hq * p.Sq * PER_ROW;
+  const unsigned nthreads = gridDim.x * blockDim.x;
+  const unsigned rows_pad = (unsigned)p.n_qt * BQ;
+  constexpr int VEC = 4;
+  for (unsigned i0 = blockIdx.x * blockDim.x + threadIdx.x; i0 < total; i0 += nthreads * VEC) {
+    float4 a[VEC], c[VEC];
+#pragma unroll
+    for (int u = 0; u < VEC; ++u) {
+      const unsigned i = i0 + u * nthreads;
+      if (i >= total) continue;
+      const unsigned r = i / PER_ROW, c8 = i - r * PER_ROW;  // r = (b*Hq + h)*Sq + q
+      const unsigned bh = r / (unsigned)p.Sq, q = r - bh * (unsigned)p.Sq;
+      const float* src = p.dq_accum + ((long long)bh * rows_pad + q) * DQK + c8 * 8;
+      a[u] = *reinterpret_cast<const float4*>(src);
+      c[u] = *reinterpret_cast<const float4*>(src + 4);
+    }
+#pragma unroll
+    for (int u = 0; u < VEC; ++u) {
+      const unsigned i = i0 + u * nthreads;
+      if (i >= total) continue;
+      uint4 out;
+      out.x = pack_bf16x2(a[u].x * p.scale, a[u].y * p.scale);
+      out.y = pack_bf16x2(a[u].z * p.scale, a[u].w * p.scale);
+      out.z = pack_bf16x2(c[u].x * p.scale, c[u].y * p.scale);
+      out.w = pack_bf16x2(c[u].z * p.scale, c[u].w * p.scale);
+      *reinterpret_cast<uint4*>(p.dq + (long long)i * 8) = out;
+    }
   }
 }
 
 // ---------------------------------------------------------------- GQA reduce
-__global__ void __launch_bounds__(256) sdpa_bwd_gqa_reduce(const ChainParams p) {
-  pdl_wait_prior_grid();
-  const long long rows = (long long)p.B * p.Hkv * p.Skv;
-  const long long nk = rows * (p.Dqk / 8), nv = rows * (p.Dv / 8);
-  const long long nthreads = (long long)gridDim.x * blockDim.x;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nk + nv; i += nthreads) {
-    const bool is_k = i < nk;
-    const long long vec = is_k ? i : i - nk;
-    const int D = is_k ? p.Dqk : p.Dv;
-    const __nv_bfloat16* ws = is_k ? p.dk_ws : p.dv_ws;
-    __nv_bfloat16* out = is_k ? p.dk : p.dv;
-    const long long row = vec / (D / 8);
-    const int c8 = (int)(vec % (D / 8));
-    const int k = (int)(row % p.Skv);
-    const long long bhk = row / p.Skv;
-    const int hk = (int)(bhk % p.Hkv);
-    const long long b = bhk / p.Hkv;
+// One output row (b, kv head, key) per item, its D/8 chunks on consecutive
+// lanes: 256 threads cover 256 / (D/8) rows per pass. dK and dV are separate
+// passes (their widths differ for MLA head dims).
+template <int D>
+__device__ __forceinline__ void gqa_reduce_part(const ChainParams& p, const __nv_bfloat16* ws,
+                                                __nv_bfloat16* out) {
+  constexpr int CPR = D / 8;               // chunks per row
+  const unsigned rows = (unsigned)p.B * p.Hkv * p.Skv;
+  const unsigned items = rows * CPR;
+  const unsigned nthreads = gridDim.x * blockDim.x;
+  for (unsigned i = blockIdx.x * blockDim.x + threadIdx.x; i < items; i += nthreads) {
+    const unsigned row = i / CPR, c8 = i - row * CPR;
+    const unsigned bhk = row / (unsigned)p.Skv, k = row - bhk * (unsigned)p.Skv;
+    const unsigned b = bhk / (unsigned)p.Hkv, hk = bhk - b * (unsigned)p.Hkv;
+    const long long head_stride = (long long)p.Skv * D;
+    const __nv_bfloat16* src = ws + ((long long)(b * p.Hq + hk * p.G)) * head_stride + (long long)k * D + c8 * 8;
+    uint4 v[8];
+    const int G = p.G;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)  // issue the group's loads together (G <= 8 here)
+      if (j < G) v[j] = *reinterpret_cast<const uint4*>(src + j * head_stride);
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < p.G; ++j) {  // ascending query head: fixed order
-      const long long h = (long long)hk * p.G + j;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {  // ascending query head: fixed order
+      if (j < G) {
+        float f[8];
+        unpack8(v[j], f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] += f[e];
+      }
+    }
+    for (int j = 8; j < G; ++j) {  // larger groups: remaining heads, same order
       float f[8];
-      unpack8(*reinterpret_cast<const uint4*>(ws + ((b * p.Hq + h) * p.Skv + k) * D + c8 * 8), f);
+      unpack8(*reinterpret_cast<const uint4*>(src + j * head_stride), f);
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[e] += f[e];
     }
@@ -152,8 +194,15 @@ __global__ void __launch_bounds__(256) sdpa_bwd_gqa_reduce(const ChainParams p) 
     o.y = pack_bf16x2(acc[2], acc[3]);
     o.z = pack_bf16x2(acc[4], acc[5]);
     o.w = pack_bf16x2(acc[6], acc[7]);
-    *reinterpret_cast<uint4*>(out + row * D + c8 * 8) = o;
+    *reinterpret_cast<uint4*>(out + (long long)row * D + c8 * 8) = o;
   }
+}
+
+template <int DQK, int DV>
+__global__ void __launch_bounds__(256) sdpa_bwd_gqa_reduce(const ChainParams p) {
+  pdl_wait_prior_grid();
+  gqa_reduce_part<DQK>(p, p.dk_ws, p.dk);
+  gqa_reduce_part<DV>(p, p.dv_ws, p.dv);
 }
 
 cudaError_t launch_preprocess(const ChainParams& p, int grid, cudaStream_t s) {
@@ -162,7 +211,11 @@ cudaError_t launch_preprocess(const ChainParams& p, int grid, cudaStream_t s) {
 }
 
 cudaError_t launch_gqa_reduce(const ChainParams& p, int grid, cudaStream_t s) {
-  return launch_kernel(sdpa_bwd_gqa_reduce, dim3(grid), dim3(256), 0, s, true, p);
+  if (p.Dqk == 64)
+    return launch_kernel(sdpa_bwd_gqa_reduce<64, 64>, dim3(grid), dim3(256), 0, s, true, p);
+  if (p.Dqk == 192)
+    return launch_kernel(sdpa_bwd_gqa_reduce<192, 128>, dim3(grid), dim3(256), 0, s, true, p);
+  return launch_kernel(sdpa_bwd_gqa_reduce<128, 128>, dim3(grid), dim3(256), 0, s, true, p);
 }
 
 cudaError_t launch_dq_convert(const ChainParams& p, int grid, cudaStream_t s) {

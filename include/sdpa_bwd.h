@@ -45,7 +45,8 @@ extern "C" {
 
 typedef enum {
   SDPA_OK = 0,
-  SDPA_ERR_INVALID = 1,     /* null pointer, bad size, H_kv not dividing H_q        */
+  SDPA_ERR_INVALID = 1,     /* null pointer, bad size (a tensor of 2^31 elements or
+                               more), H_kv not dividing H_q                          */
   SDPA_ERR_UNSUPPORTED = 2, /* head dims / mask combination / device not served     */
   SDPA_ERR_ALIGN = 3,       /* a tensor pointer is not 16-byte aligned              */
   SDPA_ERR_WORKSPACE = 4,   /* workspace smaller than sdpa_bwd_workspace_size()     */
