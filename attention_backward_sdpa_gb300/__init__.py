@@ -22,7 +22,7 @@ from . import _build
 __all__ = ["sdpa_bwd", "workspace_size", "check_device_status", "profile_enable", "profile_read",
            "library_path", "load", "SdpaError", "KERNEL_NAMES"]
 
-KERNEL_NAMES = ("preprocess", "main", "gqa_reduce", "dq")
+KERNEL_NAMES = ("preprocess", "main", "dq")
 
 _STATUS = {0: "SDPA_OK", 1: "SDPA_ERR_INVALID", 2: "SDPA_ERR_UNSUPPORTED", 3: "SDPA_ERR_ALIGN",
            4: "SDPA_ERR_WORKSPACE", 5: "SDPA_ERR_CUDA", 6: "SDPA_ERR_TIMEOUT"}
@@ -167,7 +167,7 @@ def profile_enable(on: bool = True) -> None:
 
 def profile_read():
     """{kernel name: (total ms, launches)} accumulated since profile_enable()."""
-    ms = (ctypes.c_float * 4)()
-    n = (ctypes.c_int * 4)()
-    load().sdpa_bwd_profile_read(ms, n, 4)
+    ms = (ctypes.c_float * len(KERNEL_NAMES))()
+    n = (ctypes.c_int * len(KERNEL_NAMES))()
+    load().sdpa_bwd_profile_read(ms, n, len(KERNEL_NAMES))
     return {name: (float(ms[i]), int(n[i])) for i, name in enumerate(KERNEL_NAMES)}

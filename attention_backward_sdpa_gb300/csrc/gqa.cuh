@@ -1,0 +1,83 @@
+// gqa.cuh -- the fixed-order GQA/MQA group reduction of dK/dV ("GQA/MQA group
+// reduction" section of the cuDNN frontend page "SDPA Backward (SM120)"):
+// dK[b, kv head, key] = sum over the group's query heads, in ascending head
+// order, of the per-query-head bf16 partials, accumulated in fp32 and rounded
+// once to bf16 (bitwise reproducible by construction). Run by the dQ kernels
+// over slices of the output rows, overlapping their other work.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace sdpa {
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+// Rows [row_begin, row_end) of one output (dK with D = D_qk or dV with D = D_v),
+// one 8-column chunk per item, items strided over `nthreads` threads.
+template <int D>
+__device__ __forceinline__ void gqa_reduce_rows(const ChainParams& p, const __nv_bfloat16* ws,
+                                                __nv_bfloat16* out, unsigned row_begin,
+                                                unsigned row_end, unsigned thread,
+                                                unsigned nthreads) {
+  constexpr unsigned CPR = D / 8;  // chunks per row
+  const unsigned items = (row_end > row_begin ? row_end - row_begin : 0) * CPR;
+  const long long head_stride = (long long)p.Skv * D;
+  const int G = p.G;
+  for (unsigned it = thread; it < items; it += nthreads) {
+    const unsigned row = row_begin + it / CPR, c8 = it % CPR;
+    const unsigned bhk = row / (unsigned)p.Skv, k = row - bhk * (unsigned)p.Skv;
+    const unsigned b = bhk / (unsigned)p.Hkv, hk = bhk - b * (unsigned)p.Hkv;
+    const __nv_bfloat16* src =
+        ws + (long long)(b * p.Hq + hk * G) * head_stride + (long long)k * D + c8 * 8;
+    uint4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)  // issue the group's loads together
+      if (j < G) v[j] = *reinterpret_cast<const uint4*>(src + j * head_stride);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {  // ascending query head: fixed order
+      if (j < G) {
+        float f[8];
+        unpack8(v[j], f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] += f[e];
+      }
+    }
+    for (int j = 8; j < G; ++j) {  // larger groups: the remaining heads, same order
+      float f[8];
+      unpack8(*reinterpret_cast<const uint4*>(src + j * head_stride), f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] += f[e];
+    }
+    uint4 o;
+    o.x = pack_bf16x2(acc[0], acc[1]);
+    o.y = pack_bf16x2(acc[2], acc[3]);
+    o.z = pack_bf16x2(acc[4], acc[5]);
+    o.w = pack_bf16x2(acc[6], acc[7]);
+    *reinterpret_cast<uint4*>(out + (long long)row * D + c8 * 8) = o;
+  }
+}
+
+// The slice of output rows assigned to CTA `cta` of `n_ctas` (both outputs).
+template <int DQK, int DV>
+__device__ __forceinline__ void gqa_reduce_slice(const ChainParams& p, unsigned cta, unsigned n_ctas,
+                                                 unsigned thread, unsigned nthreads) {
+  if (p.dk_ws == nullptr) return;  // MHA: the main kernel wrote dK/dV directly
+  const unsigned rows = (unsigned)p.B * p.Hkv * p.Skv;
+  const unsigned per = (rows + n_ctas - 1) / n_ctas;
+  const unsigned lo = cta * per, hi = (lo + per < rows) ? lo + per : rows;
+  gqa_reduce_rows<DQK>(p, p.dk_ws, p.dk, lo, hi, thread, nthreads);
+  gqa_reduce_rows<DV>(p, p.dv_ws, p.dv, lo, hi, thread, nthreads);
+}
+
+}  // namespace sdpa

@@ -4,7 +4,8 @@
 // One call validates its arguments, carves the workspace, encodes the four TMA
 // tensor maps and enqueues the kernel chain on the caller's stream
 // (cuDNN frontend docs, "SDPA Backward (SM120)", section "The kernel chain"):
-//   preprocess -> main -> [gqa_reduce when H_kv < H_q] -> dq_convert
+//   preprocess -> main -> dq (convert, or dS x K on the two-kernel route)
+// with the GQA group reduction of dK/dV folded into the dq kernel.
 // Every launch after the first uses programmatic dependent launch, so each
 // kernel's prologue overlaps its predecessor's tail; each kernel waits for its
 // predecessor's completion (griddepcontrol.wait) before touching its outputs.
@@ -36,8 +37,8 @@ int g_num_sms[kMaxDevices] = {};
 
 // Profiling state.
 bool g_profile = false;
-float g_prof_ms[4] = {};
-int g_prof_n[4] = {};
+float g_prof_ms[3] = {};
+int g_prof_n[3] = {};
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -141,8 +142,8 @@ bool make_bhsd_map(CUtensorMap* m, const void* base, int D, int S, long long BH,
 // resolved once at the end of the call, so no synchronization sits between
 // launches (a busy stream keeps host launch latency out of the intervals).
 struct ProfEvents {
-  cudaEvent_t ev[4][2] = {};
-  bool used[4] = {};
+  cudaEvent_t ev[3][2] = {};
+  bool used[3] = {};
   cudaStream_t s;
   explicit ProfEvents(cudaStream_t s_) : s(s_) {}
   void begin(int slot) {
@@ -156,7 +157,7 @@ struct ProfEvents {
     if (g_profile && used[slot]) cudaEventRecord(ev[slot][1], s);
   }
   ~ProfEvents() {
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 3; ++i) {
       if (!used[i]) continue;
       cudaEventSynchronize(ev[i][1]);
       float ms = 0.f;
@@ -203,7 +204,7 @@ size_t sdpa_bwd_workspace_size(int B, int H_q, int H_kv, int S_q, int S_kv, int 
 int sdpa_bwd_profile_enable(int on) {
   std::lock_guard<std::mutex> lock(g_mu);
   g_profile = on != 0;
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < 3; ++i) {
     g_prof_ms[i] = 0.f;
     g_prof_n[i] = 0;
   }
@@ -212,11 +213,11 @@ int sdpa_bwd_profile_enable(int on) {
 
 int sdpa_bwd_profile_read(float* ms, int* launches, int n) {
   std::lock_guard<std::mutex> lock(g_mu);
-  for (int i = 0; i < n && i < 4; ++i) {
+  for (int i = 0; i < n && i < 3; ++i) {
     if (ms) ms[i] = g_prof_ms[i];
     if (launches) launches[i] = g_prof_n[i];
   }
-  return 4;
+  return 3;
 }
 
 int sdpa_bwd_check_device_status(void* stream) {
@@ -337,15 +338,10 @@ int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const v
     e = D_qk == 192 ? launch_main_ds(maps, p, stream) : launch_main(maps, p, stream);
     prof.end(1);
   }
-  if (e == cudaSuccess && H_kv < H_q) {
+  if (e == cudaSuccess) {  // dQ (and, under GQA, the dK/dV group reduction)
     prof.begin(2);
-    e = launch_gqa_reduce(p, aux_grid, stream);
-    prof.end(2);
-  }
-  if (e == cudaSuccess) {
-    prof.begin(3);
     e = ds_route ? launch_dq_from_ds(maps.k, p, stream) : launch_dq_convert(p, aux_grid, stream);
-    prof.end(3);
+    prof.end(2);
   }
   if (own_ws) cudaFreeAsync(workspace, stream);
   return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;

@@ -6,29 +6,19 @@
 //               deterministic-mode counters. ("The kernel chain": dot.)
 //   dq_convert  dQ = bf16(scale * dq_accum), dropping the accumulator's
 //               padding rows. ("The kernel chain": cvt.)
-//   gqa_reduce  dK/dV of each KV head = fp32 sum of its group's per-query-head
-//               partials in ascending head order, rounded to bf16.
-//               ("GQA/MQA group reduction".)
+// The dQ convert also carries the GQA group reduction of dK/dV (gqa.cuh).
 //
-// All three move 16-byte vectors with consecutive threads on consecutive
+// Both move 16-byte vectors with consecutive threads on consecutive
 // addresses; grids are sized to a few CTAs per SM and stride over the work.
 #include <cuda_bf16.h>
 
 #include <cmath>
 
 #include "common.cuh"
+#include "gqa.cuh"
 #include "ptx.cuh"
 
 namespace sdpa {
-
-__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
-}
 
 // ---------------------------------------------------------------- preprocess
 // One 64-row query tile per CTA pass: TPR = DV/8 lanes per row (8 bf16 each),
@@ -117,9 +107,11 @@ __global__ void __launch_bounds__(256) sdpa_bwd_preprocess(const ChainParams p) 
 // ---------------------------------------------------------------- dq convert
 // dq_accum: [B*Hq][n_qt*BQ][Dqk] fp32, row-major; rows past S_q are padding.
 // Thread item i = (row, 8-column chunk) of dQ; 32-bit index arithmetic.
-template <int DQK>
+// It also carries the GQA group reduction of dK/dV (a slice per CTA).
+template <int DQK, int DV>
 __global__ void __launch_bounds__(256) sdpa_bwd_dq_convert(const ChainParams p) {
   pdl_wait_prior_grid();
+  gqa_reduce_slice<DQK, DV>(p, blockIdx.x, gridDim.x, threadIdx.x, blockDim.x);
   constexpr unsigned PER_ROW = DQK / 8;
   const unsigned total = (unsigned)p.B * p.Hq * p.Sq * PER_ROW;
   const unsigned nthreads = gridDim.x * blockDim.x;
@@ -151,76 +143,15 @@ __global__ void __launch_bounds__(256) sdpa_bwd_dq_convert(const ChainParams p) 
   }
 }
 
-// ---------------------------------------------------------------- GQA reduce
-// One output row (b, kv head, key) per item, its D/8 chunks on consecutive
-// lanes: 256 threads cover 256 / (D/8) rows per pass. dK and dV are separate
-// passes (their widths differ for MLA head dims).
-template <int D>
-__device__ __forceinline__ void gqa_reduce_part(const ChainParams& p, const __nv_bfloat16* ws,
-                                                __nv_bfloat16* out) {
-  constexpr int CPR = D / 8;               // chunks per row
-  const unsigned rows = (unsigned)p.B * p.Hkv * p.Skv;
-  const unsigned items = rows * CPR;
-  const unsigned nthreads = gridDim.x * blockDim.x;
-  for (unsigned i = blockIdx.x * blockDim.x + threadIdx.x; i < items; i += nthreads) {
-    const unsigned row = i / CPR, c8 = i - row * CPR;
-    const unsigned bhk = row / (unsigned)p.Skv, k = row - bhk * (unsigned)p.Skv;
-    const unsigned b = bhk / (unsigned)p.Hkv, hk = bhk - b * (unsigned)p.Hkv;
-    const long long head_stride = (long long)p.Skv * D;
-    const __nv_bfloat16* src = ws + ((long long)(b * p.Hq + hk * p.G)) * head_stride + (long long)k * D + c8 * 8;
-    uint4 v[8];
-    const int G = p.G;
-#pragma unroll
-    for (int j = 0; j < 8; ++j)  // issue the group's loads together (G <= 8 here)
-      if (j < G) v[j] = *reinterpret_cast<const uint4*>(src + j * head_stride);
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {  // ascending query head: fixed order
-      if (j < G) {
-        float f[8];
-        unpack8(v[j], f);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] += f[e];
-      }
-    }
-    for (int j = 8; j < G; ++j) {  // larger groups: remaining heads, same order
-      float f[8];
-      unpack8(*reinterpret_cast<const uint4*>(src + j * head_stride), f);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] += f[e];
-    }
-    uint4 o;
-    o.x = pack_bf16x2(acc[0], acc[1]);
-    o.y = pack_bf16x2(acc[2], acc[3]);
-    o.z = pack_bf16x2(acc[4], acc[5]);
-    o.w = pack_bf16x2(acc[6], acc[7]);
-    *reinterpret_cast<uint4*>(out + (long long)row * D + c8 * 8) = o;
-  }
-}
-
-template <int DQK, int DV>
-__global__ void __launch_bounds__(256) sdpa_bwd_gqa_reduce(const ChainParams p) {
-  pdl_wait_prior_grid();
-  gqa_reduce_part<DQK>(p, p.dk_ws, p.dk);
-  gqa_reduce_part<DV>(p, p.dv_ws, p.dv);
-}
-
 cudaError_t launch_preprocess(const ChainParams& p, int grid, cudaStream_t s) {
   return p.Dv == 64 ? launch_kernel(sdpa_bwd_preprocess<64>, dim3(grid), dim3(256), 0, s, false, p)
                     : launch_kernel(sdpa_bwd_preprocess<128>, dim3(grid), dim3(256), 0, s, false, p);
 }
 
-cudaError_t launch_gqa_reduce(const ChainParams& p, int grid, cudaStream_t s) {
-  if (p.Dqk == 64)
-    return launch_kernel(sdpa_bwd_gqa_reduce<64, 64>, dim3(grid), dim3(256), 0, s, true, p);
-  if (p.Dqk == 192)
-    return launch_kernel(sdpa_bwd_gqa_reduce<192, 128>, dim3(grid), dim3(256), 0, s, true, p);
-  return launch_kernel(sdpa_bwd_gqa_reduce<128, 128>, dim3(grid), dim3(256), 0, s, true, p);
-}
-
 cudaError_t launch_dq_convert(const ChainParams& p, int grid, cudaStream_t s) {
-  return p.Dqk == 64 ? launch_kernel(sdpa_bwd_dq_convert<64>, dim3(grid), dim3(256), 0, s, true, p)
-                     : launch_kernel(sdpa_bwd_dq_convert<128>, dim3(grid), dim3(256), 0, s, true, p);
+  return p.Dqk == 64
+             ? launch_kernel(sdpa_bwd_dq_convert<64, 64>, dim3(grid), dim3(256), 0, s, true, p)
+             : launch_kernel(sdpa_bwd_dq_convert<128, 128>, dim3(grid), dim3(256), 0, s, true, p);
 }
 
 }  // namespace sdpa

@@ -14,11 +14,13 @@
 // MN-major), accumulating in tensor memory. The fixed walk order makes dQ
 // bitwise reproducible; there are no atomics and no fp32 accumulator in memory.
 //
-// Warps: 0-3 epilogue (tensor memory -> scale -> bf16 -> dQ), 4 loads, 5 MMA.
+// Warps: 0-3 epilogue (tensor memory -> scale -> bf16 -> dQ; before that, the
+// CTA's slice of the GQA dK/dV group reduction), 4 loads, 5 MMA.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
 #include "common.cuh"
+#include "gqa.cuh"
 #include "ptx.cuh"
 
 namespace sdpa {
@@ -150,6 +152,9 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
+    // While the key walk runs, these warps reduce this CTA's slice of the GQA
+    // group sums (dK/dV), which depend only on the main kernel.
+    gqa_reduce_slice<D, 128>(p, blockIdx.x, gridDim.x, tid, 128);
     const int row = warp * 32 + lane;          // query within the 128-row tile
     const int q = qt0 * BQ + row;
     const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);

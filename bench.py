@@ -3,7 +3,8 @@
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl gb300|reference]
 
-One step = one full backward (preprocess -> main -> [GQA reduce] -> dQ convert)
+One step = one full backward (preprocess -> main -> dQ kernel, which also
+carries the GQA dK/dV group reduction)
 over one batch of the workload, inputs resident in HBM. Each step is timed
 with CUDA events on the launching stream; a 256 MiB buffer is written between
 steps so that every step starts with a cold L2 (the flush is outside the event
@@ -336,7 +337,7 @@ def run_gpu(args, w, t, o, lse, rank, world, device):
         "e2e": {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "clocks": clocks.summary(),
-        "gpu_launches": (4 if w.Hkv < w.Hq else 3) * args.steps,
+        "gpu_launches": 3 * args.steps,
     }
 
 

@@ -125,9 +125,9 @@ int sdpa_bwd_check_device_status(void* stream);
  * events around each launch and synchronizes the stream before returning, so
  * it is for measurement only. sdpa_bwd_profile_read() fills up to n entries of
  * ms[] (total milliseconds) and launches[] (count) per kernel in the order
- * preprocess, main, gqa_reduce, dq (the dQ convert, or on the deterministic
- * two-kernel route the dQ = scale * dS K kernel), and returns the number of
- * kernels.
+ * preprocess, main, dq (the dQ convert, or on the two-kernel route the
+ * dQ = scale * dS K kernel; under GQA it also runs the dK/dV group
+ * reduction), and returns the number of kernels (3).
  * Enabling resets the totals.
  */
 int sdpa_bwd_profile_enable(int on);
