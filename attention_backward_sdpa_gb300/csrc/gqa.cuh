@@ -68,16 +68,22 @@ __device__ __forceinline__ void gqa_reduce_rows(const ChainParams& p, const __nv
   }
 }
 
-// The slice of output rows assigned to CTA `cta` of `n_ctas` (both outputs).
+// Piece `piece` of `n_pieces` of the slice of output rows assigned to CTA
+// `cta` of `n_ctas` (both outputs). Pieces let a kernel spread the work.
 template <int DQK, int DV>
 __device__ __forceinline__ void gqa_reduce_slice(const ChainParams& p, unsigned cta, unsigned n_ctas,
-                                                 unsigned thread, unsigned nthreads) {
+                                                 unsigned thread, unsigned nthreads,
+                                                 unsigned piece = 0, unsigned n_pieces = 1) {
   if (p.dk_ws == nullptr) return;  // MHA: the main kernel wrote dK/dV directly
   const unsigned rows = (unsigned)p.B * p.Hkv * p.Skv;
   const unsigned per = (rows + n_ctas - 1) / n_ctas;
   const unsigned lo = cta * per, hi = (lo + per < rows) ? lo + per : rows;
-  gqa_reduce_rows<DQK>(p, p.dk_ws, p.dk, lo, hi, thread, nthreads);
-  gqa_reduce_rows<DV>(p, p.dv_ws, p.dv, lo, hi, thread, nthreads);
+  if (lo >= hi || piece >= n_pieces) return;
+  const unsigned pp = (hi - lo + n_pieces - 1) / n_pieces;
+  const unsigned plo = lo + piece * pp, phi = (plo + pp < hi) ? plo + pp : hi;
+  if (plo >= phi) return;
+  gqa_reduce_rows<DQK>(p, p.dk_ws, p.dk, plo, phi, thread, nthreads);
+  gqa_reduce_rows<DV>(p, p.dv_ws, p.dv, plo, phi, thread, nthreads);
 }
 
 }  // namespace sdpa

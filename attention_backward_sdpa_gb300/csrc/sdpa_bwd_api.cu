@@ -340,7 +340,7 @@ int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const v
   }
   if (e == cudaSuccess) {  // dQ (and, under GQA, the dK/dV group reduction)
     prof.begin(2);
-    e = ds_route ? launch_dq_from_ds(maps.k, p, stream) : launch_dq_convert(p, aux_grid, stream);
+    e = ds_route ? launch_dq_from_ds(maps.k, p, stream, sms) : launch_dq_convert(p, aux_grid, stream);
     prof.end(2);
   }
   if (own_ws) cudaFreeAsync(workspace, stream);

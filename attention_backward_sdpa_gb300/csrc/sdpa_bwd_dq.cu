@@ -3,8 +3,8 @@
 // "Determinism": the main kernel streams dS to a workspace and a Q-stationary
 // kernel computes dQ = scale * dS K over an ascending key walk).
 //
-// One CTA owns 128 query rows (two 64-row query tiles) of one (batch, query
-// head). It walks, in ascending order, every 128-key tile that the main kernel
+// A unit is 128 query rows (two 64-row query tiles) of one (batch, query
+// head). For each unit a CTA walks, in ascending order, every 128-key tile that the main kernel
 // visited for either of its query tiles (the same loop bounds), and for each
 // loads the key tile K (TMA) and the two stored dS^T tiles (bulk copies of the
 // main kernel's swizzled shared-memory images; a tile the main kernel did not
@@ -35,11 +35,49 @@ struct DqLayout {
   static constexpr int TILE_DS = 2 * DS_TILE_BYTES;     // two dS^T tiles: [2][128 keys][64 q]
   static constexpr int STAGE = TILE_K + TILE_DS;
   static constexpr int OFF_BAR = NSTAGE * STAGE;
-  static constexpr int BYTES = OFF_BAR + (2 * NSTAGE + 1) * 8 + 64;
-  static constexpr uint32_t TMEM_COLS = D <= 128 ? 128 : 256;
+  static constexpr int NUM_BARS = 2 * NSTAGE + 4;       // full/empty per stage, acc full/empty x2
+  static constexpr int BYTES = OFF_BAR + NUM_BARS * 8 + 64;
+  static constexpr uint32_t ACC_COLS = D <= 128 ? 128 : 256;   // one accumulator, padded
+  static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;          // double-buffered
   static_assert(BYTES <= 232448, "shared memory budget");
+  static_assert(TMEM_COLS <= 512, "tensor memory budget");
 };
 
+// Work unit u (128 query rows of one (batch, query head)): query-tile pair
+// major, so concurrently running CTAs of a wave share key tiles of a head.
+struct DqUnit {
+  int bh, qp, b, hk, qt0, qt1, Lq, Lk, kv_first, n;
+};
+
+__device__ __forceinline__ DqUnit dq_unit(const ChainParams& p, int u) {
+  DqUnit w;
+  const int n_qp = ceil_div(p.n_qt, 2);
+  w.qp = u % n_qp;
+  w.bh = u / n_qp;
+  w.b = w.bh / p.Hq;
+  w.hk = (w.bh % p.Hq) / p.G;
+  w.qt0 = 2 * w.qp;
+  w.qt1 = 2 * w.qp + 1;  // may be past the last tile
+  batch_lengths(p, w.b, w.Lq, w.Lk);
+  // Key tiles visited for either query tile, ascending: a contiguous range.
+  int first = p.n_kt, last = -1;
+  for (int kt = 0; kt < p.n_kt; ++kt) {
+    int lo, hi;
+    visited_query_tiles(kt, w.Lq, w.Lk, p.causal, p.bottom_right, p.window_left, p.window_right, lo, hi);
+    if ((lo <= w.qt0 && w.qt0 <= hi) || (w.qt1 < p.n_qt && lo <= w.qt1 && w.qt1 <= hi)) {
+      first = min(first, kt);
+      last = kt;
+    }
+  }
+  w.kv_first = first;
+  w.n = last - first + 1;  // may be <= 0
+  return w;
+}
+
+// Persistent: each CTA walks units blockIdx.x, blockIdx.x + gridDim.x, ...
+// The load warp runs ahead across unit boundaries through one stage ring; the
+// MMA warp alternates between two tensor-memory accumulators (counted over
+// non-empty units only) so that the epilogue of one unit overlaps the next.
 template <int D>
 __global__ void __launch_bounds__(DQ_THREADS, 1)
     sdpa_bwd_dq_from_ds(const __grid_constant__ CUtensorMap k_map, const ChainParams p) {
@@ -52,30 +90,11 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   }
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
   uint64_t* empty = full + L::NSTAGE;
-  uint64_t* done = empty + L::NSTAGE;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* acc_full = empty + L::NSTAGE;   // [2]
+  uint64_t* acc_empty = acc_full + 2;       // [2], 128 arrivals
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-  const int n_qp = ceil_div(p.n_qt, 2);
-  const int qp = blockIdx.x % n_qp;
-  const int bh = blockIdx.x / n_qp;
-  const int b = bh / p.Hq, h = bh % p.Hq, hk = h / p.G;
-  const int qt0 = 2 * qp, qt1 = 2 * qp + 1;  // qt1 may be past the last tile
-  int Lq, Lk;
-  batch_lengths(p, b, Lq, Lk);
-
-  // Key tiles visited for either query tile, ascending: a contiguous range.
-  int kv_first = p.n_kt, kv_last = -1;
-  for (int kt = 0; kt < p.n_kt; ++kt) {
-    int lo, hi;
-    visited_query_tiles(kt, Lq, Lk, p.causal, p.bottom_right, p.window_left, p.window_right, lo, hi);
-    const bool any = (lo <= qt0 && qt0 <= hi) || (qt1 < p.n_qt && lo <= qt1 && qt1 <= hi);
-    if (any) {
-      kv_first = min(kv_first, kt);
-      kv_last = kt;
-    }
-  }
-  const int n = kv_last - kv_first + 1;  // may be <= 0
+  const int n_units = ceil_div(p.n_qt, 2) * p.B * p.Hq;
 
   if (tid == 0) {
     *abort_flag = 0;
@@ -83,7 +102,10 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
-    mbar_init(done, 1);
+    mbar_init(&acc_full[0], 1);
+    mbar_init(&acc_full[1], 1);
+    mbar_init(&acc_empty[0], 128);
+    mbar_init(&acc_empty[1], 128);
     fence_mbar_init();
   }
   if (warp == 5) {
@@ -94,98 +116,131 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  pdl_wait_prior_grid();  // the dS tiles come from the main kernel
+  pdl_wait_prior_grid();  // the dS tiles (and GQA partials) come from the main kernel
 
   if (warp == 4) {
     // ------------------------------------------------------------ loads
-    if (lane == 0 && n > 0) {
+    if (lane == 0) {
       prefetch_tmap(&k_map);
-      for (int i = 0; i < n; ++i) {
-        const int st = i % L::NSTAGE;
-        const int kt = kv_first + i;
-        if (i >= L::NSTAGE &&
-            !mbar_wait(&empty[st], ((i / L::NSTAGE) - 1) & 1, abort_flag, DQ_WAIT_LIMIT_NS))
-          break;
-        uint8_t* stage = smem + st * L::STAGE;
-        mbar_arrive_expect_tx(&full[st], L::STAGE);
-        for (int blk = 0; blk < D / 64; ++blk)
-          tma_load_3d(stage + blk * (BN * 128), &k_map, &full[st], blk * 64, kt * BN, b * p.Hkv + hk);
-        int lo, hi;
-        visited_query_tiles(kt, Lq, Lk, p.causal, p.bottom_right, p.window_left, p.window_right, lo, hi);
-        for (int half = 0; half < 2; ++half) {
-          const int qt = qt0 + half;
-          const bool stored = qt < p.n_qt && lo <= qt && qt <= hi;
-          const uint8_t* src =
-              stored ? p.ds_ws + (((long long)bh * p.n_kt + kt) * p.n_qt + qt) * (long long)DS_TILE_BYTES
-                     : p.zero_tile;
-          bulk_load(stage + L::TILE_K + half * DS_TILE_BYTES, src, DS_TILE_BYTES, &full[st]);
+      int step = 0;
+      for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+        const DqUnit w = dq_unit(p, u);
+        for (int i = 0; i < w.n; ++i, ++step) {
+          const int st = step % L::NSTAGE;
+          const int kt = w.kv_first + i;
+          if (step >= L::NSTAGE &&
+              !mbar_wait(&empty[st], ((step / L::NSTAGE) - 1) & 1, abort_flag, DQ_WAIT_LIMIT_NS))
+            goto loads_done;
+          uint8_t* stage = smem + st * L::STAGE;
+          mbar_arrive_expect_tx(&full[st], L::STAGE);
+          for (int blk = 0; blk < D / 64; ++blk)
+            tma_load_3d(stage + blk * (BN * 128), &k_map, &full[st], blk * 64, kt * BN, w.b * p.Hkv + w.hk);
+          int lo, hi;
+          visited_query_tiles(kt, w.Lq, w.Lk, p.causal, p.bottom_right, p.window_left, p.window_right, lo, hi);
+          for (int half = 0; half < 2; ++half) {
+            const int qt = w.qt0 + half;
+            const bool stored = qt < p.n_qt && lo <= qt && qt <= hi;
+            const uint8_t* src =
+                stored ? p.ds_ws + (((long long)w.bh * p.n_kt + kt) * p.n_qt + qt) * (long long)DS_TILE_BYTES
+                       : p.zero_tile;
+            bulk_load(stage + L::TILE_K + half * DS_TILE_BYTES, src, DS_TILE_BYTES, &full[st]);
+          }
         }
       }
+    loads_done:;
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA
     constexpr uint32_t ID = idesc_bf16_f32(128, D, true, true);
     constexpr uint64_t T_MN = sdesc_sw128_template(BN * 128, 1024);  // 16 KB block stride
     bool ok = true;
-    for (int i = 0; i < n && ok; ++i) {
-      const int st = i % L::NSTAGE;
-      ok = mbar_wait(&full[st], (i / L::NSTAGE) & 1, abort_flag, DQ_WAIT_LIMIT_NS);
-      __syncwarp();
-      if (!ok) break;
-      tc_fence_after();
-      if (elect_one()) {
-        const uint32_t aK = smem_u32(smem + st * L::STAGE);
-        const uint32_t aS = aK + L::TILE_K;
-        // A = dS as (M = 128 queries, K = keys): the stored dS^T tiles are
-        // [key][query] with queries contiguous, i.e. MN-major, the two 64-query
-        // tiles 16 KB apart. B = K as (N = d, K = keys): MN-major as well.
-#pragma unroll
-        for (int k = 0; k < BN / 16; ++k)
-          mma_ss(tmem, sdesc_at(T_MN, aS + k * 2048), sdesc_at(T_MN, aK + k * 2048), ID,
-                 (i > 0 || k > 0));
-        mma_commit(&empty[st]);
-        if (i == n - 1) mma_commit(done);
+    int step = 0, done_units = 0;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      const DqUnit w = dq_unit(p, u);
+      if (w.n <= 0) continue;
+      const int buf = done_units & 1;
+      const uint32_t acc = tmem + buf * L::ACC_COLS;
+      // The accumulator was read out by the epilogue two non-empty units ago.
+      if (done_units >= 2 &&
+          !mbar_wait(&acc_empty[buf], ((done_units >> 1) - 1) & 1, abort_flag, DQ_WAIT_LIMIT_NS)) {
+        ok = false;
+        break;
       }
       __syncwarp();
+      tc_fence_after();
+      for (int i = 0; i < w.n; ++i, ++step) {
+        const int st = step % L::NSTAGE;
+        ok = mbar_wait(&full[st], (step / L::NSTAGE) & 1, abort_flag, DQ_WAIT_LIMIT_NS);
+        __syncwarp();
+        if (!ok) break;
+        tc_fence_after();
+        if (elect_one()) {
+          const uint32_t aK = smem_u32(smem + st * L::STAGE);
+          const uint32_t aS = aK + L::TILE_K;
+          // A = dS as (M = 128 queries, K = keys): the stored dS^T tiles are
+          // [key][query] with queries contiguous, i.e. MN-major, the two 64-query
+          // tiles 16 KB apart. B = K as (N = d, K = keys): MN-major as well.
+#pragma unroll
+          for (int k = 0; k < BN / 16; ++k)
+            mma_ss(acc, sdesc_at(T_MN, aS + k * 2048), sdesc_at(T_MN, aK + k * 2048), ID,
+                   (i > 0 || k > 0));
+          mma_commit(&empty[st]);
+          if (i == w.n - 1) mma_commit(&acc_full[buf]);
+        }
+        __syncwarp();
+      }
+      ++done_units;
     }
-    if (!ok && elect_one()) mma_commit(done);  // release the epilogue after an abort
-    __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    // While the key walk runs, these warps reduce this CTA's slice of the GQA
-    // group sums (dK/dV), which depend only on the main kernel.
-    gqa_reduce_slice<D, 128>(p, blockIdx.x, gridDim.x, tid, 128);
-    const int row = warp * 32 + lane;          // query within the 128-row tile
-    const int q = qt0 * BQ + row;
+    // dQ of each unit as its accumulator completes. This CTA's slice of the GQA
+    // group sums (dK/dV, which depend only on the main kernel) is split into one
+    // piece per unit, each reduced while that unit's MMAs run.
+    const int my_units = (n_units - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+    int unit_idx = 0;
+    const int row = warp * 32 + lane;          // query within the 128-row unit
     const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
-    bool have = n > 0;
-    if (have) {
-      have = mbar_wait(done, 0, abort_flag, DQ_WAIT_LIMIT_NS);
-      __syncwarp();
-      tc_fence_after();
-    }
-    const bool warp_ok = __all_sync(0xffffffffu, have);
-    __nv_bfloat16* out = p.dq + ((long long)bh * p.Sq + q) * D;
-#pragma unroll
-    for (int c32 = 0; c32 < D / 32; ++c32) {
-      uint32_t r[32];
-      if (warp_ok) {
-        tmem_ld32(t_lane + c32 * 32, r);
-        tmem_ld_wait(r);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) r[i] = 0u;
+    int done_units = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+      const DqUnit w = dq_unit(p, u);
+      const int q = w.qt0 * BQ + row;
+      __nv_bfloat16* out = p.dq + ((long long)w.bh * p.Sq + q) * D;
+      const bool have = w.n > 0;
+      const int buf = done_units & 1;
+      gqa_reduce_slice<D, 128>(p, blockIdx.x, gridDim.x, tid, 128, unit_idx++, my_units);
+      if (have && ok) {
+        ok = mbar_wait(&acc_full[buf], (done_units >> 1) & 1, abort_flag, DQ_WAIT_LIMIT_NS);
+        __syncwarp();
+        tc_fence_after();
       }
-      if (q < p.Sq) {
+      const bool warp_ok = __all_sync(0xffffffffu, ok);
 #pragma unroll
-        for (int v8 = 0; v8 < 4; ++v8) {
-          uint4 o;
-          o.x = pack_bf16x2(__uint_as_float(r[v8 * 8 + 0]) * p.scale, __uint_as_float(r[v8 * 8 + 1]) * p.scale);
-          o.y = pack_bf16x2(__uint_as_float(r[v8 * 8 + 2]) * p.scale, __uint_as_float(r[v8 * 8 + 3]) * p.scale);
-          o.z = pack_bf16x2(__uint_as_float(r[v8 * 8 + 4]) * p.scale, __uint_as_float(r[v8 * 8 + 5]) * p.scale);
-          o.w = pack_bf16x2(__uint_as_float(r[v8 * 8 + 6]) * p.scale, __uint_as_float(r[v8 * 8 + 7]) * p.scale);
-          *reinterpret_cast<uint4*>(out + c32 * 32 + v8 * 8) = o;
+      for (int c32 = 0; c32 < D / 32; ++c32) {
+        uint32_t r[32];
+        if (have && warp_ok) {
+          tmem_ld32(t_lane + buf * L::ACC_COLS + c32 * 32, r);
+          tmem_ld_wait(r);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = 0u;
         }
+        if (q < p.Sq) {
+#pragma unroll
+          for (int v8 = 0; v8 < 4; ++v8) {
+            uint4 o;
+            o.x = pack_bf16x2(__uint_as_float(r[v8 * 8 + 0]) * p.scale, __uint_as_float(r[v8 * 8 + 1]) * p.scale);
+            o.y = pack_bf16x2(__uint_as_float(r[v8 * 8 + 2]) * p.scale, __uint_as_float(r[v8 * 8 + 3]) * p.scale);
+            o.z = pack_bf16x2(__uint_as_float(r[v8 * 8 + 4]) * p.scale, __uint_as_float(r[v8 * 8 + 5]) * p.scale);
+            o.w = pack_bf16x2(__uint_as_float(r[v8 * 8 + 6]) * p.scale, __uint_as_float(r[v8 * 8 + 7]) * p.scale);
+            *reinterpret_cast<uint4*>(out + c32 * 32 + v8 * 8) = o;
+          }
+        }
+      }
+      if (have) {
+        tc_fence_before();
+        mbar_arrive(&acc_empty[buf]);
+        ++done_units;
       }
     }
   }
@@ -208,9 +263,11 @@ cudaError_t dq_kernel_setup() {
                               DqLayout<192>::BYTES);
 }
 
-// One CTA per (batch, query head, 128-row query tile).
-cudaError_t launch_dq_from_ds(const CUtensorMap& k_map, const ChainParams& p, cudaStream_t s) {
-  const dim3 grid((unsigned)(ceil_div(p.n_qt, 2) * p.B * p.Hq));
+// Persistent: one CTA per SM (at most one per unit).
+cudaError_t launch_dq_from_ds(const CUtensorMap& k_map, const ChainParams& p, cudaStream_t s,
+                              int num_sms) {
+  const int units = ceil_div(p.n_qt, 2) * p.B * p.Hq;
+  const dim3 grid((unsigned)(units < num_sms ? units : num_sms));
   if (p.Dqk == 192)
     return launch_kernel(sdpa_bwd_dq_from_ds<192>, grid, dim3(DQ_THREADS), DqLayout<192>::BYTES, s,
                          true, k_map, p);

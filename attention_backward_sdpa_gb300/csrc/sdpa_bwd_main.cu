@@ -33,10 +33,12 @@
 //
 // Shared memory (128-byte swizzle, every tile 1024-byte aligned):
 //   K, V        [D/64 blocks][128 key rows][128 B]
-//   Q, dO x3    [D/64 blocks][64 query rows][128 B]   (3-stage ring)
+//   Q, dO x3/4  [D/64 blocks][64 query rows][128 B]   (stage ring: 4 stages on the
+//                                                      two-kernel route, which
+//                                                      needs no dQ staging)
 //   dS^T x2     [128 key rows][64 queries x 2 B]      (one per slot)
 //   dQ staging  [64 queries][D] fp32                  (bulk reduction source)
-//   qstat x3    LSE*log2e[64], delta[64]
+//   qstat x3/4  LSE*log2e[64], delta[64]
 // Tensor memory (512 columns x 128 lanes, fp32):
 //   slot s: S^T at 128s + [0,64) (P^T written back as bf16 into [0,32) by the
 //           same threads that read S^T), dP^T then dQ^T at 128s + [64,128)
@@ -53,43 +55,46 @@ constexpr int MAIN_THREADS = 512;
 constexpr uint32_t REGS_COMPUTE = 160, REGS_DQ = 96, REGS_CTRL = 96;
 static_assert(128 * (2 * REGS_COMPUTE + REGS_DQ + REGS_CTRL) <= MAIN_THREADS * 128,
               "register split exceeds the launch budget");
-constexpr int NSTAGE = 3;
 constexpr uint64_t WAIT_LIMIT_NS = 4000000000ull;  // 4 s: far above any legal wait
 
 enum : int {
   BAR_KV = 0,
-  BAR_QFULL = 1,      // + stage (3)
-  BAR_QEMPTY = 4,     // + stage (3)
-  BAR_SFULL = 7,      // + slot (2)
-  BAR_DPFULL = 9,     // + slot
-  BAR_PREADY = 11,    // + slot, 128 arrivals
-  BAR_SFREE = 13,     // + slot
-  BAR_DSREADY = 15,   // + slot, 128 arrivals
-  BAR_DQFULL = 17,    // + slot
-  BAR_DQEMPTY = 19,   // + slot, 128 arrivals
-  BAR_STAGEREADY = 21,  // 128 arrivals
-  BAR_STAGEFREE = 22,
-  BAR_MMADONE = 23,     // every MMA of the CTA has completed (epilogue may read dK/dV)
-  BAR_DSCOPIED = 24,    // + slot: the slot's dS^T tile has been read out to global (dS route)
-  NUM_BARS = 26
+  BAR_QFULL = 1,        // + stage (up to 4)
+  BAR_QEMPTY = 5,       // + stage (up to 4)
+  BAR_SFULL = 9,        // + slot (2)
+  BAR_DPFULL = 11,      // + slot
+  BAR_PREADY = 13,      // + slot, 128 arrivals
+  BAR_SFREE = 15,       // + slot
+  BAR_DSREADY = 17,     // + slot, 128 arrivals
+  BAR_DQFULL = 19,      // + slot
+  BAR_DQEMPTY = 21,     // + slot, 128 arrivals
+  BAR_STAGEREADY = 23,  // 128 arrivals
+  BAR_STAGEFREE = 24,
+  BAR_MMADONE = 25,     // every MMA of the CTA has completed (epilogue may read dK/dV)
+  BAR_DSCOPIED = 26,    // + slot: the slot's dS^T tile has been read out to global (dS route)
+  BAR_DPREAD = 28,      // + slot, 128 arrivals: dP^T has been loaded into registers
+  NUM_BARS = 30
 };
 
-template <int D>
+// NST Q/dO stages; the dQ staging buffer exists only on the dQ-reduction route
+// (on the two-kernel route its space holds a fourth stage).
+template <int D, bool DS_OUT>
 struct MainLayout {
+  static constexpr int NST = DS_OUT ? 4 : 3;
   static constexpr int BLK_KV = BN * 128;          // one 64-column block of a 128-row tile
   static constexpr int BLK_Q = BQ * 128;           // one 64-column block of a 64-row tile
   static constexpr int TILE_KV = BN * D * 2;
   static constexpr int TILE_Q = BQ * D * 2;
   static constexpr int TILE_DS = BN * BQ * 2;
-  static constexpr int TILE_DQ = BQ * D * 4;
+  static constexpr int TILE_DQ = DS_OUT ? 0 : BQ * D * 4;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + TILE_KV;
   static constexpr int OFF_Q = OFF_V + TILE_KV;
-  static constexpr int OFF_DO = OFF_Q + NSTAGE * TILE_Q;
-  static constexpr int OFF_DS = OFF_DO + NSTAGE * TILE_Q;
+  static constexpr int OFF_DO = OFF_Q + NST * TILE_Q;
+  static constexpr int OFF_DS = OFF_DO + NST * TILE_Q;
   static constexpr int OFF_DQ = OFF_DS + 2 * TILE_DS;
   static constexpr int OFF_QS = OFF_DQ + TILE_DQ;
-  static constexpr int OFF_BAR = OFF_QS + NSTAGE * QSTAT_FLOATS * 4;
+  static constexpr int OFF_BAR = OFF_QS + NST * QSTAT_FLOATS * 4;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int BYTES = OFF_MISC + 64;
   static constexpr uint32_t COL_DV = 256, COL_DK = 256 + D;
@@ -109,7 +114,8 @@ __device__ __forceinline__ void set_status(int* status, int bit) { atomicOr(stat
 template <int D, bool DS_OUT>
 __global__ void __launch_bounds__(MAIN_THREADS, 1)
     sdpa_bwd_main(const __grid_constant__ MainMaps maps, const ChainParams p) {
-  using L = MainLayout<D>;
+  using L = MainLayout<D, DS_OUT>;
+  constexpr int NSTAGE = L::NST;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -134,7 +140,7 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
     for (int i = 0; i < NUM_BARS; ++i) {
       const bool threads128 = (i == BAR_PREADY || i == BAR_PREADY + 1 || i == BAR_DSREADY ||
                                i == BAR_DSREADY + 1 || i == BAR_DQEMPTY || i == BAR_DQEMPTY + 1 ||
-                               i == BAR_STAGEREADY);
+                               i == BAR_STAGEREADY || i == BAR_DPREAD || i == BAR_DPREAD + 1);
       mbar_init(&bars[i], threads128 ? 128 : 1);
     }
     fence_mbar_init();
@@ -252,9 +258,9 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
           }
           __syncwarp();
           // The slot's dP^T columns are read by the compute warpgroup of tile t-2
-          // until it has formed dS (DS_READY), and on the dQ-reduction route
-          // then hold dQ^T of tile t-2 until the dQ warpgroup has read it out.
-          if (t >= 2 && !mbar_wait(&bars[BAR_DSREADY + s], (j - 1) & 1, abort_flag, WAIT_LIMIT_NS))
+          // until it has them in registers (DP_READ), and on the dQ-reduction
+          // route then hold dQ^T of tile t-2 until the dQ warpgroup has read it.
+          if (t >= 2 && !mbar_wait(&bars[BAR_DPREAD + s], (j - 1) & 1, abort_flag, WAIT_LIMIT_NS))
             break;
           if (!DS_OUT && t >= 2 &&
               !mbar_wait(&bars[BAR_DQEMPTY + s], (j - 1) & 1, abort_flag, WAIT_LIMIT_NS))
@@ -439,14 +445,23 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
           !mbar_wait(&bars[BAR_SFULL + slot], j & 1, abort_flag, WAIT_LIMIT_NS)) { ok = false; break; }
       __syncwarp();
       tc_fence_after();
+      {
+        uint32_t ra[32], rb[32];
+        tmem_ld32(t_lane + L::col_s(slot), ra);
+        tmem_ld32(t_lane + L::col_s(slot) + 32, rb);
+        const float4* lse4 = reinterpret_cast<const float4*>(qs);
+        tmem_ld_wait(ra);
+        tmem_ld_wait(rb);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t r[32];
-        tmem_ld32(t_lane + L::col_s(slot) + half * 32, r);
-        tmem_ld_wait(r);
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          P[half * 32 + i] = ex2_approx(fmaf(__uint_as_float(r[i]), scale_log2, -qs[half * 32 + i]));
+        for (int i4 = 0; i4 < BQ / 4; ++i4) {
+          const float4 l = lse4[i4];
+          const uint32_t* r = i4 < 8 ? ra : rb;
+          const int i = (i4 & 7) * 4;
+          P[i4 * 4 + 0] = ex2_approx(fmaf(__uint_as_float(r[i + 0]), scale_log2, -l.x));
+          P[i4 * 4 + 1] = ex2_approx(fmaf(__uint_as_float(r[i + 1]), scale_log2, -l.y));
+          P[i4 * 4 + 2] = ex2_approx(fmaf(__uint_as_float(r[i + 2]), scale_log2, -l.z));
+          P[i4 * 4 + 3] = ex2_approx(fmaf(__uint_as_float(r[i + 3]), scale_log2, -l.w));
+        }
       }
       if (need_mask) {
 #pragma unroll
@@ -475,23 +490,30 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
           !mbar_wait(&bars[BAR_DSCOPIED + slot], (j - 1) & 1, abort_flag, WAIT_LIMIT_NS)) { ok = false; break; }
       __syncwarp();
       tc_fence_after();
+      {
+        uint32_t ra[32], rb[32];
+        tmem_ld32(t_lane + L::col_dp(slot), ra);
+        tmem_ld32(t_lane + L::col_dp(slot) + 32, rb);
+        tmem_ld_wait(ra);
+        tmem_ld_wait(rb);
+        tc_fence_before();
+        mbar_arrive(&bars[BAR_DPREAD + slot]);  // the dP^T columns may be overwritten
+        const float4* delta4 = reinterpret_cast<const float4*>(qs + BQ);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t r[32];
-        tmem_ld32(t_lane + L::col_dp(slot) + half * 32, r);
-        tmem_ld_wait(r);
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          uint32_t w[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int c = half * 32 + ch * 8 + 2 * i;
-            const float d0 = P[c] * (__uint_as_float(r[ch * 8 + 2 * i]) - qs[BQ + c]);
-            const float d1 = P[c + 1] * (__uint_as_float(r[ch * 8 + 2 * i + 1]) - qs[BQ + c + 1]);
-            w[i] = pack_bf16x2(d0, d1);
-          }
-          const int chunk = half * 4 + ch;
-          *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int chunk = 0; chunk < 8; ++chunk) {  // 8 queries = 16 bytes of dS^T per chunk
+          const uint32_t* r = chunk < 4 ? ra : rb;
+          const int i = (chunk & 3) * 8;
+          const float4 d0 = delta4[chunk * 2], d1 = delta4[chunk * 2 + 1];
+          const int c = chunk * 8;
+          const uint32_t w0 = pack_bf16x2(P[c + 0] * (__uint_as_float(r[i + 0]) - d0.x),
+                                          P[c + 1] * (__uint_as_float(r[i + 1]) - d0.y));
+          const uint32_t w1 = pack_bf16x2(P[c + 2] * (__uint_as_float(r[i + 2]) - d0.z),
+                                          P[c + 3] * (__uint_as_float(r[i + 3]) - d0.w));
+          const uint32_t w2 = pack_bf16x2(P[c + 4] * (__uint_as_float(r[i + 4]) - d1.x),
+                                          P[c + 5] * (__uint_as_float(r[i + 5]) - d1.y));
+          const uint32_t w3 = pack_bf16x2(P[c + 6] * (__uint_as_float(r[i + 6]) - d1.z),
+                                          P[c + 7] * (__uint_as_float(r[i + 7]) - d1.w));
+          *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (row & 7)) << 4)) = make_uint4(w0, w1, w2, w3);
         }
       }
       fence_proxy_async_smem();
@@ -561,7 +583,7 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
 template <int D, bool DS_OUT>
 static cudaError_t set_main_smem() {
   return cudaFuncSetAttribute(sdpa_bwd_main<D, DS_OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              MainLayout<D>::BYTES);
+                              MainLayout<D, DS_OUT>::BYTES);
 }
 
 cudaError_t main_kernel_setup() {
@@ -576,10 +598,13 @@ cudaError_t launch_main(const MainMaps& maps, const ChainParams& p, cudaStream_t
   const dim3 grid((unsigned)(p.n_kt * p.B * p.Hq));
   const dim3 block(MAIN_THREADS);
   if (p.Dqk == 64)
-    return launch_kernel(sdpa_bwd_main<64, false>, grid, block, MainLayout<64>::BYTES, s, true, maps, p);
+    return launch_kernel(sdpa_bwd_main<64, false>, grid, block, MainLayout<64, false>::BYTES, s, true,
+                         maps, p);
   if (p.ds_route)
-    return launch_kernel(sdpa_bwd_main<128, true>, grid, block, MainLayout<128>::BYTES, s, true, maps, p);
-  return launch_kernel(sdpa_bwd_main<128, false>, grid, block, MainLayout<128>::BYTES, s, true, maps, p);
+    return launch_kernel(sdpa_bwd_main<128, true>, grid, block, MainLayout<128, true>::BYTES, s, true,
+                         maps, p);
+  return launch_kernel(sdpa_bwd_main<128, false>, grid, block, MainLayout<128, false>::BYTES, s, true,
+                       maps, p);
 }
 
 }  // namespace sdpa
