@@ -17,7 +17,7 @@
 // dK at [192+D_v, 192+D_v+D_qk): 2*96 + 128 + 192 = 512 for MLA.
 //
 // Warps: 0-3 even tiles (slot 0), 4-7 odd tiles (slot 1), 8 TMA producer,
-// 9 G1/G2 issuer and tensor-memory owner, 10 G3/G4 issuer, 11 idle.
+// 9 G1 issuer and tensor-memory owner, 10 G3/G4 issuer, 11 G2 issuer.
 // Shared memory: K [D_qk/64][128][128 B], V [D_v/64][128][128 B], Q and dO
 // stage rings ([D/64][64][128 B]), dS^T x2 [128 keys][64 q], row statistics.
 #include <cuda.h>
@@ -173,19 +173,20 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
                   QSTAT_FLOATS * 4, full);
       }
     }
-  } else if (warp == 9 || warp == 10) {
+  } else if (warp >= 9) {
     // ------------------------------------------------------------ MMA issuers
+    // A tcgen05.mma costs its issuing thread about 120 cycles, more than these
+    // MMAs take on the tensor core, so three warps issue: 9 G1, 11 G2, 10 G3/G4.
     pdl_wait_prior_grid();
     const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
     bool ok = n > 0 && mbar_wait(&bars[BAR_KV], 0, abort_flag, WAIT_LIMIT_NS);
     if (warp == 9) {
-      // G1 of tile t+1 is issued before G2 of tile t waits for the softmax of t.
-      auto issue_g1 = [&](int t) -> bool {
+      for (int t = 0; t < n && ok; ++t) {
         const int s = t & 1, st = t % NST, j = t >> 1;
-        if (!mbar_wait(&bars[BAR_QFULL + st], (t / NST) & 1, abort_flag, WAIT_LIMIT_NS)) return false;
+        if (!mbar_wait(&bars[BAR_QFULL + st], (t / NST) & 1, abort_flag, WAIT_LIMIT_NS)) break;
         // Slot columns [0,64) hold dP^T of tile t-2 until its dS has been formed.
         if (t >= 2 && !mbar_wait(&bars[BAR_DSREADY + s], (j - 1) & 1, abort_flag, WAIT_LIMIT_NS))
-          return false;
+          break;
         __syncwarp();
         tc_fence_after();
         if (elect_one()) {
@@ -200,12 +201,11 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
           mma_commit(&bars[BAR_SFULL + s]);
         }
         __syncwarp();
-        return true;
-      };
-      if (ok) ok = issue_g1(0);
+      }
+    } else if (warp == 11) {
       for (int t = 0; t < n && ok; ++t) {
-        if (t + 1 < n && !issue_g1(t + 1)) break;
         const int s = t & 1, st = t % NST, j = t >> 1;
+        if (!mbar_wait(&bars[BAR_QFULL + st], (t / NST) & 1, abort_flag, WAIT_LIMIT_NS)) break;
         // dP^T overwrites S^T once the warpgroup has read it (P_READY).
         if (!mbar_wait(&bars[BAR_PREADY + s], j & 1, abort_flag, WAIT_LIMIT_NS)) break;
         __syncwarp();
