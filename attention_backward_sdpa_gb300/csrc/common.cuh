@@ -137,4 +137,19 @@ __device__ inline void batch_lengths(const ChainParams& p, int b, int& Lq, int& 
   Lk = p.seq_kv_lens ? min(max(p.seq_kv_lens[b], 0), p.Skv) : p.Skv;
 }
 
+// Zero rows [k0, min(k0 + BN, S_kv)) of dK and dV (or of the query head's GQA
+// partials) for a key tile that no query sees: such keys have exactly zero
+// gradient, and the outputs are overwritten in full. Called by every thread of
+// a CTA; 16-byte stores, consecutive threads on consecutive addresses.
+template <int DQK, int DV>
+__device__ inline void zero_key_tile_rows(const ChainParams& p, int b, int bh, int hk, int k0) {
+  const long long head = p.dk_ws ? (long long)bh : (long long)b * p.Hkv + hk;
+  const int rows = min(BN, p.Skv - k0);
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  uint4* dk = reinterpret_cast<uint4*>((p.dk_ws ? p.dk_ws : p.dk) + (head * p.Skv + k0) * DQK);
+  uint4* dv = reinterpret_cast<uint4*>((p.dv_ws ? p.dv_ws : p.dv) + (head * p.Skv + k0) * DV);
+  for (int i = threadIdx.x; i < rows * (DQK / 8); i += blockDim.x) dk[i] = z;
+  for (int i = threadIdx.x; i < rows * (DV / 8); i += blockDim.x) dv[i] = z;
+}
+
 }  // namespace sdpa

@@ -2,8 +2,9 @@
 //
 //   preprocess  delta = rowsum(dO * O) in fp32 and the replay statistic
 //               LSE * log2(e) (+inf for masked rows and LSE = -inf), staged
-//               per query tile; clears the fp32 dQ accumulator and the
-//               deterministic-mode counters. ("The kernel chain": dot.)
+//               per query tile; clears the fp32 dQ accumulator (rows below
+//               the query length) and the deterministic-mode counters.
+//               ("The kernel chain": dot.)
 //   dq_convert  dQ = bf16(scale * dq_accum), dropping the accumulator's
 //               padding rows. ("The kernel chain": cvt.)
 // The dQ convert also carries the GQA group reduction of dK/dV (gqa.cuh).
@@ -85,18 +86,22 @@ __global__ void __launch_bounds__(256) sdpa_bwd_preprocess(const ChainParams p) 
         qs[BQ + qi] = delta;
       }
     }
+    // dQ-reduction route: clear this tile's accumulator rows below Lq (the
+    // convert kernel writes zeros for rows at or past Lq without reading them).
+    if (p.dq_accum) {
+      const int rows = min(BQ, Lq - qt * BQ);
+      if (rows > 0) {
+        float4* acc = reinterpret_cast<float4*>(p.dq_accum + ((long long)bh * p.n_qt + qt) * BQ * p.Dqk);
+        const int n4 = rows * p.Dqk / 4;
+        for (int i = threadIdx.x; i < n4; i += blockDim.x) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
   }
 
-  // Clear the dQ accumulator (dQ-reduction route), the stand-in zero dS tile
-  // (two-kernel route), and the counters (+ ticket).
+  // Clear the stand-in zero dS tile (two-kernel route) and the counters (+ ticket).
   const long long nthreads = (long long)gridDim.x * blockDim.x;
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (p.dq_accum) {
-    float4* acc = reinterpret_cast<float4*>(p.dq_accum);
-    const long long n4 = (long long)p.B * p.Hq * p.n_qt * BQ * p.Dqk / 4;
-    for (long long i = tid; i < n4; i += nthreads) acc[i] = z;
-  }
   if (p.zero_tile) {
     float4* zt = reinterpret_cast<float4*>(p.zero_tile);
     for (long long i = tid; i < DS_TILE_BYTES / 16; i += nthreads) zt[i] = z;
@@ -125,6 +130,11 @@ __global__ void __launch_bounds__(256) sdpa_bwd_dq_convert(const ChainParams p) 
       if (i >= total) continue;
       const unsigned r = i / PER_ROW, c8 = i - r * PER_ROW;  // r = (b*Hq + h)*Sq + q
       const unsigned bh = r / (unsigned)p.Sq, q = r - bh * (unsigned)p.Sq;
+      // Rows at or past the batch row's query length are zero (and were not cleared).
+      if (p.seq_q_lens && (int)q >= min(max(__ldg(p.seq_q_lens + bh / (unsigned)p.Hq), 0), p.Sq)) {
+        a[u] = c[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        continue;
+      }
       const float* src = p.dq_accum + ((long long)bh * rows_pad + q) * DQK + c8 * 8;
       a[u] = *reinterpret_cast<const float4*>(src);
       c[u] = *reinterpret_cast<const float4*>(src + 4);

@@ -123,6 +123,20 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
     if (tid == 0) set_status(p.status, STATUS_SMEM_ALIGN);
     return;
   }
+  if (!p.deterministic) {
+    // A key tile that no query sees only has zero gradients: write them and
+    // leave before any barrier or tensor-memory setup.
+    const int BH0 = p.B * p.Hq;
+    const int kt0 = blockIdx.x / BH0, bh0 = blockIdx.x % BH0, b0 = bh0 / p.Hq;
+    int Lq0, Lk0, lo0, hi0;
+    batch_lengths(p, b0, Lq0, Lk0);
+    visited_query_tiles(kt0, Lq0, Lk0, p.causal, p.bottom_right, p.window_left, p.window_right, lo0,
+                        hi0);
+    if (hi0 < lo0) {
+      zero_key_tile_rows<D, D>(p, b0, bh0, (bh0 % p.Hq) / p.G, kt0 * BN);
+      return;
+    }
+  }
   uint8_t* sK = smem + L::OFF_K;
   uint8_t* sV = smem + L::OFF_V;
   uint8_t* sQ = smem + L::OFF_Q;

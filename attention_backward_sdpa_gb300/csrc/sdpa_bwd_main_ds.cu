@@ -102,6 +102,20 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
 
+  {
+    // A key tile that no query sees only has zero gradients: write them and
+    // leave before any barrier or tensor-memory setup.
+    const int BH0 = p.B * p.Hq;
+    const int kt0 = blockIdx.x / BH0, bh0 = blockIdx.x % BH0, b0 = bh0 / p.Hq;
+    int Lq0, Lk0, lo0, hi0;
+    batch_lengths(p, b0, Lq0, Lk0);
+    visited_query_tiles(kt0, Lq0, Lk0, p.causal, p.bottom_right, p.window_left, p.window_right, lo0,
+                        hi0);
+    if (hi0 < lo0) {
+      zero_key_tile_rows<DQK, DV>(p, b0, bh0, (bh0 % p.Hq) / p.G, kt0 * BN);
+      return;
+    }
+  }
   if (tid == 0) {
     *abort_flag = 0;
     for (int i = 0; i < NUM_BARS; ++i) {

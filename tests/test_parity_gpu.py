@@ -58,6 +58,16 @@ SMALL = {
     "gqa_det": W("gqa_det", 1, 4, 2, 520, 520, 128, 128, causal=True, deterministic=True, seed=24),
     "window_det": W("window_det", 2, 2, 1, 600, 600, 128, 128, causal=True, window_left=200,
                     deterministic=True, seed=25),
+    # deterministic D=128: the 128-row-tile main kernel (odd 64-row tile counts
+    # exercise its half-filled last tile)
+    "det_padded_odd": W("det_padded_odd", 2, 2, 2, 300, 300, 128, 128, causal=True,
+                        padded=(30, 300), deterministic=True, seed=32),
+    "det_br_long_kv": W("det_br_long_kv", 1, 2, 2, 200, 333, 128, 128, causal=True,
+                        bottom_right=True, deterministic=True, seed=33),
+    "det_dense_ragged": W("det_dense_ragged", 2, 2, 1, 130, 250, 128, 128, deterministic=True,
+                          seed=34),
+    "det_window_only": W("det_window_only", 1, 2, 2, 300, 280, 128, 128, window_left=150,
+                         bottom_right=True, deterministic=True, seed=35),
     "mla_br_causal_ragged": W("mla_br_causal_ragged", 1, 2, 2, 300, 333, 192, 128, causal=True,
                               bottom_right=True, seed=28),
     "mla_dense": W("mla_dense", 2, 2, 2, 190, 250, 192, 128, seed=29),
