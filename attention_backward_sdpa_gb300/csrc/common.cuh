@@ -88,9 +88,11 @@ __host__ __device__ inline void visited_query_tiles(int kt, int Lq, int Lk, int 
   qt_hi = (int)(q_max / BQ);
 }
 
-// TMA tensor maps of the main kernel (K and V with H_kv heads, Q and dO with H_q).
+// TMA tensor maps of the main kernels: inputs K and V with H_kv heads, Q and dO
+// with H_q; outputs dK and dV (H_kv heads, or the per-query-head partials of
+// the GQA workspace), written in 128-row boxes.
 struct MainMaps {
-  CUtensorMap q, k, v, d_o;
+  CUtensorMap q, k, v, d_o, dk_out, dv_out;
 };
 
 // Host launchers, one per kernel, defined beside their kernels. `pdl` launches

@@ -1,7 +1,7 @@
 // sdpa_bwd_api.cu -- host side of libsdpa_bwd.so: the C ABI declared in
 // include/sdpa_bwd.h.
 //
-// One call validates its arguments, carves the workspace, encodes the four TMA
+// One call validates its arguments, carves the workspace, encodes the six TMA
 // tensor maps and enqueues the kernel chain on the caller's stream
 // (cuDNN frontend docs, "SDPA Backward (SM120)", section "The kernel chain"):
 //   preprocess -> main -> dq (convert, or dS x K on the two-kernel route)
@@ -322,7 +322,11 @@ int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const v
   if (!make_bhsd_map(&maps.q, q, D_qk, S_q, BHq, BQ) ||
       !make_bhsd_map(&maps.k, k, D_qk, S_kv, BHkv, BN) ||
       !make_bhsd_map(&maps.v, v, D_v, S_kv, BHkv, BN) ||
-      !make_bhsd_map(&maps.d_o, d_o, D_v, S_q, BHq, BQ)) {
+      !make_bhsd_map(&maps.d_o, d_o, D_v, S_q, BHq, BQ) ||
+      !make_bhsd_map(&maps.dk_out, p.dk_ws ? static_cast<void*>(p.dk_ws) : dk, D_qk, S_kv,
+                     p.dk_ws ? BHq : BHkv, BN) ||
+      !make_bhsd_map(&maps.dv_out, p.dv_ws ? static_cast<void*>(p.dv_ws) : dv, D_v, S_kv,
+                     p.dv_ws ? BHq : BHkv, BN)) {
     if (own_ws) cudaFreeAsync(workspace, stream);
     return SDPA_ERR_CUDA;
   }

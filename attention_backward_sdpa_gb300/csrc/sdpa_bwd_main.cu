@@ -544,23 +544,23 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
         mbar_arrive(&bars[BAR_DSCOPIED + slot]);
       }
     }
-    if (DS_OUT && row == 0) bulk_wait_group0();  // stores complete before the kernel ends
+    if (DS_OUT && row == 0) bulk_wait_group_read0();  // the dS^T buffers have been read
 
-    // ---- epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK, one key
-    // row per thread. Every lane runs the (warp-collective) tensor-memory loads;
-    // only the stores are predicated on the row being inside the tensor.
+    // ---- epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK. Each
+    // thread converts its key row into the warpgroup's half of the (now idle)
+    // Q/dO stage ring, in the 128-byte-swizzled box layout, and one thread per
+    // warpgroup writes the rows with TMA stores, which drop rows past S_kv.
+    // Every lane runs the (warp-collective) tensor-memory loads.
     if (n > 0 && ok) {
       ok = mbar_wait(&bars[BAR_MMADONE], 0, abort_flag, WAIT_LIMIT_NS);
       __syncwarp();
       tc_fence_after();
     }
     const bool warp_ok = __all_sync(0xffffffffu, ok);
-    const bool store_row = k < p.Skv;
     const uint32_t col0 = slot ? L::COL_DK : L::COL_DV;
     const float mult = slot ? p.scale : 1.f;
-    __nv_bfloat16* base = slot ? (p.dk_ws ? p.dk_ws : p.dk) : (p.dv_ws ? p.dv_ws : p.dv);
-    const long long head = p.dk_ws ? (long long)bh : (long long)b * p.Hkv + hk;
-    __nv_bfloat16* out = base + (head * p.Skv + k) * (long long)D;
+    uint8_t* stg = slot ? sDO : sQ;
+    static_assert(L::NST * L::TILE_Q >= D / 64 * L::BLK_KV, "staging fits in a stage ring");
 #pragma unroll
     for (int c32 = 0; c32 < D / 32; ++c32) {
       uint32_t r[32];
@@ -571,17 +571,26 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) r[i] = 0u;
       }
-      if (store_row) {
+      uint8_t* dst_row = stg + (c32 >> 1) * L::BLK_KV + row * 128;
 #pragma unroll
-        for (int v8 = 0; v8 < 4; ++v8) {
-          uint4 o;
-          o.x = pack_bf16x2(__uint_as_float(r[v8 * 8 + 0]) * mult, __uint_as_float(r[v8 * 8 + 1]) * mult);
-          o.y = pack_bf16x2(__uint_as_float(r[v8 * 8 + 2]) * mult, __uint_as_float(r[v8 * 8 + 3]) * mult);
-          o.z = pack_bf16x2(__uint_as_float(r[v8 * 8 + 4]) * mult, __uint_as_float(r[v8 * 8 + 5]) * mult);
-          o.w = pack_bf16x2(__uint_as_float(r[v8 * 8 + 6]) * mult, __uint_as_float(r[v8 * 8 + 7]) * mult);
-          *reinterpret_cast<uint4*>(out + c32 * 32 + v8 * 8) = o;
-        }
+      for (int v8 = 0; v8 < 4; ++v8) {
+        uint4 o;
+        o.x = pack_bf16x2(__uint_as_float(r[v8 * 8 + 0]) * mult, __uint_as_float(r[v8 * 8 + 1]) * mult);
+        o.y = pack_bf16x2(__uint_as_float(r[v8 * 8 + 2]) * mult, __uint_as_float(r[v8 * 8 + 3]) * mult);
+        o.z = pack_bf16x2(__uint_as_float(r[v8 * 8 + 4]) * mult, __uint_as_float(r[v8 * 8 + 5]) * mult);
+        o.w = pack_bf16x2(__uint_as_float(r[v8 * 8 + 6]) * mult, __uint_as_float(r[v8 * 8 + 7]) * mult);
+        const int piece = (c32 & 1) * 4 + v8;
+        *reinterpret_cast<uint4*>(dst_row + ((piece ^ (row & 7)) << 4)) = o;
       }
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(1 + slot, 128);
+    if (row == 0) {
+      const long long head = p.dk_ws ? (long long)bh : (long long)b * p.Hkv + hk;
+      const CUtensorMap* map = slot ? &maps.dk_out : &maps.dv_out;
+      for (int blk = 0; blk < D / 64; ++blk) tma_store_3d(map, stg + blk * L::BLK_KV, blk * 64, k0, (int)head);
+      bulk_commit_group();
+      bulk_wait_group_read0();  // the CTA may exit once the copies have read shared memory
     }
   }
 
