@@ -25,8 +25,9 @@
 // (in deterministic mode after waiting its turn on the query tile's counter).
 //
 // Warps: 0-3 slot-0 compute, 4-7 slot-1 compute, 8-11 dQ, 12 TMA producer,
-// 13 score-GEMM issuer and tensor-memory owner, 14 gradient-GEMM issuer, 15 idle
-// (it completes the fourth warpgroup so that register budgets can be moved
+// 13 score-GEMM issuer and tensor-memory owner, 14 gradient-GEMM issuer, 15 the
+// dS^T store on the two-kernel route, otherwise idle (it completes the fourth
+// warpgroup so that register budgets can be moved
 // between warpgroups: launched with 128 registers per thread, the compute
 // warpgroups grow to 160 while the dQ and control warpgroups shrink to 96;
 // 128 threads x (160 + 160 + 96 + 96) = 65536 = 512 threads x 128).
@@ -340,7 +341,25 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
         if (n > 0 && elect_one()) mma_commit(&bars[BAR_MMADONE]);
         __syncwarp();
       }
-    }  // warp 15: idle member of the control warpgroup
+    } else if (DS_OUT && warp == 15) {
+      // ------------------------------------------------------------ dS^T store
+      // Two-kernel route: once a tile's dS^T is in shared memory, one thread
+      // stores it to the workspace (the dQ kernel's input) and releases the
+      // buffer when the copy has read it, so no compute warp waits on the copy.
+      if (lane == 0) {
+        for (int t = 0; t < n; ++t) {
+          const int s = t & 1, j = t >> 1;
+          if (!mbar_wait(&bars[BAR_DSREADY + s], j & 1, abort_flag, WAIT_LIMIT_NS)) break;
+          const int qt = qt_hi - t;
+          uint8_t* dst = p.ds_ws + (((long long)bh * p.n_kt + kt) * p.n_qt + qt) * (long long)DS_TILE_BYTES;
+          bulk_store(dst, sDS + s * L::TILE_DS, DS_TILE_BYTES);
+          bulk_commit_group();
+          bulk_wait_group_read0();
+          mbar_arrive(&bars[BAR_DSCOPIED + s]);
+        }
+        bulk_wait_group_read0();
+      }
+    }  // otherwise warp 15: idle member of the control warpgroup
   } else if (warp >= 8) {
     // ------------------------------------------------------------ dQ warpgroup
     regs_decrease<REGS_DQ>();
@@ -533,18 +552,7 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bars[BAR_DSREADY + slot]);
-      if (DS_OUT && row == 0) {
-        // Once the whole warpgroup has written the tile, one thread stores it.
-        if (mbar_wait(&bars[BAR_DSREADY + slot], j & 1, abort_flag, WAIT_LIMIT_NS)) {
-          uint8_t* dst = p.ds_ws + (((long long)bh * p.n_kt + kt) * p.n_qt + qt) * (long long)DS_TILE_BYTES;
-          bulk_store(dst, sDS + slot * L::TILE_DS, DS_TILE_BYTES);
-          bulk_commit_group();
-          bulk_wait_group_read0();
-        }
-        mbar_arrive(&bars[BAR_DSCOPIED + slot]);
-      }
     }
-    if (DS_OUT && row == 0) bulk_wait_group_read0();  // the dS^T buffers have been read
 
     // ---- epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK. Each
     // thread converts its key row into the warpgroup's half of the (now idle)
