@@ -17,7 +17,8 @@
 // dK at [192+D_v, 192+D_v+D_qk): 2*96 + 128 + 192 = 512 for MLA.
 //
 // Warps: 0-3 even tiles (slot 0), 4-7 odd tiles (slot 1), 8 TMA producer,
-// 9 G1 issuer and tensor-memory owner, 10 G3/G4 issuer, 11 G2 issuer.
+// 9 G1 issuer and tensor-memory owner, 10 G3/G4 issuer, 11 G2 issuer, 12 dS^T store,
+// 13-15 idle (they complete the fourth warpgroup for the register split).
 // Shared memory: K [D_qk/64][128][128 B], V [D_v/64][128][128 B], Q and dO
 // stage rings ([D/64][64][128 B]), dS^T x2 [128 keys][64 q], row statistics.
 #include <cuda.h>
@@ -30,7 +31,12 @@ namespace sdpa {
 
 namespace ds_kernel {
 
-constexpr int THREADS = 384;
+constexpr int THREADS = 512;
+// Register budgets move between warpgroups: launched with 128 registers per
+// thread, the compute warpgroups grow to 160 while the other two shrink to 96;
+// 128 threads x (160 + 160 + 96 + 96) = 65536 = 512 threads x 128.
+constexpr uint32_t REGS_COMPUTE = 160, REGS_OTHER = 96;
+static_assert(128 * (2 * REGS_COMPUTE + 2 * REGS_OTHER) <= THREADS * 128, "register split");
 constexpr uint64_t WAIT_LIMIT_NS = 4000000000ull;
 
 enum : int {
@@ -162,6 +168,8 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
   constexpr uint64_t T_KMAJ = sdesc_sw128_template(16, 1024);
   constexpr uint64_t T_MN_Q = sdesc_sw128_template(L::BLK_Q, 1024);
 
+  if (warp >= 8) {
+  regs_decrease<ds_kernel::REGS_OTHER>();
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && n > 0) {
@@ -187,7 +195,7 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
                   QSTAT_FLOATS * 4, full);
       }
     }
-  } else if (warp >= 9) {
+  } else if (warp >= 9 && warp <= 11) {
     // ------------------------------------------------------------ MMA issuers
     // A tcgen05.mma costs its issuing thread about 120 cycles, more than these
     // MMAs take on the tensor core, so three warps issue: 9 G1, 11 G2, 10 G3/G4.
@@ -272,7 +280,27 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
       if (n > 0 && elect_one()) mma_commit(&bars[BAR_MMADONE]);
       __syncwarp();
     }
-  } else if (warp < 8) {
+  } else if (warp == 12) {
+    // ------------------------------------------------------------ dS^T store
+    // Once a tile's dS^T is in shared memory, one thread stores it to the
+    // workspace and releases the buffer when the copy has read it, so no
+    // compute warp waits on the copy.
+    if (lane == 0) {
+      for (int t = 0; t < n; ++t) {
+        const int s = t & 1, j = t >> 1;
+        if (!mbar_wait(&bars[BAR_DSREADY + s], j & 1, abort_flag, WAIT_LIMIT_NS)) break;
+        const int qt = qt_hi - t;
+        uint8_t* dst = p.ds_ws + (((long long)bh * p.n_kt + kt) * p.n_qt + qt) * (long long)DS_TILE_BYTES;
+        bulk_store(dst, sDS + s * L::TILE_DS, DS_TILE_BYTES);
+        bulk_commit_group();
+        bulk_wait_group_read0();
+        mbar_arrive(&bars[BAR_DSCOPIED + s]);
+      }
+      bulk_wait_group_read0();
+    }
+  }  // warps 13-15: idle members of the fourth warpgroup
+  } else {
+    regs_increase<ds_kernel::REGS_COMPUTE>();
     // ------------------------------------------------------------ compute warpgroups
     pdl_wait_prior_grid();
     const int slot = warp >> 2;
@@ -361,17 +389,7 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bars[BAR_DSREADY + slot]);  // dP^T read, dS^T in shared memory
-      if (row == 0) {
-        if (mbar_wait(&bars[BAR_DSREADY + slot], j & 1, abort_flag, WAIT_LIMIT_NS)) {
-          uint8_t* dst = p.ds_ws + (((long long)bh * p.n_kt + kt) * p.n_qt + qt) * (long long)DS_TILE_BYTES;
-          bulk_store(dst, sDS + slot * L::TILE_DS, DS_TILE_BYTES);
-          bulk_commit_group();
-          bulk_wait_group_read0();
-        }
-        mbar_arrive(&bars[BAR_DSCOPIED + slot]);
-      }
     }
-    if (row == 0) bulk_wait_group_read0();  // the dS^T buffers have been read
 
     // ---- epilogue: warpgroup 0 writes dV (D_v columns), warpgroup 1 scale * dK
     // (D_qk). Each thread converts its key row into the (now idle) dO or Q stage
