@@ -35,16 +35,21 @@ struct DqLayout {
   static constexpr int TILE_DS = 2 * DS_TILE_BYTES;     // two dS^T tiles: [2][128 keys][64 q]
   static constexpr int STAGE = TILE_K + TILE_DS;
   static constexpr int OFF_BAR = NSTAGE * STAGE;
-  static constexpr int NUM_BARS = 2 * NSTAGE + 4;       // full/empty per stage, acc full/empty x2
-  static constexpr int BYTES = OFF_BAR + NUM_BARS * 8 + 64;
+  // full/empty per stage, acc full/empty x2, unit ring full/empty x URING
+  static constexpr int URING = 4;
+  static constexpr int NUM_BARS = 2 * NSTAGE + 4 + 2 * URING;
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;  // tmem base, abort flag, unit ring
+  static constexpr int BYTES = OFF_MISC + 64;
   static constexpr uint32_t ACC_COLS = D <= 128 ? 128 : 256;   // one accumulator, padded
   static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;          // double-buffered
   static_assert(BYTES <= 232448, "shared memory budget");
   static_assert(TMEM_COLS <= 512, "tensor memory budget");
 };
 
-// Work unit u (128 query rows of one (batch, query head)): query-tile pair
-// major, so concurrently running CTAs of a wave share key tiles of a head.
+// Work unit u (128 query rows of one (batch, query head)), in claiming order:
+// query-tile pair descending, so that under a causal mask (where later query
+// rows see more key tiles) the longest units are claimed first, and heads of
+// the same pair next to each other.
 struct DqUnit {
   int bh, qp, b, hk, qt0, qt1, Lq, Lk, kv_first, n;
 };
@@ -52,21 +57,31 @@ struct DqUnit {
 __device__ __forceinline__ DqUnit dq_unit(const ChainParams& p, int u) {
   DqUnit w;
   const int n_qp = ceil_div(p.n_qt, 2);
-  w.qp = u % n_qp;
-  w.bh = u / n_qp;
+  const int BH = p.B * p.Hq;
+  w.qp = n_qp - 1 - u / BH;
+  w.bh = u % BH;
   w.b = w.bh / p.Hq;
   w.hk = (w.bh % p.Hq) / p.G;
   w.qt0 = 2 * w.qp;
   w.qt1 = 2 * w.qp + 1;  // may be past the last tile
   batch_lengths(p, w.b, w.Lq, w.Lk);
   // Key tiles visited for either query tile, ascending: a contiguous range.
+  // The walk starts at a lower bound (no key tile below it can see query row
+  // 64*qt0 under a sliding window) and stops just past the range.
   int first = p.n_kt, last = -1;
-  for (int kt = 0; kt < p.n_kt; ++kt) {
+  int kt_start = 0;
+  if (p.window_left >= 0) {
+    const int diag = p.bottom_right ? w.Lk - w.Lq : 0;
+    kt_start = (int)max(0ll, floor_div((long long)w.qt0 * BQ + diag - p.window_left, BN) - 1);
+  }
+  for (int kt = kt_start; kt < p.n_kt; ++kt) {
     int lo, hi;
     visited_query_tiles(kt, w.Lq, w.Lk, p.causal, p.bottom_right, p.window_left, p.window_right, lo, hi);
     if ((lo <= w.qt0 && w.qt0 <= hi) || (w.qt1 < p.n_qt && lo <= w.qt1 && w.qt1 <= hi)) {
       first = min(first, kt);
       last = kt;
+    } else if (last >= 0) {
+      break;
     }
   }
   w.kv_first = first;
@@ -74,10 +89,12 @@ __device__ __forceinline__ DqUnit dq_unit(const ChainParams& p, int u) {
   return w;
 }
 
-// Persistent: each CTA walks units blockIdx.x, blockIdx.x + gridDim.x, ...
-// The load warp runs ahead across unit boundaries through one stage ring; the
-// MMA warp alternates between two tensor-memory accumulators (counted over
-// non-empty units only) so that the epilogue of one unit overlaps the next.
+// Persistent: one CTA per SM. The load warp claims units from a global ticket
+// (longest first, so the CTAs finish together) and publishes each to the MMA
+// warp and the epilogue through a small ring in shared memory; it runs ahead
+// across unit boundaries through one stage ring. The MMA warp alternates
+// between two tensor-memory accumulators (counted over non-empty units only)
+// so that the epilogue of one unit overlaps the next.
 template <int D>
 __global__ void __launch_bounds__(DQ_THREADS, 1)
     sdpa_bwd_dq_from_ds(const __grid_constant__ CUtensorMap k_map, const ChainParams p) {
@@ -92,9 +109,21 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   uint64_t* empty = full + L::NSTAGE;
   uint64_t* acc_full = empty + L::NSTAGE;   // [2]
   uint64_t* acc_empty = acc_full + 2;       // [2], 128 arrivals
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint64_t* ufull = acc_empty + 2;          // [URING]
+  uint64_t* uempty = ufull + L::URING;      // [URING], 5 arrivals (MMA warp + 4 epilogue warps)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+  volatile int* ring = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 16);
   const int n_units = ceil_div(p.n_qt, 2) * p.B * p.Hq;
+  // Reads ring entry i (a unit, or -1 at the end) and releases it; all lanes of a warp.
+  auto ring_get = [&](int i, int& unit) -> bool {
+    const int r = i % L::URING;
+    if (!mbar_wait(&ufull[r], (i / L::URING) & 1, abort_flag, DQ_WAIT_LIMIT_NS)) return false;
+    unit = ring[r];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&uempty[r]);
+    return true;
+  };
 
   if (tid == 0) {
     *abort_flag = 0;
@@ -106,6 +135,10 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     mbar_init(&acc_full[1], 1);
     mbar_init(&acc_empty[0], 128);
     mbar_init(&acc_empty[1], 128);
+    for (int i = 0; i < L::URING; ++i) {
+      mbar_init(&ufull[i], 1);
+      mbar_init(&uempty[i], 5);
+    }
     fence_mbar_init();
   }
   if (warp == 5) {
@@ -123,7 +156,17 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     if (lane == 0) {
       prefetch_tmap(&k_map);
       int step = 0;
-      for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+      for (int e = 0;; ++e) {
+        // The ticket was cleared by the preprocess kernel; on this route the
+        // main kernel does not use it.
+        const int u = atomicAdd(p.ticket, 1);
+        const int r = e % L::URING;
+        if (e >= L::URING &&
+            !mbar_wait(&uempty[r], ((e / L::URING) - 1) & 1, abort_flag, DQ_WAIT_LIMIT_NS))
+          goto loads_done;
+        ring[r] = u < n_units ? u : -1;
+        mbar_arrive(&ufull[r]);
+        if (u >= n_units) break;
         const DqUnit w = dq_unit(p, u);
         for (int i = 0; i < w.n; ++i, ++step) {
           const int st = step % L::NSTAGE;
@@ -155,7 +198,9 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     constexpr uint64_t T_MN = sdesc_sw128_template(BN * 128, 1024);  // 16 KB block stride
     bool ok = true;
     int step = 0, done_units = 0;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+    for (int e = 0; ok; ++e) {
+      int u;
+      if (!ring_get(e, u) || u < 0) break;
       const DqUnit w = dq_unit(p, u);
       if (w.n <= 0) continue;
       const int buf = done_units & 1;
@@ -196,19 +241,27 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     // dQ of each unit as its accumulator completes. This CTA's slice of the GQA
     // group sums (dK/dV, which depend only on the main kernel) is split into one
     // piece per unit, each reduced while that unit's MMAs run.
-    const int my_units = (n_units - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+    // The GQA slice is cut into as many pieces as the CTA's fair share of units;
+    // pieces left over when the CTA runs out of units are reduced at the end.
+    const int n_pieces = (n_units + (int)gridDim.x - 1) / (int)gridDim.x;
     int unit_idx = 0;
     const int row = warp * 32 + lane;          // query within the 128-row unit
     const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
     int done_units = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+    for (int e = 0;; ++e) {
+      int u;
+      if (!ring_get(e, u)) {
+        ok = false;
+        break;
+      }
+      if (u < 0) break;
       const DqUnit w = dq_unit(p, u);
       const int q = w.qt0 * BQ + row;
       __nv_bfloat16* out = p.dq + ((long long)w.bh * p.Sq + q) * D;
       const bool have = w.n > 0;
       const int buf = done_units & 1;
-      gqa_reduce_slice<D, 128>(p, blockIdx.x, gridDim.x, tid, 128, unit_idx++, my_units);
+      gqa_reduce_slice<D, 128>(p, blockIdx.x, gridDim.x, tid, 128, unit_idx++, n_pieces);
       if (have && ok) {
         ok = mbar_wait(&acc_full[buf], (done_units >> 1) & 1, abort_flag, DQ_WAIT_LIMIT_NS);
         __syncwarp();
@@ -243,6 +296,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         ++done_units;
       }
     }
+    for (; unit_idx < n_pieces; ++unit_idx)
+      gqa_reduce_slice<D, 128>(p, blockIdx.x, gridDim.x, tid, 128, unit_idx, n_pieces);
   }
 
   tc_fence_before();
