@@ -15,7 +15,8 @@
 // bitwise reproducible; there are no atomics and no fp32 accumulator in memory.
 //
 // Warps: 0-3 epilogue (tensor memory -> scale -> bf16 -> dQ; before that, the
-// CTA's slice of the GQA dK/dV group reduction), 4 loads, 5 MMA.
+// CTA's slice of the GQA dK/dV group reduction), 4 dS loads and unit claims,
+// 5 MMA, 6 K loads.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -25,19 +26,24 @@
 
 namespace sdpa {
 
-constexpr int DQ_THREADS = 192;
+constexpr int DQ_THREADS = 224;
 constexpr uint64_t DQ_WAIT_LIMIT_NS = 4000000000ull;
 
+// K tiles (from L2: every query unit of a head reads them) and dS tiles (from
+// HBM, read once) have rings of their own, so that the dS loads, whose latency
+// paces the kernel, can run further ahead.
 template <int D>
 struct DqLayout {
-  static constexpr int NSTAGE = (D <= 128) ? 3 : 2;
+  static constexpr int NK = (D <= 128) ? 3 : 2;         // K buffers
+  static constexpr int NDS = (D <= 128) ? 4 : 3;        // dS buffers
   static constexpr int TILE_K = BN * D * 2;             // [D/64 blocks][128 keys][128 B]
   static constexpr int TILE_DS = 2 * DS_TILE_BYTES;     // two dS^T tiles: [2][128 keys][64 q]
-  static constexpr int STAGE = TILE_K + TILE_DS;
-  static constexpr int OFF_BAR = NSTAGE * STAGE;
-  // full/empty per stage, acc full/empty x2, unit ring full/empty x URING
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_DS = NK * TILE_K;
+  static constexpr int OFF_BAR = OFF_DS + NDS * TILE_DS;
+  // full/empty per K and dS buffer, acc full/empty x2, unit ring full/empty x URING
   static constexpr int URING = 4;
-  static constexpr int NUM_BARS = 2 * NSTAGE + 4 + 2 * URING;
+  static constexpr int NUM_BARS = 2 * NK + 2 * NDS + 4 + 2 * URING;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;  // tmem base, abort flag, unit ring
   static constexpr int BYTES = OFF_MISC + 64;
   static constexpr uint32_t ACC_COLS = D <= 128 ? 128 : 256;   // one accumulator, padded
@@ -105,12 +111,14 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     if (tid == 0) atomicOr(p.status, STATUS_SMEM_ALIGN);
     return;
   }
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
-  uint64_t* empty = full + L::NSTAGE;
-  uint64_t* acc_full = empty + L::NSTAGE;   // [2]
+  uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+  uint64_t* kempty = kfull + L::NK;
+  uint64_t* dsfull = kempty + L::NK;
+  uint64_t* dsempty = dsfull + L::NDS;
+  uint64_t* acc_full = dsempty + L::NDS;    // [2]
   uint64_t* acc_empty = acc_full + 2;       // [2], 128 arrivals
   uint64_t* ufull = acc_empty + 2;          // [URING]
-  uint64_t* uempty = ufull + L::URING;      // [URING], 5 arrivals (MMA warp + 4 epilogue warps)
+  uint64_t* uempty = ufull + L::URING;      // [URING], 6 arrivals (K loads, MMA, 4 epilogue warps)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
   volatile int* ring = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 16);
@@ -127,9 +135,13 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
 
   if (tid == 0) {
     *abort_flag = 0;
-    for (int i = 0; i < L::NSTAGE; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+    for (int i = 0; i < L::NK; ++i) {
+      mbar_init(&kfull[i], 1);
+      mbar_init(&kempty[i], 1);
+    }
+    for (int i = 0; i < L::NDS; ++i) {
+      mbar_init(&dsfull[i], 1);
+      mbar_init(&dsempty[i], 1);
     }
     mbar_init(&acc_full[0], 1);
     mbar_init(&acc_full[1], 1);
@@ -137,7 +149,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     mbar_init(&acc_empty[1], 128);
     for (int i = 0; i < L::URING; ++i) {
       mbar_init(&ufull[i], 1);
-      mbar_init(&uempty[i], 5);
+      mbar_init(&uempty[i], 6);
     }
     fence_mbar_init();
   }
@@ -152,9 +164,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   pdl_wait_prior_grid();  // the dS tiles (and GQA partials) come from the main kernel
 
   if (warp == 4) {
-    // ------------------------------------------------------------ loads
+    // ------------------------------------------------------------ dS loads, unit claims
     if (lane == 0) {
-      prefetch_tmap(&k_map);
       int step = 0;
       for (int e = 0;; ++e) {
         // The ticket was cleared by the preprocess kernel; on this route the
@@ -169,15 +180,13 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         if (u >= n_units) break;
         const DqUnit w = dq_unit(p, u);
         for (int i = 0; i < w.n; ++i, ++step) {
-          const int st = step % L::NSTAGE;
+          const int st = step % L::NDS;
           const int kt = w.kv_first + i;
-          if (step >= L::NSTAGE &&
-              !mbar_wait(&empty[st], ((step / L::NSTAGE) - 1) & 1, abort_flag, DQ_WAIT_LIMIT_NS))
+          if (step >= L::NDS &&
+              !mbar_wait(&dsempty[st], ((step / L::NDS) - 1) & 1, abort_flag, DQ_WAIT_LIMIT_NS))
             goto loads_done;
-          uint8_t* stage = smem + st * L::STAGE;
-          mbar_arrive_expect_tx(&full[st], L::STAGE);
-          for (int blk = 0; blk < D / 64; ++blk)
-            tma_load_3d(stage + blk * (BN * 128), &k_map, &full[st], blk * 64, kt * BN, w.b * p.Hkv + w.hk);
+          uint8_t* stage = smem + L::OFF_DS + st * L::TILE_DS;
+          mbar_arrive_expect_tx(&dsfull[st], L::TILE_DS);
           int lo, hi;
           visited_query_tiles(kt, w.Lq, w.Lk, p.causal, p.bottom_right, p.window_left, p.window_right, lo, hi);
           for (int half = 0; half < 2; ++half) {
@@ -186,11 +195,37 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
             const uint8_t* src =
                 stored ? p.ds_ws + (((long long)w.bh * p.n_kt + kt) * p.n_qt + qt) * (long long)DS_TILE_BYTES
                        : p.zero_tile;
-            bulk_load(stage + L::TILE_K + half * DS_TILE_BYTES, src, DS_TILE_BYTES, &full[st]);
+            bulk_load(stage + half * DS_TILE_BYTES, src, DS_TILE_BYTES, &dsfull[st]);
           }
         }
       }
     loads_done:;
+    }
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ K loads
+    bool ok = true;
+    int step = 0;
+    if (lane == 0) prefetch_tmap(&k_map);
+    for (int e = 0; ok; ++e) {
+      int u;
+      if (!ring_get(e, u) || u < 0) break;
+      const DqUnit w = dq_unit(p, u);
+      for (int i = 0; i < w.n; ++i, ++step) {
+        const int st = step % L::NK;
+        if (step >= L::NK &&
+            !mbar_wait(&kempty[st], ((step / L::NK) - 1) & 1, abort_flag, DQ_WAIT_LIMIT_NS)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          uint8_t* stage = smem + L::OFF_K + st * L::TILE_K;
+          mbar_arrive_expect_tx(&kfull[st], L::TILE_K);
+          for (int blk = 0; blk < D / 64; ++blk)
+            tma_load_3d(stage + blk * (BN * 128), &k_map, &kfull[st], blk * 64,
+                        (w.kv_first + i) * BN, w.b * p.Hkv + w.hk);
+        }
+        __syncwarp();
+      }
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA
@@ -214,14 +249,15 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       __syncwarp();
       tc_fence_after();
       for (int i = 0; i < w.n; ++i, ++step) {
-        const int st = step % L::NSTAGE;
-        ok = mbar_wait(&full[st], (step / L::NSTAGE) & 1, abort_flag, DQ_WAIT_LIMIT_NS);
+        const int sk = step % L::NK, sd = step % L::NDS;
+        ok = mbar_wait(&kfull[sk], (step / L::NK) & 1, abort_flag, DQ_WAIT_LIMIT_NS) &&
+             mbar_wait(&dsfull[sd], (step / L::NDS) & 1, abort_flag, DQ_WAIT_LIMIT_NS);
         __syncwarp();
         if (!ok) break;
         tc_fence_after();
         if (elect_one()) {
-          const uint32_t aK = smem_u32(smem + st * L::STAGE);
-          const uint32_t aS = aK + L::TILE_K;
+          const uint32_t aK = smem_u32(smem + L::OFF_K + sk * L::TILE_K);
+          const uint32_t aS = smem_u32(smem + L::OFF_DS + sd * L::TILE_DS);
           // A = dS as (M = 128 queries, K = keys): the stored dS^T tiles are
           // [key][query] with queries contiguous, i.e. MN-major, the two 64-query
           // tiles 16 KB apart. B = K as (N = d, K = keys): MN-major as well.
@@ -229,7 +265,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
           for (int k = 0; k < BN / 16; ++k)
             mma_ss(acc, sdesc_at(T_MN, aS + k * 2048), sdesc_at(T_MN, aK + k * 2048), ID,
                    (i > 0 || k > 0));
-          mma_commit(&empty[st]);
+          mma_commit(&kempty[sk]);
+          mma_commit(&dsempty[sd]);
           if (i == w.n - 1) mma_commit(&acc_full[buf]);
         }
         __syncwarp();
