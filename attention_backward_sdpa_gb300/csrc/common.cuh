@@ -27,6 +27,11 @@ constexpr int STATUS_SMEM_ALIGN = 2;
 struct ChainParams {
   int B, Hq, Hkv, Sq, Skv, Dqk, Dv;
   int G;            // Hq / Hkv
+  // Main-kernel work units of the D_qk 64/128 kernels cover gsz query heads of
+  // one KV group (their dK/dV summed in tensor memory); n_part = G / gsz
+  // partial dK/dV sets per KV head then remain for the group reduction (none
+  // when n_part == 1). The D_qk 192 kernel always has gsz = 1.
+  int gsz, n_part;
   int n_qt, n_kt;   // ceil(Sq / BQ), ceil(Skv / BN)
   float scale;      // softmax scale
   float scale_log2; // scale * log2(e)
@@ -48,8 +53,8 @@ struct ChainParams {
   float* dq_accum;      // [B*Hq][n_qt*BQ][Dqk] row-major, rows padded to whole tiles
   int* counters;        // [B*Hq][n_qt] turn counters (deterministic mode)
   int* ticket;          // work-unit ticket
-  __nv_bfloat16* dk_ws; // GQA: [B][Hq][Skv][Dqk] partials, else null
-  __nv_bfloat16* dv_ws; // GQA: [B][Hq][Skv][Dv]
+  __nv_bfloat16* dk_ws; // n_part > 1: [B][Hkv][n_part][Skv][Dqk] partials, else null
+  __nv_bfloat16* dv_ws; // n_part > 1: [B][Hkv][n_part][Skv][Dv]
   int n_counters;       // B*Hq*n_qt + 1 (counters plus ticket)
 
   // Deterministic two-kernel route: the main kernel stores each bf16 dS^T tile
@@ -139,13 +144,13 @@ __device__ inline void batch_lengths(const ChainParams& p, int b, int& Lq, int& 
   Lk = p.seq_kv_lens ? min(max(p.seq_kv_lens[b], 0), p.Skv) : p.Skv;
 }
 
-// Zero rows [k0, min(k0 + BN, S_kv)) of dK and dV (or of the query head's GQA
-// partials) for a key tile that no query sees: such keys have exactly zero
-// gradient, and the outputs are overwritten in full. Called by every thread of
-// a CTA; 16-byte stores, consecutive threads on consecutive addresses.
+// Zero rows [k0, min(k0 + BN, S_kv)) of dK and dV (`head` indexes the KV heads,
+// or the partial sets of the group reduction when dk_ws is set) for a key tile
+// that no query sees: such keys have exactly zero gradient, and the outputs are
+// overwritten in full. Called by every thread of a CTA; 16-byte stores,
+// consecutive threads on consecutive addresses.
 template <int DQK, int DV>
-__device__ inline void zero_key_tile_rows(const ChainParams& p, int b, int bh, int hk, int k0) {
-  const long long head = p.dk_ws ? (long long)bh : (long long)b * p.Hkv + hk;
+__device__ inline void zero_key_tile_rows(const ChainParams& p, long long head, int k0) {
   const int rows = min(BN, p.Skv - k0);
   const uint4 z = make_uint4(0u, 0u, 0u, 0u);
   uint4* dk = reinterpret_cast<uint4*>((p.dk_ws ? p.dk_ws : p.dk) + (head * p.Skv + k0) * DQK);

@@ -1,9 +1,10 @@
 // gqa.cuh -- the fixed-order GQA/MQA group reduction of dK/dV ("GQA/MQA group
 // reduction" section of the cuDNN frontend page "SDPA Backward (SM120)"):
-// dK[b, kv head, key] = sum over the group's query heads, in ascending head
-// order, of the per-query-head bf16 partials, accumulated in fp32 and rounded
-// once to bf16 (bitwise reproducible by construction). Run by the dQ kernels
-// over slices of the output rows, overlapping their other work.
+// dK[b, kv head, key] = sum over the group's n_part partial sets (each the sum
+// of gsz query heads, in ascending head order), in ascending order,
+// accumulated in fp32 and rounded once to bf16 (bitwise reproducible by
+// construction). Run by the dQ kernels over slices of the output rows,
+// overlapping their other work.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -32,20 +33,20 @@ __device__ __forceinline__ void gqa_reduce_rows(const ChainParams& p, const __nv
   constexpr unsigned CPR = D / 8;  // chunks per row
   const unsigned items = (row_end > row_begin ? row_end - row_begin : 0) * CPR;
   const long long head_stride = (long long)p.Skv * D;
-  const int G = p.G;
+  const int G = p.n_part;
   for (unsigned it = thread; it < items; it += nthreads) {
     const unsigned row = row_begin + it / CPR, c8 = it % CPR;
     const unsigned bhk = row / (unsigned)p.Skv, k = row - bhk * (unsigned)p.Skv;
     const unsigned b = bhk / (unsigned)p.Hkv, hk = bhk - b * (unsigned)p.Hkv;
     const __nv_bfloat16* src =
-        ws + (long long)(b * p.Hq + hk * G) * head_stride + (long long)k * D + c8 * 8;
+        ws + (long long)(b * p.Hkv + hk) * G * head_stride + (long long)k * D + c8 * 8;
     uint4 v[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j)  // issue the group's loads together
       if (j < G) v[j] = *reinterpret_cast<const uint4*>(src + j * head_stride);
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {  // ascending query head: fixed order
+    for (int j = 0; j < 8; ++j) {  // ascending partial set: fixed order
       if (j < G) {
         float f[8];
         unpack8(v[j], f);
@@ -53,7 +54,7 @@ __device__ __forceinline__ void gqa_reduce_rows(const ChainParams& p, const __nv
         for (int e = 0; e < 8; ++e) acc[e] += f[e];
       }
     }
-    for (int j = 8; j < G; ++j) {  // larger groups: the remaining heads, same order
+    for (int j = 8; j < G; ++j) {  // more partial sets: the rest, same order
       float f[8];
       unpack8(*reinterpret_cast<const uint4*>(src + j * head_stride), f);
 #pragma unroll

@@ -286,6 +286,20 @@ int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const v
   ChainParams p{};
   p.B = B; p.Hq = H_q; p.Hkv = H_kv; p.Sq = S_q; p.Skv = S_kv; p.Dqk = D_qk; p.Dv = D_v;
   p.G = H_q / H_kv;
+  // Head-group size of the D_qk 64/128 main kernel: the largest divisor of G
+  // that still leaves at least three work units per SM (so the greedy
+  // dispatch stays balanced). Fewer, longer units pay the per-unit start and
+  // drain less often and leave fewer partial dK/dV sets to reduce.
+  p.gsz = 1;
+  if (D_qk != 192) {
+    for (int c = p.G; c > 1; --c) {
+      if (p.G % c == 0 && (long long)ceil_div(S_kv, BN) * B * H_kv * (p.G / c) >= 3ll * sms) {
+        p.gsz = c;
+        break;
+      }
+    }
+  }
+  p.n_part = p.G / p.gsz;
   p.n_qt = ceil_div(S_q, BQ);
   p.n_kt = ceil_div(S_kv, BN);
   p.scale = scale;
@@ -313,8 +327,10 @@ int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const v
   p.counters = reinterpret_cast<int*>(ws + cv.counters);
   p.n_counters = B * H_q * p.n_qt + 1;
   p.ticket = p.counters + (p.n_counters - 1);
-  p.dk_ws = H_kv < H_q ? reinterpret_cast<__nv_bfloat16*>(ws + cv.dk_ws) : nullptr;
-  p.dv_ws = H_kv < H_q ? reinterpret_cast<__nv_bfloat16*>(ws + cv.dv_ws) : nullptr;
+  // Partial dK/dV sets ([B][H_kv][n_part][S_kv][D], within the region sized for
+  // one set per query head) when a KV group spans several work units.
+  p.dk_ws = p.n_part > 1 ? reinterpret_cast<__nv_bfloat16*>(ws + cv.dk_ws) : nullptr;
+  p.dv_ws = p.n_part > 1 ? reinterpret_cast<__nv_bfloat16*>(ws + cv.dv_ws) : nullptr;
   p.status = status;
 
   MainMaps maps;

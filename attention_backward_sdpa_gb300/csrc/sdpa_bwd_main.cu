@@ -127,14 +127,14 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
   if (!p.deterministic) {
     // A key tile that no query sees only has zero gradients: write them and
     // leave before any barrier or tensor-memory setup.
-    const int BH0 = p.B * p.Hq;
-    const int kt0 = blockIdx.x / BH0, bh0 = blockIdx.x % BH0, b0 = bh0 / p.Hq;
+    const int NG0 = p.B * p.Hkv * p.n_part;
+    const int kt0 = blockIdx.x / NG0, gi0 = blockIdx.x % NG0, b0 = gi0 / (p.Hkv * p.n_part);
     int Lq0, Lk0, lo0, hi0;
     batch_lengths(p, b0, Lq0, Lk0);
     visited_query_tiles(kt0, Lq0, Lk0, p.causal, p.bottom_right, p.window_left, p.window_right, lo0,
                         hi0);
     if (hi0 < lo0) {
-      zero_key_tile_rows<D, D>(p, b0, bh0, (bh0 % p.Hq) / p.G, kt0 * BN);
+      zero_key_tile_rows<D, D>(p, p.dk_ws ? (long long)gi0 : (long long)(gi0 / p.n_part), kt0 * BN);
       return;
     }
   }
@@ -186,15 +186,20 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
   const uint32_t tmem = *tmem_slot;
   const int unit = *unit_slot;
 
-  // Units are ordered key tile major: every head's key tile 0 first. Under a
-  // causal mask low key tiles see the most query tiles, so the longest units
-  // start first.
-  const int BH = p.B * p.Hq;
-  const int kt = unit / BH;
-  const int bh = unit % BH;
-  const int b = bh / p.Hq, h = bh % p.Hq;
-  const int hk = h / p.G;
+  // A unit is one key tile of one head group: gsz query heads of one KV head
+  // (group gi = (b * Hkv + hk) * n_part + g covers query heads
+  // hk * G + g * gsz ...). Units are ordered key tile major: every group's key
+  // tile 0 first. Under a causal mask low key tiles see the most query tiles,
+  // so the longest units start first.
+  const int NG = p.B * p.Hkv * p.n_part;
+  const int kt = unit / NG;
+  const int gi = unit % NG;
+  const int kvh_g = gi / p.n_part;                 // b * Hkv + hk
+  const int b = kvh_g / p.Hkv, hk = kvh_g % p.Hkv;
+  const int bh0 = b * p.Hq + hk * p.G + (gi % p.n_part) * p.gsz;  // the group's first query head
   const int k0 = kt * BN;
+  // dK/dV destination: the KV head, or the group's partial set.
+  const long long out_head = p.dk_ws ? (long long)gi : (long long)kvh_g;
 
   int Lq, Lk;
   batch_lengths(p, b, Lq, Lk);
@@ -204,7 +209,10 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
   int qt_lo, qt_hi;
   visited_query_tiles(kt, Lq, Lk, p.causal, p.bottom_right, p.window_left, p.window_right, qt_lo,
                       qt_hi);
-  const int n = qt_hi - qt_lo + 1;  // query tiles this CTA visits (may be 0)
+  // Tiles t = 0 .. n-1 walk the visible query tiles (descending) of the group's
+  // heads in turn: head bh0 + t / n1, query tile qt_hi - t % n1.
+  const int n1 = qt_hi >= qt_lo ? qt_hi - qt_lo + 1 : 0;  // query tiles per head
+  const int n = p.gsz * n1;
 
   if (warp >= 12) {
     regs_decrease<REGS_CTRL>();
@@ -222,7 +230,8 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
         if (t >= NSTAGE && !mbar_wait(&bars[BAR_QEMPTY + st], ((t / NSTAGE) - 1) & 1, abort_flag,
                                       WAIT_LIMIT_NS))
           break;
-        const int qt = qt_hi - t;
+        const int hj = t / n1;
+        const int qt = qt_hi - (t - hj * n1), bh = bh0 + hj;
         uint64_t* full = &bars[BAR_QFULL + st];
         mbar_arrive_expect_tx(full, 2 * L::TILE_Q + QSTAT_FLOATS * 4);
         for (int blk = 0; blk < D / 64; ++blk) {
@@ -350,7 +359,8 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
         for (int t = 0; t < n; ++t) {
           const int s = t & 1, j = t >> 1;
           if (!mbar_wait(&bars[BAR_DSREADY + s], j & 1, abort_flag, WAIT_LIMIT_NS)) break;
-          const int qt = qt_hi - t;
+          const int hj = t / n1;
+          const int qt = qt_hi - (t - hj * n1), bh = bh0 + hj;
           uint8_t* dst = p.ds_ws + (((long long)bh * p.n_kt + kt) * p.n_qt + qt) * (long long)DS_TILE_BYTES;
           bulk_store(dst, sDS + s * L::TILE_DS, DS_TILE_BYTES);
           bulk_commit_group();
@@ -374,7 +384,8 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
     bool ok = true;
     for (int t = 0; t < (DS_OUT ? 0 : n) && ok; ++t) {
       const int s = t & 1, j = t >> 1;
-      const int qt = qt_hi - t;
+      const int hj = t / n1;
+      const int qt = qt_hi - (t - hj * n1), bh = bh0 + hj;
       if (!mbar_wait(&bars[BAR_DQFULL + s], j & 1, abort_flag, WAIT_LIMIT_NS)) { ok = false; break; }
       __syncwarp();
       tc_fence_after();
@@ -466,7 +477,7 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
 
     for (int t = slot; t < n && ok; t += 2) {
       const int j = t >> 1, st = t % NSTAGE;
-      const int qt = qt_hi - t, q0 = qt * BQ;
+      const int qt = qt_hi - (t % n1), q0 = qt * BQ;
       const float* qs = sQS + st * QSTAT_FLOATS;
       const bool need_mask = (k0 + BN > Lk) ||
                              (p.causal && (long long)q0 < (long long)(k0 + BN - 1) - diag - Rp) ||
@@ -594,7 +605,7 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
     fence_proxy_async_smem();
     named_bar_sync(1 + slot, 128);
     if (row == 0) {
-      const long long head = p.dk_ws ? (long long)bh : (long long)b * p.Hkv + hk;
+      const long long head = out_head;
       const CUtensorMap* map = slot ? &maps.dk_out : &maps.dv_out;
       for (int blk = 0; blk < D / 64; ++blk) tma_store_3d(map, stg + blk * L::BLK_KV, blk * 64, k0, (int)head);
       bulk_commit_group();
@@ -624,9 +635,9 @@ cudaError_t main_kernel_setup() {
   return e;
 }
 
-// One CTA per (key tile, batch, query head) work unit.
+// One CTA per (key tile, head group) work unit.
 cudaError_t launch_main(const MainMaps& maps, const ChainParams& p, cudaStream_t s) {
-  const dim3 grid((unsigned)(p.n_kt * p.B * p.Hq));
+  const dim3 grid((unsigned)(p.n_kt * p.B * p.Hkv * p.n_part));
   const dim3 block(MAIN_THREADS);
   if (p.Dqk == 64)
     return launch_kernel(sdpa_bwd_main<64, false>, grid, block, MainLayout<64, false>::BYTES, s, true,

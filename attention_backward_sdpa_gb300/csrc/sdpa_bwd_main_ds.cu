@@ -118,7 +118,9 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
     visited_query_tiles(kt0, Lq0, Lk0, p.causal, p.bottom_right, p.window_left, p.window_right, lo0,
                         hi0);
     if (hi0 < lo0) {
-      zero_key_tile_rows<DQK, DV>(p, b0, bh0, (bh0 % p.Hq) / p.G, kt0 * BN);
+      // gsz = 1: the partial set of a query head is its bh index.
+      zero_key_tile_rows<DQK, DV>(p, p.dk_ws ? (long long)bh0 : (long long)b0 * p.Hkv + (bh0 % p.Hq) / p.G,
+                                  kt0 * BN);
       return;
     }
   }

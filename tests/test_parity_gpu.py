@@ -177,7 +177,26 @@ def _sample_rows(w, lens, rng, n_rand=24):
 
 @pytest.mark.parametrize("name", workloads.ORDER)
 def test_workload_sampled_parity(name):
-    case = _case(name)
+    _sampled_check(_case(name))
+
+
+# Shapes large enough that the main kernel's work units span several query
+# heads of a KV group (their dK/dV summed in tensor memory): two heads per
+# unit with no partial sets left (G = 2), and two heads per unit with two
+# partial sets to reduce (G = 4, deterministic route).
+GROUPED = {
+    "group2_nopart": W("group2_nopart", 2, 32, 16, 2048, 2048, 128, 128, causal=True, seed=36),
+    "group2_part2_det": W("group2_part2_det", 2, 32, 8, 2048, 2048, 128, 128, causal=True,
+                          deterministic=True, seed=37),
+}
+
+
+@pytest.mark.parametrize("name", sorted(GROUPED))
+def test_grouped_units_sampled_parity(name):
+    _sampled_check(make_case(GROUPED[name]))
+
+
+def _sampled_check(case):
     w = case["workload"]
     dq, dk, dv = gpu_backward(case)
     lens = None if case["seq_q_lens"] is None else case["seq_q_lens"].numpy()
