@@ -287,13 +287,14 @@ int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const v
   p.B = B; p.Hq = H_q; p.Hkv = H_kv; p.Sq = S_q; p.Skv = S_kv; p.Dqk = D_qk; p.Dv = D_v;
   p.G = H_q / H_kv;
   // Head-group size of the D_qk 64/128 main kernel: the largest divisor of G
-  // that still leaves at least three work units per SM (so the greedy
-  // dispatch stays balanced). Fewer, longer units pay the per-unit start and
-  // drain less often and leave fewer partial dK/dV sets to reduce.
+  // that still leaves at least 1.5 work units per SM. Fewer, longer units pay
+  // the per-unit start and drain less often and leave fewer partial dK/dV sets
+  // to reduce; below 1.5 units per SM the greedy dispatch of uneven (causal)
+  // units loses more to imbalance than that saves.
   p.gsz = 1;
   if (D_qk != 192) {
     for (int c = p.G; c > 1; --c) {
-      if (p.G % c == 0 && (long long)ceil_div(S_kv, BN) * B * H_kv * (p.G / c) >= 3ll * sms) {
+      if (p.G % c == 0 && (long long)ceil_div(S_kv, BN) * B * H_kv * (p.G / c) * 2 >= 3ll * sms) {
         p.gsz = c;
         break;
       }

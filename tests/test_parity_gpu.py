@@ -181,12 +181,14 @@ def test_workload_sampled_parity(name):
 
 
 # Shapes large enough that the main kernel's work units span several query
-# heads of a KV group (their dK/dV summed in tensor memory): two heads per
-# unit with no partial sets left (G = 2), and two heads per unit with two
-# partial sets to reduce (G = 4, deterministic route).
+# heads of a KV group (their dK/dV summed in tensor memory; the host takes the
+# largest group size that leaves 1.5 units per SM): two heads per unit with no
+# partial sets left (G = 2: 16 key tiles x 2 x 16 groups = 512 units), and two
+# heads per unit with two partial sets to reduce (G = 4, deterministic route:
+# 16 x 1 x 8 x 2 = 256 units, while four heads per unit would leave 128).
 GROUPED = {
     "group2_nopart": W("group2_nopart", 2, 32, 16, 2048, 2048, 128, 128, causal=True, seed=36),
-    "group2_part2_det": W("group2_part2_det", 2, 32, 8, 2048, 2048, 128, 128, causal=True,
+    "group2_part2_det": W("group2_part2_det", 1, 32, 8, 2048, 2048, 128, 128, causal=True,
                           deterministic=True, seed=37),
 }
 
