@@ -130,9 +130,17 @@ __device__ __forceinline__ void bulk_commit_group() {
 __device__ __forceinline__ void bulk_wait_group_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
+// Waits until all but the most recent committed bulk group have read their source.
+__device__ __forceinline__ void bulk_wait_group_read1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 // Waits until every committed bulk group has completed (global writes done).
 __device__ __forceinline__ void bulk_wait_group0() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Waits until all but the two most recent committed bulk groups have completed.
+__device__ __forceinline__ void bulk_wait_group2() {
+  asm volatile("cp.async.bulk.wait_group 2;" ::: "memory");
 }
 // Waits until all but the most recent committed bulk group have completed.
 __device__ __forceinline__ void bulk_wait_group1() {

@@ -69,12 +69,12 @@ enum : int {
   BAR_DSREADY = 17,     // + slot, 128 arrivals
   BAR_DQFULL = 19,      // + slot
   BAR_DQEMPTY = 21,     // + slot, 128 arrivals
-  BAR_STAGEREADY = 23,  // 128 arrivals
-  BAR_STAGEFREE = 24,
-  BAR_MMADONE = 25,     // every MMA of the CTA has completed (epilogue may read dK/dV)
-  BAR_DSCOPIED = 26,    // + slot: the slot's dS^T tile has been read out to global (dS route)
-  BAR_DPREAD = 28,      // + slot, 128 arrivals: dP^T has been loaded into registers
-  NUM_BARS = 30
+  BAR_MMADONE = 23,     // every MMA of the CTA has completed (epilogue may read dK/dV)
+  BAR_DSCOPIED = 24,    // + slot: the slot's dS^T tile has been read out to global (dS route)
+  BAR_DPREAD = 26,      // + slot, 128 arrivals: dP^T has been loaded into registers
+  BAR_STAGEREADY = 28,  // + staging half (2), 128 arrivals: the half is written
+  BAR_STAGEFREE = 30,   // + staging half (2): its bulk reduction has read it
+  NUM_BARS = 32
 };
 
 // NST Q/dO stages; the dQ staging buffer exists only on the dQ-reduction route
@@ -155,7 +155,8 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
     for (int i = 0; i < NUM_BARS; ++i) {
       const bool threads128 = (i == BAR_PREADY || i == BAR_PREADY + 1 || i == BAR_DSREADY ||
                                i == BAR_DSREADY + 1 || i == BAR_DQEMPTY || i == BAR_DQEMPTY + 1 ||
-                               i == BAR_STAGEREADY || i == BAR_DPREAD || i == BAR_DPREAD + 1);
+                               i == BAR_STAGEREADY || i == BAR_STAGEREADY + 1 || i == BAR_DPREAD ||
+                               i == BAR_DPREAD + 1);
       mbar_init(&bars[i], threads128 ? 128 : 1);
     }
     fence_mbar_init();
@@ -381,6 +382,8 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
     const bool leader = (warp == 8 && lane == 0);
     int* pending_counter = nullptr;  // deterministic mode: turn not yet released
     int pending_turn = 0;
+    int* pending_next = nullptr;     // ... and the current tile's, once the next is issued
+    int pending_next_turn = 0;
     bool ok = true;
     for (int t = 0; t < (DS_OUT ? 0 : n) && ok; ++t) {
       const int s = t & 1, j = t >> 1;
@@ -398,58 +401,71 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
       }
       tc_fence_before();
       mbar_arrive(&bars[BAR_DQEMPTY + s]);
-      if (t >= 1 && !mbar_wait(&bars[BAR_STAGEFREE], (t - 1) & 1, abort_flag, WAIT_LIMIT_NS)) { ok = false; break; }
-      if (has_rows) {
-#pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          sDQ[q * D + d] = __uint_as_float(va[q]);
-          sDQ[(q + 32) * D + d] = __uint_as_float(vb[q]);
-        }
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(&bars[BAR_STAGEREADY]);
-      if (leader) {
-        mbar_wait(&bars[BAR_STAGEREADY], t & 1, abort_flag, WAIT_LIMIT_NS);
-        float* dst = p.dq_accum + ((long long)bh * p.n_qt + qt) * (long long)BQ * D;
-        if (p.deterministic) {
-          // Ordered relay: key tiles add into this query tile in ascending
-          // order. This tile's turn is released once its reduction has
-          // completed, which is checked after the next tile's reduction has been
-          // issued (wait_group 1), so the completion latency overlaps the next
-          // tile instead of stalling this warpgroup. A key tile only ever waits
-          // on lower key tiles, so the delayed release only skews the chain.
-          const int kv_lo = has_window ? (int)max(0ll, floor_div((long long)qt * BQ + diag -
-                                                                     p.window_left, BN))
-                                       : 0;
-          const int turn = kt - kv_lo;
-          int* counter = p.counters + (long long)bh * p.n_qt + qt;
-          const uint64_t t0 = globaltimer_ns();
-          while (ld_acquire_gpu(counter) != turn) {
-            __nanosleep(32);
-            if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
-              set_status(p.status, STATUS_TIMEOUT);
-              break;
-            }
+      // The staging buffer is used as two 16 KiB halves (query rows 0-31 and
+      // 32-63, contiguous in the accumulator), each with its own bulk reduction:
+      // the first half's copy runs while the second is written, and a half is
+      // refilled as soon as its own copy has read it.
+      float* dst = p.dq_accum + ((long long)bh * p.n_qt + qt) * (long long)BQ * D;
+      if (leader && p.deterministic) {
+        // Ordered relay: key tiles add into this query tile in ascending
+        // order. This tile's turn is released once both of its reductions have
+        // completed, which is checked after the next tile's reductions have
+        // been issued, so the completion latency overlaps the next tile instead
+        // of stalling this warpgroup. A key tile only ever waits on lower key
+        // tiles, so the delayed release only skews the chain.
+        const int kv_lo = has_window ? (int)max(0ll, floor_div((long long)qt * BQ + diag -
+                                                                   p.window_left, BN))
+                                     : 0;
+        const int turn = kt - kv_lo;
+        int* counter = p.counters + (long long)bh * p.n_qt + qt;
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_acquire_gpu(counter) != turn) {
+          __nanosleep(32);
+          if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+            set_status(p.status, STATUS_TIMEOUT);
+            break;
           }
-          fence_proxy_async_global();
-          bulk_reduce_add_f32(dst, sDQ, L::TILE_DQ);
+        }
+        fence_proxy_async_global();
+        if (pending_counter != nullptr) pending_next = counter, pending_next_turn = turn;
+        else pending_counter = counter, pending_turn = turn;
+      }
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        float* stg = sDQ + hf * (L::TILE_DQ / 8);
+        if (t >= 1 &&
+            !mbar_wait(&bars[BAR_STAGEFREE + hf], (t - 1) & 1, abort_flag, WAIT_LIMIT_NS)) {
+          ok = false;
+          break;
+        }
+        if (has_rows) {
+          const uint32_t* v = hf ? vb : va;
+#pragma unroll
+          for (int q = 0; q < 32; ++q) stg[q * D + d] = __uint_as_float(v[q]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bars[BAR_STAGEREADY + hf]);
+        if (leader) {
+          mbar_wait(&bars[BAR_STAGEREADY + hf], t & 1, abort_flag, WAIT_LIMIT_NS);
+          bulk_reduce_add_f32(dst + hf * 32 * D, stg, L::TILE_DQ / 2);
           bulk_commit_group();
-          bulk_wait_group_read0();
-          mbar_arrive(&bars[BAR_STAGEFREE]);
-          if (pending_counter != nullptr) {  // previous tile: complete -> release its turn
-            bulk_wait_group1();
+          // The previously issued half's reduction has read its buffer.
+          if (t >= 1 || hf == 1) {
+            bulk_wait_group_read1();
+            mbar_arrive(&bars[BAR_STAGEFREE + (hf ^ 1)]);
+          }
+          if (p.deterministic && hf == 1 && pending_next != nullptr) {
+            // Both halves of the previous tile complete -> release its turn.
+            bulk_wait_group2();
             fence_proxy_async_global();
             st_release_gpu(pending_counter, pending_turn + 1);
+            pending_counter = pending_next;
+            pending_turn = pending_next_turn;
+            pending_next = nullptr;
           }
-          pending_counter = counter;
-          pending_turn = turn;
-        } else {
-          bulk_reduce_add_f32(dst, sDQ, L::TILE_DQ);
-          bulk_commit_group();
-          bulk_wait_group_read0();
-          mbar_arrive(&bars[BAR_STAGEFREE]);
         }
       }
+      if (!ok) break;
     }
     if (leader) {
       bulk_wait_group0();

@@ -58,6 +58,11 @@ SMALL = {
     "gqa_det": W("gqa_det", 1, 4, 2, 520, 520, 128, 128, causal=True, deterministic=True, seed=24),
     "window_det": W("window_det", 2, 2, 1, 600, 600, 128, 128, causal=True, window_left=200,
                     deterministic=True, seed=25),
+    # deterministic D=64: the ordered relay of dQ reductions on turn counters
+    "det_d64_relay": W("det_d64_relay", 2, 4, 2, 300, 300, 64, 64, causal=True,
+                       deterministic=True, seed=38),
+    "det_d64_window": W("det_d64_window", 1, 2, 2, 400, 330, 64, 64, causal=True,
+                        bottom_right=True, window_left=90, deterministic=True, seed=39),
     # deterministic D=128: the 128-row-tile main kernel (odd 64-row tile counts
     # exercise its half-filled last tile)
     "det_padded_odd": W("det_padded_odd", 2, 2, 2, 300, 300, 128, 128, causal=True,
@@ -137,8 +142,9 @@ def test_adversarial_key_growth_masked():
         assert leak <= 1e-5 * np.abs(r).max(), f"{name}: {leak:.3e} where the oracle is exactly zero"
 
 
-def test_deterministic_bitwise_small():
-    w = SMALL["window_det"]
+@pytest.mark.parametrize("name", ["window_det", "det_d64_relay"])
+def test_deterministic_bitwise_small(name):
+    w = SMALL[name]
     case = make_case(w)
     d = to_device(case)
     first = gpu_backward(case, d)
