@@ -349,10 +349,9 @@ int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const v
   }
 
   cudaError_t e = cudaSuccess;
-  const int aux_grid = sms * 4;
   ProfEvents prof(stream);
   prof.begin(0);
-  e = launch_preprocess(p, aux_grid, stream);
+  e = launch_preprocess(p, stream);
   prof.end(0);
   if (e == cudaSuccess) {
     prof.begin(1);
@@ -361,7 +360,7 @@ int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const v
   }
   if (e == cudaSuccess) {  // dQ (and, under GQA, the dK/dV group reduction)
     prof.begin(2);
-    e = ds_route ? launch_dq_from_ds(maps.k, p, stream, sms) : launch_dq_convert(p, aux_grid, stream);
+    e = ds_route ? launch_dq_from_ds(maps.k, p, stream, sms) : launch_dq_convert(p, stream);
     prof.end(2);
   }
   if (own_ws) cudaFreeAsync(workspace, stream);

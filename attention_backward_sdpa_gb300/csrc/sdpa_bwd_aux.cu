@@ -111,57 +111,64 @@ __global__ void __launch_bounds__(256) sdpa_bwd_preprocess(const ChainParams p) 
 
 // ---------------------------------------------------------------- dq convert
 // dq_accum: [B*Hq][n_qt*BQ][Dqk] fp32, row-major; rows past S_q are padding.
-// Thread item i = (row, 8-column chunk) of dQ; 32-bit index arithmetic.
-// It also carries the GQA group reduction of dK/dV (a slice per CTA).
+// One 64-row query tile per CTA: 64 rows x DQK/8 chunks of 8 columns, every
+// thread's loads issued before any store, index arithmetic once per tile. Rows
+// at or past the batch row's query length are written as zeros without being
+// read (the preprocess kernel did not clear them). The kernel also carries a
+// slice of the GQA group reduction of dK/dV (gqa.cuh).
 template <int DQK, int DV>
 __global__ void __launch_bounds__(256) sdpa_bwd_dq_convert(const ChainParams p) {
   pdl_wait_prior_grid();
   gqa_reduce_slice<DQK, DV>(p, blockIdx.x, gridDim.x, threadIdx.x, blockDim.x);
-  constexpr unsigned PER_ROW = DQK / 8;
-  const unsigned total = (unsigned)p.B * p.Hq * p.Sq * PER_ROW;
-  const unsigned nthreads = gridDim.x * blockDim.x;
-  const unsigned rows_pad = (unsigned)p.n_qt * BQ;
-  constexpr int VEC = 4;
-  for (unsigned i0 = blockIdx.x * blockDim.x + threadIdx.x; i0 < total; i0 += nthreads * VEC) {
-    float4 a[VEC], c[VEC];
+  constexpr int CPR = DQK / 8;                 // 8-column chunks per row
+  constexpr int ITEMS = BQ * CPR / 256;        // items per thread
+  static_assert(BQ * CPR % 256 == 0, "whole items per thread");
+  const unsigned bh = blockIdx.x / (unsigned)p.n_qt;
+  const int qt = (int)(blockIdx.x - bh * (unsigned)p.n_qt);
+  int Lq, Lk;
+  batch_lengths(p, (int)(bh / (unsigned)p.Hq), Lq, Lk);
+  const int rows = min(BQ, p.Sq - qt * BQ);         // rows of dQ in this tile
+  const int live = max(0, min(rows, Lq - qt * BQ)); // rows holding accumulated values
+  const float* src = p.dq_accum + ((long long)bh * p.n_qt + qt) * BQ * DQK;
+  __nv_bfloat16* dst = p.dq + ((long long)bh * p.Sq + (long long)qt * BQ) * DQK;
+  float4 a[ITEMS], c[ITEMS];
 #pragma unroll
-    for (int u = 0; u < VEC; ++u) {
-      const unsigned i = i0 + u * nthreads;
-      if (i >= total) continue;
-      const unsigned r = i / PER_ROW, c8 = i - r * PER_ROW;  // r = (b*Hq + h)*Sq + q
-      const unsigned bh = r / (unsigned)p.Sq, q = r - bh * (unsigned)p.Sq;
-      // Rows at or past the batch row's query length are zero (and were not cleared).
-      if (p.seq_q_lens && (int)q >= min(max(__ldg(p.seq_q_lens + bh / (unsigned)p.Hq), 0), p.Sq)) {
-        a[u] = c[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        continue;
-      }
-      const float* src = p.dq_accum + ((long long)bh * rows_pad + q) * DQK + c8 * 8;
-      a[u] = *reinterpret_cast<const float4*>(src);
-      c[u] = *reinterpret_cast<const float4*>(src + 4);
+  for (int u = 0; u < ITEMS; ++u) {
+    const int i = threadIdx.x + u * 256, r = i / CPR, c8 = i % CPR;
+    if (r < live) {
+      a[u] = *reinterpret_cast<const float4*>(src + r * DQK + c8 * 8);
+      c[u] = *reinterpret_cast<const float4*>(src + r * DQK + c8 * 8 + 4);
+    } else {
+      a[u] = c[u] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
+  }
 #pragma unroll
-    for (int u = 0; u < VEC; ++u) {
-      const unsigned i = i0 + u * nthreads;
-      if (i >= total) continue;
+  for (int u = 0; u < ITEMS; ++u) {
+    const int i = threadIdx.x + u * 256, r = i / CPR, c8 = i % CPR;
+    if (r < rows) {
       uint4 out;
       out.x = pack_bf16x2(a[u].x * p.scale, a[u].y * p.scale);
       out.y = pack_bf16x2(a[u].z * p.scale, a[u].w * p.scale);
       out.z = pack_bf16x2(c[u].x * p.scale, c[u].y * p.scale);
       out.w = pack_bf16x2(c[u].z * p.scale, c[u].w * p.scale);
-      *reinterpret_cast<uint4*>(p.dq + (long long)i * 8) = out;
+      *reinterpret_cast<uint4*>(dst + r * DQK + c8 * 8) = out;
     }
   }
 }
 
-cudaError_t launch_preprocess(const ChainParams& p, int grid, cudaStream_t s) {
-  return p.Dv == 64 ? launch_kernel(sdpa_bwd_preprocess<64>, dim3(grid), dim3(256), 0, s, false, p)
-                    : launch_kernel(sdpa_bwd_preprocess<128>, dim3(grid), dim3(256), 0, s, false, p);
+// Both kernels take one 64-row query tile per CTA and leave the balancing of
+// the tiles to the hardware dispatcher.
+cudaError_t launch_preprocess(const ChainParams& p, cudaStream_t s) {
+  const dim3 grid((unsigned)(p.B * p.Hq * p.n_qt));
+  return p.Dv == 64 ? launch_kernel(sdpa_bwd_preprocess<64>, grid, dim3(256), 0, s, false, p)
+                    : launch_kernel(sdpa_bwd_preprocess<128>, grid, dim3(256), 0, s, false, p);
 }
 
-cudaError_t launch_dq_convert(const ChainParams& p, int grid, cudaStream_t s) {
+cudaError_t launch_dq_convert(const ChainParams& p, cudaStream_t s) {
+  const dim3 grid((unsigned)(p.B * p.Hq * p.n_qt));
   return p.Dqk == 64
-             ? launch_kernel(sdpa_bwd_dq_convert<64, 64>, dim3(grid), dim3(256), 0, s, true, p)
-             : launch_kernel(sdpa_bwd_dq_convert<128, 128>, dim3(grid), dim3(256), 0, s, true, p);
+             ? launch_kernel(sdpa_bwd_dq_convert<64, 64>, grid, dim3(256), 0, s, true, p)
+             : launch_kernel(sdpa_bwd_dq_convert<128, 128>, grid, dim3(256), 0, s, true, p);
 }
 
 }  // namespace sdpa
