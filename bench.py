@@ -24,6 +24,7 @@ max over ranks. `--impl reference` times the fp64 oracle on the host cores
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -240,6 +241,23 @@ def cpu_baseline_leg(w, t, target_s=12.0):
 
 
 # ---------------------------------------------------------------- GPU leg
+# DRAM bytes per launch of the main kernel (dram__bytes_read.sum +
+# dram__bytes_write.sum from one ncu capture, profiles/sdpa_bwd_main_traffic.md),
+# valid only for the kernel sources they were taken on: the digest covers the
+# main kernel's source files, and a changed kernel reports null.
+MAIN_SOURCES = ("sdpa_bwd_main.cu", "common.cuh", "ptx.cuh")
+MAIN_TRAFFIC = {
+    "5b8276b586c039a6": {"causal_mha": 112252928 + 29158144,
+                         "causal_gqa_det": 124103680 + 513449472},
+}
+
+
+def main_traffic(workload: str):
+    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "attention_backward_sdpa_gb300", "csrc")
+    blob = b"".join(open(os.path.join(csrc, f), "rb").read() for f in MAIN_SOURCES)
+    return MAIN_TRAFFIC.get(hashlib.sha256(blob).hexdigest()[:16], {}).get(workload)
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -330,7 +348,7 @@ def run_gpu(args, w, t, o, lse, rank, world, device):
     return {
         "value": value, "ms_per_step": ms_step, "flops": flops,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": achieved / peak_tf, "traffic": None,
+                     "frac": achieved / peak_tf, "traffic": main_traffic(w.name),
                      "kernel": "sdpa_bwd_main", "peak_kind": f"{peak_kind} bf16 burst",
                      "kernel_gflop": main_flops / 1e9},
         "kernel_ms": kernel_ms,
