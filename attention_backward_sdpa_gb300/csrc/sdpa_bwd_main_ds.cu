@@ -51,7 +51,9 @@ enum : int {
   BAR_DSFREE = 17,   // + slot: G4 done reading dS^T
   BAR_DSCOPIED = 19, // + slot: dS^T stored to the workspace
   BAR_MMADONE = 21,
-  NUM_BARS = 22
+  BAR_SREAD = 22,    // + slot, 128 arrivals: S^T in registers (G2 may overwrite it)
+  BAR_DPREAD = 24,   // + slot, 128 arrivals: dP^T in registers (G1 may overwrite it)
+  NUM_BARS = 26
 };
 
 template <int DQK, int DV>
@@ -128,7 +130,8 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
     *abort_flag = 0;
     for (int i = 0; i < NUM_BARS; ++i) {
       const bool threads128 = (i == BAR_PREADY || i == BAR_PREADY + 1 || i == BAR_DSREADY ||
-                               i == BAR_DSREADY + 1);
+                               i == BAR_DSREADY + 1 || i == BAR_SREAD || i == BAR_SREAD + 1 ||
+                               i == BAR_DPREAD || i == BAR_DPREAD + 1);
       mbar_init(&bars[i], threads128 ? 128 : 1);
     }
     fence_mbar_init();
@@ -208,8 +211,9 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
       for (int t = 0; t < n && ok; ++t) {
         const int s = t & 1, st = t % NST, j = t >> 1;
         if (!mbar_wait(&bars[BAR_QFULL + st], (t / NST) & 1, abort_flag, WAIT_LIMIT_NS)) break;
-        // Slot columns [0,64) hold dP^T of tile t-2 until its dS has been formed.
-        if (t >= 2 && !mbar_wait(&bars[BAR_DSREADY + s], (j - 1) & 1, abort_flag, WAIT_LIMIT_NS))
+        // Slot columns [0,64) hold dP^T of tile t-2 until the warpgroup has it
+        // in registers.
+        if (t >= 2 && !mbar_wait(&bars[BAR_DPREAD + s], (j - 1) & 1, abort_flag, WAIT_LIMIT_NS))
           break;
         __syncwarp();
         tc_fence_after();
@@ -230,8 +234,9 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
       for (int t = 0; t < n && ok; ++t) {
         const int s = t & 1, st = t % NST, j = t >> 1;
         if (!mbar_wait(&bars[BAR_QFULL + st], (t / NST) & 1, abort_flag, WAIT_LIMIT_NS)) break;
-        // dP^T overwrites S^T once the warpgroup has read it (P_READY).
-        if (!mbar_wait(&bars[BAR_PREADY + s], j & 1, abort_flag, WAIT_LIMIT_NS)) break;
+        // dP^T overwrites S^T once the warpgroup has it in registers (S_READ),
+        // so G2 runs while the softmax is computed.
+        if (!mbar_wait(&bars[BAR_SREAD + s], j & 1, abort_flag, WAIT_LIMIT_NS)) break;
         __syncwarp();
         tc_fence_after();
         if (elect_one()) {
@@ -333,10 +338,18 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
         tmem_ld32(t_lane + L::col_s(slot) + 32, rb);
         tmem_ld_wait(ra);
         tmem_ld_wait(rb);
+        tc_fence_before();
+        mbar_arrive(&bars[BAR_SREAD + slot]);  // the S^T columns may be overwritten
+        const float4* lse4 = reinterpret_cast<const float4*>(qs);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          P[i] = ex2_approx(fmaf(__uint_as_float(ra[i]), p.scale_log2, -qs[i]));
-          P[32 + i] = ex2_approx(fmaf(__uint_as_float(rb[i]), p.scale_log2, -qs[32 + i]));
+        for (int i4 = 0; i4 < BQ / 4; ++i4) {
+          const float4 l = lse4[i4];
+          const uint32_t* r = i4 < 8 ? ra : rb;
+          const int i = (i4 & 7) * 4;
+          P[i4 * 4 + 0] = ex2_approx(fmaf(__uint_as_float(r[i + 0]), p.scale_log2, -l.x));
+          P[i4 * 4 + 1] = ex2_approx(fmaf(__uint_as_float(r[i + 1]), p.scale_log2, -l.y));
+          P[i4 * 4 + 2] = ex2_approx(fmaf(__uint_as_float(r[i + 2]), p.scale_log2, -l.z));
+          P[i4 * 4 + 3] = ex2_approx(fmaf(__uint_as_float(r[i + 3]), p.scale_log2, -l.w));
         }
       }
       if (need_mask) {
@@ -369,23 +382,30 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
       }
       __syncwarp();
       tc_fence_after();
+      {
+        uint32_t ra[32], rb[32];
+        tmem_ld32(t_lane + L::col_s(slot), ra);
+        tmem_ld32(t_lane + L::col_s(slot) + 32, rb);
+        tmem_ld_wait(ra);
+        tmem_ld_wait(rb);
+        tc_fence_before();
+        mbar_arrive(&bars[BAR_DPREAD + slot]);  // the dP^T columns may be overwritten
+        const float4* delta4 = reinterpret_cast<const float4*>(qs + BQ);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t r[32];
-        tmem_ld32(t_lane + L::col_s(slot) + half * 32, r);
-        tmem_ld_wait(r);
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          uint32_t w[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int c = half * 32 + ch * 8 + 2 * i;
-            const float d0 = P[c] * (__uint_as_float(r[ch * 8 + 2 * i]) - qs[BQ + c]);
-            const float d1 = P[c + 1] * (__uint_as_float(r[ch * 8 + 2 * i + 1]) - qs[BQ + c + 1]);
-            w[i] = pack_bf16x2(d0, d1);
-          }
-          const int chunk = half * 4 + ch;
-          *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int chunk = 0; chunk < 8; ++chunk) {  // 8 queries = 16 bytes of dS^T per chunk
+          const uint32_t* r = chunk < 4 ? ra : rb;
+          const int i = (chunk & 3) * 8;
+          const float4 d0 = delta4[chunk * 2], d1 = delta4[chunk * 2 + 1];
+          const int c = chunk * 8;
+          const uint32_t w0 = pack_bf16x2(P[c + 0] * (__uint_as_float(r[i + 0]) - d0.x),
+                                          P[c + 1] * (__uint_as_float(r[i + 1]) - d0.y));
+          const uint32_t w1 = pack_bf16x2(P[c + 2] * (__uint_as_float(r[i + 2]) - d0.z),
+                                          P[c + 3] * (__uint_as_float(r[i + 3]) - d0.w));
+          const uint32_t w2 = pack_bf16x2(P[c + 4] * (__uint_as_float(r[i + 4]) - d1.x),
+                                          P[c + 5] * (__uint_as_float(r[i + 5]) - d1.y));
+          const uint32_t w3 = pack_bf16x2(P[c + 6] * (__uint_as_float(r[i + 6]) - d1.z),
+                                          P[c + 7] * (__uint_as_float(r[i + 7]) - d1.w));
+          *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (row & 7)) << 4)) = make_uint4(w0, w1, w2, w3);
         }
       }
       fence_proxy_async_smem();
