@@ -41,19 +41,21 @@ constexpr uint64_t WAIT_LIMIT_NS = 4000000000ull;
 
 enum : int {
   BAR_KV = 0,
-  BAR_QFULL = 1,     // + stage (up to 3)
-  BAR_QEMPTY = 4,    // + stage
-  BAR_SFULL = 7,     // + slot: S^T in tensor memory
-  BAR_PREADY = 9,    // + slot, 128 arrivals: S^T read, P^T written
-  BAR_DPFULL = 11,   // + slot: dP^T in tensor memory
-  BAR_SFREE = 13,    // + slot: G3 done reading P^T
-  BAR_DSREADY = 15,  // + slot, 128 arrivals: dP^T read, dS^T in shared memory
-  BAR_DSFREE = 17,   // + slot: G4 done reading dS^T
-  BAR_DSCOPIED = 19, // + slot: dS^T stored to the workspace
-  BAR_MMADONE = 21,
-  BAR_SREAD = 22,    // + slot, 128 arrivals: S^T in registers (G2 may overwrite it)
-  BAR_DPREAD = 24,   // + slot, 128 arrivals: dP^T in registers (G1 may overwrite it)
-  NUM_BARS = 26
+  BAR_QFULL = 1,     // + Q stage (up to 3): Q tile and row statistics landed
+  BAR_QEMPTY = 4,    // + Q stage: G4 done reading Q
+  BAR_DOFULL = 7,    // + dO stage (2)
+  BAR_DOEMPTY = 9,   // + dO stage, 2 arrivals: G2 and G3 done reading dO
+  BAR_SFULL = 11,    // + slot: S^T in tensor memory
+  BAR_PREADY = 13,   // + slot, 128 arrivals: P^T written
+  BAR_DPFULL = 15,   // + slot: dP^T in tensor memory
+  BAR_SFREE = 17,    // + slot: G3 done reading P^T
+  BAR_DSREADY = 19,  // + slot, 128 arrivals: dS^T in shared memory
+  BAR_DSFREE = 21,   // + slot: G4 done reading dS^T
+  BAR_DSCOPIED = 23, // + slot: dS^T stored to the workspace
+  BAR_MMADONE = 25,
+  BAR_SREAD = 26,    // + slot, 128 arrivals: S^T in registers (G2 may overwrite it)
+  BAR_DPREAD = 28,   // + slot, 128 arrivals: dP^T in registers (G1 may overwrite it)
+  NUM_BARS = 30
 };
 
 template <int DQK, int DV>
@@ -66,15 +68,19 @@ struct Layout {
   static constexpr int TILE_DO = BQ * DV * 2;
   static constexpr int TILE_DS = BN * BQ * 2;
   static constexpr int FIXED = TILE_K + TILE_V + 2 * TILE_DS;
-  static constexpr int PER_STAGE = TILE_Q + TILE_DO + QSTAT_FLOATS * 4;
-  static constexpr int NSTAGE = (FIXED + 3 * PER_STAGE + NUM_BARS * 8 + 64 <= 232448) ? 3 : 2;
+  // Q (with the row statistics) is held from G1 to G4, the whole tile, while
+  // dO is released by G3; so Q gets the deeper ring. Three Q stages cover the
+  // ~2000-cycle load latency at the tensor pipe's tile rate, two would not.
+  static constexpr int NDO = 2;
+  static constexpr int NQ =
+      (FIXED + 3 * (TILE_Q + QSTAT_FLOATS * 4) + NDO * TILE_DO + NUM_BARS * 8 + 64 <= 232448) ? 3 : 2;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + TILE_K;
   static constexpr int OFF_DS = OFF_V + TILE_V;
   static constexpr int OFF_Q = OFF_DS + 2 * TILE_DS;
-  static constexpr int OFF_DO = OFF_Q + NSTAGE * TILE_Q;
-  static constexpr int OFF_QS = OFF_DO + NSTAGE * TILE_DO;
-  static constexpr int OFF_BAR = OFF_QS + NSTAGE * QSTAT_FLOATS * 4;
+  static constexpr int OFF_DO = OFF_Q + NQ * TILE_Q;
+  static constexpr int OFF_QS = OFF_DO + NDO * TILE_DO;
+  static constexpr int OFF_BAR = OFF_QS + NQ * QSTAT_FLOATS * 4;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int BYTES = OFF_MISC + 64;
   static constexpr uint32_t COL_DV = 192, COL_DK = 192 + DV;
@@ -93,7 +99,7 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
     sdpa_bwd_main_ds(const __grid_constant__ MainMaps maps, const ChainParams p) {
   using namespace ds_kernel;
   using L = Layout<DQK, DV>;
-  constexpr int NST = L::NSTAGE;
+  constexpr int NQ = L::NQ, NDO = L::NDO;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if ((smem_u32(smem) & 1023u) != 0) {
@@ -132,7 +138,8 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
       const bool threads128 = (i == BAR_PREADY || i == BAR_PREADY + 1 || i == BAR_DSREADY ||
                                i == BAR_DSREADY + 1 || i == BAR_SREAD || i == BAR_SREAD + 1 ||
                                i == BAR_DPREAD || i == BAR_DPREAD + 1);
-      mbar_init(&bars[i], threads128 ? 128 : 1);
+      const bool two = (i == BAR_DOEMPTY || i == BAR_DOEMPTY + 1);
+      mbar_init(&bars[i], threads128 ? 128 : (two ? 2 : 1));
     }
     fence_mbar_init();
   }
@@ -184,20 +191,27 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
       for (int blk = 0; blk < DV / 64; ++blk)
         tma_load_3d(sV + blk * L::BLK_KV, &maps.v, &bars[BAR_KV], blk * 64, k0, b * p.Hkv + hk);
       pdl_wait_prior_grid();
+      // Q(t) waits for G4(t - NQ), dO(t) for G2 and G3 of tile t - NDO; G3(t - 2)
+      // is issued after G4(t - 3), so issuing Q(t) first never delays dO(t).
       for (int t = 0; t < n; ++t) {
-        const int st = t % NST;
-        if (t >= NST &&
-            !mbar_wait(&bars[BAR_QEMPTY + st], ((t / NST) - 1) & 1, abort_flag, WAIT_LIMIT_NS))
-          break;
+        const int sq = t % NQ, sd = t % NDO;
         const int qt = qt_hi - t;
-        uint64_t* full = &bars[BAR_QFULL + st];
-        mbar_arrive_expect_tx(full, L::TILE_Q + L::TILE_DO + QSTAT_FLOATS * 4);
+        if (t >= NQ &&
+            !mbar_wait(&bars[BAR_QEMPTY + sq], ((t / NQ) - 1) & 1, abort_flag, WAIT_LIMIT_NS))
+          break;
+        uint64_t* qfull = &bars[BAR_QFULL + sq];
+        mbar_arrive_expect_tx(qfull, L::TILE_Q + QSTAT_FLOATS * 4);
         for (int blk = 0; blk < DQK / 64; ++blk)
-          tma_load_3d(sQ + st * L::TILE_Q + blk * L::BLK_Q, &maps.q, full, blk * 64, qt * BQ, bh);
+          tma_load_3d(sQ + sq * L::TILE_Q + blk * L::BLK_Q, &maps.q, qfull, blk * 64, qt * BQ, bh);
+        bulk_load(sQS + sq * QSTAT_FLOATS, p.qstat + ((long long)bh * p.n_qt + qt) * QSTAT_FLOATS,
+                  QSTAT_FLOATS * 4, qfull);
+        if (t >= NDO &&
+            !mbar_wait(&bars[BAR_DOEMPTY + sd], ((t / NDO) - 1) & 1, abort_flag, WAIT_LIMIT_NS))
+          break;
+        uint64_t* dofull = &bars[BAR_DOFULL + sd];
+        mbar_arrive_expect_tx(dofull, L::TILE_DO);
         for (int blk = 0; blk < DV / 64; ++blk)
-          tma_load_3d(sDO + st * L::TILE_DO + blk * L::BLK_Q, &maps.d_o, full, blk * 64, qt * BQ, bh);
-        bulk_load(sQS + st * QSTAT_FLOATS, p.qstat + ((long long)bh * p.n_qt + qt) * QSTAT_FLOATS,
-                  QSTAT_FLOATS * 4, full);
+          tma_load_3d(sDO + sd * L::TILE_DO + blk * L::BLK_Q, &maps.d_o, dofull, blk * 64, qt * BQ, bh);
       }
     }
   } else if (warp >= 9 && warp <= 11) {
@@ -209,8 +223,8 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
     bool ok = n > 0 && mbar_wait(&bars[BAR_KV], 0, abort_flag, WAIT_LIMIT_NS);
     if (warp == 9) {
       for (int t = 0; t < n && ok; ++t) {
-        const int s = t & 1, st = t % NST, j = t >> 1;
-        if (!mbar_wait(&bars[BAR_QFULL + st], (t / NST) & 1, abort_flag, WAIT_LIMIT_NS)) break;
+        const int s = t & 1, st = t % NQ, j = t >> 1;
+        if (!mbar_wait(&bars[BAR_QFULL + st], (t / NQ) & 1, abort_flag, WAIT_LIMIT_NS)) break;
         // Slot columns [0,64) hold dP^T of tile t-2 until the warpgroup has it
         // in registers.
         if (t >= 2 && !mbar_wait(&bars[BAR_DPREAD + s], (j - 1) & 1, abort_flag, WAIT_LIMIT_NS))
@@ -232,8 +246,8 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
       }
     } else if (warp == 11) {
       for (int t = 0; t < n && ok; ++t) {
-        const int s = t & 1, st = t % NST, j = t >> 1;
-        if (!mbar_wait(&bars[BAR_QFULL + st], (t / NST) & 1, abort_flag, WAIT_LIMIT_NS)) break;
+        const int s = t & 1, st = t % NDO, j = t >> 1;
+        if (!mbar_wait(&bars[BAR_DOFULL + st], (t / NDO) & 1, abort_flag, WAIT_LIMIT_NS)) break;
         // dP^T overwrites S^T once the warpgroup has it in registers (S_READ),
         // so G2 runs while the softmax is computed.
         if (!mbar_wait(&bars[BAR_SREAD + s], j & 1, abort_flag, WAIT_LIMIT_NS)) break;
@@ -249,22 +263,26 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
                    k > 0);
           }
           mma_commit(&bars[BAR_DPFULL + s]);
+          if (t + NDO < n) mma_commit(&bars[BAR_DOEMPTY + st]);  // G2's share of the release
         }
         __syncwarp();
       }
     } else {
       for (int u = 0; u < n && ok; ++u) {
-        const int su = u & 1, stu = u % NST, ju = u >> 1;
+        const int su = u & 1, sdu = u % NDO, squ = u % NQ, ju = u >> 1;
         if (!mbar_wait(&bars[BAR_PREADY + su], ju & 1, abort_flag, WAIT_LIMIT_NS)) break;
+        // G3 reads dO(u) too; only the G2 issuer has waited for it so far.
+        if (!mbar_wait(&bars[BAR_DOFULL + sdu], (u / NDO) & 1, abort_flag, WAIT_LIMIT_NS)) break;
         __syncwarp();
         tc_fence_after();
         if (elect_one()) {
           // G3: dV[key, d] += sum_q P^T[key, q] dO[q, d]
-          const uint32_t aDO = smem_u32(sDO + stu * L::TILE_DO);
+          const uint32_t aDO = smem_u32(sDO + sdu * L::TILE_DO);
 #pragma unroll
           for (int k = 0; k < BQ / 16; ++k)
             mma_ts(tmem + L::COL_DV, tmem + L::col_p(su) + 8 * k, sdesc_at(T_MN_Q, aDO + k * 2048),
                    ID_G3, (u > 0 || k > 0));
+          if (u + NDO < n) mma_commit(&bars[BAR_DOEMPTY + sdu]);  // G3's share
           mma_commit(&bars[BAR_SFREE + su]);
         }
         __syncwarp();
@@ -273,13 +291,13 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
         tc_fence_after();
         if (elect_one()) {
           // G4: dK[key, d] += sum_q dS^T[key, q] Q[q, d]
-          const uint32_t aQ = smem_u32(sQ + stu * L::TILE_Q);
+          const uint32_t aQ = smem_u32(sQ + squ * L::TILE_Q);
           const uint32_t aDS = smem_u32(sDS + su * L::TILE_DS);
 #pragma unroll
           for (int k = 0; k < BQ / 16; ++k)
             mma_ss(tmem + L::COL_DK, sdesc_at(T_KMAJ, aDS + k * 32), sdesc_at(T_MN_Q, aQ + k * 2048),
                    ID_G4, (u > 0 || k > 0));
-          if (u + NST < n) mma_commit(&bars[BAR_QEMPTY + stu]);
+          if (u + NQ < n) mma_commit(&bars[BAR_QEMPTY + squ]);
           mma_commit(&bars[BAR_DSFREE + su]);
         }
         __syncwarp();
@@ -322,13 +340,13 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
     float P[BQ];
     bool ok = true;
     for (int t = slot; t < n && ok; t += 2) {
-      const int j = t >> 1, st = t % NST;
+      const int j = t >> 1, st = t % NQ;
       const int qt = qt_hi - t, q0 = qt * BQ;
       const float* qs = sQS + st * QSTAT_FLOATS;
       const bool need_mask = (k0 + BN > Lk) ||
                              (p.causal && (long long)q0 < (long long)(k0 + BN - 1) - diag - Rp) ||
                              (has_window && (long long)(q0 + BQ - 1) > (long long)k0 - diag + p.window_left);
-      if (!mbar_wait(&bars[BAR_QFULL + st], (t / NST) & 1, abort_flag, WAIT_LIMIT_NS) ||
+      if (!mbar_wait(&bars[BAR_QFULL + st], (t / NQ) & 1, abort_flag, WAIT_LIMIT_NS) ||
           !mbar_wait(&bars[BAR_SFULL + slot], j & 1, abort_flag, WAIT_LIMIT_NS)) { ok = false; break; }
       __syncwarp();
       tc_fence_after();
@@ -427,8 +445,8 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
     const uint32_t col0 = slot ? L::COL_DK : L::COL_DV;
     const float mult = slot ? p.scale : 1.f;
     uint8_t* stg = slot ? sQ : sDO;
-    static_assert(L::NSTAGE * L::TILE_Q >= DQK / 64 * L::BLK_KV &&
-                      L::NSTAGE * L::TILE_DO >= DV / 64 * L::BLK_KV,
+    static_assert(L::NQ * L::TILE_Q >= DQK / 64 * L::BLK_KV &&
+                      L::NDO * L::TILE_DO >= DV / 64 * L::BLK_KV,
                   "staging fits in the stage rings");
     for (int c32 = 0; c32 < D / 32; ++c32) {
       uint32_t r[32];
@@ -477,20 +495,14 @@ static cudaError_t set_ds_smem() {
                               ds_kernel::Layout<DQK, DV>::BYTES);
 }
 
-cudaError_t main_ds_kernel_setup() {
-  cudaError_t e = set_ds_smem<192, 128>();
-  if (e == cudaSuccess) e = set_ds_smem<128, 128>();
-  return e;
-}
+cudaError_t main_ds_kernel_setup() { return set_ds_smem<192, 128>(); }
 
 cudaError_t launch_main_ds(const MainMaps& maps, const ChainParams& p, cudaStream_t s) {
   const dim3 grid((unsigned)(p.n_kt * p.B * p.Hq));
   const dim3 block(ds_kernel::THREADS);
-  if (p.Dqk == 192)
-    return launch_kernel(sdpa_bwd_main_ds<192, 128>, grid, block, ds_kernel::Layout<192, 128>::BYTES,
-                         s, true, maps, p);
-  return launch_kernel(sdpa_bwd_main_ds<128, 128>, grid, block, ds_kernel::Layout<128, 128>::BYTES, s,
-                       true, maps, p);
+  if (p.Dqk != 192 || p.Dv != 128) return cudaErrorInvalidValue;
+  return launch_kernel(sdpa_bwd_main_ds<192, 128>, grid, block, ds_kernel::Layout<192, 128>::BYTES,
+                       s, true, maps, p);
 }
 
 }  // namespace sdpa
