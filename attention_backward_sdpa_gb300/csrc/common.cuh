@@ -149,6 +149,55 @@ __device__ inline void batch_lengths(const ChainParams& p, int b, int& Lq, int& 
 // that no query sees: such keys have exactly zero gradient, and the outputs are
 // overwritten in full. Called by every thread of a CTA; 16-byte stores,
 // consecutive threads on consecutive addresses.
+// Key tiles that no query of their batch row sees (padding, windows) only have
+// zero gradients. On the non-deterministic launch their CTAs leave at once and
+// the head group's other CTAs write those rows with an otherwise idle warp:
+// the r-th key tile with a visible query (ascending) takes the tiles with none
+// whose index among them is r modulo the number of visible ones. Every batch
+// row with at least one query and one key has a visible pair (the diagonal
+// q + diag is inside the causal band and the window), so only a row with no
+// query or no key leaves its CTAs to zero their own rows.
+__device__ inline bool row_has_visible_pair(int Lq, int Lk) { return Lq > 0 && Lk > 0; }
+
+// One warp: zeroes the dK/dV rows of this CTA's share of the empty key tiles of
+// its head group (dK/dV destination `head`), classifying tiles with the same
+// visited_query_tiles() that every kernel walks.
+template <int DQK, int DV>
+__device__ void zero_group_share_of_empty_key_tiles(const ChainParams& p, long long head, int kt_self,
+                                                    int Lq, int Lk, int lane) {
+  int rank = 0, n_vis = 0;
+  for (int base = 0; base < p.n_kt; base += 32) {
+    const int kt = base + lane;
+    int lo = 0, hi = -1;
+    if (kt < p.n_kt)
+      visited_query_tiles(kt, Lq, Lk, p.causal, p.bottom_right, p.window_left, p.window_right, lo, hi);
+    const unsigned vis = __ballot_sync(0xffffffffu, kt < p.n_kt && hi >= lo);
+    if (kt_self >= base && kt_self < base + 32) rank = n_vis + __popc(vis & ((1u << (kt_self - base)) - 1u));
+    n_vis += __popc(vis);
+  }
+  if (n_vis == 0) return;
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  int j = 0;  // index among the empty tiles
+  for (int base = 0; base < p.n_kt; base += 32) {
+    const int kt = base + lane;
+    int lo = 0, hi = -1;
+    if (kt < p.n_kt)
+      visited_query_tiles(kt, Lq, Lk, p.causal, p.bottom_right, p.window_left, p.window_right, lo, hi);
+    unsigned empty = __ballot_sync(0xffffffffu, kt < p.n_kt && hi < lo);
+    while (empty != 0u) {
+      const int e = base + __ffs(empty) - 1;
+      empty &= empty - 1u;
+      if (j++ % n_vis != rank) continue;
+      const int k0 = e * BN;
+      const int rows = min(BN, p.Skv - k0);
+      uint4* dk = reinterpret_cast<uint4*>((p.dk_ws ? p.dk_ws : p.dk) + (head * p.Skv + k0) * DQK);
+      uint4* dv = reinterpret_cast<uint4*>((p.dv_ws ? p.dv_ws : p.dv) + (head * p.Skv + k0) * DV);
+      for (int i = lane; i < rows * (DQK / 8); i += 32) dk[i] = z;
+      for (int i = lane; i < rows * (DV / 8); i += 32) dv[i] = z;
+    }
+  }
+}
+
 template <int DQK, int DV>
 __device__ inline void zero_key_tile_rows(const ChainParams& p, long long head, int k0) {
   const int rows = min(BN, p.Skv - k0);

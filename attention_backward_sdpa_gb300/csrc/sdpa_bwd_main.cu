@@ -125,8 +125,9 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
     return;
   }
   if (!p.deterministic) {
-    // A key tile that no query sees only has zero gradients: write them and
-    // leave before any barrier or tensor-memory setup.
+    // A key tile that no query sees only has zero gradients. Its rows are
+    // written by an idle warp of the group's other CTAs (or here, when the
+    // batch row has no query or no key); leave before any setup.
     const int NG0 = p.B * p.Hkv * p.n_part;
     const int kt0 = blockIdx.x / NG0, gi0 = blockIdx.x % NG0, b0 = gi0 / (p.Hkv * p.n_part);
     int Lq0, Lk0, lo0, hi0;
@@ -134,7 +135,8 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
     visited_query_tiles(kt0, Lq0, Lk0, p.causal, p.bottom_right, p.window_left, p.window_right, lo0,
                         hi0);
     if (hi0 < lo0) {
-      zero_key_tile_rows<D, D>(p, p.dk_ws ? (long long)gi0 : (long long)(gi0 / p.n_part), kt0 * BN);
+      if (!row_has_visible_pair(Lq0, Lk0))
+        zero_key_tile_rows<D, D>(p, p.dk_ws ? (long long)gi0 : (long long)(gi0 / p.n_part), kt0 * BN);
       return;
     }
   }
@@ -351,6 +353,9 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
         if (n > 0 && elect_one()) mma_commit(&bars[BAR_MMADONE]);
         __syncwarp();
       }
+    } else if (!DS_OUT && warp == 15) {
+      // Idle on this route: this CTA's share of the group's empty key tiles.
+      if (!p.deterministic) zero_group_share_of_empty_key_tiles<D, D>(p, out_head, kt, Lq, Lk, lane);
     } else if (DS_OUT && warp == 15) {
       // ------------------------------------------------------------ dS^T store
       // Two-kernel route: once a tile's dS^T is in shared memory, one thread
@@ -374,6 +379,10 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
   } else if (warp >= 8) {
     // ------------------------------------------------------------ dQ warpgroup
     regs_decrease<REGS_DQ>();
+    // Idle on the two-kernel route: warp 9 writes this CTA's share of the
+    // group's empty key tiles.
+    if (DS_OUT && warp == 9 && !p.deterministic)
+      zero_group_share_of_empty_key_tiles<D, D>(p, out_head, kt, Lq, Lk, lane);
     pdl_wait_prior_grid();
     const int quarter = warp & 3;
     const int d = quarter * 32 + lane;                 // dQ^T lane = head-dim column

@@ -117,8 +117,9 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
 
   {
-    // A key tile that no query sees only has zero gradients: write them and
-    // leave before any barrier or tensor-memory setup.
+    // A key tile that no query sees only has zero gradients. Its rows are
+    // written by an idle warp of the head's other CTAs (or here, when the
+    // batch row has no query or no key); leave before any setup.
     const int BH0 = p.B * p.Hq;
     const int kt0 = blockIdx.x / BH0, bh0 = blockIdx.x % BH0, b0 = bh0 / p.Hq;
     int Lq0, Lk0, lo0, hi0;
@@ -127,8 +128,9 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
                         hi0);
     if (hi0 < lo0) {
       // gsz = 1: the partial set of a query head is its bh index.
-      zero_key_tile_rows<DQK, DV>(p, p.dk_ws ? (long long)bh0 : (long long)b0 * p.Hkv + (bh0 % p.Hq) / p.G,
-                                  kt0 * BN);
+      if (!row_has_visible_pair(Lq0, Lk0))
+        zero_key_tile_rows<DQK, DV>(p, p.dk_ws ? (long long)bh0 : (long long)b0 * p.Hkv + (bh0 % p.Hq) / p.G,
+                                    kt0 * BN);
       return;
     }
   }
@@ -323,7 +325,12 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
       }
       bulk_wait_group_read0();
     }
-  }  // warps 13-15: idle members of the fourth warpgroup
+  } else if (warp == 13) {
+    // This CTA's share of the head's empty key tiles (gsz = 1: the partial
+    // set of a query head is its bh index).
+    zero_group_share_of_empty_key_tiles<DQK, DV>(p, p.dk_ws ? (long long)bh : (long long)b * p.Hkv + hk,
+                                                 kt, Lq, Lk, lane);
+  }  // warps 14-15: idle members of the fourth warpgroup
   } else {
     regs_increase<ds_kernel::REGS_COMPUTE>();
     // ------------------------------------------------------------ compute warpgroups
