@@ -90,6 +90,8 @@ def _load():
         C = ctypes.POINTER(_Cfg)
         I64 = ctypes.POINTER(ctypes.c_int64)
         lib.oracle_forward.argtypes = [C, P, P, P, P, P]
+        lib.oracle_forward_sink.argtypes = [C, P, P, P, P, P, P]
+        lib.oracle_dsink.argtypes = [C, P, P, P, P]
         lib.oracle_delta.argtypes = [C, P, P, P]
         lib.oracle_backward.argtypes = [C, P, P, P, P, P, P, P, P, P]
         lib.oracle_backward_sampled.argtypes = [C, P, P, P, P, P, P, ctypes.c_long, I64, P,
@@ -118,8 +120,9 @@ def _check_heads(p: Problem):
         raise ValueError("H_kv must divide H_q")
 
 
-def forward(p: Problem, q, k, v):
-    """Returns (O, LSE) in float64; LSE is the natural-log row log-sum-exp."""
+def forward(p: Problem, q, k, v, sink=None):
+    """Returns (O, LSE) in float64; LSE is the natural-log row log-sum-exp.
+    ``sink`` (H_q,) adds a per-head sink logit to every row's denominator."""
     _check_heads(p)
     lib = _load()
     q = _f64(q, (p.B, p.Hq, p.Sq, p.Dqk))
@@ -128,8 +131,24 @@ def forward(p: Problem, q, k, v):
     o = np.zeros((p.B, p.Hq, p.Sq, p.Dv))
     lse = np.zeros((p.B, p.Hq, p.Sq))
     s, keep = p._struct()
-    lib.oracle_forward(ctypes.byref(s), _p(q), _p(k), _p(v), _p(o), _p(lse))
+    if sink is None:
+        lib.oracle_forward(ctypes.byref(s), _p(q), _p(k), _p(v), _p(o), _p(lse))
+    else:
+        sk = _f64(sink, (p.Hq,))
+        lib.oracle_forward_sink(ctypes.byref(s), _p(q), _p(k), _p(v), _p(sk), _p(o), _p(lse))
     return o, lse
+
+
+def dsink(p: Problem, sink, lse, delta_):
+    """dsink[h] = -sum_{b, q < L_q} exp(sink[h] - LSE[b,h,q]) * delta[b,h,q], shape (H_q,)."""
+    lib = _load()
+    sk = _f64(sink, (p.Hq,))
+    lse = _f64(lse, (p.B, p.Hq, p.Sq))
+    dl = _f64(delta_, (p.B, p.Hq, p.Sq))
+    out = np.zeros(p.Hq)
+    s, keep = p._struct()
+    lib.oracle_dsink(ctypes.byref(s), _p(sk), _p(lse), _p(dl), _p(out))
+    return out
 
 
 def delta(p: Problem, o, do):

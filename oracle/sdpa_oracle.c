@@ -21,6 +21,11 @@
  *     k <= q + diag + R; a left window masks k < q + diag - W; keys at or past
  *     seq_kv_lens[b] and queries at or past seq_q_lens[b] are masked; a row
  *     with no visible key has LSE = -inf and gets P = 0 (not NaN).
+ *   - Sink tokens (Capabilities list and the `dsink` step of the kernel
+ *     chain): a per-query-head sink logit joins every row's softmax
+ *     denominator without a value row, so the forward LSE includes it and
+ *     dQ/dK/dV keep their formulas; the extra output is
+ *     dsink[h] = -sum_{b,q} exp(sink[h] - LSE[b,h,q]) * delta[b,h,q].
  *
  * Every quantity is computed straight from its definition, one output row at
  * a time, in double precision. There is no tiling, fusion or reordering.
@@ -110,10 +115,13 @@ long long oracle_count_visible(const oracle_cfg *c) {
     return total;
 }
 
-/* Forward: LSE_q = log sum_{visible k} exp(s_qk), s_qk = scale * Q_q . K_k;
- * O_q = sum_k exp(s_qk - LSE_q) V_k. An empty row gives LSE = -inf, O = 0. */
-void oracle_forward(const oracle_cfg *c, const double *Q, const double *K, const double *V,
-                    double *O, double *LSE) {
+/* Forward: LSE_q = log( sum_{visible k} exp(s_qk) [+ exp(sink_h)] ),
+ * s_qk = scale * Q_q . K_k; O_q = sum_k exp(s_qk - LSE_q) V_k (the sink has no
+ * value row). Without a sink an empty row gives LSE = -inf, O = 0; with one it
+ * gives LSE = sink_h, O = 0. Rows at or past seq_q_lens[b] are empty rows.
+ * `sink` is (H_q,) or NULL. */
+void oracle_forward_sink(const oracle_cfg *c, const double *Q, const double *K, const double *V,
+                         const double *sink, double *O, double *LSE) {
     const int G = c->Hq / c->Hkv;
     const long rows = (long)c->B * c->Hq * c->Sq;
 #pragma omp parallel
@@ -128,7 +136,8 @@ void oracle_forward(const oracle_cfg *c, const double *Q, const double *K, const
             lengths(c, b, &Lq, &Lk);
             const double *qr = row_of(Q, bh, q, c->Sq, c->Dqk);
             double *orow = O + r * c->Dv;
-            double m = -INFINITY;
+            const double sk = sink ? sink[h] : -INFINITY;
+            double m = sk;
             for (long k = 0; k < c->Skv; ++k) {
                 if (!visible(c, Lq, Lk, q, k)) continue;
                 s[k] = c->scale * dot(qr, row_of(K, bhk, k, c->Skv, c->Dqk), c->Dqk);
@@ -136,7 +145,7 @@ void oracle_forward(const oracle_cfg *c, const double *Q, const double *K, const
             }
             for (int d = 0; d < c->Dv; ++d) orow[d] = 0.0;
             if (m == -INFINITY) { LSE[r] = -INFINITY; continue; }
-            double l = 0.0;
+            double l = sink ? exp(sk - m) : 0.0;
             for (long k = 0; k < c->Skv; ++k)
                 if (visible(c, Lq, Lk, q, k)) l += exp(s[k] - m);
             double lse = m + log(l);
@@ -149,6 +158,32 @@ void oracle_forward(const oracle_cfg *c, const double *Q, const double *K, const
             }
         }
         free(s);
+    }
+}
+
+void oracle_forward(const oracle_cfg *c, const double *Q, const double *K, const double *V,
+                    double *O, double *LSE) {
+    oracle_forward_sink(c, Q, K, V, NULL, O, LSE);
+}
+
+/* dsink[h] = -sum over b and query rows q < L_q of P_sink * delta, with
+ * P_sink = exp(sink[h] - LSE[b,h,q]) (0 when LSE = -inf, as for P). Summed in
+ * ascending (b, q) order in double precision. */
+void oracle_dsink(const oracle_cfg *c, const double *sink, const double *LSE, const double *delta,
+                  double *dsink) {
+    for (int h = 0; h < c->Hq; ++h) {
+        double acc = 0.0;
+        for (int b = 0; b < c->B; ++b) {
+            int Lq, Lk;
+            lengths(c, b, &Lq, &Lk);
+            const long bh = (long)b * c->Hq + h;
+            for (long q = 0; q < Lq; ++q) {
+                const double lse = LSE[bh * c->Sq + q];
+                if (lse == -INFINITY) continue;
+                acc += exp(sink[h] - lse) * delta[bh * c->Sq + q];
+            }
+        }
+        dsink[h] = -acc;
     }
 }
 

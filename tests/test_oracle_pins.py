@@ -307,3 +307,94 @@ def test_negative_infinite_lse_gives_zero_probability(oracle_mod):
     # with dO zeroed the row still has P != 0 but dP = 0 and delta = 0, so dS = 0 and P*dO = 0
     np.testing.assert_allclose(dk, dk_ref, atol=1e-13)
     np.testing.assert_allclose(dv, dv_ref, atol=1e-13)
+
+
+# ---------------------------------------------------------------- sink tokens
+# A per-query-head sink logit joins every row's softmax denominator without a
+# value row ("SDPA Backward (SM120)", Capabilities: sink tokens; kernel chain
+# step `dsink`). The pins below fix the oracle's sink forward and dsink to
+# central differences of L = sum(O * dO), to the no-sink limit and to a closed
+# form, none of which the oracle computes that way.
+SINK_CASES = ["dense", "causal_br_long_kv", "padded", "gqa", "window_causal"]
+
+
+def _sink(p, seed):
+    return np.random.default_rng(seed).standard_normal(p.Hq) * 0.8
+
+
+@pytest.mark.parametrize("name", SINK_CASES)
+def test_dsink_matches_central_differences(oracle_mod, name):
+    p = FD_CASES[name]
+    q, k, v, do = _inputs(p, seed=11)
+    sink = _sink(p, 12)
+    o, lse = oracle_mod.forward(p, q, k, v, sink)
+    ds = oracle_mod.dsink(p, sink, lse, oracle_mod.delta(p, o, do))
+    h = 1e-6
+    fd = np.zeros(p.Hq)
+    for i in range(p.Hq):
+        sp, sm = sink.copy(), sink.copy()
+        sp[i] += h
+        sm[i] -= h
+        op, _ = oracle_mod.forward(p, q, k, v, sp)
+        om, _ = oracle_mod.forward(p, q, k, v, sm)
+        fd[i] = float(np.sum((op - om) * do)) / (2 * h)
+    np.testing.assert_allclose(ds, fd, rtol=0, atol=2e-7 * max(1.0, np.abs(fd).max()))
+
+
+@pytest.mark.parametrize("name", ["causal_br_long_kv", "padded", "gqa"])
+def test_sink_backward_matches_central_differences(oracle_mod, name):
+    """With a sink the forward's LSE carries it, and dQ/dK/dV from the same
+    formulas still match central differences of L = sum(O * dO)."""
+    p = FD_CASES[name]
+    q, k, v, do = _inputs(p, seed=13)
+    sink = _sink(p, 14)
+    o, lse = oracle_mod.forward(p, q, k, v, sink)
+    dq, dk, dv = oracle_mod.backward(p, q, k, v, o, do, lse)
+    h = 1e-6
+    for tensor, grad, which in ((q, dq, "q"), (k, dk, "k"), (v, dv, "v")):
+        fd = np.zeros_like(tensor)
+        it = np.nditer(tensor, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            args = {"q": q, "k": k, "v": v}
+            for sgn in (1, -1):
+                t = tensor.copy()
+                t[idx] += sgn * h
+                args[which] = t
+                o2, _ = oracle_mod.forward(p, args["q"], args["k"], args["v"], sink)
+                fd[idx] += sgn * float(np.sum(o2 * do)) / (2 * h)
+        np.testing.assert_allclose(grad, fd, rtol=0, atol=2e-7 * max(1.0, float(np.abs(fd).max())),
+                                   err_msg=f"d{which}")
+
+
+def test_sink_at_minus_infinity_is_no_sink(oracle_mod):
+    p = FD_CASES["padded"]
+    q, k, v, do = _inputs(p, seed=15)
+    o0, lse0 = oracle_mod.forward(p, q, k, v)
+    sink = np.full(p.Hq, -np.inf)
+    o1, lse1 = oracle_mod.forward(p, q, k, v, sink)
+    np.testing.assert_array_equal(o1, o0)
+    np.testing.assert_array_equal(lse1, lse0)
+    assert np.all(oracle_mod.dsink(p, sink, lse1, oracle_mod.delta(p, o1, do)) == 0.0)
+
+
+def test_sink_single_key_closed_form(oracle_mod):
+    """One key with score s and a sink logit c: LSE = log(e^s + e^c),
+    O = V / (1 + e^(c - s)), and with delta = dO . O,
+    dsink = -sum_q e^(c - LSE_q) delta_q."""
+    p = Problem(1, 1, 1, 3, 1, 2, 2, scale=1.0)
+    q = np.array([[[[0.5, -1.0], [2.0, 0.25], [-0.75, 0.0]]]])
+    k = np.array([[[[1.0, 0.5]]]])
+    v = np.array([[[[2.0, -3.0]]]])
+    do = np.array([[[[1.0, 0.5], [-2.0, 1.5], [0.25, 0.25]]]])
+    c = 0.4
+    o, lse = oracle_mod.forward(p, q, k, v, np.array([c]))
+    ds = oracle_mod.dsink(p, np.array([c]), lse, oracle_mod.delta(p, o, do))
+    want_ds = 0.0
+    for i in range(3):
+        s = float(q[0, 0, i] @ k[0, 0, 0])
+        assert abs(lse[0, 0, i] - math.log(math.exp(s) + math.exp(c))) < 1e-14
+        w = 1.0 / (1.0 + math.exp(c - s))
+        np.testing.assert_allclose(o[0, 0, i], w * v[0, 0, 0], atol=1e-15)
+        want_ds -= (1.0 - w) * float(w * v[0, 0, 0] @ do[0, 0, i])
+    assert abs(ds[0] - want_ds) < 1e-14
