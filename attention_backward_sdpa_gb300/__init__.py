@@ -57,6 +57,8 @@ def load(build_if_missing: bool = False):
     lib.sdpa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, ctypes.c_float,
                              i, i, i, i, i, vp, vp, vp, sz, vp]
     lib.sdpa_bwd.restype = i
+    lib.sdpa_bwd_sink.argtypes = list(lib.sdpa_bwd.argtypes[:-1]) + [vp, vp, vp]
+    lib.sdpa_bwd_sink.restype = i
     lib.sdpa_bwd_workspace_size.argtypes = [i, i, i, i, i, i, i, i]
     lib.sdpa_bwd_workspace_size.restype = sz
     lib.sdpa_status_string.argtypes = [i]
@@ -107,13 +109,16 @@ def sdpa_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
              deterministic: bool = False, seq_q_lens: Optional[torch.Tensor] = None,
              seq_kv_lens: Optional[torch.Tensor] = None, dq: Optional[torch.Tensor] = None,
              dk: Optional[torch.Tensor] = None, dv: Optional[torch.Tensor] = None,
-             workspace: Optional[torch.Tensor] = None,
-             stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+             workspace: Optional[torch.Tensor] = None, sink: Optional[torch.Tensor] = None,
+             dsink: Optional[torch.Tensor] = None,
+             stream: Optional[torch.cuda.Stream] = None):
     """dQ, dK, dV of scaled-dot-product attention (see include/sdpa_bwd.h).
 
     q (B,Hq,Sq,Dqk), k (B,Hkv,Skv,Dqk), v (B,Hkv,Skv,Dv), o/do (B,Hq,Sq,Dv): bf16 CUDA,
     contiguous. lse (B,Hq,Sq) fp32 natural-log forward statistic. Lengths: int32 (B,) CUDA.
     Outputs are allocated when not given. Runs on ``stream`` (default: current stream).
+    With ``sink`` (fp32 (Hq,) CUDA sink logits, already folded into ``lse`` by the
+    forward) the call goes through sdpa_bwd_sink and returns (dq, dk, dv, dsink).
     """
     lib = load()
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
@@ -145,13 +150,26 @@ def sdpa_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
             raise ValueError("workspace must be a contiguous CUDA tensor")
         ws_bytes = workspace.numel() * workspace.element_size()
     sc = 0.0 if scale is None else float(scale)
-    rc = lib.sdpa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
-                      _ptr(dv), B, Hq, Hkv, Sq, Skv, Dqk, Dv, sc, int(causal), int(bottom_right),
-                      int(window_left), int(window_right), int(deterministic), _ptr(seq_q_lens),
-                      _ptr(seq_kv_lens), _ptr(workspace), ws_bytes, _stream_handle(stream))
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
+            _ptr(dv), B, Hq, Hkv, Sq, Skv, Dqk, Dv, sc, int(causal), int(bottom_right),
+            int(window_left), int(window_right), int(deterministic), _ptr(seq_q_lens),
+            _ptr(seq_kv_lens), _ptr(workspace), ws_bytes)
+    if sink is None:
+        rc = lib.sdpa_bwd(*args, _stream_handle(stream))
+        if rc != 0:
+            raise SdpaError(rc, "sdpa_bwd")
+        return dq, dk, dv
+    if sink.dtype != torch.float32 or not sink.is_cuda or not sink.is_contiguous() \
+            or sink.numel() != Hq:
+        raise ValueError("sink must be a contiguous fp32 CUDA tensor of Hq elements")
+    dsink = torch.empty_like(sink) if dsink is None else dsink
+    if dsink.dtype != torch.float32 or not dsink.is_cuda or not dsink.is_contiguous() \
+            or dsink.numel() != Hq:
+        raise ValueError("dsink must be a contiguous fp32 CUDA tensor of Hq elements")
+    rc = lib.sdpa_bwd_sink(*args, _ptr(sink), _ptr(dsink), _stream_handle(stream))
     if rc != 0:
-        raise SdpaError(rc, "sdpa_bwd")
-    return dq, dk, dv
+        raise SdpaError(rc, "sdpa_bwd_sink")
+    return dq, dk, dv, dsink
 
 
 def check_device_status(stream: Optional[torch.cuda.Stream] = None) -> None:

@@ -57,6 +57,12 @@ struct ChainParams {
   __nv_bfloat16* dv_ws; // n_part > 1: [B][Hkv][n_part][Skv][Dv]
   int n_counters;       // B*Hq*n_qt + 1 (counters plus ticket)
 
+  // Sink tokens (optional): the forward's LSE already folds the sink logits in,
+  // so dQ/dK/dV need nothing; dsink[h] = -sum_{b,q} exp(sink[h] - LSE) * delta.
+  const float* sink;    // (Hq,) sink logits, or null
+  float* dsink;         // (Hq,) output, or null
+  float* dsink_part;    // [B*Hq][n_qt] per-tile partial sums (fixed order within a tile)
+
   // Deterministic two-kernel route: the main kernel stores each bf16 dS^T tile
   // (its swizzled shared-memory image, DS_TILE_BYTES) at
   // ds_ws + ((bh * n_kt + kt) * n_qt + qt) * DS_TILE_BYTES, and the dQ kernel
@@ -106,6 +112,7 @@ struct MainMaps {
 cudaError_t launch_preprocess(const ChainParams& p, cudaStream_t s);
 cudaError_t launch_main(const MainMaps& maps, const ChainParams& p, cudaStream_t s);
 cudaError_t launch_dq_convert(const ChainParams& p, cudaStream_t s);
+cudaError_t launch_dsink(const ChainParams& p, cudaStream_t s);
 cudaError_t launch_dq_from_ds(const CUtensorMap& k_map, const ChainParams& p, cudaStream_t s,
                               int num_sms);
 cudaError_t dq_kernel_setup();  // per device: opt in to the dQ kernel's shared memory

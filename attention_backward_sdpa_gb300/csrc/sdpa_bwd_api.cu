@@ -49,7 +49,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 bool use_ds_route(int deterministic, int Dqk) { return Dqk == 192 || (deterministic && Dqk == 128); }
 
 struct Carve {
-  size_t qstat, dq_accum, ds_ws, zero_tile, counters, dk_ws, dv_ws, total;
+  size_t qstat, dq_accum, ds_ws, zero_tile, counters, dk_ws, dv_ws, dsink_part, total;
 };
 
 Carve carve(int B, int Hq, int Hkv, int Sq, int Skv, int Dqk, int Dv, bool ds_route) {
@@ -72,6 +72,8 @@ Carve carve(int B, int Hq, int Hkv, int Sq, int Skv, int Dqk, int Dv, bool ds_ro
   }
   c.counters = off;
   off = align256(off + (bh * n_qt + 1) * sizeof(int));
+  c.dsink_part = off;  // sink-token partials (one float per 64-row tile); used only by sdpa_bwd_sink
+  off = align256(off + bh * n_qt * sizeof(float));
   if (Hkv < Hq) {
     c.dk_ws = off;
     off = align256(off + bh * (size_t)Skv * Dqk * 2);
@@ -238,18 +240,26 @@ int sdpa_bwd_check_device_status(void* stream) {
   return SDPA_OK;
 }
 
-int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const void* d_o,
-             const float* lse, void* dq, void* dk, void* dv, int B, int H_q, int H_kv, int S_q,
-             int S_kv, int D_qk, int D_v, float scale, int causal, int bottom_right,
-             int window_left, int window_right, int deterministic, const int32_t* seq_q_lens,
-             const int32_t* seq_kv_lens, void* workspace, size_t workspace_bytes, void* stream_) {
+}  // extern "C"
+
+namespace {
+
+// The whole chain; sink/dsink are null for sdpa_bwd().
+int run_chain(const void* q, const void* k, const void* v, const void* o, const void* d_o,
+              const float* lse, void* dq, void* dk, void* dv, int B, int H_q, int H_kv, int S_q,
+              int S_kv, int D_qk, int D_v, float scale, int causal, int bottom_right,
+              int window_left, int window_right, int deterministic, const int32_t* seq_q_lens,
+              const int32_t* seq_kv_lens, void* workspace, size_t workspace_bytes,
+              const float* sink, float* dsink, void* stream_) {
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   int rc = basic_checks(B, H_q, H_kv, S_q, S_kv, D_qk, D_v);
   if (rc != SDPA_OK) return rc;
   if (!q || !k || !v || !o || !d_o || !lse || !dq || !dk || !dv) return SDPA_ERR_INVALID;
+  if (dsink && !sink) return SDPA_ERR_INVALID;
   for (const void* ptr : {q, k, v, o, d_o, (const void*)dq, (const void*)dk, (const void*)dv})
     if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return SDPA_ERR_ALIGN;
-  if (reinterpret_cast<uintptr_t>(lse) % 4 != 0) return SDPA_ERR_ALIGN;
+  for (const void* ptr : {(const void*)lse, (const void*)sink, (const void*)dsink})
+    if (reinterpret_cast<uintptr_t>(ptr) % 4 != 0) return SDPA_ERR_ALIGN;
   if (window_right >= 0 && !causal) return SDPA_ERR_UNSUPPORTED;
   if (!(scale > 0.f) || !std::isfinite(scale)) scale = 1.0f / std::sqrt((float)D_qk);
 
@@ -264,9 +274,11 @@ int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const v
   const size_t dk_bytes = (size_t)B * H_kv * S_kv * D_qk * 2;
   const size_t dv_bytes = (size_t)B * H_kv * S_kv * D_v * 2;
   if (S_q == 0 || S_kv == 0) {  // no (query, key) pair: every gradient is zero
+    // (and O = 0, so delta = 0 and dsink = 0)
     if (cudaMemsetAsync(dq, 0, dq_bytes, stream) != cudaSuccess ||
         cudaMemsetAsync(dk, 0, dk_bytes, stream) != cudaSuccess ||
-        cudaMemsetAsync(dv, 0, dv_bytes, stream) != cudaSuccess)
+        cudaMemsetAsync(dv, 0, dv_bytes, stream) != cudaSuccess ||
+        (dsink && cudaMemsetAsync(dsink, 0, (size_t)H_q * sizeof(float), stream) != cudaSuccess))
       return SDPA_ERR_CUDA;
     return SDPA_OK;
   }
@@ -333,6 +345,9 @@ int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const v
   p.dk_ws = p.n_part > 1 ? reinterpret_cast<__nv_bfloat16*>(ws + cv.dk_ws) : nullptr;
   p.dv_ws = p.n_part > 1 ? reinterpret_cast<__nv_bfloat16*>(ws + cv.dv_ws) : nullptr;
   p.status = status;
+  p.sink = dsink ? sink : nullptr;
+  p.dsink = dsink;
+  p.dsink_part = dsink ? reinterpret_cast<float*>(ws + cv.dsink_part) : nullptr;
 
   MainMaps maps;
   const long long BHq = (long long)B * H_q, BHkv = (long long)B * H_kv;
@@ -363,8 +378,35 @@ int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const v
     e = ds_route ? launch_dq_from_ds(maps.k, p, stream, sms) : launch_dq_convert(p, stream);
     prof.end(2);
   }
+  if (e == cudaSuccess && dsink) e = launch_dsink(p, stream);
   if (own_ws) cudaFreeAsync(workspace, stream);
   return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const void* d_o,
+             const float* lse, void* dq, void* dk, void* dv, int B, int H_q, int H_kv, int S_q,
+             int S_kv, int D_qk, int D_v, float scale, int causal, int bottom_right,
+             int window_left, int window_right, int deterministic, const int32_t* seq_q_lens,
+             const int32_t* seq_kv_lens, void* workspace, size_t workspace_bytes, void* stream) {
+  return run_chain(q, k, v, o, d_o, lse, dq, dk, dv, B, H_q, H_kv, S_q, S_kv, D_qk, D_v, scale,
+                   causal, bottom_right, window_left, window_right, deterministic, seq_q_lens,
+                   seq_kv_lens, workspace, workspace_bytes, nullptr, nullptr, stream);
+}
+
+int sdpa_bwd_sink(const void* q, const void* k, const void* v, const void* o, const void* d_o,
+                  const float* lse, void* dq, void* dk, void* dv, int B, int H_q, int H_kv,
+                  int S_q, int S_kv, int D_qk, int D_v, float scale, int causal, int bottom_right,
+                  int window_left, int window_right, int deterministic,
+                  const int32_t* seq_q_lens, const int32_t* seq_kv_lens, void* workspace,
+                  size_t workspace_bytes, const float* sink, float* dsink, void* stream) {
+  if (!sink || !dsink) return SDPA_ERR_INVALID;
+  return run_chain(q, k, v, o, d_o, lse, dq, dk, dv, B, H_q, H_kv, S_q, S_kv, D_qk, D_v, scale,
+                   causal, bottom_right, window_left, window_right, deterministic, seq_q_lens,
+                   seq_kv_lens, workspace, workspace_bytes, sink, dsink, stream);
 }
 
 }  // extern "C"

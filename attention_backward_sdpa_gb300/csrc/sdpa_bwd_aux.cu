@@ -42,6 +42,7 @@ __global__ void __launch_bounds__(256) sdpa_bwd_preprocess(const ChainParams p) 
   const int sub = threadIdx.x % TPR;
   const int rsub = threadIdx.x / TPR;
   const unsigned n_tiles = (unsigned)p.B * p.Hq * p.n_qt;
+  __shared__ float sink_terms[BQ];  // per-row sink terms of the current tile
 
   for (unsigned t = blockIdx.x; t < n_tiles; t += gridDim.x) {
     const unsigned bh = t / (unsigned)p.n_qt;
@@ -63,6 +64,7 @@ __global__ void __launch_bounds__(256) sdpa_bwd_preprocess(const ChainParams p) 
       }
     }
     float* qs = p.qstat + (long long)t * QSTAT_FLOATS;
+    const float sink2 = p.dsink_part ? p.sink[bh % (unsigned)p.Hq] * LOG2E : 0.f;
 #pragma unroll
     for (int u = 0; u < PASSES; ++u) {
       const int qi = u * RPP + rsub;
@@ -84,7 +86,21 @@ __global__ void __launch_bounds__(256) sdpa_bwd_preprocess(const ChainParams p) 
         }
         qs[qi] = lse2;
         qs[BQ + qi] = delta;
+        // Sink term of this row: exp(sink - LSE) * delta (0 for a row past the
+        // length, whose delta is 0, or with LSE = -inf, whose lse2 is +inf).
+        if (p.dsink_part) sink_terms[qi] = exp2f(sink2 - lse2) * delta;
       }
+    }
+    if (p.dsink_part) {
+      // The tile's 64 terms in ascending row order, by one thread: bitwise
+      // reproducible, and so is the fixed-order sum of the tiles (dsink kernel).
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        float acc = 0.f;
+        for (int i = 0; i < BQ; ++i) acc += sink_terms[i];
+        p.dsink_part[t] = acc;
+      }
+      __syncthreads();
     }
     // dQ-reduction route: clear this tile's accumulator rows below Lq (the
     // convert kernel writes zeros for rows at or past Lq without reading them).
@@ -154,6 +170,37 @@ __global__ void __launch_bounds__(256) sdpa_bwd_dq_convert(const ChainParams p) 
       *reinterpret_cast<uint4*>(dst + r * DQK + c8 * 8) = out;
     }
   }
+}
+
+// ---------------------------------------------------------------- dsink
+// dsink[h] = -sum_{b,q} exp(sink[h] - LSE[b,h,q]) * delta[b,h,q] ("SDPA
+// Backward (SM120)", the `dsink` step of the kernel chain and the sink-token
+// capability). The preprocess kernel left one fixed-order partial per 64-row
+// tile; one CTA per head sums the head's B * n_qt partials: each thread a fixed
+// strided subset in ascending order, then a fixed-shape tree. Every run adds
+// in the same order, so dsink is bitwise reproducible.
+constexpr int DSINK_THREADS = 256;
+
+__global__ void __launch_bounds__(DSINK_THREADS) sdpa_bwd_dsink(const ChainParams p) {
+  __shared__ float part[DSINK_THREADS];
+  const int h = blockIdx.x;
+  const int n = p.B * p.n_qt;  // partials of head h: index b * n_qt + qt
+  float acc = 0.f;
+  for (int i = threadIdx.x; i < n; i += DSINK_THREADS) {
+    const int b = i / p.n_qt, qt = i - b * p.n_qt;
+    acc += p.dsink_part[((long long)b * p.Hq + h) * p.n_qt + qt];
+  }
+  part[threadIdx.x] = acc;
+  __syncthreads();
+  for (int w = DSINK_THREADS / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) part[threadIdx.x] += part[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) p.dsink[h] = -part[0];
+}
+
+cudaError_t launch_dsink(const ChainParams& p, cudaStream_t s) {
+  return launch_kernel(sdpa_bwd_dsink, dim3((unsigned)p.Hq), dim3(DSINK_THREADS), 0, s, false, p);
 }
 
 // Both kernels take one 64-row query tile per CTA and leave the balancing of

@@ -59,8 +59,9 @@ typedef enum {
  * The workspace holds, each region 256-byte aligned: per-query-tile fp32 row
  * statistics (LSE * log2(e) and delta); the fp32 dQ accumulator, or on the
  * deterministic two-kernel route the bf16 dS tiles; the deterministic-mode turn
- * counters and a work ticket; and, when H_kv < H_q, the per-query-head bf16
- * dK/dV partials of the GQA reduction.
+ * counters and a work ticket; one fp32 sink-token partial per query tile
+ * (sdpa_bwd_sink); and, when H_kv < H_q, the per-query-head bf16 dK/dV
+ * partials of the GQA reduction.
  * Returns 0 for arguments sdpa_bwd() would reject.
  */
 size_t sdpa_bwd_workspace_size(int B, int H_q, int H_kv, int S_q, int S_kv, int D_qk, int D_v,
@@ -108,6 +109,29 @@ int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const v
              int S_kv, int D_qk, int D_v, float scale, int causal, int bottom_right,
              int window_left, int window_right, int deterministic, const int32_t* seq_q_lens,
              const int32_t* seq_kv_lens, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * SDPA backward with sink tokens (cuDNN frontend docs, "SDPA Backward (SM120)":
+ * the sink-token capability and the `dsink` step of the kernel chain). A sink
+ * logit per query head joins every row's softmax denominator without a value
+ * row. The forward's LSE already includes it, so dQ, dK and dV are exactly
+ * those of sdpa_bwd() with the same lse; this call also writes
+ *     dsink[h] = -sum_{b, q < L_q} exp(sink[h] - LSE[b,h,q]) * delta[b,h,q]
+ * (terms with LSE = -inf count as 0). The sum runs in a fixed order (one
+ * fp32 partial per 64-row query tile, then the tiles of a head in a fixed
+ * tree), so dsink is bitwise reproducible in both modes.
+ * Arguments: those of sdpa_bwd(), then
+ *   sink      device fp32 (H_q,) sink logits (4-byte aligned).
+ *   dsink     device fp32 (H_q,) output (4-byte aligned).
+ * Returns SDPA_ERR_INVALID when sink or dsink is NULL; otherwise as sdpa_bwd().
+ * The workspace size is sdpa_bwd_workspace_size() (it includes the partials).
+ */
+int sdpa_bwd_sink(const void* q, const void* k, const void* v, const void* o, const void* d_o,
+                  const float* lse, void* dq, void* dk, void* dv, int B, int H_q, int H_kv,
+                  int S_q, int S_kv, int D_qk, int D_v, float scale, int causal, int bottom_right,
+                  int window_left, int window_right, int deterministic,
+                  const int32_t* seq_q_lens, const int32_t* seq_kv_lens, void* workspace,
+                  size_t workspace_bytes, const float* sink, float* dsink, void* stream);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* sdpa_status_string(int status);

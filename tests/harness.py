@@ -25,15 +25,18 @@ def f64(x: torch.Tensor) -> np.ndarray:
     return x.double().numpy()
 
 
-def make_case(w: workloads.Workload):
-    """Seeded inputs plus O (bf16) and LSE (fp32) from the oracle forward."""
+def make_case(w: workloads.Workload, sink: bool = False):
+    """Seeded inputs plus O (bf16) and LSE (fp32) from the oracle forward; with
+    ``sink`` the forward takes the workload's sink logits (case["sink"])."""
     t = workloads.generate(w)
+    t["sink"] = workloads.sink_logits(w) if sink else None
     p = oracle.Problem(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.Dqk, w.Dv, scale=w.resolved_scale,
                        causal=w.causal, bottom_right=w.bottom_right, window_left=w.window_left,
                        window_right=w.window_right,
                        seq_q_lens=None if t["seq_q_lens"] is None else t["seq_q_lens"].numpy(),
                        seq_kv_lens=None if t["seq_kv_lens"] is None else t["seq_kv_lens"].numpy())
-    o64, lse64 = oracle.forward(p, f64(t["q"]), f64(t["k"]), f64(t["v"]))
+    o64, lse64 = oracle.forward(p, f64(t["q"]), f64(t["k"]), f64(t["v"]),
+                                None if t["sink"] is None else t["sink"].double().numpy())
     t["o"] = torch.from_numpy(o64).to(torch.bfloat16)
     t["lse"] = torch.from_numpy(lse64).float()
     t["problem"] = p
@@ -47,6 +50,17 @@ def oracle_backward(case):
                            f64(case["do"]), case["lse"].double().numpy())
 
 
+def oracle_dsink(case):
+    """(dsink, sum of |terms|) per head from the bf16 O / dO and fp32 LSE the GPU sees."""
+    p = case["problem"]
+    lse = case["lse"].double().numpy()
+    dl = oracle.delta(p, f64(case["o"]), f64(case["do"]))
+    sink = case["sink"].double().numpy()
+    ds = oracle.dsink(p, sink, lse, dl)
+    mag = oracle.dsink(p, sink, lse, np.abs(dl))  # -sum of |terms|
+    return ds, -mag
+
+
 def oracle_sampled(case, q_rows, kv_rows):
     p = case["problem"]
     return oracle.backward_sampled(p, f64(case["q"]), f64(case["k"]), f64(case["v"]),
@@ -56,6 +70,7 @@ def oracle_sampled(case, q_rows, kv_rows):
 
 def to_device(case, dev="cuda"):
     d = {k: case[k].to(dev) for k in ("q", "k", "v", "o", "do", "lse")}
+    d["sink"] = None if case.get("sink") is None else case["sink"].to(dev)
     for k in ("seq_q_lens", "seq_kv_lens"):
         d[k] = None if case[k] is None else case[k].to(dev)
     return d

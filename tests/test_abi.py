@@ -54,8 +54,9 @@ def expected_workspace(B, Hq, Hkv, Sq, Skv, Dqk, Dv, det=0):
     """Documented layout: per-query-tile row statistics (2 x 64 fp32 per 64-row tile);
     then either the fp32 dQ accumulator over whole 64-row tiles, or (deterministic,
     D_qk = 128: two-kernel route) one 16 KiB bf16 dS^T tile per (128-key tile,
-    64-query tile) plus one zero tile; one int per query tile plus a ticket; and for
-    GQA the bf16 dK/dV partials with H_q heads. Every region 256-byte aligned."""
+    64-query tile) plus one zero tile; one int per query tile plus a ticket; one fp32
+    sink-token partial per query tile; and for GQA the bf16 dK/dV partials with H_q
+    heads. Every region 256-byte aligned."""
     n_qt, n_kt = -(-Sq // 64), -(-Skv // 128)
     total = _a256(B * Hq * n_qt * 128 * 4)
     if (det and Dqk == 128) or Dqk == 192:
@@ -63,6 +64,7 @@ def expected_workspace(B, Hq, Hkv, Sq, Skv, Dqk, Dv, det=0):
     else:
         total += _a256(B * Hq * n_qt * 64 * Dqk * 4)
     total += _a256((B * Hq * n_qt + 1) * 4)
+    total += _a256(B * Hq * n_qt * 4)
     if Hkv < Hq:
         total += _a256(B * Hq * Skv * Dqk * 2) + _a256(B * Hq * Skv * Dv * 2)
     return total
@@ -114,6 +116,26 @@ def test_argument_validation(lib):
     ptrs[5] = FAKE + 2  # lse needs 4-byte alignment
     assert call(lib, ptrs) == ALIGN
     assert call(lib, wr=3, causal=0) == UNSUPPORTED  # a right band only widens a causal mask
+
+
+def call_sink(lib, sink, dsink, ptrs=None):
+    ptrs = ptrs or [FAKE] * 9
+    vp = [ctypes.c_void_p(p) for p in ptrs]
+    return lib.sdpa_bwd_sink(*vp, 1, 2, 2, 128, 128, 128, 128, ctypes.c_float(0.0), 0, 0, -1, -1, 0,
+                             None, None, None, 0,
+                             None if sink is None else ctypes.c_void_p(sink),
+                             None if dsink is None else ctypes.c_void_p(dsink), None)
+
+
+def test_sink_argument_validation(lib):
+    lib.sdpa_bwd_sink.restype = ctypes.c_int
+    assert call_sink(lib, None, FAKE) == INVALID
+    assert call_sink(lib, FAKE, None) == INVALID
+    assert call_sink(lib, FAKE + 2, FAKE) == ALIGN  # fp32 vectors need 4-byte alignment
+    assert call_sink(lib, FAKE, FAKE + 1) == ALIGN
+    ptrs = [FAKE] * 9
+    ptrs[0] = FAKE + 8
+    assert call_sink(lib, FAKE, FAKE, ptrs) == ALIGN
 
 
 def test_python_binding_rejects_cpu_tensors():

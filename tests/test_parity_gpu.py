@@ -13,7 +13,7 @@ import torch
 
 import workloads
 from harness import (assert_close, errors, gpu_backward, make_case, oracle_backward,
-                     oracle_sampled, to_device)
+                     oracle_dsink, oracle_sampled, to_device)
 
 pytestmark = pytest.mark.gpu
 
@@ -232,3 +232,50 @@ def test_workload_deterministic_bitwise_10_runs():
         again = gpu_backward(case, d, poison=True)
         for a, b in zip(first, again):
             assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+# ---------------------------------------------------------------- sink tokens
+# With a sink the forward's LSE includes it; dQ/dK/dV come out of the same
+# kernels and dsink from the preprocess partials plus the fixed-order reduce.
+SINK_CASES = {
+    "d128_causal_ragged": SMALL["d128_causal_ragged"],
+    "gqa_det": SMALL["gqa_det"],
+    "det_padded_odd": SMALL["det_padded_odd"],
+    "padded_nondet": SMALL["det_padded_odd"].with_(name="padded_nondet", deterministic=False),
+    "mla_gqa_window": SMALL["mla_gqa_window"],
+    "tl_causal_long_q_d64": SMALL["tl_causal_long_q"],
+    "mid_gqa": W("mid_gqa", 2, 8, 2, 1024, 1024, 128, 128, causal=True, seed=40),
+}
+
+
+def _dsink_close(gpu, ref, mag):
+    err = np.abs(gpu - ref)
+    # fp32 delta, exp2 and sums against fp64: a few ulp of the terms' magnitude
+    assert np.all(err <= 1e-4 * mag + 1e-6), f"dsink: err {err.max():.3e}, mag {mag.max():.3e}"
+
+
+@pytest.mark.parametrize("name", sorted(SINK_CASES))
+def test_sink_parity(name):
+    case = make_case(SINK_CASES[name], sink=True)
+    d = to_device(case)
+    dq, dk, dv, dsink = gpu_backward(case, d, sink=d["sink"])
+    rq, rk, rv = oracle_backward(case)
+    assert_close("dq", dq.double().cpu().numpy(), rq)
+    assert_close("dk", dk.double().cpu().numpy(), rk)
+    assert_close("dv", dv.double().cpu().numpy(), rv)
+    ref, mag = oracle_dsink(case)
+    _dsink_close(dsink.double().cpu().numpy(), ref, mag)
+    # dQ/dK/dV need no sink code: the plain call gives the same bits
+    dq2, dk2, dv2 = gpu_backward(case, d)
+    if case["workload"].deterministic or case["workload"].Dqk == 192:
+        for a, b in ((dq, dq2), (dk, dk2), (dv, dv2)):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_dsink_bitwise_reproducible():
+    case = make_case(SINK_CASES["mid_gqa"], sink=True)
+    d = to_device(case)
+    first = gpu_backward(case, d, sink=d["sink"])[3].clone()
+    for _ in range(9):
+        again = gpu_backward(case, d, sink=d["sink"])[3]
+        assert torch.equal(first.view(torch.int32), again.view(torch.int32))

@@ -82,3 +82,9 @@ def generate(w: Workload) -> Dict[str, Optional[torch.Tensor]]:
     do = draw(w.B, w.Hq, w.Sq, w.Dv)
     return {"q": q, "k": k, "v": v, "do": do,
             "seq_q_lens": lens, "seq_kv_lens": None if lens is None else lens.clone()}
+
+
+def sink_logits(w: Workload) -> torch.Tensor:
+    """Seeded fp32 (Hq,) sink-token logits, N(0, 1), from a stream of their own."""
+    g = torch.Generator("cpu").manual_seed(w.seed + 1_000_003)
+    return torch.randn(w.Hq, generator=g, dtype=torch.float32)
