@@ -244,18 +244,26 @@ def cpu_baseline_leg(w, t, target_s=12.0):
 # DRAM bytes per launch of the main kernel (dram__bytes_read.sum +
 # dram__bytes_write.sum from one ncu capture, profiles/sdpa_bwd_main_traffic.md),
 # valid only for the kernel sources they were taken on: the digest covers the
-# main kernel's source files, and a changed kernel reports null.
-MAIN_SOURCES = ("sdpa_bwd_main.cu", "common.cuh", "ptx.cuh")
+# kernel's source files, and a changed kernel reports null. D_qk = 192 runs
+# sdpa_bwd_main_ds, every other head dim sdpa_bwd_main.
+MAIN_SOURCES = {"sdpa_bwd_main": ("sdpa_bwd_main.cu", "common.cuh", "ptx.cuh"),
+                "sdpa_bwd_main_ds": ("sdpa_bwd_main_ds.cu", "common.cuh", "ptx.cuh")}
 MAIN_TRAFFIC = {
-    "5b8276b586c039a6": {"causal_mha": 112252928 + 29158144,
-                         "causal_gqa_det": 124103680 + 513449472},
+    "fa34d64d4753c107": {"causal_mha": 114246144 + 31919360,
+                         "causal_gqa_det": 134530048 + 515341568,
+                         "swa_causal_padded": 245091328 + 185813248},
+    "25168dca819c0205": {"mla_br_causal": 132380928 + 263462144},
 }
 
 
-def main_traffic(workload: str):
+def main_kernel_name(w) -> str:
+    return "sdpa_bwd_main_ds" if w.Dqk == 192 else "sdpa_bwd_main"
+
+
+def main_traffic(w):
     csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "attention_backward_sdpa_gb300", "csrc")
-    blob = b"".join(open(os.path.join(csrc, f), "rb").read() for f in MAIN_SOURCES)
-    return MAIN_TRAFFIC.get(hashlib.sha256(blob).hexdigest()[:16], {}).get(workload)
+    blob = b"".join(open(os.path.join(csrc, f), "rb").read() for f in MAIN_SOURCES[main_kernel_name(w)])
+    return MAIN_TRAFFIC.get(hashlib.sha256(blob).hexdigest()[:16], {}).get(w.name)
 
 
 def peaks():
@@ -283,6 +291,10 @@ def run_gpu(args, w, t, o, lse, rank, world, device):
               window_left=w.window_left, window_right=w.window_right,
               deterministic=w.deterministic, seq_q_lens=lq, seq_kv_lens=lk, dq=dq, dk=dk, dv=dv,
               workspace=ws)
+
+    if args.sink:  # sink tokens: the same chain plus the dsink partials and reduce
+        kw["sink"] = workloads.sink_logits(w).to(device)
+        kw["dsink"] = torch.empty_like(kw["sink"])
 
     def step():
         pkg.sdpa_bwd(d["q"], d["k"], d["v"], d["o"], d["do"], d["lse"], **kw)
@@ -348,14 +360,14 @@ def run_gpu(args, w, t, o, lse, rank, world, device):
     return {
         "value": value, "ms_per_step": ms_step, "flops": flops,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": achieved / peak_tf, "traffic": main_traffic(w.name),
-                     "kernel": "sdpa_bwd_main", "peak_kind": f"{peak_kind} bf16 burst",
+                     "frac": achieved / peak_tf, "traffic": main_traffic(w),
+                     "kernel": main_kernel_name(w), "peak_kind": f"{peak_kind} bf16 burst",
                      "kernel_gflop": main_flops / 1e9},
         "kernel_ms": kernel_ms,
         "e2e": {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "clocks": clocks.summary(),
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (4 if args.sink else 3) * args.steps,
     }
 
 
@@ -397,6 +409,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--sink", action="store_true",
+                    help="time sdpa_bwd_sink (sink-token logits, dsink output) instead of sdpa_bwd")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip timing the oracle backward (O/LSE still come from the oracle forward)")
     args = ap.parse_args(argv)
@@ -433,6 +447,7 @@ def main(argv=None):
                            "S_kv": w.Skv, "D_qk": w.Dqk, "D_v": w.Dv, "causal": w.causal,
                            "bottom_right": w.bottom_right, "window_left": w.window_left,
                            "deterministic": w.deterministic, "seed": w.seed,
+                           "sink": bool(args.sink),
                            "gflop_per_step": r["flops"] / 1e9,
                            "l2": "256 MiB buffer written between timed steps",
                            "parallelism": f"replicas{world}" if world > 1 else "single"},
