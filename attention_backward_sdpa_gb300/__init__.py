@@ -59,6 +59,9 @@ def load(build_if_missing: bool = False):
     lib.sdpa_bwd.restype = i
     lib.sdpa_bwd_sink.argtypes = list(lib.sdpa_bwd.argtypes[:-1]) + [vp, vp, vp]
     lib.sdpa_bwd_sink.restype = i
+    lib.sdpa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, ctypes.c_float, i, i, i, i,
+                             vp, vp, vp, vp]
+    lib.sdpa_fwd.restype = i
     lib.sdpa_bwd_workspace_size.argtypes = [i, i, i, i, i, i, i, i]
     lib.sdpa_bwd_workspace_size.restype = sz
     lib.sdpa_status_string.argtypes = [i]
@@ -170,6 +173,45 @@ def sdpa_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
     if rc != 0:
         raise SdpaError(rc, "sdpa_bwd_sink")
     return dq, dk, dv, dsink
+
+
+def sdpa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: Optional[float] = None,
+             causal: bool = False, bottom_right: bool = False, window_left: int = -1,
+             window_right: int = -1, seq_q_lens: Optional[torch.Tensor] = None,
+             seq_kv_lens: Optional[torch.Tensor] = None, sink: Optional[torch.Tensor] = None,
+             o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+             stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """O (bf16, (B,Hq,Sq,Dv)) and natural-log LSE (fp32, (B,Hq,Sq)) of the masked
+    softmax attention (see include/sdpa_bwd.h); the inputs of sdpa_bwd."""
+    lib = load()
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be (B, H, S, D)")
+    B, Hq, Sq, Dqk = q.shape
+    Hkv, Skv = k.shape[1], k.shape[2]
+    Dv = v.shape[3]
+    _check_bf16("q", q, (B, Hq, Sq, Dqk))
+    _check_bf16("k", k, (B, Hkv, Skv, Dqk))
+    _check_bf16("v", v, (B, Hkv, Skv, Dv))
+    for name, lens in (("seq_q_lens", seq_q_lens), ("seq_kv_lens", seq_kv_lens)):
+        if lens is not None and (lens.dtype != torch.int32 or not lens.is_cuda or lens.numel() != B
+                                 or not lens.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor of B elements")
+    if sink is not None and (sink.dtype != torch.float32 or not sink.is_cuda
+                             or not sink.is_contiguous() or sink.numel() != Hq):
+        raise ValueError("sink must be a contiguous fp32 CUDA tensor of Hq elements")
+    o = torch.empty((B, Hq, Sq, Dv), dtype=torch.bfloat16, device=q.device) if o is None else o
+    lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check_bf16("o", o, (B, Hq, Sq, Dv))
+    if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous() \
+            or lse.numel() != B * Hq * Sq:
+        raise ValueError("lse must be a contiguous fp32 CUDA tensor with B*Hq*Sq elements")
+    sc = 0.0 if scale is None else float(scale)
+    rc = lib.sdpa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Skv, Dqk, Dv, sc,
+                      int(causal), int(bottom_right), int(window_left), int(window_right),
+                      _ptr(seq_q_lens), _ptr(seq_kv_lens), _ptr(sink), _stream_handle(stream))
+    if rc != 0:
+        raise SdpaError(rc, "sdpa_fwd")
+    return o, lse
 
 
 def check_device_status(stream: Optional[torch.cuda.Stream] = None) -> None:

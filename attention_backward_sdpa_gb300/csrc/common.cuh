@@ -99,6 +99,25 @@ __host__ __device__ inline void visited_query_tiles(int kt, int Lq, int Lk, int 
   qt_hi = (int)(q_max / BQ);
 }
 
+// Forward pass (sdpa_fwd.cu): O and the natural-log LSE of the masked softmax.
+struct FwdParams {
+  int B, Hq, Hkv, Sq, Skv, Dqk, Dv;
+  int G;            // Hq / Hkv
+  int n_qt;         // ceil(Sq / 128): 128-row query tiles
+  float scale_log2; // scale * log2(e)
+  int causal, bottom_right, window_left, window_right;
+  const int32_t* seq_q_lens;  // (B,) or null
+  const int32_t* seq_kv_lens; // (B,) or null
+  const float* sink;          // (Hq,) sink logits, or null
+  float* lse;                 // (B, Hq, Sq) output
+  int* status;                // device status word
+};
+struct FwdMaps {
+  CUtensorMap q, k, v, o;  // 128-row boxes
+};
+cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, cudaStream_t s);
+cudaError_t fwd_kernel_setup();
+
 // TMA tensor maps of the main kernels: inputs K and V with H_kv heads, Q and dO
 // with H_q; outputs dK and dV (H_kv heads, or the per-query-head partials of
 // the GQA workspace), written in 128-row boxes.

@@ -119,7 +119,7 @@ int device_state(int dev, int** status_out, int* sms_out) {
       if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return SDPA_ERR_CUDA;
       g_status_ptr[dev] = static_cast<int*>(p);
       if (main_kernel_setup() != cudaSuccess || main_ds_kernel_setup() != cudaSuccess ||
-          dq_kernel_setup() != cudaSuccess)
+          dq_kernel_setup() != cudaSuccess || fwd_kernel_setup() != cudaSuccess)
         return SDPA_ERR_CUDA;
     }
     g_device_checked[dev] = true;
@@ -395,6 +395,57 @@ int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const v
   return run_chain(q, k, v, o, d_o, lse, dq, dk, dv, B, H_q, H_kv, S_q, S_kv, D_qk, D_v, scale,
                    causal, bottom_right, window_left, window_right, deterministic, seq_q_lens,
                    seq_kv_lens, workspace, workspace_bytes, nullptr, nullptr, stream);
+}
+
+int sdpa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
+             int H_kv, int S_q, int S_kv, int D_qk, int D_v, float scale, int causal,
+             int bottom_right, int window_left, int window_right, const int32_t* seq_q_lens,
+             const int32_t* seq_kv_lens, const float* sink, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  int rc = basic_checks(B, H_q, H_kv, S_q, S_kv, D_qk, D_v);
+  if (rc != SDPA_OK) return rc;
+  if (!q || !k || !v || !o || !lse) return SDPA_ERR_INVALID;
+  for (const void* ptr : {q, k, v, (const void*)o})
+    if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return SDPA_ERR_ALIGN;
+  for (const void* ptr : {(const void*)lse, (const void*)sink})
+    if (reinterpret_cast<uintptr_t>(ptr) % 4 != 0) return SDPA_ERR_ALIGN;
+  if (window_right >= 0 && !causal) return SDPA_ERR_UNSUPPORTED;
+  if (!(scale > 0.f) || !std::isfinite(scale)) scale = 1.0f / std::sqrt((float)D_qk);
+  if (S_q == 0) return SDPA_OK;  // no rows
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SDPA_ERR_CUDA;
+  int* status = nullptr;
+  int sms = 0;
+  rc = device_state(dev, &status, &sms);
+  if (rc != SDPA_OK) return rc;
+
+  FwdParams p{};
+  p.B = B; p.Hq = H_q; p.Hkv = H_kv; p.Sq = S_q; p.Skv = S_kv; p.Dqk = D_qk; p.Dv = D_v;
+  p.G = H_q / H_kv;
+  p.n_qt = ceil_div(S_q, 128);
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.causal = causal ? 1 : 0;
+  p.bottom_right = bottom_right ? 1 : 0;
+  p.window_left = window_left < 0 ? -1 : window_left;
+  p.window_right = (causal && window_right > 0) ? window_right : -1;
+  p.seq_q_lens = seq_q_lens;
+  p.seq_kv_lens = seq_kv_lens;
+  p.sink = sink;
+  p.lse = lse;
+  p.status = status;
+  FwdMaps maps;
+  const long long BHq = (long long)B * H_q, BHkv = (long long)B * H_kv;
+  // An empty key axis still needs valid K/V maps: point them at Q (never read).
+  const int Skv_map = S_kv > 0 ? S_kv : 1;
+  const void* kb = S_kv > 0 ? k : q;
+  const void* vb = S_kv > 0 ? v : q;
+  if (!make_bhsd_map(&maps.q, q, D_qk, S_q, BHq, 128) ||
+      !make_bhsd_map(&maps.k, kb, D_qk, Skv_map, S_kv > 0 ? BHkv : BHq, 128) ||
+      !make_bhsd_map(&maps.v, vb, D_v, Skv_map, S_kv > 0 ? BHkv : BHq, 128) ||
+      !make_bhsd_map(&maps.o, o, D_v, S_q, BHq, 128))
+    return SDPA_ERR_CUDA;
+  return launch_fwd(maps, p, stream) == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }
 
 int sdpa_bwd_sink(const void* q, const void* k, const void* v, const void* o, const void* d_o,

@@ -44,6 +44,7 @@ if ROOT not in sys.path:
 import workloads  # noqa: E402
 
 METRIC = "SDPA backward TFLOP/s (bf16, 1xGB300) and fraction of dense tensor peak"
+METRIC_FWD = "SDPA forward TFLOP/s (bf16, 1xGB300) and fraction of dense tensor peak"
 DEFAULT_WORKLOAD = "causal_mha"
 L2_FLUSH_BYTES = 256 << 20
 
@@ -72,6 +73,11 @@ def visible_pairs(w: workloads.Workload, lens) -> int:
 
 def flops_per_pair(w: workloads.Workload) -> int:
     return 2 * (3 * w.Dqk + 2 * w.Dv)
+
+
+def fwd_flops_per_pair(w: workloads.Workload) -> int:
+    """S = Q K^T and O = P V: 2 * (D_qk + D_v) per visible pair."""
+    return 2 * (w.Dqk + w.Dv)
 
 
 def main_kernel_flops_per_pair(w: workloads.Workload) -> int:
@@ -219,6 +225,103 @@ def oracle_backward_sample(w, t, o, lse, groups):
     oracle.backward(p, *args)
     dt = time.perf_counter() - t0
     return dt, visible_pairs(ws, t["seq_q_lens"]) * flops_per_pair(ws)
+
+
+def cpu_baseline_fwd(w, t, target_s=12.0):
+    """The fp64 oracle forward on the first KV-head groups of every batch row."""
+    import oracle
+
+    def sample(groups):
+        G = w.Hq // w.Hkv
+        ws = w.with_(Hq=groups * G, Hkv=groups)
+        p = _problem(ws, t["seq_q_lens"])
+        a = [t["q"][:, :groups * G].contiguous().double().numpy(),
+             t["k"][:, :groups].contiguous().double().numpy(),
+             t["v"][:, :groups].contiguous().double().numpy()]
+        t0 = time.perf_counter()
+        oracle.forward(p, *a)
+        return time.perf_counter() - t0, visible_pairs(ws, t["seq_q_lens"]) * fwd_flops_per_pair(ws)
+
+    dt, fl = sample(1)
+    groups = max(1, min(w.Hkv, int(target_s / max(dt, 1e-3))))
+    if groups > 1:
+        dt, fl = sample(groups)
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"fp64 oracle forward of {groups} of {w.Hkv} KV-head groups x B={w.B} "
+                      f"({fl / 1e9:.2f} GFLOP algorithmic in {dt:.2f} s)"}
+
+
+def run_gpu_fwd(args, w, t, rank, world, device):
+    """Times sdpa_fwd: one kernel per step, so the step time is the kernel's."""
+    import attention_backward_sdpa_gb300 as pkg
+    pkg.load()
+    lens = t["seq_q_lens"]
+    d = {k: t[k].to(device) for k in ("q", "k", "v")}
+    lq = None if lens is None else lens.to(device)
+    lk = None if t["seq_kv_lens"] is None else t["seq_kv_lens"].to(device)
+    o = torch.empty((w.B, w.Hq, w.Sq, w.Dv), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=device)
+    sink = workloads.sink_logits(w).to(device) if args.sink else None
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    kw = dict(scale=w.resolved_scale, causal=w.causal, bottom_right=w.bottom_right,
+              window_left=w.window_left, window_right=w.window_right, seq_q_lens=lq,
+              seq_kv_lens=lk, sink=sink, o=o, lse=lse)
+
+    def step():
+        pkg.sdpa_fwd(d["q"], d["k"], d["v"], **kw)
+
+    pairs = visible_pairs(w, None if lens is None else lens.numpy())
+    flops = pairs * fwd_flops_per_pair(w)
+    with ClockSampler(device.index if device.index is not None else 0) as clocks:
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize(device)
+        pkg.check_device_status()
+        barrier(world)
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        torch.cuda.synchronize(device)
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(device)
+        barrier(world)
+        total_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
+        host_in = {k: v.cpu().pin_memory() for k, v in d.items()}
+        host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (o, lse)]
+        h2d = sum(x.numel() * x.element_size() for x in host_in.values())
+        d2h = sum(x.numel() * x.element_size() for x in host_out)
+        e2e_steps = max(3, min(args.steps, 50))
+        torch.cuda.synchronize(device)
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            for k, v in host_in.items():
+                d[k].copy_(v, non_blocking=True)
+            step()
+            for hh, x in zip(host_out, (o, lse)):
+                hh.copy_(x, non_blocking=True)
+            torch.cuda.synchronize(device)
+        e2e_s = (time.perf_counter() - t0) / e2e_steps
+    pkg.check_device_status()
+    ms_step = max_over_ranks(total_ms / args.steps, world, device)
+    e2e_s = max_over_ranks(e2e_s, world, device)
+    peak_tf, peak_hbm, peak_kind = peaks()
+    achieved = flops / (ms_step * 1e-3) / 1e12
+    return {
+        "value": world * achieved, "ms_per_step": ms_step, "flops": flops,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": achieved / peak_tf, "traffic": None, "kernel": "sdpa_fwd_kernel",
+                     "peak_kind": f"{peak_kind} bf16 burst", "kernel_gflop": flops / 1e9},
+        "kernel_ms": {"fwd": round(ms_step, 5)},
+        "e2e": {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "clocks": clocks.summary(),
+        "gpu_launches": args.steps,
+    }
 
 
 def cpu_baseline_leg(w, t, target_s=12.0):
@@ -411,6 +514,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--sink", action="store_true",
                     help="time sdpa_bwd_sink (sink-token logits, dsink output) instead of sdpa_bwd")
+    ap.add_argument("--pass", dest="pass_", default="bwd", choices=["bwd", "fwd"],
+                    help="bwd: the backward chain (default); fwd: sdpa_fwd, the forward (O, LSE)")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip timing the oracle backward (O/LSE still come from the oracle forward)")
     args = ap.parse_args(argv)
@@ -424,6 +529,15 @@ def main(argv=None):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     t = workloads.generate(w)
+    if args.pass_ == "fwd":
+        cb = cpu_baseline_fwd(w, t) if (rank == 0 and not args.no_cpu_baseline) else None
+        r = run_gpu_fwd(args, w, t, rank, world, device)
+        if rank == 0:
+            print(json.dumps(result_line(args, w, world, r, cb, METRIC_FWD)), flush=True)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
     o = torch.empty((w.B, w.Hq, w.Sq, w.Dv), dtype=torch.bfloat16)
     lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32)
     cb = None
@@ -439,26 +553,30 @@ def main(argv=None):
         o, lse = o_d.cpu(), l_d.cpu()
     r = run_gpu(args, w, t, o, lse, rank, world, device)
     if rank == 0:
-        line = {"metric": METRIC, "value": r["value"], "unit": "TFLOP/s", "n_gpus": world,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-                "data": "synthetic",
-                "config": {"workload": w.name, "B": w.B, "H_q": w.Hq, "H_kv": w.Hkv, "S_q": w.Sq,
-                           "S_kv": w.Skv, "D_qk": w.Dqk, "D_v": w.Dv, "causal": w.causal,
-                           "bottom_right": w.bottom_right, "window_left": w.window_left,
-                           "deterministic": w.deterministic, "seed": w.seed,
-                           "sink": bool(args.sink),
-                           "gflop_per_step": r["flops"] / 1e9,
-                           "l2": "256 MiB buffer written between timed steps",
-                           "parallelism": f"replicas{world}" if world > 1 else "single"},
-                "roofline": r["roofline"], "cpu_baseline": cb, "e2e": r["e2e"],
-                "gpu_launches": r["gpu_launches"], "kernel_ms": r["kernel_ms"],
-                "clocks": r["clocks"]}
-        print(json.dumps(line), flush=True)
+        print(json.dumps(result_line(args, w, world, r, cb, METRIC)), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def result_line(args, w, world, r, cb, metric):
+    """The JSON line of a GPU run (rank 0)."""
+    return {"metric": metric, "value": r["value"], "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H_q": w.Hq, "H_kv": w.Hkv, "S_q": w.Sq,
+                       "S_kv": w.Skv, "D_qk": w.Dqk, "D_v": w.Dv, "causal": w.causal,
+                       "bottom_right": w.bottom_right, "window_left": w.window_left,
+                       "deterministic": w.deterministic, "seed": w.seed,
+                       "pass": args.pass_, "sink": bool(args.sink),
+                       "gflop_per_step": r["flops"] / 1e9,
+                       "l2": "256 MiB buffer written between timed steps",
+                       "parallelism": f"replicas{world}" if world > 1 else "single"},
+            "roofline": r["roofline"], "cpu_baseline": cb, "e2e": r["e2e"],
+            "gpu_launches": r["gpu_launches"], "kernel_ms": r["kernel_ms"],
+            "clocks": r["clocks"]}
 
 
 if __name__ == "__main__":

@@ -133,6 +133,28 @@ int sdpa_bwd_sink(const void* q, const void* k, const void* v, const void* o, co
                   const int32_t* seq_q_lens, const int32_t* seq_kv_lens, void* workspace,
                   size_t workspace_bytes, const float* sink, float* dsink, void* stream);
 
+/*
+ * SDPA forward: the O and natural-log LSE that sdpa_bwd() takes (cuDNN frontend
+ * docs, "SDPA Backward (SM120)": the forward statistics of "API Usage", the
+ * masks of "Causal, sliding-window, and padding masks", GQA/MQA, and sink
+ * tokens), so that a forward and a backward form a training step:
+ *     S   = scale * Q K^T over the visible keys,
+ *     LSE = log( sum_k exp(S) [+ exp(sink[h])] ),   O = sum_k exp(S - LSE) V.
+ * A row with no visible key (queries at or past seq_q_lens[b] included) gets
+ * O = 0 and LSE = -inf, or LSE = sink[h] with a sink.
+ * Arguments are those of sdpa_bwd() with:
+ *   o      device bf16 (B, H_q, S_q, D_v) output, 16-byte aligned.
+ *   lse    device fp32 (B, H_q, S_q) output, 4-byte aligned.
+ *   sink   device fp32 (H_q,) sink logits, or NULL.
+ * No workspace. Returns SDPA_OK once the kernel is enqueued on `stream`, else an
+ * error code (nothing enqueued); a device-side timeout is reported by
+ * sdpa_bwd_check_device_status().
+ */
+int sdpa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
+             int H_kv, int S_q, int S_kv, int D_qk, int D_v, float scale, int causal,
+             int bottom_right, int window_left, int window_right, const int32_t* seq_q_lens,
+             const int32_t* seq_kv_lens, const float* sink, void* stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* sdpa_status_string(int status);
 

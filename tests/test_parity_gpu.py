@@ -279,3 +279,87 @@ def test_dsink_bitwise_reproducible():
     for _ in range(9):
         again = gpu_backward(case, d, sink=d["sink"])[3]
         assert torch.equal(first.view(torch.int32), again.view(torch.int32))
+
+
+# ---------------------------------------------------------------- forward
+# The fused forward against the oracle forward: O (bf16) within the gradient
+# tolerance, LSE within 1e-3 (fp32 scores of bf16 products, ex2.approx), rows
+# without a visible key exactly -inf (or the sink).
+FWD_CASES = {
+    "tiny_dense": SMALL["tiny_dense"],
+    "d128_causal_ragged": SMALL["d128_causal_ragged"],
+    "br_causal_long_kv": SMALL["br_causal_long_kv"],
+    "br_causal_long_q": SMALL["br_causal_long_q"],
+    "tl_causal_long_q_d64": SMALL["tl_causal_long_q"],
+    "window_causal": SMALL["window_causal"],
+    "window_only": SMALL["window_only"],
+    "gqa_det": SMALL["gqa_det"],
+    "det_padded_odd": SMALL["det_padded_odd"],
+    "single_query": SMALL["single_query"],
+    "mla_gqa_window": SMALL["mla_gqa_window"],
+    "mla_padded_det": SMALL["mla_padded_det"],
+}
+
+
+def _check_fwd(case, o, lse, rows=None):
+    ro = case["o"].double().numpy()
+    rl = case["lse"].double().numpy()
+    go = o.double().cpu().numpy()
+    gl = lse.double().cpu().numpy()
+    if rows is not None:
+        ro, rl = ro.reshape(-1, ro.shape[-1])[rows], rl.reshape(-1)[rows]
+        go, gl = go.reshape(-1, go.shape[-1])[rows], gl.reshape(-1)[rows]
+    assert_close("o", go, ro)
+    fin = np.isfinite(rl)
+    assert np.array_equal(fin, np.isfinite(gl)), "LSE: -inf rows differ"
+    assert np.all(gl[~fin] == rl[~fin])
+    err = np.abs(gl[fin] - rl[fin])
+    assert err.size == 0 or err.max() <= 1e-3 * max(1.0, np.abs(rl[fin]).max()), f"lse err {err.max():.3e}"
+
+
+def _gpu_fwd(case, d):
+    import attention_backward_sdpa_gb300 as pkg
+    w = case["workload"]
+    o, lse = pkg.sdpa_fwd(d["q"], d["k"], d["v"], scale=w.resolved_scale, causal=w.causal,
+                          bottom_right=w.bottom_right, window_left=w.window_left,
+                          window_right=w.window_right, seq_q_lens=d["seq_q_lens"],
+                          seq_kv_lens=d["seq_kv_lens"], sink=d.get("sink"),
+                          o=torch.full((w.B, w.Hq, w.Sq, w.Dv), float("nan"), dtype=torch.bfloat16,
+                                       device="cuda"),
+                          lse=torch.full((w.B, w.Hq, w.Sq), float("nan"), device="cuda"))
+    pkg.check_device_status()
+    return o, lse
+
+
+@pytest.mark.parametrize("name", sorted(FWD_CASES))
+@pytest.mark.parametrize("sink", [False, True])
+def test_forward_parity(name, sink):
+    case = make_case(FWD_CASES[name], sink=sink)
+    d = to_device(case)
+    o, lse = _gpu_fwd(case, d)
+    _check_fwd(case, o, lse)
+
+
+@pytest.mark.parametrize("name", workloads.ORDER)
+def test_forward_full_size(name):
+    case = _case(name)
+    d = to_device(case)
+    o, lse = _gpu_fwd(case, d)
+    w = case["workload"]
+    rng = np.random.default_rng(w.seed + 7)
+    rows = np.unique(rng.integers(0, w.B * w.Hq * w.Sq, 4096))
+    _check_fwd(case, o, lse, rows)
+
+
+def test_forward_then_backward_matches_oracle():
+    """A training step: the GPU forward's O/LSE into the GPU backward, against the
+    oracle backward of the same O/LSE."""
+    case = make_case(SMALL["gqa_det"])
+    d = to_device(case)
+    o, lse = _gpu_fwd(case, d)
+    case["o"], case["lse"] = o.cpu(), lse.cpu()
+    dq, dk, dv = gpu_backward(case)
+    rq, rk, rv = oracle_backward(case)
+    assert_close("dq", dq.double().cpu().numpy(), rq)
+    assert_close("dk", dk.double().cpu().numpy(), rk)
+    assert_close("dv", dv.double().cpu().numpy(), rv)
