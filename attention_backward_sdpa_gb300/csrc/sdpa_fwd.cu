@@ -249,11 +249,18 @@ __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
         v_hi = (int)min((long long)BK - 1, min((long long)Lk - 1, k_vis_hi) - k0);
         v_lo = (int)max(0ll, k_vis_lo - k0);
       }
+      // A tile whose keys this row all sees (every tile but the edges) takes the
+      // unmasked path: the maximum of the raw scores, then one FFMA + ex2 each.
+      const bool full = v_lo == 0 && v_hi == BK - 1;
       float mt = -INFINITY;
+      if (full) {
 #pragma unroll
-      for (int i = 0; i < BK; ++i) {
-        const float x = __uint_as_float(sr[i >> 5][i & 31]) * c;
-        if (i >= v_lo && i <= v_hi) mt = fmaxf(mt, x);
+        for (int i = 0; i < BK; ++i) mt = fmaxf(mt, __uint_as_float(sr[i >> 5][i & 31]));
+        mt *= c;  // c > 0
+      } else {
+#pragma unroll
+        for (int i = 0; i < BK; ++i)
+          if (i >= v_lo && i <= v_hi) mt = fmaxf(mt, __uint_as_float(sr[i >> 5][i & 31]) * c);
       }
       // Raise the reference when the tile's maximum exceeds it by more than the
       // threshold (or when it is the row's first visible key).
@@ -291,23 +298,36 @@ __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
       m = m_new;
       // P = exp2(x - m) on visible keys, written as bf16 pairs into the slot's
       // first 64 columns (this thread's own lane, already read above).
-      float rs = 0.f;
+      float rs0 = 0.f, rs1 = 0.f;
+      const float neg_m = -m;
 #pragma unroll
       for (int c16 = 0; c16 < 4; ++c16) {
         uint32_t w[16];
+        if (full) {
 #pragma unroll
-        for (int i2 = 0; i2 < 16; ++i2) {
-          const int i = c16 * 32 + 2 * i2;
-          const float x0 = __uint_as_float(sr[i >> 5][i & 31]) * c;
-          const float x1 = __uint_as_float(sr[(i + 1) >> 5][(i + 1) & 31]) * c;
-          const float p0 = (i >= v_lo && i <= v_hi) ? ex2_approx(x0 - m) : 0.f;
-          const float p1 = (i + 1 >= v_lo && i + 1 <= v_hi) ? ex2_approx(x1 - m) : 0.f;
-          rs += p0 + p1;
-          w[i2] = pack_bf16x2(p0, p1);
+          for (int i2 = 0; i2 < 16; ++i2) {
+            const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c16][2 * i2]), c, neg_m));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c16][2 * i2 + 1]), c, neg_m));
+            rs0 += p0;
+            rs1 += p1;
+            w[i2] = pack_bf16x2(p0, p1);
+          }
+        } else {
+#pragma unroll
+          for (int i2 = 0; i2 < 16; ++i2) {
+            const int i = c16 * 32 + 2 * i2;
+            const float p0 = (i >= v_lo && i <= v_hi)
+                                 ? ex2_approx(fmaf(__uint_as_float(sr[c16][2 * i2]), c, neg_m)) : 0.f;
+            const float p1 = (i + 1 >= v_lo && i + 1 <= v_hi)
+                                 ? ex2_approx(fmaf(__uint_as_float(sr[c16][2 * i2 + 1]), c, neg_m)) : 0.f;
+            rs0 += p0;
+            rs1 += p1;
+            w[i2] = pack_bf16x2(p0, p1);
+          }
         }
         tmem_st16(t_lane + 128u * s + c16 * 16, w);
       }
-      l += rs;
+      l += rs0 + rs1;
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars[BAR_PREADY + s]);
