@@ -13,18 +13,23 @@
 // Schedule. One CTA owns 128 query rows of one (batch, query head) and walks the
 // key tiles (128 keys) that any of its rows sees, in ascending order. Per key tile j:
 //   G1  S   = Q K_j^T        -> tensor-memory slot j % 2 (128 fp32 columns)
-//       P   = exp2(S * scale * log2e - m)   (the softmax warpgroup, one row per thread)
-//           -> bf16 into the slot's first 64 columns
-//   G2  O  += P V_j           (A = P from tensor memory, B = V_j MN-major)
-// m is a per-row running reference that is raised only when the row's maximum
-// exceeds it by more than 8 (in log2 units). Until then P stays below 2^8, which
-// bf16 and fp32 hold exactly enough, so the O accumulator is rescaled only on
-// those rare raises (after the previous G2 has completed). The row sum l is kept
-// in fp32 alongside; at the end O / l and LSE = (m + log2 l) * ln 2.
+//       P   = exp2(S * scale * log2e - m)   (two softmax warpgroups, half a row each)
+//           -> bf16 pairs, half h into the slot's columns [64 h, 64 h + 32)
+//   G2  O_h += P[:, half h] V_j[half h, :]   (A = P from tensor memory, B = V_j
+//           MN-major; keys 0-63 into O_0, 64-127 into O_1)
+// Each half h of a row keeps its own softmax state: a running reference m_h
+// that is raised only when the half's maximum exceeds it by more than 8 (in
+// log2 units), an fp32 sum l_h and the accumulator O_h. Until a raise P stays
+// below 2^8, which bf16 and fp32 hold exactly enough, so O_h is rescaled only on
+// those rare raises (after the previous G2 has completed). At the end, with
+// M = max(m_0, m_1) and a_h = 2^(m_h - M): O = (O_0 a_0 + O_1 a_1) / L,
+// L = l_0 a_0 + l_1 a_1, LSE = (M + log2 L) * ln 2.
 //
-// Warps: 0-3 the softmax warpgroup (thread = query row = tensor-memory lane), 4 the
-// TMA producer (Q once, K/V stage ring), 5 the MMA issuer and tensor-memory owner,
-// 6-7 idle. Tensor memory: slots at [0,128) and [128,256), O at [256, 256+D_v).
+// Warps: 0-7 two softmax warpgroups (a row's keys split between warps w and w+4,
+// which read the same tensor-memory lanes; one warp per SMSP did not hide the
+// instruction latencies), 8 the TMA producer (Q once, K/V stage ring), 9 the MMA
+// issuer and tensor-memory owner, 10-11 idle. Tensor memory: S/P slots at
+// [0,128) and [128,256), O_0 at [256, 256+D_v), O_1 at [384, 384+D_v).
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -35,20 +40,21 @@ namespace sdpa {
 
 namespace fwd_kernel {
 
-constexpr int THREADS = 256;
+constexpr int THREADS = 384;
 constexpr int BM = 128;  // query rows per CTA
 constexpr int BK = 128;  // keys per tile
 constexpr uint64_t WAIT_LIMIT_NS = 4000000000ull;
 constexpr float RESCALE_THRESHOLD = 8.f;  // log2 units
+constexpr int NSLOT = 2;                  // S/P slots in tensor memory
 
 enum : int {
   BAR_QFULL = 0,
-  BAR_KVFULL = 1,   // + stage (up to 4)
-  BAR_KVEMPTY = 5,  // + stage: G2 of the tile completed (K read by G1 before it)
-  BAR_SFULL = 9,    // + slot: S in tensor memory
-  BAR_PREADY = 11,  // + slot, 128 arrivals: P written
-  BAR_PVDONE = 13,  // + slot: G2 of the slot's tile completed
-  NUM_BARS = 15
+  BAR_KVFULL = 1,                // + stage (up to 4)
+  BAR_KVEMPTY = 5,               // + stage: G2 of the tile completed (K read by G1 before it)
+  BAR_SFULL = 9,                 // + slot: S in tensor memory
+  BAR_PREADY = BAR_SFULL + NSLOT,  // + slot, 256 arrivals: P written (both halves)
+  BAR_PVDONE = BAR_PREADY + NSLOT, // + slot: G2 of the slot's tile completed
+  NUM_BARS = BAR_PVDONE + NSLOT
 };
 
 template <int DQK, int DV>
@@ -58,19 +64,21 @@ struct Layout {
   static constexpr int TILE_K = BK * DQK * 2;
   static constexpr int TILE_V = BK * DV * 2;
   static constexpr int STAGE = TILE_K + TILE_V;
-  static constexpr int NS_FIT = (232448 - TILE_Q - NUM_BARS * 8 - 64) / STAGE;
+  static constexpr int NS_FIT = (232448 - TILE_Q - NUM_BARS * 8 - 2 * 256 * 4 - 64) / STAGE;
   static constexpr int NS = NS_FIT > 4 ? 4 : NS_FIT;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = TILE_Q;
   static constexpr int OFF_BAR = OFF_KV + NS * STAGE;
-  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int OFF_XCH = OFF_BAR + NUM_BARS * 8;   // the halves' (m, l) at the end
+  static constexpr int OFF_MISC = OFF_XCH + 2 * 256 * 4;
   // More than half an SM's shared memory keeps one CTA per SM, so the 512
   // tensor-memory columns are never contended.
   static constexpr int BYTES_RAW = OFF_MISC + 64;
   static constexpr int BYTES = BYTES_RAW > 120 * 1024 ? BYTES_RAW : 120 * 1024;
-  static constexpr uint32_t COL_O = 256;
+  // Two O accumulators, one per half of the keys: O_h at COL_O + 128 h.
+  static constexpr uint32_t COL_O = 128 * NSLOT;
   static_assert(NS >= 2, "stage ring");
-  static_assert(COL_O + DV <= 512, "tensor memory budget");
+  static_assert(COL_O + 128 + DV <= 512 && DV <= 128, "tensor memory budget");
   static_assert(BYTES <= 232448, "shared memory budget");
   static_assert(TILE_Q % 1024 == 0 && TILE_K % 1024 == 0 && TILE_V % 1024 == 0, "alignment");
   static_assert(DV <= DQK, "O staging reuses the Q tile");
@@ -128,16 +136,16 @@ __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
   if (tid == 0) {
     *abort_flag = 0;
     for (int i = 0; i < NUM_BARS; ++i)
-      mbar_init(&bars[i], (i == BAR_PREADY || i == BAR_PREADY + 1) ? 128 : 1);
+      mbar_init(&bars[i], (i >= BAR_PREADY && i < BAR_PREADY + NSLOT) ? 256 : 1);
     fence_mbar_init();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == 8 && lane == 0) {
     prefetch_tmap(&maps.q);
     prefetch_tmap(&maps.k);
     prefetch_tmap(&maps.v);
     prefetch_tmap(&maps.o);
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -146,7 +154,7 @@ __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && n > 0) {
       mbar_arrive_expect_tx(&bars[BAR_QFULL], L::TILE_Q);
@@ -168,10 +176,10 @@ __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
           tma_load_3d(sV + blk * L::BLK, &maps.v, full, blk * 64, k0, kvh);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     // Order: G1(0), then for j >= 1: G1(j), G2(j-1); finally G2(n-1). G1(j)
-    // reuses the slot of tile j-2, whose P G2(j-2) read; G2(j-1) needs P(j-1).
+    // reuses the slot of tile j-3, whose P G2(j-3) read; G2(j-1) needs P(j-1).
     constexpr uint32_t ID_S = idesc_bf16_f32(BM, BK, false, false);  // S = Q K^T
     constexpr uint32_t ID_O = idesc_bf16_f32(BM, DV, false, true);   // O += P V
     constexpr uint64_t T_KMAJ = sdesc_sw128_template(16, 1024);
@@ -180,9 +188,10 @@ __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
     const uint32_t aQ = smem_u32(sQ);
     for (int j = 0; j <= n && ok; ++j) {
       if (j < n) {
-        const int st = j % NS, s = j & 1;
+        const int st = j % NS, s = j % NSLOT;
         ok = mbar_wait(&bars[BAR_KVFULL + st], (j / NS) & 1, abort_flag, WAIT_LIMIT_NS);
-        if (ok && j >= 2) ok = mbar_wait(&bars[BAR_PVDONE + s], ((j - 2) >> 1) & 1, abort_flag, WAIT_LIMIT_NS);
+        if (ok && j >= NSLOT)
+          ok = mbar_wait(&bars[BAR_PVDONE + s], ((j - NSLOT) / NSLOT) & 1, abort_flag, WAIT_LIMIT_NS);
         if (!ok) break;
         __syncwarp();
         tc_fence_after();
@@ -198,49 +207,58 @@ __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
         __syncwarp();
       }
       if (j >= 1) {
-        const int u = j - 1, su = u & 1, stu = u % NS;
-        if (!mbar_wait(&bars[BAR_PREADY + su], (u >> 1) & 1, abort_flag, WAIT_LIMIT_NS)) break;
+        const int u = j - 1, su = u % NSLOT, stu = u % NS;
+        if (!mbar_wait(&bars[BAR_PREADY + su], (u / NSLOT) & 1, abort_flag, WAIT_LIMIT_NS)) break;
         __syncwarp();
         tc_fence_after();
         if (elect_one()) {
           const uint32_t aV = smem_u32(sKV + stu * L::STAGE + L::TILE_K);
+          // O_h += P[:, keys of half h] V[keys of half h, :]; P of half h sits in
+          // the slot's columns [64 h, 64 h + 32).
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            mma_ts(tmem + L::COL_O, tmem + 128u * su + 8 * k, sdesc_at(T_MN_V, aV + k * 2048), ID_O,
-                   (u > 0 || k > 0));
+            mma_ts(tmem + L::COL_O + 128u * (k >> 2), tmem + 128u * su + 64u * (k >> 2) + 8 * (k & 3),
+                   sdesc_at(T_MN_V, aV + k * 2048), ID_O, (u > 0 || (k & 3) > 0));
           mma_commit(&bars[BAR_PVDONE + su]);
           if (u + NS < n) mma_commit(&bars[BAR_KVEMPTY + stu]);
         }
         __syncwarp();
       }
     }
-  } else if (warp < 4) {
-    // ------------------------------------------------------------ softmax warpgroup
-    const int row = warp * 32 + lane;
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ softmax warpgroups
+    // Warps w and w + 4 read the same tensor-memory lanes (w % 4): warpgroup
+    // `half` takes keys [64 half, 64 half + 64) of each tile. Each half keeps a
+    // softmax of its own (reference m, sum l, accumulator O_half): no exchange
+    // per tile; the two are combined once at the end.
+    const int half = warp >> 2, quarter = warp & 3;
+    const int row = quarter * 32 + lane;
     const int q = q0 + row;
-    const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+    float* xch = reinterpret_cast<float*>(smem + L::OFF_XCH);  // epilogue: [m, l][2 half][128]
     const float c = p.scale_log2;
     const bool live = q < Lq;
-    // Running reference m (log2 units) and row sum l; the sink starts them.
-    float m = -INFINITY, l = 0.f;
-    if (p.sink) {
+    float m = -INFINITY, l = 0.f;  // this half's reference and sum (the sink goes to half 0)
+    if (p.sink && half == 0) {
       m = p.sink[h] * 1.4426950408889634f;
       l = 1.f;
     }
+    const uint32_t col_o = L::COL_O + 128u * half;  // this half's O accumulator
     bool ok = true;
     const long long k_vis_hi = p.causal ? (long long)q + diag + Rp : (1ll << 40);
     const long long k_vis_lo = has_window ? (long long)q + diag - p.window_left : -(1ll << 40);
+    const int i0 = half * 64;  // this half's first key within a tile
     for (int j = 0; j < n && ok; ++j) {
-      const int s = j & 1;
+      const int s = j % NSLOT;
       const int k0 = (kt_lo + j) * BK;
-      if (!mbar_wait(&bars[BAR_SFULL + s], (j >> 1) & 1, abort_flag, WAIT_LIMIT_NS)) { ok = false; break; }
+      if (!mbar_wait(&bars[BAR_SFULL + s], (j / NSLOT) & 1, abort_flag, WAIT_LIMIT_NS)) { ok = false; break; }
       __syncwarp();
       tc_fence_after();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int c32 = 0; c32 < 4; ++c32) tmem_ld32(t_lane + 128u * s + c32 * 32, sr[c32]);
-#pragma unroll
-      for (int c32 = 0; c32 < 4; ++c32) tmem_ld_wait(sr[c32]);
+      uint32_t sr[2][32];
+      tmem_ld32(t_lane + 128u * s + i0, sr[0]);
+      tmem_ld32(t_lane + 128u * s + i0 + 32, sr[1]);
+      tmem_ld_wait(sr[0]);
+      tmem_ld_wait(sr[1]);
       // Visible keys of this row within the tile: [v_lo, v_hi] relative to k0.
       int v_lo = 0, v_hi = BK - 1;
       if (!live) {
@@ -249,30 +267,36 @@ __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
         v_hi = (int)min((long long)BK - 1, min((long long)Lk - 1, k_vis_hi) - k0);
         v_lo = (int)max(0ll, k_vis_lo - k0);
       }
-      // A tile whose keys this row all sees (every tile but the edges) takes the
-      // unmasked path: the maximum of the raw scores, then one FFMA + ex2 each.
-      const bool full = v_lo == 0 && v_hi == BK - 1;
-      float mt = -INFINITY;
+      // Unmasked path when this half is fully visible for the whole warp (every
+      // tile but the mask edges). The choice is warp-uniform: the tensor-memory
+      // stores below are .sync.aligned, and a warp split between the two paths
+      // would reach them diverged.
+      const bool full = __all_sync(0xffffffffu, v_lo <= i0 && v_hi >= i0 + 63);
+      float mp[8];
+#pragma unroll
+      for (int a = 0; a < 8; ++a) mp[a] = -INFINITY;
       if (full) {
 #pragma unroll
-        for (int i = 0; i < BK; ++i) mt = fmaxf(mt, __uint_as_float(sr[i >> 5][i & 31]));
-        mt *= c;  // c > 0
+        for (int i = 0; i < 64; ++i) mp[i & 7] = fmaxf(mp[i & 7], __uint_as_float(sr[i >> 5][i & 31]));
       } else {
 #pragma unroll
-        for (int i = 0; i < BK; ++i)
-          if (i >= v_lo && i <= v_hi) mt = fmaxf(mt, __uint_as_float(sr[i >> 5][i & 31]) * c);
+        for (int i = 0; i < 64; ++i)
+          if (i0 + i >= v_lo && i0 + i <= v_hi) mp[i & 7] = fmaxf(mp[i & 7], __uint_as_float(sr[i >> 5][i & 31]));
       }
+      const float mt = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * c;  // c > 0
       // Raise the reference when the tile's maximum exceeds it by more than the
       // threshold (or when it is the row's first visible key).
       const bool raise = mt > m + RESCALE_THRESHOLD || (m == -INFINITY && mt > -INFINITY);
       const float m_new = raise ? mt : m;
       const float alpha = raise ? ex2_approx(m - m_new) : 1.f;  // 0 when m was -inf
-      // O holds this row's contributions of tiles < j when l > 0 and j > 0. Its
-      // lane is rescaled once G2(j-1) has completed (no G2 reads or writes O
-      // meanwhile: G2(j) waits for this warpgroup's P_READY(j)).
-      const bool rescale_o = raise && j > 0 && l > 0.f;
+      // O_half holds contributions of earlier tiles once m is finite and j > 0.
+      // It is rescaled once G2(j-1) has completed (G2(j) waits for this tile's
+      // P_READY).
+      const bool rescale_o = raise && j > 0 && m > -INFINITY;
       if (__any_sync(0xffffffffu, rescale_o)) {
-        if (!mbar_wait(&bars[BAR_PVDONE + (s ^ 1)], ((j - 1) >> 1) & 1, abort_flag, WAIT_LIMIT_NS)) {
+        if (!mbar_wait(&bars[BAR_PVDONE + (j - 1) % NSLOT], ((j - 1) / NSLOT) & 1, abort_flag,
+                       WAIT_LIMIT_NS)) {
           ok = false;
         }
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -280,8 +304,9 @@ __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
         const float f = rescale_o ? alpha : 1.f;
 #pragma unroll 1
         for (int c32 = 0; c32 < DV / 32; ++c32) {
+          const uint32_t col = col_o + c32 * 32;
           uint32_t o[32];
-          tmem_ld32(t_lane + L::COL_O + c32 * 32, o);
+          tmem_ld32(t_lane + col, o);
           tmem_ld_wait(o);
           uint32_t w0[16], w1[16];
 #pragma unroll
@@ -289,90 +314,116 @@ __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
             w0[i] = __float_as_uint(__uint_as_float(o[i]) * f);
             w1[i] = __float_as_uint(__uint_as_float(o[16 + i]) * f);
           }
-          tmem_st16(t_lane + L::COL_O + c32 * 32, w0);
-          tmem_st16(t_lane + L::COL_O + c32 * 32 + 16, w1);
+          tmem_st16(t_lane + col, w0);
+          tmem_st16(t_lane + col + 16, w1);
         }
         tmem_st_wait();
       }
       l *= alpha;
       m = m_new;
-      // P = exp2(x - m) on visible keys, written as bf16 pairs into the slot's
-      // first 64 columns (this thread's own lane, already read above).
-      float rs0 = 0.f, rs1 = 0.f;
+      // P = exp2(x - m) on visible keys, as bf16 pairs into the slot's columns
+      // [64 half, 64 half + 32): inside this half's own S columns, which this
+      // warp has already read. (Writing into the other half's S columns raced
+      // with that half's warp, which may still be a tile behind.)
+      float rs[8];
+#pragma unroll
+      for (int a = 0; a < 8; ++a) rs[a] = 0.f;
       const float neg_m = -m;
 #pragma unroll
-      for (int c16 = 0; c16 < 4; ++c16) {
+      for (int c16 = 0; c16 < 2; ++c16) {
         uint32_t w[16];
         if (full) {
 #pragma unroll
           for (int i2 = 0; i2 < 16; ++i2) {
             const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c16][2 * i2]), c, neg_m));
             const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c16][2 * i2 + 1]), c, neg_m));
-            rs0 += p0;
-            rs1 += p1;
+            rs[(2 * i2) & 7] += p0;
+            rs[(2 * i2 + 1) & 7] += p1;
             w[i2] = pack_bf16x2(p0, p1);
           }
         } else {
 #pragma unroll
           for (int i2 = 0; i2 < 16; ++i2) {
-            const int i = c16 * 32 + 2 * i2;
+            const int i = i0 + c16 * 32 + 2 * i2;
             const float p0 = (i >= v_lo && i <= v_hi)
                                  ? ex2_approx(fmaf(__uint_as_float(sr[c16][2 * i2]), c, neg_m)) : 0.f;
             const float p1 = (i + 1 >= v_lo && i + 1 <= v_hi)
                                  ? ex2_approx(fmaf(__uint_as_float(sr[c16][2 * i2 + 1]), c, neg_m)) : 0.f;
-            rs0 += p0;
-            rs1 += p1;
+            rs[(2 * i2) & 7] += p0;
+            rs[(2 * i2 + 1) & 7] += p1;
             w[i2] = pack_bf16x2(p0, p1);
           }
         }
-        tmem_st16(t_lane + 128u * s + c16 * 16, w);
+        __syncwarp();
+        tmem_st16(t_lane + 128u * s + half * 64 + c16 * 16, w);
       }
-      l += rs0 + rs1;
+      l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars[BAR_PREADY + s]);
     }
 
-    // ---- epilogue: O / l (bf16) staged row by row into the Q tile in the
-    // 128-byte-swizzled box layout and written by TMA (rows past S_q dropped);
-    // LSE in natural-log units.
+    // ---- epilogue: the halves combine, O = (O_0 a_0 + O_1 a_1) / (l_0 a_0 + l_1 a_1)
+    // with a_h = 2^(m_h - M), M = max(m_0, m_1). O (bf16) is staged row by row
+    // into the Q tile in the 128-byte-swizzled box layout and written by TMA
+    // (rows past S_q dropped); each half writes D_v/2 columns. LSE in
+    // natural-log units.
     const bool have_o = n > 0 && ok;
     if (have_o) {
-      ok = mbar_wait(&bars[BAR_PVDONE + ((n - 1) & 1)], ((n - 1) >> 1) & 1, abort_flag, WAIT_LIMIT_NS);
+      ok = mbar_wait(&bars[BAR_PVDONE + (n - 1) % NSLOT], ((n - 1) / NSLOT) & 1, abort_flag,
+                     WAIT_LIMIT_NS);
     }
     const bool warp_ok = __all_sync(0xffffffffu, ok);
     if (have_o && warp_ok) tc_fence_after();
-    const float inv_l = (l > 0.f && live) ? 1.f / l : 0.f;
+    xch[half * 128 + row] = m;
+    xch[256 + half * 128 + row] = l;
+    named_bar_sync(1, 256);
+    const float m0 = xch[row], m1 = xch[128 + row];
+    const float l0 = xch[256 + row], l1 = xch[384 + row];
+    const float M = fmaxf(m0, m1);
+    const float a0 = (m0 == -INFINITY) ? 0.f : ex2_approx(m0 - M);
+    const float a1 = (m1 == -INFINITY) ? 0.f : ex2_approx(m1 - M);
+    const float lt = l0 * a0 + l1 * a1;
+    const float inv_l = (lt > 0.f && live) ? 1.f / lt : 0.f;
+    const float f0 = a0 * inv_l, f1 = a1 * inv_l;
     uint8_t* dst_row = sQ + row * 128;
 #pragma unroll 1
-    for (int c32 = 0; c32 < DV / 32; ++c32) {
-      uint32_t o[32];
+    for (int c32 = 0; c32 < DV / 64; ++c32) {
+      const int cbase = half * (DV / 2) + c32 * 32;  // first O column of this chunk
+      uint32_t o0[32], o1[32];
       if (have_o && warp_ok) {
-        tmem_ld32(t_lane + L::COL_O + c32 * 32, o);
-        tmem_ld_wait(o);
+        tmem_ld32(t_lane + L::COL_O + cbase, o0);
+        tmem_ld32(t_lane + L::COL_O + 128 + cbase, o1);
+        tmem_ld_wait(o0);
+        tmem_ld_wait(o1);
       } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = 0u;
+        for (int i = 0; i < 32; ++i) o0[i] = o1[i] = 0u;
       }
 #pragma unroll
       for (int v8 = 0; v8 < 4; ++v8) {
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          y[e] = __uint_as_float(o0[v8 * 8 + e]) * f0 + __uint_as_float(o1[v8 * 8 + e]) * f1;
         uint4 w;
-        w.x = pack_bf16x2(__uint_as_float(o[v8 * 8 + 0]) * inv_l, __uint_as_float(o[v8 * 8 + 1]) * inv_l);
-        w.y = pack_bf16x2(__uint_as_float(o[v8 * 8 + 2]) * inv_l, __uint_as_float(o[v8 * 8 + 3]) * inv_l);
-        w.z = pack_bf16x2(__uint_as_float(o[v8 * 8 + 4]) * inv_l, __uint_as_float(o[v8 * 8 + 5]) * inv_l);
-        w.w = pack_bf16x2(__uint_as_float(o[v8 * 8 + 6]) * inv_l, __uint_as_float(o[v8 * 8 + 7]) * inv_l);
-        const int piece = (c32 & 1) * 4 + v8;
-        *reinterpret_cast<uint4*>(dst_row + (c32 >> 1) * L::BLK + ((piece ^ (row & 7)) << 4)) = w;
+        w.x = pack_bf16x2(y[0], y[1]);
+        w.y = pack_bf16x2(y[2], y[3]);
+        w.z = pack_bf16x2(y[4], y[5]);
+        w.w = pack_bf16x2(y[6], y[7]);
+        const int cc = cbase + v8 * 8;          // column of this 16-byte piece
+        const int piece = (cc & 63) >> 3;
+        *reinterpret_cast<uint4*>(dst_row + (cc >> 6) * L::BLK + ((piece ^ (row & 7)) << 4)) = w;
       }
     }
-    if (q < p.Sq) {
+    if (half == 0 && q < p.Sq) {
       float lse = -INFINITY;
-      if (l > 0.f) lse = (m + __log2f(l)) * 0.6931471805599453f;  // a padded row with a sink: the sink
+      if (lt > 0.f) lse = (M + __log2f(lt)) * 0.6931471805599453f;  // a padded row with a sink: the sink
       p.lse[(long long)bh * p.Sq + q] = lse;
     }
     fence_proxy_async_smem();
-    named_bar_sync(1, 128);
-    if (row == 0) {
+    named_bar_sync(1, 256);
+    if (half == 0 && row == 0) {
       for (int blk = 0; blk < DV / 64; ++blk) tma_store_3d(&maps.o, sQ + blk * L::BLK, blk * 64, q0, bh);
       bulk_commit_group();
       bulk_wait_group_read0();
@@ -382,7 +433,7 @@ __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
   tc_fence_before();
   __syncthreads();
   if (*abort_flag && tid == 0) atomicOr(p.status, STATUS_TIMEOUT);
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }

@@ -292,7 +292,8 @@ FWD_CASES = {
     "br_causal_long_q": SMALL["br_causal_long_q"],
     "tl_causal_long_q_d64": SMALL["tl_causal_long_q"],
     "window_causal": SMALL["window_causal"],
-    "window_only": SMALL["window_only"],
+    "window_only": SMALL["window_only"],        # warps whose rows split across mask paths
+    "d128_dense_ragged": SMALL["d128_dense_ragged"],
     "gqa_det": SMALL["gqa_det"],
     "det_padded_odd": SMALL["det_padded_odd"],
     "single_query": SMALL["single_query"],
