@@ -145,3 +145,32 @@ def test_python_binding_rejects_cpu_tensors():
     lse = torch.zeros(1, 2, 128)
     with pytest.raises(ValueError):
         pkg.sdpa_bwd(x, x, x, x, x, lse)
+
+
+def call_fwd(lib, ptrs=None, B=1, Hq=2, Hkv=2, Sq=128, Skv=128, Dqk=128, Dv=128, causal=0, wr=-1,
+             sink=None):
+    ptrs = ptrs or [FAKE] * 5
+    vp = [ctypes.c_void_p(p) if p is not None else None for p in ptrs]
+    return lib.sdpa_fwd(*vp, B, Hq, Hkv, Sq, Skv, Dqk, Dv, ctypes.c_float(0.0), causal, 0, -1, wr,
+                        None, None, None if sink is None else ctypes.c_void_p(sink), None)
+
+
+def test_forward_argument_validation(lib):
+    lib.sdpa_fwd.restype = ctypes.c_int
+    assert call_fwd(lib, Hq=3, Hkv=2) == INVALID
+    assert call_fwd(lib, B=0) == INVALID
+    assert call_fwd(lib, Dqk=96, Dv=96) == UNSUPPORTED
+    assert call_fwd(lib, Dqk=192, Dv=192) == UNSUPPORTED
+    for i in range(5):
+        ptrs = [FAKE] * 5
+        ptrs[i] = None
+        assert call_fwd(lib, ptrs) == INVALID
+    for i in range(4):  # q, k, v, o: 16-byte alignment
+        ptrs = [FAKE] * 5
+        ptrs[i] = FAKE + 8
+        assert call_fwd(lib, ptrs) == ALIGN
+    ptrs = [FAKE] * 5
+    ptrs[4] = FAKE + 2  # lse: 4-byte alignment
+    assert call_fwd(lib, ptrs) == ALIGN
+    assert call_fwd(lib, sink=FAKE + 1) == ALIGN
+    assert call_fwd(lib, wr=3, causal=0) == UNSUPPORTED
