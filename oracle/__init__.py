@@ -34,6 +34,8 @@ class _Cfg(ctypes.Structure):
         ("window_left", ctypes.c_int), ("window_right", ctypes.c_int),
         ("seq_q_lens", ctypes.POINTER(ctypes.c_int32)),
         ("seq_kv_lens", ctypes.POINTER(ctypes.c_int32)),
+        ("bias", ctypes.POINTER(ctypes.c_double)),
+        ("bias_batch", ctypes.c_int),
     ]
 
 
@@ -59,7 +61,7 @@ class Problem:
     def resolved_scale(self) -> float:
         return 1.0 / math.sqrt(self.Dqk) if self.scale is None else float(self.scale)
 
-    def _struct(self):
+    def _struct(self, bias=None):
         keep = []
 
         def lens(a):
@@ -72,8 +74,22 @@ class Problem:
         s = _Cfg(self.B, self.Hq, self.Hkv, self.Sq, self.Skv, self.Dqk, self.Dv,
                  self.resolved_scale, int(self.causal), int(self.bottom_right),
                  int(self.window_left), int(self.window_right),
-                 lens(self.seq_q_lens), lens(self.seq_kv_lens))
+                 lens(self.seq_q_lens), lens(self.seq_kv_lens),
+                 ctypes.POINTER(ctypes.c_double)(), 0)
+        if bias is not None:
+            arr = self.check_bias(bias)
+            keep.append(arr)
+            s.bias = _p(arr)
+            s.bias_batch = arr.shape[0]
         return s, keep
+
+    def check_bias(self, bias):
+        """The bias as a contiguous float64 (1|B, Hq, Sq, Skv) array."""
+        arr = np.ascontiguousarray(np.asarray(bias, dtype=np.float64))
+        if arr.ndim != 4 or arr.shape[0] not in (1, self.B) or \
+                tuple(arr.shape[1:]) != (self.Hq, self.Sq, self.Skv):
+            raise ValueError(f"bias must be (1|B, Hq, Sq, Skv), got {arr.shape}")
+        return arr
 
 
 _lib = None
@@ -96,6 +112,7 @@ def _load():
         lib.oracle_backward.argtypes = [C, P, P, P, P, P, P, P, P, P]
         lib.oracle_backward_sampled.argtypes = [C, P, P, P, P, P, P, ctypes.c_long, I64, P,
                                                 ctypes.c_long, I64, P, P]
+        lib.oracle_dbias.argtypes = [C, P, P, P, P, P, P, P]
         lib.oracle_count_visible.argtypes = [C]
         lib.oracle_count_visible.restype = ctypes.c_longlong
         lib.oracle_max_threads.restype = ctypes.c_int
@@ -120,9 +137,10 @@ def _check_heads(p: Problem):
         raise ValueError("H_kv must divide H_q")
 
 
-def forward(p: Problem, q, k, v, sink=None):
+def forward(p: Problem, q, k, v, sink=None, bias=None):
     """Returns (O, LSE) in float64; LSE is the natural-log row log-sum-exp.
-    ``sink`` (H_q,) adds a per-head sink logit to every row's denominator."""
+    ``sink`` (H_q,) adds a per-head sink logit to every row's denominator;
+    ``bias`` (1|B, H_q, S_q, S_kv) is added to the scaled scores."""
     _check_heads(p)
     lib = _load()
     q = _f64(q, (p.B, p.Hq, p.Sq, p.Dqk))
@@ -130,7 +148,7 @@ def forward(p: Problem, q, k, v, sink=None):
     v = _f64(v, (p.B, p.Hkv, p.Skv, p.Dv))
     o = np.zeros((p.B, p.Hq, p.Sq, p.Dv))
     lse = np.zeros((p.B, p.Hq, p.Sq))
-    s, keep = p._struct()
+    s, keep = p._struct(bias)
     if sink is None:
         lib.oracle_forward(ctypes.byref(s), _p(q), _p(k), _p(v), _p(o), _p(lse))
     else:
@@ -162,8 +180,9 @@ def delta(p: Problem, o, do):
     return out
 
 
-def backward(p: Problem, q, k, v, o, do, lse):
-    """Returns (dQ, dK, dV) in float64 from the given forward tensors."""
+def backward(p: Problem, q, k, v, o, do, lse, bias=None):
+    """Returns (dQ, dK, dV) in float64 from the given forward tensors (``bias``
+    as in forward(): the replayed P includes it)."""
     _check_heads(p)
     lib = _load()
     q = _f64(q, (p.B, p.Hq, p.Sq, p.Dqk))
@@ -175,13 +194,13 @@ def backward(p: Problem, q, k, v, o, do, lse):
     dq = np.zeros_like(q)
     dk = np.zeros_like(k)
     dv = np.zeros_like(v)
-    s, keep = p._struct()
+    s, keep = p._struct(bias)
     lib.oracle_backward(ctypes.byref(s), _p(q), _p(k), _p(v), _p(o), _p(do), _p(lse),
                         _p(dq), _p(dk), _p(dv))
     return dq, dk, dv
 
 
-def backward_sampled(p: Problem, q, k, v, o, do, lse, q_rows, kv_rows):
+def backward_sampled(p: Problem, q, k, v, o, do, lse, q_rows, kv_rows, bias=None):
     """dQ at the flat query rows ``q_rows`` ((b*Hq + h)*Sq + q) and dK/dV at the
     flat key rows ``kv_rows`` ((b*Hkv + hk)*Skv + k). Returns three 2-D arrays."""
     _check_heads(p)
@@ -197,12 +216,29 @@ def backward_sampled(p: Problem, q, k, v, o, do, lse, q_rows, kv_rows):
     dq = np.zeros((len(qi), p.Dqk))
     dk = np.zeros((len(ki), p.Dqk))
     dv = np.zeros((len(ki), p.Dv))
-    s, keep = p._struct()
+    s, keep = p._struct(bias)
     I64 = ctypes.POINTER(ctypes.c_int64)
     lib.oracle_backward_sampled(ctypes.byref(s), _p(q), _p(k), _p(v), _p(o), _p(do), _p(lse),
                                 len(qi), qi.ctypes.data_as(I64), _p(dq),
                                 len(ki), ki.ctypes.data_as(I64), _p(dk), _p(dv))
     return dq, dk, dv
+
+
+def dbias(p: Problem, q, k, v, o, do, lse, bias):
+    """Gradient of the additive bias: dS = P * (dP - delta) at visible pairs,
+    shaped like ``bias``; a one-batch bias gets the sum over the batch rows."""
+    _check_heads(p)
+    lib = _load()
+    q = _f64(q, (p.B, p.Hq, p.Sq, p.Dqk))
+    k = _f64(k, (p.B, p.Hkv, p.Skv, p.Dqk))
+    v = _f64(v, (p.B, p.Hkv, p.Skv, p.Dv))
+    o = _f64(o, (p.B, p.Hq, p.Sq, p.Dv))
+    do = _f64(do, (p.B, p.Hq, p.Sq, p.Dv))
+    lse = _f64(lse, (p.B, p.Hq, p.Sq))
+    s, keep = p._struct(bias)
+    out = np.zeros((s.bias_batch, p.Hq, p.Sq, p.Skv))
+    lib.oracle_dbias(ctypes.byref(s), _p(q), _p(k), _p(v), _p(o), _p(do), _p(lse), _p(out))
+    return out
 
 
 def count_visible(p: Problem) -> int:

@@ -26,6 +26,12 @@
  *     denominator without a value row, so the forward LSE includes it and
  *     dQ/dK/dV keep their formulas; the extra output is
  *     dsink[h] = -sum_{b,q} exp(sink[h] - LSE[b,h,q]) * delta[b,h,q].
+ *   - Additive bias (Capabilities list): a (1|B, H_q, S_q, S_kv) tensor added
+ *     to the scaled scores before the softmax, s_qk = scale * Q_q.K_k +
+ *     bias[b,h,q,k]; the forward LSE includes it, so the backward replays P
+ *     with it and keeps its formulas. The extra output is the gradient of the
+ *     bias, dBias = dS (the softmax VJP without the scale factor), summed over
+ *     the batch when one bias batch serves every batch row.
  *
  * Every quantity is computed straight from its definition, one output row at
  * a time, in double precision. There is no tiling, fusion or reordering.
@@ -49,6 +55,8 @@ typedef struct {
     int window_right;     /* R: widens the causal diagonal; < 0 means 0      */
     const int32_t *seq_q_lens;   /* (B,) or NULL: every row is S_q long     */
     const int32_t *seq_kv_lens;  /* (B,) or NULL: every row is S_kv long    */
+    const double *bias;   /* (bias_batch, Hq, Sq, Skv) additive bias, or NULL */
+    int bias_batch;       /* 1 (shared by every batch row) or B              */
 } oracle_cfg;
 
 /* ---- the mask predicate ("Causal, sliding-window, and padding masks") ---- */
@@ -85,6 +93,20 @@ static double dot(const double *a, const double *b, int n) {
     return acc;
 }
 
+/* Bias of query head bh (= b * Hq + h) at (q, k); 0 without a bias. */
+static double bias_at(const oracle_cfg *c, long bh, long q, long k) {
+    if (!c->bias) return 0.0;
+    long b = bh / c->Hq, h = bh % c->Hq;
+    long bb = c->bias_batch == 1 ? 0 : b;
+    return c->bias[((bb * c->Hq + h) * c->Sq + q) * c->Skv + k];
+}
+
+/* The score that enters the softmax: scale * Q_q . K_k + bias. */
+static double score(const oracle_cfg *c, const double *qr, const double *kr, long bh, long q,
+                    long k) {
+    return c->scale * dot(qr, kr, c->Dqk) + bias_at(c, bh, q, k);
+}
+
 int oracle_max_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();
@@ -116,7 +138,7 @@ long long oracle_count_visible(const oracle_cfg *c) {
 }
 
 /* Forward: LSE_q = log( sum_{visible k} exp(s_qk) [+ exp(sink_h)] ),
- * s_qk = scale * Q_q . K_k; O_q = sum_k exp(s_qk - LSE_q) V_k (the sink has no
+ * s_qk = scale * Q_q . K_k [+ bias]; O_q = sum_k exp(s_qk - LSE_q) V_k (the sink has no
  * value row). Without a sink an empty row gives LSE = -inf, O = 0; with one it
  * gives LSE = sink_h, O = 0. Rows at or past seq_q_lens[b] are empty rows.
  * `sink` is (H_q,) or NULL. */
@@ -140,7 +162,7 @@ void oracle_forward_sink(const oracle_cfg *c, const double *Q, const double *K, 
             double m = sk;
             for (long k = 0; k < c->Skv; ++k) {
                 if (!visible(c, Lq, Lk, q, k)) continue;
-                s[k] = c->scale * dot(qr, row_of(K, bhk, k, c->Skv, c->Dqk), c->Dqk);
+                s[k] = score(c, qr, row_of(K, bhk, k, c->Skv, c->Dqk), bh, q, k);
                 if (s[k] > m) m = s[k];
             }
             for (int d = 0; d < c->Dv; ++d) orow[d] = 0.0;
@@ -217,7 +239,7 @@ static void dq_row(const oracle_cfg *c, const double *Q, const double *K, const 
     for (long k = 0; k < c->Skv; ++k) {
         if (!visible(c, Lq, Lk, q, k)) continue;
         const double *kr = row_of(K, bhk, k, c->Skv, c->Dqk);
-        double p = prob(c, c->scale * dot(qr, kr, c->Dqk), lse);
+        double p = prob(c, score(c, qr, kr, bh, q, k), lse);
         double dp = dot(dor, row_of(V, bhk, k, c->Skv, c->Dv), c->Dv);
         double ds = p * (dp - D);
         for (int d = 0; d < c->Dqk; ++d) out[d] += ds * kr[d];
@@ -244,7 +266,7 @@ static void dkv_row(const oracle_cfg *c, const double *Q, const double *K, const
             if (!visible(c, Lq, Lk, q, k)) continue;
             const double *qr = row_of(Q, bh, q, c->Sq, c->Dqk);
             const double *dor = row_of(dO, bh, q, c->Sq, c->Dv);
-            double p = prob(c, c->scale * dot(qr, kr, c->Dqk), LSE[bh * c->Sq + q]);
+            double p = prob(c, score(c, qr, kr, bh, q, k), LSE[bh * c->Sq + q]);
             double dp = dot(dor, vr, c->Dv);
             double ds = p * (dp - delta[bh * c->Sq + q]);
             for (int d = 0; d < c->Dqk; ++d) dk_out[d] += ds * qr[d];
@@ -289,5 +311,43 @@ void oracle_backward_sampled(const oracle_cfg *c, const double *Q, const double 
     for (long i = 0; i < n_k; ++i)
         dkv_row(c, Q, K, V, dO, LSE, delta, k_idx[i] / c->Skv, k_idx[i] % c->Skv,
                 dK_rows + i * c->Dqk, dV_rows + i * c->Dv);
+    free(delta);
+}
+
+/* dBias (bias_batch, Hq, Sq, Skv): dS_qk = P_qk (dP_qk - delta_q) at every
+ * visible pair, 0 elsewhere; with bias_batch = 1 (and B > 1) the batch rows'
+ * dS are summed, in ascending b order. Requires c->bias (P replays the biased
+ * scores). */
+void oracle_dbias(const oracle_cfg *c, const double *Q, const double *K, const double *V,
+                  const double *O, const double *dO, const double *LSE, double *dBias) {
+    const int G = c->Hq / c->Hkv;
+    const long qrows = (long)c->B * c->Hq * c->Sq;
+    double *delta = (double *)malloc(sizeof(double) * (size_t)(qrows > 0 ? qrows : 1));
+    oracle_delta(c, O, dO, delta);
+    const long out_rows = (long)c->bias_batch * c->Hq * c->Sq;
+#pragma omp parallel for schedule(dynamic, 8)
+    for (long r = 0; r < out_rows; ++r) {
+        const long q = r % c->Sq, bbh = r / c->Sq;
+        const int bb = (int)(bbh / c->Hq), h = (int)(bbh % c->Hq);
+        double *out = dBias + r * c->Skv;
+        for (long k = 0; k < c->Skv; ++k) out[k] = 0.0;
+        const int b_lo = c->bias_batch == 1 ? 0 : bb;
+        const int b_hi = c->bias_batch == 1 ? c->B : bb + 1;
+        for (int b = b_lo; b < b_hi; ++b) {
+            int Lq, Lk;
+            lengths(c, b, &Lq, &Lk);
+            const long bh = (long)b * c->Hq + h, bhk = (long)b * c->Hkv + h / G;
+            const double *qr = row_of(Q, bh, q, c->Sq, c->Dqk);
+            const double *dor = row_of(dO, bh, q, c->Sq, c->Dv);
+            const double lse = LSE[bh * c->Sq + q], D = delta[bh * c->Sq + q];
+            for (long k = 0; k < c->Skv; ++k) {
+                if (!visible(c, Lq, Lk, q, k)) continue;
+                const double *kr = row_of(K, bhk, k, c->Skv, c->Dqk);
+                double p = prob(c, score(c, qr, kr, bh, q, k), lse);
+                double dp = dot(dor, row_of(V, bhk, k, c->Skv, c->Dv), c->Dv);
+                out[k] += p * (dp - D);
+            }
+        }
+    }
     free(delta);
 }

@@ -398,3 +398,165 @@ def test_sink_single_key_closed_form(oracle_mod):
         np.testing.assert_allclose(o[0, 0, i], w * v[0, 0, 0], atol=1e-15)
         want_ds -= (1.0 - w) * float(w * v[0, 0, 0] @ do[0, 0, i])
     assert abs(ds[0] - want_ds) < 1e-14
+
+
+# ---- additive bias (Capabilities list: a (1|B, H_q, S_q, S_kv) tensor added
+# after the scale and before the softmax, with its gradient dBias). The pins
+# fix the oracle's biased forward, its backward and dBias to central
+# differences, to torch's float attention mask under float64 autograd (which
+# also differentiates the mask), to the mask it can stand in for, to softmax
+# shift invariance and to one extra head dimension.
+BIAS_CASES = ["dense", "causal_br_long_kv", "padded", "gqa", "window_causal"]
+
+
+def _bias(p, seed, batch):
+    return np.random.default_rng(seed).standard_normal((batch, p.Hq, p.Sq, p.Skv)) * 0.7
+
+
+@pytest.mark.parametrize("batch1", [False, True])
+@pytest.mark.parametrize("name", BIAS_CASES)
+def test_dbias_matches_central_differences(oracle_mod, name, batch1):
+    p = FD_CASES[name]
+    q, k, v, do = _inputs(p, seed=21)
+    bias = _bias(p, 22, 1 if batch1 else p.B)
+    o, lse = oracle_mod.forward(p, q, k, v, bias=bias)
+    db = oracle_mod.dbias(p, q, k, v, o, do, lse, bias)
+    assert db.shape == bias.shape
+    h = 1e-6
+    fd = np.zeros_like(bias)
+    it = np.nditer(bias, flags=["multi_index"])
+    for _ in it:
+        idx = it.multi_index
+        bp, bm = bias.copy(), bias.copy()
+        bp[idx] += h
+        bm[idx] -= h
+        op, _ = oracle_mod.forward(p, q, k, v, bias=bp)
+        om, _ = oracle_mod.forward(p, q, k, v, bias=bm)
+        fd[idx] = float(np.sum((op - om) * do)) / (2 * h)
+    np.testing.assert_allclose(db, fd, rtol=0, atol=2e-7 * max(1.0, float(np.abs(fd).max())))
+
+
+@pytest.mark.parametrize("name,batch1", [("causal_br_long_kv", False), ("padded", True), ("gqa", False)])
+def test_bias_backward_matches_central_differences(oracle_mod, name, batch1):
+    p = FD_CASES[name]
+    q, k, v, do = _inputs(p, seed=23)
+    bias = _bias(p, 24, 1 if batch1 else p.B)
+    o, lse = oracle_mod.forward(p, q, k, v, bias=bias)
+    dq, dk, dv = oracle_mod.backward(p, q, k, v, o, do, lse, bias=bias)
+    h = 1e-6
+    for tensor, grad, which in ((q, dq, "q"), (k, dk, "k"), (v, dv, "v")):
+        fd = np.zeros_like(tensor)
+        it = np.nditer(tensor, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            args = {"q": q, "k": k, "v": v}
+            for sgn in (1, -1):
+                t = tensor.copy()
+                t[idx] += sgn * h
+                args[which] = t
+                o2, _ = oracle_mod.forward(p, args["q"], args["k"], args["v"], bias=bias)
+                fd[idx] += sgn * float(np.sum(o2 * do)) / (2 * h)
+        np.testing.assert_allclose(grad, fd, rtol=0, atol=2e-7 * max(1.0, float(np.abs(fd).max())),
+                                   err_msg=f"d{which}")
+
+
+@pytest.mark.parametrize("batch1", [False, True])
+@pytest.mark.parametrize("name", ["dense", "causal_tl", "window_only", "padded", "gqa", "mqa_scale"])
+def test_bias_matches_torch_sdpa_float64(oracle_mod, name, batch1):
+    """torch SDPA adds a float attn_mask to the scaled scores; under float64
+    autograd it returns dQ/dK/dV and the mask's gradient (summed over the batch
+    when the mask broadcasts), on rows that see at least one key."""
+    p = FD_CASES[name]
+    q, k, v, do = _inputs(p, seed=25)
+    bias = _bias(p, 26, 1 if batch1 else p.B)
+    G = p.Hq // p.Hkv
+    mask = _torch_mask(p)
+    rows = mask.any(-1)
+    live = rows.expand(-1, p.Hq, -1)
+    do = do * live[..., None].numpy()  # dO on empty rows is irrelevant to the oracle
+    o, lse = oracle_mod.forward(p, q, k, v, bias=bias)
+    dq, dk, dv = oracle_mod.backward(p, q, k, v, o, do, lse, bias=bias)
+    db = oracle_mod.dbias(p, q, k, v, o, do, lse, bias)
+    tq = torch.tensor(q, requires_grad=True)
+    tk = torch.tensor(k, requires_grad=True)
+    tv = torch.tensor(v, requires_grad=True)
+    tb = torch.tensor(bias, requires_grad=True)
+    add = tb.masked_fill(~mask, float("-inf")) if batch1 is False else \
+        tb.expand(p.B, -1, -1, -1).masked_fill(~mask, float("-inf"))
+    out = torch.nn.functional.scaled_dot_product_attention(
+        tq, tk.repeat_interleave(G, 1), tv.repeat_interleave(G, 1), attn_mask=add,
+        scale=p.resolved_scale)
+    out = torch.where(live[..., None], out, torch.zeros_like(out))
+    (out * torch.tensor(do)).sum().backward()
+    np.testing.assert_allclose(o, out.detach().numpy(), atol=1e-12)
+    np.testing.assert_allclose(dq, tq.grad.numpy(), atol=1e-11)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), atol=1e-11)
+    np.testing.assert_allclose(dv, tv.grad.numpy(), atol=1e-11)
+    tgrad = torch.nan_to_num(tb.grad, nan=0.0).numpy()
+    np.testing.assert_allclose(db, tgrad, atol=1e-11)
+
+
+def test_minus_infinity_bias_equals_the_causal_mask(oracle_mod):
+    """A bias of -inf above the diagonal reproduces causal=True: the bias is
+    indexed (query, key), not transposed."""
+    pc = Problem(2, 2, 1, 6, 9, 4, 3, causal=True, bottom_right=True)
+    pn = Problem(2, 2, 1, 6, 9, 4, 3)
+    q, k, v, do = _inputs(pc, seed=27)
+    diag = 9 - 6
+    qi, ki = np.meshgrid(np.arange(6), np.arange(9), indexing="ij")
+    bias = np.where(ki > qi + diag, -np.inf, 0.0)[None, None].repeat(2, 0).repeat(2, 1)
+    o0, lse0 = oracle_mod.forward(pc, q, k, v)
+    o1, lse1 = oracle_mod.forward(pn, q, k, v, bias=bias)
+    np.testing.assert_allclose(o1, o0, atol=1e-14)
+    np.testing.assert_allclose(lse1, lse0, atol=1e-14)
+    g0 = oracle_mod.backward(pc, q, k, v, o0, do, lse0)
+    g1 = oracle_mod.backward(pn, q, k, v, o1, do, lse1, bias=bias)
+    for a, b in zip(g1, g0):
+        np.testing.assert_allclose(a, b, atol=1e-13)
+    db = oracle_mod.dbias(pn, q, k, v, o1, do, lse1, bias)
+    assert np.all(db[..., ki > qi + diag] == 0.0)
+
+
+def test_row_constant_bias_only_shifts_lse(oracle_mod):
+    """bias[q, k] = c_q: softmax is shift invariant, so O and dQ/dK/dV are
+    unchanged, LSE moves by c_q, and every dBias row sums to zero."""
+    p = FD_CASES["window_causal"]
+    q, k, v, do = _inputs(p, seed=28)
+    c = np.random.default_rng(29).standard_normal((p.B, p.Hq, p.Sq))
+    bias = np.repeat(c[..., None], p.Skv, -1)
+    o0, lse0 = oracle_mod.forward(p, q, k, v)
+    o1, lse1 = oracle_mod.forward(p, q, k, v, bias=bias)
+    np.testing.assert_allclose(o1, o0, atol=1e-14)
+    np.testing.assert_allclose(lse1, lse0 + c, atol=1e-13)
+    for a, b in zip(oracle_mod.backward(p, q, k, v, o1, do, lse1, bias=bias),
+                    oracle_mod.backward(p, q, k, v, o0, do, lse0)):
+        np.testing.assert_allclose(a, b, atol=1e-13)
+    db = oracle_mod.dbias(p, q, k, v, o1, do, lse1, bias)
+    np.testing.assert_allclose(db.sum(-1), 0.0, atol=1e-13)
+
+
+def test_rank_one_bias_equals_one_more_head_dim(oracle_mod):
+    """bias[q, k] = u_q w_k is one more head dimension with Q' = [Q, u / scale]
+    and K' = [K, w]: O and LSE agree, dQ and dK agree on the first D_qk columns,
+    and sum_k dBias[q, k] w_k = dQ'[q, D_qk] / scale."""
+    p = Problem(1, 2, 2, 5, 7, 3, 4, causal=True, bottom_right=True)
+    pa = Problem(1, 2, 2, 5, 7, 4, 4, causal=True, bottom_right=True, scale=p.resolved_scale)
+    q, k, v, do = _inputs(p, seed=30)
+    rng = np.random.default_rng(31)
+    u = rng.standard_normal((1, 2, 5))
+    w = rng.standard_normal((1, 2, 7))
+    bias = u[..., :, None] * w[..., None, :]
+    qa = np.concatenate([q, (u / p.resolved_scale)[..., None]], -1)
+    ka = np.concatenate([k, w[..., None]], -1)
+    o, lse = oracle_mod.forward(p, q, k, v, bias=bias)
+    oa, lsea = oracle_mod.forward(pa, qa, ka, v)
+    np.testing.assert_allclose(o, oa, atol=1e-14)
+    np.testing.assert_allclose(lse, lsea, atol=1e-14)
+    dq, dk, dv = oracle_mod.backward(p, q, k, v, o, do, lse, bias=bias)
+    dqa, dka, dva = oracle_mod.backward(pa, qa, ka, v, oa, do, lsea)
+    np.testing.assert_allclose(dq, dqa[..., :3], atol=1e-13)
+    np.testing.assert_allclose(dk, dka[..., :3], atol=1e-13)
+    np.testing.assert_allclose(dv, dva, atol=1e-13)
+    db = oracle_mod.dbias(p, q, k, v, o, do, lse, bias)
+    np.testing.assert_allclose((db * w[..., None, :]).sum(-1), dqa[..., 3] / p.resolved_scale,
+                               atol=1e-13)
