@@ -59,6 +59,8 @@ def load(build_if_missing: bool = False):
     lib.sdpa_bwd.restype = i
     lib.sdpa_bwd_sink.argtypes = list(lib.sdpa_bwd.argtypes[:-1]) + [vp, vp, vp]
     lib.sdpa_bwd_sink.restype = i
+    lib.sdpa_bwd_bias.argtypes = list(lib.sdpa_bwd.argtypes[:-1]) + [vp, vp, vp, i, i, vp, vp]
+    lib.sdpa_bwd_bias.restype = i
     lib.sdpa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, ctypes.c_float, i, i, i, i,
                              vp, vp, vp, vp]
     lib.sdpa_fwd.restype = i
@@ -113,7 +115,8 @@ def sdpa_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
              seq_kv_lens: Optional[torch.Tensor] = None, dq: Optional[torch.Tensor] = None,
              dk: Optional[torch.Tensor] = None, dv: Optional[torch.Tensor] = None,
              workspace: Optional[torch.Tensor] = None, sink: Optional[torch.Tensor] = None,
-             dsink: Optional[torch.Tensor] = None,
+             dsink: Optional[torch.Tensor] = None, bias: Optional[torch.Tensor] = None,
+             dbias: Optional[torch.Tensor] = None, bias_grad: bool = True,
              stream: Optional[torch.cuda.Stream] = None):
     """dQ, dK, dV of scaled-dot-product attention (see include/sdpa_bwd.h).
 
@@ -122,6 +125,10 @@ def sdpa_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
     Outputs are allocated when not given. Runs on ``stream`` (default: current stream).
     With ``sink`` (fp32 (Hq,) CUDA sink logits, already folded into ``lse`` by the
     forward) the call goes through sdpa_bwd_sink and returns (dq, dk, dv, dsink).
+    With ``bias`` ((1|B, Hq, Sq, Skv) bf16 or fp32 CUDA, contiguous: the additive
+    bias that ``lse`` was computed with) the call goes through sdpa_bwd_bias and,
+    unless ``bias_grad`` is False, appends the fp32 dBias (shaped like ``bias``) to
+    the returned tuple.
     """
     lib = load()
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
@@ -157,22 +164,52 @@ def sdpa_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
             _ptr(dv), B, Hq, Hkv, Sq, Skv, Dqk, Dv, sc, int(causal), int(bottom_right),
             int(window_left), int(window_right), int(deterministic), _ptr(seq_q_lens),
             _ptr(seq_kv_lens), _ptr(workspace), ws_bytes)
-    if sink is None:
+    if sink is None and bias is None:
         rc = lib.sdpa_bwd(*args, _stream_handle(stream))
         if rc != 0:
             raise SdpaError(rc, "sdpa_bwd")
         return dq, dk, dv
-    if sink.dtype != torch.float32 or not sink.is_cuda or not sink.is_contiguous() \
-            or sink.numel() != Hq:
-        raise ValueError("sink must be a contiguous fp32 CUDA tensor of Hq elements")
-    dsink = torch.empty_like(sink) if dsink is None else dsink
-    if dsink.dtype != torch.float32 or not dsink.is_cuda or not dsink.is_contiguous() \
-            or dsink.numel() != Hq:
-        raise ValueError("dsink must be a contiguous fp32 CUDA tensor of Hq elements")
-    rc = lib.sdpa_bwd_sink(*args, _ptr(sink), _ptr(dsink), _stream_handle(stream))
+    if sink is not None:
+        if sink.dtype != torch.float32 or not sink.is_cuda or not sink.is_contiguous() \
+                or sink.numel() != Hq:
+            raise ValueError("sink must be a contiguous fp32 CUDA tensor of Hq elements")
+        dsink = torch.empty_like(sink) if dsink is None else dsink
+        if dsink.dtype != torch.float32 or not dsink.is_cuda or not dsink.is_contiguous() \
+                or dsink.numel() != Hq:
+            raise ValueError("dsink must be a contiguous fp32 CUDA tensor of Hq elements")
+    if bias is None:
+        rc = lib.sdpa_bwd_sink(*args, _ptr(sink), _ptr(dsink), _stream_handle(stream))
+        if rc != 0:
+            raise SdpaError(rc, "sdpa_bwd_sink")
+        return dq, dk, dv, dsink
+    bias_dtype = _check_bias(bias, B, Hq, Sq, Skv)
+    if bias_grad:
+        dbias = torch.empty(bias.shape, dtype=torch.float32, device=bias.device) if dbias is None else dbias
+        if dbias.dtype != torch.float32 or not dbias.is_cuda or not dbias.is_contiguous() \
+                or tuple(dbias.shape) != tuple(bias.shape):
+            raise ValueError("dbias must be a contiguous fp32 CUDA tensor shaped like bias")
+    else:
+        dbias = None
+    rc = lib.sdpa_bwd_bias(*args, _ptr(sink), _ptr(dsink if sink is not None else None), _ptr(bias),
+                           bias_dtype, int(bias.shape[0]), _ptr(dbias), _stream_handle(stream))
     if rc != 0:
-        raise SdpaError(rc, "sdpa_bwd_sink")
-    return dq, dk, dv, dsink
+        raise SdpaError(rc, "sdpa_bwd_bias")
+    out = (dq, dk, dv) + ((dsink,) if sink is not None else ())
+    return out + ((dbias,) if bias_grad else ())
+
+
+# Element-type codes of the C ABI (sdpa_dtype).
+DTYPE_BF16, DTYPE_F32 = 0, 1
+
+
+def _check_bias(bias, B, Hq, Sq, Skv) -> int:
+    if not isinstance(bias, torch.Tensor) or not bias.is_cuda or not bias.is_contiguous():
+        raise ValueError("bias must be a contiguous CUDA tensor")
+    if bias.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("bias must be bf16 or fp32")
+    if bias.dim() != 4 or bias.shape[0] not in (1, B) or tuple(bias.shape[1:]) != (Hq, Sq, Skv):
+        raise ValueError(f"bias must be (1|B, Hq, Sq, Skv), got {tuple(bias.shape)}")
+    return DTYPE_F32 if bias.dtype == torch.float32 else DTYPE_BF16
 
 
 def sdpa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: Optional[float] = None,

@@ -63,6 +63,18 @@ struct ChainParams {
   float* dsink;         // (Hq,) output, or null
   float* dsink_part;    // [B*Hq][n_qt] per-tile partial sums (fixed order within a tile)
 
+  // Additive bias (optional), added to the scaled scores before the softmax:
+  // element (b, h, q, k) at bias[b * bias_bstride + (h * Sq + q) * Skv + k],
+  // bf16 or fp32; bias_bstride = 0 when one bias batch serves every batch row.
+  // dbias (fp32, same indexing with dbias_bstride) receives dS = P * (dP - delta);
+  // with dbias_red the batch rows' terms are added atomically into one batch.
+  const void* bias;     // or null
+  int bias_fp32;
+  long long bias_bstride;
+  float* dbias;         // or null
+  long long dbias_bstride;
+  int dbias_red;
+
   // Deterministic two-kernel route: the main kernel stores each bf16 dS^T tile
   // (its swizzled shared-memory image, DS_TILE_BYTES) at
   // ds_ws + ((bh * n_kt + kt) * n_qt + qt) * DS_TILE_BYTES, and the dQ kernel
@@ -138,6 +150,8 @@ cudaError_t dq_kernel_setup();  // per device: opt in to the dQ kernel's shared 
 cudaError_t launch_main_ds(const MainMaps& maps, const ChainParams& p, cudaStream_t s);
 cudaError_t main_ds_kernel_setup();
 cudaError_t main_kernel_setup();  // per device: opt in to the main kernel's shared memory
+cudaError_t launch_main_bias(const MainMaps& maps, const ChainParams& p, cudaStream_t s);
+cudaError_t main_bias_kernel_setup();
 
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,

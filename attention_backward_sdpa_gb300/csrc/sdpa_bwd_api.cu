@@ -244,18 +244,37 @@ int sdpa_bwd_check_device_status(void* stream) {
 
 namespace {
 
+// Optional additive bias of sdpa_bwd_bias(); all null/zero for the other calls.
+struct BiasArgs {
+  const void* bias = nullptr;
+  int dtype = SDPA_DTYPE_BF16;
+  int batch = 0;  // 1 or B
+  float* dbias = nullptr;
+};
+
 // The whole chain; sink/dsink are null for sdpa_bwd().
 int run_chain(const void* q, const void* k, const void* v, const void* o, const void* d_o,
               const float* lse, void* dq, void* dk, void* dv, int B, int H_q, int H_kv, int S_q,
               int S_kv, int D_qk, int D_v, float scale, int causal, int bottom_right,
               int window_left, int window_right, int deterministic, const int32_t* seq_q_lens,
               const int32_t* seq_kv_lens, void* workspace, size_t workspace_bytes,
-              const float* sink, float* dsink, void* stream_) {
+              const float* sink, float* dsink, const BiasArgs& ba, void* stream_) {
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   int rc = basic_checks(B, H_q, H_kv, S_q, S_kv, D_qk, D_v);
   if (rc != SDPA_OK) return rc;
   if (!q || !k || !v || !o || !d_o || !lse || !dq || !dk || !dv) return SDPA_ERR_INVALID;
   if (dsink && !sink) return SDPA_ERR_INVALID;
+  if (ba.bias) {
+    if (ba.dtype != SDPA_DTYPE_BF16 && ba.dtype != SDPA_DTYPE_F32) return SDPA_ERR_INVALID;
+    if (ba.batch != 1 && ba.batch != B) return SDPA_ERR_INVALID;
+    // A one-batch dBias summed over B > 1 batch rows is added atomically: not
+    // reproducible, so deterministic mode rejects it.
+    if (deterministic && ba.dbias && ba.batch == 1 && B > 1) return SDPA_ERR_INVALID;
+    if (reinterpret_cast<uintptr_t>(ba.bias) % (ba.dtype == SDPA_DTYPE_F32 ? 4 : 2) != 0 ||
+        reinterpret_cast<uintptr_t>(ba.dbias) % 4 != 0)
+      return SDPA_ERR_ALIGN;
+    if (D_qk == 192) return SDPA_ERR_UNSUPPORTED;
+  }
   for (const void* ptr : {q, k, v, o, d_o, (const void*)dq, (const void*)dk, (const void*)dv})
     if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return SDPA_ERR_ALIGN;
   for (const void* ptr : {(const void*)lse, (const void*)sink, (const void*)dsink})
@@ -278,7 +297,9 @@ int run_chain(const void* q, const void* k, const void* v, const void* o, const 
     if (cudaMemsetAsync(dq, 0, dq_bytes, stream) != cudaSuccess ||
         cudaMemsetAsync(dk, 0, dk_bytes, stream) != cudaSuccess ||
         cudaMemsetAsync(dv, 0, dv_bytes, stream) != cudaSuccess ||
-        (dsink && cudaMemsetAsync(dsink, 0, (size_t)H_q * sizeof(float), stream) != cudaSuccess))
+        (dsink && cudaMemsetAsync(dsink, 0, (size_t)H_q * sizeof(float), stream) != cudaSuccess) ||
+        (ba.dbias && cudaMemsetAsync(ba.dbias, 0, (size_t)ba.batch * H_q * S_q * S_kv * sizeof(float),
+                                     stream) != cudaSuccess))
       return SDPA_ERR_CUDA;
     return SDPA_OK;
   }
@@ -348,6 +369,16 @@ int run_chain(const void* q, const void* k, const void* v, const void* o, const 
   p.sink = dsink ? sink : nullptr;
   p.dsink = dsink;
   p.dsink_part = dsink ? reinterpret_cast<float*>(ws + cv.dsink_part) : nullptr;
+  if (ba.bias) {
+    const long long per_batch = (long long)H_q * S_q * S_kv;
+    const bool shared = ba.batch == 1 && B > 1;
+    p.bias = ba.bias;
+    p.bias_fp32 = ba.dtype == SDPA_DTYPE_F32 ? 1 : 0;
+    p.bias_bstride = shared ? 0 : per_batch;
+    p.dbias = ba.dbias;
+    p.dbias_bstride = shared ? 0 : per_batch;
+    p.dbias_red = (ba.dbias && shared) ? 1 : 0;
+  }
 
   MainMaps maps;
   const long long BHq = (long long)B * H_q, BHkv = (long long)B * H_kv;
@@ -394,7 +425,7 @@ int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const v
              const int32_t* seq_kv_lens, void* workspace, size_t workspace_bytes, void* stream) {
   return run_chain(q, k, v, o, d_o, lse, dq, dk, dv, B, H_q, H_kv, S_q, S_kv, D_qk, D_v, scale,
                    causal, bottom_right, window_left, window_right, deterministic, seq_q_lens,
-                   seq_kv_lens, workspace, workspace_bytes, nullptr, nullptr, stream);
+                   seq_kv_lens, workspace, workspace_bytes, nullptr, nullptr, BiasArgs{}, stream);
 }
 
 int sdpa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
@@ -457,7 +488,26 @@ int sdpa_bwd_sink(const void* q, const void* k, const void* v, const void* o, co
   if (!sink || !dsink) return SDPA_ERR_INVALID;
   return run_chain(q, k, v, o, d_o, lse, dq, dk, dv, B, H_q, H_kv, S_q, S_kv, D_qk, D_v, scale,
                    causal, bottom_right, window_left, window_right, deterministic, seq_q_lens,
-                   seq_kv_lens, workspace, workspace_bytes, sink, dsink, stream);
+                   seq_kv_lens, workspace, workspace_bytes, sink, dsink, BiasArgs{}, stream);
+}
+
+int sdpa_bwd_bias(const void* q, const void* k, const void* v, const void* o, const void* d_o,
+                  const float* lse, void* dq, void* dk, void* dv, int B, int H_q, int H_kv,
+                  int S_q, int S_kv, int D_qk, int D_v, float scale, int causal, int bottom_right,
+                  int window_left, int window_right, int deterministic,
+                  const int32_t* seq_q_lens, const int32_t* seq_kv_lens, void* workspace,
+                  size_t workspace_bytes, const float* sink, float* dsink, const void* bias,
+                  int bias_dtype, int bias_batch, float* dbias, void* stream) {
+  if (!bias || (dsink && !sink)) return SDPA_ERR_INVALID;
+  BiasArgs ba;
+  ba.bias = bias;
+  ba.dtype = bias_dtype;
+  ba.batch = bias_batch;
+  ba.dbias = dbias;
+  return run_chain(q, k, v, o, d_o, lse, dq, dk, dv, B, H_q, H_kv, S_q, S_kv, D_qk, D_v, scale,
+                   causal, bottom_right, window_left, window_right, deterministic, seq_q_lens,
+                   seq_kv_lens, workspace, workspace_bytes, dsink ? sink : nullptr, dsink, ba,
+                   stream);
 }
 
 }  // extern "C"

@@ -1,677 +1,18 @@
-// sdpa_bwd_main.cu -- fused five-GEMM SDPA backward main kernel for sm_103a.
-//
-// What it computes (cuDNN frontend docs, "SDPA Backward (SM120)", section
-// "Main-kernel pipeline: KV-stationary, five chained GEMMs"): one CTA owns one
-// tile of BN = 128 keys of one query head (its KV head is h / G), keeps K and V
-// of that tile in shared memory, and walks the visible query tiles of BQ = 64
-// rows in descending order. Per query tile t:
-//   G1  S^T  = K Q^T                       (tensor memory, fp32)
-//       P^T  = exp2(S^T * scale*log2e - LSE*log2e), masked -> 0
-//   G2  dP^T = V dO^T                      (tensor memory, fp32)
-//       dS^T = P^T * (dP^T - delta)        -> bf16 in shared memory
-//   G3  dV  += P^T dO                      (A = P^T read from tensor memory)
-//   G4  dK  += dS^T Q
-//   G5  dQ^T = K^T dS^T  -> one TMA bulk reduce-add into the fp32 dQ accumulator
-// Masks follow "Causal, sliding-window, and padding masks": loop bounds skip
-// fully masked tiles and only edge tiles mask in registers.
-//
-// Schedule. Two query tiles are in flight: tensor memory holds two slots, each
-// with S^T and dP^T (dQ^T reuses the dP^T columns once dS is formed). Compute
-// warpgroup 0 owns the even tiles (slot 0), warpgroup 1 the odd ones (slot 1).
-// One MMA warp issues G1/G2 of tile t while the other issues G3/G4/G5 of tile
-// t-1, so the tensor core works on one tile while a warpgroup replays the
-// softmax of the other. A third warpgroup moves each dQ^T tile from tensor
-// memory to shared memory and hands it to the TMA engine as one bulk reduction
-// (in deterministic mode after waiting its turn on the query tile's counter).
-//
-// Warps: 0-3 slot-0 compute, 4-7 slot-1 compute, 8-11 dQ, 12 TMA producer,
-// 13 score-GEMM issuer and tensor-memory owner, 14 gradient-GEMM issuer, 15 the
-// dS^T store on the two-kernel route, otherwise idle (it completes the fourth
-// warpgroup so that register budgets can be moved
-// between warpgroups: launched with 128 registers per thread, the compute
-// warpgroups grow to 160 while the dQ and control warpgroups shrink to 96;
-// 128 threads x (160 + 160 + 96 + 96) = 65536 = 512 threads x 128).
-//
-// Shared memory (128-byte swizzle, every tile 1024-byte aligned):
-//   K, V        [D/64 blocks][128 key rows][128 B]
-//   Q, dO x3/4  [D/64 blocks][64 query rows][128 B]   (stage ring: 4 stages on the
-//                                                      two-kernel route, which
-//                                                      needs no dQ staging)
-//   dS^T x2     [128 key rows][64 queries x 2 B]      (one per slot)
-//   dQ staging  [64 queries][D] fp32                  (bulk reduction source)
-//   qstat x3/4  LSE*log2e[64], delta[64]
-// Tensor memory (512 columns x 128 lanes, fp32):
-//   slot s: S^T at 128s + [0,64) (P^T written back as bf16 into [0,32) by the
-//           same threads that read S^T), dP^T then dQ^T at 128s + [64,128)
-//   dV at [256, 256+D), dK at [256+D, 256+2D)
-#include <cuda.h>
-#include <cuda_bf16.h>
-
-#include "common.cuh"
-#include "ptx.cuh"
+// sdpa_bwd_main.cu -- the main kernels without a bias (sdpa_bwd_main.cuh) and
+// the launcher that picks between them and the biased ones.
+#include "sdpa_bwd_main.cuh"
 
 namespace sdpa {
 
-constexpr int MAIN_THREADS = 512;
-constexpr uint32_t REGS_COMPUTE = 160, REGS_DQ = 96, REGS_CTRL = 96;
-static_assert(128 * (2 * REGS_COMPUTE + REGS_DQ + REGS_CTRL) <= MAIN_THREADS * 128,
-              "register split exceeds the launch budget");
-constexpr uint64_t WAIT_LIMIT_NS = 4000000000ull;  // 4 s: far above any legal wait
-
-enum : int {
-  BAR_KV = 0,
-  BAR_QFULL = 1,        // + stage (up to 4)
-  BAR_QEMPTY = 5,       // + stage (up to 4)
-  BAR_SFULL = 9,        // + slot (2)
-  BAR_DPFULL = 11,      // + slot
-  BAR_PREADY = 13,      // + slot, 128 arrivals
-  BAR_SFREE = 15,       // + slot
-  BAR_DSREADY = 17,     // + slot, 128 arrivals
-  BAR_DQFULL = 19,      // + slot
-  BAR_DQEMPTY = 21,     // + slot, 128 arrivals
-  BAR_MMADONE = 23,     // every MMA of the CTA has completed (epilogue may read dK/dV)
-  BAR_DSCOPIED = 24,    // + slot: the slot's dS^T tile has been read out to global (dS route)
-  BAR_DPREAD = 26,      // + slot, 128 arrivals: dP^T has been loaded into registers
-  BAR_STAGEREADY = 28,  // + staging half (2), 128 arrivals: the half is written
-  BAR_STAGEFREE = 30,   // + staging half (2): its bulk reduction has read it
-  NUM_BARS = 32
-};
-
-// NST Q/dO stages; the dQ staging buffer exists only on the dQ-reduction route
-// (on the two-kernel route its space holds a fourth stage).
-template <int D, bool DS_OUT>
-struct MainLayout {
-  static constexpr int NST = DS_OUT ? 4 : 3;
-  static constexpr int BLK_KV = BN * 128;          // one 64-column block of a 128-row tile
-  static constexpr int BLK_Q = BQ * 128;           // one 64-column block of a 64-row tile
-  static constexpr int TILE_KV = BN * D * 2;
-  static constexpr int TILE_Q = BQ * D * 2;
-  static constexpr int TILE_DS = BN * BQ * 2;
-  static constexpr int TILE_DQ = DS_OUT ? 0 : BQ * D * 4;
-  static constexpr int OFF_K = 0;
-  static constexpr int OFF_V = OFF_K + TILE_KV;
-  static constexpr int OFF_Q = OFF_V + TILE_KV;
-  static constexpr int OFF_DO = OFF_Q + NST * TILE_Q;
-  static constexpr int OFF_DS = OFF_DO + NST * TILE_Q;
-  static constexpr int OFF_DQ = OFF_DS + 2 * TILE_DS;
-  static constexpr int OFF_QS = OFF_DQ + TILE_DQ;
-  static constexpr int OFF_BAR = OFF_QS + NST * QSTAT_FLOATS * 4;
-  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int BYTES = OFF_MISC + 64;
-  static constexpr uint32_t COL_DV = 256, COL_DK = 256 + D;
-  __host__ __device__ static constexpr uint32_t col_s(int slot) { return 128u * slot; }
-  __host__ __device__ static constexpr uint32_t col_dp(int slot) { return 128u * slot + 64u; }
-  static_assert(COL_DK + D <= 512, "tensor memory budget");
-  static_assert(BYTES <= 232448, "shared memory budget");
-  // More than half an SM's shared memory: one CTA per SM, so a CTA never waits
-  // for tensor memory held by a co-resident CTA that may be waiting on it.
-  static_assert(BYTES > 116 * 1024, "one CTA per SM");
-};
-
-__device__ __forceinline__ void set_status(int* status, int bit) { atomicOr(status, bit); }
-
-// DS_OUT selects the deterministic two-kernel route: instead of G5 and the dQ
-// reduction, every dS^T tile is stored to the workspace for the dQ kernel.
-template <int D, bool DS_OUT>
-__global__ void __launch_bounds__(MAIN_THREADS, 1)
-    sdpa_bwd_main(const __grid_constant__ MainMaps maps, const ChainParams p) {
-  using L = MainLayout<D, DS_OUT>;
-  constexpr int NSTAGE = L::NST;
-  extern __shared__ __align__(1024) uint8_t smem[];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-  if ((smem_u32(smem) & 1023u) != 0) {  // the swizzled layouts need 1 KB alignment
-    if (tid == 0) set_status(p.status, STATUS_SMEM_ALIGN);
-    return;
-  }
-  if (!p.deterministic) {
-    // A key tile that no query sees only has zero gradients. Its rows are
-    // written by an idle warp of the group's other CTAs (or here, when the
-    // batch row has no query or no key); leave before any setup.
-    const int NG0 = p.B * p.Hkv * p.n_part;
-    const int kt0 = blockIdx.x / NG0, gi0 = blockIdx.x % NG0, b0 = gi0 / (p.Hkv * p.n_part);
-    int Lq0, Lk0, lo0, hi0;
-    batch_lengths(p, b0, Lq0, Lk0);
-    visited_query_tiles(kt0, Lq0, Lk0, p.causal, p.bottom_right, p.window_left, p.window_right, lo0,
-                        hi0);
-    if (hi0 < lo0) {
-      if (!row_has_visible_pair(Lq0, Lk0))
-        zero_key_tile_rows<D, D>(p, p.dk_ws ? (long long)gi0 : (long long)(gi0 / p.n_part), kt0 * BN);
-      return;
-    }
-  }
-  uint8_t* sK = smem + L::OFF_K;
-  uint8_t* sV = smem + L::OFF_V;
-  uint8_t* sQ = smem + L::OFF_Q;
-  uint8_t* sDO = smem + L::OFF_DO;
-  uint8_t* sDS = smem + L::OFF_DS;
-  float* sDQ = reinterpret_cast<float*>(smem + L::OFF_DQ);
-  float* sQS = reinterpret_cast<float*>(smem + L::OFF_QS);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
-  int* unit_slot = reinterpret_cast<int*>(smem + L::OFF_MISC + 8);
-
-  if (tid == 0) {
-    *abort_flag = 0;
-    for (int i = 0; i < NUM_BARS; ++i) {
-      const bool threads128 = (i == BAR_PREADY || i == BAR_PREADY + 1 || i == BAR_DSREADY ||
-                               i == BAR_DSREADY + 1 || i == BAR_DQEMPTY || i == BAR_DQEMPTY + 1 ||
-                               i == BAR_STAGEREADY || i == BAR_STAGEREADY + 1 || i == BAR_DPREAD ||
-                               i == BAR_DPREAD + 1);
-      mbar_init(&bars[i], threads128 ? 128 : 1);
-    }
-    fence_mbar_init();
-  }
-  if (warp == 12 && lane == 0) {
-    prefetch_tmap(&maps.q);
-    prefetch_tmap(&maps.k);
-    prefetch_tmap(&maps.v);
-    prefetch_tmap(&maps.d_o);
-  }
-  if (warp == 13) {
-    tmem_alloc(tmem_slot, 512);
-    tmem_relinquish();
-  }
-
-  // Work unit. Deterministic mode claims units from a ticket so that a unit is
-  // only ever claimed after every unit it waits on (the same query tile, a
-  // lower key tile) has been claimed by a running CTA.
-  if (p.deterministic) {
-    pdl_wait_prior_grid();  // the ticket is cleared by the preprocess kernel
-    if (tid == 0) *unit_slot = atomicAdd(p.ticket, 1);
-  } else if (tid == 0) {
-    *unit_slot = blockIdx.x;
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const int unit = *unit_slot;
-
-  // A unit is one key tile of one head group: gsz query heads of one KV head
-  // (group gi = (b * Hkv + hk) * n_part + g covers query heads
-  // hk * G + g * gsz ...). Units are ordered key tile major: every group's key
-  // tile 0 first. Under a causal mask low key tiles see the most query tiles,
-  // so the longest units start first.
-  const int NG = p.B * p.Hkv * p.n_part;
-  const int kt = unit / NG;
-  const int gi = unit % NG;
-  const int kvh_g = gi / p.n_part;                 // b * Hkv + hk
-  const int b = kvh_g / p.Hkv, hk = kvh_g % p.Hkv;
-  const int bh0 = b * p.Hq + hk * p.G + (gi % p.n_part) * p.gsz;  // the group's first query head
-  const int k0 = kt * BN;
-  // dK/dV destination: the KV head, or the group's partial set.
-  const long long out_head = p.dk_ws ? (long long)gi : (long long)kvh_g;
-
-  int Lq, Lk;
-  batch_lengths(p, b, Lq, Lk);
-  const int diag = p.bottom_right ? Lk - Lq : 0;
-  const int Rp = p.window_right > 0 ? p.window_right : 0;
-  const bool has_window = p.window_left >= 0;
-  int qt_lo, qt_hi;
-  visited_query_tiles(kt, Lq, Lk, p.causal, p.bottom_right, p.window_left, p.window_right, qt_lo,
-                      qt_hi);
-  // Tiles t = 0 .. n-1 walk the visible query tiles (descending) of the group's
-  // heads in turn: head bh0 + t / n1, query tile qt_hi - t % n1.
-  const int n1 = qt_hi >= qt_lo ? qt_hi - qt_lo + 1 : 0;  // query tiles per head
-  const int n = p.gsz * n1;
-
-  if (warp >= 12) {
-    regs_decrease<REGS_CTRL>();
-    if (warp == 12) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0 && n > 0) {
-      mbar_arrive_expect_tx(&bars[BAR_KV], 2 * L::TILE_KV);
-      for (int blk = 0; blk < D / 64; ++blk) {
-        tma_load_3d(sK + blk * L::BLK_KV, &maps.k, &bars[BAR_KV], blk * 64, k0, b * p.Hkv + hk);
-        tma_load_3d(sV + blk * L::BLK_KV, &maps.v, &bars[BAR_KV], blk * 64, k0, b * p.Hkv + hk);
-      }
-      pdl_wait_prior_grid();  // row statistics come from the preprocess kernel
-      for (int t = 0; t < n; ++t) {
-        const int st = t % NSTAGE;
-        if (t >= NSTAGE && !mbar_wait(&bars[BAR_QEMPTY + st], ((t / NSTAGE) - 1) & 1, abort_flag,
-                                      WAIT_LIMIT_NS))
-          break;
-        const int hj = t / n1;
-        const int qt = qt_hi - (t - hj * n1), bh = bh0 + hj;
-        uint64_t* full = &bars[BAR_QFULL + st];
-        mbar_arrive_expect_tx(full, 2 * L::TILE_Q + QSTAT_FLOATS * 4);
-        for (int blk = 0; blk < D / 64; ++blk) {
-          tma_load_3d(sQ + st * L::TILE_Q + blk * L::BLK_Q, &maps.q, full, blk * 64, qt * BQ, bh);
-          tma_load_3d(sDO + st * L::TILE_Q + blk * L::BLK_Q, &maps.d_o, full, blk * 64, qt * BQ, bh);
-        }
-        bulk_load(sQS + st * QSTAT_FLOATS,
-                  p.qstat + ((long long)bh * p.n_qt + qt) * QSTAT_FLOATS, QSTAT_FLOATS * 4, full);
-      }
-    }
-    } else if (warp == 13 || warp == 14) {
-      // ---------------------------------------------------------- MMA issuers
-      // A tcgen05.mma costs its issuing thread on the order of 100 cycles, more
-      // than a 64-column MMA takes on the tensor core, so two warps issue: warp
-      // 13 the score GEMMs G1/G2 of every tile, warp 14 the gradient GEMMs
-      // G3/G4/G5. Each warp stays converged and issues from one elected lane;
-      // mbarriers carry every dependency between the two streams.
-      pdl_wait_prior_grid();
-      constexpr uint32_t ID_G12 = idesc_bf16_f32(128, BQ, false, false);  // S^T, dP^T
-      constexpr uint32_t ID_G34 = idesc_bf16_f32(128, D, false, true);    // dV, dK
-      constexpr uint32_t ID_G5 = idesc_bf16_f32(128, BQ, true, true);     // dQ^T (rows >= D unused)
-      constexpr uint64_t T_KMAJ = sdesc_sw128_template(16, 1024);          // K-major operands
-      constexpr uint64_t T_MN_Q = sdesc_sw128_template(L::BLK_Q, 1024);    // MN-major, 64-row tiles
-      constexpr uint64_t T_MN_KV = sdesc_sw128_template(L::BLK_KV, 1024);  // MN-major, 128-row tiles
-      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
-      bool ok = n > 0 && mbar_wait(&bars[BAR_KV], 0, abort_flag, WAIT_LIMIT_NS);
-      if (warp == 13) {
-        for (int t = 0; t < n && ok; ++t) {
-          const int s = t & 1, st = t % NSTAGE, j = t >> 1;
-          const uint32_t aQ = smem_u32(sQ + st * L::TILE_Q);
-          const uint32_t aDO = smem_u32(sDO + st * L::TILE_Q);
-          ok = mbar_wait(&bars[BAR_QFULL + st], (t / NSTAGE) & 1, abort_flag, WAIT_LIMIT_NS);
-          // The slot's S^T columns hold P^T of tile t-2 until its G3 completes.
-          if (ok && t >= 2) ok = mbar_wait(&bars[BAR_SFREE + s], (j - 1) & 1, abort_flag, WAIT_LIMIT_NS);
-          if (!ok) break;
-          __syncwarp();
-          tc_fence_after();
-          if (elect_one()) {
-            // G1: S^T[key, q] = sum_d K[key, d] Q[q, d]   (both K-major)
-#pragma unroll
-            for (int k = 0; k < D / 16; ++k) {
-              const uint32_t kk = (k >> 2) * L::BLK_KV + (k & 3) * 32;
-              const uint32_t kq = (k >> 2) * L::BLK_Q + (k & 3) * 32;
-              mma_ss(tmem + L::col_s(s), sdesc_at(T_KMAJ, aK + kk), sdesc_at(T_KMAJ, aQ + kq), ID_G12,
-                     k > 0);
-            }
-            mma_commit(&bars[BAR_SFULL + s]);
-          }
-          __syncwarp();
-          // The slot's dP^T columns are read by the compute warpgroup of tile t-2
-          // until it has them in registers (DP_READ), and on the dQ-reduction
-          // route then hold dQ^T of tile t-2 until the dQ warpgroup has read it.
-          if (t >= 2 && !mbar_wait(&bars[BAR_DPREAD + s], (j - 1) & 1, abort_flag, WAIT_LIMIT_NS))
-            break;
-          if (!DS_OUT && t >= 2 &&
-              !mbar_wait(&bars[BAR_DQEMPTY + s], (j - 1) & 1, abort_flag, WAIT_LIMIT_NS))
-            break;
-          __syncwarp();
-          tc_fence_after();
-          if (elect_one()) {
-            // G2: dP^T[key, q] = sum_d V[key, d] dO[q, d]
-#pragma unroll
-            for (int k = 0; k < D / 16; ++k) {
-              const uint32_t kk = (k >> 2) * L::BLK_KV + (k & 3) * 32;
-              const uint32_t kq = (k >> 2) * L::BLK_Q + (k & 3) * 32;
-              mma_ss(tmem + L::col_dp(s), sdesc_at(T_KMAJ, aV + kk), sdesc_at(T_KMAJ, aDO + kq), ID_G12,
-                     k > 0);
-            }
-            mma_commit(&bars[BAR_DPFULL + s]);
-          }
-          __syncwarp();
-        }
-      } else {
-        for (int u = 0; u < n && ok; ++u) {
-          const int su = u & 1, stu = u % NSTAGE, ju = u >> 1;
-          const uint32_t aQ = smem_u32(sQ + stu * L::TILE_Q);
-          const uint32_t aDO = smem_u32(sDO + stu * L::TILE_Q);
-          const uint32_t aDS = smem_u32(sDS + su * L::TILE_DS);
-          if (!mbar_wait(&bars[BAR_PREADY + su], ju & 1, abort_flag, WAIT_LIMIT_NS)) break;
-          __syncwarp();
-          tc_fence_after();
-          if (elect_one()) {
-            // G3: dV[key, d] += sum_q P^T[key, q] dO[q, d]; P^T pairs in columns [0,32) of the slot.
-#pragma unroll
-            for (int k = 0; k < BQ / 16; ++k)
-              mma_ts(tmem + L::COL_DV, tmem + L::col_s(su) + 8 * k, sdesc_at(T_MN_Q, aDO + k * 2048),
-                     ID_G34, (u > 0 || k > 0));
-            mma_commit(&bars[BAR_SFREE + su]);
-          }
-          __syncwarp();
-          if (!mbar_wait(&bars[BAR_DSREADY + su], ju & 1, abort_flag, WAIT_LIMIT_NS)) break;
-          __syncwarp();
-          tc_fence_after();
-          if (elect_one()) {
-            // G4: dK[key, d] += sum_q dS^T[key, q] Q[q, d]   (dS^T K-major, Q MN-major)
-#pragma unroll
-            for (int k = 0; k < BQ / 16; ++k)
-              mma_ss(tmem + L::COL_DK, sdesc_at(T_KMAJ, aDS + k * 32), sdesc_at(T_MN_Q, aQ + k * 2048),
-                     ID_G34, (u > 0 || k > 0));
-            // Stage u is refilled for tile u+3 once G4 is done (G1/G2 of tile u
-            // completed before P_READY / DS_READY could arrive).
-            if (u + NSTAGE < n) mma_commit(&bars[BAR_QEMPTY + stu]);
-            if (!DS_OUT) {
-              // G5: dQ^T[d, q] = sum_key K[key, d] dS^T[key, q]   (both MN-major)
-#pragma unroll
-              for (int k = 0; k < BN / 16; ++k)
-                mma_ss(tmem + L::col_dp(su), sdesc_at(T_MN_KV, aK + k * 2048),
-                       sdesc_at(T_MN_KV, aDS + k * 2048), ID_G5, k > 0);
-            }
-            // dQ^T ready (dQ route) / the slot's dS^T buffer no longer read by MMAs.
-            mma_commit(&bars[BAR_DQFULL + su]);
-          }
-          __syncwarp();
-        }
-        // After the last tile (also releases the epilogue on abort).
-        if (n > 0 && elect_one()) mma_commit(&bars[BAR_MMADONE]);
-        __syncwarp();
-      }
-    } else if (!DS_OUT && warp == 15) {
-      // Idle on this route: this CTA's share of the group's empty key tiles.
-      if (!p.deterministic) zero_group_share_of_empty_key_tiles<D, D>(p, out_head, kt, Lq, Lk, lane);
-    } else if (DS_OUT && warp == 15) {
-      // ------------------------------------------------------------ dS^T store
-      // Two-kernel route: once a tile's dS^T is in shared memory, one thread
-      // stores it to the workspace (the dQ kernel's input) and releases the
-      // buffer when the copy has read it, so no compute warp waits on the copy.
-      if (lane == 0) {
-        for (int t = 0; t < n; ++t) {
-          const int s = t & 1, j = t >> 1;
-          if (!mbar_wait(&bars[BAR_DSREADY + s], j & 1, abort_flag, WAIT_LIMIT_NS)) break;
-          const int hj = t / n1;
-          const int qt = qt_hi - (t - hj * n1), bh = bh0 + hj;
-          uint8_t* dst = p.ds_ws + (((long long)bh * p.n_kt + kt) * p.n_qt + qt) * (long long)DS_TILE_BYTES;
-          bulk_store(dst, sDS + s * L::TILE_DS, DS_TILE_BYTES);
-          bulk_commit_group();
-          bulk_wait_group_read0();
-          mbar_arrive(&bars[BAR_DSCOPIED + s]);
-        }
-        bulk_wait_group_read0();
-      }
-    }  // otherwise warp 15: idle member of the control warpgroup
-  } else if (warp >= 8) {
-    // ------------------------------------------------------------ dQ warpgroup
-    regs_decrease<REGS_DQ>();
-    // Idle on the two-kernel route: warp 9 writes this CTA's share of the
-    // group's empty key tiles.
-    if (DS_OUT && warp == 9 && !p.deterministic)
-      zero_group_share_of_empty_key_tiles<D, D>(p, out_head, kt, Lq, Lk, lane);
-    pdl_wait_prior_grid();
-    const int quarter = warp & 3;
-    const int d = quarter * 32 + lane;                 // dQ^T lane = head-dim column
-    const bool has_rows = quarter * 32 < D;            // warp-uniform
-    const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
-    const bool leader = (warp == 8 && lane == 0);
-    int* pending_counter = nullptr;  // deterministic mode: turn not yet released
-    int pending_turn = 0;
-    int* pending_next = nullptr;     // ... and the current tile's, once the next is issued
-    int pending_next_turn = 0;
-    bool ok = true;
-    for (int t = 0; t < (DS_OUT ? 0 : n) && ok; ++t) {
-      const int s = t & 1, j = t >> 1;
-      const int hj = t / n1;
-      const int qt = qt_hi - (t - hj * n1), bh = bh0 + hj;
-      if (!mbar_wait(&bars[BAR_DQFULL + s], j & 1, abort_flag, WAIT_LIMIT_NS)) { ok = false; break; }
-      __syncwarp();
-      tc_fence_after();
-      uint32_t va[32], vb[32];
-      if (has_rows) {
-        tmem_ld32(t_lane + L::col_dp(s), va);
-        tmem_ld32(t_lane + L::col_dp(s) + 32, vb);
-        tmem_ld_wait(va);
-        tmem_ld_wait(vb);
-      }
-      tc_fence_before();
-      mbar_arrive(&bars[BAR_DQEMPTY + s]);
-      // The staging buffer is used as two 16 KiB halves (query rows 0-31 and
-      // 32-63, contiguous in the accumulator), each with its own bulk reduction:
-      // the first half's copy runs while the second is written, and a half is
-      // refilled as soon as its own copy has read it.
-      float* dst = p.dq_accum + ((long long)bh * p.n_qt + qt) * (long long)BQ * D;
-      if (leader && p.deterministic) {
-        // Ordered relay: key tiles add into this query tile in ascending
-        // order. This tile's turn is released once both of its reductions have
-        // completed, which is checked after the next tile's reductions have
-        // been issued, so the completion latency overlaps the next tile instead
-        // of stalling this warpgroup. A key tile only ever waits on lower key
-        // tiles, so the delayed release only skews the chain.
-        const int kv_lo = has_window ? (int)max(0ll, floor_div((long long)qt * BQ + diag -
-                                                                   p.window_left, BN))
-                                     : 0;
-        const int turn = kt - kv_lo;
-        int* counter = p.counters + (long long)bh * p.n_qt + qt;
-        const uint64_t t0 = globaltimer_ns();
-        while (ld_acquire_gpu(counter) != turn) {
-          __nanosleep(32);
-          if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
-            set_status(p.status, STATUS_TIMEOUT);
-            break;
-          }
-        }
-        fence_proxy_async_global();
-        if (pending_counter != nullptr) pending_next = counter, pending_next_turn = turn;
-        else pending_counter = counter, pending_turn = turn;
-      }
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        float* stg = sDQ + hf * (L::TILE_DQ / 8);
-        if (t >= 1 &&
-            !mbar_wait(&bars[BAR_STAGEFREE + hf], (t - 1) & 1, abort_flag, WAIT_LIMIT_NS)) {
-          ok = false;
-          break;
-        }
-        if (has_rows) {
-          const uint32_t* v = hf ? vb : va;
-#pragma unroll
-          for (int q = 0; q < 32; ++q) stg[q * D + d] = __uint_as_float(v[q]);
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(&bars[BAR_STAGEREADY + hf]);
-        if (leader) {
-          mbar_wait(&bars[BAR_STAGEREADY + hf], t & 1, abort_flag, WAIT_LIMIT_NS);
-          bulk_reduce_add_f32(dst + hf * 32 * D, stg, L::TILE_DQ / 2);
-          bulk_commit_group();
-          // The previously issued half's reduction has read its buffer.
-          if (t >= 1 || hf == 1) {
-            bulk_wait_group_read1();
-            mbar_arrive(&bars[BAR_STAGEFREE + (hf ^ 1)]);
-          }
-          if (p.deterministic && hf == 1 && pending_next != nullptr) {
-            // Both halves of the previous tile complete -> release its turn.
-            bulk_wait_group2();
-            fence_proxy_async_global();
-            st_release_gpu(pending_counter, pending_turn + 1);
-            pending_counter = pending_next;
-            pending_turn = pending_next_turn;
-            pending_next = nullptr;
-          }
-        }
-      }
-      if (!ok) break;
-    }
-    if (leader) {
-      bulk_wait_group0();
-      if (pending_counter != nullptr) {
-        fence_proxy_async_global();
-        st_release_gpu(pending_counter, pending_turn + 1);
-      }
-    }
-  } else {
-    // ------------------------------------------------------------ compute warpgroups
-    regs_increase<REGS_COMPUTE>();
-    pdl_wait_prior_grid();
-    const int slot = warp >> 2;        // warpgroup: even (0) or odd (1) query tiles
-    const int quarter = warp & 3;      // tensor-memory lane quarter
-    const int row = quarter * 32 + lane;
-    const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
-    const int k = k0 + row;            // this thread's key (S^T / dP^T lane)
-    const bool row_dead = k >= Lk;
-    const long long q_lo_vis = p.causal ? (long long)k - diag - Rp : -(1ll << 40);
-    const long long q_hi_vis = has_window ? (long long)k - diag + p.window_left : (1ll << 40);
-    const float scale_log2 = p.scale_log2;
-    uint8_t* ds_row = sDS + slot * L::TILE_DS + row * 128;
-    float P[BQ];
-    bool ok = true;
-
-    for (int t = slot; t < n && ok; t += 2) {
-      const int j = t >> 1, st = t % NSTAGE;
-      const int qt = qt_hi - (t % n1), q0 = qt * BQ;
-      const float* qs = sQS + st * QSTAT_FLOATS;
-      const bool need_mask = (k0 + BN > Lk) ||
-                             (p.causal && (long long)q0 < (long long)(k0 + BN - 1) - diag - Rp) ||
-                             (has_window && (long long)(q0 + BQ - 1) > (long long)k0 - diag + p.window_left);
-
-      // ---- softmax replay: P^T from S^T. The row statistics were written by
-      // TMA, so this thread waits on the stage's transaction barrier itself.
-      if (!mbar_wait(&bars[BAR_QFULL + st], (t / NSTAGE) & 1, abort_flag, WAIT_LIMIT_NS) ||
-          !mbar_wait(&bars[BAR_SFULL + slot], j & 1, abort_flag, WAIT_LIMIT_NS)) { ok = false; break; }
-      __syncwarp();
-      tc_fence_after();
-      {
-        uint32_t ra[32], rb[32];
-        tmem_ld32(t_lane + L::col_s(slot), ra);
-        tmem_ld32(t_lane + L::col_s(slot) + 32, rb);
-        const float4* lse4 = reinterpret_cast<const float4*>(qs);
-        tmem_ld_wait(ra);
-        tmem_ld_wait(rb);
-#pragma unroll
-        for (int i4 = 0; i4 < BQ / 4; ++i4) {
-          const float4 l = lse4[i4];
-          const uint32_t* r = i4 < 8 ? ra : rb;
-          const int i = (i4 & 7) * 4;
-          P[i4 * 4 + 0] = ex2_approx(fmaf(__uint_as_float(r[i + 0]), scale_log2, -l.x));
-          P[i4 * 4 + 1] = ex2_approx(fmaf(__uint_as_float(r[i + 1]), scale_log2, -l.y));
-          P[i4 * 4 + 2] = ex2_approx(fmaf(__uint_as_float(r[i + 2]), scale_log2, -l.z));
-          P[i4 * 4 + 3] = ex2_approx(fmaf(__uint_as_float(r[i + 3]), scale_log2, -l.w));
-        }
-      }
-      if (need_mask) {
-#pragma unroll
-        for (int i = 0; i < BQ; ++i) {
-          const long long q = q0 + i;
-          if (row_dead || q < q_lo_vis || q > q_hi_vis) P[i] = 0.f;
-        }
-      }
-#pragma unroll
-      for (int c16 = 0; c16 < 2; ++c16) {
-        uint32_t w[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(P[c16 * 32 + 2 * i], P[c16 * 32 + 2 * i + 1]);
-        tmem_st16(t_lane + L::col_s(slot) + c16 * 16, w);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bars[BAR_PREADY + slot]);
-
-      // ---- dS^T = P^T * (dP^T - delta) -> shared memory (K-major, swizzled)
-      if (!mbar_wait(&bars[BAR_DPFULL + slot], j & 1, abort_flag, WAIT_LIMIT_NS)) { ok = false; break; }
-      // This slot's dS^T buffer is read by G4/G5 of tile t-2 until they complete
-      // (and, on the dS route, by the bulk store of tile t-2).
-      if (j >= 1 && !mbar_wait(&bars[BAR_DQFULL + slot], (j - 1) & 1, abort_flag, WAIT_LIMIT_NS)) { ok = false; break; }
-      if (DS_OUT && j >= 1 &&
-          !mbar_wait(&bars[BAR_DSCOPIED + slot], (j - 1) & 1, abort_flag, WAIT_LIMIT_NS)) { ok = false; break; }
-      __syncwarp();
-      tc_fence_after();
-      {
-        uint32_t ra[32], rb[32];
-        tmem_ld32(t_lane + L::col_dp(slot), ra);
-        tmem_ld32(t_lane + L::col_dp(slot) + 32, rb);
-        tmem_ld_wait(ra);
-        tmem_ld_wait(rb);
-        tc_fence_before();
-        mbar_arrive(&bars[BAR_DPREAD + slot]);  // the dP^T columns may be overwritten
-        const float4* delta4 = reinterpret_cast<const float4*>(qs + BQ);
-#pragma unroll
-        for (int chunk = 0; chunk < 8; ++chunk) {  // 8 queries = 16 bytes of dS^T per chunk
-          const uint32_t* r = chunk < 4 ? ra : rb;
-          const int i = (chunk & 3) * 8;
-          const float4 d0 = delta4[chunk * 2], d1 = delta4[chunk * 2 + 1];
-          const int c = chunk * 8;
-          const uint32_t w0 = pack_bf16x2(P[c + 0] * (__uint_as_float(r[i + 0]) - d0.x),
-                                          P[c + 1] * (__uint_as_float(r[i + 1]) - d0.y));
-          const uint32_t w1 = pack_bf16x2(P[c + 2] * (__uint_as_float(r[i + 2]) - d0.z),
-                                          P[c + 3] * (__uint_as_float(r[i + 3]) - d0.w));
-          const uint32_t w2 = pack_bf16x2(P[c + 4] * (__uint_as_float(r[i + 4]) - d1.x),
-                                          P[c + 5] * (__uint_as_float(r[i + 5]) - d1.y));
-          const uint32_t w3 = pack_bf16x2(P[c + 6] * (__uint_as_float(r[i + 6]) - d1.z),
-                                          P[c + 7] * (__uint_as_float(r[i + 7]) - d1.w));
-          *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (row & 7)) << 4)) = make_uint4(w0, w1, w2, w3);
-        }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&bars[BAR_DSREADY + slot]);
-    }
-
-    // ---- epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK. Each
-    // thread converts its key row into the warpgroup's half of the (now idle)
-    // Q/dO stage ring, in the 128-byte-swizzled box layout, and one thread per
-    // warpgroup writes the rows with TMA stores, which drop rows past S_kv.
-    // Every lane runs the (warp-collective) tensor-memory loads.
-    if (n > 0 && ok) {
-      ok = mbar_wait(&bars[BAR_MMADONE], 0, abort_flag, WAIT_LIMIT_NS);
-      __syncwarp();
-      tc_fence_after();
-    }
-    const bool warp_ok = __all_sync(0xffffffffu, ok);
-    const uint32_t col0 = slot ? L::COL_DK : L::COL_DV;
-    const float mult = slot ? p.scale : 1.f;
-    uint8_t* stg = slot ? sDO : sQ;
-    static_assert(L::NST * L::TILE_Q >= D / 64 * L::BLK_KV, "staging fits in a stage ring");
-#pragma unroll
-    for (int c32 = 0; c32 < D / 32; ++c32) {
-      uint32_t r[32];
-      if (n > 0 && warp_ok) {
-        tmem_ld32(t_lane + col0 + c32 * 32, r);
-        tmem_ld_wait(r);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) r[i] = 0u;
-      }
-      uint8_t* dst_row = stg + (c32 >> 1) * L::BLK_KV + row * 128;
-#pragma unroll
-      for (int v8 = 0; v8 < 4; ++v8) {
-        uint4 o;
-        o.x = pack_bf16x2(__uint_as_float(r[v8 * 8 + 0]) * mult, __uint_as_float(r[v8 * 8 + 1]) * mult);
-        o.y = pack_bf16x2(__uint_as_float(r[v8 * 8 + 2]) * mult, __uint_as_float(r[v8 * 8 + 3]) * mult);
-        o.z = pack_bf16x2(__uint_as_float(r[v8 * 8 + 4]) * mult, __uint_as_float(r[v8 * 8 + 5]) * mult);
-        o.w = pack_bf16x2(__uint_as_float(r[v8 * 8 + 6]) * mult, __uint_as_float(r[v8 * 8 + 7]) * mult);
-        const int piece = (c32 & 1) * 4 + v8;
-        *reinterpret_cast<uint4*>(dst_row + ((piece ^ (row & 7)) << 4)) = o;
-      }
-    }
-    fence_proxy_async_smem();
-    named_bar_sync(1 + slot, 128);
-    if (row == 0) {
-      const long long head = out_head;
-      const CUtensorMap* map = slot ? &maps.dk_out : &maps.dv_out;
-      for (int blk = 0; blk < D / 64; ++blk) tma_store_3d(map, stg + blk * L::BLK_KV, blk * 64, k0, (int)head);
-      bulk_commit_group();
-      bulk_wait_group_read0();  // the CTA may exit once the copies have read shared memory
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (*abort_flag && tid == 0) set_status(p.status, STATUS_TIMEOUT);
-  if (warp == 13) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
-}
-
-template <int D, bool DS_OUT>
-static cudaError_t set_main_smem() {
-  return cudaFuncSetAttribute(sdpa_bwd_main<D, DS_OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              MainLayout<D, DS_OUT>::BYTES);
-}
-
 cudaError_t main_kernel_setup() {
-  cudaError_t e = set_main_smem<64, false>();
-  if (e == cudaSuccess) e = set_main_smem<128, false>();
-  if (e == cudaSuccess) e = set_main_smem<128, true>();
+  cudaError_t e = main_variant_setup<false>();
+  if (e == cudaSuccess) e = main_bias_kernel_setup();
   return e;
 }
 
-// One CTA per (key tile, head group) work unit.
 cudaError_t launch_main(const MainMaps& maps, const ChainParams& p, cudaStream_t s) {
-  const dim3 grid((unsigned)(p.n_kt * p.B * p.Hkv * p.n_part));
-  const dim3 block(MAIN_THREADS);
-  if (p.Dqk == 64)
-    return launch_kernel(sdpa_bwd_main<64, false>, grid, block, MainLayout<64, false>::BYTES, s, true,
-                         maps, p);
-  if (p.ds_route)
-    return launch_kernel(sdpa_bwd_main<128, true>, grid, block, MainLayout<128, true>::BYTES, s, true,
-                         maps, p);
-  return launch_kernel(sdpa_bwd_main<128, false>, grid, block, MainLayout<128, false>::BYTES, s, true,
-                       maps, p);
+  if (p.bias != nullptr) return launch_main_bias(maps, p, s);
+  return launch_main_variant<false>(maps, p, s);
 }
 
 }  // namespace sdpa

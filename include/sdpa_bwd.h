@@ -54,6 +54,12 @@ typedef enum {
   SDPA_ERR_TIMEOUT = 6      /* a device-side bounded wait ran out (reported later)  */
 } sdpa_status;
 
+/* Element type of an optional additive bias (sdpa_bwd_bias, sdpa_fwd_bias). */
+typedef enum {
+  SDPA_DTYPE_BF16 = 0,
+  SDPA_DTYPE_F32 = 1
+} sdpa_dtype;
+
 /*
  * Bytes of device workspace sdpa_bwd() needs for this problem (0 when none).
  * The workspace holds, each region 256-byte aligned: per-query-tile fp32 row
@@ -132,6 +138,40 @@ int sdpa_bwd_sink(const void* q, const void* k, const void* v, const void* o, co
                   int window_left, int window_right, int deterministic,
                   const int32_t* seq_q_lens, const int32_t* seq_kv_lens, void* workspace,
                   size_t workspace_bytes, const float* sink, float* dsink, void* stream);
+
+/*
+ * SDPA backward with an additive bias (cuDNN frontend docs, "SDPA Backward
+ * (SM120)": the bias capability). A (bias_batch, H_q, S_q, S_kv) tensor is
+ * added to the scaled scores before the softmax,
+ *     P = exp(scale * Q K^T + bias - LSE),
+ * where lse is the forward's LSE of the same biased scores. dQ, dK and dV keep
+ * their formulas with this P; the gradient of the bias is
+ *     dBias = dS = P * (dP - delta)     (fp32, 0 at masked pairs),
+ * summed over the batch rows when bias_batch = 1 and B > 1.
+ * Arguments: those of sdpa_bwd_sink(), where sink and dsink may both be NULL
+ * (no sink) or dsink alone NULL (a sink in the forward's LSE, no dsink), then
+ *   bias        device (bias_batch, H_q, S_q, S_kv) tensor, contiguous, S_kv
+ *               innermost; bf16 (2-byte aligned) or fp32 (4-byte aligned).
+ *   bias_dtype  SDPA_DTYPE_BF16 or SDPA_DTYPE_F32.
+ *   bias_batch  1 (one bias shared by every batch row) or B.
+ *   dbias       device fp32 output shaped like bias (4-byte aligned), or NULL.
+ *               Every element is overwritten. With bias_batch = B, or B = 1,
+ *               each element is written once and the result is bitwise
+ *               reproducible; with bias_batch = 1 and B > 1 the batch rows
+ *               add into it atomically (not reproducible), which deterministic
+ *               mode rejects.
+ * Served for D_qk = D_v = 64 or 128. Returns SDPA_ERR_INVALID for a NULL bias,
+ * an unknown dtype, bias_batch not 1 or B, or the deterministic case above;
+ * SDPA_ERR_UNSUPPORTED for D_qk = 192; otherwise as sdpa_bwd(). Workspace as
+ * sdpa_bwd_workspace_size().
+ */
+int sdpa_bwd_bias(const void* q, const void* k, const void* v, const void* o, const void* d_o,
+                  const float* lse, void* dq, void* dk, void* dv, int B, int H_q, int H_kv,
+                  int S_q, int S_kv, int D_qk, int D_v, float scale, int causal, int bottom_right,
+                  int window_left, int window_right, int deterministic,
+                  const int32_t* seq_q_lens, const int32_t* seq_kv_lens, void* workspace,
+                  size_t workspace_bytes, const float* sink, float* dsink, const void* bias,
+                  int bias_dtype, int bias_batch, float* dbias, void* stream);
 
 /*
  * SDPA forward: the O and natural-log LSE that sdpa_bwd() takes (cuDNN frontend

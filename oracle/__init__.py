@@ -113,6 +113,7 @@ def _load():
         lib.oracle_backward_sampled.argtypes = [C, P, P, P, P, P, P, ctypes.c_long, I64, P,
                                                 ctypes.c_long, I64, P, P]
         lib.oracle_dbias.argtypes = [C, P, P, P, P, P, P, P]
+        lib.oracle_dbias_rows.argtypes = [C, P, P, P, P, P, P, ctypes.c_long, I64, P]
         lib.oracle_count_visible.argtypes = [C]
         lib.oracle_count_visible.restype = ctypes.c_longlong
         lib.oracle_max_threads.restype = ctypes.c_int
@@ -238,6 +239,26 @@ def dbias(p: Problem, q, k, v, o, do, lse, bias):
     s, keep = p._struct(bias)
     out = np.zeros((s.bias_batch, p.Hq, p.Sq, p.Skv))
     lib.oracle_dbias(ctypes.byref(s), _p(q), _p(k), _p(v), _p(o), _p(do), _p(lse), _p(out))
+    return out
+
+
+def dbias_rows(p: Problem, q, k, v, o, do, lse, bias, rows):
+    """dbias() at the flat bias rows ``rows`` ((bb * Hq + h) * Sq + q), (len(rows), Skv)."""
+    _check_heads(p)
+    lib = _load()
+    q = _f64(q, (p.B, p.Hq, p.Sq, p.Dqk))
+    k = _f64(k, (p.B, p.Hkv, p.Skv, p.Dqk))
+    v = _f64(v, (p.B, p.Hkv, p.Skv, p.Dv))
+    o = _f64(o, (p.B, p.Hq, p.Sq, p.Dv))
+    do = _f64(do, (p.B, p.Hq, p.Sq, p.Dv))
+    lse = _f64(lse, (p.B, p.Hq, p.Sq))
+    s, keep = p._struct(bias)
+    ri = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    if ri.size and (ri.min() < 0 or ri.max() >= s.bias_batch * p.Hq * p.Sq):
+        raise ValueError("bias row out of range")
+    out = np.zeros((len(ri), p.Skv))
+    lib.oracle_dbias_rows(ctypes.byref(s), _p(q), _p(k), _p(v), _p(o), _p(do), _p(lse), len(ri),
+                          ri.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), _p(out))
     return out
 
 

@@ -318,36 +318,52 @@ void oracle_backward_sampled(const oracle_cfg *c, const double *Q, const double 
  * visible pair, 0 elsewhere; with bias_batch = 1 (and B > 1) the batch rows'
  * dS are summed, in ascending b order. Requires c->bias (P replays the biased
  * scores). */
+/* One dBias row: flat bias row r = (bb * Hq + h) * Sq + q, all S_kv keys. */
+static void dbias_row(const oracle_cfg *c, const double *Q, const double *K, const double *V,
+                      const double *dO, const double *LSE, const double *delta, long r,
+                      double *out) {
+    const int G = c->Hq / c->Hkv;
+    const long q = r % c->Sq, bbh = r / c->Sq;
+    const int bb = (int)(bbh / c->Hq), h = (int)(bbh % c->Hq);
+    for (long k = 0; k < c->Skv; ++k) out[k] = 0.0;
+    const int b_lo = c->bias_batch == 1 ? 0 : bb;
+    const int b_hi = c->bias_batch == 1 ? c->B : bb + 1;
+    for (int b = b_lo; b < b_hi; ++b) {
+        int Lq, Lk;
+        lengths(c, b, &Lq, &Lk);
+        const long bh = (long)b * c->Hq + h, bhk = (long)b * c->Hkv + h / G;
+        const double *qr = row_of(Q, bh, q, c->Sq, c->Dqk);
+        const double *dor = row_of(dO, bh, q, c->Sq, c->Dv);
+        const double lse = LSE[bh * c->Sq + q], D = delta[bh * c->Sq + q];
+        for (long k = 0; k < c->Skv; ++k) {
+            if (!visible(c, Lq, Lk, q, k)) continue;
+            const double *kr = row_of(K, bhk, k, c->Skv, c->Dqk);
+            double p = prob(c, score(c, qr, kr, bh, q, k), lse);
+            double dp = dot(dor, row_of(V, bhk, k, c->Skv, c->Dv), c->Dv);
+            out[k] += p * (dp - D);
+        }
+    }
+}
+
 void oracle_dbias(const oracle_cfg *c, const double *Q, const double *K, const double *V,
                   const double *O, const double *dO, const double *LSE, double *dBias) {
-    const int G = c->Hq / c->Hkv;
     const long qrows = (long)c->B * c->Hq * c->Sq;
     double *delta = (double *)malloc(sizeof(double) * (size_t)(qrows > 0 ? qrows : 1));
     oracle_delta(c, O, dO, delta);
     const long out_rows = (long)c->bias_batch * c->Hq * c->Sq;
 #pragma omp parallel for schedule(dynamic, 8)
-    for (long r = 0; r < out_rows; ++r) {
-        const long q = r % c->Sq, bbh = r / c->Sq;
-        const int bb = (int)(bbh / c->Hq), h = (int)(bbh % c->Hq);
-        double *out = dBias + r * c->Skv;
-        for (long k = 0; k < c->Skv; ++k) out[k] = 0.0;
-        const int b_lo = c->bias_batch == 1 ? 0 : bb;
-        const int b_hi = c->bias_batch == 1 ? c->B : bb + 1;
-        for (int b = b_lo; b < b_hi; ++b) {
-            int Lq, Lk;
-            lengths(c, b, &Lq, &Lk);
-            const long bh = (long)b * c->Hq + h, bhk = (long)b * c->Hkv + h / G;
-            const double *qr = row_of(Q, bh, q, c->Sq, c->Dqk);
-            const double *dor = row_of(dO, bh, q, c->Sq, c->Dv);
-            const double lse = LSE[bh * c->Sq + q], D = delta[bh * c->Sq + q];
-            for (long k = 0; k < c->Skv; ++k) {
-                if (!visible(c, Lq, Lk, q, k)) continue;
-                const double *kr = row_of(K, bhk, k, c->Skv, c->Dqk);
-                double p = prob(c, score(c, qr, kr, bh, q, k), lse);
-                double dp = dot(dor, row_of(V, bhk, k, c->Skv, c->Dv), c->Dv);
-                out[k] += p * (dp - D);
-            }
-        }
-    }
+    for (long r = 0; r < out_rows; ++r) dbias_row(c, Q, K, V, dO, LSE, delta, r, dBias + r * c->Skv);
+    free(delta);
+}
+
+/* dBias at the flat bias rows rows[i] = (bb * Hq + h) * Sq + q: out is (n, S_kv). */
+void oracle_dbias_rows(const oracle_cfg *c, const double *Q, const double *K, const double *V,
+                       const double *O, const double *dO, const double *LSE, long n,
+                       const int64_t *rows, double *out) {
+    const long qrows = (long)c->B * c->Hq * c->Sq;
+    double *delta = (double *)malloc(sizeof(double) * (size_t)(qrows > 0 ? qrows : 1));
+    oracle_delta(c, O, dO, delta);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long i = 0; i < n; ++i) dbias_row(c, Q, K, V, dO, LSE, delta, rows[i], out + i * c->Skv);
     free(delta);
 }

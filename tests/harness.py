@@ -25,18 +25,22 @@ def f64(x: torch.Tensor) -> np.ndarray:
     return x.double().numpy()
 
 
-def make_case(w: workloads.Workload, sink: bool = False):
+def make_case(w: workloads.Workload, sink: bool = False, bias=None):
     """Seeded inputs plus O (bf16) and LSE (fp32) from the oracle forward; with
-    ``sink`` the forward takes the workload's sink logits (case["sink"])."""
+    ``sink`` the forward takes the workload's sink logits (case["sink"]); with
+    ``bias`` = (batch, dtype) an additive bias of that batch (1 or B) and element
+    type (case["bias"]), which the oracle sees exactly as the GPU does."""
     t = workloads.generate(w)
     t["sink"] = workloads.sink_logits(w) if sink else None
+    t["bias"] = None if bias is None else workloads.bias_tensor(w, bias[0], bias[1])
     p = oracle.Problem(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.Dqk, w.Dv, scale=w.resolved_scale,
                        causal=w.causal, bottom_right=w.bottom_right, window_left=w.window_left,
                        window_right=w.window_right,
                        seq_q_lens=None if t["seq_q_lens"] is None else t["seq_q_lens"].numpy(),
                        seq_kv_lens=None if t["seq_kv_lens"] is None else t["seq_kv_lens"].numpy())
     o64, lse64 = oracle.forward(p, f64(t["q"]), f64(t["k"]), f64(t["v"]),
-                                None if t["sink"] is None else t["sink"].double().numpy())
+                                None if t["sink"] is None else t["sink"].double().numpy(),
+                                bias=None if t["bias"] is None else f64(t["bias"]))
     t["o"] = torch.from_numpy(o64).to(torch.bfloat16)
     t["lse"] = torch.from_numpy(lse64).float()
     t["problem"] = p
@@ -44,10 +48,23 @@ def make_case(w: workloads.Workload, sink: bool = False):
     return t
 
 
+def _bias64(case):
+    return None if case.get("bias") is None else f64(case["bias"])
+
+
 def oracle_backward(case):
     p = case["problem"]
     return oracle.backward(p, f64(case["q"]), f64(case["k"]), f64(case["v"]), f64(case["o"]),
-                           f64(case["do"]), case["lse"].double().numpy())
+                           f64(case["do"]), case["lse"].double().numpy(), bias=_bias64(case))
+
+
+def oracle_dbias(case, rows=None):
+    """dBias from the bf16 inputs and fp32 LSE the GPU sees: in full, or at the
+    flat bias rows ``rows`` ((bb * Hq + h) * Sq + q) as a (len(rows), Skv) array."""
+    p = case["problem"]
+    args = (p, f64(case["q"]), f64(case["k"]), f64(case["v"]), f64(case["o"]), f64(case["do"]),
+            case["lse"].double().numpy(), _bias64(case))
+    return oracle.dbias(*args) if rows is None else oracle.dbias_rows(*args, rows)
 
 
 def oracle_dsink(case):
@@ -65,12 +82,13 @@ def oracle_sampled(case, q_rows, kv_rows):
     p = case["problem"]
     return oracle.backward_sampled(p, f64(case["q"]), f64(case["k"]), f64(case["v"]),
                                    f64(case["o"]), f64(case["do"]), case["lse"].double().numpy(),
-                                   q_rows, kv_rows)
+                                   q_rows, kv_rows, bias=_bias64(case))
 
 
 def to_device(case, dev="cuda"):
     d = {k: case[k].to(dev) for k in ("q", "k", "v", "o", "do", "lse")}
     d["sink"] = None if case.get("sink") is None else case["sink"].to(dev)
+    d["bias"] = None if case.get("bias") is None else case["bias"].to(dev)
     for k in ("seq_q_lens", "seq_kv_lens"):
         d[k] = None if case[k] is None else case[k].to(dev)
     return d

@@ -174,3 +174,29 @@ def test_forward_argument_validation(lib):
     assert call_fwd(lib, ptrs) == ALIGN
     assert call_fwd(lib, sink=FAKE + 1) == ALIGN
     assert call_fwd(lib, wr=3, causal=0) == UNSUPPORTED
+
+
+def call_bias(lib, bias, dtype=0, batch=1, dbias=FAKE, B=1, det=0, Dqk=128, Dv=128, sink=None,
+              dsink=None):
+    vp = [ctypes.c_void_p(FAKE)] * 9
+    return lib.sdpa_bwd_bias(*vp, B, 2, 2, 128, 128, Dqk, Dv, ctypes.c_float(0.0), 0, 0, -1, -1, det,
+                             None, None, None, 0,
+                             None if sink is None else ctypes.c_void_p(sink),
+                             None if dsink is None else ctypes.c_void_p(dsink),
+                             None if bias is None else ctypes.c_void_p(bias), dtype, batch,
+                             None if dbias is None else ctypes.c_void_p(dbias), None)
+
+
+def test_bias_argument_validation(lib):
+    lib.sdpa_bwd_bias.restype = ctypes.c_int
+    assert call_bias(lib, None) == INVALID
+    assert call_bias(lib, FAKE, dtype=2) == INVALID          # unknown element type
+    assert call_bias(lib, FAKE, batch=3, B=2) == INVALID     # bias batch is 1 or B
+    assert call_bias(lib, FAKE, batch=0) == INVALID
+    # a one-batch dBias summed over B > 1 batch rows is atomic: not in deterministic mode
+    assert call_bias(lib, FAKE, batch=1, B=2, det=1) == INVALID
+    assert call_bias(lib, FAKE, dsink=FAKE) == INVALID        # dsink needs the sink logits
+    assert call_bias(lib, FAKE + 1, dtype=0) == ALIGN         # bf16 bias: 2-byte alignment
+    assert call_bias(lib, FAKE + 2, dtype=1) == ALIGN         # fp32 bias: 4-byte alignment
+    assert call_bias(lib, FAKE, dbias=FAKE + 2) == ALIGN      # fp32 dBias: 4-byte alignment
+    assert call_bias(lib, FAKE, Dqk=192, Dv=128) == UNSUPPORTED

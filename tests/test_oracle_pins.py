@@ -560,3 +560,15 @@ def test_rank_one_bias_equals_one_more_head_dim(oracle_mod):
     db = oracle_mod.dbias(p, q, k, v, o, do, lse, bias)
     np.testing.assert_allclose((db * w[..., None, :]).sum(-1), dqa[..., 3] / p.resolved_scale,
                                atol=1e-13)
+
+
+def test_dbias_rows_equal_full_dbias(oracle_mod):
+    for batch1 in (False, True):
+        p = FD_CASES["padded"]
+        q, k, v, do = _inputs(p, seed=32)
+        bias = _bias(p, 33, 1 if batch1 else p.B)
+        o, lse = oracle_mod.forward(p, q, k, v, bias=bias)
+        full = oracle_mod.dbias(p, q, k, v, o, do, lse, bias).reshape(-1, p.Skv)
+        rows = [0, 3, 5, full.shape[0] - 1]
+        np.testing.assert_array_equal(oracle_mod.dbias_rows(p, q, k, v, o, do, lse, bias, rows),
+                                      full[rows])

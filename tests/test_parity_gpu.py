@@ -13,7 +13,7 @@ import torch
 
 import workloads
 from harness import (assert_close, errors, gpu_backward, make_case, oracle_backward,
-                     oracle_dsink, oracle_sampled, to_device)
+                     oracle_dbias, oracle_dsink, oracle_sampled, to_device)
 
 pytestmark = pytest.mark.gpu
 
@@ -364,3 +364,146 @@ def test_forward_then_backward_matches_oracle():
     assert_close("dq", dq.double().cpu().numpy(), rq)
     assert_close("dk", dk.double().cpu().numpy(), rk)
     assert_close("dv", dv.double().cpu().numpy(), rv)
+
+
+# ---------------------------------------------------------------- additive bias
+# The bias joins the scores before the softmax (the oracle forward gives the
+# LSE of the biased scores); dQ/dK/dV and the fp32 dBias are checked against
+# the oracle with the gradient bar. dBias comes back NaN-poisoned, so every
+# element must be written: visited tiles by the main kernel (masked pairs as
+# 0), the others by the preprocess. "1" marks one bias batch shared by B > 1
+# batch rows (dBias summed atomically), "B" a bias per batch row.
+BIAS_CASES = {
+    "d128_causal_ragged_B_bf16": (SMALL["d128_causal_ragged"], "B", torch.bfloat16),
+    "gqa_shared_f32": (SMALL["gqa"], "1", torch.float32),
+    "gqa_det_B_bf16": (SMALL["gqa_det"], "B", torch.bfloat16),          # stored-dS route
+    "det_padded_odd_B_f32": (SMALL["det_padded_odd"], "B", torch.float32),
+    "padded_window_shared_bf16": (SMALL["padded_window"], "1", torch.bfloat16),
+    "tl_causal_long_q_d64_B_bf16": (SMALL["tl_causal_long_q"], "B", torch.bfloat16),
+    "det_d64_relay_B_f32": (SMALL["det_d64_relay"], "B", torch.float32),
+    "window_only_B_bf16": (SMALL["window_only"], "B", torch.bfloat16),
+    "single_key_d64_B_f32": (SMALL["single_key"], "B", torch.float32),
+    "d128_dense_ragged_shared_bf16": (SMALL["d128_dense_ragged"], "1", torch.bfloat16),
+    "br_causal_long_kv_B_f32": (SMALL["br_causal_long_kv"], "B", torch.float32),
+}
+
+
+def _bias_case(w, kind, dtype):
+    return make_case(w, bias=(1 if kind == "1" else w.B, dtype))
+
+
+def _gpu_bias(case, d):
+    dbias = torch.full(tuple(d["bias"].shape), float("nan"), dtype=torch.float32, device="cuda")
+    out = gpu_backward(case, d, bias=d["bias"], dbias=dbias)
+    assert len(out) == 4 and out[3] is dbias
+    return out
+
+
+@pytest.mark.parametrize("name", sorted(BIAS_CASES))
+def test_bias_parity(name):
+    case = _bias_case(*BIAS_CASES[name])
+    d = to_device(case)
+    dq, dk, dv, dbias = _gpu_bias(case, d)
+    rq, rk, rv = oracle_backward(case)
+    assert_close("dq", dq.double().cpu().numpy(), rq)
+    assert_close("dk", dk.double().cpu().numpy(), rk)
+    assert_close("dv", dv.double().cpu().numpy(), rv)
+    rb = oracle_dbias(case)
+    gb = dbias.double().cpu().numpy()
+    assert_close("dbias", gb, rb)
+    # masked pairs and padding carry exact zeros
+    masked = ~_visible_mask(case)
+    if masked.any():
+        assert np.all(gb[np.broadcast_to(masked, gb.shape)] == 0.0)
+
+
+def _visible_mask(case):
+    """(bias_batch, 1, Sq, Skv) pairs visible in every batch row the bias serves."""
+    w = case["workload"]
+    p = case["problem"]
+    qi = np.arange(w.Sq)[:, None]
+    ki = np.arange(w.Skv)[None, :]
+    vis = []
+    for b in range(w.B):
+        Lq = w.Sq if p.seq_q_lens is None else int(p.seq_q_lens[b])
+        Lk = w.Skv if p.seq_kv_lens is None else int(p.seq_kv_lens[b])
+        diag = (Lk - Lq) if w.bottom_right else 0
+        m = (qi < Lq) & (ki < Lk)
+        if w.causal:
+            m &= ki <= qi + diag + max(w.window_right, 0)
+        if w.window_left >= 0:
+            m &= ki >= qi + diag - w.window_left
+        vis.append(m)
+    vis = np.stack(vis)[:, None]
+    if case["bias"].shape[0] == 1:
+        vis = vis.any(0, keepdims=True)
+    return vis
+
+
+def test_bias_without_dbias_matches():
+    """bias_grad=False computes the same dQ/dK/dV without writing a dBias."""
+    case = _bias_case(*BIAS_CASES["gqa_det_B_bf16"])
+    d = to_device(case)
+    a = _gpu_bias(case, d)
+    b = gpu_backward(case, d, bias=d["bias"], bias_grad=False)
+    assert len(b) == 3
+    for x, y in zip(a[:3], b):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+
+
+def test_bias_with_sink():
+    case = make_case(SMALL["det_padded_odd"], sink=True, bias=(2, torch.float32))
+    d = to_device(case)
+    dbias = torch.full(tuple(d["bias"].shape), float("nan"), dtype=torch.float32, device="cuda")
+    dq, dk, dv, dsink, db = gpu_backward(case, d, sink=d["sink"], bias=d["bias"], dbias=dbias)
+    rq, rk, rv = oracle_backward(case)
+    assert_close("dq", dq.double().cpu().numpy(), rq)
+    assert_close("dk", dk.double().cpu().numpy(), rk)
+    assert_close("dv", dv.double().cpu().numpy(), rv)
+    assert_close("dbias", db.double().cpu().numpy(), oracle_dbias(case))
+    ref, mag = oracle_dsink(case)
+    _dsink_close(dsink.double().cpu().numpy(), ref, mag)
+
+
+@pytest.mark.parametrize("name", ["gqa_det_B_bf16", "det_d64_relay_B_f32"])
+def test_dbias_bitwise_reproducible(name):
+    """A per-batch dBias is written once per element: bitwise reproducible
+    (10 runs), like dQ/dK/dV in deterministic mode."""
+    case = _bias_case(*BIAS_CASES[name])
+    d = to_device(case)
+    first = [t.clone() for t in _gpu_bias(case, d)]
+    for _ in range(9):
+        again = _gpu_bias(case, d)
+        for a, b in zip(first, again):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+# Full-size bias cases: the causal MHA workload with one bias shared by both
+# batch rows (atomic dBias), and a grouped shape whose work units carry two
+# query heads (G = 8, 8 key tiles x 8 groups x 4 parts x 2 >= 1.5 units per SM).
+BIAS_FULL = {
+    "causal_mha_shared_bf16": (workloads.WORKLOADS["causal_mha"], "1", torch.bfloat16),
+    "grouped_B_f32": (W("bias_groups", 1, 64, 8, 1024, 1024, 128, 128, causal=True, seed=41), "B",
+                      torch.float32),
+}
+
+
+@pytest.mark.parametrize("name", sorted(BIAS_FULL))
+def test_bias_full_size_sampled(name):
+    case = _bias_case(*BIAS_FULL[name])
+    w = case["workload"]
+    d = to_device(case)
+    dq, dk, dv, dbias = _gpu_bias(case, d)
+    q_rows, kv_rows = _sample_rows(w, None, np.random.default_rng(w.seed))
+    rq, rk, rv = oracle_sampled(case, q_rows, kv_rows)
+    assert_close("dq", dq.reshape(-1, w.Dqk)[torch.from_numpy(q_rows).cuda()].double().cpu().numpy(), rq)
+    assert_close("dk", dk.reshape(-1, w.Dqk)[torch.from_numpy(kv_rows).cuda()].double().cpu().numpy(), rk)
+    assert_close("dv", dv.reshape(-1, w.Dv)[torch.from_numpy(kv_rows).cuda()].double().cpu().numpy(), rv)
+    nb = dbias.shape[0]
+    rows = np.unique(np.array([(bb * w.Hq + h) * w.Sq + q for bb in range(nb) for h in (0, w.Hq - 1)
+                               for q in (0, 63, 64, 127, 128, w.Sq // 2 + 5, w.Sq - 1)] +
+                              list(np.random.default_rng(w.seed + 1).integers(0, nb * w.Hq * w.Sq, 16))))
+    rb = oracle_dbias(case, rows)
+    gb = dbias.reshape(-1, w.Skv)[torch.from_numpy(rows).cuda()].double().cpu().numpy()
+    assert_close("dbias", gb, rb)
+    assert torch.isfinite(dbias).all()

@@ -84,6 +84,15 @@ def generate(w: Workload) -> Dict[str, Optional[torch.Tensor]]:
             "seq_q_lens": lens, "seq_kv_lens": None if lens is None else lens.clone()}
 
 
+def bias_tensor(w: Workload, batch: int, dtype=torch.bfloat16) -> torch.Tensor:
+    """Seeded additive bias (batch, Hq, Sq, Skv), batch 1 or B, N(0, 1) rounded to
+    ``dtype``, from a stream of its own."""
+    if batch not in (1, w.B):
+        raise ValueError("the bias batch is 1 or B")
+    g = torch.Generator("cpu").manual_seed(w.seed + 2_000_003)
+    return torch.randn(batch, w.Hq, w.Sq, w.Skv, generator=g, dtype=torch.float32).to(dtype)
+
+
 def sink_logits(w: Workload) -> torch.Tensor:
     """Seeded fp32 (Hq,) sink-token logits, N(0, 1), from a stream of their own."""
     g = torch.Generator("cpu").manual_seed(w.seed + 1_000_003)
