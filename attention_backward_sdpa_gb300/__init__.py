@@ -64,6 +64,8 @@ def load(build_if_missing: bool = False):
     lib.sdpa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, ctypes.c_float, i, i, i, i,
                              vp, vp, vp, vp]
     lib.sdpa_fwd.restype = i
+    lib.sdpa_fwd_bias.argtypes = list(lib.sdpa_fwd.argtypes[:-1]) + [vp, i, i, vp]
+    lib.sdpa_fwd_bias.restype = i
     lib.sdpa_bwd_workspace_size.argtypes = [i, i, i, i, i, i, i, i]
     lib.sdpa_bwd_workspace_size.restype = sz
     lib.sdpa_status_string.argtypes = [i]
@@ -216,10 +218,13 @@ def sdpa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: Option
              causal: bool = False, bottom_right: bool = False, window_left: int = -1,
              window_right: int = -1, seq_q_lens: Optional[torch.Tensor] = None,
              seq_kv_lens: Optional[torch.Tensor] = None, sink: Optional[torch.Tensor] = None,
+             bias: Optional[torch.Tensor] = None,
              o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
              stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
     """O (bf16, (B,Hq,Sq,Dv)) and natural-log LSE (fp32, (B,Hq,Sq)) of the masked
-    softmax attention (see include/sdpa_bwd.h); the inputs of sdpa_bwd."""
+    softmax attention (see include/sdpa_bwd.h); the inputs of sdpa_bwd. ``bias``
+    ((1|B, Hq, Sq, Skv) bf16 or fp32 CUDA, contiguous) is added to the scaled
+    scores (sdpa_fwd_bias)."""
     lib = load()
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
         raise ValueError("q, k, v must be (B, H, S, D)")
@@ -243,11 +248,16 @@ def sdpa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: Option
             or lse.numel() != B * Hq * Sq:
         raise ValueError("lse must be a contiguous fp32 CUDA tensor with B*Hq*Sq elements")
     sc = 0.0 if scale is None else float(scale)
-    rc = lib.sdpa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Skv, Dqk, Dv, sc,
-                      int(causal), int(bottom_right), int(window_left), int(window_right),
-                      _ptr(seq_q_lens), _ptr(seq_kv_lens), _ptr(sink), _stream_handle(stream))
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Skv, Dqk, Dv, sc,
+            int(causal), int(bottom_right), int(window_left), int(window_right),
+            _ptr(seq_q_lens), _ptr(seq_kv_lens), _ptr(sink))
+    if bias is None:
+        rc = lib.sdpa_fwd(*args, _stream_handle(stream))
+    else:
+        dt = _check_bias(bias, B, Hq, Sq, Skv)
+        rc = lib.sdpa_fwd_bias(*args, _ptr(bias), dt, int(bias.shape[0]), _stream_handle(stream))
     if rc != 0:
-        raise SdpaError(rc, "sdpa_fwd")
+        raise SdpaError(rc, "sdpa_fwd_bias" if bias is not None else "sdpa_fwd")
     return o, lse
 
 

@@ -121,6 +121,12 @@ struct FwdParams {
   const int32_t* seq_q_lens;  // (B,) or null
   const int32_t* seq_kv_lens; // (B,) or null
   const float* sink;          // (Hq,) sink logits, or null
+  // Additive bias (optional), as in ChainParams: element (b, h, q, k) at
+  // bias[b * bias_bstride + (h * Sq + q) * Skv + k], bf16 or fp32.
+  const void* bias;
+  int bias_fp32;
+  long long bias_bstride;
+  int bias_vec;               // rows allow 16-byte loads (S_kv * size % 16 == 0, base aligned)
   float* lse;                 // (B, Hq, Sq) output
   int* status;                // device status word
 };

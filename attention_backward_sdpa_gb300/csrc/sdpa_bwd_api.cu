@@ -428,10 +428,14 @@ int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const v
                    seq_kv_lens, workspace, workspace_bytes, nullptr, nullptr, BiasArgs{}, stream);
 }
 
-int sdpa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
-             int H_kv, int S_q, int S_kv, int D_qk, int D_v, float scale, int causal,
-             int bottom_right, int window_left, int window_right, const int32_t* seq_q_lens,
-             const int32_t* seq_kv_lens, const float* sink, void* stream_) {
+}  // extern "C"
+
+namespace {
+
+int run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
+            int H_kv, int S_q, int S_kv, int D_qk, int D_v, float scale, int causal,
+            int bottom_right, int window_left, int window_right, const int32_t* seq_q_lens,
+            const int32_t* seq_kv_lens, const float* sink, const BiasArgs& ba, void* stream_) {
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   int rc = basic_checks(B, H_q, H_kv, S_q, S_kv, D_qk, D_v);
   if (rc != SDPA_OK) return rc;
@@ -440,6 +444,12 @@ int sdpa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
     if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return SDPA_ERR_ALIGN;
   for (const void* ptr : {(const void*)lse, (const void*)sink})
     if (reinterpret_cast<uintptr_t>(ptr) % 4 != 0) return SDPA_ERR_ALIGN;
+  if (ba.bias) {
+    if (ba.dtype != SDPA_DTYPE_BF16 && ba.dtype != SDPA_DTYPE_F32) return SDPA_ERR_INVALID;
+    if (ba.batch != 1 && ba.batch != B) return SDPA_ERR_INVALID;
+    if (reinterpret_cast<uintptr_t>(ba.bias) % (ba.dtype == SDPA_DTYPE_F32 ? 4 : 2) != 0)
+      return SDPA_ERR_ALIGN;
+  }
   if (window_right >= 0 && !causal) return SDPA_ERR_UNSUPPORTED;
   if (!(scale > 0.f) || !std::isfinite(scale)) scale = 1.0f / std::sqrt((float)D_qk);
   if (S_q == 0) return SDPA_OK;  // no rows
@@ -463,6 +473,13 @@ int sdpa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.seq_q_lens = seq_q_lens;
   p.seq_kv_lens = seq_kv_lens;
   p.sink = sink;
+  if (ba.bias) {
+    const int esz = ba.dtype == SDPA_DTYPE_F32 ? 4 : 2;
+    p.bias = ba.bias;
+    p.bias_fp32 = esz == 4;
+    p.bias_bstride = (ba.batch == 1) ? 0 : (long long)H_q * S_q * S_kv;
+    p.bias_vec = ((long long)S_kv * esz) % 16 == 0 && reinterpret_cast<uintptr_t>(ba.bias) % 16 == 0;
+  }
   p.lse = lse;
   p.status = status;
   FwdMaps maps;
@@ -477,6 +494,32 @@ int sdpa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
       !make_bhsd_map(&maps.o, o, D_v, S_q, BHq, 128))
     return SDPA_ERR_CUDA;
   return launch_fwd(maps, p, stream) == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int sdpa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
+             int H_kv, int S_q, int S_kv, int D_qk, int D_v, float scale, int causal,
+             int bottom_right, int window_left, int window_right, const int32_t* seq_q_lens,
+             const int32_t* seq_kv_lens, const float* sink, void* stream) {
+  return run_fwd(q, k, v, o, lse, B, H_q, H_kv, S_q, S_kv, D_qk, D_v, scale, causal, bottom_right,
+                 window_left, window_right, seq_q_lens, seq_kv_lens, sink, BiasArgs{}, stream);
+}
+
+int sdpa_fwd_bias(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
+                  int H_kv, int S_q, int S_kv, int D_qk, int D_v, float scale, int causal,
+                  int bottom_right, int window_left, int window_right, const int32_t* seq_q_lens,
+                  const int32_t* seq_kv_lens, const float* sink, const void* bias, int bias_dtype,
+                  int bias_batch, void* stream) {
+  if (!bias) return SDPA_ERR_INVALID;
+  BiasArgs ba;
+  ba.bias = bias;
+  ba.dtype = bias_dtype;
+  ba.batch = bias_batch;
+  return run_fwd(q, k, v, o, lse, B, H_q, H_kv, S_q, S_kv, D_qk, D_v, scale, causal, bottom_right,
+                 window_left, window_right, seq_q_lens, seq_kv_lens, sink, ba, stream);
 }
 
 int sdpa_bwd_sink(const void* q, const void* k, const void* v, const void* o, const void* d_o,

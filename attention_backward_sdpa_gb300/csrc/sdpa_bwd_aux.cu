@@ -4,8 +4,8 @@
 //               LSE * log2(e) (+inf for masked rows and LSE = -inf), staged
 //               per query tile; clears the fp32 dQ accumulator (rows below
 //               the query length) and the deterministic-mode counters;
-//               with a dBias output, writes the zeros of the dBias tiles that
-//               the main kernel does not visit. ("The kernel chain": dot.)
+//               clears a dBias that B > 1 batch rows add into atomically.
+//               ("The kernel chain": dot.)
 //   dq_convert  dQ = bf16(scale * dq_accum), dropping the accumulator's
 //               padding rows. ("The kernel chain": cvt.)
 // The dQ convert also carries the GQA group reduction of dK/dV (gqa.cuh).
@@ -23,31 +23,24 @@
 namespace sdpa {
 
 // ---------------------------------------------------------------- dBias zeros
-// dBias rows of query tile qt of query head bh that the main kernel leaves
-// alone: the main kernel writes every element of the (query tile, key tile)
-// pairs it visits (masked ones as 0), so a per-batch dBias needs zeros exactly
-// on the other key tiles of this query tile. A one-batch dBias that the batch
-// rows add into atomically is cleared in full, once (by batch row 0).
-__device__ void zero_unvisited_dbias(const ChainParams& p, unsigned bh, int qt, int Lq, int Lk) {
+// One dBias shared by B > 1 batch rows receives their terms by atomic adds, so
+// it must be all zeros before the main kernel starts: the batch-row-0 tiles of
+// this kernel clear it, query tile by query tile (16-byte stores where the
+// rows allow). A per-batch dBias is not touched here: the main kernel writes
+// every element of the blocks it computes and zeros the others.
+__device__ void zero_shared_dbias_rows(const ChainParams& p, unsigned bh, int qt) {
   const int b = (int)(bh / (unsigned)p.Hq), h = (int)(bh % (unsigned)p.Hq);
-  if (p.dbias_red && b != 0) return;
+  if (b != 0) return;
   const int q0 = qt * BQ, rows = min(BQ, p.Sq - q0);
-  float* base = p.dbias + (long long)b * p.dbias_bstride + ((long long)h * p.Sq + q0) * p.Skv;
-  if (p.dbias_red) {
-    const long long n = (long long)rows * p.Skv;  // contiguous rows
-    for (long long i = threadIdx.x; i < n; i += blockDim.x) base[i] = 0.f;
-    return;
-  }
-  for (int kt = 0; kt < p.n_kt; ++kt) {
-    int lo, hi;
-    visited_query_tiles(kt, Lq, Lk, p.causal, p.bottom_right, p.window_left, p.window_right, lo, hi);
-    if (qt >= lo && qt <= hi) continue;
-    const int k0 = kt * BN, cols = min(BN, p.Skv - k0);
-    for (int i = threadIdx.x; i < rows * BN; i += blockDim.x) {
-      const int r = i / BN, c = i % BN;
-      if (c < cols) base[(long long)r * p.Skv + k0 + c] = 0.f;
-    }
-  }
+  float* base = p.dbias + ((long long)h * p.Sq + q0) * p.Skv;
+  const long long n = (long long)rows * p.Skv;  // contiguous rows
+  long long i0 = 0;
+  while (i0 < n && ((reinterpret_cast<uintptr_t>(base + i0) & 15u) != 0)) ++i0;  // scalar head
+  if ((long long)threadIdx.x < i0) base[threadIdx.x] = 0.f;
+  const long long n4 = (n - i0) / 4;
+  float4* v = reinterpret_cast<float4*>(base + i0);
+  for (long long i = threadIdx.x; i < n4; i += blockDim.x) v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (long long i = i0 + 4 * n4 + threadIdx.x; i < n; i += blockDim.x) base[i] = 0.f;  // tail
 }
 
 // ---------------------------------------------------------------- preprocess
@@ -131,7 +124,7 @@ __global__ void __launch_bounds__(256) sdpa_bwd_preprocess(const ChainParams p) 
       }
       __syncthreads();
     }
-    if (p.dbias) zero_unvisited_dbias(p, bh, qt, Lq, Lk);
+    if (p.dbias_red) zero_shared_dbias_rows(p, bh, qt);
     // dQ-reduction route: clear this tile's accumulator rows below Lq (the
     // convert kernel writes zeros for rows at or past Lq without reading them).
     if (p.dq_accum) {

@@ -22,9 +22,13 @@
 // LSE*log2e), and dS' = P^T * (dP^T - delta) is also written out in fp32 as
 // dBias. A thread owns one key, so a warp's 32 keys of one query row are 32
 // consecutive elements of a bias or dBias row: each load and store of a tile
-// column is one coalesced 64- or 128-byte access. The bias of a query tile is
-// requested before the thread waits for its S^T, and the lines of the
-// warpgroup's next tile are prefetched into L2 one tile ahead.
+// column is one coalesced 64- or 128-byte access. A warpgroup requests the
+// bias of its next tile as soon as it has formed dS of the current one (the
+// registers are free then), so the loads are in flight while it waits for the
+// next S^T, and the tile after that is prefetched into L2. dBias tiles that no
+// CTA visits get their zeros from an otherwise idle warp of the CTA that owns
+// their key tile (per-batch dBias), or from the preprocess kernel (one shared
+// dBias, which the batch rows add into atomically).
 //
 // Schedule. Two query tiles are in flight: tensor memory holds two slots, each
 // with S^T and dP^T (dQ^T reuses the dP^T columns once dS is formed). Compute
@@ -152,6 +156,38 @@ __device__ __forceinline__ void load_bias_column(const ChainParams& p, long long
   }
 }
 
+// Zeros `rows` rows of `cols` floats, `ld` floats apart, with threads
+// thr = 0 .. nthr-1 (nthr a multiple of 32). A full 128-column block row is 32
+// 16-byte stores, one per lane of a warp; other shapes take scalar stores.
+__device__ __forceinline__ void zero_float_rows(float* base, int rows, int cols, long long ld, int thr,
+                                                int nthr) {
+  if (cols == BN && (reinterpret_cast<uintptr_t>(base) & 15u) == 0 && (ld & 3) == 0) {
+    const int rstep = nthr >> 5, c = (thr & 31) * 4;
+    for (int r = thr >> 5; r < rows; r += rstep)
+      *reinterpret_cast<float4*>(base + (long long)r * ld + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+  } else {
+    for (int r = 0; r < rows; ++r)
+      for (int c = thr; c < cols; c += nthr) base[(long long)r * ld + c] = 0.f;
+  }
+}
+
+// Per-batch dBias: zeros of the (query tile, key tile kt) blocks of query heads
+// bh0 .. bh0 + gsz - 1 whose query tile lies outside [qt_lo, qt_hi], i.e. the
+// blocks of this key tile that no CTA computes.
+__device__ inline void zero_unvisited_dbias_blocks(const ChainParams& p, int b, int bh0, int gsz, int kt,
+                                                   int qt_lo, int qt_hi, int thr, int nthr) {
+  const int k0 = kt * BN, cols = min(BN, p.Skv - k0);
+  for (int hj = 0; hj < gsz; ++hj) {
+    const int hq = bh0 + hj - b * p.Hq;
+    for (int qt = 0; qt < p.n_qt; ++qt) {
+      if (qt >= qt_lo && qt <= qt_hi) continue;
+      const int q0 = qt * BQ;
+      zero_float_rows(p.dbias + (long long)b * p.dbias_bstride + ((long long)hq * p.Sq + q0) * p.Skv + k0,
+                      min(BQ, p.Sq - q0), cols, p.Skv, thr, nthr);
+    }
+  }
+}
+
 // L2 prefetch of one BQ x BN bias tile (rows q0.., keys k0..) by 128 threads:
 // each takes one (bf16) or two (fp32) of its 128-byte lines.
 __device__ __forceinline__ void prefetch_bias_tile(const ChainParams& p, long long tile_off, int q0,
@@ -196,6 +232,11 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
     if (hi0 < lo0) {
       if (!row_has_visible_pair(Lq0, Lk0))
         zero_key_tile_rows<D, D>(p, p.dk_ws ? (long long)gi0 : (long long)(gi0 / p.n_part), kt0 * BN);
+      if (BIAS && p.dbias != nullptr && !p.dbias_red) {
+        const int hk0 = (gi0 / p.n_part) % p.Hkv;
+        zero_unvisited_dbias_blocks(p, b0, b0 * p.Hq + hk0 * p.G + (gi0 % p.n_part) * p.gsz, p.gsz, kt0,
+                                    lo0, hi0, threadIdx.x, blockDim.x);
+      }
       return;
     }
   }
@@ -413,8 +454,11 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
         __syncwarp();
       }
     } else if (!DS_OUT && warp == 15) {
-      // Idle on this route: this CTA's share of the group's empty key tiles.
+      // Idle on this route: this CTA's share of the group's empty key tiles,
+      // and the dBias blocks of its key tile that no CTA computes.
       if (!p.deterministic) zero_group_share_of_empty_key_tiles<D, D>(p, out_head, kt, Lq, Lk, lane);
+      if (BIAS && p.dbias != nullptr && !p.dbias_red)
+        zero_unvisited_dbias_blocks(p, b, bh0, p.gsz, kt, qt_lo, qt_hi, lane, 32);
     } else if (DS_OUT && warp == 15) {
       // ------------------------------------------------------------ dS^T store
       // Two-kernel route: once a tile's dS^T is in shared memory, one thread
@@ -442,6 +486,9 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
     // group's empty key tiles.
     if (DS_OUT && warp == 9 && !p.deterministic)
       zero_group_share_of_empty_key_tiles<D, D>(p, out_head, kt, Lq, Lk, lane);
+    // ... and the dBias blocks of this key tile that no CTA computes.
+    if (BIAS && DS_OUT && p.dbias != nullptr && !p.dbias_red)
+      zero_unvisited_dbias_blocks(p, b, bh0, p.gsz, kt, qt_lo, qt_hi, threadIdx.x - 256, 128);
     pdl_wait_prior_grid();
     const int quarter = warp & 3;
     const int d = quarter * 32 + lane;                 // dQ^T lane = head-dim column
@@ -561,6 +608,21 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
     constexpr float LOG2E_F = 1.4426950408889634f;
     const bool key_in = k < p.Skv;
 
+    // Bias (BIAS): element offset of (head, first query, this key) of tile t
+    // inside one batch, and that tile's column of this thread's key.
+    auto bias_tile_off = [&](int tt) -> long long {
+      const int hq = bh0 + tt / n1 - b * p.Hq;
+      return ((long long)hq * p.Sq + (qt_hi - tt % n1) * BQ) * p.Skv + k;
+    };
+    float bz[BIAS ? BQ : 1];
+    if constexpr (BIAS) {
+      if (slot < n)
+        load_bias_column(p, (long long)b * p.bias_bstride + bias_tile_off(slot), key_in,
+                         (qt_hi - slot % n1) * BQ, bz);
+      else
+        for (int i = 0; i < BQ; ++i) bz[i] = 0.f;
+    }
+
     for (int t = slot; t < n && ok; t += 2) {
       const int j = t >> 1, st = t % NSTAGE;
       const int qt = qt_hi - (t % n1), q0 = qt * BQ;
@@ -568,20 +630,7 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
       const bool need_mask = (k0 + BN > Lk) ||
                              (p.causal && (long long)q0 < (long long)(k0 + BN - 1) - diag - Rp) ||
                              (has_window && (long long)(q0 + BQ - 1) > (long long)k0 - diag + p.window_left);
-      // Bias of this tile (this thread's key, the tile's BQ queries), requested
-      // before the waits; the next tile of this warpgroup is prefetched.
-      float bz[BIAS ? BQ : 1];
-      long long bias_off = 0;  // element offset of (head, q0, k) inside one batch
-      if constexpr (BIAS) {
-        const int hq = bh0 + t / n1 - b * p.Hq;
-        bias_off = ((long long)hq * p.Sq + q0) * p.Skv + k;
-        load_bias_column(p, (long long)b * p.bias_bstride + bias_off, key_in, q0, bz);
-        if (t + 2 < n) {
-          const int t2 = t + 2, hq2 = bh0 + t2 / n1 - b * p.Hq, q02 = (qt_hi - t2 % n1) * BQ;
-          prefetch_bias_tile(p, (long long)b * p.bias_bstride + ((long long)hq2 * p.Sq + q02) * p.Skv + k0,
-                             q02, k0, row);
-        }
-      }
+      const long long bias_off = BIAS ? bias_tile_off(t) : 0;
 
       // ---- softmax replay: P^T from S^T. The row statistics were written by
       // TMA, so this thread waits on the stage's transaction barrier itself.
@@ -690,6 +739,19 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bars[BAR_DSREADY + slot]);
+      if constexpr (BIAS) {
+        // The next tile's bias column now (its loads overlap the wait for its
+        // S^T), and the tile after it into L2.
+        // (Unconditional, zeros past the last tile, so that the old values are
+        // dead here rather than carried through this tile's dS step.)
+        const int tn = t + 2 < n ? t + 2 : t;
+        load_bias_column(p, (long long)b * p.bias_bstride + bias_tile_off(tn), key_in && t + 2 < n,
+                         (qt_hi - tn % n1) * BQ, bz);
+        if (t + 4 < n) {
+          const int t4 = t + 4, q04 = (qt_hi - t4 % n1) * BQ;
+          prefetch_bias_tile(p, (long long)b * p.bias_bstride + bias_tile_off(t4) - k + k0, q04, k0, row);
+        }
+      }
     }
 
     // ---- epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK. Each

@@ -4,9 +4,12 @@
 // Backward (SM120)", API Usage: `o` and the natural-log `stats`; the masks of
 // "Causal, sliding-window, and padding masks"; GQA/MQA head mapping; the sink
 // token of the Capabilities list, which joins every row's softmax denominator
-// without a value row):
-//   S = scale Q K^T (masked entries removed), LSE = log(sum_k exp(S) [+ exp(sink)]),
-//   O = sum_k exp(S - LSE) V.
+// without a value row; and the additive bias of the same list, added to the
+// scaled scores):
+//   S = scale Q K^T [+ bias] (masked entries removed),
+//   LSE = log(sum_k exp(S) [+ exp(sink)]),   O = sum_k exp(S - LSE) V.
+// With a bias each softmax thread loads its row's 64 bias values of a tile
+// (16-byte loads along the keys) before it waits for that tile's S.
 // A row with no visible key and no sink gets LSE = -inf and O = 0; with a sink
 // LSE = sink and O = 0.
 //
@@ -86,7 +89,56 @@ struct Layout {
 
 }  // namespace fwd_kernel
 
-template <int DQK, int DV>
+// This row's bias for keys kb .. kb + 63 as 32-bit words: on the 16-byte path
+// bf16 pairs (`packed`, 32 words) or fp32 values (64 words); otherwise fp32
+// values from scalar loads, 0 past S_kv.
+__device__ __forceinline__ void load_fwd_bias_row(const FwdParams& p, long long row_off, int kb, bool live,
+                                                  uint32_t (&raw)[64], bool& packed) {
+  const bool vec = p.bias_vec && kb + 64 <= p.Skv;  // uniform across the warp
+  packed = vec && !p.bias_fp32;
+  if (!live) {
+#pragma unroll
+    for (int i = 0; i < 64; ++i) raw[i] = 0u;
+    return;
+  }
+  if (vec) {
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const char*>(p.bias) +
+                                                      (row_off + kb) * (p.bias_fp32 ? 4 : 2));
+    if (p.bias_fp32) {
+#pragma unroll
+      for (int v = 0; v < 16; ++v) {
+        const uint4 x = __ldcs(src + v);
+        raw[4 * v] = x.x; raw[4 * v + 1] = x.y; raw[4 * v + 2] = x.z; raw[4 * v + 3] = x.w;
+      }
+    } else {
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const uint4 x = __ldcs(src + v);
+        raw[4 * v] = x.x; raw[4 * v + 1] = x.y; raw[4 * v + 2] = x.z; raw[4 * v + 3] = x.w;
+      }
+#pragma unroll
+      for (int i = 32; i < 64; ++i) raw[i] = 0u;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+      float x = 0.f;
+      if (kb + i < p.Skv)
+        x = p.bias_fp32 ? __ldcs(static_cast<const float*>(p.bias) + row_off + kb + i)
+                        : __uint_as_float((uint32_t)__ldcs(static_cast<const unsigned short*>(p.bias) +
+                                                           row_off + kb + i) << 16);
+      raw[i] = __float_as_uint(x);
+    }
+  }
+}
+
+__device__ __forceinline__ float fwd_bias_at(const uint32_t (&raw)[64], bool packed, int i) {
+  return packed ? __uint_as_float((i & 1) ? (raw[i >> 1] & 0xFFFF0000u) : (raw[i >> 1] << 16))
+                : __uint_as_float(raw[i]);
+}
+
+// BIAS adds the additive bias (FwdParams::bias) to the scaled scores.
+template <int DQK, int DV, bool BIAS>
 __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
     sdpa_fwd_kernel(const __grid_constant__ FwdMaps maps, const FwdParams p) {
   using namespace fwd_kernel;
@@ -248,9 +300,16 @@ __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
     const long long k_vis_hi = p.causal ? (long long)q + diag + Rp : (1ll << 40);
     const long long k_vis_lo = has_window ? (long long)q + diag - p.window_left : -(1ll << 40);
     const int i0 = half * 64;  // this half's first key within a tile
+    // With a bias the scores are rewritten in place as x = s * c + bias * log2e,
+    // and everything below reads them with the factor cs = 1 instead of c.
+    const float cs = BIAS ? 1.f : c;
+    const long long bias_row = BIAS ? (long long)b * p.bias_bstride + ((long long)h * p.Sq + q) * p.Skv : 0;
     for (int j = 0; j < n && ok; ++j) {
       const int s = j % NSLOT;
       const int k0 = (kt_lo + j) * BK;
+      uint32_t braw[BIAS ? 64 : 1];
+      bool bpacked = false;
+      if constexpr (BIAS) load_fwd_bias_row(p, bias_row, k0 + i0, live, braw, bpacked);
       if (!mbar_wait(&bars[BAR_SFULL + s], (j / NSLOT) & 1, abort_flag, WAIT_LIMIT_NS)) { ok = false; break; }
       __syncwarp();
       tc_fence_after();
@@ -259,6 +318,13 @@ __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
       tmem_ld32(t_lane + 128u * s + i0 + 32, sr[1]);
       tmem_ld_wait(sr[0]);
       tmem_ld_wait(sr[1]);
+      if constexpr (BIAS) {
+        constexpr float LOG2E_F = 1.4426950408889634f;
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+          sr[i >> 5][i & 31] = __float_as_uint(
+              fmaf(__uint_as_float(sr[i >> 5][i & 31]), c, fwd_bias_at(braw, bpacked, i) * LOG2E_F));
+      }
       // Visible keys of this row within the tile: [v_lo, v_hi] relative to k0.
       int v_lo = 0, v_hi = BK - 1;
       if (!live) {
@@ -284,7 +350,7 @@ __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
           if (i0 + i >= v_lo && i0 + i <= v_hi) mp[i & 7] = fmaxf(mp[i & 7], __uint_as_float(sr[i >> 5][i & 31]));
       }
       const float mt = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * c;  // c > 0
+                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * cs;  // cs > 0
       // Raise the reference when the tile's maximum exceeds it by more than the
       // threshold (or when it is the row's first visible key).
       const bool raise = mt > m + RESCALE_THRESHOLD || (m == -INFINITY && mt > -INFINITY);
@@ -328,15 +394,17 @@ __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
       float rs[8];
 #pragma unroll
       for (int a = 0; a < 8; ++a) rs[a] = 0.f;
-      const float neg_m = -m;
+      // (m stays -inf only if every visible score so far is -inf, which only a
+      // bias can make; P is 0 then, and exp2(-inf + 0) gives it without a NaN.)
+      const float neg_m = m == -INFINITY ? 0.f : -m;
 #pragma unroll
       for (int c16 = 0; c16 < 2; ++c16) {
         uint32_t w[16];
         if (full) {
 #pragma unroll
           for (int i2 = 0; i2 < 16; ++i2) {
-            const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c16][2 * i2]), c, neg_m));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c16][2 * i2 + 1]), c, neg_m));
+            const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c16][2 * i2]), cs, neg_m));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c16][2 * i2 + 1]), cs, neg_m));
             rs[(2 * i2) & 7] += p0;
             rs[(2 * i2 + 1) & 7] += p1;
             w[i2] = pack_bf16x2(p0, p1);
@@ -346,9 +414,9 @@ __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
           for (int i2 = 0; i2 < 16; ++i2) {
             const int i = i0 + c16 * 32 + 2 * i2;
             const float p0 = (i >= v_lo && i <= v_hi)
-                                 ? ex2_approx(fmaf(__uint_as_float(sr[c16][2 * i2]), c, neg_m)) : 0.f;
+                                 ? ex2_approx(fmaf(__uint_as_float(sr[c16][2 * i2]), cs, neg_m)) : 0.f;
             const float p1 = (i + 1 >= v_lo && i + 1 <= v_hi)
-                                 ? ex2_approx(fmaf(__uint_as_float(sr[c16][2 * i2 + 1]), c, neg_m)) : 0.f;
+                                 ? ex2_approx(fmaf(__uint_as_float(sr[c16][2 * i2 + 1]), cs, neg_m)) : 0.f;
             rs[(2 * i2) & 7] += p0;
             rs[(2 * i2 + 1) & 7] += p1;
             w[i2] = pack_bf16x2(p0, p1);
@@ -439,32 +507,44 @@ __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
   }
 }
 
-template <int DQK, int DV>
+template <int DQK, int DV, bool BIAS>
 static cudaError_t set_fwd_smem() {
-  return cudaFuncSetAttribute(sdpa_fwd_kernel<DQK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(sdpa_fwd_kernel<DQK, DV, BIAS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               fwd_kernel::Layout<DQK, DV>::BYTES);
 }
 
-cudaError_t fwd_kernel_setup() {
-  cudaError_t e = set_fwd_smem<64, 64>();
-  if (e == cudaSuccess) e = set_fwd_smem<128, 128>();
-  if (e == cudaSuccess) e = set_fwd_smem<192, 128>();
+template <bool BIAS>
+static cudaError_t fwd_setup_variant() {
+  cudaError_t e = set_fwd_smem<64, 64, BIAS>();
+  if (e == cudaSuccess) e = set_fwd_smem<128, 128, BIAS>();
+  if (e == cudaSuccess) e = set_fwd_smem<192, 128, BIAS>();
   return e;
 }
 
-cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, cudaStream_t s) {
+cudaError_t fwd_kernel_setup() {
+  cudaError_t e = fwd_setup_variant<false>();
+  if (e == cudaSuccess) e = fwd_setup_variant<true>();
+  return e;
+}
+
+template <bool BIAS>
+static cudaError_t launch_fwd_variant(const FwdMaps& maps, const FwdParams& p, cudaStream_t s) {
   const dim3 grid((unsigned)(p.n_qt * p.B * p.Hq));
   const dim3 block(fwd_kernel::THREADS);
   if (p.Dqk == 64 && p.Dv == 64)
-    return launch_kernel(sdpa_fwd_kernel<64, 64>, grid, block, fwd_kernel::Layout<64, 64>::BYTES, s,
-                         false, maps, p);
+    return launch_kernel(sdpa_fwd_kernel<64, 64, BIAS>, grid, block, fwd_kernel::Layout<64, 64>::BYTES,
+                         s, false, maps, p);
   if (p.Dqk == 128 && p.Dv == 128)
-    return launch_kernel(sdpa_fwd_kernel<128, 128>, grid, block, fwd_kernel::Layout<128, 128>::BYTES,
-                         s, false, maps, p);
+    return launch_kernel(sdpa_fwd_kernel<128, 128, BIAS>, grid, block,
+                         fwd_kernel::Layout<128, 128>::BYTES, s, false, maps, p);
   if (p.Dqk == 192 && p.Dv == 128)
-    return launch_kernel(sdpa_fwd_kernel<192, 128>, grid, block, fwd_kernel::Layout<192, 128>::BYTES,
-                         s, false, maps, p);
+    return launch_kernel(sdpa_fwd_kernel<192, 128, BIAS>, grid, block,
+                         fwd_kernel::Layout<192, 128>::BYTES, s, false, maps, p);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, cudaStream_t s) {
+  return p.bias ? launch_fwd_variant<true>(maps, p, s) : launch_fwd_variant<false>(maps, p, s);
 }
 
 }  // namespace sdpa

@@ -90,6 +90,20 @@ def main_kernel_flops_per_pair(w: workloads.Workload) -> int:
     return flops_per_pair(w)
 
 
+def main_kernel_bytes_bias(w: workloads.Workload, pairs: int, bias) -> int:
+    """Algorithmic DRAM bytes of one biased main-kernel launch: the bias at the
+    visible pairs (its element size each), every fp32 dBias element written once,
+    and each Q, K, V, dO, dK, dV element moved once with the fp32 dQ accumulator
+    read and written once (the reduction route; the stored-dS route moves bf16 dS
+    instead, counted the same here)."""
+    esz = bias.element_size()
+    dbias = bias.numel() * 4
+    qdo = 2 * w.B * w.Hq * w.Sq * w.Dqk * 2
+    kv = w.B * w.Hkv * w.Skv * (w.Dqk + w.Dv) * 2
+    dq_acc = 2 * w.B * w.Hq * w.Sq * w.Dqk * 4
+    return pairs * esz + dbias + qdo + 2 * kv + dq_acc
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons while the GPU works."""
@@ -195,11 +209,14 @@ def _problem(w, lens):
 
 
 def oracle_forward_inputs(w, t):
-    """O (bf16) and LSE (fp32) of the workload from the fp64 oracle forward."""
+    """O (bf16) and LSE (fp32) of the workload from the fp64 oracle forward (with
+    the additive bias t["bias"] when there is one)."""
     import oracle
     p = _problem(w, t["seq_q_lens"])
+    bias = t.get("bias")
     o64, lse64 = oracle.forward(p, t["q"].double().numpy(), t["k"].double().numpy(),
-                                t["v"].double().numpy())
+                                t["v"].double().numpy(),
+                                bias=None if bias is None else bias.double().numpy())
     return torch.from_numpy(o64).to(torch.bfloat16), torch.from_numpy(lse64).float()
 
 
@@ -221,8 +238,14 @@ def oracle_backward_sample(w, t, o, lse, groups):
     p = _problem(ws, t["seq_q_lens"])
     args = [sl["q"].double().numpy(), sl["k"].double().numpy(), sl["v"].double().numpy(),
             os_.double().numpy(), sl["do"].double().numpy(), ls.double().numpy()]
+    bias = t.get("bias")
     t0 = time.perf_counter()
-    oracle.backward(p, *args)
+    if bias is None:
+        oracle.backward(p, *args)
+    else:  # the biased backward plus dBias, on the sample's heads
+        b64 = bias[:, :hq].contiguous().double().numpy()
+        oracle.backward(p, *args, bias=b64)
+        oracle.dbias(p, *args, b64)
     dt = time.perf_counter() - t0
     return dt, visible_pairs(ws, t["seq_q_lens"]) * flops_per_pair(ws)
 
@@ -349,7 +372,7 @@ def cpu_baseline_leg(w, t, target_s=12.0):
 # valid only for the kernel sources they were taken on: the digest covers the
 # kernel's source files, and a changed kernel reports null. D_qk = 192 runs
 # sdpa_bwd_main_ds, every other head dim sdpa_bwd_main.
-MAIN_SOURCES = {"sdpa_bwd_main": ("sdpa_bwd_main.cu", "common.cuh", "ptx.cuh"),
+MAIN_SOURCES = {"sdpa_bwd_main": ("sdpa_bwd_main.cuh", "common.cuh", "ptx.cuh"),
                 "sdpa_bwd_main_ds": ("sdpa_bwd_main_ds.cu", "common.cuh", "ptx.cuh")}
 MAIN_TRAFFIC = {
     "fa34d64d4753c107": {"causal_mha": 114246144 + 31919360,
@@ -363,10 +386,20 @@ def main_kernel_name(w) -> str:
     return "sdpa_bwd_main_ds" if w.Dqk == 192 else "sdpa_bwd_main"
 
 
-def main_traffic(w):
+def main_traffic(w, tag=None):
     csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "attention_backward_sdpa_gb300", "csrc")
     blob = b"".join(open(os.path.join(csrc, f), "rb").read() for f in MAIN_SOURCES[main_kernel_name(w)])
-    return MAIN_TRAFFIC.get(hashlib.sha256(blob).hexdigest()[:16], {}).get(w.name)
+    key = w.name if tag is None else f"{w.name}/{tag}"
+    return MAIN_TRAFFIC.get(hashlib.sha256(blob).hexdigest()[:16], {}).get(key)
+
+
+def bias_tag(t):
+    """'bias-<batch>-<dtype>' for a biased run (the traffic table's key suffix), else None."""
+    b = t.get("bias")
+    if b is None:
+        return None
+    return f"bias-{'shared' if b.shape[0] == 1 and t['q'].shape[0] > 1 else 'B'}-" \
+           f"{'f32' if b.dtype == torch.float32 else 'bf16'}"
 
 
 def peaks():
@@ -398,9 +431,17 @@ def run_gpu(args, w, t, o, lse, rank, world, device):
     if args.sink:  # sink tokens: the same chain plus the dsink partials and reduce
         kw["sink"] = workloads.sink_logits(w).to(device)
         kw["dsink"] = torch.empty_like(kw["sink"])
+    outs = [dq, dk, dv]
+    if "bias" in t:  # additive bias: read by the main kernel, dBias written by it
+        d["bias"] = t["bias"].to(device)
+        kw["dbias"] = torch.empty(tuple(t["bias"].shape), dtype=torch.float32, device=device)
+        outs.append(kw["dbias"])
+
+    def call_kw():
+        return dict(kw, bias=d["bias"]) if "bias" in d else kw
 
     def step():
-        pkg.sdpa_bwd(d["q"], d["k"], d["v"], d["o"], d["do"], d["lse"], **kw)
+        pkg.sdpa_bwd(d["q"], d["k"], d["v"], d["o"], d["do"], d["lse"], **call_kw())
 
     def timed_loop(n, profile=False):
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
@@ -438,7 +479,7 @@ def run_gpu(args, w, t, o, lse, rank, world, device):
         # End to end through the public API with host buffers: pinned host -> device
         # copies of the inputs and a device -> host read of dQ/dK/dV every step.
         host_in = {k: v.cpu().pin_memory() for k, v in d.items()}
-        host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (dq, dk, dv)]
+        host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in outs]
         h2d = sum(x.numel() * x.element_size() for x in host_in.values())
         d2h = sum(x.numel() * x.element_size() for x in host_out)
         e2e_steps = max(3, min(args.steps, 50))
@@ -448,7 +489,7 @@ def run_gpu(args, w, t, o, lse, rank, world, device):
             for k, v in host_in.items():
                 d[k].copy_(v, non_blocking=True)
             step()
-            for h, x in zip(host_out, (dq, dk, dv)):
+            for h, x in zip(host_out, outs):
                 h.copy_(x, non_blocking=True)
             torch.cuda.synchronize(device)
         e2e_s = (time.perf_counter() - t0) / e2e_steps
@@ -460,12 +501,23 @@ def run_gpu(args, w, t, o, lse, rank, world, device):
     achieved = main_flops / (main_ms * 1e-3) / 1e12
     value = world * flops / (ms_step * 1e-3) / 1e12
     kernel_ms = {k: round(v[0] / max(v[1], 1), 5) for k, v in prof.items() if v[1]}
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+            "frac": achieved / peak_tf, "traffic": main_traffic(w, bias_tag(t)),
+            "kernel": main_kernel_name(w), "peak_kind": f"{peak_kind} bf16 burst",
+            "kernel_gflop": main_flops / 1e9}
+    if "bias" in t:
+        # With a bias the main kernel streams the bias and the fp32 dBias: it is
+        # bound by HBM, against the measured copy bandwidth.
+        nbytes = main_kernel_bytes_bias(w, pairs, t["bias"])
+        gbs = nbytes / (main_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": gbs, "peak": peak_hbm, "unit": "GB/s",
+                "frac": gbs / peak_hbm, "traffic": main_traffic(w, bias_tag(t)),
+                "kernel": main_kernel_name(w), "peak_kind": f"{peak_kind} HBM copy",
+                "algorithmic_bytes": nbytes, "tensor_tflops": achieved,
+                "tensor_frac": achieved / peak_tf}
     return {
         "value": value, "ms_per_step": ms_step, "flops": flops,
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": achieved / peak_tf, "traffic": main_traffic(w),
-                     "kernel": main_kernel_name(w), "peak_kind": f"{peak_kind} bf16 burst",
-                     "kernel_gflop": main_flops / 1e9},
+        "roofline": roof,
         "kernel_ms": kernel_ms,
         "e2e": {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -514,11 +566,17 @@ def main(argv=None):
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--sink", action="store_true",
                     help="time sdpa_bwd_sink (sink-token logits, dsink output) instead of sdpa_bwd")
+    ap.add_argument("--bias", default="none", choices=["none", "B", "1"],
+                    help="time sdpa_bwd_bias with an additive bias of B batches or 1 shared batch "
+                         "(dBias written in fp32)")
+    ap.add_argument("--bias-dtype", default="bf16", choices=["bf16", "f32"])
     ap.add_argument("--pass", dest="pass_", default="bwd", choices=["bwd", "fwd"],
                     help="bwd: the backward chain (default); fwd: sdpa_fwd, the forward (O, LSE)")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip timing the oracle backward (O/LSE still come from the oracle forward)")
     args = ap.parse_args(argv)
+    if args.bias != "none" and args.pass_ == "fwd":
+        ap.error("--bias times the backward (sdpa_bwd_bias); the forward takes no bias")
     args.warmup = max(args.warmup, 3)
     args.steps = max(args.steps, 1)
     rank, world, local = init_dist()
@@ -529,6 +587,9 @@ def main(argv=None):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     t = workloads.generate(w)
+    if args.bias != "none":
+        t["bias"] = workloads.bias_tensor(w, 1 if args.bias == "1" else w.B,
+                                          torch.float32 if args.bias_dtype == "f32" else torch.bfloat16)
     if args.pass_ == "fwd":
         cb = cpu_baseline_fwd(w, t) if (rank == 0 and not args.no_cpu_baseline) else None
         r = run_gpu_fwd(args, w, t, rank, world, device)
@@ -571,6 +632,8 @@ def result_line(args, w, world, r, cb, metric):
                        "bottom_right": w.bottom_right, "window_left": w.window_left,
                        "deterministic": w.deterministic, "seed": w.seed,
                        "pass": args.pass_, "sink": bool(args.sink),
+                       "bias": None if args.bias == "none" else
+                       {"batch": args.bias, "dtype": args.bias_dtype, "dbias": "f32"},
                        "gflop_per_step": r["flops"] / 1e9,
                        "l2": "256 MiB buffer written between timed steps",
                        "parallelism": f"replicas{world}" if world > 1 else "single"},

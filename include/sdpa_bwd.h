@@ -195,6 +195,29 @@ int sdpa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
              int bottom_right, int window_left, int window_right, const int32_t* seq_q_lens,
              const int32_t* seq_kv_lens, const float* sink, void* stream);
 
+/*
+ * SDPA forward with an additive bias (cuDNN frontend docs, "SDPA Backward
+ * (SM120)": the bias capability): as sdpa_fwd() with the scores
+ *     S = scale * Q K^T + bias      (before the masks and the softmax),
+ * so that O and LSE are the inputs sdpa_bwd_bias() takes with the same bias.
+ * A visible key whose bias is -inf contributes nothing; a row whose visible
+ * keys all have a -inf bias gets O = 0 and LSE = -inf (or the sink).
+ * Arguments: those of sdpa_fwd(), then
+ *   bias        device (bias_batch, H_q, S_q, S_kv) tensor, contiguous, S_kv
+ *               innermost; bf16 (2-byte aligned) or fp32 (4-byte aligned).
+ *               Rows are read with 16-byte loads when S_kv times the element
+ *               size is a multiple of 16 and bias is 16-byte aligned.
+ *   bias_dtype  SDPA_DTYPE_BF16 or SDPA_DTYPE_F32.
+ *   bias_batch  1 (one bias for every batch row) or B.
+ * Returns SDPA_ERR_INVALID for a NULL bias, an unknown dtype or bias_batch
+ * not 1 or B; otherwise as sdpa_fwd().
+ */
+int sdpa_fwd_bias(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
+                  int H_kv, int S_q, int S_kv, int D_qk, int D_v, float scale, int causal,
+                  int bottom_right, int window_left, int window_right, const int32_t* seq_q_lens,
+                  const int32_t* seq_kv_lens, const float* sink, const void* bias, int bias_dtype,
+                  int bias_batch, void* stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* sdpa_status_string(int status);
 

@@ -200,3 +200,18 @@ def test_bias_argument_validation(lib):
     assert call_bias(lib, FAKE + 2, dtype=1) == ALIGN         # fp32 bias: 4-byte alignment
     assert call_bias(lib, FAKE, dbias=FAKE + 2) == ALIGN      # fp32 dBias: 4-byte alignment
     assert call_bias(lib, FAKE, Dqk=192, Dv=128) == UNSUPPORTED
+
+
+def test_forward_bias_argument_validation(lib):
+    lib.sdpa_fwd_bias.restype = ctypes.c_int
+    vp = [ctypes.c_void_p(FAKE)] * 5
+
+    def call(bias, dtype=0, batch=1, B=1):
+        return lib.sdpa_fwd_bias(*vp, B, 2, 2, 128, 128, 128, 128, ctypes.c_float(0.0), 0, 0, -1, -1,
+                                 None, None, None, None if bias is None else ctypes.c_void_p(bias),
+                                 dtype, batch, None)
+    assert call(None) == INVALID
+    assert call(FAKE, dtype=5) == INVALID
+    assert call(FAKE, batch=2, B=3) == INVALID
+    assert call(FAKE + 1, dtype=0) == ALIGN
+    assert call(FAKE + 2, dtype=1) == ALIGN

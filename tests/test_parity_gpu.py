@@ -324,7 +324,7 @@ def _gpu_fwd(case, d):
     o, lse = pkg.sdpa_fwd(d["q"], d["k"], d["v"], scale=w.resolved_scale, causal=w.causal,
                           bottom_right=w.bottom_right, window_left=w.window_left,
                           window_right=w.window_right, seq_q_lens=d["seq_q_lens"],
-                          seq_kv_lens=d["seq_kv_lens"], sink=d.get("sink"),
+                          seq_kv_lens=d["seq_kv_lens"], sink=d.get("sink"), bias=d.get("bias"),
                           o=torch.full((w.B, w.Hq, w.Sq, w.Dv), float("nan"), dtype=torch.bfloat16,
                                        device="cuda"),
                           lse=torch.full((w.B, w.Hq, w.Sq), float("nan"), device="cuda"))
@@ -507,3 +507,63 @@ def test_bias_full_size_sampled(name):
     gb = dbias.reshape(-1, w.Skv)[torch.from_numpy(rows).cuda()].double().cpu().numpy()
     assert_close("dbias", gb, rb)
     assert torch.isfinite(dbias).all()
+
+
+# Forward with a bias: O and LSE of the biased scores against the oracle forward
+# with the same bias (16-byte bias rows and ragged ones, per-batch and shared,
+# bf16 and fp32, every head-dim pair).
+FWD_BIAS_CASES = {
+    "d128_causal_ragged_B_bf16": (SMALL["d128_causal_ragged"], "B", torch.bfloat16),  # S_kv 300
+    "d128_dense_ragged_shared_f32": (SMALL["d128_dense_ragged"], "1", torch.float32),
+    "gqa_B_f32": (SMALL["gqa"], "B", torch.float32),
+    "padded_window_shared_bf16": (SMALL["padded_window"], "1", torch.bfloat16),
+    "tl_causal_long_q_d64_B_f32": (SMALL["tl_causal_long_q"], "B", torch.float32),   # S_kv 200
+    "window_only_B_bf16": (SMALL["window_only"], "B", torch.bfloat16),               # S_kv 280
+    "mla_gqa_window_B_bf16": (SMALL["mla_gqa_window"], "B", torch.bfloat16),
+    "single_query_B_f32": (SMALL["single_query"], "B", torch.float32),
+}
+
+
+@pytest.mark.parametrize("name", sorted(FWD_BIAS_CASES))
+def test_forward_bias_parity(name):
+    case = _bias_case(*FWD_BIAS_CASES[name])
+    d = to_device(case)
+    o, lse = _gpu_fwd(case, d)
+    _check_fwd(case, o, lse)
+
+
+def test_forward_bias_minus_infinity_rows():
+    """A bias of -inf on every key of some rows empties them (O = 0, LSE = -inf);
+    -inf on some keys removes just those."""
+    w = SMALL["d128_causal_ragged"]
+    bias = workloads.bias_tensor(w, 1, torch.float32)
+    bias[0, 0, 5:9, :] = float("-inf")       # whole rows
+    bias[0, 1, :, 7::3] = float("-inf")      # a comb of keys
+    case = make_case(w, bias=(1, torch.float32))
+    case["bias"] = bias
+    import oracle
+    from harness import f64
+    o64, lse64 = oracle.forward(case["problem"], f64(case["q"]), f64(case["k"]), f64(case["v"]),
+                                bias=bias.double().numpy())
+    case["o"] = torch.from_numpy(o64).to(torch.bfloat16)
+    case["lse"] = torch.from_numpy(lse64).float()
+    d = to_device(case)
+    o, lse = _gpu_fwd(case, d)
+    _check_fwd(case, o, lse)
+    assert torch.all(lse[0, 0, 5:9] == float("-inf")) and torch.all(o[0, 0, 5:9] == 0)
+
+
+@pytest.mark.parametrize("name", ["gqa_B_f32", "d128_causal_ragged_B_bf16"])
+def test_forward_then_backward_with_bias(name):
+    """sdpa_fwd_bias then sdpa_bwd_bias on the GPU's own O/LSE match the oracle's
+    forward and backward."""
+    case = _bias_case(*FWD_BIAS_CASES[name])
+    d = to_device(case)
+    o, lse = _gpu_fwd(case, d)
+    d["o"], d["lse"] = o, lse
+    dq, dk, dv, dbias = _gpu_bias(case, d)
+    rq, rk, rv = oracle_backward(case)
+    assert_close("dq", dq.double().cpu().numpy(), rq)
+    assert_close("dk", dk.double().cpu().numpy(), rk)
+    assert_close("dv", dv.double().cpu().numpy(), rv)
+    assert_close("dbias", dbias.double().cpu().numpy(), oracle_dbias(case))
