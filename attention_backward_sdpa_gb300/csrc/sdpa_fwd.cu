@@ -309,7 +309,16 @@ __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
       const int k0 = (kt_lo + j) * BK;
       uint32_t braw[BIAS ? 64 : 1];
       bool bpacked = false;
-      if constexpr (BIAS) load_fwd_bias_row(p, bias_row, k0 + i0, live, braw, bpacked);
+      if constexpr (BIAS) {
+        load_fwd_bias_row(p, bias_row, k0 + i0, live, braw, bpacked);
+        // The row's segment of the tile after next into L2 (one or two lines).
+        const int kp = k0 + 2 * BK + i0;
+        if (live && j + 2 < n && kp < p.Skv) {
+          const char* a = static_cast<const char*>(p.bias) + (bias_row + kp) * (p.bias_fp32 ? 4 : 2);
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+          if (p.bias_fp32 && kp + 32 < p.Skv) asm volatile("prefetch.global.L2 [%0];" ::"l"(a + 128));
+        }
+      }
       if (!mbar_wait(&bars[BAR_SFULL + s], (j / NSLOT) & 1, abort_flag, WAIT_LIMIT_NS)) { ok = false; break; }
       __syncwarp();
       tc_fence_after();

@@ -291,6 +291,9 @@ def run_gpu_fwd(args, w, t, rank, world, device):
     kw = dict(scale=w.resolved_scale, causal=w.causal, bottom_right=w.bottom_right,
               window_left=w.window_left, window_right=w.window_right, seq_q_lens=lq,
               seq_kv_lens=lk, sink=sink, o=o, lse=lse)
+    if "bias" in t:  # sdpa_fwd_bias
+        d["bias"] = t["bias"].to(device)
+        kw["bias"] = d["bias"]
 
     def step():
         pkg.sdpa_fwd(d["q"], d["k"], d["v"], **kw)
@@ -567,16 +570,14 @@ def main(argv=None):
     ap.add_argument("--sink", action="store_true",
                     help="time sdpa_bwd_sink (sink-token logits, dsink output) instead of sdpa_bwd")
     ap.add_argument("--bias", default="none", choices=["none", "B", "1"],
-                    help="time sdpa_bwd_bias with an additive bias of B batches or 1 shared batch "
-                         "(dBias written in fp32)")
+                    help="add a bias of B batches or 1 shared batch: sdpa_bwd_bias (dBias written "
+                         "in fp32), or sdpa_fwd_bias with --pass fwd")
     ap.add_argument("--bias-dtype", default="bf16", choices=["bf16", "f32"])
     ap.add_argument("--pass", dest="pass_", default="bwd", choices=["bwd", "fwd"],
                     help="bwd: the backward chain (default); fwd: sdpa_fwd, the forward (O, LSE)")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip timing the oracle backward (O/LSE still come from the oracle forward)")
     args = ap.parse_args(argv)
-    if args.bias != "none" and args.pass_ == "fwd":
-        ap.error("--bias times the backward (sdpa_bwd_bias); the forward takes no bias")
     args.warmup = max(args.warmup, 3)
     args.steps = max(args.steps, 1)
     rank, world, local = init_dist()
