@@ -114,6 +114,13 @@ def _load():
                                                 ctypes.c_long, I64, P, P]
         lib.oracle_dbias.argtypes = [C, P, P, P, P, P, P, P]
         lib.oracle_dbias_rows.argtypes = [C, P, P, P, P, P, P, ctypes.c_long, I64, P]
+        lib.oracle_round_e4m3.argtypes = [ctypes.c_double]
+        lib.oracle_round_e4m3.restype = ctypes.c_double
+        lib.oracle_round_e2m1.argtypes = [ctypes.c_double]
+        lib.oracle_round_e2m1.restype = ctypes.c_double
+        lib.oracle_fake_nvfp4.argtypes = [P, P, ctypes.c_long, ctypes.c_int]
+        lib.oracle_qat_forward.argtypes = [C, P, P, P, P, P, P]
+        lib.oracle_qat_backward.argtypes = [C, P, P, P, P, P, P, P, P, P]
         lib.oracle_count_visible.argtypes = [C]
         lib.oracle_count_visible.restype = ctypes.c_longlong
         lib.oracle_max_threads.restype = ctypes.c_int
@@ -260,6 +267,61 @@ def dbias_rows(p: Problem, q, k, v, o, do, lse, bias, rows):
     lib.oracle_dbias_rows(ctypes.byref(s), _p(q), _p(k), _p(v), _p(o), _p(do), _p(lse), len(ri),
                           ri.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), _p(out))
     return out
+
+
+def round_e4m3(x: float) -> float:
+    """Nearest E4M3 value (ties to even, saturating at 448)."""
+    return float(_load().oracle_round_e4m3(float(x)))
+
+
+def round_e2m1(x: float) -> float:
+    """Nearest E2M1 value (ties to even, saturating at 6)."""
+    return float(_load().oracle_round_e2m1(float(x)))
+
+
+def fake_nvfp4(x):
+    """NVFP4 fake quantization along the last axis, blocks of 16 values: E4M3
+    local scale amax/6, values rounded to E2M1 multiples of it (float64 out)."""
+    arr = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    out = np.zeros_like(arr)
+    cols = arr.shape[-1] if arr.ndim else 1
+    rows = arr.size // cols if cols else 0
+    _load().oracle_fake_nvfp4(_p(arr), _p(out), rows, cols)
+    return out
+
+
+def qat_forward(p: Problem, q, k, v):
+    """NVFP4 QAT forward: (O_hp, LSE, O_user). O_hp and LSE are the forward of
+    the fake-quantized Q, K, V; O_user = fake_nvfp4(P) V_hat."""
+    _check_heads(p)
+    lib = _load()
+    q = _f64(q, (p.B, p.Hq, p.Sq, p.Dqk))
+    k = _f64(k, (p.B, p.Hkv, p.Skv, p.Dqk))
+    v = _f64(v, (p.B, p.Hkv, p.Skv, p.Dv))
+    o = np.zeros((p.B, p.Hq, p.Sq, p.Dv))
+    lse = np.zeros((p.B, p.Hq, p.Sq))
+    ou = np.zeros_like(o)
+    s, keep = p._struct()
+    lib.oracle_qat_forward(ctypes.byref(s), _p(q), _p(k), _p(v), _p(o), _p(lse), _p(ou))
+    return o, lse, ou
+
+
+def qat_backward(p: Problem, q, k, v, o_hp, do, lse):
+    """NVFP4 QAT backward: (dQ, dK, dV) from the unquantized Q, K, V, the
+    high-precision forward output O_hp and its LSE."""
+    _check_heads(p)
+    lib = _load()
+    q = _f64(q, (p.B, p.Hq, p.Sq, p.Dqk))
+    k = _f64(k, (p.B, p.Hkv, p.Skv, p.Dqk))
+    v = _f64(v, (p.B, p.Hkv, p.Skv, p.Dv))
+    o = _f64(o_hp, (p.B, p.Hq, p.Sq, p.Dv))
+    do = _f64(do, (p.B, p.Hq, p.Sq, p.Dv))
+    lse = _f64(lse, (p.B, p.Hq, p.Sq))
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    s, keep = p._struct()
+    lib.oracle_qat_backward(ctypes.byref(s), _p(q), _p(k), _p(v), _p(o), _p(do), _p(lse),
+                            _p(dq), _p(dk), _p(dv))
+    return dq, dk, dv
 
 
 def count_visible(p: Problem) -> int:

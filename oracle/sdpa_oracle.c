@@ -26,6 +26,8 @@
  *     denominator without a value row, so the forward LSE includes it and
  *     dQ/dK/dV keep their formulas; the extra output is
  *     dsink[h] = -sum_{b,q} exp(sink[h] - LSE[b,h,q]) * delta[b,h,q].
+ *   - NVFP4 QAT backward (page "NVFP4 Attention QAT Backward", Overview): see
+ *     the section of that name at the end of this file.
  *   - Additive bias (Capabilities list): a (1|B, H_q, S_q, S_kv) tensor added
  *     to the scaled scores before the softmax, s_qk = scale * Q_q.K_k +
  *     bias[b,h,q,k]; the forward LSE includes it, so the backward replays P
@@ -366,4 +368,180 @@ void oracle_dbias_rows(const oracle_cfg *c, const double *Q, const double *K, co
 #pragma omp parallel for schedule(dynamic, 1)
     for (long i = 0; i < n; ++i) dbias_row(c, Q, K, V, dO, LSE, delta, rows[i], out + i * c->Skv);
     free(delta);
+}
+
+/* ---- NVFP4 fake quantization and the QAT backward ("NVFP4 Attention QAT
+ * Backward" page, Overview). Q, K and V are fake-quantized in blocks of 16
+ * consecutive values along the head dimension: each block gets a local scale
+ * in E4M3 and its values are rounded to E2M1 multiples of that scale. P = the
+ * softmax of the quantized scores; dQ and dK use P itself (straight-through
+ * estimator) and dV uses P fake-quantized in blocks of 16 consecutive keys of
+ * a query row. The local scale is amax / 6 and each value is divided by the
+ * scale, both as correctly rounded fp32 divisions (the page's "precise
+ * division"), so that the E2M1 rounding sees exact midpoints as midpoints. ---- */
+
+/* |a| rounded to a multiple of `quantum` (a power of two), ties to even. */
+static double round_to_quantum(double a, double quantum) {
+    return nearbyint(a / quantum) * quantum;
+}
+
+/* Nearest E4M3 value: sign, 4 exponent bits (bias 7), 3 mantissa bits; normal
+ * magnitudes 2^-6 .. 448, subnormal steps of 2^-9, no infinities. Ties go to the
+ * even mantissa; magnitudes beyond 448 saturate to 448. */
+double oracle_round_e4m3(double x) {
+    double a = fabs(x), q;
+    if (a >= 448.0) {
+        q = 448.0;
+    } else if (a < 0.015625) {          /* below 2^-6: subnormal grid */
+        q = round_to_quantum(a, 0.001953125);
+    } else {
+        int e;
+        frexp(a, &e);                   /* a = f * 2^e, f in [0.5, 1) */
+        q = round_to_quantum(a, ldexp(1.0, e - 1 - 3));
+        if (q > 448.0) q = 448.0;
+    }
+    return x < 0 ? -q : q;
+}
+
+/* Nearest E2M1 value: sign, 2 exponent bits (bias 1), 1 mantissa bit; the
+ * magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6. Ties go to the even mantissa;
+ * magnitudes beyond 6 saturate to 6. */
+double oracle_round_e2m1(double x) {
+    double a = fabs(x), q;
+    if (a < 2.0) q = round_to_quantum(a, 0.5);        /* 0, 0.5 | 1, 1.5 */
+    else if (a < 4.0) q = round_to_quantum(a, 1.0);   /* 2, 3 */
+    else q = round_to_quantum(a, 2.0);                /* 4, 6 */
+    if (q > 6.0) q = 6.0;
+    return x < 0 ? -q : q;
+}
+
+/* One block of n <= 16 values (a short block at the end of a row counts only
+ * its own values). */
+static void fake_nvfp4_block(const double *x, double *y, int n) {
+    float amax = 0.0f;
+    for (int i = 0; i < n; ++i) {
+        float a = fabsf((float)x[i]);
+        if (a > amax) amax = a;
+    }
+    const float s = (float)oracle_round_e4m3((double)(amax / 6.0f));
+    for (int i = 0; i < n; ++i)
+        y[i] = s == 0.0f ? 0.0 : oracle_round_e2m1((double)((float)x[i] / s)) * (double)s;
+}
+
+/* Fake-quantizes `rows` rows of `cols` values (blocks of 16 along each row). */
+void oracle_fake_nvfp4(const double *x, double *y, long rows, int cols) {
+#pragma omp parallel for schedule(static)
+    for (long r = 0; r < rows; ++r)
+        for (int c0 = 0; c0 < cols; c0 += 16)
+            fake_nvfp4_block(x + r * cols + c0, y + r * cols + c0, cols - c0 < 16 ? cols - c0 : 16);
+}
+
+static double *fake_copy(const double *x, long rows, int cols) {
+    double *y = (double *)malloc(sizeof(double) * (size_t)(rows * cols > 0 ? rows * cols : 1));
+    oracle_fake_nvfp4(x, y, rows, cols);
+    return y;
+}
+
+/* The fake-quantized probability matrix of query head bh: Ph[q * Skv + k] =
+ * fake_nvfp4 of P's row q (blocks of 16 keys), P = exp(score - LSE) at visible
+ * pairs and 0 elsewhere, scores from the given (already quantized) Q and K. */
+static void qat_probabilities(const oracle_cfg *c, const double *Qh, const double *Kh,
+                              const double *LSE, long bh, double *Ph) {
+    const int G = c->Hq / c->Hkv;
+    const int b = (int)(bh / c->Hq), h = (int)(bh % c->Hq);
+    const long bhk = (long)b * c->Hkv + h / G;
+    int Lq, Lk;
+    lengths(c, b, &Lq, &Lk);
+#pragma omp parallel
+    {
+        double *prow = (double *)malloc(sizeof(double) * (size_t)(c->Skv > 0 ? c->Skv : 1));
+#pragma omp for schedule(dynamic, 8)
+        for (long q = 0; q < c->Sq; ++q) {
+            const double *qr = row_of(Qh, bh, q, c->Sq, c->Dqk);
+            const double lse = LSE[bh * c->Sq + q];
+            for (long k = 0; k < c->Skv; ++k)
+                prow[k] = visible(c, Lq, Lk, q, k)
+                              ? prob(c, score(c, qr, row_of(Kh, bhk, k, c->Skv, c->Dqk), bh, q, k), lse)
+                              : 0.0;
+            oracle_fake_nvfp4(prow, Ph + q * c->Skv, 1, c->Skv);
+        }
+        free(prow);
+    }
+}
+
+/* QAT forward: O_hp and LSE are the plain forward of the fake-quantized Q, K,
+ * V (O_hp = P V_hat with P unquantized, "high precision"); O_user = fq(P) V_hat
+ * is the user-visible output. Any of the outputs may be NULL. */
+void oracle_qat_forward(const oracle_cfg *c, const double *Q, const double *K, const double *V,
+                        double *O_hp, double *LSE, double *O_user) {
+    const long qrows = (long)c->B * c->Hq * c->Sq, krows = (long)c->B * c->Hkv * c->Skv;
+    double *Qh = fake_copy(Q, qrows, c->Dqk), *Kh = fake_copy(K, krows, c->Dqk);
+    double *Vh = fake_copy(V, krows, c->Dv);
+    double *o = O_hp ? O_hp : (double *)malloc(sizeof(double) * (size_t)(qrows * c->Dv > 0 ? qrows * c->Dv : 1));
+    double *l = LSE ? LSE : (double *)malloc(sizeof(double) * (size_t)(qrows > 0 ? qrows : 1));
+    oracle_forward_sink(c, Qh, Kh, Vh, NULL, o, l);
+    if (O_user) {
+        const int G = c->Hq / c->Hkv;
+        double *Ph = (double *)malloc(sizeof(double) * (size_t)((long)c->Sq * c->Skv > 0 ? (long)c->Sq * c->Skv : 1));
+        for (long bh = 0; bh < (long)c->B * c->Hq; ++bh) {
+            qat_probabilities(c, Qh, Kh, l, bh, Ph);
+            const long bhk = (bh / c->Hq) * c->Hkv + (bh % c->Hq) / G;
+#pragma omp parallel for schedule(static)
+            for (long q = 0; q < c->Sq; ++q) {
+                double *out = O_user + (bh * c->Sq + q) * c->Dv;
+                for (int d = 0; d < c->Dv; ++d) out[d] = 0.0;
+                for (long k = 0; k < c->Skv; ++k) {
+                    const double p = Ph[q * c->Skv + k];
+                    if (p == 0.0) continue;
+                    const double *vr = row_of(Vh, bhk, k, c->Skv, c->Dv);
+                    for (int d = 0; d < c->Dv; ++d) out[d] += p * vr[d];
+                }
+            }
+        }
+        free(Ph);
+    }
+    if (!O_hp) free(o);
+    if (!LSE) free(l);
+    free(Qh); free(Kh); free(Vh);
+}
+
+/* QAT backward: dQ = scale dS K_hat, dK = scale dS^T Q_hat with dS = P (dP -
+ * delta), dP = dO V_hat^T, delta = rowsum(O_hp * dO) (P unquantized), and
+ * dV = fq(P)^T dO. O is the high-precision forward output, LSE its statistic. */
+void oracle_qat_backward(const oracle_cfg *c, const double *Q, const double *K, const double *V,
+                         const double *O, const double *dO, const double *LSE, double *dQ,
+                         double *dK, double *dV) {
+    const int G = c->Hq / c->Hkv;
+    const long qrows = (long)c->B * c->Hq * c->Sq, krows = (long)c->B * c->Hkv * c->Skv;
+    double *Qh = fake_copy(Q, qrows, c->Dqk), *Kh = fake_copy(K, krows, c->Dqk);
+    double *Vh = fake_copy(V, krows, c->Dv);
+    double *delta = (double *)malloc(sizeof(double) * (size_t)(qrows > 0 ? qrows : 1));
+    double *dv_plain = (double *)malloc(sizeof(double) * (size_t)(krows * c->Dv > 0 ? krows * c->Dv : 1));
+    oracle_delta(c, O, dO, delta);
+#pragma omp parallel for schedule(dynamic, 8)
+    for (long r = 0; r < qrows; ++r)
+        dq_row(c, Qh, Kh, Vh, dO, LSE, delta, r / c->Sq, r % c->Sq, dQ + r * c->Dqk);
+#pragma omp parallel for schedule(dynamic, 8)
+    for (long r = 0; r < krows; ++r)
+        dkv_row(c, Qh, Kh, Vh, dO, LSE, delta, r / c->Skv, r % c->Skv, dK + r * c->Dqk,
+                dv_plain + r * c->Dv);
+    /* dV with the fake-quantized probabilities, head by head of each group */
+    for (long r = 0; r < krows * c->Dv; ++r) dV[r] = 0.0;
+    double *Ph = (double *)malloc(sizeof(double) * (size_t)((long)c->Sq * c->Skv > 0 ? (long)c->Sq * c->Skv : 1));
+    for (long bh = 0; bh < qrows / (c->Sq > 0 ? c->Sq : 1); ++bh) {
+        qat_probabilities(c, Qh, Kh, LSE, bh, Ph);
+        const long bhk = (bh / c->Hq) * c->Hkv + (bh % c->Hq) / G;
+#pragma omp parallel for schedule(static)
+        for (long k = 0; k < c->Skv; ++k) {
+            double *out = dV + (bhk * c->Skv + k) * c->Dv;
+            for (long q = 0; q < c->Sq; ++q) {
+                const double p = Ph[q * c->Skv + k];
+                if (p == 0.0) continue;
+                const double *dor = row_of(dO, bh, q, c->Sq, c->Dv);
+                for (int d = 0; d < c->Dv; ++d) out[d] += p * dor[d];
+            }
+        }
+    }
+    free(Ph); free(dv_plain); free(delta);
+    free(Qh); free(Kh); free(Vh);
 }

@@ -572,3 +572,151 @@ def test_dbias_rows_equal_full_dbias(oracle_mod):
         rows = [0, 3, 5, full.shape[0] - 1]
         np.testing.assert_array_equal(oracle_mod.dbias_rows(p, q, k, v, o, do, lse, bias, rows),
                                       full[rows])
+
+
+# ---- NVFP4 QAT ("NVFP4 Attention QAT Backward" page, Overview). The pins fix the
+# oracle's E4M3 / E2M1 rounding to brute force over every code of each format
+# (decoded from its bit fields here) and to torch's float8_e4m3fn cast, its
+# block fake quantization to a block worked by hand, and its QAT backward to
+# the plain (pinned) backward on the quantized operands for dQ/dK and to a
+# fake-quantized P built here, independently, for dV and the QAT forward.
+def _e4m3_values():
+    vals = []
+    for e in range(16):
+        for m in range(8):
+            if e == 15 and m == 7:
+                continue  # NaN
+            vals.append((m / 8 * 2.0 ** -6) if e == 0 else (1 + m / 8) * 2.0 ** (e - 7))
+    return np.array(vals), np.array([m for e in range(16) for m in range(8) if not (e == 15 and m == 7)])
+
+
+def _e2m1_values():
+    vals, mant = [], []
+    for e in range(4):
+        for m in range(2):
+            vals.append(m * 0.5 if e == 0 else (1 + m / 2) * 2.0 ** (e - 1))
+            mant.append(m)
+    return np.array(vals), np.array(mant)
+
+
+def _nearest(x, vals, mant, top):
+    a = min(abs(x), top)
+    d = np.abs(vals - a)
+    best = np.flatnonzero(d == d.min())
+    if len(best) > 1:  # a tie: the even mantissa
+        best = [b for b in best if mant[b] % 2 == 0]
+    q = vals[best[0]]
+    return -q if x < 0 else q
+
+
+def _probe_points(vals, rng):
+    v = np.unique(vals)
+    mids = (v[1:] + v[:-1]) / 2
+    pts = np.concatenate([v, mids, mids * (1 + 1e-9), mids * (1 - 1e-9), v * 1.3,
+                          rng.uniform(0, v.max() * 1.2, 400)])
+    return np.concatenate([pts, -pts])
+
+
+def test_e4m3_rounding_matches_brute_force_and_torch(oracle_mod):
+    vals, mant = _e4m3_values()
+    rng = np.random.default_rng(40)
+    pts = _probe_points(vals, rng)
+    for x in pts:
+        assert oracle_mod.round_e4m3(x) == _nearest(x, vals, mant, 448.0), x
+    # torch casts through fp32, so compare on fp32 inputs (no double rounding)
+    inr = pts[np.abs(pts) <= 448.0].astype(np.float32).astype(np.float64)
+    t = torch.tensor(inr, dtype=torch.float32).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(np.array([oracle_mod.round_e4m3(x) for x in inr]), t)
+
+
+def test_e2m1_rounding_matches_brute_force(oracle_mod):
+    vals, mant = _e2m1_values()
+    rng = np.random.default_rng(41)
+    for x in _probe_points(vals, rng):
+        assert oracle_mod.round_e2m1(x) == _nearest(x, vals, mant, 6.0), x
+
+
+def test_fake_nvfp4_block_worked_by_hand(oracle_mod):
+    """amax 1.25: scale = E4M3(1.25/6 = 0.2083) = 0.203125 (13/64; the E4M3
+    neighbours are 0.203125 and 0.21875); 0.1 -> 0.1/0.203125 = 0.49 -> 0.5 ->
+    0.1015625; -0.5 -> -2.46 -> -2 -> -0.40625; 1.25 -> 6.15 -> 6 -> 1.21875."""
+    x = np.zeros((2, 32))
+    x[0, :4] = [1.25, 0.1, -0.5, 0.3]
+    x[0, 16:20] = [6.0, -3.0, 1.5, 0.5]        # scale 1: E2M1 values are kept
+    x[1, :2] = [1e4, 100.0]                     # scale saturates at 448
+    y = oracle_mod.fake_nvfp4(x)
+    np.testing.assert_array_equal(y[0, :4], [1.21875, 0.1015625, -0.40625, 0.3046875])
+    np.testing.assert_array_equal(y[0, 16:20], [6.0, -3.0, 1.5, 0.5])
+    assert np.all(y[0, 4:16] == 0) and np.all(y[0, 20:] == 0)
+    # 1e4/448 = 22.3 saturates to 6; 100/448 = 0.223 rounds to 0
+    np.testing.assert_array_equal(y[1, :2], [6 * 448.0, 0.0])
+    assert np.all(y[1, 16:] == 0)  # an all-zero block stays zero
+
+
+def test_fake_nvfp4_invariants(oracle_mod):
+    rng = np.random.default_rng(42)
+    x = rng.standard_normal((64, 48)) * rng.uniform(0.01, 50, (64, 1))
+    y = oracle_mod.fake_nvfp4(x)
+    np.testing.assert_array_equal(oracle_mod.fake_nvfp4(y), y)       # idempotent
+    np.testing.assert_array_equal(oracle_mod.fake_nvfp4(-x), -y)     # odd
+    np.testing.assert_array_equal(oracle_mod.fake_nvfp4(4 * x), 4 * y)  # power-of-two scaling
+    x2 = x.copy()
+    x2[:, 16:32] *= 3.0
+    np.testing.assert_array_equal(oracle_mod.fake_nvfp4(x2)[:, :16], y[:, :16])  # blocks independent
+    assert np.all(np.abs(y - x) <= np.abs(x).reshape(64, 3, 16).max(-1).repeat(16, -1) / 6 * 1.07 + 1e-12)
+
+
+def _fq_independent(x):
+    """Fake quantization written here from the brute-force format tables."""
+    ev, em = _e4m3_values()
+    fv, fm = _e2m1_values()
+    x = np.asarray(x, dtype=np.float64)
+    out = np.zeros_like(x)
+    flat, oflat = x.reshape(-1, x.shape[-1]), out.reshape(-1, x.shape[-1])
+    for r in range(flat.shape[0]):
+        for c0 in range(0, flat.shape[1], 16):
+            blk = flat[r, c0:c0 + 16].astype(np.float32)
+            amax = np.float32(np.abs(blk).max()) if blk.size else np.float32(0)
+            s = np.float32(_nearest(float(amax / np.float32(6.0)), ev, em, 448.0))
+            if s == 0:
+                continue
+            oflat[r, c0:c0 + 16] = [_nearest(float(v / s), fv, fm, 6.0) * float(s) for v in blk]
+    return out
+
+
+def test_qat_oracle_against_independent_pieces(oracle_mod):
+    p = Problem(1, 2, 2, 9, 21, 32, 16, causal=True, bottom_right=True)
+    q, k, v, do = _inputs(p, seed=43)
+    o_hp, lse, o_user = oracle_mod.qat_forward(p, q, k, v)
+    qh, kh, vh = _fq_independent(q), _fq_independent(k), _fq_independent(v)
+    np.testing.assert_array_equal(oracle_mod.fake_nvfp4(q), qh)
+    # O_hp / LSE: the plain forward of the quantized operands
+    o2, lse2 = oracle_mod.forward(p, qh, kh, vh)
+    np.testing.assert_array_equal(o_hp, o2)
+    np.testing.assert_array_equal(lse, lse2)
+    # P from the quantized scores (torch mask helper), fake-quantized along keys
+    mask = _torch_mask(p).numpy()[:, 0]
+    s = np.einsum("bhqd,bhkd->bhqk", qh, kh) * p.resolved_scale
+    P = np.where(mask[:, None], np.exp(s - lse[..., None]), 0.0)
+    Ph = _fq_independent(P)
+    np.testing.assert_allclose(o_user, np.einsum("bhqk,bhkd->bhqd", Ph, vh), atol=1e-12)
+    dq, dk, dv = oracle_mod.qat_backward(p, q, k, v, o_hp, do, lse)
+    rq, rk, rv = oracle_mod.backward(p, qh, kh, vh, o_hp, do, lse)  # straight-through dQ, dK
+    np.testing.assert_allclose(dq, rq, atol=1e-13)
+    np.testing.assert_allclose(dk, rk, atol=1e-13)
+    np.testing.assert_allclose(dv, np.einsum("bhqk,bhqd->bhkd", Ph, do), atol=1e-12)
+    assert np.abs(dv - rv).max() > 1e-6  # the quantized P really differs from P
+
+
+def test_qat_backward_gqa_sums_group_heads(oracle_mod):
+    """dK/dV of a KV head equal the sums of an explicit MHA problem over its group."""
+    p = Problem(1, 4, 2, 7, 18, 32, 32, causal=True)
+    q, k, v, do = _inputs(p, seed=44)
+    o, lse, _ = oracle_mod.qat_forward(p, q, k, v)
+    dq, dk, dv = oracle_mod.qat_backward(p, q, k, v, o, do, lse)
+    pm = Problem(1, 4, 4, 7, 18, 32, 32, causal=True)
+    kr, vr = np.repeat(k, 2, axis=1), np.repeat(v, 2, axis=1)
+    dq2, dk2, dv2 = oracle_mod.qat_backward(pm, q, kr, vr, o, do, lse)
+    np.testing.assert_allclose(dq, dq2, atol=1e-13)
+    np.testing.assert_allclose(dk, dk2.reshape(1, 2, 2, 18, 32).sum(2), atol=1e-13)
+    np.testing.assert_allclose(dv, dv2.reshape(1, 2, 2, 18, 32).sum(2), atol=1e-13)
