@@ -66,6 +66,13 @@ def load(build_if_missing: bool = False):
     lib.sdpa_fwd.restype = i
     lib.sdpa_fwd_bias.argtypes = list(lib.sdpa_fwd.argtypes[:-1]) + [vp, i, i, vp]
     lib.sdpa_fwd_bias.restype = i
+    lib.sdpa_nvfp4_fake_quant.argtypes = [vp, vp, ctypes.c_longlong, vp]
+    lib.sdpa_nvfp4_fake_quant.restype = i
+    lib.sdpa_bwd_nvfp4_qat_workspace_size.argtypes = [i, i, i, i, i, i, i]
+    lib.sdpa_bwd_nvfp4_qat_workspace_size.restype = sz
+    lib.sdpa_bwd_nvfp4_qat.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i,
+                                       ctypes.c_float, i, i, i, i, vp, vp, vp, sz, vp]
+    lib.sdpa_bwd_nvfp4_qat.restype = i
     lib.sdpa_bwd_workspace_size.argtypes = [i, i, i, i, i, i, i, i]
     lib.sdpa_bwd_workspace_size.restype = sz
     lib.sdpa_status_string.argtypes = [i]
@@ -259,6 +266,69 @@ def sdpa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: Option
     if rc != 0:
         raise SdpaError(rc, "sdpa_fwd_bias" if bias is not None else "sdpa_fwd")
     return o, lse
+
+
+def nvfp4_fake_quant(x: torch.Tensor, out: Optional[torch.Tensor] = None,
+                     stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """NVFP4 fake quantization of a contiguous bf16 CUDA tensor in blocks of 16
+    consecutive values (sdpa_nvfp4_fake_quant); numel must be a multiple of 16."""
+    lib = load()
+    if not isinstance(x, torch.Tensor) or x.dtype != torch.bfloat16 or not x.is_cuda \
+            or not x.is_contiguous():
+        raise ValueError("x must be a contiguous bf16 CUDA tensor")
+    out = torch.empty_like(x) if out is None else out
+    _check_bf16("out", out, x.shape)
+    rc = lib.sdpa_nvfp4_fake_quant(_ptr(x), _ptr(out), x.numel(), _stream_handle(stream))
+    if rc != 0:
+        raise SdpaError(rc, "sdpa_nvfp4_fake_quant")
+    return out
+
+
+def sdpa_fwd_nvfp4_qat(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, **kw):
+    """The QAT forward statistics the QAT backward takes: sdpa_fwd() of the
+    fake-quantized q, k, v, i.e. (O_hp, LSE) with O_hp = softmax(scale q^ k^^T) v^."""
+    stream = kw.get("stream")
+    return sdpa_fwd(nvfp4_fake_quant(q, stream=stream), nvfp4_fake_quant(k, stream=stream),
+                    nvfp4_fake_quant(v, stream=stream), **kw)
+
+
+def sdpa_bwd_nvfp4_qat(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o_hp: torch.Tensor,
+                       do: torch.Tensor, lse: torch.Tensor, *, scale: Optional[float] = None,
+                       causal: bool = False, bottom_right: bool = False, window_left: int = -1,
+                       window_right: int = -1, seq_q_lens: Optional[torch.Tensor] = None,
+                       seq_kv_lens: Optional[torch.Tensor] = None, dq: Optional[torch.Tensor] = None,
+                       dk: Optional[torch.Tensor] = None, dv: Optional[torch.Tensor] = None,
+                       workspace: Optional[torch.Tensor] = None,
+                       stream: Optional[torch.cuda.Stream] = None):
+    """dQ, dK, dV of NVFP4 QAT attention (sdpa_bwd_nvfp4_qat): q, k, v unquantized,
+    o_hp / lse from sdpa_fwd_nvfp4_qat. D = 128."""
+    lib = load()
+    B, Hq, Sq, Dqk = q.shape
+    Hkv, Skv, Dv = k.shape[1], k.shape[2], v.shape[3]
+    for name, t, shape in (("q", q, (B, Hq, Sq, Dqk)), ("k", k, (B, Hkv, Skv, Dqk)),
+                           ("v", v, (B, Hkv, Skv, Dv)), ("o_hp", o_hp, (B, Hq, Sq, Dv)),
+                           ("do", do, (B, Hq, Sq, Dv))):
+        _check_bf16(name, t, shape)
+    if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous() \
+            or lse.numel() != B * Hq * Sq:
+        raise ValueError("lse must be a contiguous fp32 CUDA tensor with B*Hq*Sq elements")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.sdpa_bwd_nvfp4_qat(_ptr(q), _ptr(k), _ptr(v), _ptr(o_hp), _ptr(do), _ptr(lse), _ptr(dq),
+                                _ptr(dk), _ptr(dv), B, Hq, Hkv, Sq, Skv, Dqk, Dv,
+                                0.0 if scale is None else float(scale), int(causal),
+                                int(bottom_right), int(window_left), int(window_right),
+                                _ptr(seq_q_lens), _ptr(seq_kv_lens), _ptr(workspace), ws_bytes,
+                                _stream_handle(stream))
+    if rc != 0:
+        raise SdpaError(rc, "sdpa_bwd_nvfp4_qat")
+    return dq, dk, dv
+
+
+def nvfp4_qat_workspace_size(B, Hq, Hkv, Sq, Skv, Dqk, Dv) -> int:
+    return int(load().sdpa_bwd_nvfp4_qat_workspace_size(B, Hq, Hkv, Sq, Skv, Dqk, Dv))
 
 
 def check_device_status(stream: Optional[torch.cuda.Stream] = None) -> None:

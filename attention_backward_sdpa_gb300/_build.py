@@ -18,10 +18,11 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsdpa_bwd.so")
-SOURCES = ["sdpa_bwd_api.cu", "sdpa_bwd_main.cu", "sdpa_bwd_main_bias.cu", "sdpa_bwd_main_ds.cu",
+SOURCES = ["sdpa_bwd_api.cu", "sdpa_bwd_main.cu", "sdpa_bwd_main_bias.cu", "sdpa_bwd_main_qat.cu",
+           "sdpa_bwd_main_ds.cu",
            "sdpa_bwd_aux.cu",
            "sdpa_bwd_dq.cu", "sdpa_bwd_noalloc.cu", "sdpa_fwd.cu"]
-HEADERS = ["common.cuh", "gqa.cuh", "ptx.cuh", "tmap.h", "sdpa_bwd_main.cuh"]
+HEADERS = ["common.cuh", "gqa.cuh", "ptx.cuh", "tmap.h", "sdpa_bwd_main.cuh", "nvfp4.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",

@@ -158,6 +158,11 @@ cudaError_t main_ds_kernel_setup();
 cudaError_t main_kernel_setup();  // per device: opt in to the main kernel's shared memory
 cudaError_t launch_main_bias(const MainMaps& maps, const ChainParams& p, cudaStream_t s);
 cudaError_t main_bias_kernel_setup();
+cudaError_t launch_main_qat(const MainMaps& maps, const ChainParams& p, cudaStream_t s);
+cudaError_t main_qat_kernel_setup();
+// NVFP4 fake quantization of n_blocks blocks of 16 consecutive bf16 values.
+cudaError_t launch_nvfp4_fake_quant(const void* x, void* y, long long n_blocks, int num_sms,
+                                    cudaStream_t s);
 
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,

@@ -49,10 +49,12 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 bool use_ds_route(int deterministic, int Dqk) { return Dqk == 192 || (deterministic && Dqk == 128); }
 
 struct Carve {
-  size_t qstat, dq_accum, ds_ws, zero_tile, counters, dk_ws, dv_ws, dsink_part, total;
+  size_t qstat, dq_accum, ds_ws, zero_tile, counters, dk_ws, dv_ws, dsink_part;
+  size_t q_hat, k_hat, v_hat;  // NVFP4 QAT: the fake-quantized Q, K, V
+  size_t total;
 };
 
-Carve carve(int B, int Hq, int Hkv, int Sq, int Skv, int Dqk, int Dv, bool ds_route) {
+Carve carve(int B, int Hq, int Hkv, int Sq, int Skv, int Dqk, int Dv, bool ds_route, bool qat = false) {
   const size_t n_qt = (size_t)ceil_div(Sq, BQ), n_kt = (size_t)ceil_div(Skv, BN);
   const size_t bh = (size_t)B * Hq;
   Carve c{};
@@ -81,6 +83,15 @@ Carve carve(int B, int Hq, int Hkv, int Sq, int Skv, int Dqk, int Dv, bool ds_ro
     off = align256(off + bh * (size_t)Skv * Dv * 2);
   } else {
     c.dk_ws = c.dv_ws = SIZE_MAX;
+  }
+  c.q_hat = c.k_hat = c.v_hat = SIZE_MAX;
+  if (qat) {
+    c.q_hat = off;
+    off = align256(off + bh * (size_t)Sq * Dqk * 2);
+    c.k_hat = off;
+    off = align256(off + (size_t)B * Hkv * Skv * Dqk * 2);
+    c.v_hat = off;
+    off = align256(off + (size_t)B * Hkv * Skv * Dv * 2);
   }
   c.total = off;
   return c;
@@ -203,6 +214,13 @@ size_t sdpa_bwd_workspace_size(int B, int H_q, int H_kv, int S_q, int S_kv, int 
   return carve(B, H_q, H_kv, S_q, S_kv, D_qk, D_v, use_ds_route(deterministic, D_qk)).total;
 }
 
+size_t sdpa_bwd_nvfp4_qat_workspace_size(int B, int H_q, int H_kv, int S_q, int S_kv, int D_qk,
+                                         int D_v) {
+  if (basic_checks(B, H_q, H_kv, S_q, S_kv, D_qk, D_v) != SDPA_OK) return 0;
+  if (D_qk != 128 || D_v != 128 || S_q == 0 || S_kv == 0) return 0;
+  return carve(B, H_q, H_kv, S_q, S_kv, D_qk, D_v, false, true).total;
+}
+
 int sdpa_bwd_profile_enable(int on) {
   std::lock_guard<std::mutex> lock(g_mu);
   g_profile = on != 0;
@@ -258,10 +276,13 @@ int run_chain(const void* q, const void* k, const void* v, const void* o, const 
               int S_kv, int D_qk, int D_v, float scale, int causal, int bottom_right,
               int window_left, int window_right, int deterministic, const int32_t* seq_q_lens,
               const int32_t* seq_kv_lens, void* workspace, size_t workspace_bytes,
-              const float* sink, float* dsink, const BiasArgs& ba, void* stream_) {
+              const float* sink, float* dsink, const BiasArgs& ba, void* stream_,
+              bool qat = false) {
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   int rc = basic_checks(B, H_q, H_kv, S_q, S_kv, D_qk, D_v);
   if (rc != SDPA_OK) return rc;
+  // NVFP4 QAT: D 128, the dQ-reduction route, no bias or sink.
+  if (qat && (D_qk != 128 || D_v != 128)) return SDPA_ERR_UNSUPPORTED;
   if (!q || !k || !v || !o || !d_o || !lse || !dq || !dk || !dv) return SDPA_ERR_INVALID;
   if (dsink && !sink) return SDPA_ERR_INVALID;
   if (ba.bias) {
@@ -305,7 +326,7 @@ int run_chain(const void* q, const void* k, const void* v, const void* o, const 
   }
 
   const bool ds_route = use_ds_route(deterministic, D_qk);
-  const Carve cv = carve(B, H_q, H_kv, S_q, S_kv, D_qk, D_v, ds_route);
+  const Carve cv = carve(B, H_q, H_kv, S_q, S_kv, D_qk, D_v, ds_route, qat);
   bool own_ws = false;
   if (workspace == nullptr) {
     if (cudaMallocAsync(&workspace, cv.total, stream) != cudaSuccess) return SDPA_ERR_CUDA;
@@ -382,9 +403,13 @@ int run_chain(const void* q, const void* k, const void* v, const void* o, const 
 
   MainMaps maps;
   const long long BHq = (long long)B * H_q, BHkv = (long long)B * H_kv;
-  if (!make_bhsd_map(&maps.q, q, D_qk, S_q, BHq, BQ) ||
-      !make_bhsd_map(&maps.k, k, D_qk, S_kv, BHkv, BN) ||
-      !make_bhsd_map(&maps.v, v, D_v, S_kv, BHkv, BN) ||
+  // QAT: the GEMMs read the fake-quantized copies, written first.
+  const void* qg = qat ? static_cast<const void*>(ws + cv.q_hat) : q;
+  const void* kg = qat ? static_cast<const void*>(ws + cv.k_hat) : k;
+  const void* vg = qat ? static_cast<const void*>(ws + cv.v_hat) : v;
+  if (!make_bhsd_map(&maps.q, qg, D_qk, S_q, BHq, BQ) ||
+      !make_bhsd_map(&maps.k, kg, D_qk, S_kv, BHkv, BN) ||
+      !make_bhsd_map(&maps.v, vg, D_v, S_kv, BHkv, BN) ||
       !make_bhsd_map(&maps.d_o, d_o, D_v, S_q, BHq, BQ) ||
       !make_bhsd_map(&maps.dk_out, p.dk_ws ? static_cast<void*>(p.dk_ws) : dk, D_qk, S_kv,
                      p.dk_ws ? BHq : BHkv, BN) ||
@@ -397,11 +422,17 @@ int run_chain(const void* q, const void* k, const void* v, const void* o, const 
   cudaError_t e = cudaSuccess;
   ProfEvents prof(stream);
   prof.begin(0);
-  e = launch_preprocess(p, stream);
+  if (qat) {
+    e = launch_nvfp4_fake_quant(q, ws + cv.q_hat, BHq * S_q * D_qk / 16, sms, stream);
+    if (e == cudaSuccess) e = launch_nvfp4_fake_quant(k, ws + cv.k_hat, BHkv * S_kv * D_qk / 16, sms, stream);
+    if (e == cudaSuccess) e = launch_nvfp4_fake_quant(v, ws + cv.v_hat, BHkv * S_kv * D_v / 16, sms, stream);
+  }
+  if (e == cudaSuccess) e = launch_preprocess(p, stream);
   prof.end(0);
   if (e == cudaSuccess) {
     prof.begin(1);
-    e = D_qk == 192 ? launch_main_ds(maps, p, stream) : launch_main(maps, p, stream);
+    e = D_qk == 192 ? launch_main_ds(maps, p, stream)
+                    : (qat ? launch_main_qat(maps, p, stream) : launch_main(maps, p, stream));
     prof.end(1);
   }
   if (e == cudaSuccess) {  // dQ (and, under GQA, the dK/dV group reduction)
@@ -532,6 +563,32 @@ int sdpa_bwd_sink(const void* q, const void* k, const void* v, const void* o, co
   return run_chain(q, k, v, o, d_o, lse, dq, dk, dv, B, H_q, H_kv, S_q, S_kv, D_qk, D_v, scale,
                    causal, bottom_right, window_left, window_right, deterministic, seq_q_lens,
                    seq_kv_lens, workspace, workspace_bytes, sink, dsink, BiasArgs{}, stream);
+}
+
+int sdpa_bwd_nvfp4_qat(const void* q, const void* k, const void* v, const void* o_hp,
+                       const void* d_o, const float* lse, void* dq, void* dk, void* dv, int B,
+                       int H_q, int H_kv, int S_q, int S_kv, int D_qk, int D_v, float scale,
+                       int causal, int bottom_right, int window_left, int window_right,
+                       const int32_t* seq_q_lens, const int32_t* seq_kv_lens, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  return run_chain(q, k, v, o_hp, d_o, lse, dq, dk, dv, B, H_q, H_kv, S_q, S_kv, D_qk, D_v, scale,
+                   causal, bottom_right, window_left, window_right, 0, seq_q_lens, seq_kv_lens,
+                   workspace, workspace_bytes, nullptr, nullptr, BiasArgs{}, stream, true);
+}
+
+int sdpa_nvfp4_fake_quant(const void* x, void* y, long long n, void* stream) {
+  if (!x || !y || n < 0 || n % 16 != 0) return SDPA_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(x) % 16 != 0 || reinterpret_cast<uintptr_t>(y) % 16 != 0)
+    return SDPA_ERR_ALIGN;
+  if (n == 0) return SDPA_OK;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SDPA_ERR_CUDA;
+  int* status = nullptr;
+  int sms = 0;
+  const int rc = device_state(dev, &status, &sms);
+  if (rc != SDPA_OK) return rc;
+  return launch_nvfp4_fake_quant(x, y, n / 16, sms, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? SDPA_OK : SDPA_ERR_CUDA;
 }
 
 int sdpa_bwd_bias(const void* q, const void* k, const void* v, const void* o, const void* d_o,

@@ -7,6 +7,7 @@ namespace sdpa {
 cudaError_t main_kernel_setup() {
   cudaError_t e = main_variant_setup<false>();
   if (e == cudaSuccess) e = main_bias_kernel_setup();
+  if (e == cudaSuccess) e = main_qat_kernel_setup();
   return e;
 }
 

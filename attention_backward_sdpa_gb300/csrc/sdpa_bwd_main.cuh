@@ -1,6 +1,7 @@
 // sdpa_bwd_main.cuh -- fused five-GEMM SDPA backward main kernel for sm_103a
-// (D_qk = D_v = 64 or 128). Instantiated without a bias in sdpa_bwd_main.cu and
-// with one in sdpa_bwd_main_bias.cu.
+// (D_qk = D_v = 64 or 128). Instantiated without a bias in sdpa_bwd_main.cu, with
+// one in sdpa_bwd_main_bias.cu, and for the NVFP4 QAT backward in
+// sdpa_bwd_main_qat.cu.
 //
 // What it computes (cuDNN frontend docs, "SDPA Backward (SM120)", section
 // "Main-kernel pipeline: KV-stationary, five chained GEMMs"): one CTA owns one
@@ -29,6 +30,15 @@
 // CTA visits get their zeros from an otherwise idle warp of the CTA that owns
 // their key tile (per-batch dBias), or from the preprocess kernel (one shared
 // dBias, which the batch rows add into atomically).
+//
+// NVFP4 QAT (QAT; page "NVFP4 Attention QAT Backward", Overview): Q, K and V
+// arrive already fake-quantized, so the GEMMs are unchanged; dS (hence dQ and
+// dK) uses P itself (straight-through), while G3 takes P fake-quantized to
+// NVFP4 in blocks of 16 consecutive keys of each query: the 16 keys of a block
+// are 16 lanes of one warp, whose maximum one warp reduction gives. The local
+// scale amax/6 and each value's division by it are correctly rounded fp32
+// divisions; the E4M3 and E2M1 roundings are the hardware conversions
+// (round to nearest even, saturating).
 //
 // Schedule. Two query tiles are in flight: tensor memory holds two slots, each
 // with S^T and dP^T (dQ^T reuses the dP^T columns once dS is formed). Compute
@@ -65,6 +75,7 @@
 #include <cuda_bf16.h>
 
 #include "common.cuh"
+#include "nvfp4.cuh"
 #include "ptx.cuh"
 
 namespace sdpa {
@@ -126,6 +137,16 @@ struct MainLayout {
 };
 
 __device__ __forceinline__ void set_main_status(int* status, int bit) { atomicOr(status, bit); }
+
+// Largest value of `v` (>= 0) over this lane's 16-lane half of the warp (all
+// lanes take part): non-negative floats order like their bit patterns.
+__device__ __forceinline__ float half_warp_max_nonneg(float v, bool upper) {
+  uint32_t lo, hi;
+  const uint32_t x = __float_as_uint(v);
+  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(lo) : "r"(upper ? 0u : x));
+  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(hi) : "r"(upper ? x : 0u));
+  return __uint_as_float(upper ? hi : lo);
+}
 
 // Bias column of one query tile for this thread's key: bz[i] = bias(q0 + i, k)
 // (0 past S_q or S_kv). `off` is the element offset of (batch row, head, q0, k).
@@ -207,7 +228,8 @@ __device__ __forceinline__ void prefetch_bias_tile(const ChainParams& p, long lo
 // DS_OUT selects the deterministic two-kernel route: instead of G5 and the dQ
 // reduction, every dS^T tile is stored to the workspace for the dQ kernel.
 // BIAS adds the additive bias to the replay and writes dBias (when p.dbias).
-template <int D, bool DS_OUT, bool BIAS>
+// QAT writes G3's P^T fake-quantized to NVFP4.
+template <int D, bool DS_OUT, bool BIAS, bool QAT = false>
 __global__ void __launch_bounds__(MAIN_THREADS, 1)
     sdpa_bwd_main(const __grid_constant__ MainMaps maps, const ChainParams p) {
   using L = MainLayout<D, DS_OUT>;
@@ -673,8 +695,19 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
 #pragma unroll
       for (int c16 = 0; c16 < 2; ++c16) {
         uint32_t w[16];
+        if constexpr (QAT) {
+          // G3 reads P fake-quantized over blocks of 16 keys (16 lanes).
+          const bool upper = (lane & 16) != 0;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(P[c16 * 32 + 2 * i], P[c16 * 32 + 2 * i + 1]);
+          for (int i = 0; i < 16; ++i) {
+            const float p0 = P[c16 * 32 + 2 * i], p1 = P[c16 * 32 + 2 * i + 1];
+            const float2 sc = nvfp4_scales(half_warp_max_nonneg(p0, upper), half_warp_max_nonneg(p1, upper));
+            w[i] = fake_nvfp4_pair_bf16(p0, p1, sc.x, sc.y);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(P[c16 * 32 + 2 * i], P[c16 * 32 + 2 * i + 1]);
+        }
         tmem_st16(t_lane + L::col_s(slot) + c16 * 16, w);
       }
       tmem_st_wait();
@@ -811,9 +844,9 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
   }
 }
 
-template <int D, bool DS_OUT, bool BIAS>
+template <int D, bool DS_OUT, bool BIAS, bool QAT = false>
 static cudaError_t set_main_smem() {
-  return cudaFuncSetAttribute(sdpa_bwd_main<D, DS_OUT, BIAS>,
+  return cudaFuncSetAttribute(sdpa_bwd_main<D, DS_OUT, BIAS, QAT>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, MainLayout<D, DS_OUT>::BYTES);
 }
 

@@ -218,6 +218,54 @@ int sdpa_fwd_bias(const void* q, const void* k, const void* v, void* o, float* l
                   const int32_t* seq_kv_lens, const float* sink, const void* bias, int bias_dtype,
                   int bias_batch, void* stream);
 
+/*
+ * NVFP4 fake quantization ("NVFP4 Attention QAT Backward" page, Overview):
+ * y = fake_nvfp4(x) for n contiguous bf16 values, in blocks of 16 consecutive
+ * values. A block's local scale is s = E4M3(amax / 6), amax its largest
+ * magnitude; each value becomes E2M1(x / s) * s (0 when s is 0). Both
+ * divisions are correctly rounded fp32 divisions; E4M3 and E2M1 roundings go to
+ * the nearest value, ties to even, saturating at 448 and 6. Every result is
+ * exact in bf16. For a (..., D) tensor with D a multiple of 16 the blocks run
+ * along D.
+ *   x, y    device bf16 buffers of n values, 16-byte aligned (may be equal).
+ *   n       a multiple of 16 (>= 0).
+ * Returns SDPA_ERR_INVALID for NULL pointers or n not a multiple of 16,
+ * SDPA_ERR_ALIGN for misaligned pointers; enqueued on `stream`.
+ */
+int sdpa_nvfp4_fake_quant(const void* x, void* y, long long n, void* stream);
+
+/*
+ * Bytes of workspace sdpa_bwd_nvfp4_qat() needs: sdpa_bwd_workspace_size()'s
+ * regions (non-deterministic route) plus bf16 copies of the fake-quantized Q,
+ * K and V. Returns 0 for arguments sdpa_bwd_nvfp4_qat() would reject.
+ */
+size_t sdpa_bwd_nvfp4_qat_workspace_size(int B, int H_q, int H_kv, int S_q, int S_kv, int D_qk,
+                                         int D_v);
+
+/*
+ * NVFP4 QAT backward ("NVFP4 Attention QAT Backward" page, Overview): with
+ * Q^, K^, V^ the fake-quantized Q, K, V (sdpa_nvfp4_fake_quant),
+ *     P  = exp(scale * Q^ K^^T - LSE),   dS = P * (dO V^^T - rowsum(O_hp * dO)),
+ *     dQ = scale * dS K^,   dK = scale * dS^T Q^,   dV = fake_nvfp4(P)^T dO,
+ * where dQ and dK use P itself (straight-through estimator) and dV uses P
+ * fake-quantized in blocks of 16 consecutive keys of each query row (blocks
+ * start at key 0; masked entries count as 0).
+ * Arguments as sdpa_bwd() (no deterministic flag: the dQ-reduction route), with
+ *   q, k, v   the unquantized bf16 activations (the library quantizes them
+ *             into the workspace first).
+ *   o_hp      the high-precision forward output softmax(scale Q^ K^^T) V^,
+ *             i.e. sdpa_fwd() of the fake-quantized inputs, and lse its LSE.
+ *   workspace >= sdpa_bwd_nvfp4_qat_workspace_size() bytes, or NULL.
+ * Served for D_qk = D_v = 128 (SDPA_ERR_UNSUPPORTED otherwise), with every
+ * mask, padding and GQA of sdpa_bwd(). Returns as sdpa_bwd().
+ */
+int sdpa_bwd_nvfp4_qat(const void* q, const void* k, const void* v, const void* o_hp,
+                       const void* d_o, const float* lse, void* dq, void* dk, void* dv, int B,
+                       int H_q, int H_kv, int S_q, int S_kv, int D_qk, int D_v, float scale,
+                       int causal, int bottom_right, int window_left, int window_right,
+                       const int32_t* seq_q_lens, const int32_t* seq_kv_lens, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* sdpa_status_string(int status);
 
@@ -234,9 +282,11 @@ int sdpa_bwd_check_device_status(void* stream);
  * events around each launch and synchronizes the stream before returning, so
  * it is for measurement only. sdpa_bwd_profile_read() fills up to n entries of
  * ms[] (total milliseconds) and launches[] (count) per kernel in the order
- * preprocess, main, dq (the dQ convert, or on the two-kernel route the
+ * preprocess (with, for sdpa_bwd_nvfp4_qat(), the fake quantization of Q, K
+ * and V before it), main, dq (the dQ convert, or on the two-kernel route the
  * dQ = scale * dS K kernel; under GQA it also runs the dK/dV group
- * reduction), and returns the number of kernels (3).
+ * reduction), and returns the number of entries (3). sdpa_bwd_sink(),
+ * sdpa_bwd_bias() and sdpa_bwd_nvfp4_qat() are timed the same way.
  * Enabling resets the totals.
  */
 int sdpa_bwd_profile_enable(int on);

@@ -215,3 +215,27 @@ def test_forward_bias_argument_validation(lib):
     assert call(FAKE, batch=2, B=3) == INVALID
     assert call(FAKE + 1, dtype=0) == ALIGN
     assert call(FAKE + 2, dtype=1) == ALIGN
+
+
+def test_nvfp4_qat_argument_validation(lib):
+    lib.sdpa_bwd_nvfp4_qat.restype = ctypes.c_int
+    lib.sdpa_nvfp4_fake_quant.restype = ctypes.c_int
+    lib.sdpa_bwd_nvfp4_qat_workspace_size.restype = ctypes.c_size_t
+    vp = [ctypes.c_void_p(FAKE)] * 9
+
+    def call(Dqk=128, Dv=128, Hq=2, Hkv=2):
+        return lib.sdpa_bwd_nvfp4_qat(*vp, 1, Hq, Hkv, 128, 128, Dqk, Dv, ctypes.c_float(0.0), 1, 0,
+                                      -1, -1, None, None, None, ctypes.c_size_t(0), None)
+    assert call(Dqk=64, Dv=64) == UNSUPPORTED       # D = 128 only
+    assert call(Dqk=192, Dv=128) == UNSUPPORTED
+    assert call(Hq=3, Hkv=2) == INVALID
+    fq = lib.sdpa_nvfp4_fake_quant
+    assert fq(ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), ctypes.c_longlong(17), None) == INVALID
+    assert fq(None, ctypes.c_void_p(FAKE), ctypes.c_longlong(16), None) == INVALID
+    assert fq(ctypes.c_void_p(FAKE + 8), ctypes.c_void_p(FAKE), ctypes.c_longlong(16), None) == ALIGN
+    assert fq(ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), ctypes.c_longlong(0), None) == OK
+    # workspace: the plain chain's regions plus bf16 copies of Q, K and V
+    ws = lib.sdpa_bwd_nvfp4_qat_workspace_size(1, 2, 2, 128, 128, 128, 128)
+    base = lib.sdpa_bwd_workspace_size(1, 2, 2, 128, 128, 128, 128, 0)
+    assert ws == base + 3 * 2 * 128 * 128 * 2
+    assert lib.sdpa_bwd_nvfp4_qat_workspace_size(1, 2, 2, 128, 128, 64, 64) == 0

@@ -567,3 +567,106 @@ def test_forward_then_backward_with_bias(name):
     assert_close("dk", dk.double().cpu().numpy(), rk)
     assert_close("dv", dv.double().cpu().numpy(), rv)
     assert_close("dbias", dbias.double().cpu().numpy(), oracle_dbias(case))
+
+
+# ---------------------------------------------------------------- NVFP4 QAT
+# The fake quantization is a rounding: the GPU's must equal the oracle's bit
+# for bit. The QAT backward (quantized Q, K, V in the GEMMs, P fake-quantized
+# over 16-key blocks for dV only) is checked against the oracle's with the
+# gradient bar; O_hp / LSE come from the oracle's QAT forward.
+def test_nvfp4_fake_quant_bitwise():
+    import attention_backward_sdpa_gb300 as pkg
+    import oracle
+    g = torch.Generator("cpu").manual_seed(50)
+    n_blocks = 8192
+    mag = 10.0 ** (torch.rand(n_blocks, 1, generator=g) * 10 - 6)   # 1e-6 .. 1e4 per block
+    x = (torch.randn(n_blocks, 16, generator=g) * mag)
+    x[:64] = 0.0                                                      # zero blocks
+    x[64:128] *= 1e6                                                  # saturated scales
+    x[128:192, :8] = 0.0                                              # half-empty blocks
+    xb = x.to(torch.bfloat16)
+    y = pkg.nvfp4_fake_quant(xb.cuda()).cpu()
+    ref64 = torch.from_numpy(oracle.fake_nvfp4(xb.double().numpy()))
+    ref = ref64.to(torch.bfloat16)
+    assert torch.equal(ref.double(), ref64)  # every fake-quantized value is exact in bf16
+    diff = (y.view(torch.int16) != ref.view(torch.int16)).nonzero()
+    assert diff.numel() == 0, f"{diff.shape[0]} values differ, first at {diff[:4].tolist()}"
+
+
+QAT_CASES = {
+    "mha_causal_ragged": W("qat_mha_causal", 1, 2, 2, 300, 300, 128, 128, causal=True, seed=51),
+    "mha_dense_cross": W("qat_mha_dense", 2, 2, 2, 190, 250, 128, 128, seed=52),
+    "gqa_causal": W("qat_gqa", 1, 4, 2, 256, 256, 128, 128, causal=True, seed=53),
+    "padded_window": W("qat_padded_window", 2, 2, 2, 300, 300, 128, 128, causal=True,
+                       window_left=100, padded=(100, 300), seed=54),
+}
+
+
+def _qat_case(w):
+    import oracle
+    from harness import f64
+    t = workloads.generate(w)
+    p = oracle.Problem(
+        w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.Dqk, w.Dv, scale=w.resolved_scale, causal=w.causal,
+        bottom_right=w.bottom_right, window_left=w.window_left, window_right=w.window_right,
+        seq_q_lens=None if t["seq_q_lens"] is None else t["seq_q_lens"].numpy(),
+        seq_kv_lens=None if t["seq_kv_lens"] is None else t["seq_kv_lens"].numpy())
+    o_hp, lse, _ = oracle.qat_forward(p, f64(t["q"]), f64(t["k"]), f64(t["v"]))
+    t["o"] = torch.from_numpy(o_hp).to(torch.bfloat16)
+    t["lse"] = torch.from_numpy(lse).float()
+    t["problem"], t["workload"] = p, w
+    return t
+
+
+def _gpu_qat(case, d):
+    import attention_backward_sdpa_gb300 as pkg
+    w = case["workload"]
+    nan = float("nan")
+    out = pkg.sdpa_bwd_nvfp4_qat(d["q"], d["k"], d["v"], d["o"], d["do"], d["lse"],
+                                 scale=w.resolved_scale, causal=w.causal,
+                                 bottom_right=w.bottom_right, window_left=w.window_left,
+                                 window_right=w.window_right, seq_q_lens=d["seq_q_lens"],
+                                 seq_kv_lens=d["seq_kv_lens"], dq=torch.full_like(d["q"], nan),
+                                 dk=torch.full_like(d["k"], nan), dv=torch.full_like(d["v"], nan))
+    pkg.check_device_status()
+    return out
+
+
+@pytest.mark.parametrize("name", sorted(QAT_CASES))
+def test_nvfp4_qat_parity(name):
+    import oracle
+    from harness import f64
+    case = _qat_case(QAT_CASES[name])
+    d = to_device(case)
+    dq, dk, dv = _gpu_qat(case, d)
+    rq, rk, rv = oracle.qat_backward(case["problem"], f64(case["q"]), f64(case["k"]), f64(case["v"]),
+                                     f64(case["o"]), f64(case["do"]), case["lse"].double().numpy())
+    assert_close("dq", dq.double().cpu().numpy(), rq)
+    assert_close("dk", dk.double().cpu().numpy(), rk)
+    assert_close("dv", dv.double().cpu().numpy(), rv)
+    # dV really used the quantized P: the plain backward's dV is further away
+    _, _, pv = oracle.backward(case["problem"], oracle.fake_nvfp4(f64(case["q"])),
+                               oracle.fake_nvfp4(f64(case["k"])), oracle.fake_nvfp4(f64(case["v"])),
+                               f64(case["o"]), f64(case["do"]), case["lse"].double().numpy())
+    g = dv.double().cpu().numpy()
+    assert np.linalg.norm(g - rv) < 0.5 * np.linalg.norm(g - pv)
+
+
+def test_nvfp4_qat_forward_then_backward():
+    """Fake quantization and sdpa_fwd on the GPU give O_hp / LSE; the QAT
+    backward on them matches the oracle's QAT forward + backward."""
+    import attention_backward_sdpa_gb300 as pkg
+    import oracle
+    from harness import f64
+    case = _qat_case(QAT_CASES["gqa_causal"])
+    w = case["workload"]
+    d = to_device(case)
+    o, lse = pkg.sdpa_fwd_nvfp4_qat(d["q"], d["k"], d["v"], scale=w.resolved_scale, causal=w.causal)
+    _check_fwd(case, o, lse)
+    d["o"], d["lse"] = o, lse
+    dq, dk, dv = _gpu_qat(case, d)
+    rq, rk, rv = oracle.qat_backward(case["problem"], f64(case["q"]), f64(case["k"]), f64(case["v"]),
+                                     f64(case["o"]), f64(case["do"]), case["lse"].double().numpy())
+    assert_close("dq", dq.double().cpu().numpy(), rq)
+    assert_close("dk", dk.double().cpu().numpy(), rk)
+    assert_close("dv", dv.double().cpu().numpy(), rv)
