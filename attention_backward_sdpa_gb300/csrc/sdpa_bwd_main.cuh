@@ -35,10 +35,9 @@
 // arrive already fake-quantized, so the GEMMs are unchanged; dS (hence dQ and
 // dK) uses P itself (straight-through), while G3 takes P fake-quantized to
 // NVFP4 in blocks of 16 consecutive keys of each query: the 16 keys of a block
-// are 16 lanes of one warp, whose maximum one warp reduction gives. The local
-// scale amax/6 and each value's division by it are correctly rounded fp32
-// divisions; the E4M3 and E2M1 roundings are the hardware conversions
-// (round to nearest even, saturating).
+// are 16 lanes of one warp (block maxima by shuffles, p_block_scales). The E4M3
+// and E2M1 roundings are the hardware conversions (round to nearest even,
+// saturating).
 //
 // Schedule. Two query tiles are in flight: tensor memory holds two slots, each
 // with S^T and dP^T (dQ^T reuses the dP^T columns once dS is formed). Compute
@@ -138,14 +137,59 @@ struct MainLayout {
 
 __device__ __forceinline__ void set_main_status(int* status, int bit) { atomicOr(status, bit); }
 
-// Largest value of `v` (>= 0) over this lane's 16-lane half of the warp (all
-// lanes take part): non-negative floats order like their bit patterns.
-__device__ __forceinline__ float half_warp_max_nonneg(float v, bool upper) {
-  uint32_t lo, hi;
-  const uint32_t x = __float_as_uint(v);
-  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(lo) : "r"(upper ? 0u : x));
-  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(hi) : "r"(upper ? x : 0u));
-  return __uint_as_float(upper ? hi : lo);
+// NVFP4 local scales of P's 16-key blocks for all BQ (= 64) query columns of
+// this lane's key: the 16 keys of a block are the 16 lanes of one half warp
+// (l = lane & 15). Four rounds of recursive halving (exchange half of the
+// columns with lane l ^ o, keep the maxima of the other half) leave lane l with
+// the block maxima of columns 4l .. 4l+3; it turns them into scales,
+// E4M3(amax / 6) with a correctly rounded division, and four rounds of
+// recursive doubling hand every lane all 64 scales. (A half-warp reduction
+// instruction per column measured four times slower.)
+__device__ __forceinline__ void p_block_scales(const float (&P)[BQ], float (&sc)[BQ], int l) {
+  static_assert(BQ == 64, "four halving rounds take 64 columns to 4");
+#pragma unroll
+  for (int i = 0; i < BQ; ++i) sc[i] = P[i];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int o = 8 >> r, n = BQ >> r;
+    const bool up = (l & o) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = up ? sc[i] : sc[i + n / 2];
+      const float keep = up ? sc[i + n / 2] : sc[i];
+      sc[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, o));
+    }
+  }
+  const float2 s01 = nvfp4_scales(sc[0], sc[1]), s23 = nvfp4_scales(sc[2], sc[3]);
+  sc[0] = s01.x;
+  sc[1] = s01.y;
+  sc[2] = s23.x;
+  sc[3] = s23.y;
+#pragma unroll
+  for (int r = 3; r >= 0; --r) {
+    const int o = 8 >> r, n = 4 << (3 - r);
+    const bool up = (l & o) != 0;
+#pragma unroll
+    for (int i = 0; i < n; ++i) {
+      const float recv = __shfl_xor_sync(0xffffffffu, sc[i], o);
+      const float own = sc[i];
+      sc[i] = up ? recv : own;
+      sc[i + n] = up ? own : recv;
+    }
+  }
+}
+
+// Fake NVFP4 of two P values with their blocks' scales. P is itself the
+// ex2.approx replay of the softmax, so each value's division by its scale is a
+// product with the reciprocal (within an ulp or two of the correctly rounded
+// quotient; an E2M1 rounding can differ only for a value that close to a
+// rounding boundary, well inside P's own error).
+__device__ __forceinline__ uint32_t fake_nvfp4_p_pair(float p0, float p1, float s0, float s1) {
+  float r0, r1;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r0) : "f"(s0));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r1) : "f"(s1));
+  const float2 q = round_e2m1x2(s0 > 0.f ? p0 * r0 : 0.f, s1 > 0.f ? p1 * r1 : 0.f);
+  return pack_bf16x2(q.x * s0, q.y * s1);
 }
 
 // Bias column of one query tile for this thread's key: bz[i] = bias(q0 + i, k)
@@ -692,18 +736,17 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
           if (row_dead || q < q_lo_vis || q > q_hi_vis) P[i] = 0.f;
         }
       }
+      // QAT: G3 reads P fake-quantized over blocks of 16 keys (16 lanes).
+      float psc[QAT ? BQ : 1];
+      if constexpr (QAT) p_block_scales(P, psc, lane & 15);
 #pragma unroll
       for (int c16 = 0; c16 < 2; ++c16) {
         uint32_t w[16];
         if constexpr (QAT) {
-          // G3 reads P fake-quantized over blocks of 16 keys (16 lanes).
-          const bool upper = (lane & 16) != 0;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float p0 = P[c16 * 32 + 2 * i], p1 = P[c16 * 32 + 2 * i + 1];
-            const float2 sc = nvfp4_scales(half_warp_max_nonneg(p0, upper), half_warp_max_nonneg(p1, upper));
-            w[i] = fake_nvfp4_pair_bf16(p0, p1, sc.x, sc.y);
-          }
+          for (int i = 0; i < 16; ++i)
+            w[i] = fake_nvfp4_p_pair(P[c16 * 32 + 2 * i], P[c16 * 32 + 2 * i + 1], psc[c16 * 32 + 2 * i],
+                                     psc[c16 * 32 + 2 * i + 1]);
         } else {
 #pragma unroll
           for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(P[c16 * 32 + 2 * i], P[c16 * 32 + 2 * i + 1]);

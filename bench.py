@@ -214,8 +214,10 @@ def oracle_forward_inputs(w, t):
     import oracle
     p = _problem(w, t["seq_q_lens"])
     bias = t.get("bias")
-    o64, lse64 = oracle.forward(p, t["q"].double().numpy(), t["k"].double().numpy(),
-                                t["v"].double().numpy(),
+    q64, k64, v64 = (t[x].double().numpy() for x in ("q", "k", "v"))
+    if t.get("qat"):  # NVFP4 QAT: the high-precision O of the fake-quantized inputs
+        q64, k64, v64 = oracle.fake_nvfp4(q64), oracle.fake_nvfp4(k64), oracle.fake_nvfp4(v64)
+    o64, lse64 = oracle.forward(p, q64, k64, v64,
                                 bias=None if bias is None else bias.double().numpy())
     return torch.from_numpy(o64).to(torch.bfloat16), torch.from_numpy(lse64).float()
 
@@ -240,7 +242,9 @@ def oracle_backward_sample(w, t, o, lse, groups):
             os_.double().numpy(), sl["do"].double().numpy(), ls.double().numpy()]
     bias = t.get("bias")
     t0 = time.perf_counter()
-    if bias is None:
+    if t.get("qat"):
+        oracle.qat_backward(p, *args)
+    elif bias is None:
         oracle.backward(p, *args)
     else:  # the biased backward plus dBias, on the sample's heads
         b64 = bias[:, :hq].contiguous().double().numpy()
@@ -443,7 +447,20 @@ def run_gpu(args, w, t, o, lse, rank, world, device):
     def call_kw():
         return dict(kw, bias=d["bias"]) if "bias" in d else kw
 
+    qat_ws = None
+    if t.get("qat"):
+        qat_ws = torch.empty(max(pkg.nvfp4_qat_workspace_size(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.Dqk,
+                                                              w.Dv), 256), dtype=torch.uint8,
+                             device=device)
+
     def step():
+        if qat_ws is not None:
+            pkg.sdpa_bwd_nvfp4_qat(d["q"], d["k"], d["v"], d["o"], d["do"], d["lse"],
+                                   scale=w.resolved_scale, causal=w.causal,
+                                   bottom_right=w.bottom_right, window_left=w.window_left,
+                                   window_right=w.window_right, seq_q_lens=lq, seq_kv_lens=lk,
+                                   dq=dq, dk=dk, dv=dv, workspace=qat_ws)
+            return
         pkg.sdpa_bwd(d["q"], d["k"], d["v"], d["o"], d["do"], d["lse"], **call_kw())
 
     def timed_loop(n, profile=False):
@@ -525,7 +542,7 @@ def run_gpu(args, w, t, o, lse, rank, world, device):
         "e2e": {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "clocks": clocks.summary(),
-        "gpu_launches": (4 if args.sink else 3) * args.steps,
+        "gpu_launches": (4 if args.sink else 6 if t.get("qat") else 3) * args.steps,
     }
 
 
@@ -573,6 +590,9 @@ def main(argv=None):
                     help="add a bias of B batches or 1 shared batch: sdpa_bwd_bias (dBias written "
                          "in fp32), or sdpa_fwd_bias with --pass fwd")
     ap.add_argument("--bias-dtype", default="bf16", choices=["bf16", "f32"])
+    ap.add_argument("--qat", action="store_true",
+                    help="time sdpa_bwd_nvfp4_qat (NVFP4 fake-quantized Q/K/V, P fake-quantized "
+                         "for dV; D = 128, non-deterministic)")
     ap.add_argument("--pass", dest="pass_", default="bwd", choices=["bwd", "fwd"],
                     help="bwd: the backward chain (default); fwd: sdpa_fwd, the forward (O, LSE)")
     ap.add_argument("--no-cpu-baseline", action="store_true",
@@ -588,6 +608,11 @@ def main(argv=None):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     t = workloads.generate(w)
+    if args.qat:
+        if w.Dqk != 128 or w.Dv != 128 or w.deterministic or args.bias != "none" or args.sink \
+                or args.pass_ != "bwd":
+            ap.error("--qat: a D = 128 non-deterministic workload, backward, no bias or sink")
+        t["qat"] = True
     if args.bias != "none":
         t["bias"] = workloads.bias_tensor(w, 1 if args.bias == "1" else w.B,
                                           torch.float32 if args.bias_dtype == "f32" else torch.bfloat16)
@@ -632,7 +657,7 @@ def result_line(args, w, world, r, cb, metric):
                        "S_kv": w.Skv, "D_qk": w.Dqk, "D_v": w.Dv, "causal": w.causal,
                        "bottom_right": w.bottom_right, "window_left": w.window_left,
                        "deterministic": w.deterministic, "seed": w.seed,
-                       "pass": args.pass_, "sink": bool(args.sink),
+                       "pass": args.pass_, "sink": bool(args.sink), "nvfp4_qat": bool(args.qat),
                        "bias": None if args.bias == "none" else
                        {"batch": args.bias, "dtype": args.bias_dtype, "dbias": "f32"},
                        "gflop_per_step": r["flops"] / 1e9,

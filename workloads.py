@@ -60,6 +60,10 @@ WORKLOADS: Dict[str, Workload] = {
                                   padded=(512, 4096), seed=3),
     "mla_br_causal": Workload("mla_br_causal", B=1, Hq=16, Hkv=16, Sq=4096, Skv=4096, Dqk=192,
                               Dv=128, causal=True, bottom_right=True, seed=4),
+    # The NVFP4 QAT backward page's example shape (BHSD (1, 16, 4096, 128),
+    # non-causal), for the QAT path; not one of the five above.
+    "qat_dense": Workload("qat_dense", B=1, Hq=16, Hkv=16, Sq=4096, Skv=4096, Dqk=128, Dv=128,
+                          seed=5),
 }
 
 ORDER = ["tiny_dense", "causal_mha", "causal_gqa_det", "swa_causal_padded", "mla_br_causal"]
