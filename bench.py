@@ -379,13 +379,15 @@ def cpu_baseline_leg(w, t, target_s=12.0):
 # valid only for the kernel sources they were taken on: the digest covers the
 # kernel's source files, and a changed kernel reports null. D_qk = 192 runs
 # sdpa_bwd_main_ds, every other head dim sdpa_bwd_main.
-MAIN_SOURCES = {"sdpa_bwd_main": ("sdpa_bwd_main.cuh", "common.cuh", "ptx.cuh"),
+MAIN_SOURCES = {"sdpa_bwd_main": ("sdpa_bwd_main.cuh", "common.cuh", "ptx.cuh", "nvfp4.cuh"),
                 "sdpa_bwd_main_ds": ("sdpa_bwd_main_ds.cu", "common.cuh", "ptx.cuh")}
 MAIN_TRAFFIC = {
-    "fa34d64d4753c107": {"causal_mha": 114246144 + 31919360,
-                         "causal_gqa_det": 134530048 + 515341568,
-                         "swa_causal_padded": 245091328 + 185813248},
-    "25168dca819c0205": {"mla_br_causal": 132380928 + 263462144},
+    "8126bd09ad511676": {"causal_mha": 114586624 + 31854336,
+                         "causal_gqa_det": 135143936 + 515680512,
+                         "swa_causal_padded": 245902336 + 185991680,
+                         "causal_mha/bias-B-f32": 468585216 + 584235520,
+                         "causal_mha/qat": 113126656 + 29260544},
+    "1a2f7841b4750af2": {"mla_br_causal": 132356352 + 263149824},
 }
 
 
@@ -401,7 +403,10 @@ def main_traffic(w, tag=None):
 
 
 def bias_tag(t):
-    """'bias-<batch>-<dtype>' for a biased run (the traffic table's key suffix), else None."""
+    """The traffic table's key suffix: 'bias-<batch>-<dtype>' for a biased run,
+    'qat' for the NVFP4 QAT backward, else None."""
+    if t.get("qat"):
+        return "qat"
     b = t.get("bias")
     if b is None:
         return None
