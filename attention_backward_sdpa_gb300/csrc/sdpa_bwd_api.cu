@@ -294,7 +294,6 @@ int run_chain(const void* q, const void* k, const void* v, const void* o, const 
     if (reinterpret_cast<uintptr_t>(ba.bias) % (ba.dtype == SDPA_DTYPE_F32 ? 4 : 2) != 0 ||
         reinterpret_cast<uintptr_t>(ba.dbias) % 4 != 0)
       return SDPA_ERR_ALIGN;
-    if (D_qk == 192) return SDPA_ERR_UNSUPPORTED;
   }
   for (const void* ptr : {q, k, v, o, d_o, (const void*)dq, (const void*)dk, (const void*)dv})
     if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return SDPA_ERR_ALIGN;

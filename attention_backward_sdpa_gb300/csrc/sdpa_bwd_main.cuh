@@ -73,6 +73,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include "bias.cuh"
 #include "common.cuh"
 #include "nvfp4.cuh"
 #include "ptx.cuh"
@@ -190,83 +191,6 @@ __device__ __forceinline__ uint32_t fake_nvfp4_p_pair(float p0, float p1, float 
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r1) : "f"(s1));
   const float2 q = round_e2m1x2(s0 > 0.f ? p0 * r0 : 0.f, s1 > 0.f ? p1 * r1 : 0.f);
   return pack_bf16x2(q.x * s0, q.y * s1);
-}
-
-// Bias column of one query tile for this thread's key: bz[i] = bias(q0 + i, k)
-// (0 past S_q or S_kv). `off` is the element offset of (batch row, head, q0, k).
-template <int N>
-__device__ __forceinline__ void load_bias_column(const ChainParams& p, long long off, bool key_in,
-                                                 int q0, float (&bz)[N]) {
-  const long long ld = p.Skv;
-  const int rows = key_in ? min(N, p.Sq - q0) : 0;
-  if (p.bias_fp32) {
-    const float* src = static_cast<const float*>(p.bias) + off;
-    if (rows == N) {
-#pragma unroll
-      for (int i = 0; i < N; ++i) bz[i] = __ldcs(src + i * ld);
-    } else {
-#pragma unroll
-      for (int i = 0; i < N; ++i) bz[i] = i < rows ? __ldcs(src + i * ld) : 0.f;
-    }
-  } else {
-    const unsigned short* src = static_cast<const unsigned short*>(p.bias) + off;
-    if (rows == N) {
-#pragma unroll
-      for (int i = 0; i < N; ++i) bz[i] = __uint_as_float((uint32_t)__ldcs(src + i * ld) << 16);
-    } else {
-#pragma unroll
-      for (int i = 0; i < N; ++i)
-        bz[i] = i < rows ? __uint_as_float((uint32_t)__ldcs(src + i * ld) << 16) : 0.f;
-    }
-  }
-}
-
-// Zeros `rows` rows of `cols` floats, `ld` floats apart, with threads
-// thr = 0 .. nthr-1 (nthr a multiple of 32). A full 128-column block row is 32
-// 16-byte stores, one per lane of a warp; other shapes take scalar stores.
-__device__ __forceinline__ void zero_float_rows(float* base, int rows, int cols, long long ld, int thr,
-                                                int nthr) {
-  if (cols == BN && (reinterpret_cast<uintptr_t>(base) & 15u) == 0 && (ld & 3) == 0) {
-    const int rstep = nthr >> 5, c = (thr & 31) * 4;
-    for (int r = thr >> 5; r < rows; r += rstep)
-      *reinterpret_cast<float4*>(base + (long long)r * ld + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-  } else {
-    for (int r = 0; r < rows; ++r)
-      for (int c = thr; c < cols; c += nthr) base[(long long)r * ld + c] = 0.f;
-  }
-}
-
-// Per-batch dBias: zeros of the (query tile, key tile kt) blocks of query heads
-// bh0 .. bh0 + gsz - 1 whose query tile lies outside [qt_lo, qt_hi], i.e. the
-// blocks of this key tile that no CTA computes.
-__device__ inline void zero_unvisited_dbias_blocks(const ChainParams& p, int b, int bh0, int gsz, int kt,
-                                                   int qt_lo, int qt_hi, int thr, int nthr) {
-  const int k0 = kt * BN, cols = min(BN, p.Skv - k0);
-  for (int hj = 0; hj < gsz; ++hj) {
-    const int hq = bh0 + hj - b * p.Hq;
-    for (int qt = 0; qt < p.n_qt; ++qt) {
-      if (qt >= qt_lo && qt <= qt_hi) continue;
-      const int q0 = qt * BQ;
-      zero_float_rows(p.dbias + (long long)b * p.dbias_bstride + ((long long)hq * p.Sq + q0) * p.Skv + k0,
-                      min(BQ, p.Sq - q0), cols, p.Skv, thr, nthr);
-    }
-  }
-}
-
-// L2 prefetch of one BQ x BN bias tile (rows q0.., keys k0..) by 128 threads:
-// each takes one (bf16) or two (fp32) of its 128-byte lines.
-__device__ __forceinline__ void prefetch_bias_tile(const ChainParams& p, long long tile_off, int q0,
-                                                   int k0, int thread) {
-  const int esz = p.bias_fp32 ? 4 : 2;
-  const int lines_per_row = BN * esz / 128;
-  for (int line = thread; line < BQ * lines_per_row; line += 128) {
-    const int r = line / lines_per_row, key = (line % lines_per_row) * (128 / esz);
-    if (q0 + r < p.Sq && k0 + key < p.Skv) {
-      const char* a = static_cast<const char*>(p.bias) +
-                      (tile_off + (long long)r * p.Skv + key) * esz;
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
-    }
-  }
 }
 
 // DS_OUT selects the deterministic two-kernel route: instead of G5 and the dQ

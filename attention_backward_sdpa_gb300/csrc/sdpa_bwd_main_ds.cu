@@ -24,6 +24,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include "bias.cuh"
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -94,7 +95,11 @@ struct Layout {
 
 }  // namespace ds_kernel
 
-template <int DQK, int DV>
+// BIAS: the additive bias in the replay and the fp32 dBias output, as in the
+// D_qk 64/128 kernel (bias.cuh): loads of the next tile's bias column issued
+// right after dS, dS' stored as dBias, and the dBias blocks no CTA computes
+// zeroed by an idle warp (or by an empty unit's whole CTA).
+template <int DQK, int DV, bool BIAS>
 __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
     sdpa_bwd_main_ds(const __grid_constant__ MainMaps maps, const ChainParams p) {
   using namespace ds_kernel;
@@ -131,6 +136,8 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
       if (!row_has_visible_pair(Lq0, Lk0))
         zero_key_tile_rows<DQK, DV>(p, p.dk_ws ? (long long)bh0 : (long long)b0 * p.Hkv + (bh0 % p.Hq) / p.G,
                                     kt0 * BN);
+      if (BIAS && p.dbias != nullptr && !p.dbias_red)
+        zero_unvisited_dbias_blocks(p, b0, bh0, 1, kt0, lo0, hi0, threadIdx.x, blockDim.x);
       return;
     }
   }
@@ -330,7 +337,10 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
     // set of a query head is its bh index).
     zero_group_share_of_empty_key_tiles<DQK, DV>(p, p.dk_ws ? (long long)bh : (long long)b * p.Hkv + hk,
                                                  kt, Lq, Lk, lane);
-  }  // warps 14-15: idle members of the fourth warpgroup
+  } else if (BIAS && warp == 14) {
+    // The dBias blocks of this key tile that no CTA computes.
+    if (p.dbias != nullptr && !p.dbias_red) zero_unvisited_dbias_blocks(p, b, bh, 1, kt, qt_lo, qt_hi, lane, 32);
+  }  // warp 15 (and 14 without a bias): idle members of the fourth warpgroup
   } else {
     regs_increase<ds_kernel::REGS_COMPUTE>();
     // ------------------------------------------------------------ compute warpgroups
@@ -346,10 +356,25 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
     uint8_t* ds_row = sDS + slot * L::TILE_DS + row * 128;
     float P[BQ];
     bool ok = true;
+    constexpr float LOG2E_F = 1.4426950408889634f;
+    const bool key_in = k < p.Skv;
+    // Bias (BIAS): element offset of (head, first query, this key) of tile t
+    // inside one batch, and that tile's column of this thread's key.
+    auto bias_tile_off = [&](int tt) -> long long {
+      return ((long long)h * p.Sq + (qt_hi - tt) * BQ) * p.Skv + k;
+    };
+    float bz[BIAS ? BQ : 1];
+    if constexpr (BIAS) {
+      if (slot < n)
+        load_bias_column(p, (long long)b * p.bias_bstride + bias_tile_off(slot), key_in, (qt_hi - slot) * BQ, bz);
+      else
+        for (int i = 0; i < BQ; ++i) bz[i] = 0.f;
+    }
     for (int t = slot; t < n && ok; t += 2) {
       const int j = t >> 1, st = t % NQ;
       const int qt = qt_hi - t, q0 = qt * BQ;
       const float* qs = sQS + st * QSTAT_FLOATS;
+      const long long bias_off = BIAS ? bias_tile_off(t) : 0;
       const bool need_mask = (k0 + BN > Lk) ||
                              (p.causal && (long long)q0 < (long long)(k0 + BN - 1) - diag - Rp) ||
                              (has_window && (long long)(q0 + BQ - 1) > (long long)k0 - diag + p.window_left);
@@ -371,10 +396,16 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
           const float4 l = lse4[i4];
           const uint32_t* r = i4 < 8 ? ra : rb;
           const int i = (i4 & 7) * 4;
-          P[i4 * 4 + 0] = ex2_approx(fmaf(__uint_as_float(r[i + 0]), p.scale_log2, -l.x));
-          P[i4 * 4 + 1] = ex2_approx(fmaf(__uint_as_float(r[i + 1]), p.scale_log2, -l.y));
-          P[i4 * 4 + 2] = ex2_approx(fmaf(__uint_as_float(r[i + 2]), p.scale_log2, -l.z));
-          P[i4 * 4 + 3] = ex2_approx(fmaf(__uint_as_float(r[i + 3]), p.scale_log2, -l.w));
+          float x[4] = {fmaf(__uint_as_float(r[i + 0]), p.scale_log2, -l.x),
+                        fmaf(__uint_as_float(r[i + 1]), p.scale_log2, -l.y),
+                        fmaf(__uint_as_float(r[i + 2]), p.scale_log2, -l.z),
+                        fmaf(__uint_as_float(r[i + 3]), p.scale_log2, -l.w)};
+          if constexpr (BIAS) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[e] = fmaf(bz[i4 * 4 + e], LOG2E_F, x[e]);
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) P[i4 * 4 + e] = ex2_approx(x[e]);
         }
       }
       if (need_mask) {
@@ -422,20 +453,49 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
           const int i = (chunk & 3) * 8;
           const float4 d0 = delta4[chunk * 2], d1 = delta4[chunk * 2 + 1];
           const int c = chunk * 8;
-          const uint32_t w0 = pack_bf16x2(P[c + 0] * (__uint_as_float(r[i + 0]) - d0.x),
-                                          P[c + 1] * (__uint_as_float(r[i + 1]) - d0.y));
-          const uint32_t w1 = pack_bf16x2(P[c + 2] * (__uint_as_float(r[i + 2]) - d0.z),
-                                          P[c + 3] * (__uint_as_float(r[i + 3]) - d0.w));
-          const uint32_t w2 = pack_bf16x2(P[c + 4] * (__uint_as_float(r[i + 4]) - d1.x),
-                                          P[c + 5] * (__uint_as_float(r[i + 5]) - d1.y));
-          const uint32_t w3 = pack_bf16x2(P[c + 6] * (__uint_as_float(r[i + 6]) - d1.z),
-                                          P[c + 7] * (__uint_as_float(r[i + 7]) - d1.w));
+          const float ds[8] = {P[c + 0] * (__uint_as_float(r[i + 0]) - d0.x),
+                               P[c + 1] * (__uint_as_float(r[i + 1]) - d0.y),
+                               P[c + 2] * (__uint_as_float(r[i + 2]) - d0.z),
+                               P[c + 3] * (__uint_as_float(r[i + 3]) - d0.w),
+                               P[c + 4] * (__uint_as_float(r[i + 4]) - d1.x),
+                               P[c + 5] * (__uint_as_float(r[i + 5]) - d1.y),
+                               P[c + 6] * (__uint_as_float(r[i + 6]) - d1.z),
+                               P[c + 7] * (__uint_as_float(r[i + 7]) - d1.w)};
+          const uint32_t w0 = pack_bf16x2(ds[0], ds[1]);
+          const uint32_t w1 = pack_bf16x2(ds[2], ds[3]);
+          const uint32_t w2 = pack_bf16x2(ds[4], ds[5]);
+          const uint32_t w3 = pack_bf16x2(ds[6], ds[7]);
           *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (row & 7)) << 4)) = make_uint4(w0, w1, w2, w3);
+          if constexpr (BIAS) {
+            if (p.dbias != nullptr && key_in) {
+              float* dst = p.dbias + (long long)b * p.dbias_bstride + bias_off + (long long)c * p.Skv;
+              const int rows_in = min(8, p.Sq - q0 - c);
+              if (p.dbias_red) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                  if (e < rows_in) atomicAdd(dst + (long long)e * p.Skv, ds[e]);
+              } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                  if (e < rows_in) __stcs(dst + (long long)e * p.Skv, ds[e]);
+              }
+            }
+          }
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bars[BAR_DSREADY + slot]);  // dP^T read, dS^T in shared memory
+      if constexpr (BIAS) {
+        // The next tile's bias column (unconditional, zeros past the last
+        // tile, so that the old values are dead here), the one after into L2.
+        const int tn = t + 2 < n ? t + 2 : t;
+        load_bias_column(p, (long long)b * p.bias_bstride + bias_tile_off(tn), key_in && t + 2 < n,
+                         (qt_hi - tn) * BQ, bz);
+        if (t + 4 < n)
+          prefetch_bias_tile(p, (long long)b * p.bias_bstride + bias_tile_off(t + 4) - k + k0,
+                             (qt_hi - t - 4) * BQ, k0, row);
+      }
     }
 
     // ---- epilogue: warpgroup 0 writes dV (D_v columns), warpgroup 1 scale * dK
@@ -496,19 +556,26 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
   }
 }
 
-template <int DQK, int DV>
+template <int DQK, int DV, bool BIAS>
 static cudaError_t set_ds_smem() {
-  return cudaFuncSetAttribute(sdpa_bwd_main_ds<DQK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(sdpa_bwd_main_ds<DQK, DV, BIAS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               ds_kernel::Layout<DQK, DV>::BYTES);
 }
 
-cudaError_t main_ds_kernel_setup() { return set_ds_smem<192, 128>(); }
+cudaError_t main_ds_kernel_setup() {
+  cudaError_t e = set_ds_smem<192, 128, false>();
+  if (e == cudaSuccess) e = set_ds_smem<192, 128, true>();
+  return e;
+}
 
 cudaError_t launch_main_ds(const MainMaps& maps, const ChainParams& p, cudaStream_t s) {
   const dim3 grid((unsigned)(p.n_kt * p.B * p.Hq));
   const dim3 block(ds_kernel::THREADS);
   if (p.Dqk != 192 || p.Dv != 128) return cudaErrorInvalidValue;
-  return launch_kernel(sdpa_bwd_main_ds<192, 128>, grid, block, ds_kernel::Layout<192, 128>::BYTES,
+  if (p.bias != nullptr)
+    return launch_kernel(sdpa_bwd_main_ds<192, 128, true>, grid, block,
+                         ds_kernel::Layout<192, 128>::BYTES, s, true, maps, p);
+  return launch_kernel(sdpa_bwd_main_ds<192, 128, false>, grid, block, ds_kernel::Layout<192, 128>::BYTES,
                        s, true, maps, p);
 }
 

@@ -160,10 +160,9 @@ int sdpa_bwd_sink(const void* q, const void* k, const void* v, const void* o, co
  *               reproducible; with bias_batch = 1 and B > 1 the batch rows
  *               add into it atomically (not reproducible), which deterministic
  *               mode rejects.
- * Served for D_qk = D_v = 64 or 128. Returns SDPA_ERR_INVALID for a NULL bias,
- * an unknown dtype, bias_batch not 1 or B, or the deterministic case above;
- * SDPA_ERR_UNSUPPORTED for D_qk = 192; otherwise as sdpa_bwd(). Workspace as
- * sdpa_bwd_workspace_size().
+ * Served for every head-dim pair of sdpa_bwd(). Returns SDPA_ERR_INVALID for a
+ * NULL bias, an unknown dtype, bias_batch not 1 or B, or the deterministic case
+ * above; otherwise as sdpa_bwd(). Workspace as sdpa_bwd_workspace_size().
  */
 int sdpa_bwd_bias(const void* q, const void* k, const void* v, const void* o, const void* d_o,
                   const float* lse, void* dq, void* dk, void* dv, int B, int H_q, int H_kv,

@@ -199,7 +199,7 @@ def test_bias_argument_validation(lib):
     assert call_bias(lib, FAKE + 1, dtype=0) == ALIGN         # bf16 bias: 2-byte alignment
     assert call_bias(lib, FAKE + 2, dtype=1) == ALIGN         # fp32 bias: 4-byte alignment
     assert call_bias(lib, FAKE, dbias=FAKE + 2) == ALIGN      # fp32 dBias: 4-byte alignment
-    assert call_bias(lib, FAKE, Dqk=192, Dv=128) == UNSUPPORTED
+    assert call_bias(lib, FAKE, Dqk=96, Dv=96) == UNSUPPORTED
 
 
 def test_forward_bias_argument_validation(lib):

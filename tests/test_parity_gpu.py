@@ -385,6 +385,11 @@ BIAS_CASES = {
     "single_key_d64_B_f32": (SMALL["single_key"], "B", torch.float32),
     "d128_dense_ragged_shared_bf16": (SMALL["d128_dense_ragged"], "1", torch.bfloat16),
     "br_causal_long_kv_B_f32": (SMALL["br_causal_long_kv"], "B", torch.float32),
+    # D_qk 192 / D_v 128 (the MLA kernel)
+    "mla_br_causal_ragged_B_bf16": (SMALL["mla_br_causal_ragged"], "B", torch.bfloat16),
+    "mla_dense_shared_f32": (SMALL["mla_dense"], "1", torch.float32),
+    "mla_gqa_window_B_f32": (SMALL["mla_gqa_window"], "B", torch.float32),
+    "mla_padded_det_B_bf16": (SMALL["mla_padded_det"], "B", torch.bfloat16),
 }
 
 
@@ -465,7 +470,7 @@ def test_bias_with_sink():
     _dsink_close(dsink.double().cpu().numpy(), ref, mag)
 
 
-@pytest.mark.parametrize("name", ["gqa_det_B_bf16", "det_d64_relay_B_f32"])
+@pytest.mark.parametrize("name", ["gqa_det_B_bf16", "det_d64_relay_B_f32", "mla_padded_det_B_bf16"])
 def test_dbias_bitwise_reproducible(name):
     """A per-batch dBias is written once per element: bitwise reproducible
     (10 runs), like dQ/dK/dV in deterministic mode."""
