@@ -66,6 +66,10 @@ def load(build_if_missing: bool = False):
     lib.sdpa_fwd.restype = i
     lib.sdpa_fwd_bias.argtypes = list(lib.sdpa_fwd.argtypes[:-1]) + [vp, i, i, vp]
     lib.sdpa_fwd_bias.restype = i
+    lib.sdpa_bwd_typed.argtypes = [i] + list(lib.sdpa_bwd.argtypes[:-1]) + [vp, vp, vp]
+    lib.sdpa_bwd_typed.restype = i
+    lib.sdpa_fwd_typed.argtypes = [i] + list(lib.sdpa_fwd.argtypes)
+    lib.sdpa_fwd_typed.restype = i
     lib.sdpa_nvfp4_fake_quant.argtypes = [vp, vp, ctypes.c_longlong, vp]
     lib.sdpa_nvfp4_fake_quant.restype = i
     lib.sdpa_bwd_nvfp4_qat_workspace_size.argtypes = [i, i, i, i, i, i, i]
@@ -108,13 +112,23 @@ def workspace_size(B, Hq, Hkv, Sq, Skv, Dqk, Dv, deterministic=False) -> int:
     return int(load().sdpa_bwd_workspace_size(B, Hq, Hkv, Sq, Skv, Dqk, Dv, int(deterministic)))
 
 
-def _check_bf16(name, t, shape):
+def _check_bf16(name, t, shape, dtype=torch.bfloat16):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
-        raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+    if t.dtype != dtype or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {dtype} CUDA tensor")
     if tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+# io element types of the C ABI (sdpa_dtype) for the typed entry points.
+_IO_CODES = {torch.bfloat16: 0, torch.float16: 2}
+
+
+def _io_dtype(q):
+    if not isinstance(q, torch.Tensor) or q.dtype not in _IO_CODES:
+        raise ValueError("q must be a bf16 or fp16 tensor")
+    return q.dtype
 
 
 def sdpa_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, do: torch.Tensor,
@@ -142,14 +156,15 @@ def sdpa_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
     lib = load()
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
         raise ValueError("q, k, v must be (B, H, S, D)")
+    io = _io_dtype(q)
     B, Hq, Sq, Dqk = q.shape
     Hkv, Skv = k.shape[1], k.shape[2]
     Dv = v.shape[3]
-    _check_bf16("q", q, (B, Hq, Sq, Dqk))
-    _check_bf16("k", k, (B, Hkv, Skv, Dqk))
-    _check_bf16("v", v, (B, Hkv, Skv, Dv))
-    _check_bf16("o", o, (B, Hq, Sq, Dv))
-    _check_bf16("do", do, (B, Hq, Sq, Dv))
+    _check_bf16("q", q, (B, Hq, Sq, Dqk), io)
+    _check_bf16("k", k, (B, Hkv, Skv, Dqk), io)
+    _check_bf16("v", v, (B, Hkv, Skv, Dv), io)
+    _check_bf16("o", o, (B, Hq, Sq, Dv), io)
+    _check_bf16("do", do, (B, Hq, Sq, Dv), io)
     if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous() \
             or lse.numel() != B * Hq * Sq:
         raise ValueError("lse must be a contiguous fp32 CUDA tensor with B*Hq*Sq elements")
@@ -160,9 +175,9 @@ def sdpa_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    _check_bf16("dq", dq, q.shape)
-    _check_bf16("dk", dk, k.shape)
-    _check_bf16("dv", dv, v.shape)
+    _check_bf16("dq", dq, q.shape, io)
+    _check_bf16("dk", dk, k.shape, io)
+    _check_bf16("dv", dv, v.shape, io)
     ws_bytes = 0
     if workspace is not None:
         if not workspace.is_cuda or not workspace.is_contiguous():
@@ -173,6 +188,16 @@ def sdpa_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
             _ptr(dv), B, Hq, Hkv, Sq, Skv, Dqk, Dv, sc, int(causal), int(bottom_right),
             int(window_left), int(window_right), int(deterministic), _ptr(seq_q_lens),
             _ptr(seq_kv_lens), _ptr(workspace), ws_bytes)
+    if io == torch.float16:  # fp16 io: the typed entry (sink optional, no bias)
+        if bias is not None:
+            raise ValueError("an additive bias needs bf16 io tensors")
+        if sink is not None:
+            dsink = torch.empty_like(sink) if dsink is None else dsink
+        rc = lib.sdpa_bwd_typed(_IO_CODES[io], *args, _ptr(sink), _ptr(dsink if sink is not None else None),
+                                _stream_handle(stream))
+        if rc != 0:
+            raise SdpaError(rc, "sdpa_bwd_typed")
+        return (dq, dk, dv) if sink is None else (dq, dk, dv, dsink)
     if sink is None and bias is None:
         rc = lib.sdpa_bwd(*args, _stream_handle(stream))
         if rc != 0:
@@ -235,12 +260,13 @@ def sdpa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: Option
     lib = load()
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
         raise ValueError("q, k, v must be (B, H, S, D)")
+    io = _io_dtype(q)
     B, Hq, Sq, Dqk = q.shape
     Hkv, Skv = k.shape[1], k.shape[2]
     Dv = v.shape[3]
-    _check_bf16("q", q, (B, Hq, Sq, Dqk))
-    _check_bf16("k", k, (B, Hkv, Skv, Dqk))
-    _check_bf16("v", v, (B, Hkv, Skv, Dv))
+    _check_bf16("q", q, (B, Hq, Sq, Dqk), io)
+    _check_bf16("k", k, (B, Hkv, Skv, Dqk), io)
+    _check_bf16("v", v, (B, Hkv, Skv, Dv), io)
     for name, lens in (("seq_q_lens", seq_q_lens), ("seq_kv_lens", seq_kv_lens)):
         if lens is not None and (lens.dtype != torch.int32 or not lens.is_cuda or lens.numel() != B
                                  or not lens.is_contiguous()):
@@ -248,9 +274,9 @@ def sdpa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: Option
     if sink is not None and (sink.dtype != torch.float32 or not sink.is_cuda
                              or not sink.is_contiguous() or sink.numel() != Hq):
         raise ValueError("sink must be a contiguous fp32 CUDA tensor of Hq elements")
-    o = torch.empty((B, Hq, Sq, Dv), dtype=torch.bfloat16, device=q.device) if o is None else o
+    o = torch.empty((B, Hq, Sq, Dv), dtype=io, device=q.device) if o is None else o
     lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device) if lse is None else lse
-    _check_bf16("o", o, (B, Hq, Sq, Dv))
+    _check_bf16("o", o, (B, Hq, Sq, Dv), io)
     if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous() \
             or lse.numel() != B * Hq * Sq:
         raise ValueError("lse must be a contiguous fp32 CUDA tensor with B*Hq*Sq elements")
@@ -258,7 +284,11 @@ def sdpa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: Option
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Skv, Dqk, Dv, sc,
             int(causal), int(bottom_right), int(window_left), int(window_right),
             _ptr(seq_q_lens), _ptr(seq_kv_lens), _ptr(sink))
-    if bias is None:
+    if io == torch.float16:
+        if bias is not None:
+            raise ValueError("an additive bias needs bf16 io tensors")
+        rc = lib.sdpa_fwd_typed(_IO_CODES[io], *args, _stream_handle(stream))
+    elif bias is None:
         rc = lib.sdpa_fwd(*args, _stream_handle(stream))
     else:
         dt = _check_bias(bias, B, Hq, Sq, Skv)

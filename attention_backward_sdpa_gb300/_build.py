@@ -19,6 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsdpa_bwd.so")
 SOURCES = ["sdpa_bwd_api.cu", "sdpa_bwd_main.cu", "sdpa_bwd_main_bias.cu", "sdpa_bwd_main_qat.cu",
+           "sdpa_bwd_main_f16.cu",
            "sdpa_bwd_main_ds.cu",
            "sdpa_bwd_aux.cu",
            "sdpa_bwd_dq.cu", "sdpa_bwd_noalloc.cu", "sdpa_fwd.cu"]

@@ -36,6 +36,7 @@ struct ChainParams {
   float scale;      // softmax scale
   float scale_log2; // scale * log2(e)
   int causal, bottom_right, window_left, window_right, deterministic;
+  int f16;          // io tensors are fp16 (the __nv_bfloat16 pointers below then hold fp16)
   const int32_t* seq_q_lens;   // (B,) or null
   const int32_t* seq_kv_lens;  // (B,) or null
 
@@ -117,6 +118,7 @@ struct FwdParams {
   int G;            // Hq / Hkv
   int n_qt;         // ceil(Sq / 128): 128-row query tiles
   float scale_log2; // scale * log2(e)
+  int f16;          // io tensors are fp16
   int causal, bottom_right, window_left, window_right;
   const int32_t* seq_q_lens;  // (B,) or null
   const int32_t* seq_kv_lens; // (B,) or null
@@ -157,6 +159,8 @@ cudaError_t launch_main_ds(const MainMaps& maps, const ChainParams& p, cudaStrea
 cudaError_t main_ds_kernel_setup();
 cudaError_t main_kernel_setup();  // per device: opt in to the main kernel's shared memory
 cudaError_t launch_main_bias(const MainMaps& maps, const ChainParams& p, cudaStream_t s);
+cudaError_t launch_main_f16(const MainMaps& maps, const ChainParams& p, cudaStream_t s);
+cudaError_t main_f16_kernel_setup();
 cudaError_t main_bias_kernel_setup();
 cudaError_t launch_main_qat(const MainMaps& maps, const ChainParams& p, cudaStream_t s);
 cudaError_t main_qat_kernel_setup();

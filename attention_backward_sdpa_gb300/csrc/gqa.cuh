@@ -14,18 +14,20 @@
 
 namespace sdpa {
 
+// Eight io elements (bf16, or fp16 when F16) widened to fp32.
+template <bool F16 = false>
 __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    f[2 * i] = io_lo<F16>(w[i]);
+    f[2 * i + 1] = io_hi<F16>(w[i]);
   }
 }
 
 // Rows [row_begin, row_end) of one output (dK with D = D_qk or dV with D = D_v),
 // one 8-column chunk per item, items strided over `nthreads` threads.
-template <int D>
+template <int D, bool F16>
 __device__ __forceinline__ void gqa_reduce_rows(const ChainParams& p, const __nv_bfloat16* ws,
                                                 __nv_bfloat16* out, unsigned row_begin,
                                                 unsigned row_end, unsigned thread,
@@ -49,29 +51,29 @@ __device__ __forceinline__ void gqa_reduce_rows(const ChainParams& p, const __nv
     for (int j = 0; j < 8; ++j) {  // ascending partial set: fixed order
       if (j < G) {
         float f[8];
-        unpack8(v[j], f);
+        unpack8<F16>(v[j], f);
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] += f[e];
       }
     }
     for (int j = 8; j < G; ++j) {  // more partial sets: the rest, same order
       float f[8];
-      unpack8(*reinterpret_cast<const uint4*>(src + j * head_stride), f);
+      unpack8<F16>(*reinterpret_cast<const uint4*>(src + j * head_stride), f);
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[e] += f[e];
     }
     uint4 o;
-    o.x = pack_bf16x2(acc[0], acc[1]);
-    o.y = pack_bf16x2(acc[2], acc[3]);
-    o.z = pack_bf16x2(acc[4], acc[5]);
-    o.w = pack_bf16x2(acc[6], acc[7]);
+    o.x = pack_io2<F16>(acc[0], acc[1]);
+    o.y = pack_io2<F16>(acc[2], acc[3]);
+    o.z = pack_io2<F16>(acc[4], acc[5]);
+    o.w = pack_io2<F16>(acc[6], acc[7]);
     *reinterpret_cast<uint4*>(out + (long long)row * D + c8 * 8) = o;
   }
 }
 
 // Piece `piece` of `n_pieces` of the slice of output rows assigned to CTA
 // `cta` of `n_ctas` (both outputs). Pieces let a kernel spread the work.
-template <int DQK, int DV>
+template <int DQK, int DV, bool F16 = false>
 __device__ __forceinline__ void gqa_reduce_slice(const ChainParams& p, unsigned cta, unsigned n_ctas,
                                                  unsigned thread, unsigned nthreads,
                                                  unsigned piece = 0, unsigned n_pieces = 1) {
@@ -83,8 +85,8 @@ __device__ __forceinline__ void gqa_reduce_slice(const ChainParams& p, unsigned 
   const unsigned pp = (hi - lo + n_pieces - 1) / n_pieces;
   const unsigned plo = lo + piece * pp, phi = (plo + pp < hi) ? plo + pp : hi;
   if (plo >= phi) return;
-  gqa_reduce_rows<DQK>(p, p.dk_ws, p.dk, plo, phi, thread, nthreads);
-  gqa_reduce_rows<DV>(p, p.dv_ws, p.dv, plo, phi, thread, nthreads);
+  gqa_reduce_rows<DQK, F16>(p, p.dk_ws, p.dk, plo, phi, thread, nthreads);
+  gqa_reduce_rows<DV, F16>(p, p.dv_ws, p.dv, plo, phi, thread, nthreads);
 }
 
 }  // namespace sdpa

@@ -215,6 +215,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
          | ((uint32_t)(N >> 3) << 17)           // N / 8
          | ((uint32_t)(M >> 4) << 24);          // M / 16
 }
+// The same with fp16 A/B (operand format 0) when `f16` is set: the io element
+// type of the fp16 instantiations (A and B always share one type).
+__host__ __device__ constexpr uint32_t idesc_io(int M, int N, bool a_mn, bool b_mn, bool f16) {
+  return f16 ? (idesc_bf16_f32(M, N, a_mn, b_mn) & ~((7u << 7) | (7u << 10)))
+             : idesc_bf16_f32(M, N, a_mn, b_mn);
+}
 
 // Shared-memory matrix descriptor with 128-byte swizzling.
 //   K-major operand: rows of 128 B (64 bf16 along K), 8-row groups SBO apart.
@@ -297,6 +303,36 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+// Packs two floats into f16x2 (round to nearest even); `lo` lands in bits 0..15.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// The io element type's pair pack: bf16x2, or f16x2 for the fp16 instantiations.
+template <bool F16>
+__device__ __forceinline__ uint32_t pack_io2(float lo, float hi) {
+  return F16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
+}
+// Widens the low / high element of an io pair to fp32.
+template <bool F16>
+__device__ __forceinline__ float io_lo(uint32_t w) {
+  if (F16) {
+    float f;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, l;\n\t}" : "=f"(f) : "r"(w));
+    return f;
+  }
+  return __uint_as_float(w << 16);
+}
+template <bool F16>
+__device__ __forceinline__ float io_hi(uint32_t w) {
+  if (F16) {
+    float f;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, h;\n\t}" : "=f"(f) : "r"(w));
+    return f;
+  }
+  return __uint_as_float(w & 0xFFFF0000u);
 }
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;

@@ -143,12 +143,13 @@ int device_state(int dev, int** status_out, int* sms_out) {
 
 // 3-D map {D, S, B*H} of a contiguous (B, H, S, D) bf16 tensor; boxes of 64
 // columns (128 bytes, the swizzle span) by `rows` sequence positions.
-bool make_bhsd_map(CUtensorMap* m, const void* base, int D, int S, long long BH, int rows) {
+bool make_bhsd_map(CUtensorMap* m, const void* base, int D, int S, long long BH, int rows,
+                   bool f16 = false) {
   const uint64_t dims[3] = {(uint64_t)D, (uint64_t)S, (uint64_t)BH};
   const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)S * D * 2};
   const uint32_t box[3] = {64, (uint32_t)rows, 1};
-  return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box,
-                   CU_TENSOR_MAP_SWIZZLE_128B);
+  return make_tmap(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base,
+                   dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // Records one event pair per launch while profiling is on; the pairs are
@@ -277,10 +278,12 @@ int run_chain(const void* q, const void* k, const void* v, const void* o, const 
               int window_left, int window_right, int deterministic, const int32_t* seq_q_lens,
               const int32_t* seq_kv_lens, void* workspace, size_t workspace_bytes,
               const float* sink, float* dsink, const BiasArgs& ba, void* stream_,
-              bool qat = false) {
+              bool qat = false, bool f16 = false) {
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   int rc = basic_checks(B, H_q, H_kv, S_q, S_kv, D_qk, D_v);
   if (rc != SDPA_OK) return rc;
+  // fp16 io: the plain chain (and sink tokens); the bias and QAT paths are bf16.
+  if (f16 && (qat || ba.bias)) return SDPA_ERR_UNSUPPORTED;
   // NVFP4 QAT: D 128, the dQ-reduction route, no bias or sink.
   if (qat && (D_qk != 128 || D_v != 128)) return SDPA_ERR_UNSUPPORTED;
   if (!q || !k || !v || !o || !d_o || !lse || !dq || !dk || !dv) return SDPA_ERR_INVALID;
@@ -365,6 +368,7 @@ int run_chain(const void* q, const void* k, const void* v, const void* o, const 
   // The two-kernel route is deterministic by construction (no cross-CTA
   // reduction); `deterministic` inside the kernels selects the ordered relay.
   p.deterministic = (deterministic && !ds_route) ? 1 : 0;
+  p.f16 = f16 ? 1 : 0;
   p.ds_route = ds_route ? 1 : 0;
   p.seq_q_lens = seq_q_lens;
   p.seq_kv_lens = seq_kv_lens;
@@ -406,14 +410,14 @@ int run_chain(const void* q, const void* k, const void* v, const void* o, const 
   const void* qg = qat ? static_cast<const void*>(ws + cv.q_hat) : q;
   const void* kg = qat ? static_cast<const void*>(ws + cv.k_hat) : k;
   const void* vg = qat ? static_cast<const void*>(ws + cv.v_hat) : v;
-  if (!make_bhsd_map(&maps.q, qg, D_qk, S_q, BHq, BQ) ||
-      !make_bhsd_map(&maps.k, kg, D_qk, S_kv, BHkv, BN) ||
-      !make_bhsd_map(&maps.v, vg, D_v, S_kv, BHkv, BN) ||
-      !make_bhsd_map(&maps.d_o, d_o, D_v, S_q, BHq, BQ) ||
+  if (!make_bhsd_map(&maps.q, qg, D_qk, S_q, BHq, BQ, f16) ||
+      !make_bhsd_map(&maps.k, kg, D_qk, S_kv, BHkv, BN, f16) ||
+      !make_bhsd_map(&maps.v, vg, D_v, S_kv, BHkv, BN, f16) ||
+      !make_bhsd_map(&maps.d_o, d_o, D_v, S_q, BHq, BQ, f16) ||
       !make_bhsd_map(&maps.dk_out, p.dk_ws ? static_cast<void*>(p.dk_ws) : dk, D_qk, S_kv,
-                     p.dk_ws ? BHq : BHkv, BN) ||
+                     p.dk_ws ? BHq : BHkv, BN, f16) ||
       !make_bhsd_map(&maps.dv_out, p.dv_ws ? static_cast<void*>(p.dv_ws) : dv, D_v, S_kv,
-                     p.dv_ws ? BHq : BHkv, BN)) {
+                     p.dv_ws ? BHq : BHkv, BN, f16)) {
     if (own_ws) cudaFreeAsync(workspace, stream);
     return SDPA_ERR_CUDA;
   }
@@ -465,10 +469,12 @@ namespace {
 int run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
             int H_kv, int S_q, int S_kv, int D_qk, int D_v, float scale, int causal,
             int bottom_right, int window_left, int window_right, const int32_t* seq_q_lens,
-            const int32_t* seq_kv_lens, const float* sink, const BiasArgs& ba, void* stream_) {
+            const int32_t* seq_kv_lens, const float* sink, const BiasArgs& ba, void* stream_,
+            bool f16 = false) {
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   int rc = basic_checks(B, H_q, H_kv, S_q, S_kv, D_qk, D_v);
   if (rc != SDPA_OK) return rc;
+  if (f16 && ba.bias) return SDPA_ERR_UNSUPPORTED;
   if (!q || !k || !v || !o || !lse) return SDPA_ERR_INVALID;
   for (const void* ptr : {q, k, v, (const void*)o})
     if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return SDPA_ERR_ALIGN;
@@ -496,6 +502,7 @@ int run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
   p.G = H_q / H_kv;
   p.n_qt = ceil_div(S_q, 128);
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.f16 = f16 ? 1 : 0;
   p.causal = causal ? 1 : 0;
   p.bottom_right = bottom_right ? 1 : 0;
   p.window_left = window_left < 0 ? -1 : window_left;
@@ -518,10 +525,10 @@ int run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
   const int Skv_map = S_kv > 0 ? S_kv : 1;
   const void* kb = S_kv > 0 ? k : q;
   const void* vb = S_kv > 0 ? v : q;
-  if (!make_bhsd_map(&maps.q, q, D_qk, S_q, BHq, 128) ||
-      !make_bhsd_map(&maps.k, kb, D_qk, Skv_map, S_kv > 0 ? BHkv : BHq, 128) ||
-      !make_bhsd_map(&maps.v, vb, D_v, Skv_map, S_kv > 0 ? BHkv : BHq, 128) ||
-      !make_bhsd_map(&maps.o, o, D_v, S_q, BHq, 128))
+  if (!make_bhsd_map(&maps.q, q, D_qk, S_q, BHq, 128, f16) ||
+      !make_bhsd_map(&maps.k, kb, D_qk, Skv_map, S_kv > 0 ? BHkv : BHq, 128, f16) ||
+      !make_bhsd_map(&maps.v, vb, D_v, Skv_map, S_kv > 0 ? BHkv : BHq, 128, f16) ||
+      !make_bhsd_map(&maps.o, o, D_v, S_q, BHq, 128, f16))
     return SDPA_ERR_CUDA;
   return launch_fwd(maps, p, stream) == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }
@@ -536,6 +543,17 @@ int sdpa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
              const int32_t* seq_kv_lens, const float* sink, void* stream) {
   return run_fwd(q, k, v, o, lse, B, H_q, H_kv, S_q, S_kv, D_qk, D_v, scale, causal, bottom_right,
                  window_left, window_right, seq_q_lens, seq_kv_lens, sink, BiasArgs{}, stream);
+}
+
+int sdpa_fwd_typed(int io_dtype, const void* q, const void* k, const void* v, void* o, float* lse,
+                   int B, int H_q, int H_kv, int S_q, int S_kv, int D_qk, int D_v, float scale,
+                   int causal, int bottom_right, int window_left, int window_right,
+                   const int32_t* seq_q_lens, const int32_t* seq_kv_lens, const float* sink,
+                   void* stream) {
+  if (io_dtype != SDPA_DTYPE_BF16 && io_dtype != SDPA_DTYPE_F16) return SDPA_ERR_INVALID;
+  return run_fwd(q, k, v, o, lse, B, H_q, H_kv, S_q, S_kv, D_qk, D_v, scale, causal, bottom_right,
+                 window_left, window_right, seq_q_lens, seq_kv_lens, sink, BiasArgs{}, stream,
+                 io_dtype == SDPA_DTYPE_F16);
 }
 
 int sdpa_fwd_bias(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
@@ -562,6 +580,20 @@ int sdpa_bwd_sink(const void* q, const void* k, const void* v, const void* o, co
   return run_chain(q, k, v, o, d_o, lse, dq, dk, dv, B, H_q, H_kv, S_q, S_kv, D_qk, D_v, scale,
                    causal, bottom_right, window_left, window_right, deterministic, seq_q_lens,
                    seq_kv_lens, workspace, workspace_bytes, sink, dsink, BiasArgs{}, stream);
+}
+
+int sdpa_bwd_typed(int io_dtype, const void* q, const void* k, const void* v, const void* o,
+                   const void* d_o, const float* lse, void* dq, void* dk, void* dv, int B, int H_q,
+                   int H_kv, int S_q, int S_kv, int D_qk, int D_v, float scale, int causal,
+                   int bottom_right, int window_left, int window_right, int deterministic,
+                   const int32_t* seq_q_lens, const int32_t* seq_kv_lens, void* workspace,
+                   size_t workspace_bytes, const float* sink, float* dsink, void* stream) {
+  if (io_dtype != SDPA_DTYPE_BF16 && io_dtype != SDPA_DTYPE_F16) return SDPA_ERR_INVALID;
+  if (dsink && !sink) return SDPA_ERR_INVALID;
+  return run_chain(q, k, v, o, d_o, lse, dq, dk, dv, B, H_q, H_kv, S_q, S_kv, D_qk, D_v, scale,
+                   causal, bottom_right, window_left, window_right, deterministic, seq_q_lens,
+                   seq_kv_lens, workspace, workspace_bytes, dsink ? sink : nullptr, dsink, BiasArgs{},
+                   stream, false, io_dtype == SDPA_DTYPE_F16);
 }
 
 int sdpa_bwd_nvfp4_qat(const void* q, const void* k, const void* v, const void* o_hp,

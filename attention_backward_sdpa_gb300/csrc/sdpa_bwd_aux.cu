@@ -48,7 +48,7 @@ __device__ void zero_shared_dbias_rows(const ChainParams& p, unsigned bh, int qt
 // 256 / TPR rows per pass, all loads of a tile issued before any reduction.
 // Index arithmetic is done once per tile in 32 bits (the host rejects tensors
 // of 2^31 elements or more).
-template <int DV>
+template <int DV, bool F16>
 __global__ void __launch_bounds__(256) sdpa_bwd_preprocess(const ChainParams p) {
   // The main kernel may start its prologue (barrier setup, TMEM allocation,
   // K/V loads) while this grid runs; it waits for completion before reading
@@ -92,8 +92,8 @@ __global__ void __launch_bounds__(256) sdpa_bwd_preprocess(const ChainParams p) 
       const int qi = u * RPP + rsub;
       const int q = qt * BQ + qi;
       float fo[8], fd[8];
-      unpack8(vo[u], fo);
-      unpack8(vd[u], fd);
+      unpack8<F16>(vo[u], fo);
+      unpack8<F16>(vd[u], fd);
       float dot = 0.f;
 #pragma unroll
       for (int i = 0; i < 8; ++i) dot = fmaf(fo[i], fd[i], dot);
@@ -155,10 +155,10 @@ __global__ void __launch_bounds__(256) sdpa_bwd_preprocess(const ChainParams p) 
 // at or past the batch row's query length are written as zeros without being
 // read (the preprocess kernel did not clear them). The kernel also carries a
 // slice of the GQA group reduction of dK/dV (gqa.cuh).
-template <int DQK, int DV>
+template <int DQK, int DV, bool F16>
 __global__ void __launch_bounds__(256) sdpa_bwd_dq_convert(const ChainParams p) {
   pdl_wait_prior_grid();
-  gqa_reduce_slice<DQK, DV>(p, blockIdx.x, gridDim.x, threadIdx.x, blockDim.x);
+  gqa_reduce_slice<DQK, DV, F16>(p, blockIdx.x, gridDim.x, threadIdx.x, blockDim.x);
   constexpr int CPR = DQK / 8;                 // 8-column chunks per row
   constexpr int ITEMS = BQ * CPR / 256;        // items per thread
   static_assert(BQ * CPR % 256 == 0, "whole items per thread");
@@ -186,10 +186,10 @@ __global__ void __launch_bounds__(256) sdpa_bwd_dq_convert(const ChainParams p) 
     const int i = threadIdx.x + u * 256, r = i / CPR, c8 = i % CPR;
     if (r < rows) {
       uint4 out;
-      out.x = pack_bf16x2(a[u].x * p.scale, a[u].y * p.scale);
-      out.y = pack_bf16x2(a[u].z * p.scale, a[u].w * p.scale);
-      out.z = pack_bf16x2(c[u].x * p.scale, c[u].y * p.scale);
-      out.w = pack_bf16x2(c[u].z * p.scale, c[u].w * p.scale);
+      out.x = pack_io2<F16>(a[u].x * p.scale, a[u].y * p.scale);
+      out.y = pack_io2<F16>(a[u].z * p.scale, a[u].w * p.scale);
+      out.z = pack_io2<F16>(c[u].x * p.scale, c[u].y * p.scale);
+      out.w = pack_io2<F16>(c[u].z * p.scale, c[u].w * p.scale);
       *reinterpret_cast<uint4*>(dst + r * DQK + c8 * 8) = out;
     }
   }
@@ -230,15 +230,22 @@ cudaError_t launch_dsink(const ChainParams& p, cudaStream_t s) {
 // the tiles to the hardware dispatcher.
 cudaError_t launch_preprocess(const ChainParams& p, cudaStream_t s) {
   const dim3 grid((unsigned)(p.B * p.Hq * p.n_qt));
-  return p.Dv == 64 ? launch_kernel(sdpa_bwd_preprocess<64>, grid, dim3(256), 0, s, false, p)
-                    : launch_kernel(sdpa_bwd_preprocess<128>, grid, dim3(256), 0, s, false, p);
+  if (p.f16)
+    return p.Dv == 64 ? launch_kernel(sdpa_bwd_preprocess<64, true>, grid, dim3(256), 0, s, false, p)
+                      : launch_kernel(sdpa_bwd_preprocess<128, true>, grid, dim3(256), 0, s, false, p);
+  return p.Dv == 64 ? launch_kernel(sdpa_bwd_preprocess<64, false>, grid, dim3(256), 0, s, false, p)
+                    : launch_kernel(sdpa_bwd_preprocess<128, false>, grid, dim3(256), 0, s, false, p);
 }
 
 cudaError_t launch_dq_convert(const ChainParams& p, cudaStream_t s) {
   const dim3 grid((unsigned)(p.B * p.Hq * p.n_qt));
+  if (p.f16)
+    return p.Dqk == 64
+               ? launch_kernel(sdpa_bwd_dq_convert<64, 64, true>, grid, dim3(256), 0, s, true, p)
+               : launch_kernel(sdpa_bwd_dq_convert<128, 128, true>, grid, dim3(256), 0, s, true, p);
   return p.Dqk == 64
-             ? launch_kernel(sdpa_bwd_dq_convert<64, 64>, grid, dim3(256), 0, s, true, p)
-             : launch_kernel(sdpa_bwd_dq_convert<128, 128>, grid, dim3(256), 0, s, true, p);
+             ? launch_kernel(sdpa_bwd_dq_convert<64, 64, false>, grid, dim3(256), 0, s, true, p)
+             : launch_kernel(sdpa_bwd_dq_convert<128, 128, false>, grid, dim3(256), 0, s, true, p);
 }
 
 }  // namespace sdpa

@@ -101,7 +101,7 @@ __device__ __forceinline__ DqUnit dq_unit(const ChainParams& p, int u) {
 // across unit boundaries through one stage ring. The MMA warp alternates
 // between two tensor-memory accumulators (counted over non-empty units only)
 // so that the epilogue of one unit overlaps the next.
-template <int D>
+template <int D, bool F16 = false>
 __global__ void __launch_bounds__(DQ_THREADS, 1)
     sdpa_bwd_dq_from_ds(const __grid_constant__ CUtensorMap k_map, const ChainParams p) {
   using L = DqLayout<D>;
@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA
-    constexpr uint32_t ID = idesc_bf16_f32(128, D, true, true);
+    constexpr uint32_t ID = idesc_io(128, D, true, true, F16);
     constexpr uint64_t T_MN = sdesc_sw128_template(BN * 128, 1024);  // 16 KB block stride
     bool ok = true;
     int step = 0, done_units = 0;
@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       __nv_bfloat16* out = p.dq + ((long long)w.bh * p.Sq + q) * D;
       const bool have = w.n > 0;
       const int buf = done_units & 1;
-      gqa_reduce_slice<D, 128>(p, blockIdx.x, gridDim.x, tid, 128, unit_idx++, n_pieces);
+      gqa_reduce_slice<D, 128, F16>(p, blockIdx.x, gridDim.x, tid, 128, unit_idx++, n_pieces);
       if (have && ok) {
         ok = mbar_wait(&acc_full[buf], (done_units >> 1) & 1, abort_flag, DQ_WAIT_LIMIT_NS);
         __syncwarp();
@@ -319,10 +319,10 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
 #pragma unroll
           for (int v8 = 0; v8 < 4; ++v8) {
             uint4 o;
-            o.x = pack_bf16x2(__uint_as_float(r[v8 * 8 + 0]) * p.scale, __uint_as_float(r[v8 * 8 + 1]) * p.scale);
-            o.y = pack_bf16x2(__uint_as_float(r[v8 * 8 + 2]) * p.scale, __uint_as_float(r[v8 * 8 + 3]) * p.scale);
-            o.z = pack_bf16x2(__uint_as_float(r[v8 * 8 + 4]) * p.scale, __uint_as_float(r[v8 * 8 + 5]) * p.scale);
-            o.w = pack_bf16x2(__uint_as_float(r[v8 * 8 + 6]) * p.scale, __uint_as_float(r[v8 * 8 + 7]) * p.scale);
+            o.x = pack_io2<F16>(__uint_as_float(r[v8 * 8 + 0]) * p.scale, __uint_as_float(r[v8 * 8 + 1]) * p.scale);
+            o.y = pack_io2<F16>(__uint_as_float(r[v8 * 8 + 2]) * p.scale, __uint_as_float(r[v8 * 8 + 3]) * p.scale);
+            o.z = pack_io2<F16>(__uint_as_float(r[v8 * 8 + 4]) * p.scale, __uint_as_float(r[v8 * 8 + 5]) * p.scale);
+            o.w = pack_io2<F16>(__uint_as_float(r[v8 * 8 + 6]) * p.scale, __uint_as_float(r[v8 * 8 + 7]) * p.scale);
             *reinterpret_cast<uint4*>(out + c32 * 32 + v8 * 8) = o;
           }
         }
@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       }
     }
     for (; unit_idx < n_pieces; ++unit_idx)
-      gqa_reduce_slice<D, 128>(p, blockIdx.x, gridDim.x, tid, 128, unit_idx, n_pieces);
+      gqa_reduce_slice<D, 128, F16>(p, blockIdx.x, gridDim.x, tid, 128, unit_idx, n_pieces);
   }
 
   tc_fence_before();
@@ -346,13 +346,28 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   }
 }
 
+template <int D, bool F16>
+static cudaError_t set_dq_smem() {
+  return cudaFuncSetAttribute(sdpa_bwd_dq_from_ds<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              DqLayout<D>::BYTES);
+}
+
 cudaError_t dq_kernel_setup() {
-  cudaError_t e = cudaFuncSetAttribute(sdpa_bwd_dq_from_ds<128>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       DqLayout<128>::BYTES);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(sdpa_bwd_dq_from_ds<192>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              DqLayout<192>::BYTES);
+  cudaError_t e = set_dq_smem<128, false>();
+  if (e == cudaSuccess) e = set_dq_smem<192, false>();
+  if (e == cudaSuccess) e = set_dq_smem<128, true>();
+  if (e == cudaSuccess) e = set_dq_smem<192, true>();
+  return e;
+}
+
+template <bool F16>
+static cudaError_t launch_dq_variant(const CUtensorMap& k_map, const ChainParams& p, cudaStream_t s,
+                                     dim3 grid) {
+  if (p.Dqk == 192)
+    return launch_kernel(sdpa_bwd_dq_from_ds<192, F16>, grid, dim3(DQ_THREADS), DqLayout<192>::BYTES, s,
+                         true, k_map, p);
+  return launch_kernel(sdpa_bwd_dq_from_ds<128, F16>, grid, dim3(DQ_THREADS), DqLayout<128>::BYTES, s,
+                       true, k_map, p);
 }
 
 // Persistent: one CTA per SM (at most one per unit).
@@ -360,11 +375,7 @@ cudaError_t launch_dq_from_ds(const CUtensorMap& k_map, const ChainParams& p, cu
                               int num_sms) {
   const int units = ceil_div(p.n_qt, 2) * p.B * p.Hq;
   const dim3 grid((unsigned)(units < num_sms ? units : num_sms));
-  if (p.Dqk == 192)
-    return launch_kernel(sdpa_bwd_dq_from_ds<192>, grid, dim3(DQ_THREADS), DqLayout<192>::BYTES, s,
-                         true, k_map, p);
-  return launch_kernel(sdpa_bwd_dq_from_ds<128>, grid, dim3(DQ_THREADS), DqLayout<128>::BYTES, s,
-                       true, k_map, p);
+  return p.f16 ? launch_dq_variant<true>(k_map, p, s, grid) : launch_dq_variant<false>(k_map, p, s, grid);
 }
 
 }  // namespace sdpa

@@ -196,8 +196,9 @@ __device__ __forceinline__ uint32_t fake_nvfp4_p_pair(float p0, float p1, float 
 // DS_OUT selects the deterministic two-kernel route: instead of G5 and the dQ
 // reduction, every dS^T tile is stored to the workspace for the dQ kernel.
 // BIAS adds the additive bias to the replay and writes dBias (when p.dbias).
-// QAT writes G3's P^T fake-quantized to NVFP4.
-template <int D, bool DS_OUT, bool BIAS, bool QAT = false>
+// QAT writes G3's P^T fake-quantized to NVFP4. F16: fp16 io tensors (and
+// fp16 P^T / dS^T MMA operands) instead of bf16.
+template <int D, bool DS_OUT, bool BIAS, bool QAT = false, bool F16 = false>
 __global__ void __launch_bounds__(MAIN_THREADS, 1)
     sdpa_bwd_main(const __grid_constant__ MainMaps maps, const ChainParams p) {
   using L = MainLayout<D, DS_OUT>;
@@ -343,9 +344,9 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
       // G3/G4/G5. Each warp stays converged and issues from one elected lane;
       // mbarriers carry every dependency between the two streams.
       pdl_wait_prior_grid();
-      constexpr uint32_t ID_G12 = idesc_bf16_f32(128, BQ, false, false);  // S^T, dP^T
-      constexpr uint32_t ID_G34 = idesc_bf16_f32(128, D, false, true);    // dV, dK
-      constexpr uint32_t ID_G5 = idesc_bf16_f32(128, BQ, true, true);     // dQ^T (rows >= D unused)
+      constexpr uint32_t ID_G12 = idesc_io(128, BQ, false, false, F16);  // S^T, dP^T
+      constexpr uint32_t ID_G34 = idesc_io(128, D, false, true, F16);    // dV, dK
+      constexpr uint32_t ID_G5 = idesc_io(128, BQ, true, true, F16);     // dQ^T (rows >= D unused)
       constexpr uint64_t T_KMAJ = sdesc_sw128_template(16, 1024);          // K-major operands
       constexpr uint64_t T_MN_Q = sdesc_sw128_template(L::BLK_Q, 1024);    // MN-major, 64-row tiles
       constexpr uint64_t T_MN_KV = sdesc_sw128_template(L::BLK_KV, 1024);  // MN-major, 128-row tiles
@@ -673,7 +674,7 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
                                      psc[c16 * 32 + 2 * i + 1]);
         } else {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(P[c16 * 32 + 2 * i], P[c16 * 32 + 2 * i + 1]);
+          for (int i = 0; i < 16; ++i) w[i] = pack_io2<F16>(P[c16 * 32 + 2 * i], P[c16 * 32 + 2 * i + 1]);
         }
         tmem_st16(t_lane + L::col_s(slot) + c16 * 16, w);
       }
@@ -713,10 +714,10 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
                                P[c + 5] * (__uint_as_float(r[i + 5]) - d1.y),
                                P[c + 6] * (__uint_as_float(r[i + 6]) - d1.z),
                                P[c + 7] * (__uint_as_float(r[i + 7]) - d1.w)};
-          const uint32_t w0 = pack_bf16x2(ds[0], ds[1]);
-          const uint32_t w1 = pack_bf16x2(ds[2], ds[3]);
-          const uint32_t w2 = pack_bf16x2(ds[4], ds[5]);
-          const uint32_t w3 = pack_bf16x2(ds[6], ds[7]);
+          const uint32_t w0 = pack_io2<F16>(ds[0], ds[1]);
+          const uint32_t w1 = pack_io2<F16>(ds[2], ds[3]);
+          const uint32_t w2 = pack_io2<F16>(ds[4], ds[5]);
+          const uint32_t w3 = pack_io2<F16>(ds[6], ds[7]);
           *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (row & 7)) << 4)) = make_uint4(w0, w1, w2, w3);
           if constexpr (BIAS) {
             // dBias = dS' in fp32: one column segment of this thread's key.
@@ -783,10 +784,10 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
 #pragma unroll
       for (int v8 = 0; v8 < 4; ++v8) {
         uint4 o;
-        o.x = pack_bf16x2(__uint_as_float(r[v8 * 8 + 0]) * mult, __uint_as_float(r[v8 * 8 + 1]) * mult);
-        o.y = pack_bf16x2(__uint_as_float(r[v8 * 8 + 2]) * mult, __uint_as_float(r[v8 * 8 + 3]) * mult);
-        o.z = pack_bf16x2(__uint_as_float(r[v8 * 8 + 4]) * mult, __uint_as_float(r[v8 * 8 + 5]) * mult);
-        o.w = pack_bf16x2(__uint_as_float(r[v8 * 8 + 6]) * mult, __uint_as_float(r[v8 * 8 + 7]) * mult);
+        o.x = pack_io2<F16>(__uint_as_float(r[v8 * 8 + 0]) * mult, __uint_as_float(r[v8 * 8 + 1]) * mult);
+        o.y = pack_io2<F16>(__uint_as_float(r[v8 * 8 + 2]) * mult, __uint_as_float(r[v8 * 8 + 3]) * mult);
+        o.z = pack_io2<F16>(__uint_as_float(r[v8 * 8 + 4]) * mult, __uint_as_float(r[v8 * 8 + 5]) * mult);
+        o.w = pack_io2<F16>(__uint_as_float(r[v8 * 8 + 6]) * mult, __uint_as_float(r[v8 * 8 + 7]) * mult);
         const int piece = (c32 & 1) * 4 + v8;
         *reinterpret_cast<uint4*>(dst_row + ((piece ^ (row & 7)) << 4)) = o;
       }
@@ -811,32 +812,32 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
   }
 }
 
-template <int D, bool DS_OUT, bool BIAS, bool QAT = false>
+template <int D, bool DS_OUT, bool BIAS, bool QAT = false, bool F16 = false>
 static cudaError_t set_main_smem() {
-  return cudaFuncSetAttribute(sdpa_bwd_main<D, DS_OUT, BIAS, QAT>,
+  return cudaFuncSetAttribute(sdpa_bwd_main<D, DS_OUT, BIAS, QAT, F16>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, MainLayout<D, DS_OUT>::BYTES);
 }
 
 // One CTA per (key tile, head group) work unit.
-template <bool BIAS>
+template <bool BIAS, bool F16 = false>
 static cudaError_t launch_main_variant(const MainMaps& maps, const ChainParams& p, cudaStream_t s) {
   const dim3 grid((unsigned)(p.n_kt * p.B * p.Hkv * p.n_part));
   const dim3 block(MAIN_THREADS);
   if (p.Dqk == 64)
-    return launch_kernel(sdpa_bwd_main<64, false, BIAS>, grid, block, MainLayout<64, false>::BYTES, s,
-                         true, maps, p);
+    return launch_kernel(sdpa_bwd_main<64, false, BIAS, false, F16>, grid, block,
+                         MainLayout<64, false>::BYTES, s, true, maps, p);
   if (p.ds_route)
-    return launch_kernel(sdpa_bwd_main<128, true, BIAS>, grid, block, MainLayout<128, true>::BYTES, s,
-                         true, maps, p);
-  return launch_kernel(sdpa_bwd_main<128, false, BIAS>, grid, block, MainLayout<128, false>::BYTES, s,
-                       true, maps, p);
+    return launch_kernel(sdpa_bwd_main<128, true, BIAS, false, F16>, grid, block,
+                         MainLayout<128, true>::BYTES, s, true, maps, p);
+  return launch_kernel(sdpa_bwd_main<128, false, BIAS, false, F16>, grid, block,
+                       MainLayout<128, false>::BYTES, s, true, maps, p);
 }
 
-template <bool BIAS>
+template <bool BIAS, bool F16 = false>
 static cudaError_t main_variant_setup() {
-  cudaError_t e = set_main_smem<64, false, BIAS>();
-  if (e == cudaSuccess) e = set_main_smem<128, false, BIAS>();
-  if (e == cudaSuccess) e = set_main_smem<128, true, BIAS>();
+  cudaError_t e = set_main_smem<64, false, BIAS, false, F16>();
+  if (e == cudaSuccess) e = set_main_smem<128, false, BIAS, false, F16>();
+  if (e == cudaSuccess) e = set_main_smem<128, true, BIAS, false, F16>();
   return e;
 }
 

@@ -99,7 +99,7 @@ struct Layout {
 // D_qk 64/128 kernel (bias.cuh): loads of the next tile's bias column issued
 // right after dS, dS' stored as dBias, and the dBias blocks no CTA computes
 // zeroed by an idle warp (or by an empty unit's whole CTA).
-template <int DQK, int DV, bool BIAS>
+template <int DQK, int DV, bool BIAS, bool F16 = false>
 __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
     sdpa_bwd_main_ds(const __grid_constant__ MainMaps maps, const ChainParams p) {
   using namespace ds_kernel;
@@ -182,10 +182,10 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
                       qt_hi);
   const int n = qt_hi - qt_lo + 1;
 
-  constexpr uint32_t ID_G1 = idesc_bf16_f32(128, BQ, false, false);
-  constexpr uint32_t ID_G2 = idesc_bf16_f32(128, BQ, false, false);
-  constexpr uint32_t ID_G3 = idesc_bf16_f32(128, DV, false, true);
-  constexpr uint32_t ID_G4 = idesc_bf16_f32(128, DQK, false, true);
+  constexpr uint32_t ID_G1 = idesc_io(128, BQ, false, false, F16);
+  constexpr uint32_t ID_G2 = idesc_io(128, BQ, false, false, F16);
+  constexpr uint32_t ID_G3 = idesc_io(128, DV, false, true, F16);
+  constexpr uint32_t ID_G4 = idesc_io(128, DQK, false, true, F16);
   constexpr uint64_t T_KMAJ = sdesc_sw128_template(16, 1024);
   constexpr uint64_t T_MN_Q = sdesc_sw128_template(L::BLK_Q, 1024);
 
@@ -422,7 +422,7 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
       for (int c16 = 0; c16 < 2; ++c16) {
         uint32_t w[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(P[c16 * 32 + 2 * i], P[c16 * 32 + 2 * i + 1]);
+        for (int i = 0; i < 16; ++i) w[i] = pack_io2<F16>(P[c16 * 32 + 2 * i], P[c16 * 32 + 2 * i + 1]);
         tmem_st16(t_lane + L::col_p(slot) + c16 * 16, w);
       }
       tmem_st_wait();
@@ -461,10 +461,10 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
                                P[c + 5] * (__uint_as_float(r[i + 5]) - d1.y),
                                P[c + 6] * (__uint_as_float(r[i + 6]) - d1.z),
                                P[c + 7] * (__uint_as_float(r[i + 7]) - d1.w)};
-          const uint32_t w0 = pack_bf16x2(ds[0], ds[1]);
-          const uint32_t w1 = pack_bf16x2(ds[2], ds[3]);
-          const uint32_t w2 = pack_bf16x2(ds[4], ds[5]);
-          const uint32_t w3 = pack_bf16x2(ds[6], ds[7]);
+          const uint32_t w0 = pack_io2<F16>(ds[0], ds[1]);
+          const uint32_t w1 = pack_io2<F16>(ds[2], ds[3]);
+          const uint32_t w2 = pack_io2<F16>(ds[4], ds[5]);
+          const uint32_t w3 = pack_io2<F16>(ds[6], ds[7]);
           *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (row & 7)) << 4)) = make_uint4(w0, w1, w2, w3);
           if constexpr (BIAS) {
             if (p.dbias != nullptr && key_in) {
@@ -528,10 +528,10 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
 #pragma unroll
       for (int v8 = 0; v8 < 4; ++v8) {
         uint4 o;
-        o.x = pack_bf16x2(__uint_as_float(r[v8 * 8 + 0]) * mult, __uint_as_float(r[v8 * 8 + 1]) * mult);
-        o.y = pack_bf16x2(__uint_as_float(r[v8 * 8 + 2]) * mult, __uint_as_float(r[v8 * 8 + 3]) * mult);
-        o.z = pack_bf16x2(__uint_as_float(r[v8 * 8 + 4]) * mult, __uint_as_float(r[v8 * 8 + 5]) * mult);
-        o.w = pack_bf16x2(__uint_as_float(r[v8 * 8 + 6]) * mult, __uint_as_float(r[v8 * 8 + 7]) * mult);
+        o.x = pack_io2<F16>(__uint_as_float(r[v8 * 8 + 0]) * mult, __uint_as_float(r[v8 * 8 + 1]) * mult);
+        o.y = pack_io2<F16>(__uint_as_float(r[v8 * 8 + 2]) * mult, __uint_as_float(r[v8 * 8 + 3]) * mult);
+        o.z = pack_io2<F16>(__uint_as_float(r[v8 * 8 + 4]) * mult, __uint_as_float(r[v8 * 8 + 5]) * mult);
+        o.w = pack_io2<F16>(__uint_as_float(r[v8 * 8 + 6]) * mult, __uint_as_float(r[v8 * 8 + 7]) * mult);
         const int piece = (c32 & 1) * 4 + v8;
         *reinterpret_cast<uint4*>(dst_row + ((piece ^ (row & 7)) << 4)) = o;
       }
@@ -556,15 +556,16 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
   }
 }
 
-template <int DQK, int DV, bool BIAS>
+template <int DQK, int DV, bool BIAS, bool F16 = false>
 static cudaError_t set_ds_smem() {
-  return cudaFuncSetAttribute(sdpa_bwd_main_ds<DQK, DV, BIAS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(sdpa_bwd_main_ds<DQK, DV, BIAS, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               ds_kernel::Layout<DQK, DV>::BYTES);
 }
 
 cudaError_t main_ds_kernel_setup() {
   cudaError_t e = set_ds_smem<192, 128, false>();
   if (e == cudaSuccess) e = set_ds_smem<192, 128, true>();
+  if (e == cudaSuccess) e = set_ds_smem<192, 128, false, true>();
   return e;
 }
 
@@ -574,6 +575,9 @@ cudaError_t launch_main_ds(const MainMaps& maps, const ChainParams& p, cudaStrea
   if (p.Dqk != 192 || p.Dv != 128) return cudaErrorInvalidValue;
   if (p.bias != nullptr)
     return launch_kernel(sdpa_bwd_main_ds<192, 128, true>, grid, block,
+                         ds_kernel::Layout<192, 128>::BYTES, s, true, maps, p);
+  if (p.f16)
+    return launch_kernel(sdpa_bwd_main_ds<192, 128, false, true>, grid, block,
                          ds_kernel::Layout<192, 128>::BYTES, s, true, maps, p);
   return launch_kernel(sdpa_bwd_main_ds<192, 128, false>, grid, block, ds_kernel::Layout<192, 128>::BYTES,
                        s, true, maps, p);

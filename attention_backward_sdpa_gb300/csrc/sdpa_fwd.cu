@@ -137,8 +137,9 @@ __device__ __forceinline__ float fwd_bias_at(const uint32_t (&raw)[64], bool pac
                 : __uint_as_float(raw[i]);
 }
 
-// BIAS adds the additive bias (FwdParams::bias) to the scaled scores.
-template <int DQK, int DV, bool BIAS>
+// BIAS adds the additive bias (FwdParams::bias) to the scaled scores. F16:
+// fp16 io tensors (and fp16 P for the PV GEMM) instead of bf16.
+template <int DQK, int DV, bool BIAS, bool F16 = false>
 __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
     sdpa_fwd_kernel(const __grid_constant__ FwdMaps maps, const FwdParams p) {
   using namespace fwd_kernel;
@@ -232,8 +233,8 @@ __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     // Order: G1(0), then for j >= 1: G1(j), G2(j-1); finally G2(n-1). G1(j)
     // reuses the slot of tile j-3, whose P G2(j-3) read; G2(j-1) needs P(j-1).
-    constexpr uint32_t ID_S = idesc_bf16_f32(BM, BK, false, false);  // S = Q K^T
-    constexpr uint32_t ID_O = idesc_bf16_f32(BM, DV, false, true);   // O += P V
+    constexpr uint32_t ID_S = idesc_io(BM, BK, false, false, F16);  // S = Q K^T
+    constexpr uint32_t ID_O = idesc_io(BM, DV, false, true, F16);   // O += P V
     constexpr uint64_t T_KMAJ = sdesc_sw128_template(16, 1024);
     constexpr uint64_t T_MN_V = sdesc_sw128_template(L::BLK, 1024);
     bool ok = n > 0 && mbar_wait(&bars[BAR_QFULL], 0, abort_flag, WAIT_LIMIT_NS);
@@ -416,7 +417,7 @@ __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
             const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c16][2 * i2 + 1]), cs, neg_m));
             rs[(2 * i2) & 7] += p0;
             rs[(2 * i2 + 1) & 7] += p1;
-            w[i2] = pack_bf16x2(p0, p1);
+            w[i2] = pack_io2<F16>(p0, p1);
           }
         } else {
 #pragma unroll
@@ -428,7 +429,7 @@ __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
                                  ? ex2_approx(fmaf(__uint_as_float(sr[c16][2 * i2 + 1]), cs, neg_m)) : 0.f;
             rs[(2 * i2) & 7] += p0;
             rs[(2 * i2 + 1) & 7] += p1;
-            w[i2] = pack_bf16x2(p0, p1);
+            w[i2] = pack_io2<F16>(p0, p1);
           }
         }
         __syncwarp();
@@ -484,10 +485,10 @@ __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
         for (int e = 0; e < 8; ++e)
           y[e] = __uint_as_float(o0[v8 * 8 + e]) * f0 + __uint_as_float(o1[v8 * 8 + e]) * f1;
         uint4 w;
-        w.x = pack_bf16x2(y[0], y[1]);
-        w.y = pack_bf16x2(y[2], y[3]);
-        w.z = pack_bf16x2(y[4], y[5]);
-        w.w = pack_bf16x2(y[6], y[7]);
+        w.x = pack_io2<F16>(y[0], y[1]);
+        w.y = pack_io2<F16>(y[2], y[3]);
+        w.z = pack_io2<F16>(y[4], y[5]);
+        w.w = pack_io2<F16>(y[6], y[7]);
         const int cc = cbase + v8 * 8;          // column of this 16-byte piece
         const int piece = (cc & 63) >> 3;
         *reinterpret_cast<uint4*>(dst_row + (cc >> 6) * L::BLK + ((piece ^ (row & 7)) << 4)) = w;
@@ -516,44 +517,47 @@ __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
   }
 }
 
-template <int DQK, int DV, bool BIAS>
+template <int DQK, int DV, bool BIAS, bool F16>
 static cudaError_t set_fwd_smem() {
-  return cudaFuncSetAttribute(sdpa_fwd_kernel<DQK, DV, BIAS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              fwd_kernel::Layout<DQK, DV>::BYTES);
+  return cudaFuncSetAttribute(sdpa_fwd_kernel<DQK, DV, BIAS, F16>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, fwd_kernel::Layout<DQK, DV>::BYTES);
 }
 
-template <bool BIAS>
+template <bool BIAS, bool F16>
 static cudaError_t fwd_setup_variant() {
-  cudaError_t e = set_fwd_smem<64, 64, BIAS>();
-  if (e == cudaSuccess) e = set_fwd_smem<128, 128, BIAS>();
-  if (e == cudaSuccess) e = set_fwd_smem<192, 128, BIAS>();
+  cudaError_t e = set_fwd_smem<64, 64, BIAS, F16>();
+  if (e == cudaSuccess) e = set_fwd_smem<128, 128, BIAS, F16>();
+  if (e == cudaSuccess) e = set_fwd_smem<192, 128, BIAS, F16>();
   return e;
 }
 
 cudaError_t fwd_kernel_setup() {
-  cudaError_t e = fwd_setup_variant<false>();
-  if (e == cudaSuccess) e = fwd_setup_variant<true>();
+  cudaError_t e = fwd_setup_variant<false, false>();
+  if (e == cudaSuccess) e = fwd_setup_variant<true, false>();
+  if (e == cudaSuccess) e = fwd_setup_variant<false, true>();
   return e;
 }
 
-template <bool BIAS>
+template <bool BIAS, bool F16>
 static cudaError_t launch_fwd_variant(const FwdMaps& maps, const FwdParams& p, cudaStream_t s) {
   const dim3 grid((unsigned)(p.n_qt * p.B * p.Hq));
   const dim3 block(fwd_kernel::THREADS);
   if (p.Dqk == 64 && p.Dv == 64)
-    return launch_kernel(sdpa_fwd_kernel<64, 64, BIAS>, grid, block, fwd_kernel::Layout<64, 64>::BYTES,
-                         s, false, maps, p);
+    return launch_kernel(sdpa_fwd_kernel<64, 64, BIAS, F16>, grid, block,
+                         fwd_kernel::Layout<64, 64>::BYTES, s, false, maps, p);
   if (p.Dqk == 128 && p.Dv == 128)
-    return launch_kernel(sdpa_fwd_kernel<128, 128, BIAS>, grid, block,
+    return launch_kernel(sdpa_fwd_kernel<128, 128, BIAS, F16>, grid, block,
                          fwd_kernel::Layout<128, 128>::BYTES, s, false, maps, p);
   if (p.Dqk == 192 && p.Dv == 128)
-    return launch_kernel(sdpa_fwd_kernel<192, 128, BIAS>, grid, block,
+    return launch_kernel(sdpa_fwd_kernel<192, 128, BIAS, F16>, grid, block,
                          fwd_kernel::Layout<192, 128>::BYTES, s, false, maps, p);
   return cudaErrorInvalidValue;
 }
 
+// The bias variants are bf16 only (the host rejects a bias with fp16 io).
 cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, cudaStream_t s) {
-  return p.bias ? launch_fwd_variant<true>(maps, p, s) : launch_fwd_variant<false>(maps, p, s);
+  if (p.bias) return launch_fwd_variant<true, false>(maps, p, s);
+  return p.f16 ? launch_fwd_variant<false, true>(maps, p, s) : launch_fwd_variant<false, false>(maps, p, s);
 }
 
 }  // namespace sdpa

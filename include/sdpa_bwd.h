@@ -54,10 +54,13 @@ typedef enum {
   SDPA_ERR_TIMEOUT = 6      /* a device-side bounded wait ran out (reported later)  */
 } sdpa_status;
 
-/* Element type of an optional additive bias (sdpa_bwd_bias, sdpa_fwd_bias). */
+/* Element types: of an optional additive bias (sdpa_bwd_bias, sdpa_fwd_bias:
+ * BF16 or F32) and of the io tensors (sdpa_bwd_typed, sdpa_fwd_typed: BF16 or
+ * F16). */
 typedef enum {
   SDPA_DTYPE_BF16 = 0,
-  SDPA_DTYPE_F32 = 1
+  SDPA_DTYPE_F32 = 1,
+  SDPA_DTYPE_F16 = 2
 } sdpa_dtype;
 
 /*
@@ -216,6 +219,34 @@ int sdpa_fwd_bias(const void* q, const void* k, const void* v, void* o, float* l
                   int bottom_right, int window_left, int window_right, const int32_t* seq_q_lens,
                   const int32_t* seq_kv_lens, const float* sink, const void* bias, int bias_dtype,
                   int bias_batch, void* stream);
+
+/*
+ * SDPA backward with the io element type as an argument ("SDPA Backward
+ * (SM120)", support surface: FP16 / BF16, LSE fp32). io_dtype is
+ * SDPA_DTYPE_BF16 (exactly sdpa_bwd_sink() / sdpa_bwd()) or SDPA_DTYPE_F16: q,
+ * k, v, o, d_o, dq, dk and dv are fp16, the GEMMs take fp16 operands (P and
+ * dS rounded to fp16), and every accumulation stays fp32. The other arguments
+ * are those of sdpa_bwd_sink(), where sink and dsink may both be NULL.
+ * Returns SDPA_ERR_INVALID for another io_dtype; otherwise as sdpa_bwd().
+ * The workspace size does not depend on the io type.
+ */
+int sdpa_bwd_typed(int io_dtype, const void* q, const void* k, const void* v, const void* o,
+                   const void* d_o, const float* lse, void* dq, void* dk, void* dv, int B, int H_q,
+                   int H_kv, int S_q, int S_kv, int D_qk, int D_v, float scale, int causal,
+                   int bottom_right, int window_left, int window_right, int deterministic,
+                   const int32_t* seq_q_lens, const int32_t* seq_kv_lens, void* workspace,
+                   size_t workspace_bytes, const float* sink, float* dsink, void* stream);
+
+/*
+ * SDPA forward with the io element type as an argument: sdpa_fwd() for
+ * io_dtype SDPA_DTYPE_BF16, or with fp16 q, k, v and o (P rounded to fp16 for
+ * the PV GEMM) for SDPA_DTYPE_F16. Returns SDPA_ERR_INVALID for another io_dtype.
+ */
+int sdpa_fwd_typed(int io_dtype, const void* q, const void* k, const void* v, void* o, float* lse,
+                   int B, int H_q, int H_kv, int S_q, int S_kv, int D_qk, int D_v, float scale,
+                   int causal, int bottom_right, int window_left, int window_right,
+                   const int32_t* seq_q_lens, const int32_t* seq_kv_lens, const float* sink,
+                   void* stream);
 
 /*
  * NVFP4 fake quantization ("NVFP4 Attention QAT Backward" page, Overview):

@@ -25,12 +25,13 @@ def f64(x: torch.Tensor) -> np.ndarray:
     return x.double().numpy()
 
 
-def make_case(w: workloads.Workload, sink: bool = False, bias=None):
+def make_case(w: workloads.Workload, sink: bool = False, bias=None, io=torch.bfloat16):
     """Seeded inputs plus O (bf16) and LSE (fp32) from the oracle forward; with
     ``sink`` the forward takes the workload's sink logits (case["sink"]); with
     ``bias`` = (batch, dtype) an additive bias of that batch (1 or B) and element
-    type (case["bias"]), which the oracle sees exactly as the GPU does."""
-    t = workloads.generate(w)
+    type (case["bias"]), which the oracle sees exactly as the GPU does. ``io``
+    is the element type of Q, K, V, dO and O (bf16 or fp16)."""
+    t = workloads.generate(w, io)
     t["sink"] = workloads.sink_logits(w) if sink else None
     t["bias"] = None if bias is None else workloads.bias_tensor(w, bias[0], bias[1])
     p = oracle.Problem(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.Dqk, w.Dv, scale=w.resolved_scale,
@@ -41,7 +42,7 @@ def make_case(w: workloads.Workload, sink: bool = False, bias=None):
     o64, lse64 = oracle.forward(p, f64(t["q"]), f64(t["k"]), f64(t["v"]),
                                 None if t["sink"] is None else t["sink"].double().numpy(),
                                 bias=None if t["bias"] is None else f64(t["bias"]))
-    t["o"] = torch.from_numpy(o64).to(torch.bfloat16)
+    t["o"] = torch.from_numpy(o64).to(io)
     t["lse"] = torch.from_numpy(lse64).float()
     t["problem"] = p
     t["workload"] = w

@@ -239,3 +239,22 @@ def test_nvfp4_qat_argument_validation(lib):
     base = lib.sdpa_bwd_workspace_size(1, 2, 2, 128, 128, 128, 128, 0)
     assert ws == base + 3 * 2 * 128 * 128 * 2
     assert lib.sdpa_bwd_nvfp4_qat_workspace_size(1, 2, 2, 128, 128, 64, 64) == 0
+
+
+def test_typed_entry_validation(lib):
+    lib.sdpa_bwd_typed.restype = ctypes.c_int
+    lib.sdpa_fwd_typed.restype = ctypes.c_int
+    vp = [ctypes.c_void_p(FAKE)] * 9
+
+    def bwd(io, sink=None, dsink=None):
+        return lib.sdpa_bwd_typed(io, *vp, 1, 2, 2, 128, 128, 128, 128, ctypes.c_float(0.0), 0, 0, -1,
+                                  -1, 0, None, None, None, ctypes.c_size_t(0),
+                                  None if sink is None else ctypes.c_void_p(sink),
+                                  None if dsink is None else ctypes.c_void_p(dsink), None)
+    assert bwd(1) == INVALID          # fp32 io is not an io type
+    assert bwd(7) == INVALID
+    assert bwd(2, dsink=FAKE) == INVALID
+    assert bwd(2, sink=FAKE + 1, dsink=FAKE) == ALIGN
+    fv = [ctypes.c_void_p(FAKE)] * 5
+    assert lib.sdpa_fwd_typed(3, *fv, 1, 2, 2, 128, 128, 128, 128, ctypes.c_float(0.0), 0, 0, -1, -1,
+                              None, None, None, None) == INVALID

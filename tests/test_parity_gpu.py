@@ -325,7 +325,7 @@ def _gpu_fwd(case, d):
                           bottom_right=w.bottom_right, window_left=w.window_left,
                           window_right=w.window_right, seq_q_lens=d["seq_q_lens"],
                           seq_kv_lens=d["seq_kv_lens"], sink=d.get("sink"), bias=d.get("bias"),
-                          o=torch.full((w.B, w.Hq, w.Sq, w.Dv), float("nan"), dtype=torch.bfloat16,
+                          o=torch.full((w.B, w.Hq, w.Sq, w.Dv), float("nan"), dtype=d["q"].dtype,
                                        device="cuda"),
                           lse=torch.full((w.B, w.Hq, w.Sq), float("nan"), device="cuda"))
     pkg.check_device_status()
@@ -675,3 +675,69 @@ def test_nvfp4_qat_forward_then_backward():
     assert_close("dq", dq.double().cpu().numpy(), rq)
     assert_close("dk", dk.double().cpu().numpy(), rk)
     assert_close("dv", dv.double().cpu().numpy(), rv)
+
+
+# ---------------------------------------------------------------- fp16 io
+# The same chain with fp16 Q, K, V, O, dO, dQ, dK, dV (fp16 MMA operands, P and
+# dS rounded to fp16, fp32 accumulation), against the oracle on the fp16 values.
+F16_CASES = {
+    "d128_causal_ragged": SMALL["d128_causal_ragged"],
+    "gqa_det": SMALL["gqa_det"],                    # stored-dS route, dQ-from-dS kernel
+    "gqa": SMALL["gqa"],                            # GQA partial sets, reduction route
+    "tl_causal_long_q_d64": SMALL["tl_causal_long_q"],
+    "det_d64_relay": SMALL["det_d64_relay"],
+    "padded_window": SMALL["padded_window"],
+    "window_only": SMALL["window_only"],
+    "mla_br_causal_ragged": SMALL["mla_br_causal_ragged"],
+    "mla_gqa_window": SMALL["mla_gqa_window"],
+}
+
+
+@pytest.mark.parametrize("name", sorted(F16_CASES))
+def test_f16_parity(name):
+    case = make_case(F16_CASES[name], io=torch.float16)
+    d = to_device(case)
+    dq, dk, dv = gpu_backward(case, d)
+    assert dq.dtype == torch.float16 and dk.dtype == torch.float16
+    rq, rk, rv = oracle_backward(case)
+    assert_close("dq", dq.double().cpu().numpy(), rq)
+    assert_close("dk", dk.double().cpu().numpy(), rk)
+    assert_close("dv", dv.double().cpu().numpy(), rv)
+
+
+@pytest.mark.parametrize("name", ["d128_causal_ragged", "mla_gqa_window", "tl_causal_long_q_d64",
+                                  "padded_window"])
+def test_f16_forward_parity(name):
+    case = make_case(F16_CASES[name], io=torch.float16)
+    d = to_device(case)
+    o, lse = _gpu_fwd(case, d)
+    assert o.dtype == torch.float16
+    _check_fwd(case, o, lse)
+
+
+def test_f16_sink_and_bitwise():
+    case = make_case(SMALL["det_padded_odd"], sink=True, io=torch.float16)
+    d = to_device(case)
+    first = gpu_backward(case, d, sink=d["sink"])
+    rq, rk, rv = oracle_backward(case)
+    assert_close("dq", first[0].double().cpu().numpy(), rq)
+    ref, mag = oracle_dsink(case)
+    _dsink_close(first[3].double().cpu().numpy(), ref, mag)
+    first = [t.clone() for t in first]
+    for _ in range(9):
+        again = gpu_backward(case, d, sink=d["sink"])
+        for a, b in zip(first, again):
+            assert torch.equal(a.view(torch.int16) if a.dtype != torch.float32 else a.view(torch.int32),
+                               b.view(torch.int16) if b.dtype != torch.float32 else b.view(torch.int32))
+
+
+def test_f16_full_size_sampled():
+    """causal_mha's shape with fp16 io, sampled rows against the oracle."""
+    w = workloads.WORKLOADS["causal_mha"]
+    case = make_case(w, io=torch.float16)
+    dq, dk, dv = gpu_backward(case)
+    q_rows, kv_rows = _sample_rows(w, None, np.random.default_rng(7))
+    rq, rk, rv = oracle_sampled(case, q_rows, kv_rows)
+    assert_close("dq", dq.reshape(-1, w.Dqk)[torch.from_numpy(q_rows).cuda()].double().cpu().numpy(), rq)
+    assert_close("dk", dk.reshape(-1, w.Dqk)[torch.from_numpy(kv_rows).cuda()].double().cpu().numpy(), rk)
+    assert_close("dv", dv.reshape(-1, w.Dv)[torch.from_numpy(kv_rows).cuda()].double().cpu().numpy(), rv)

@@ -69,8 +69,9 @@ WORKLOADS: Dict[str, Workload] = {
 ORDER = ["tiny_dense", "causal_mha", "causal_gqa_det", "swa_causal_padded", "mla_br_causal"]
 
 
-def generate(w: Workload) -> Dict[str, Optional[torch.Tensor]]:
-    """Seeded CPU tensors: q, k, v, do (bf16) and seq_q_lens/seq_kv_lens (int32 or None)."""
+def generate(w: Workload, dtype=torch.bfloat16) -> Dict[str, Optional[torch.Tensor]]:
+    """Seeded CPU tensors: q, k, v, do (bf16, or ``dtype``: the same fp32 draws
+    rounded to fp16 for fp16 io) and seq_q_lens/seq_kv_lens (int32 or None)."""
     g = torch.Generator("cpu").manual_seed(w.seed)
     lens = None
     if w.padded is not None:
@@ -78,7 +79,7 @@ def generate(w: Workload) -> Dict[str, Optional[torch.Tensor]]:
         lens = torch.randint(lo, hi + 1, (w.B,), generator=g, dtype=torch.int64).to(torch.int32)
 
     def draw(*shape):
-        return torch.randn(*shape, generator=g, dtype=torch.float32).to(torch.bfloat16)
+        return torch.randn(*shape, generator=g, dtype=torch.float32).to(dtype)
 
     q = draw(w.B, w.Hq, w.Sq, w.Dqk)
     k = draw(w.B, w.Hkv, w.Skv, w.Dqk)
