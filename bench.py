@@ -219,7 +219,7 @@ def oracle_forward_inputs(w, t):
         q64, k64, v64 = oracle.fake_nvfp4(q64), oracle.fake_nvfp4(k64), oracle.fake_nvfp4(v64)
     o64, lse64 = oracle.forward(p, q64, k64, v64,
                                 bias=None if bias is None else bias.double().numpy())
-    return torch.from_numpy(o64).to(torch.bfloat16), torch.from_numpy(lse64).float()
+    return torch.from_numpy(o64).to(t["q"].dtype), torch.from_numpy(lse64).float()
 
 
 def _head_slice(w, t, o, lse, G_groups):
@@ -287,7 +287,7 @@ def run_gpu_fwd(args, w, t, rank, world, device):
     d = {k: t[k].to(device) for k in ("q", "k", "v")}
     lq = None if lens is None else lens.to(device)
     lk = None if t["seq_kv_lens"] is None else t["seq_kv_lens"].to(device)
-    o = torch.empty((w.B, w.Hq, w.Sq, w.Dv), dtype=torch.bfloat16, device=device)
+    o = torch.empty((w.B, w.Hq, w.Sq, w.Dv), dtype=t["q"].dtype, device=device)
     lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=device)
     sink = workloads.sink_logits(w).to(device) if args.sink else None
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
@@ -379,15 +379,16 @@ def cpu_baseline_leg(w, t, target_s=12.0):
 # valid only for the kernel sources they were taken on: the digest covers the
 # kernel's source files, and a changed kernel reports null. D_qk = 192 runs
 # sdpa_bwd_main_ds, every other head dim sdpa_bwd_main.
-MAIN_SOURCES = {"sdpa_bwd_main": ("sdpa_bwd_main.cuh", "common.cuh", "ptx.cuh", "nvfp4.cuh"),
-                "sdpa_bwd_main_ds": ("sdpa_bwd_main_ds.cu", "common.cuh", "ptx.cuh")}
+MAIN_SOURCES = {"sdpa_bwd_main": ("sdpa_bwd_main.cuh", "common.cuh", "ptx.cuh", "nvfp4.cuh", "bias.cuh"),
+                "sdpa_bwd_main_ds": ("sdpa_bwd_main_ds.cu", "common.cuh", "ptx.cuh", "bias.cuh")}
 MAIN_TRAFFIC = {
-    "8126bd09ad511676": {"causal_mha": 114586624 + 31854336,
-                         "causal_gqa_det": 135143936 + 515680512,
-                         "swa_causal_padded": 245902336 + 185991680,
-                         "causal_mha/bias-B-f32": 468585216 + 584235520,
-                         "causal_mha/qat": 113126656 + 29260544},
-    "1a2f7841b4750af2": {"mla_br_causal": 132356352 + 263149824},
+    "9f0248d141f4a824": {"causal_mha": 113898496 + 31285248,
+                         "causal_gqa_det": 124068864 + 513333504,
+                         "swa_causal_padded": 246296320 + 186098432,
+                         "causal_mha/bias-B-f32": 468734976 + 583854592,
+                         "causal_mha/qat": 112215808 + 27959808},
+    "595df10a88242d87": {"mla_br_causal": 132132352 + 263815680,
+                         "mla_br_causal/bias-B-bf16": 425211136 + 1330963456},
 }
 
 
@@ -404,9 +405,11 @@ def main_traffic(w, tag=None):
 
 def bias_tag(t):
     """The traffic table's key suffix: 'bias-<batch>-<dtype>' for a biased run,
-    'qat' for the NVFP4 QAT backward, else None."""
+    'qat' for the NVFP4 QAT backward, 'f16' for fp16 io, else None."""
     if t.get("qat"):
         return "qat"
+    if t["q"].dtype == torch.float16:
+        return "f16"
     b = t.get("bias")
     if b is None:
         return None
@@ -595,6 +598,8 @@ def main(argv=None):
                     help="add a bias of B batches or 1 shared batch: sdpa_bwd_bias (dBias written "
                          "in fp32), or sdpa_fwd_bias with --pass fwd")
     ap.add_argument("--bias-dtype", default="bf16", choices=["bf16", "f32"])
+    ap.add_argument("--io", default="bf16", choices=["bf16", "f16"],
+                    help="element type of Q, K, V, O, dO and the gradients (f16: sdpa_bwd_typed)")
     ap.add_argument("--qat", action="store_true",
                     help="time sdpa_bwd_nvfp4_qat (NVFP4 fake-quantized Q/K/V, P fake-quantized "
                          "for dV; D = 128, non-deterministic)")
@@ -612,7 +617,10 @@ def main(argv=None):
         return 0
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-    t = workloads.generate(w)
+    io = torch.float16 if args.io == "f16" else torch.bfloat16
+    if args.io == "f16" and (args.bias != "none" or args.qat):
+        ap.error("--io f16: the plain chain (a bias or QAT needs bf16)")
+    t = workloads.generate(w, io)
     if args.qat:
         if w.Dqk != 128 or w.Dv != 128 or w.deterministic or args.bias != "none" or args.sink \
                 or args.pass_ != "bwd":
@@ -630,7 +638,7 @@ def main(argv=None):
             import torch.distributed as dist
             dist.destroy_process_group()
         return 0
-    o = torch.empty((w.B, w.Hq, w.Sq, w.Dv), dtype=torch.bfloat16)
+    o = torch.empty((w.B, w.Hq, w.Sq, w.Dv), dtype=io)
     lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32)
     cb = None
     if rank == 0:
@@ -656,7 +664,7 @@ def result_line(args, w, world, r, cb, metric):
     """The JSON line of a GPU run (rank 0)."""
     return {"metric": metric, "value": r["value"], "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": args.io,
             "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "H_q": w.Hq, "H_kv": w.Hkv, "S_q": w.Sq,
                        "S_kv": w.Skv, "D_qk": w.Dqk, "D_v": w.Dv, "causal": w.causal,
