@@ -51,7 +51,8 @@ struct ChainParams {
 
   // workspace regions
   float* qstat;         // [B*Hq][n_qt][QSTAT_FLOATS]
-  float* dq_accum;      // [B*Hq][n_qt*BQ][Dqk] row-major, rows padded to whole tiles
+  float* dq_accum;      // [B*Hq][n_qt*BQ][dq_acc_cols] row-major, rows padded to whole tiles
+  int dq_acc_cols;      // max(Dqk, 64): a D_qk of 32 runs on the 64-column kernels
   int* counters;        // [B*Hq][n_qt] turn counters (deterministic mode)
   int* ticket;          // work-unit ticket
   __nv_bfloat16* dk_ws; // n_part > 1: [B][Hkv][n_part][Skv][Dqk] partials, else null
@@ -217,8 +218,7 @@ __device__ inline bool row_has_visible_pair(int Lq, int Lk) { return Lq > 0 && L
 // One warp: zeroes the dK/dV rows of this CTA's share of the empty key tiles of
 // its head group (dK/dV destination `head`), classifying tiles with the same
 // visited_query_tiles() that every kernel walks.
-template <int DQK, int DV>
-__device__ void zero_group_share_of_empty_key_tiles(const ChainParams& p, long long head, int kt_self,
+__device__ inline void zero_group_share_of_empty_key_tiles(const ChainParams& p, long long head, int kt_self,
                                                     int Lq, int Lk, int lane) {
   int rank = 0, n_vis = 0;
   for (int base = 0; base < p.n_kt; base += 32) {
@@ -245,22 +245,21 @@ __device__ void zero_group_share_of_empty_key_tiles(const ChainParams& p, long l
       if (j++ % n_vis != rank) continue;
       const int k0 = e * BN;
       const int rows = min(BN, p.Skv - k0);
-      uint4* dk = reinterpret_cast<uint4*>((p.dk_ws ? p.dk_ws : p.dk) + (head * p.Skv + k0) * DQK);
-      uint4* dv = reinterpret_cast<uint4*>((p.dv_ws ? p.dv_ws : p.dv) + (head * p.Skv + k0) * DV);
-      for (int i = lane; i < rows * (DQK / 8); i += 32) dk[i] = z;
-      for (int i = lane; i < rows * (DV / 8); i += 32) dv[i] = z;
+      uint4* dk = reinterpret_cast<uint4*>((p.dk_ws ? p.dk_ws : p.dk) + (head * p.Skv + k0) * p.Dqk);
+      uint4* dv = reinterpret_cast<uint4*>((p.dv_ws ? p.dv_ws : p.dv) + (head * p.Skv + k0) * p.Dv);
+      for (int i = lane; i < rows * (p.Dqk / 8); i += 32) dk[i] = z;
+      for (int i = lane; i < rows * (p.Dv / 8); i += 32) dv[i] = z;
     }
   }
 }
 
-template <int DQK, int DV>
 __device__ inline void zero_key_tile_rows(const ChainParams& p, long long head, int k0) {
   const int rows = min(BN, p.Skv - k0);
   const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-  uint4* dk = reinterpret_cast<uint4*>((p.dk_ws ? p.dk_ws : p.dk) + (head * p.Skv + k0) * DQK);
-  uint4* dv = reinterpret_cast<uint4*>((p.dv_ws ? p.dv_ws : p.dv) + (head * p.Skv + k0) * DV);
-  for (int i = threadIdx.x; i < rows * (DQK / 8); i += blockDim.x) dk[i] = z;
-  for (int i = threadIdx.x; i < rows * (DV / 8); i += blockDim.x) dv[i] = z;
+  uint4* dk = reinterpret_cast<uint4*>((p.dk_ws ? p.dk_ws : p.dk) + (head * p.Skv + k0) * p.Dqk);
+  uint4* dv = reinterpret_cast<uint4*>((p.dv_ws ? p.dv_ws : p.dv) + (head * p.Skv + k0) * p.Dv);
+  for (int i = threadIdx.x; i < rows * (p.Dqk / 8); i += blockDim.x) dk[i] = z;
+  for (int i = threadIdx.x; i < rows * (p.Dv / 8); i += blockDim.x) dv[i] = z;
 }
 
 }  // namespace sdpa

@@ -130,8 +130,8 @@ __global__ void __launch_bounds__(256) sdpa_bwd_preprocess(const ChainParams p) 
     if (p.dq_accum) {
       const int rows = min(BQ, Lq - qt * BQ);
       if (rows > 0) {
-        float4* acc = reinterpret_cast<float4*>(p.dq_accum + ((long long)bh * p.n_qt + qt) * BQ * p.Dqk);
-        const int n4 = rows * p.Dqk / 4;
+        float4* acc = reinterpret_cast<float4*>(p.dq_accum + ((long long)bh * p.n_qt + qt) * BQ * p.dq_acc_cols);
+        const int n4 = rows * p.dq_acc_cols / 4;
         for (int i = threadIdx.x; i < n4; i += blockDim.x) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
@@ -168,15 +168,17 @@ __global__ void __launch_bounds__(256) sdpa_bwd_dq_convert(const ChainParams p) 
   batch_lengths(p, (int)(bh / (unsigned)p.Hq), Lq, Lk);
   const int rows = min(BQ, p.Sq - qt * BQ);         // rows of dQ in this tile
   const int live = max(0, min(rows, Lq - qt * BQ)); // rows holding accumulated values
-  const float* src = p.dq_accum + ((long long)bh * p.n_qt + qt) * BQ * DQK;
+  // A D_qk of 32 accumulates in 64-column rows (the D 64 kernels' tiles).
+  constexpr int ACC = DQK < 64 ? 64 : DQK;
+  const float* src = p.dq_accum + ((long long)bh * p.n_qt + qt) * BQ * ACC;
   __nv_bfloat16* dst = p.dq + ((long long)bh * p.Sq + (long long)qt * BQ) * DQK;
   float4 a[ITEMS], c[ITEMS];
 #pragma unroll
   for (int u = 0; u < ITEMS; ++u) {
     const int i = threadIdx.x + u * 256, r = i / CPR, c8 = i % CPR;
     if (r < live) {
-      a[u] = *reinterpret_cast<const float4*>(src + r * DQK + c8 * 8);
-      c[u] = *reinterpret_cast<const float4*>(src + r * DQK + c8 * 8 + 4);
+      a[u] = *reinterpret_cast<const float4*>(src + r * ACC + c8 * 8);
+      c[u] = *reinterpret_cast<const float4*>(src + r * ACC + c8 * 8 + 4);
     } else {
       a[u] = c[u] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
@@ -228,24 +230,28 @@ cudaError_t launch_dsink(const ChainParams& p, cudaStream_t s) {
 
 // Both kernels take one 64-row query tile per CTA and leave the balancing of
 // the tiles to the hardware dispatcher.
-cudaError_t launch_preprocess(const ChainParams& p, cudaStream_t s) {
+template <bool F16>
+static cudaError_t launch_preprocess_io(const ChainParams& p, cudaStream_t s) {
   const dim3 grid((unsigned)(p.B * p.Hq * p.n_qt));
-  if (p.f16)
-    return p.Dv == 64 ? launch_kernel(sdpa_bwd_preprocess<64, true>, grid, dim3(256), 0, s, false, p)
-                      : launch_kernel(sdpa_bwd_preprocess<128, true>, grid, dim3(256), 0, s, false, p);
-  return p.Dv == 64 ? launch_kernel(sdpa_bwd_preprocess<64, false>, grid, dim3(256), 0, s, false, p)
-                    : launch_kernel(sdpa_bwd_preprocess<128, false>, grid, dim3(256), 0, s, false, p);
+  if (p.Dv == 32) return launch_kernel(sdpa_bwd_preprocess<32, F16>, grid, dim3(256), 0, s, false, p);
+  if (p.Dv == 64) return launch_kernel(sdpa_bwd_preprocess<64, F16>, grid, dim3(256), 0, s, false, p);
+  return launch_kernel(sdpa_bwd_preprocess<128, F16>, grid, dim3(256), 0, s, false, p);
+}
+
+cudaError_t launch_preprocess(const ChainParams& p, cudaStream_t s) {
+  return p.f16 ? launch_preprocess_io<true>(p, s) : launch_preprocess_io<false>(p, s);
+}
+
+template <bool F16>
+static cudaError_t launch_dq_convert_io(const ChainParams& p, cudaStream_t s) {
+  const dim3 grid((unsigned)(p.B * p.Hq * p.n_qt));
+  if (p.Dqk == 32) return launch_kernel(sdpa_bwd_dq_convert<32, 32, F16>, grid, dim3(256), 0, s, true, p);
+  if (p.Dqk == 64) return launch_kernel(sdpa_bwd_dq_convert<64, 64, F16>, grid, dim3(256), 0, s, true, p);
+  return launch_kernel(sdpa_bwd_dq_convert<128, 128, F16>, grid, dim3(256), 0, s, true, p);
 }
 
 cudaError_t launch_dq_convert(const ChainParams& p, cudaStream_t s) {
-  const dim3 grid((unsigned)(p.B * p.Hq * p.n_qt));
-  if (p.f16)
-    return p.Dqk == 64
-               ? launch_kernel(sdpa_bwd_dq_convert<64, 64, true>, grid, dim3(256), 0, s, true, p)
-               : launch_kernel(sdpa_bwd_dq_convert<128, 128, true>, grid, dim3(256), 0, s, true, p);
-  return p.Dqk == 64
-             ? launch_kernel(sdpa_bwd_dq_convert<64, 64, false>, grid, dim3(256), 0, s, true, p)
-             : launch_kernel(sdpa_bwd_dq_convert<128, 128, false>, grid, dim3(256), 0, s, true, p);
+  return p.f16 ? launch_dq_convert_io<true>(p, s) : launch_dq_convert_io<false>(p, s);
 }
 
 }  // namespace sdpa

@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
                         hi0);
     if (hi0 < lo0) {
       if (!row_has_visible_pair(Lq0, Lk0))
-        zero_key_tile_rows<D, D>(p, p.dk_ws ? (long long)gi0 : (long long)(gi0 / p.n_part), kt0 * BN);
+        zero_key_tile_rows(p, p.dk_ws ? (long long)gi0 : (long long)(gi0 / p.n_part), kt0 * BN);
       if (BIAS && p.dbias != nullptr && !p.dbias_red) {
         const int hk0 = (gi0 / p.n_part) % p.Hkv;
         zero_unvisited_dbias_blocks(p, b0, b0 * p.Hq + hk0 * p.G + (gi0 % p.n_part) * p.gsz, p.gsz, kt0,
@@ -447,7 +447,7 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
     } else if (!DS_OUT && warp == 15) {
       // Idle on this route: this CTA's share of the group's empty key tiles,
       // and the dBias blocks of its key tile that no CTA computes.
-      if (!p.deterministic) zero_group_share_of_empty_key_tiles<D, D>(p, out_head, kt, Lq, Lk, lane);
+      if (!p.deterministic) zero_group_share_of_empty_key_tiles(p, out_head, kt, Lq, Lk, lane);
       if (BIAS && p.dbias != nullptr && !p.dbias_red)
         zero_unvisited_dbias_blocks(p, b, bh0, p.gsz, kt, qt_lo, qt_hi, lane, 32);
     } else if (DS_OUT && warp == 15) {
@@ -476,7 +476,7 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
     // Idle on the two-kernel route: warp 9 writes this CTA's share of the
     // group's empty key tiles.
     if (DS_OUT && warp == 9 && !p.deterministic)
-      zero_group_share_of_empty_key_tiles<D, D>(p, out_head, kt, Lq, Lk, lane);
+      zero_group_share_of_empty_key_tiles(p, out_head, kt, Lq, Lk, lane);
     // ... and the dBias blocks of this key tile that no CTA computes.
     if (BIAS && DS_OUT && p.dbias != nullptr && !p.dbias_red)
       zero_unvisited_dbias_blocks(p, b, bh0, p.gsz, kt, qt_lo, qt_hi, threadIdx.x - 256, 128);
@@ -823,7 +823,7 @@ template <bool BIAS, bool F16 = false>
 static cudaError_t launch_main_variant(const MainMaps& maps, const ChainParams& p, cudaStream_t s) {
   const dim3 grid((unsigned)(p.n_kt * p.B * p.Hkv * p.n_part));
   const dim3 block(MAIN_THREADS);
-  if (p.Dqk == 64)
+  if (p.Dqk <= 64)  // a D_qk of 32 runs here, its columns 32..63 zero-filled by TMA
     return launch_kernel(sdpa_bwd_main<64, false, BIAS, false, F16>, grid, block,
                          MainLayout<64, false>::BYTES, s, true, maps, p);
   if (p.ds_route)

@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
     if (hi0 < lo0) {
       // gsz = 1: the partial set of a query head is its bh index.
       if (!row_has_visible_pair(Lq0, Lk0))
-        zero_key_tile_rows<DQK, DV>(p, p.dk_ws ? (long long)bh0 : (long long)b0 * p.Hkv + (bh0 % p.Hq) / p.G,
+        zero_key_tile_rows(p, p.dk_ws ? (long long)bh0 : (long long)b0 * p.Hkv + (bh0 % p.Hq) / p.G,
                                     kt0 * BN);
       if (BIAS && p.dbias != nullptr && !p.dbias_red)
         zero_unvisited_dbias_blocks(p, b0, bh0, 1, kt0, lo0, hi0, threadIdx.x, blockDim.x);
@@ -335,7 +335,7 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
   } else if (warp == 13) {
     // This CTA's share of the head's empty key tiles (gsz = 1: the partial
     // set of a query head is its bh index).
-    zero_group_share_of_empty_key_tiles<DQK, DV>(p, p.dk_ws ? (long long)bh : (long long)b * p.Hkv + hk,
+    zero_group_share_of_empty_key_tiles(p, p.dk_ws ? (long long)bh : (long long)b * p.Hkv + hk,
                                                  kt, Lq, Lk, lane);
   } else if (BIAS && warp == 14) {
     // The dBias blocks of this key tile that no CTA computes.

@@ -52,7 +52,8 @@ def _a256(x):
 
 def expected_workspace(B, Hq, Hkv, Sq, Skv, Dqk, Dv, det=0):
     """Documented layout: per-query-tile row statistics (2 x 64 fp32 per 64-row tile);
-    then either the fp32 dQ accumulator over whole 64-row tiles, or (deterministic,
+    then either the fp32 dQ accumulator over whole 64-row tiles (rows of max(D_qk, 64)
+    columns: D_qk 32 runs on the 64-column kernels), or (deterministic,
     D_qk = 128: two-kernel route) one 16 KiB bf16 dS^T tile per (128-key tile,
     64-query tile) plus one zero tile; one int per query tile plus a ticket; one fp32
     sink-token partial per query tile; and for GQA the bf16 dK/dV partials with H_q
@@ -62,7 +63,7 @@ def expected_workspace(B, Hq, Hkv, Sq, Skv, Dqk, Dv, det=0):
     if (det and Dqk == 128) or Dqk == 192:
         total += _a256(B * Hq * n_kt * n_qt * 16384) + _a256(16384)
     else:
-        total += _a256(B * Hq * n_qt * 64 * Dqk * 4)
+        total += _a256(B * Hq * n_qt * 64 * max(Dqk, 64) * 4)
     total += _a256((B * Hq * n_qt + 1) * 4)
     total += _a256(B * Hq * n_qt * 4)
     if Hkv < Hq:
@@ -73,7 +74,7 @@ def expected_workspace(B, Hq, Hkv, Sq, Skv, Dqk, Dv, det=0):
 @pytest.mark.parametrize("shape", [(1, 2, 2, 128, 128, 64, 64), (2, 16, 16, 2048, 2048, 128, 128),
                                    (1, 32, 8, 4096, 4096, 128, 128), (3, 4, 1, 300, 177, 128, 128),
                                    (1, 1, 1, 1, 1, 64, 64), (1, 16, 16, 4096, 4096, 192, 128),
-                                   (2, 4, 2, 300, 177, 192, 128)])
+                                   (2, 4, 2, 300, 177, 192, 128), (2, 4, 2, 300, 177, 32, 32)])
 def test_workspace_size_matches_layout(lib, shape):
     for det in (0, 1):
         assert lib.sdpa_bwd_workspace_size(*shape, det) == expected_workspace(*shape, det=det)
@@ -103,6 +104,8 @@ def test_argument_validation(lib):
     assert call(lib, Sq=-1) == INVALID
     assert call(lib, Dqk=96, Dv=96) == UNSUPPORTED
     assert call(lib, Dqk=128, Dv=64) == UNSUPPORTED
+    assert call(lib, Dqk=32, Dv=64) == UNSUPPORTED
+    assert call(lib, Dqk=256, Dv=256) == UNSUPPORTED
     assert call(lib, Dqk=192, Dv=192) == UNSUPPORTED
     for i in range(9):
         ptrs = [FAKE] * 9

@@ -741,3 +741,57 @@ def test_f16_full_size_sampled():
     assert_close("dq", dq.reshape(-1, w.Dqk)[torch.from_numpy(q_rows).cuda()].double().cpu().numpy(), rq)
     assert_close("dk", dk.reshape(-1, w.Dqk)[torch.from_numpy(kv_rows).cuda()].double().cpu().numpy(), rk)
     assert_close("dv", dv.reshape(-1, w.Dv)[torch.from_numpy(kv_rows).cuda()].double().cpu().numpy(), rv)
+
+
+# ---------------------------------------------------------------- head dim 32
+# D = 32 runs on the 64-column kernels: TMA loads zero-fill columns 32..63 (so
+# the extra columns add nothing to any product) and TMA stores drop them; the
+# dQ accumulator keeps 64-column rows.
+D32_CASES = {
+    "d32_causal_ragged": W("d32_causal_ragged", 1, 2, 2, 300, 300, 32, 32, causal=True, seed=60),
+    "d32_gqa_det_relay": W("d32_gqa_det", 1, 4, 2, 260, 260, 32, 32, causal=True, deterministic=True,
+                           seed=61),
+    "d32_padded_window": W("d32_padded_window", 2, 2, 2, 300, 300, 32, 32, causal=True, window_left=90,
+                           padded=(100, 300), seed=62),
+    "d32_dense_cross_gqa": W("d32_dense_cross", 2, 2, 1, 190, 250, 32, 32, seed=63),
+}
+
+
+@pytest.mark.parametrize("name", sorted(D32_CASES))
+def test_d32_parity(name):
+    case = make_case(D32_CASES[name])
+    d = to_device(case)
+    dq, dk, dv = gpu_backward(case, d)
+    rq, rk, rv = oracle_backward(case)
+    assert_close("dq", dq.double().cpu().numpy(), rq)
+    assert_close("dk", dk.double().cpu().numpy(), rk)
+    assert_close("dv", dv.double().cpu().numpy(), rv)
+
+
+@pytest.mark.parametrize("name", ["d32_causal_ragged", "d32_padded_window"])
+def test_d32_forward_parity(name):
+    case = make_case(D32_CASES[name])
+    d = to_device(case)
+    o, lse = _gpu_fwd(case, d)
+    _check_fwd(case, o, lse)
+
+
+def test_d32_f16_bias_and_bitwise():
+    w = D32_CASES["d32_causal_ragged"]
+    case = make_case(w, io=torch.float16)
+    d = to_device(case)
+    dq, dk, dv = gpu_backward(case, d)
+    for g, r, n in zip((dq, dk, dv), oracle_backward(case), ("dq", "dk", "dv")):
+        assert_close(n, g.double().cpu().numpy(), r)
+    case = make_case(w, bias=(1, torch.float32))
+    d = to_device(case)
+    dq, dk, dv, db = _gpu_bias(case, d)
+    for g, r, n in zip((dq, dk, dv), oracle_backward(case), ("dq", "dk", "dv")):
+        assert_close(n, g.double().cpu().numpy(), r)
+    assert_close("dbias", db.double().cpu().numpy(), oracle_dbias(case))
+    case = make_case(D32_CASES["d32_gqa_det_relay"])
+    d = to_device(case)
+    first = [t.clone() for t in gpu_backward(case, d)]
+    for _ in range(9):
+        for a, b in zip(first, gpu_backward(case, d)):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
