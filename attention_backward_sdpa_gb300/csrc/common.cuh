@@ -52,7 +52,7 @@ struct ChainParams {
   // workspace regions
   float* qstat;         // [B*Hq][n_qt][QSTAT_FLOATS]
   float* dq_accum;      // [B*Hq][n_qt*BQ][dq_acc_cols] row-major, rows padded to whole tiles
-  int dq_acc_cols;      // max(Dqk, 64): a D_qk of 32 runs on the 64-column kernels
+  int dq_acc_cols;      // 64 or 128: the column count of the main kernel that runs (D_qk <= it)
   int* counters;        // [B*Hq][n_qt] turn counters (deterministic mode)
   int* ticket;          // work-unit ticket
   __nv_bfloat16* dk_ws; // n_part > 1: [B][Hkv][n_part][Skv][Dqk] partials, else null

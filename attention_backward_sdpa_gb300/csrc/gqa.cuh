@@ -25,14 +25,15 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
   }
 }
 
-// Rows [row_begin, row_end) of one output (dK with D = D_qk or dV with D = D_v),
-// one 8-column chunk per item, items strided over `nthreads` threads.
-template <int D, bool F16>
+// Rows [row_begin, row_end) of one output (dK with D = D_qk or dV with D = D_v,
+// a multiple of 8), one 8-column chunk per item, items strided over `nthreads`
+// threads.
+template <bool F16>
 __device__ __forceinline__ void gqa_reduce_rows(const ChainParams& p, const __nv_bfloat16* ws,
-                                                __nv_bfloat16* out, unsigned row_begin,
+                                                __nv_bfloat16* out, int D, unsigned row_begin,
                                                 unsigned row_end, unsigned thread,
                                                 unsigned nthreads) {
-  constexpr unsigned CPR = D / 8;  // chunks per row
+  const unsigned CPR = (unsigned)D / 8;  // chunks per row
   const unsigned items = (row_end > row_begin ? row_end - row_begin : 0) * CPR;
   const long long head_stride = (long long)p.Skv * D;
   const int G = p.n_part;
@@ -73,7 +74,7 @@ __device__ __forceinline__ void gqa_reduce_rows(const ChainParams& p, const __nv
 
 // Piece `piece` of `n_pieces` of the slice of output rows assigned to CTA
 // `cta` of `n_ctas` (both outputs). Pieces let a kernel spread the work.
-template <int DQK, int DV, bool F16 = false>
+template <bool F16 = false>
 __device__ __forceinline__ void gqa_reduce_slice(const ChainParams& p, unsigned cta, unsigned n_ctas,
                                                  unsigned thread, unsigned nthreads,
                                                  unsigned piece = 0, unsigned n_pieces = 1) {
@@ -85,8 +86,8 @@ __device__ __forceinline__ void gqa_reduce_slice(const ChainParams& p, unsigned 
   const unsigned pp = (hi - lo + n_pieces - 1) / n_pieces;
   const unsigned plo = lo + piece * pp, phi = (plo + pp < hi) ? plo + pp : hi;
   if (plo >= phi) return;
-  gqa_reduce_rows<DQK, F16>(p, p.dk_ws, p.dk, plo, phi, thread, nthreads);
-  gqa_reduce_rows<DV, F16>(p, p.dv_ws, p.dv, plo, phi, thread, nthreads);
+  gqa_reduce_rows<F16>(p, p.dk_ws, p.dk, p.Dqk, plo, phi, thread, nthreads);
+  gqa_reduce_rows<F16>(p, p.dv_ws, p.dv, p.Dv, plo, phi, thread, nthreads);
 }
 
 }  // namespace sdpa

@@ -69,8 +69,8 @@ Carve carve(int B, int Hq, int Hkv, int Sq, int Skv, int Dqk, int Dv, bool ds_ro
     off = align256(off + DS_TILE_BYTES);
   } else {
     c.ds_ws = c.zero_tile = SIZE_MAX;
-    c.dq_accum = off;  // rows of max(D_qk, 64) columns
-    off = align256(off + bh * n_qt * BQ * (size_t)(Dqk < 64 ? 64 : Dqk) * sizeof(float));
+    c.dq_accum = off;  // rows of 64 or 128 columns: the width of the main kernel that runs
+    off = align256(off + bh * n_qt * BQ * (size_t)(Dqk <= 64 ? 64 : 128) * sizeof(float));
   }
   c.counters = off;
   off = align256(off + (bh * n_qt + 1) * sizeof(int));
@@ -98,8 +98,9 @@ Carve carve(int B, int Hq, int Hkv, int Sq, int Skv, int Dqk, int Dv, bool ds_ro
 }
 
 bool dims_supported(int Dqk, int Dv) {
-  return (Dqk == 32 && Dv == 32) || (Dqk == 64 && Dv == 64) || (Dqk == 128 && Dv == 128) ||
-         (Dqk == 192 && Dv == 128);
+  // D_qk = D_v, a multiple of 8 up to 128: the 64- or 128-column kernels, the
+  // columns past D zero-filled by TMA; and the MLA pair 192/128.
+  return (Dqk == Dv && Dqk % 8 == 0 && Dqk >= 8 && Dqk <= 128) || (Dqk == 192 && Dv == 128);
 }
 
 int basic_checks(int B, int Hq, int Hkv, int Sq, int Skv, int Dqk, int Dv) {
@@ -381,7 +382,7 @@ int run_chain(const void* q, const void* k, const void* v, const void* o, const 
   p.dv = static_cast<__nv_bfloat16*>(dv);
   p.qstat = reinterpret_cast<float*>(ws + cv.qstat);
   p.dq_accum = ds_route ? nullptr : reinterpret_cast<float*>(ws + cv.dq_accum);
-  p.dq_acc_cols = D_qk < 64 ? 64 : D_qk;
+  p.dq_acc_cols = D_qk <= 64 ? 64 : 128;
   p.ds_ws = ds_route ? ws + cv.ds_ws : nullptr;
   p.zero_tile = ds_route ? ws + cv.zero_tile : nullptr;
   p.counters = reinterpret_cast<int*>(ws + cv.counters);

@@ -48,14 +48,16 @@ __device__ void zero_shared_dbias_rows(const ChainParams& p, unsigned bh, int qt
 // 256 / TPR rows per pass, all loads of a tile issued before any reduction.
 // Index arithmetic is done once per tile in 32 bits (the host rejects tensors
 // of 2^31 elements or more).
-template <int DV, bool F16>
+// TPR lanes share a row: D_v/8 of them load 8 values each (the rest, when D_v
+// is not a power-of-two multiple of 8, load nothing).
+template <int TPR, bool F16>
 __global__ void __launch_bounds__(256) sdpa_bwd_preprocess(const ChainParams p) {
   // The main kernel may start its prologue (barrier setup, TMEM allocation,
   // K/V loads) while this grid runs; it waits for completion before reading
   // anything written here.
   pdl_launch_dependents();
 
-  constexpr int TPR = DV / 8;              // lanes per query row
+  const int DV = p.Dv;                     // row width of O and dO
   constexpr int RPP = 256 / TPR;           // rows per pass
   constexpr int PASSES = BQ / RPP;         // passes per 64-row tile
   constexpr float LOG2E = 1.4426950408889634f;
@@ -77,7 +79,7 @@ __global__ void __launch_bounds__(256) sdpa_bwd_preprocess(const ChainParams p) 
 #pragma unroll
     for (int u = 0; u < PASSES; ++u) {
       const int q = qt * BQ + u * RPP + rsub;
-      if (q < Lq) {
+      if (q < Lq && sub * 8 < DV) {
         vo[u] = *reinterpret_cast<const uint4*>(o_base + (long long)q * DV);
         vd[u] = *reinterpret_cast<const uint4*>(do_base + (long long)q * DV);
       } else {
@@ -155,26 +157,26 @@ __global__ void __launch_bounds__(256) sdpa_bwd_preprocess(const ChainParams p) 
 // at or past the batch row's query length are written as zeros without being
 // read (the preprocess kernel did not clear them). The kernel also carries a
 // slice of the GQA group reduction of dK/dV (gqa.cuh).
-template <int DQK, int DV, bool F16>
+// ACC: the accumulator's row width (64 or 128, that of the main kernel that
+// ran); D_qk (<= ACC, a multiple of 8) is the width of dQ.
+template <int ACC, bool F16>
 __global__ void __launch_bounds__(256) sdpa_bwd_dq_convert(const ChainParams p) {
   pdl_wait_prior_grid();
-  gqa_reduce_slice<DQK, DV, F16>(p, blockIdx.x, gridDim.x, threadIdx.x, blockDim.x);
-  constexpr int CPR = DQK / 8;                 // 8-column chunks per row
-  constexpr int ITEMS = BQ * CPR / 256;        // items per thread
-  static_assert(BQ * CPR % 256 == 0, "whole items per thread");
+  gqa_reduce_slice<F16>(p, blockIdx.x, gridDim.x, threadIdx.x, blockDim.x);
+  const int DQK = p.Dqk;
+  const int CPR = DQK / 8;                      // 8-column chunks per row of dQ
+  constexpr int MAX_ITEMS = BQ * (ACC / 8) / 256;
   const unsigned bh = blockIdx.x / (unsigned)p.n_qt;
   const int qt = (int)(blockIdx.x - bh * (unsigned)p.n_qt);
   int Lq, Lk;
   batch_lengths(p, (int)(bh / (unsigned)p.Hq), Lq, Lk);
   const int rows = min(BQ, p.Sq - qt * BQ);         // rows of dQ in this tile
   const int live = max(0, min(rows, Lq - qt * BQ)); // rows holding accumulated values
-  // A D_qk of 32 accumulates in 64-column rows (the D 64 kernels' tiles).
-  constexpr int ACC = DQK < 64 ? 64 : DQK;
   const float* src = p.dq_accum + ((long long)bh * p.n_qt + qt) * BQ * ACC;
   __nv_bfloat16* dst = p.dq + ((long long)bh * p.Sq + (long long)qt * BQ) * DQK;
-  float4 a[ITEMS], c[ITEMS];
+  float4 a[MAX_ITEMS], c[MAX_ITEMS];
 #pragma unroll
-  for (int u = 0; u < ITEMS; ++u) {
+  for (int u = 0; u < MAX_ITEMS; ++u) {
     const int i = threadIdx.x + u * 256, r = i / CPR, c8 = i % CPR;
     if (r < live) {
       a[u] = *reinterpret_cast<const float4*>(src + r * ACC + c8 * 8);
@@ -184,7 +186,7 @@ __global__ void __launch_bounds__(256) sdpa_bwd_dq_convert(const ChainParams p) 
     }
   }
 #pragma unroll
-  for (int u = 0; u < ITEMS; ++u) {
+  for (int u = 0; u < MAX_ITEMS; ++u) {
     const int i = threadIdx.x + u * 256, r = i / CPR, c8 = i % CPR;
     if (r < rows) {
       uint4 out;
@@ -233,9 +235,9 @@ cudaError_t launch_dsink(const ChainParams& p, cudaStream_t s) {
 template <bool F16>
 static cudaError_t launch_preprocess_io(const ChainParams& p, cudaStream_t s) {
   const dim3 grid((unsigned)(p.B * p.Hq * p.n_qt));
-  if (p.Dv == 32) return launch_kernel(sdpa_bwd_preprocess<32, F16>, grid, dim3(256), 0, s, false, p);
-  if (p.Dv == 64) return launch_kernel(sdpa_bwd_preprocess<64, F16>, grid, dim3(256), 0, s, false, p);
-  return launch_kernel(sdpa_bwd_preprocess<128, F16>, grid, dim3(256), 0, s, false, p);
+  if (p.Dv <= 32) return launch_kernel(sdpa_bwd_preprocess<4, F16>, grid, dim3(256), 0, s, false, p);
+  if (p.Dv <= 64) return launch_kernel(sdpa_bwd_preprocess<8, F16>, grid, dim3(256), 0, s, false, p);
+  return launch_kernel(sdpa_bwd_preprocess<16, F16>, grid, dim3(256), 0, s, false, p);
 }
 
 cudaError_t launch_preprocess(const ChainParams& p, cudaStream_t s) {
@@ -245,9 +247,8 @@ cudaError_t launch_preprocess(const ChainParams& p, cudaStream_t s) {
 template <bool F16>
 static cudaError_t launch_dq_convert_io(const ChainParams& p, cudaStream_t s) {
   const dim3 grid((unsigned)(p.B * p.Hq * p.n_qt));
-  if (p.Dqk == 32) return launch_kernel(sdpa_bwd_dq_convert<32, 32, F16>, grid, dim3(256), 0, s, true, p);
-  if (p.Dqk == 64) return launch_kernel(sdpa_bwd_dq_convert<64, 64, F16>, grid, dim3(256), 0, s, true, p);
-  return launch_kernel(sdpa_bwd_dq_convert<128, 128, F16>, grid, dim3(256), 0, s, true, p);
+  if (p.dq_acc_cols == 64) return launch_kernel(sdpa_bwd_dq_convert<64, F16>, grid, dim3(256), 0, s, true, p);
+  return launch_kernel(sdpa_bwd_dq_convert<128, F16>, grid, dim3(256), 0, s, true, p);
 }
 
 cudaError_t launch_dq_convert(const ChainParams& p, cudaStream_t s) {

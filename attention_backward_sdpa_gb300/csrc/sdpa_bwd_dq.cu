@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       __nv_bfloat16* out = p.dq + ((long long)w.bh * p.Sq + q) * D;
       const bool have = w.n > 0;
       const int buf = done_units & 1;
-      gqa_reduce_slice<D, 128, F16>(p, blockIdx.x, gridDim.x, tid, 128, unit_idx++, n_pieces);
+      gqa_reduce_slice<F16>(p, blockIdx.x, gridDim.x, tid, 128, unit_idx++, n_pieces);
       if (have && ok) {
         ok = mbar_wait(&acc_full[buf], (done_units >> 1) & 1, abort_flag, DQ_WAIT_LIMIT_NS);
         __syncwarp();
@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       }
     }
     for (; unit_idx < n_pieces; ++unit_idx)
-      gqa_reduce_slice<D, 128, F16>(p, blockIdx.x, gridDim.x, tid, 128, unit_idx, n_pieces);
+      gqa_reduce_slice<F16>(p, blockIdx.x, gridDim.x, tid, 128, unit_idx, n_pieces);
   }
 
   tc_fence_before();

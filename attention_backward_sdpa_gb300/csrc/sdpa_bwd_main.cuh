@@ -823,7 +823,9 @@ template <bool BIAS, bool F16 = false>
 static cudaError_t launch_main_variant(const MainMaps& maps, const ChainParams& p, cudaStream_t s) {
   const dim3 grid((unsigned)(p.n_kt * p.B * p.Hkv * p.n_part));
   const dim3 block(MAIN_THREADS);
-  if (p.Dqk <= 64)  // a D_qk of 32 runs here, its columns 32..63 zero-filled by TMA
+  // D_qk = D_v up to 64 runs on the 64-column kernels, up to 128 on the 128-column
+  // ones: TMA zero-fills the columns past D on loads and drops them on stores.
+  if (p.Dqk <= 64)
     return launch_kernel(sdpa_bwd_main<64, false, BIAS, false, F16>, grid, block,
                          MainLayout<64, false>::BYTES, s, true, maps, p);
   if (p.ds_route)

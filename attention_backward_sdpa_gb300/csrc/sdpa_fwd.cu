@@ -542,10 +542,12 @@ template <bool BIAS, bool F16>
 static cudaError_t launch_fwd_variant(const FwdMaps& maps, const FwdParams& p, cudaStream_t s) {
   const dim3 grid((unsigned)(p.n_qt * p.B * p.Hq));
   const dim3 block(fwd_kernel::THREADS);
-  if (p.Dqk <= 64 && p.Dv == p.Dqk)  // D 32 runs here, columns 32..63 zero-filled by TMA
+  // D_qk = D_v up to 64 runs on the 64-column kernel, up to 128 on the 128-column
+  // one: TMA zero-fills the columns past D on loads and drops them on stores.
+  if (p.Dqk <= 64 && p.Dv == p.Dqk)
     return launch_kernel(sdpa_fwd_kernel<64, 64, BIAS, F16>, grid, block,
                          fwd_kernel::Layout<64, 64>::BYTES, s, false, maps, p);
-  if (p.Dqk == 128 && p.Dv == 128)
+  if (p.Dqk <= 128 && p.Dv == p.Dqk)
     return launch_kernel(sdpa_fwd_kernel<128, 128, BIAS, F16>, grid, block,
                          fwd_kernel::Layout<128, 128>::BYTES, s, false, maps, p);
   if (p.Dqk == 192 && p.Dv == 128)

@@ -53,7 +53,8 @@ def _a256(x):
 def expected_workspace(B, Hq, Hkv, Sq, Skv, Dqk, Dv, det=0):
     """Documented layout: per-query-tile row statistics (2 x 64 fp32 per 64-row tile);
     then either the fp32 dQ accumulator over whole 64-row tiles (rows of max(D_qk, 64)
-    columns: D_qk 32 runs on the 64-column kernels), or (deterministic,
+    columns: D_qk up to 64 runs on the 64-column kernels, up to 128 on the 128-column
+    ones), or (deterministic,
     D_qk = 128: two-kernel route) one 16 KiB bf16 dS^T tile per (128-key tile,
     64-query tile) plus one zero tile; one int per query tile plus a ticket; one fp32
     sink-token partial per query tile; and for GQA the bf16 dK/dV partials with H_q
@@ -63,7 +64,7 @@ def expected_workspace(B, Hq, Hkv, Sq, Skv, Dqk, Dv, det=0):
     if (det and Dqk == 128) or Dqk == 192:
         total += _a256(B * Hq * n_kt * n_qt * 16384) + _a256(16384)
     else:
-        total += _a256(B * Hq * n_qt * 64 * max(Dqk, 64) * 4)
+        total += _a256(B * Hq * n_qt * 64 * (64 if Dqk <= 64 else 128) * 4)
     total += _a256((B * Hq * n_qt + 1) * 4)
     total += _a256(B * Hq * n_qt * 4)
     if Hkv < Hq:
@@ -74,7 +75,8 @@ def expected_workspace(B, Hq, Hkv, Sq, Skv, Dqk, Dv, det=0):
 @pytest.mark.parametrize("shape", [(1, 2, 2, 128, 128, 64, 64), (2, 16, 16, 2048, 2048, 128, 128),
                                    (1, 32, 8, 4096, 4096, 128, 128), (3, 4, 1, 300, 177, 128, 128),
                                    (1, 1, 1, 1, 1, 64, 64), (1, 16, 16, 4096, 4096, 192, 128),
-                                   (2, 4, 2, 300, 177, 192, 128), (2, 4, 2, 300, 177, 32, 32)])
+                                   (2, 4, 2, 300, 177, 192, 128), (2, 4, 2, 300, 177, 32, 32),
+                                   (1, 3, 1, 200, 130, 96, 96), (2, 2, 2, 65, 70, 8, 8)])
 def test_workspace_size_matches_layout(lib, shape):
     for det in (0, 1):
         assert lib.sdpa_bwd_workspace_size(*shape, det) == expected_workspace(*shape, det=det)
@@ -82,7 +84,7 @@ def test_workspace_size_matches_layout(lib, shape):
 
 def test_workspace_size_rejects(lib):
     assert lib.sdpa_bwd_workspace_size(1, 3, 2, 128, 128, 128, 128, 0) == 0  # Hkv does not divide
-    assert lib.sdpa_bwd_workspace_size(1, 2, 2, 128, 128, 96, 96, 0) == 0    # head dim not served
+    assert lib.sdpa_bwd_workspace_size(1, 2, 2, 128, 128, 100, 100, 0) == 0  # head dim not served
     assert lib.sdpa_bwd_workspace_size(0, 2, 2, 128, 128, 128, 128, 0) == 0
     assert lib.sdpa_bwd_workspace_size(1, 2, 2, 0, 128, 128, 128, 0) == 0    # nothing to stage
 
@@ -102,7 +104,8 @@ def test_argument_validation(lib):
     assert call(lib, Hq=3, Hkv=2) == INVALID
     assert call(lib, B=0) == INVALID
     assert call(lib, Sq=-1) == INVALID
-    assert call(lib, Dqk=96, Dv=96) == UNSUPPORTED
+    assert call(lib, Dqk=100, Dv=100) == UNSUPPORTED   # not a multiple of 8
+    assert call(lib, Dqk=136, Dv=136) == UNSUPPORTED   # past 128 (other than 192/128)
     assert call(lib, Dqk=128, Dv=64) == UNSUPPORTED
     assert call(lib, Dqk=32, Dv=64) == UNSUPPORTED
     assert call(lib, Dqk=256, Dv=256) == UNSUPPORTED
@@ -162,7 +165,7 @@ def test_forward_argument_validation(lib):
     lib.sdpa_fwd.restype = ctypes.c_int
     assert call_fwd(lib, Hq=3, Hkv=2) == INVALID
     assert call_fwd(lib, B=0) == INVALID
-    assert call_fwd(lib, Dqk=96, Dv=96) == UNSUPPORTED
+    assert call_fwd(lib, Dqk=100, Dv=100) == UNSUPPORTED
     assert call_fwd(lib, Dqk=192, Dv=192) == UNSUPPORTED
     for i in range(5):
         ptrs = [FAKE] * 5
@@ -202,7 +205,7 @@ def test_bias_argument_validation(lib):
     assert call_bias(lib, FAKE + 1, dtype=0) == ALIGN         # bf16 bias: 2-byte alignment
     assert call_bias(lib, FAKE + 2, dtype=1) == ALIGN         # fp32 bias: 4-byte alignment
     assert call_bias(lib, FAKE, dbias=FAKE + 2) == ALIGN      # fp32 dBias: 4-byte alignment
-    assert call_bias(lib, FAKE, Dqk=96, Dv=96) == UNSUPPORTED
+    assert call_bias(lib, FAKE, Dqk=100, Dv=100) == UNSUPPORTED
 
 
 def test_forward_bias_argument_validation(lib):

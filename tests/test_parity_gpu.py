@@ -795,3 +795,42 @@ def test_d32_f16_bias_and_bitwise():
     for _ in range(9):
         for a, b in zip(first, gpu_backward(case, d)):
             assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+# Other multiples of 8 up to 128 run on the next larger kernel (64 or 128
+# columns) the same way; in deterministic mode those on the 128-column kernel
+# take the ordered relay (the stored-dS route is for exactly 128).
+DPAD_CASES = {
+    "d8_causal": W("d8_causal", 1, 2, 2, 150, 150, 8, 8, causal=True, seed=64),
+    "d40_gqa_window": W("d40_gqa_window", 1, 4, 2, 260, 230, 40, 40, causal=True, bottom_right=True,
+                        window_left=70, seed=65),
+    "d72_dense_cross": W("d72_dense_cross", 2, 2, 2, 190, 250, 72, 72, seed=66),
+    "d96_det_relay": W("d96_det", 1, 4, 2, 260, 260, 96, 96, causal=True, deterministic=True, seed=67),
+    "d120_padded": W("d120_padded", 2, 2, 2, 300, 300, 120, 120, causal=True, padded=(100, 300), seed=68),
+}
+
+
+@pytest.mark.parametrize("name", sorted(DPAD_CASES))
+def test_padded_head_dim_parity(name):
+    case = make_case(DPAD_CASES[name])
+    d = to_device(case)
+    dq, dk, dv = gpu_backward(case, d)
+    rq, rk, rv = oracle_backward(case)
+    assert_close("dq", dq.double().cpu().numpy(), rq)
+    assert_close("dk", dk.double().cpu().numpy(), rk)
+    assert_close("dv", dv.double().cpu().numpy(), rv)
+    o, lse = _gpu_fwd(case, d)
+    _check_fwd(case, o, lse)
+
+
+def test_padded_head_dim_f16_and_bitwise():
+    case = make_case(DPAD_CASES["d40_gqa_window"], io=torch.float16)
+    d = to_device(case)
+    for g, r, n in zip(gpu_backward(case, d), oracle_backward(case), ("dq", "dk", "dv")):
+        assert_close(n, g.double().cpu().numpy(), r)
+    case = make_case(DPAD_CASES["d96_det_relay"])
+    d = to_device(case)
+    first = [t.clone() for t in gpu_backward(case, d)]
+    for _ in range(9):
+        for a, b in zip(first, gpu_backward(case, d)):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
