@@ -610,21 +610,22 @@ def main(argv=None):
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
     args.steps = max(args.steps, 1)
-    rank, world, local = init_dist()
     w = workloads.WORKLOADS[args.workload]
+    # option checks first: no process group or device is touched for a bad line
+    if args.io == "f16" and (args.bias != "none" or args.qat):
+        ap.error("--io f16: the plain chain (a bias or QAT needs bf16)")
+    if args.qat and (w.Dqk != 128 or w.Dv != 128 or w.deterministic or args.bias != "none"
+                     or args.sink or args.pass_ != "bwd"):
+        ap.error("--qat: a D = 128 non-deterministic workload, backward, no bias or sink")
+    rank, world, local = init_dist()
     if args.impl == "reference":
         run_reference(args, w, rank, world)
         return 0
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     io = torch.float16 if args.io == "f16" else torch.bfloat16
-    if args.io == "f16" and (args.bias != "none" or args.qat):
-        ap.error("--io f16: the plain chain (a bias or QAT needs bf16)")
     t = workloads.generate(w, io)
     if args.qat:
-        if w.Dqk != 128 or w.Dv != 128 or w.deterministic or args.bias != "none" or args.sink \
-                or args.pass_ != "bwd":
-            ap.error("--qat: a D = 128 non-deterministic workload, backward, no bias or sink")
         t["qat"] = True
     if args.bias != "none":
         t["bias"] = workloads.bias_tensor(w, 1 if args.bias == "1" else w.B,

@@ -57,3 +57,33 @@ def test_two_rank_reduction_and_broadcast():
         res = dict(out)
     assert res[0][0] == res[1][0] == 2.5          # max over ranks
     assert res[0][1] == res[1][1] == [0.0, 0.0, 0.0]  # rank 0's tensor on every rank
+
+
+@pytest.mark.parametrize("argv", [["--qat", "--workload", "causal_gqa_det"],     # deterministic
+                                  ["--qat", "--workload", "mla_br_causal"],      # D 192
+                                  ["--qat", "--bias", "B"],
+                                  ["--io", "f16", "--bias", "1"],
+                                  ["--io", "f16", "--qat"]])
+def test_bench_rejects_unsupported_combinations(argv):
+    """The option checks run before any GPU work (argparse exits with status 2)."""
+    with pytest.raises(SystemExit) as e:
+        bench.main(argv + ["--steps", "1", "--warmup", "3"])
+    assert e.value.code == 2
+
+
+def test_bias_bytes_and_traffic_keys():
+    w = workloads.WORKLOADS["causal_mha"]
+    pairs = bench.visible_pairs(w, None)
+    b = torch.zeros((2, 16, 2048, 2048), dtype=torch.bfloat16)
+    nbytes = bench.main_kernel_bytes_bias(w, pairs, b)
+    # bias at the visible pairs + every fp32 dBias element + Q, dO, K, V, dK, dV, dQ accumulator
+    expect = pairs * 2 + b.numel() * 4 + 2 * 2 * 16 * 2048 * 128 * 2 + 2 * (2 * 16 * 2048 * 256 * 2) \
+        + 2 * 2 * 16 * 2048 * 128 * 4
+    assert nbytes == expect
+    t = {"q": torch.zeros(2, 1, 1, 1, dtype=torch.bfloat16), "bias": b}
+    assert bench.bias_tag(t) == "bias-B-bf16"
+    t["bias"] = torch.zeros((1, 16, 2048, 2048), dtype=torch.float32)
+    assert bench.bias_tag(t) == "bias-shared-f32"
+    assert bench.bias_tag({"q": t["q"], "qat": True}) == "qat"
+    assert bench.bias_tag({"q": t["q"].half()}) == "f16"
+    assert bench.bias_tag({"q": t["q"]}) is None
