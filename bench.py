@@ -382,13 +382,13 @@ def cpu_baseline_leg(w, t, target_s=12.0):
 MAIN_SOURCES = {"sdpa_bwd_main": ("sdpa_bwd_main.cuh", "common.cuh", "ptx.cuh", "nvfp4.cuh", "bias.cuh"),
                 "sdpa_bwd_main_ds": ("sdpa_bwd_main_ds.cu", "common.cuh", "ptx.cuh", "bias.cuh")}
 MAIN_TRAFFIC = {
-    "9f0248d141f4a824": {"causal_mha": 113898496 + 31285248,
-                         "causal_gqa_det": 124068864 + 513333504,
-                         "swa_causal_padded": 246296320 + 186098432,
-                         "causal_mha/bias-B-f32": 468734976 + 583854592,
-                         "causal_mha/qat": 112215808 + 27959808},
-    "595df10a88242d87": {"mla_br_causal": 132132352 + 263815680,
-                         "mla_br_causal/bias-B-bf16": 425211136 + 1330963456},
+    "5323b92209cf2a25": {"causal_mha": 114467072 + 31501056,
+                         "causal_gqa_det": 123357696 + 513710592,
+                         "swa_causal_padded": 247575296 + 186622208,
+                         "causal_mha/bias-B-f32": 469117696 + 584227328,
+                         "causal_mha/qat": 113707264 + 30040832},
+    "08f360987d2b81ca": {"mla_br_causal": 132029184 + 263661568,
+                         "mla_br_causal/bias-B-bf16": 425198848 + 1331085056},
 }
 
 
