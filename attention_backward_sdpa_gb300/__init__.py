@@ -66,9 +66,9 @@ def load(build_if_missing: bool = False):
     lib.sdpa_fwd.restype = i
     lib.sdpa_fwd_bias.argtypes = list(lib.sdpa_fwd.argtypes[:-1]) + [vp, i, i, vp]
     lib.sdpa_fwd_bias.restype = i
-    lib.sdpa_bwd_typed.argtypes = [i] + list(lib.sdpa_bwd.argtypes[:-1]) + [vp, vp, vp]
+    lib.sdpa_bwd_typed.argtypes = [i] + list(lib.sdpa_bwd.argtypes[:-1]) + [vp, vp, vp, i, i, vp, vp]
     lib.sdpa_bwd_typed.restype = i
-    lib.sdpa_fwd_typed.argtypes = [i] + list(lib.sdpa_fwd.argtypes)
+    lib.sdpa_fwd_typed.argtypes = [i] + list(lib.sdpa_fwd.argtypes[:-1]) + [vp, i, i, vp]
     lib.sdpa_fwd_typed.restype = i
     lib.sdpa_nvfp4_fake_quant.argtypes = [vp, vp, ctypes.c_longlong, vp]
     lib.sdpa_nvfp4_fake_quant.restype = i
@@ -188,16 +188,26 @@ def sdpa_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
             _ptr(dv), B, Hq, Hkv, Sq, Skv, Dqk, Dv, sc, int(causal), int(bottom_right),
             int(window_left), int(window_right), int(deterministic), _ptr(seq_q_lens),
             _ptr(seq_kv_lens), _ptr(workspace), ws_bytes)
-    if io == torch.float16:  # fp16 io: the typed entry (sink optional, no bias)
-        if bias is not None:
-            raise ValueError("an additive bias needs bf16 io tensors")
+    if io == torch.float16:  # fp16 io: the general typed entry (sink and bias optional)
         if sink is not None:
             dsink = torch.empty_like(sink) if dsink is None else dsink
+        bias_dtype, bias_batch = 0, 0
+        if bias is not None:
+            bias_dtype = _check_bias(bias, B, Hq, Sq, Skv)
+            bias_batch = int(bias.shape[0])
+            if bias_grad:
+                dbias = torch.empty(bias.shape, dtype=torch.float32, device=bias.device) \
+                    if dbias is None else dbias
+            else:
+                dbias = None
+        else:
+            dbias = None
         rc = lib.sdpa_bwd_typed(_IO_CODES[io], *args, _ptr(sink), _ptr(dsink if sink is not None else None),
-                                _stream_handle(stream))
+                                _ptr(bias), bias_dtype, bias_batch, _ptr(dbias), _stream_handle(stream))
         if rc != 0:
             raise SdpaError(rc, "sdpa_bwd_typed")
-        return (dq, dk, dv) if sink is None else (dq, dk, dv, dsink)
+        out = (dq, dk, dv) + ((dsink,) if sink is not None else ())
+        return out + ((dbias,) if bias is not None and bias_grad else ())
     if sink is None and bias is None:
         rc = lib.sdpa_bwd(*args, _stream_handle(stream))
         if rc != 0:
@@ -233,17 +243,17 @@ def sdpa_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
 
 
 # Element-type codes of the C ABI (sdpa_dtype).
-DTYPE_BF16, DTYPE_F32 = 0, 1
+DTYPE_BF16, DTYPE_F32, DTYPE_F16 = 0, 1, 2
 
 
 def _check_bias(bias, B, Hq, Sq, Skv) -> int:
     if not isinstance(bias, torch.Tensor) or not bias.is_cuda or not bias.is_contiguous():
         raise ValueError("bias must be a contiguous CUDA tensor")
-    if bias.dtype not in (torch.bfloat16, torch.float32):
-        raise ValueError("bias must be bf16 or fp32")
+    if bias.dtype not in (torch.bfloat16, torch.float16, torch.float32):
+        raise ValueError("bias must be bf16, fp16 or fp32")
     if bias.dim() != 4 or bias.shape[0] not in (1, B) or tuple(bias.shape[1:]) != (Hq, Sq, Skv):
         raise ValueError(f"bias must be (1|B, Hq, Sq, Skv), got {tuple(bias.shape)}")
-    return DTYPE_F32 if bias.dtype == torch.float32 else DTYPE_BF16
+    return {torch.float32: DTYPE_F32, torch.float16: DTYPE_F16}.get(bias.dtype, DTYPE_BF16)
 
 
 def sdpa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: Optional[float] = None,
@@ -285,9 +295,9 @@ def sdpa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: Option
             int(causal), int(bottom_right), int(window_left), int(window_right),
             _ptr(seq_q_lens), _ptr(seq_kv_lens), _ptr(sink))
     if io == torch.float16:
-        if bias is not None:
-            raise ValueError("an additive bias needs bf16 io tensors")
-        rc = lib.sdpa_fwd_typed(_IO_CODES[io], *args, _stream_handle(stream))
+        bias_dtype = _check_bias(bias, B, Hq, Sq, Skv) if bias is not None else 0
+        rc = lib.sdpa_fwd_typed(_IO_CODES[io], *args, _ptr(bias), bias_dtype,
+                                0 if bias is None else int(bias.shape[0]), _stream_handle(stream))
     elif bias is None:
         rc = lib.sdpa_fwd(*args, _stream_handle(stream))
     else:

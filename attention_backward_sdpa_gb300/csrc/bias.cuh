@@ -11,7 +11,7 @@
 namespace sdpa {
 
 // Bias column of one query tile for this thread's key: bz[i] = bias(q0 + i, k)
-// (0 past S_q or S_kv). `off` is the element offset of (batch row, head, q0, k).
+// (0 past S_q or S_kv); bf16, fp16 or fp32 elements. `off` is the element offset of (batch row, head, q0, k).
 template <int N>
 __device__ __forceinline__ void load_bias_column(const ChainParams& p, long long off, bool key_in,
                                                  int q0, float (&bz)[N]) {
@@ -28,13 +28,13 @@ __device__ __forceinline__ void load_bias_column(const ChainParams& p, long long
     }
   } else {
     const unsigned short* src = static_cast<const unsigned short*>(p.bias) + off;
+    const bool f16 = p.bias_f16 != 0;
     if (rows == N) {
 #pragma unroll
-      for (int i = 0; i < N; ++i) bz[i] = __uint_as_float((uint32_t)__ldcs(src + i * ld) << 16);
+      for (int i = 0; i < N; ++i) bz[i] = bias16_to_f32(__ldcs(src + i * ld), f16);
     } else {
 #pragma unroll
-      for (int i = 0; i < N; ++i)
-        bz[i] = i < rows ? __uint_as_float((uint32_t)__ldcs(src + i * ld) << 16) : 0.f;
+      for (int i = 0; i < N; ++i) bz[i] = i < rows ? bias16_to_f32(__ldcs(src + i * ld), f16) : 0.f;
     }
   }
 }

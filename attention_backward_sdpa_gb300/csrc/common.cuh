@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <utility>
@@ -72,6 +73,7 @@ struct ChainParams {
   // with dbias_red the batch rows' terms are added atomically into one batch.
   const void* bias;     // or null
   int bias_fp32;
+  int bias_f16;         // 16-bit bias elements are fp16 (else bf16)
   long long bias_bstride;
   float* dbias;         // or null
   long long dbias_bstride;
@@ -128,6 +130,7 @@ struct FwdParams {
   // bias[b * bias_bstride + (h * Sq + q) * Skv + k], bf16 or fp32.
   const void* bias;
   int bias_fp32;
+  int bias_f16;               // 16-bit bias elements are fp16 (else bf16)
   long long bias_bstride;
   int bias_vec;               // rows allow 16-byte loads (S_kv * size % 16 == 0, base aligned)
   float* lse;                 // (B, Hq, Sq) output
@@ -192,6 +195,11 @@ __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; 
 // floor(a / b) for b > 0 and any sign of a.
 __host__ __device__ inline long long floor_div(long long a, long long b) {
   return a >= 0 ? a / b : -((-a + b - 1) / b);
+}
+
+// A 16-bit bias element (bf16, or fp16 when f16) widened to fp32.
+__device__ __forceinline__ float bias16_to_f32(unsigned short v, bool f16) {
+  return f16 ? __half2float(__ushort_as_half(v)) : __uint_as_float((uint32_t)v << 16);
 }
 
 // Valid lengths of batch row b (the full S when no length array is given).

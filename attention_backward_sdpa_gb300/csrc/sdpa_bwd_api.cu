@@ -284,14 +284,15 @@ int run_chain(const void* q, const void* k, const void* v, const void* o, const 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   int rc = basic_checks(B, H_q, H_kv, S_q, S_kv, D_qk, D_v);
   if (rc != SDPA_OK) return rc;
-  // fp16 io: the plain chain (and sink tokens); the bias and QAT paths are bf16.
-  if (f16 && (qat || ba.bias)) return SDPA_ERR_UNSUPPORTED;
+  // The QAT path is bf16 (the page's QAT kernels take BF16 activations only).
+  if (f16 && qat) return SDPA_ERR_UNSUPPORTED;
   // NVFP4 QAT: D 128, the dQ-reduction route, no bias or sink.
   if (qat && (D_qk != 128 || D_v != 128)) return SDPA_ERR_UNSUPPORTED;
   if (!q || !k || !v || !o || !d_o || !lse || !dq || !dk || !dv) return SDPA_ERR_INVALID;
   if (dsink && !sink) return SDPA_ERR_INVALID;
   if (ba.bias) {
-    if (ba.dtype != SDPA_DTYPE_BF16 && ba.dtype != SDPA_DTYPE_F32) return SDPA_ERR_INVALID;
+    if (ba.dtype != SDPA_DTYPE_BF16 && ba.dtype != SDPA_DTYPE_F32 && ba.dtype != SDPA_DTYPE_F16)
+      return SDPA_ERR_INVALID;
     if (ba.batch != 1 && ba.batch != B) return SDPA_ERR_INVALID;
     // A one-batch dBias summed over B > 1 batch rows is added atomically: not
     // reproducible, so deterministic mode rejects it.
@@ -401,6 +402,7 @@ int run_chain(const void* q, const void* k, const void* v, const void* o, const 
     const bool shared = ba.batch == 1 && B > 1;
     p.bias = ba.bias;
     p.bias_fp32 = ba.dtype == SDPA_DTYPE_F32 ? 1 : 0;
+    p.bias_f16 = ba.dtype == SDPA_DTYPE_F16 ? 1 : 0;
     p.bias_bstride = shared ? 0 : per_batch;
     p.dbias = ba.dbias;
     p.dbias_bstride = shared ? 0 : per_batch;
@@ -477,14 +479,14 @@ int run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   int rc = basic_checks(B, H_q, H_kv, S_q, S_kv, D_qk, D_v);
   if (rc != SDPA_OK) return rc;
-  if (f16 && ba.bias) return SDPA_ERR_UNSUPPORTED;
   if (!q || !k || !v || !o || !lse) return SDPA_ERR_INVALID;
   for (const void* ptr : {q, k, v, (const void*)o})
     if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return SDPA_ERR_ALIGN;
   for (const void* ptr : {(const void*)lse, (const void*)sink})
     if (reinterpret_cast<uintptr_t>(ptr) % 4 != 0) return SDPA_ERR_ALIGN;
   if (ba.bias) {
-    if (ba.dtype != SDPA_DTYPE_BF16 && ba.dtype != SDPA_DTYPE_F32) return SDPA_ERR_INVALID;
+    if (ba.dtype != SDPA_DTYPE_BF16 && ba.dtype != SDPA_DTYPE_F32 && ba.dtype != SDPA_DTYPE_F16)
+      return SDPA_ERR_INVALID;
     if (ba.batch != 1 && ba.batch != B) return SDPA_ERR_INVALID;
     if (reinterpret_cast<uintptr_t>(ba.bias) % (ba.dtype == SDPA_DTYPE_F32 ? 4 : 2) != 0)
       return SDPA_ERR_ALIGN;
@@ -517,6 +519,7 @@ int run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
     const int esz = ba.dtype == SDPA_DTYPE_F32 ? 4 : 2;
     p.bias = ba.bias;
     p.bias_fp32 = esz == 4;
+    p.bias_f16 = ba.dtype == SDPA_DTYPE_F16 ? 1 : 0;
     p.bias_bstride = (ba.batch == 1) ? 0 : (long long)H_q * S_q * S_kv;
     p.bias_vec = ((long long)S_kv * esz) % 16 == 0 && reinterpret_cast<uintptr_t>(ba.bias) % 16 == 0;
   }
@@ -552,10 +555,14 @@ int sdpa_fwd_typed(int io_dtype, const void* q, const void* k, const void* v, vo
                    int B, int H_q, int H_kv, int S_q, int S_kv, int D_qk, int D_v, float scale,
                    int causal, int bottom_right, int window_left, int window_right,
                    const int32_t* seq_q_lens, const int32_t* seq_kv_lens, const float* sink,
-                   void* stream) {
+                   const void* bias, int bias_dtype, int bias_batch, void* stream) {
   if (io_dtype != SDPA_DTYPE_BF16 && io_dtype != SDPA_DTYPE_F16) return SDPA_ERR_INVALID;
+  BiasArgs ba;
+  ba.bias = bias;
+  ba.dtype = bias_dtype;
+  ba.batch = bias_batch;
   return run_fwd(q, k, v, o, lse, B, H_q, H_kv, S_q, S_kv, D_qk, D_v, scale, causal, bottom_right,
-                 window_left, window_right, seq_q_lens, seq_kv_lens, sink, BiasArgs{}, stream,
+                 window_left, window_right, seq_q_lens, seq_kv_lens, sink, ba, stream,
                  io_dtype == SDPA_DTYPE_F16);
 }
 
@@ -590,12 +597,19 @@ int sdpa_bwd_typed(int io_dtype, const void* q, const void* k, const void* v, co
                    int H_kv, int S_q, int S_kv, int D_qk, int D_v, float scale, int causal,
                    int bottom_right, int window_left, int window_right, int deterministic,
                    const int32_t* seq_q_lens, const int32_t* seq_kv_lens, void* workspace,
-                   size_t workspace_bytes, const float* sink, float* dsink, void* stream) {
+                   size_t workspace_bytes, const float* sink, float* dsink, const void* bias,
+                   int bias_dtype, int bias_batch, float* dbias, void* stream) {
   if (io_dtype != SDPA_DTYPE_BF16 && io_dtype != SDPA_DTYPE_F16) return SDPA_ERR_INVALID;
   if (dsink && !sink) return SDPA_ERR_INVALID;
+  if (!bias && dbias) return SDPA_ERR_INVALID;
+  BiasArgs ba;
+  ba.bias = bias;
+  ba.dtype = bias_dtype;
+  ba.batch = bias_batch;
+  ba.dbias = dbias;
   return run_chain(q, k, v, o, d_o, lse, dq, dk, dv, B, H_q, H_kv, S_q, S_kv, D_qk, D_v, scale,
                    causal, bottom_right, window_left, window_right, deterministic, seq_q_lens,
-                   seq_kv_lens, workspace, workspace_bytes, dsink ? sink : nullptr, dsink, BiasArgs{},
+                   seq_kv_lens, workspace, workspace_bytes, dsink ? sink : nullptr, dsink, ba,
                    stream, false, io_dtype == SDPA_DTYPE_F16);
 }
 

@@ -5,10 +5,14 @@
 
 namespace sdpa {
 
-cudaError_t main_bias_kernel_setup() { return main_variant_setup<true>(); }
+cudaError_t main_bias_kernel_setup() {
+  cudaError_t e = main_variant_setup<true, false>();
+  if (e == cudaSuccess) e = main_variant_setup<true, true>();
+  return e;
+}
 
 cudaError_t launch_main_bias(const MainMaps& maps, const ChainParams& p, cudaStream_t s) {
-  return launch_main_variant<true>(maps, p, s);
+  return p.f16 ? launch_main_variant<true, true>(maps, p, s) : launch_main_variant<true, false>(maps, p, s);
 }
 
 }  // namespace sdpa

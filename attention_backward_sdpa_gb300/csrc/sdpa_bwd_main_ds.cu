@@ -566,6 +566,7 @@ cudaError_t main_ds_kernel_setup() {
   cudaError_t e = set_ds_smem<192, 128, false>();
   if (e == cudaSuccess) e = set_ds_smem<192, 128, true>();
   if (e == cudaSuccess) e = set_ds_smem<192, 128, false, true>();
+  if (e == cudaSuccess) e = set_ds_smem<192, 128, true, true>();
   return e;
 }
 
@@ -573,6 +574,9 @@ cudaError_t launch_main_ds(const MainMaps& maps, const ChainParams& p, cudaStrea
   const dim3 grid((unsigned)(p.n_kt * p.B * p.Hq));
   const dim3 block(ds_kernel::THREADS);
   if (p.Dqk != 192 || p.Dv != 128) return cudaErrorInvalidValue;
+  if (p.bias != nullptr && p.f16)
+    return launch_kernel(sdpa_bwd_main_ds<192, 128, true, true>, grid, block,
+                         ds_kernel::Layout<192, 128>::BYTES, s, true, maps, p);
   if (p.bias != nullptr)
     return launch_kernel(sdpa_bwd_main_ds<192, 128, true>, grid, block,
                          ds_kernel::Layout<192, 128>::BYTES, s, true, maps, p);

@@ -90,7 +90,7 @@ struct Layout {
 }  // namespace fwd_kernel
 
 // This row's bias for keys kb .. kb + 63 as 32-bit words: on the 16-byte path
-// bf16 pairs (`packed`, 32 words) or fp32 values (64 words); otherwise fp32
+// 16-bit pairs (`packed`, 32 words) or fp32 values (64 words); otherwise fp32
 // values from scalar loads, 0 past S_kv.
 __device__ __forceinline__ void load_fwd_bias_row(const FwdParams& p, long long row_off, int kb, bool live,
                                                   uint32_t (&raw)[64], bool& packed) {
@@ -125,15 +125,15 @@ __device__ __forceinline__ void load_fwd_bias_row(const FwdParams& p, long long 
       float x = 0.f;
       if (kb + i < p.Skv)
         x = p.bias_fp32 ? __ldcs(static_cast<const float*>(p.bias) + row_off + kb + i)
-                        : __uint_as_float((uint32_t)__ldcs(static_cast<const unsigned short*>(p.bias) +
-                                                           row_off + kb + i) << 16);
+                        : bias16_to_f32(__ldcs(static_cast<const unsigned short*>(p.bias) + row_off + kb + i),
+                                        p.bias_f16 != 0);
       raw[i] = __float_as_uint(x);
     }
   }
 }
 
-__device__ __forceinline__ float fwd_bias_at(const uint32_t (&raw)[64], bool packed, int i) {
-  return packed ? __uint_as_float((i & 1) ? (raw[i >> 1] & 0xFFFF0000u) : (raw[i >> 1] << 16))
+__device__ __forceinline__ float fwd_bias_at(const uint32_t (&raw)[64], bool packed, bool f16, int i) {
+  return packed ? bias16_to_f32((unsigned short)((i & 1) ? (raw[i >> 1] >> 16) : (raw[i >> 1] & 0xFFFFu)), f16)
                 : __uint_as_float(raw[i]);
 }
 
@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 64; ++i)
           sr[i >> 5][i & 31] = __float_as_uint(
-              fmaf(__uint_as_float(sr[i >> 5][i & 31]), c, fwd_bias_at(braw, bpacked, i) * LOG2E_F));
+              fmaf(__uint_as_float(sr[i >> 5][i & 31]), c, fwd_bias_at(braw, bpacked, p.bias_f16 != 0, i) * LOG2E_F));
       }
       // Visible keys of this row within the tile: [v_lo, v_hi] relative to k0.
       int v_lo = 0, v_hi = BK - 1;
@@ -535,6 +535,7 @@ cudaError_t fwd_kernel_setup() {
   cudaError_t e = fwd_setup_variant<false, false>();
   if (e == cudaSuccess) e = fwd_setup_variant<true, false>();
   if (e == cudaSuccess) e = fwd_setup_variant<false, true>();
+  if (e == cudaSuccess) e = fwd_setup_variant<true, true>();
   return e;
 }
 
@@ -556,9 +557,9 @@ static cudaError_t launch_fwd_variant(const FwdMaps& maps, const FwdParams& p, c
   return cudaErrorInvalidValue;
 }
 
-// The bias variants are bf16 only (the host rejects a bias with fp16 io).
 cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, cudaStream_t s) {
-  if (p.bias) return launch_fwd_variant<true, false>(maps, p, s);
+  if (p.bias)
+    return p.f16 ? launch_fwd_variant<true, true>(maps, p, s) : launch_fwd_variant<true, false>(maps, p, s);
   return p.f16 ? launch_fwd_variant<false, true>(maps, p, s) : launch_fwd_variant<false, false>(maps, p, s);
 }
 

@@ -54,9 +54,8 @@ typedef enum {
   SDPA_ERR_TIMEOUT = 6      /* a device-side bounded wait ran out (reported later)  */
 } sdpa_status;
 
-/* Element types: of an optional additive bias (sdpa_bwd_bias, sdpa_fwd_bias:
- * BF16 or F32) and of the io tensors (sdpa_bwd_typed, sdpa_fwd_typed: BF16 or
- * F16). */
+/* Element types: of an optional additive bias (BF16, F16 or F32) and of the
+ * io tensors (sdpa_bwd_typed, sdpa_fwd_typed: BF16 or F16). */
 typedef enum {
   SDPA_DTYPE_BF16 = 0,
   SDPA_DTYPE_F32 = 1,
@@ -154,8 +153,8 @@ int sdpa_bwd_sink(const void* q, const void* k, const void* v, const void* o, co
  * Arguments: those of sdpa_bwd_sink(), where sink and dsink may both be NULL
  * (no sink) or dsink alone NULL (a sink in the forward's LSE, no dsink), then
  *   bias        device (bias_batch, H_q, S_q, S_kv) tensor, contiguous, S_kv
- *               innermost; bf16 (2-byte aligned) or fp32 (4-byte aligned).
- *   bias_dtype  SDPA_DTYPE_BF16 or SDPA_DTYPE_F32.
+ *               innermost; bf16 or fp16 (2-byte aligned), or fp32 (4-byte aligned).
+ *   bias_dtype  SDPA_DTYPE_BF16, SDPA_DTYPE_F16 or SDPA_DTYPE_F32.
  *   bias_batch  1 (one bias shared by every batch row) or B.
  *   dbias       device fp32 output shaped like bias (4-byte aligned), or NULL.
  *               Every element is overwritten. With bias_batch = B, or B = 1,
@@ -206,10 +205,10 @@ int sdpa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
  * keys all have a -inf bias gets O = 0 and LSE = -inf (or the sink).
  * Arguments: those of sdpa_fwd(), then
  *   bias        device (bias_batch, H_q, S_q, S_kv) tensor, contiguous, S_kv
- *               innermost; bf16 (2-byte aligned) or fp32 (4-byte aligned).
+ *               innermost; bf16 or fp16 (2-byte aligned), or fp32 (4-byte aligned).
  *               Rows are read with 16-byte loads when S_kv times the element
  *               size is a multiple of 16 and bias is 16-byte aligned.
- *   bias_dtype  SDPA_DTYPE_BF16 or SDPA_DTYPE_F32.
+ *   bias_dtype  SDPA_DTYPE_BF16, SDPA_DTYPE_F16 or SDPA_DTYPE_F32.
  *   bias_batch  1 (one bias for every batch row) or B.
  * Returns SDPA_ERR_INVALID for a NULL bias, an unknown dtype or bias_batch
  * not 1 or B; otherwise as sdpa_fwd().
@@ -221,32 +220,39 @@ int sdpa_fwd_bias(const void* q, const void* k, const void* v, void* o, float* l
                   int bias_batch, void* stream);
 
 /*
- * SDPA backward with the io element type as an argument ("SDPA Backward
- * (SM120)", support surface: FP16 / BF16, LSE fp32). io_dtype is
- * SDPA_DTYPE_BF16 (exactly sdpa_bwd_sink() / sdpa_bwd()) or SDPA_DTYPE_F16: q,
- * k, v, o, d_o, dq, dk and dv are fp16, the GEMMs take fp16 operands (P and
- * dS rounded to fp16), and every accumulation stays fp32. The other arguments
- * are those of sdpa_bwd_sink(), where sink and dsink may both be NULL.
- * Returns SDPA_ERR_INVALID for another io_dtype; otherwise as sdpa_bwd().
- * The workspace size does not depend on the io type.
+ * The general SDPA backward: the io element type as an argument ("SDPA
+ * Backward (SM120)", support surface: FP16 / BF16, LSE fp32) and every optional
+ * input of the other entry points. io_dtype is SDPA_DTYPE_BF16 or
+ * SDPA_DTYPE_F16: with F16, q, k, v, o, d_o, dq, dk and dv are fp16, the GEMMs
+ * take fp16 operands (P and dS rounded to fp16), and every accumulation stays
+ * fp32. sink/dsink are as in sdpa_bwd_sink() and bias/bias_dtype/bias_batch/
+ * dbias as in sdpa_bwd_bias(), each optional (NULL: absent); bias_dtype may
+ * also be SDPA_DTYPE_F16 (the io type of an fp16 call, or any call).
+ * With io_dtype BF16 and no bias this is sdpa_bwd_sink() / sdpa_bwd().
+ * Returns SDPA_ERR_INVALID for another io_dtype, or dsink without sink, or
+ * dbias without bias; otherwise as sdpa_bwd_bias(). The workspace size does
+ * not depend on the io type.
  */
 int sdpa_bwd_typed(int io_dtype, const void* q, const void* k, const void* v, const void* o,
                    const void* d_o, const float* lse, void* dq, void* dk, void* dv, int B, int H_q,
                    int H_kv, int S_q, int S_kv, int D_qk, int D_v, float scale, int causal,
                    int bottom_right, int window_left, int window_right, int deterministic,
                    const int32_t* seq_q_lens, const int32_t* seq_kv_lens, void* workspace,
-                   size_t workspace_bytes, const float* sink, float* dsink, void* stream);
+                   size_t workspace_bytes, const float* sink, float* dsink, const void* bias,
+                   int bias_dtype, int bias_batch, float* dbias, void* stream);
 
 /*
- * SDPA forward with the io element type as an argument: sdpa_fwd() for
- * io_dtype SDPA_DTYPE_BF16, or with fp16 q, k, v and o (P rounded to fp16 for
- * the PV GEMM) for SDPA_DTYPE_F16. Returns SDPA_ERR_INVALID for another io_dtype.
+ * The general SDPA forward: sdpa_fwd() / sdpa_fwd_bias() with the io element
+ * type as an argument (SDPA_DTYPE_BF16, or SDPA_DTYPE_F16: fp16 q, k, v and o,
+ * P rounded to fp16 for the PV GEMM) and an optional bias (NULL: none; bf16,
+ * fp16 or fp32). Returns SDPA_ERR_INVALID for another io_dtype; otherwise as
+ * sdpa_fwd_bias().
  */
 int sdpa_fwd_typed(int io_dtype, const void* q, const void* k, const void* v, void* o, float* lse,
                    int B, int H_q, int H_kv, int S_q, int S_kv, int D_qk, int D_v, float scale,
                    int causal, int bottom_right, int window_left, int window_right,
                    const int32_t* seq_q_lens, const int32_t* seq_kv_lens, const float* sink,
-                   void* stream);
+                   const void* bias, int bias_dtype, int bias_batch, void* stream);
 
 /*
  * NVFP4 fake quantization ("NVFP4 Attention QAT Backward" page, Overview):

@@ -196,7 +196,7 @@ def call_bias(lib, bias, dtype=0, batch=1, dbias=FAKE, B=1, det=0, Dqk=128, Dv=1
 def test_bias_argument_validation(lib):
     lib.sdpa_bwd_bias.restype = ctypes.c_int
     assert call_bias(lib, None) == INVALID
-    assert call_bias(lib, FAKE, dtype=2) == INVALID          # unknown element type
+    assert call_bias(lib, FAKE, dtype=3) == INVALID          # unknown element type
     assert call_bias(lib, FAKE, batch=3, B=2) == INVALID     # bias batch is 1 or B
     assert call_bias(lib, FAKE, batch=0) == INVALID
     # a one-batch dBias summed over B > 1 batch rows is atomic: not in deterministic mode
@@ -252,15 +252,20 @@ def test_typed_entry_validation(lib):
     lib.sdpa_fwd_typed.restype = ctypes.c_int
     vp = [ctypes.c_void_p(FAKE)] * 9
 
-    def bwd(io, sink=None, dsink=None):
+    def bwd(io, sink=None, dsink=None, bias=None, bias_dtype=0, dbias=None):
         return lib.sdpa_bwd_typed(io, *vp, 1, 2, 2, 128, 128, 128, 128, ctypes.c_float(0.0), 0, 0, -1,
                                   -1, 0, None, None, None, ctypes.c_size_t(0),
                                   None if sink is None else ctypes.c_void_p(sink),
-                                  None if dsink is None else ctypes.c_void_p(dsink), None)
+                                  None if dsink is None else ctypes.c_void_p(dsink),
+                                  None if bias is None else ctypes.c_void_p(bias), bias_dtype, 1,
+                                  None if dbias is None else ctypes.c_void_p(dbias), None)
     assert bwd(1) == INVALID          # fp32 io is not an io type
     assert bwd(7) == INVALID
     assert bwd(2, dsink=FAKE) == INVALID
     assert bwd(2, sink=FAKE + 1, dsink=FAKE) == ALIGN
+    assert bwd(2, dbias=FAKE) == INVALID                     # dbias without a bias
+    assert bwd(2, bias=FAKE, bias_dtype=5) == INVALID
+    assert bwd(2, bias=FAKE + 1, bias_dtype=2) == ALIGN      # fp16 bias: 2-byte alignment
     fv = [ctypes.c_void_p(FAKE)] * 5
     assert lib.sdpa_fwd_typed(3, *fv, 1, 2, 2, 128, 128, 128, 128, ctypes.c_float(0.0), 0, 0, -1, -1,
-                              None, None, None, None) == INVALID
+                              None, None, None, None, 0, 0, None) == INVALID

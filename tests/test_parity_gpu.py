@@ -834,3 +834,26 @@ def test_padded_head_dim_f16_and_bitwise():
     for _ in range(9):
         for a, b in zip(first, gpu_backward(case, d)):
             assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+# fp16 io with an additive bias (fp16 or fp32 bias elements), backward and forward.
+F16_BIAS_CASES = {
+    "d128_causal_ragged_B_f16": (SMALL["d128_causal_ragged"], "B", torch.float16),
+    "gqa_shared_f32": (SMALL["gqa"], "1", torch.float32),
+    "gqa_det_B_f16": (SMALL["gqa_det"], "B", torch.float16),
+    "mla_gqa_window_B_f16": (SMALL["mla_gqa_window"], "B", torch.float16),
+}
+
+
+@pytest.mark.parametrize("name", sorted(F16_BIAS_CASES))
+def test_f16_bias_parity(name):
+    w, kind, dt = F16_BIAS_CASES[name]
+    case = make_case(w, bias=(1 if kind == "1" else w.B, dt), io=torch.float16)
+    d = to_device(case)
+    dq, dk, dv, dbias = _gpu_bias(case, d)
+    assert dq.dtype == torch.float16
+    for g, r, n in zip((dq, dk, dv), oracle_backward(case), ("dq", "dk", "dv")):
+        assert_close(n, g.double().cpu().numpy(), r)
+    assert_close("dbias", dbias.double().cpu().numpy(), oracle_dbias(case))
+    o, lse = _gpu_fwd(case, d)
+    _check_fwd(case, o, lse)
