@@ -66,7 +66,7 @@ def load(build_if_missing: bool = False):
     lib.sdpa_fwd.restype = i
     lib.sdpa_fwd_bias.argtypes = list(lib.sdpa_fwd.argtypes[:-1]) + [vp, i, i, vp]
     lib.sdpa_fwd_bias.restype = i
-    lib.sdpa_bwd_typed.argtypes = [i] + list(lib.sdpa_bwd.argtypes[:-1]) + [vp, vp, vp, i, i, vp, vp]
+    lib.sdpa_bwd_typed.argtypes = [i] + list(lib.sdpa_bwd.argtypes[:-1]) + [vp, vp, vp, i, i, vp, i, vp]
     lib.sdpa_bwd_typed.restype = i
     lib.sdpa_fwd_typed.argtypes = [i] + list(lib.sdpa_fwd.argtypes[:-1]) + [vp, i, i, vp]
     lib.sdpa_fwd_typed.restype = i
@@ -140,6 +140,7 @@ def sdpa_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
              workspace: Optional[torch.Tensor] = None, sink: Optional[torch.Tensor] = None,
              dsink: Optional[torch.Tensor] = None, bias: Optional[torch.Tensor] = None,
              dbias: Optional[torch.Tensor] = None, bias_grad: bool = True,
+             dbias_dtype: torch.dtype = torch.float32,
              stream: Optional[torch.cuda.Stream] = None):
     """dQ, dK, dV of scaled-dot-product attention (see include/sdpa_bwd.h).
 
@@ -151,7 +152,8 @@ def sdpa_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
     With ``bias`` ((1|B, Hq, Sq, Skv) bf16 or fp32 CUDA, contiguous: the additive
     bias that ``lse`` was computed with) the call goes through sdpa_bwd_bias and,
     unless ``bias_grad`` is False, appends the fp32 dBias (shaped like ``bias``) to
-    the returned tuple.
+    the returned tuple (``dbias_dtype`` float32, or bfloat16 / float16 for the
+    io-type dBias of the general entry point).
     """
     lib = load()
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
@@ -188,7 +190,8 @@ def sdpa_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
             _ptr(dv), B, Hq, Hkv, Sq, Skv, Dqk, Dv, sc, int(causal), int(bottom_right),
             int(window_left), int(window_right), int(deterministic), _ptr(seq_q_lens),
             _ptr(seq_kv_lens), _ptr(workspace), ws_bytes)
-    if io == torch.float16:  # fp16 io: the general typed entry (sink and bias optional)
+    if io == torch.float16 or (bias is not None and bias_grad and dbias_dtype != torch.float32):
+        # the general typed entry: fp16 io, or an io-type dBias (sink and bias optional)
         if sink is not None:
             dsink = torch.empty_like(sink) if dsink is None else dsink
         bias_dtype, bias_batch = 0, 0
@@ -196,14 +199,22 @@ def sdpa_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
             bias_dtype = _check_bias(bias, B, Hq, Sq, Skv)
             bias_batch = int(bias.shape[0])
             if bias_grad:
-                dbias = torch.empty(bias.shape, dtype=torch.float32, device=bias.device) \
+                if dbias_dtype not in (torch.float32, torch.bfloat16, torch.float16):
+                    raise ValueError("dbias_dtype must be float32, bfloat16 or float16")
+                dbias = torch.empty(bias.shape, dtype=dbias_dtype, device=bias.device) \
                     if dbias is None else dbias
+                if dbias.dtype != dbias_dtype or not dbias.is_cuda or not dbias.is_contiguous() \
+                        or tuple(dbias.shape) != tuple(bias.shape):
+                    raise ValueError("dbias must be a contiguous CUDA tensor shaped like bias, of dbias_dtype")
             else:
                 dbias = None
         else:
             dbias = None
+        dbias_code = {torch.float32: DTYPE_F32, torch.bfloat16: DTYPE_BF16,
+                      torch.float16: DTYPE_F16}[dbias.dtype] if dbias is not None else DTYPE_F32
         rc = lib.sdpa_bwd_typed(_IO_CODES[io], *args, _ptr(sink), _ptr(dsink if sink is not None else None),
-                                _ptr(bias), bias_dtype, bias_batch, _ptr(dbias), _stream_handle(stream))
+                                _ptr(bias), bias_dtype, bias_batch, _ptr(dbias), dbias_code,
+                                _stream_handle(stream))
         if rc != 0:
             raise SdpaError(rc, "sdpa_bwd_typed")
         out = (dq, dk, dv) + ((dsink,) if sink is not None else ())

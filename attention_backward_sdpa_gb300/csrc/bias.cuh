@@ -39,18 +39,24 @@ __device__ __forceinline__ void load_bias_column(const ChainParams& p, long long
   }
 }
 
-// Zeros `rows` rows of `cols` floats, `ld` floats apart, with threads
-// thr = 0 .. nthr-1 (nthr a multiple of 32). A full 128-column block row is 32
-// 16-byte stores, one per lane of a warp; other shapes take scalar stores.
-__device__ __forceinline__ void zero_float_rows(float* base, int rows, int cols, long long ld, int thr,
-                                                int nthr) {
-  if (cols == BN && (reinterpret_cast<uintptr_t>(base) & 15u) == 0 && (ld & 3) == 0) {
-    const int rstep = nthr >> 5, c = (thr & 31) * 4;
-    for (int r = thr >> 5; r < rows; r += rstep)
-      *reinterpret_cast<float4*>(base + (long long)r * ld + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+// Zeros `rows` rows of `cols` elements of `esz` bytes (4 or 2), `ld` elements
+// apart, with threads thr = 0 .. nthr-1 (nthr a multiple of 32). A full
+// 128-column block row is 32 (fp32) or 16 (16-bit) 16-byte stores, one per lane
+// of a warp; other shapes take element stores.
+__device__ __forceinline__ void zero_elem_rows(char* base, int esz, int rows, int cols, long long ld,
+                                               int thr, int nthr) {
+  const int vec_per_row = BN * esz / 16;  // 32 or 16
+  if (cols == BN && (reinterpret_cast<uintptr_t>(base) & 15u) == 0 && ((ld * esz) & 15) == 0) {
+    const int rows_per_pass = nthr / vec_per_row, c = thr % vec_per_row;
+    for (int r = thr / vec_per_row; r < rows; r += rows_per_pass)
+      *reinterpret_cast<uint4*>(base + ((long long)r * ld) * esz + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+  } else if (esz == 4) {
+    for (int r = 0; r < rows; ++r)
+      for (int c = thr; c < cols; c += nthr) reinterpret_cast<float*>(base)[(long long)r * ld + c] = 0.f;
   } else {
     for (int r = 0; r < rows; ++r)
-      for (int c = thr; c < cols; c += nthr) base[(long long)r * ld + c] = 0.f;
+      for (int c = thr; c < cols; c += nthr)
+        reinterpret_cast<unsigned short*>(base)[(long long)r * ld + c] = 0;
   }
 }
 
@@ -65,8 +71,10 @@ __device__ inline void zero_unvisited_dbias_blocks(const ChainParams& p, int b, 
     for (int qt = 0; qt < p.n_qt; ++qt) {
       if (qt >= qt_lo && qt <= qt_hi) continue;
       const int q0 = qt * BQ;
-      zero_float_rows(p.dbias + (long long)b * p.dbias_bstride + ((long long)hq * p.Sq + q0) * p.Skv + k0,
-                      min(BQ, p.Sq - q0), cols, p.Skv, thr, nthr);
+      const int esz = p.dbias_out ? 2 : 4;
+      zero_elem_rows(reinterpret_cast<char*>(p.dbias) +
+                         ((long long)b * p.dbias_bstride + ((long long)hq * p.Sq + q0) * p.Skv + k0) * esz,
+                     esz, min(BQ, p.Sq - q0), cols, p.Skv, thr, nthr);
     }
   }
 }

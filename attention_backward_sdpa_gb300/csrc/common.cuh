@@ -75,9 +75,10 @@ struct ChainParams {
   int bias_fp32;
   int bias_f16;         // 16-bit bias elements are fp16 (else bf16)
   long long bias_bstride;
-  float* dbias;         // or null
+  float* dbias;         // or null (holds bf16 / fp16 elements when dbias_out is 1 / 2)
   long long dbias_bstride;
   int dbias_red;
+  int dbias_out;        // element type written: 0 fp32, 1 bf16, 2 fp16 (0 whenever dbias_red)
 
   // Deterministic two-kernel route: the main kernel stores each bf16 dS^T tile
   // (its swizzled shared-memory image, DS_TILE_BYTES) at
@@ -156,6 +157,10 @@ cudaError_t launch_preprocess(const ChainParams& p, cudaStream_t s);
 cudaError_t launch_main(const MainMaps& maps, const ChainParams& p, cudaStream_t s);
 cudaError_t launch_dq_convert(const ChainParams& p, cudaStream_t s);
 cudaError_t launch_dsink(const ChainParams& p, cudaStream_t s);
+// fp32 -> 16-bit (bf16, or fp16 when f16) copy of n elements: the io-type dBias
+// of a shared bias, whose batch rows add into an fp32 buffer first.
+cudaError_t launch_dbias_cast(const float* src, void* dst, long long n, bool f16, int num_sms,
+                              cudaStream_t s);
 cudaError_t launch_dq_from_ds(const CUtensorMap& k_map, const ChainParams& p, cudaStream_t s,
                               int num_sms);
 cudaError_t dq_kernel_setup();  // per device: opt in to the dQ kernel's shared memory
@@ -200,6 +205,11 @@ __host__ __device__ inline long long floor_div(long long a, long long b) {
 // A 16-bit bias element (bf16, or fp16 when f16) widened to fp32.
 __device__ __forceinline__ float bias16_to_f32(unsigned short v, bool f16) {
   return f16 ? __half2float(__ushort_as_half(v)) : __uint_as_float((uint32_t)v << 16);
+}
+
+// fp32 to a 16-bit dBias element (bf16, or fp16 when f16), round to nearest even.
+__device__ __forceinline__ unsigned short f32_to_16(float x, bool f16) {
+  return f16 ? __half_as_ushort(__float2half_rn(x)) : __bfloat16_as_ushort(__float2bfloat16_rn(x));
 }
 
 // Valid lengths of batch row b (the full S when no length array is given).

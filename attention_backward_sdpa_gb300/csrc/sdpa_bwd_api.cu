@@ -270,7 +270,8 @@ struct BiasArgs {
   const void* bias = nullptr;
   int dtype = SDPA_DTYPE_BF16;
   int batch = 0;  // 1 or B
-  float* dbias = nullptr;
+  void* dbias = nullptr;
+  int dbias_dtype = SDPA_DTYPE_F32;
 };
 
 // The whole chain; sink/dsink are null for sdpa_bwd().
@@ -297,8 +298,11 @@ int run_chain(const void* q, const void* k, const void* v, const void* o, const 
     // A one-batch dBias summed over B > 1 batch rows is added atomically: not
     // reproducible, so deterministic mode rejects it.
     if (deterministic && ba.dbias && ba.batch == 1 && B > 1) return SDPA_ERR_INVALID;
+    if (ba.dbias_dtype != SDPA_DTYPE_F32 && ba.dbias_dtype != SDPA_DTYPE_BF16 &&
+        ba.dbias_dtype != SDPA_DTYPE_F16)
+      return SDPA_ERR_INVALID;
     if (reinterpret_cast<uintptr_t>(ba.bias) % (ba.dtype == SDPA_DTYPE_F32 ? 4 : 2) != 0 ||
-        reinterpret_cast<uintptr_t>(ba.dbias) % 4 != 0)
+        reinterpret_cast<uintptr_t>(ba.dbias) % (ba.dbias_dtype == SDPA_DTYPE_F32 ? 4 : 2) != 0)
       return SDPA_ERR_ALIGN;
   }
   for (const void* ptr : {q, k, v, o, d_o, (const void*)dq, (const void*)dk, (const void*)dv})
@@ -324,7 +328,8 @@ int run_chain(const void* q, const void* k, const void* v, const void* o, const 
         cudaMemsetAsync(dk, 0, dk_bytes, stream) != cudaSuccess ||
         cudaMemsetAsync(dv, 0, dv_bytes, stream) != cudaSuccess ||
         (dsink && cudaMemsetAsync(dsink, 0, (size_t)H_q * sizeof(float), stream) != cudaSuccess) ||
-        (ba.dbias && cudaMemsetAsync(ba.dbias, 0, (size_t)ba.batch * H_q * S_q * S_kv * sizeof(float),
+        (ba.dbias && cudaMemsetAsync(ba.dbias, 0, (size_t)ba.batch * H_q * S_q * S_kv *
+                                                      (ba.dbias_dtype == SDPA_DTYPE_F32 ? 4 : 2),
                                      stream) != cudaSuccess))
       return SDPA_ERR_CUDA;
     return SDPA_OK;
@@ -343,6 +348,7 @@ int run_chain(const void* q, const void* k, const void* v, const void* o, const 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
 
   ChainParams p{};
+  float* dbias_tmp = nullptr;  // fp32 sum of a shared bias's dBias before its io-type cast
   p.B = B; p.Hq = H_q; p.Hkv = H_kv; p.Sq = S_q; p.Skv = S_kv; p.Dqk = D_qk; p.Dv = D_v;
   p.G = H_q / H_kv;
   // Head-group size of the D_qk 64/128 main kernel: the largest divisor of G
@@ -404,9 +410,23 @@ int run_chain(const void* q, const void* k, const void* v, const void* o, const 
     p.bias_fp32 = ba.dtype == SDPA_DTYPE_F32 ? 1 : 0;
     p.bias_f16 = ba.dtype == SDPA_DTYPE_F16 ? 1 : 0;
     p.bias_bstride = shared ? 0 : per_batch;
-    p.dbias = ba.dbias;
+    p.dbias = static_cast<float*>(ba.dbias);
     p.dbias_bstride = shared ? 0 : per_batch;
     p.dbias_red = (ba.dbias && shared) ? 1 : 0;
+    // A 16-bit dBias is written directly (each element once), except for a
+    // shared bias: its batch rows add into an fp32 buffer, cast at the end.
+    if (ba.dbias && ba.dbias_dtype != SDPA_DTYPE_F32) {
+      if (shared) {
+        if (cudaMallocAsync(reinterpret_cast<void**>(&p.dbias), (size_t)per_batch * sizeof(float), stream) !=
+            cudaSuccess) {
+          if (own_ws) cudaFreeAsync(workspace, stream);
+          return SDPA_ERR_CUDA;
+        }
+        dbias_tmp = p.dbias;
+      } else {
+        p.dbias_out = ba.dbias_dtype == SDPA_DTYPE_F16 ? 2 : 1;
+      }
+    }
   }
 
   MainMaps maps;
@@ -423,6 +443,7 @@ int run_chain(const void* q, const void* k, const void* v, const void* o, const 
                      p.dk_ws ? BHq : BHkv, BN, f16) ||
       !make_bhsd_map(&maps.dv_out, p.dv_ws ? static_cast<void*>(p.dv_ws) : dv, D_v, S_kv,
                      p.dv_ws ? BHq : BHkv, BN, f16)) {
+    if (dbias_tmp) cudaFreeAsync(dbias_tmp, stream);
     if (own_ws) cudaFreeAsync(workspace, stream);
     return SDPA_ERR_CUDA;
   }
@@ -449,6 +470,12 @@ int run_chain(const void* q, const void* k, const void* v, const void* o, const 
     prof.end(2);
   }
   if (e == cudaSuccess && dsink) e = launch_dsink(p, stream);
+  if (dbias_tmp) {
+    if (e == cudaSuccess)
+      e = launch_dbias_cast(dbias_tmp, ba.dbias, (long long)H_q * S_q * S_kv,
+                            ba.dbias_dtype == SDPA_DTYPE_F16, sms, stream);
+    cudaFreeAsync(dbias_tmp, stream);
+  }
   if (own_ws) cudaFreeAsync(workspace, stream);
   return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }
@@ -598,7 +625,7 @@ int sdpa_bwd_typed(int io_dtype, const void* q, const void* k, const void* v, co
                    int bottom_right, int window_left, int window_right, int deterministic,
                    const int32_t* seq_q_lens, const int32_t* seq_kv_lens, void* workspace,
                    size_t workspace_bytes, const float* sink, float* dsink, const void* bias,
-                   int bias_dtype, int bias_batch, float* dbias, void* stream) {
+                   int bias_dtype, int bias_batch, void* dbias, int dbias_dtype, void* stream) {
   if (io_dtype != SDPA_DTYPE_BF16 && io_dtype != SDPA_DTYPE_F16) return SDPA_ERR_INVALID;
   if (dsink && !sink) return SDPA_ERR_INVALID;
   if (!bias && dbias) return SDPA_ERR_INVALID;
@@ -607,6 +634,7 @@ int sdpa_bwd_typed(int io_dtype, const void* q, const void* k, const void* v, co
   ba.dtype = bias_dtype;
   ba.batch = bias_batch;
   ba.dbias = dbias;
+  ba.dbias_dtype = dbias_dtype;
   return run_chain(q, k, v, o, d_o, lse, dq, dk, dv, B, H_q, H_kv, S_q, S_kv, D_qk, D_v, scale,
                    causal, bottom_right, window_left, window_right, deterministic, seq_q_lens,
                    seq_kv_lens, workspace, workspace_bytes, dsink ? sink : nullptr, dsink, ba,

@@ -226,6 +226,21 @@ __global__ void __launch_bounds__(DSINK_THREADS) sdpa_bwd_dsink(const ChainParam
   if (threadIdx.x == 0) p.dsink[h] = -part[0];
 }
 
+__global__ void __launch_bounds__(256) sdpa_dbias_cast(const float* __restrict__ src,
+                                                       unsigned short* __restrict__ dst, long long n,
+                                                       int f16) {
+  for (long long i = (long long)blockIdx.x * 256 + threadIdx.x; i < n; i += (long long)gridDim.x * 256)
+    dst[i] = f32_to_16(src[i], f16 != 0);
+}
+
+cudaError_t launch_dbias_cast(const float* src, void* dst, long long n, bool f16, int num_sms,
+                              cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  const long long want = (n + 255) / 256, cap = (long long)num_sms * 8;
+  return launch_kernel(sdpa_dbias_cast, dim3((unsigned)(want < cap ? want : cap)), dim3(256), 0, s, false,
+                       src, static_cast<unsigned short*>(dst), n, f16 ? 1 : 0);
+}
+
 cudaError_t launch_dsink(const ChainParams& p, cudaStream_t s) {
   return launch_kernel(sdpa_bwd_dsink, dim3((unsigned)p.Hq), dim3(DSINK_THREADS), 0, s, false, p);
 }

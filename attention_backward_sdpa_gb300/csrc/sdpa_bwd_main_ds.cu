@@ -468,16 +468,24 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
           *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (row & 7)) << 4)) = make_uint4(w0, w1, w2, w3);
           if constexpr (BIAS) {
             if (p.dbias != nullptr && key_in) {
-              float* dst = p.dbias + (long long)b * p.dbias_bstride + bias_off + (long long)c * p.Skv;
+              const long long off = (long long)b * p.dbias_bstride + bias_off + (long long)c * p.Skv;
               const int rows_in = min(8, p.Sq - q0 - c);
               if (p.dbias_red) {
+                float* dst = p.dbias + off;
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
                   if (e < rows_in) atomicAdd(dst + (long long)e * p.Skv, ds[e]);
-              } else {
+              } else if (p.dbias_out == 0) {
+                float* dst = p.dbias + off;
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
                   if (e < rows_in) __stcs(dst + (long long)e * p.Skv, ds[e]);
+              } else {  // a 16-bit dBias (the io type): half the store bytes
+                unsigned short* dst = reinterpret_cast<unsigned short*>(p.dbias) + off;
+                const bool f16 = p.dbias_out == 2;
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                  if (e < rows_in) __stcs(dst + (long long)e * p.Skv, f32_to_16(ds[e], f16));
               }
             }
           }

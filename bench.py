@@ -90,14 +90,15 @@ def main_kernel_flops_per_pair(w: workloads.Workload) -> int:
     return flops_per_pair(w)
 
 
-def main_kernel_bytes_bias(w: workloads.Workload, pairs: int, bias) -> int:
+def main_kernel_bytes_bias(w: workloads.Workload, pairs: int, bias, dbias_esz: int = 4) -> int:
     """Algorithmic DRAM bytes of one biased main-kernel launch: the bias at the
-    visible pairs (its element size each), every fp32 dBias element written once,
+    visible pairs (its element size each), every dBias element written once
+    (``dbias_esz`` bytes: 4 for fp32, 2 for the io-type dBias),
     and each Q, K, V, dO, dK, dV element moved once with the fp32 dQ accumulator
     read and written once (the reduction route; the stored-dS route moves bf16 dS
     instead, counted the same here)."""
     esz = bias.element_size()
-    dbias = bias.numel() * 4
+    dbias = bias.numel() * dbias_esz
     qdo = 2 * w.B * w.Hq * w.Sq * w.Dqk * 2
     kv = w.B * w.Hkv * w.Skv * (w.Dqk + w.Dv) * 2
     dq_acc = 2 * w.B * w.Hq * w.Sq * w.Dqk * 4
@@ -413,8 +414,10 @@ def bias_tag(t):
     b = t.get("bias")
     if b is None:
         return None
-    return f"bias-{'shared' if b.shape[0] == 1 and t['q'].shape[0] > 1 else 'B'}-" \
-           f"{'f32' if b.dtype == torch.float32 else 'bf16'}"
+    name = {torch.float32: "f32", torch.float16: "f16"}.get(b.dtype, "bf16")
+    tag = f"bias-{'shared' if b.shape[0] == 1 and t['q'].shape[0] > 1 else 'B'}-{name}"
+    dbt = t.get("dbias_dtype", torch.float32)
+    return tag if dbt == torch.float32 else tag + "-dbias" + {torch.float16: "f16"}.get(dbt, "bf16")
 
 
 def peaks():
@@ -449,7 +452,8 @@ def run_gpu(args, w, t, o, lse, rank, world, device):
     outs = [dq, dk, dv]
     if "bias" in t:  # additive bias: read by the main kernel, dBias written by it
         d["bias"] = t["bias"].to(device)
-        kw["dbias"] = torch.empty(tuple(t["bias"].shape), dtype=torch.float32, device=device)
+        kw["dbias_dtype"] = t["dbias_dtype"]
+        kw["dbias"] = torch.empty(tuple(t["bias"].shape), dtype=t["dbias_dtype"], device=device)
         outs.append(kw["dbias"])
 
     def call_kw():
@@ -536,7 +540,7 @@ def run_gpu(args, w, t, o, lse, rank, world, device):
     if "bias" in t:
         # With a bias the main kernel streams the bias and the fp32 dBias: it is
         # bound by HBM, against the measured copy bandwidth.
-        nbytes = main_kernel_bytes_bias(w, pairs, t["bias"])
+        nbytes = main_kernel_bytes_bias(w, pairs, t["bias"], t["dbias_dtype"].itemsize)
         gbs = nbytes / (main_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": gbs, "peak": peak_hbm, "unit": "GB/s",
                 "frac": gbs / peak_hbm, "traffic": main_traffic(w, bias_tag(t)),
@@ -597,7 +601,9 @@ def main(argv=None):
     ap.add_argument("--bias", default="none", choices=["none", "B", "1"],
                     help="add a bias of B batches or 1 shared batch: sdpa_bwd_bias (dBias written "
                          "in fp32), or sdpa_fwd_bias with --pass fwd")
-    ap.add_argument("--bias-dtype", default="bf16", choices=["bf16", "f32"])
+    ap.add_argument("--bias-dtype", default="bf16", choices=["bf16", "f16", "f32"])
+    ap.add_argument("--dbias-dtype", default="f32", choices=["f32", "bf16", "f16"],
+                    help="element type of the dBias output (bf16/f16: the io-type dBias)")
     ap.add_argument("--io", default="bf16", choices=["bf16", "f16"],
                     help="element type of Q, K, V, O, dO and the gradients (f16: sdpa_bwd_typed)")
     ap.add_argument("--qat", action="store_true",
@@ -612,8 +618,8 @@ def main(argv=None):
     args.steps = max(args.steps, 1)
     w = workloads.WORKLOADS[args.workload]
     # option checks first: no process group or device is touched for a bad line
-    if args.io == "f16" and (args.bias != "none" or args.qat):
-        ap.error("--io f16: the plain chain (a bias or QAT needs bf16)")
+    if args.io == "f16" and args.qat:
+        ap.error("--io f16: QAT needs bf16")
     if args.qat and (w.Dqk != 128 or w.Dv != 128 or w.deterministic or args.bias != "none"
                      or args.sink or args.pass_ != "bwd"):
         ap.error("--qat: a D = 128 non-deterministic workload, backward, no bias or sink")
@@ -628,8 +634,9 @@ def main(argv=None):
     if args.qat:
         t["qat"] = True
     if args.bias != "none":
-        t["bias"] = workloads.bias_tensor(w, 1 if args.bias == "1" else w.B,
-                                          torch.float32 if args.bias_dtype == "f32" else torch.bfloat16)
+        dts = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
+        t["bias"] = workloads.bias_tensor(w, 1 if args.bias == "1" else w.B, dts[args.bias_dtype])
+        t["dbias_dtype"] = dts[args.dbias_dtype]
     if args.pass_ == "fwd":
         cb = cpu_baseline_fwd(w, t) if (rank == 0 and not args.no_cpu_baseline) else None
         r = run_gpu_fwd(args, w, t, rank, world, device)
@@ -673,7 +680,7 @@ def result_line(args, w, world, r, cb, metric):
                        "deterministic": w.deterministic, "seed": w.seed,
                        "pass": args.pass_, "sink": bool(args.sink), "nvfp4_qat": bool(args.qat),
                        "bias": None if args.bias == "none" else
-                       {"batch": args.bias, "dtype": args.bias_dtype, "dbias": "f32"},
+                       {"batch": args.bias, "dtype": args.bias_dtype, "dbias": args.dbias_dtype},
                        "gflop_per_step": r["flops"] / 1e9,
                        "l2": "256 MiB buffer written between timed steps",
                        "parallelism": f"replicas{world}" if world > 1 else "single"},

@@ -228,9 +228,15 @@ int sdpa_fwd_bias(const void* q, const void* k, const void* v, void* o, float* l
  * fp32. sink/dsink are as in sdpa_bwd_sink() and bias/bias_dtype/bias_batch/
  * dbias as in sdpa_bwd_bias(), each optional (NULL: absent); bias_dtype may
  * also be SDPA_DTYPE_F16 (the io type of an fp16 call, or any call).
+ * dbias_dtype is the element type of dbias: SDPA_DTYPE_F32 (as sdpa_bwd_bias),
+ * or SDPA_DTYPE_BF16 / SDPA_DTYPE_F16 (the page's io-dtype dBias, rounded to
+ * nearest even; written directly, at half the bytes, for a per-batch bias; a
+ * shared bias with B > 1 is summed in a temporary fp32 buffer, taken from the
+ * stream-ordered allocator, and cast at the end). dbias then needs 2-byte
+ * alignment.
  * With io_dtype BF16 and no bias this is sdpa_bwd_sink() / sdpa_bwd().
- * Returns SDPA_ERR_INVALID for another io_dtype, or dsink without sink, or
- * dbias without bias; otherwise as sdpa_bwd_bias(). The workspace size does
+ * Returns SDPA_ERR_INVALID for another io_dtype or dbias_dtype, or dsink
+ * without sink, or dbias without bias; otherwise as sdpa_bwd_bias(). The workspace size does
  * not depend on the io type.
  */
 int sdpa_bwd_typed(int io_dtype, const void* q, const void* k, const void* v, const void* o,
@@ -239,7 +245,7 @@ int sdpa_bwd_typed(int io_dtype, const void* q, const void* k, const void* v, co
                    int bottom_right, int window_left, int window_right, int deterministic,
                    const int32_t* seq_q_lens, const int32_t* seq_kv_lens, void* workspace,
                    size_t workspace_bytes, const float* sink, float* dsink, const void* bias,
-                   int bias_dtype, int bias_batch, float* dbias, void* stream);
+                   int bias_dtype, int bias_batch, void* dbias, int dbias_dtype, void* stream);
 
 /*
  * The general SDPA forward: sdpa_fwd() / sdpa_fwd_bias() with the io element

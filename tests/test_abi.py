@@ -252,13 +252,13 @@ def test_typed_entry_validation(lib):
     lib.sdpa_fwd_typed.restype = ctypes.c_int
     vp = [ctypes.c_void_p(FAKE)] * 9
 
-    def bwd(io, sink=None, dsink=None, bias=None, bias_dtype=0, dbias=None):
+    def bwd(io, sink=None, dsink=None, bias=None, bias_dtype=0, dbias=None, dbias_dtype=1):
         return lib.sdpa_bwd_typed(io, *vp, 1, 2, 2, 128, 128, 128, 128, ctypes.c_float(0.0), 0, 0, -1,
                                   -1, 0, None, None, None, ctypes.c_size_t(0),
                                   None if sink is None else ctypes.c_void_p(sink),
                                   None if dsink is None else ctypes.c_void_p(dsink),
                                   None if bias is None else ctypes.c_void_p(bias), bias_dtype, 1,
-                                  None if dbias is None else ctypes.c_void_p(dbias), None)
+                                  None if dbias is None else ctypes.c_void_p(dbias), dbias_dtype, None)
     assert bwd(1) == INVALID          # fp32 io is not an io type
     assert bwd(7) == INVALID
     assert bwd(2, dsink=FAKE) == INVALID
@@ -266,6 +266,9 @@ def test_typed_entry_validation(lib):
     assert bwd(2, dbias=FAKE) == INVALID                     # dbias without a bias
     assert bwd(2, bias=FAKE, bias_dtype=5) == INVALID
     assert bwd(2, bias=FAKE + 1, bias_dtype=2) == ALIGN      # fp16 bias: 2-byte alignment
+    assert bwd(2, bias=FAKE, dbias=FAKE, dbias_dtype=7) == INVALID
+    assert bwd(2, bias=FAKE, dbias=FAKE + 2, dbias_dtype=1) == ALIGN   # fp32 dBias: 4-byte
+    assert bwd(2, bias=FAKE, dbias=FAKE + 1, dbias_dtype=0) == ALIGN   # bf16 dBias: 2-byte
     fv = [ctypes.c_void_p(FAKE)] * 5
     assert lib.sdpa_fwd_typed(3, *fv, 1, 2, 2, 128, 128, 128, 128, ctypes.c_float(0.0), 0, 0, -1, -1,
                               None, None, None, None, 0, 0, None) == INVALID

@@ -62,7 +62,6 @@ def test_two_rank_reduction_and_broadcast():
 @pytest.mark.parametrize("argv", [["--qat", "--workload", "causal_gqa_det"],     # deterministic
                                   ["--qat", "--workload", "mla_br_causal"],      # D 192
                                   ["--qat", "--bias", "B"],
-                                  ["--io", "f16", "--bias", "1"],
                                   ["--io", "f16", "--qat"]])
 def test_bench_rejects_unsupported_combinations(argv):
     """The option checks run before any GPU work (argparse exits with status 2)."""
@@ -75,7 +74,7 @@ def test_bias_bytes_and_traffic_keys():
     w = workloads.WORKLOADS["causal_mha"]
     pairs = bench.visible_pairs(w, None)
     b = torch.zeros((2, 16, 2048, 2048), dtype=torch.bfloat16)
-    nbytes = bench.main_kernel_bytes_bias(w, pairs, b)
+    nbytes = bench.main_kernel_bytes_bias(w, pairs, b)  # fp32 dBias
     # bias at the visible pairs + every fp32 dBias element + Q, dO, K, V, dK, dV, dQ accumulator
     expect = pairs * 2 + b.numel() * 4 + 2 * 2 * 16 * 2048 * 128 * 2 + 2 * (2 * 16 * 2048 * 256 * 2) \
         + 2 * 2 * 16 * 2048 * 128 * 4

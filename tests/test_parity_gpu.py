@@ -857,3 +857,32 @@ def test_f16_bias_parity(name):
     assert_close("dbias", dbias.double().cpu().numpy(), oracle_dbias(case))
     o, lse = _gpu_fwd(case, d)
     _check_fwd(case, o, lse)
+
+
+# The io-type dBias (bf16 / fp16 elements): written directly for a per-batch
+# bias (half the bytes), summed in fp32 and cast for a shared one.
+DBIAS16_CASES = {
+    "d128_causal_ragged_B_bf16out": (SMALL["d128_causal_ragged"], "B", torch.bfloat16, torch.bfloat16),
+    "gqa_shared_f16out": (SMALL["gqa"], "1", torch.float32, torch.float16),
+    "padded_window_B_bf16out": (SMALL["padded_window"], "B", torch.bfloat16, torch.bfloat16),
+    "mla_dense_shared_bf16out": (SMALL["mla_dense"], "1", torch.bfloat16, torch.bfloat16),
+    "d40_f16io_B_f16out": (DPAD_CASES["d40_gqa_window"], "B", torch.float16, torch.float16),
+}
+
+
+@pytest.mark.parametrize("name", sorted(DBIAS16_CASES))
+def test_io_type_dbias(name):
+    w, kind, bdt, odt = DBIAS16_CASES[name]
+    io = torch.float16 if bdt == torch.float16 and odt == torch.float16 else torch.bfloat16
+    case = make_case(w, bias=(1 if kind == "1" else w.B, bdt), io=io)
+    d = to_device(case)
+    dbias = torch.full(tuple(d["bias"].shape), float("nan"), dtype=odt, device="cuda")
+    dq, dk, dv, db = gpu_backward(case, d, bias=d["bias"], dbias=dbias, dbias_dtype=odt)
+    assert db is dbias and db.dtype == odt
+    for g, r, n in zip((dq, dk, dv), oracle_backward(case), ("dq", "dk", "dv")):
+        assert_close(n, g.double().cpu().numpy(), r)
+    gb = db.double().cpu().numpy()
+    assert_close("dbias", gb, oracle_dbias(case))
+    masked = ~_visible_mask(case)
+    if masked.any():
+        assert np.all(gb[np.broadcast_to(masked, gb.shape)] == 0.0)
