@@ -27,36 +27,45 @@ __device__ __forceinline__ void load_bias_column(const ChainParams& p, long long
       for (int i = 0; i < N; ++i) bz[i] = i < rows ? __ldcs(src + i * ld) : 0.f;
     }
   } else {
+    // (One loop per element type: a per-element choice cost the replay a
+    // select on every value.)
     const unsigned short* src = static_cast<const unsigned short*>(p.bias) + off;
-    const bool f16 = p.bias_f16 != 0;
-    if (rows == N) {
+    if (p.bias_f16) {
 #pragma unroll
-      for (int i = 0; i < N; ++i) bz[i] = bias16_to_f32(__ldcs(src + i * ld), f16);
+      for (int i = 0; i < N; ++i) bz[i] = i < rows ? __half2float(__ushort_as_half(__ldcs(src + i * ld))) : 0.f;
+    } else if (rows == N) {
+#pragma unroll
+      for (int i = 0; i < N; ++i) bz[i] = __uint_as_float((uint32_t)__ldcs(src + i * ld) << 16);
     } else {
 #pragma unroll
-      for (int i = 0; i < N; ++i) bz[i] = i < rows ? bias16_to_f32(__ldcs(src + i * ld), f16) : 0.f;
+      for (int i = 0; i < N; ++i)
+        bz[i] = i < rows ? __uint_as_float((uint32_t)__ldcs(src + i * ld) << 16) : 0.f;
     }
   }
 }
 
-// Zeros `rows` rows of `cols` elements of `esz` bytes (4 or 2), `ld` elements
+// Zeros `rows` rows of `cols` elements of ESZ bytes (4 or 2), `ld` elements
 // apart, with threads thr = 0 .. nthr-1 (nthr a multiple of 32). A full
 // 128-column block row is 32 (fp32) or 16 (16-bit) 16-byte stores, one per lane
-// of a warp; other shapes take element stores.
-__device__ __forceinline__ void zero_elem_rows(char* base, int esz, int rows, int cols, long long ld,
-                                               int thr, int nthr) {
-  const int vec_per_row = BN * esz / 16;  // 32 or 16
-  if (cols == BN && (reinterpret_cast<uintptr_t>(base) & 15u) == 0 && ((ld * esz) & 15) == 0) {
-    const int rows_per_pass = nthr / vec_per_row, c = thr % vec_per_row;
-    for (int r = thr / vec_per_row; r < rows; r += rows_per_pass)
-      *reinterpret_cast<uint4*>(base + ((long long)r * ld) * esz + c * 16) = make_uint4(0u, 0u, 0u, 0u);
-  } else if (esz == 4) {
-    for (int r = 0; r < rows; ++r)
-      for (int c = thr; c < cols; c += nthr) reinterpret_cast<float*>(base)[(long long)r * ld + c] = 0.f;
+// of a warp; other shapes take element stores. (The element size is a template
+// argument: computed at run time it cost the biased kernel 10 % through this
+// loop.)
+template <int ESZ>
+__device__ __forceinline__ void zero_elem_rows(char* base, int rows, int cols, long long ld, int thr,
+                                               int nthr) {
+  constexpr int VPR = BN * ESZ / 16;  // 16-byte vectors per full row
+  if (cols == BN && (reinterpret_cast<uintptr_t>(base) & 15u) == 0 && ((ld * ESZ) & 15) == 0) {
+    const int rstep = nthr / VPR, c = (thr % VPR) * 16;
+    for (int r = thr / VPR; r < rows; r += rstep)
+      *reinterpret_cast<uint4*>(base + (long long)r * ld * ESZ + c) = make_uint4(0u, 0u, 0u, 0u);
   } else {
     for (int r = 0; r < rows; ++r)
-      for (int c = thr; c < cols; c += nthr)
-        reinterpret_cast<unsigned short*>(base)[(long long)r * ld + c] = 0;
+      for (int c = thr; c < cols; c += nthr) {
+        if (ESZ == 4)
+          reinterpret_cast<float*>(base)[(long long)r * ld + c] = 0.f;
+        else
+          reinterpret_cast<unsigned short*>(base)[(long long)r * ld + c] = 0;
+      }
   }
 }
 
@@ -71,10 +80,11 @@ __device__ inline void zero_unvisited_dbias_blocks(const ChainParams& p, int b, 
     for (int qt = 0; qt < p.n_qt; ++qt) {
       if (qt >= qt_lo && qt <= qt_hi) continue;
       const int q0 = qt * BQ;
-      const int esz = p.dbias_out ? 2 : 4;
-      zero_elem_rows(reinterpret_cast<char*>(p.dbias) +
-                         ((long long)b * p.dbias_bstride + ((long long)hq * p.Sq + q0) * p.Skv + k0) * esz,
-                     esz, min(BQ, p.Sq - q0), cols, p.Skv, thr, nthr);
+      const long long e0 = (long long)b * p.dbias_bstride + ((long long)hq * p.Sq + q0) * p.Skv + k0;
+      if (p.dbias_out)
+        zero_elem_rows<2>(reinterpret_cast<char*>(p.dbias) + e0 * 2, min(BQ, p.Sq - q0), cols, p.Skv, thr, nthr);
+      else
+        zero_elem_rows<4>(reinterpret_cast<char*>(p.dbias) + e0 * 4, min(BQ, p.Sq - q0), cols, p.Skv, thr, nthr);
     }
   }
 }

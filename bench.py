@@ -383,13 +383,13 @@ def cpu_baseline_leg(w, t, target_s=12.0):
 MAIN_SOURCES = {"sdpa_bwd_main": ("sdpa_bwd_main.cuh", "common.cuh", "ptx.cuh", "nvfp4.cuh", "bias.cuh"),
                 "sdpa_bwd_main_ds": ("sdpa_bwd_main_ds.cu", "common.cuh", "ptx.cuh", "bias.cuh")}
 MAIN_TRAFFIC = {
-    "5323b92209cf2a25": {"causal_mha": 114467072 + 31501056,
-                         "causal_gqa_det": 123357696 + 513710592,
-                         "swa_causal_padded": 247575296 + 186622208,
-                         "causal_mha/bias-B-f32": 469117696 + 584227328,
-                         "causal_mha/qat": 113707264 + 30040832},
-    "08f360987d2b81ca": {"mla_br_causal": 132029184 + 263661568,
-                         "mla_br_causal/bias-B-bf16": 425198848 + 1331085056},
+    "a926472069a766b7": {"causal_mha": 114335744 + 31287296,
+                         "causal_gqa_det": 123873024 + 513597184,
+                         "swa_causal_padded": 246441984 + 186258176,
+                         "causal_mha/bias-B-f32": 468652800 + 583614464,
+                         "causal_mha/qat": 113163264 + 28805888},
+    "1bc28627359d3791": {"mla_br_causal": 131945216 + 263809792,
+                         "mla_br_causal/bias-B-bf16": 423982336 + 1331097344},
 }
 
 
