@@ -18,7 +18,8 @@
  *
  * Conventions shared by every entry point:
  *   - Tensors are dense, contiguous, row-major (B, H, S, D) bf16 device
- *     buffers, D innermost; every tensor pointer must be 16-byte aligned.
+ *     buffers (fp16 through sdpa_bwd_typed / sdpa_fwd_typed), D innermost;
+ *     every tensor pointer must be 16-byte aligned.
  *     Q, O, dO, dQ have H_q heads; K, V, dK, dV have H_kv heads.
  *     Q, K, dQ, dK have D_qk columns; V, O, dO, dV have D_v columns.
  *   - lse is fp32 (B, H_q, S_q), natural log; -inf marks a row with no key.
@@ -65,11 +66,12 @@ typedef enum {
 /*
  * Bytes of device workspace sdpa_bwd() needs for this problem (0 when none).
  * The workspace holds, each region 256-byte aligned: per-query-tile fp32 row
- * statistics (LSE * log2(e) and delta); the fp32 dQ accumulator, or on the
- * deterministic two-kernel route the bf16 dS tiles; the deterministic-mode turn
+ * statistics (LSE * log2(e) and delta); the fp32 dQ accumulator (rows of 64
+ * columns for D_qk up to 64, else 128), or on the deterministic two-kernel
+ * route the 16-bit dS tiles; the deterministic-mode turn
  * counters and a work ticket; one fp32 sink-token partial per query tile
- * (sdpa_bwd_sink); and, when H_kv < H_q, the per-query-head bf16 dK/dV
- * partials of the GQA reduction.
+ * (sdpa_bwd_sink); and, when H_kv < H_q, the per-query-head 16-bit dK/dV
+ * partials of the GQA reduction. The size does not depend on the io type.
  * Returns 0 for arguments sdpa_bwd() would reject.
  */
 size_t sdpa_bwd_workspace_size(int B, int H_q, int H_kv, int S_q, int S_kv, int D_qk, int D_v,
@@ -82,7 +84,10 @@ size_t sdpa_bwd_workspace_size(int B, int H_q, int H_kv, int S_q, int S_kv, int 
  *   dq, dk, dv        device bf16 outputs (same shapes as q, k, v).
  *   B, H_q, H_kv      batch and head counts; H_kv must divide H_q.
  *   S_q, S_kv         sequence lengths (>= 0; a zero length gives zero gradients).
- *   D_qk, D_v         head dims; served: (64, 64), (128, 128) and (192, 128).
+ *   D_qk, D_v         head dims; served: D_qk = D_v, any multiple of 8 from 8 to
+ *                     128 (up to 64 on the 64-column kernels, above on the
+ *                     128-column ones, the columns past D zero-filled by TMA),
+ *                     and (192, 128).
  *   scale             softmax scale applied to Q K^T; <= 0 or NaN selects 1/sqrt(D_qk).
  *   causal            1: keep key k for query q only if k <= q + diag + max(window_right, 0).
  *   bottom_right      1: diag = L_kv - L_q (the actual lengths of the batch row);
@@ -94,8 +99,8 @@ size_t sdpa_bwd_workspace_size(int B, int H_q, int H_kv, int S_q, int S_kv, int 
  *                     128 the main kernel stores dS and a second kernel forms
  *                     dQ = scale * dS K over an ascending key walk (larger
  *                     workspace: 2 bytes per (query, key) position); for
- *                     D_qk = 64 the dQ partials of the KV tiles are added in
- *                     ascending KV-tile order. D_qk = 192 always takes the
+ *                     other D_qk up to 128 the dQ partials of the KV tiles are
+ *                     added in ascending KV-tile order. D_qk = 192 always takes the
  *                     stored-dS route, so its dQ is reproducible in both
  *                     modes. dK and dV are bitwise reproducible in both modes.
  *   seq_q_lens,       device int32 (B,) per-batch valid lengths, or NULL for
