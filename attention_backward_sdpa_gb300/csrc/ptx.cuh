@@ -142,10 +142,6 @@ __device__ __forceinline__ void bulk_wait_group0() {
 __device__ __forceinline__ void bulk_wait_group2() {
   asm volatile("cp.async.bulk.wait_group 2;" ::: "memory");
 }
-// Waits until all but the most recent committed bulk group have completed.
-__device__ __forceinline__ void bulk_wait_group1() {
-  asm volatile("cp.async.bulk.wait_group 1;" ::: "memory");
-}
 // Orders generic-proxy and async-proxy accesses to global memory.
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -222,23 +218,14 @@ __host__ __device__ constexpr uint32_t idesc_io(int M, int N, bool a_mn, bool b_
              : idesc_bf16_f32(M, N, a_mn, b_mn);
 }
 
-// Shared-memory matrix descriptor with 128-byte swizzling.
-//   K-major operand: rows of 128 B (64 bf16 along K), 8-row groups SBO apart.
-//   MN-major operand: rows of 128 B along MN (64 bf16), one row per K index;
+// Shared-memory matrix descriptor with 128-byte swizzling, split into a
+// compile-time template (the layout fields: LBO, SBO, the tcgen05 descriptor
+// version, the swizzle mode) and the start address, so that issuing an MMA
+// costs one shift and one OR.
+//   K-major operand: rows of 128 B (64 16-bit values along K), 8-row groups SBO
+//     apart.
+//   MN-major operand: rows of 128 B along MN (64 values), one row per K index;
 //     8-K-row groups SBO apart, 64-wide MN blocks LBO apart.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes,
-                                                uint32_t sbo_bytes) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
-  d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
-  d |= (uint64_t)1 << 46;  // descriptor version for tcgen05
-  d |= (uint64_t)2 << 61;  // 128-byte swizzle
-  return d;
-}
-
-// The same descriptor split into a compile-time template (layout fields) and the
-// start address, so that issuing an MMA costs one shift and one OR.
 __host__ __device__ constexpr uint64_t sdesc_sw128_template(uint32_t lbo_bytes, uint32_t sbo_bytes) {
   return ((uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16) | ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) |
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
@@ -257,13 +244,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
       "%28, %29, %30, %31}, [%32];"
       : SDPA_R8(0), SDPA_R8(8), SDPA_R8(16), SDPA_R8(24)
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15}, [%16];"
-      : SDPA_R8(0), SDPA_R8(8)
       : "r"(taddr));
 }
 #undef SDPA_R8
@@ -364,12 +344,6 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-// Vector fp32 reduction into global memory (relaxed, gpu scope).
-__device__ __forceinline__ void red_add_v4(float* gaddr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(gaddr), "f"(a), "f"(b),
-               "f"(c), "f"(d)
-               : "memory");
-}
 
 __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
   int v;
