@@ -383,13 +383,13 @@ def cpu_baseline_leg(w, t, target_s=12.0):
 MAIN_SOURCES = {"sdpa_bwd_main": ("sdpa_bwd_main.cuh", "common.cuh", "ptx.cuh", "nvfp4.cuh", "bias.cuh"),
                 "sdpa_bwd_main_ds": ("sdpa_bwd_main_ds.cu", "common.cuh", "ptx.cuh", "bias.cuh")}
 MAIN_TRAFFIC = {
-    "a926472069a766b7": {"causal_mha": 114335744 + 31287296,
-                         "causal_gqa_det": 123873024 + 513597184,
-                         "swa_causal_padded": 246441984 + 186258176,
-                         "causal_mha/bias-B-f32": 468652800 + 583614464,
-                         "causal_mha/qat": 113163264 + 28805888},
-    "1bc28627359d3791": {"mla_br_causal": 131945216 + 263809792,
-                         "mla_br_causal/bias-B-bf16": 423982336 + 1331097344},
+    "128fcc156055751a": {"causal_mha": 114551296 + 31852544,
+                         "causal_gqa_det": 123352320 + 513683200,
+                         "swa_causal_padded": 247342336 + 186045952,
+                         "causal_mha/bias-B-f32": 468788992 + 584808704,
+                         "causal_mha/qat": 113423360 + 29674752},
+    "0ac47d748bd4a176": {"mla_br_causal": 131985152 + 263710976,
+                         "mla_br_causal/bias-B-bf16": 426161664 + 1331418368},
 }
 
 
