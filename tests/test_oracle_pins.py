@@ -720,3 +720,31 @@ def test_qat_backward_gqa_sums_group_heads(oracle_mod):
     np.testing.assert_allclose(dq, dq2, atol=1e-13)
     np.testing.assert_allclose(dk, dk2.reshape(1, 2, 2, 18, 32).sum(2), atol=1e-13)
     np.testing.assert_allclose(dv, dv2.reshape(1, 2, 2, 18, 32).sum(2), atol=1e-13)
+
+
+@pytest.mark.parametrize("name", ["padded", "window_causal", "window_only"])
+def test_qat_oracle_under_masks(oracle_mod, name):
+    """The QAT backward under padding and windows: dQ/dK are the plain backward
+    of the quantized operands, dV uses the independently quantized P (masked
+    entries 0 inside their 16-key blocks); D 16/32 so that blocks are whole."""
+    base = FD_CASES[name]
+    p = Problem(base.B, base.Hq, base.Hkv, base.Sq, base.Skv, 32, 16, causal=base.causal,
+                bottom_right=base.bottom_right, window_left=base.window_left,
+                window_right=base.window_right, seq_q_lens=base.seq_q_lens,
+                seq_kv_lens=base.seq_kv_lens)
+    q, k, v, do = _inputs(p, seed=45)
+    o_hp, lse, _ = oracle_mod.qat_forward(p, q, k, v)
+    qh, kh, vh = _fq_independent(q), _fq_independent(k), _fq_independent(v)
+    dq, dk, dv = oracle_mod.qat_backward(p, q, k, v, o_hp, do, lse)
+    rq, rk, _ = oracle_mod.backward(p, qh, kh, vh, o_hp, do, lse)
+    np.testing.assert_allclose(dq, rq, atol=1e-13)
+    np.testing.assert_allclose(dk, rk, atol=1e-13)
+    mask = _torch_mask(p).numpy()[:, 0]
+    s = np.einsum("bhqd,bhkd->bhqk", qh, np.repeat(kh, p.Hq // p.Hkv, axis=1)) * p.resolved_scale
+    with np.errstate(invalid="ignore", over="ignore"):
+        P = np.where(mask[:, None], np.exp(s - lse[..., None]), 0.0)
+    P = np.nan_to_num(P, nan=0.0, posinf=0.0)
+    Ph = _fq_independent(P)
+    dv_ref = np.einsum("bhqk,bhqd->bhkd", Ph, do)
+    dv_ref = dv_ref.reshape(p.B, p.Hkv, p.Hq // p.Hkv, p.Skv, p.Dv).sum(2)
+    np.testing.assert_allclose(dv, dv_ref, atol=1e-12)
