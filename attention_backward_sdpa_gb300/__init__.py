@@ -19,8 +19,9 @@ import torch
 
 from . import _build
 
-__all__ = ["sdpa_bwd", "workspace_size", "check_device_status", "profile_enable", "profile_read",
-           "library_path", "load", "SdpaError", "KERNEL_NAMES"]
+__all__ = ["sdpa_bwd", "sdpa_fwd", "workspace_size", "nvfp4_fake_quant", "sdpa_fwd_nvfp4_qat",
+           "sdpa_bwd_nvfp4_qat", "nvfp4_qat_workspace_size", "check_device_status",
+           "profile_enable", "profile_read", "library_path", "load", "SdpaError", "KERNEL_NAMES"]
 
 KERNEL_NAMES = ("preprocess", "main", "dq")
 

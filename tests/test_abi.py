@@ -153,6 +153,21 @@ def test_python_binding_rejects_cpu_tensors():
         pkg.sdpa_bwd(x, x, x, x, x, lse)
 
 
+def test_python_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    """No fallback: with the shared library absent, loading raises instead of
+    routing anywhere else."""
+    import attention_backward_sdpa_gb300 as pkg
+    monkeypatch.setattr(pkg, "_lib", None)
+    monkeypatch.setattr(pkg._build, "LIB", str(tmp_path / "libsdpa_bwd.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        pkg.load()
+
+
+def test_public_names_exist():
+    import attention_backward_sdpa_gb300 as pkg
+    assert [n for n in pkg.__all__ if not hasattr(pkg, n)] == []
+
+
 def call_fwd(lib, ptrs=None, B=1, Hq=2, Hkv=2, Sq=128, Skv=128, Dqk=128, Dv=128, causal=0, wr=-1,
              sink=None):
     ptrs = ptrs or [FAKE] * 5
