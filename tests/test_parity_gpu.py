@@ -265,7 +265,7 @@ def test_sink_parity(name):
     assert_close("dv", dv.double().cpu().numpy(), rv)
     ref, mag = oracle_dsink(case)
     _dsink_close(dsink.double().cpu().numpy(), ref, mag)
-    # dQ/dK/dV need no sink code: the plain call gives the same bits
+    # The sink enters dQ/dK/dV only through the LSE: the plain call gives the same bits
     dq2, dk2, dv2 = gpu_backward(case, d)
     if case["workload"].deterministic or case["workload"].Dqk == 192:
         for a, b in ((dq, dq2), (dk, dk2), (dv, dv2)):
