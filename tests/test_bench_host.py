@@ -1,6 +1,7 @@
 """Host-side logic of bench.py that needs no GPU: the algorithmic FLOP count
 (visible pairs) against the oracle's brute-force count, and the multi-rank
-timing reduction / input broadcast over world_size-2 gloo ranks."""
+timing reduction / input broadcast over world_size-2 gloo ranks, and the
+reference arm (the oracle on the host cores) at one and two ranks."""
 import os
 
 import numpy as np
@@ -86,3 +87,50 @@ def test_bias_bytes_and_traffic_keys():
     assert bench.bias_tag({"q": t["q"], "qat": True}) == "qat"
     assert bench.bias_tag({"q": t["q"].half()}) == "f16"
     assert bench.bias_tag({"q": t["q"]}) is None
+
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _json_lines(out: str):
+    import json
+    return [json.loads(l) for l in out.splitlines() if l.startswith("{")]
+
+
+def _run(cmd):
+    import subprocess
+    import sys
+    env = dict(os.environ, MASTER_ADDR="127.0.0.1")
+    r = subprocess.run([sys.executable] + cmd, cwd=ROOT, env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    return _json_lines(r.stdout)
+
+
+def _check_reference_line(line, n_gpus):
+    assert line["impl"] == "reference" and line["n_gpus"] == n_gpus
+    assert line["value"] > 0 and line["unit"] == "TFLOP/s" and line["higher_is_better"] is True
+    assert line["steps"] == 1 and line["warmup"] == 3 and line["dtype"] == "f64"
+    assert line["config"]["workload"] == "tiny_dense"
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1
+    assert line["e2e"] == {"value": line["value"], "unit": "TFLOP/s",
+                           "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_prints_one_line():
+    """`--impl reference` times the oracle on the host cores and needs no GPU."""
+    lines = _run(["bench.py", "--impl", "reference", "--workload", "tiny_dense",
+                  "--steps", "1", "--warmup", "3"])
+    assert len(lines) == 1
+    _check_reference_line(lines[0], 1)
+
+
+def test_reference_arm_two_ranks_rank0_only():
+    """Under the two-process launcher rank 0 alone prints; the other rank exits 0."""
+    lines = _run(["-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+                  "--master-addr", "127.0.0.1", "--master-port", "29541", "bench.py",
+                  "--impl", "reference", "--workload", "tiny_dense", "--gpus", "2",
+                  "--steps", "1", "--warmup", "3"])
+    assert len(lines) == 1
+    _check_reference_line(lines[0], 2)
