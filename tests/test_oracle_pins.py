@@ -54,15 +54,10 @@ def _loss(oracle_mod, p, q, k, v, do):
     return float(np.sum(o * do))
 
 
-@pytest.mark.parametrize("name", sorted(FD_CASES))
-def test_backward_matches_central_differences(oracle_mod, name):
-    """dL/dQ, dL/dK, dL/dV of L = sum(O * dO) by central differences of the forward."""
-    p = FD_CASES[name]
-    q, k, v, do = _inputs(p, seed=sum(map(ord, name)))
-    o, lse = oracle_mod.forward(p, q, k, v)
-    dq, dk, dv = oracle_mod.backward(p, q, k, v, o, do, lse)
-    h = 1e-6
-    for tensor, grad, which in ((q, dq, "q"), (k, dk, "k"), (v, dv, "v")):
+def _central_differences(oracle_mod, p, q, k, v, do, h=1e-6):
+    """dL/dQ, dL/dK, dL/dV of L = sum(O * dO), element by element, from the forward alone."""
+    out = []
+    for which, tensor in (("q", q), ("k", k), ("v", v)):
         fd = np.zeros_like(tensor)
         it = np.nditer(tensor, flags=["multi_index"])
         for _ in it:
@@ -77,8 +72,50 @@ def test_backward_matches_central_differences(oracle_mod, name):
             args[which] = minus
             lm = _loss(oracle_mod, p, args["q"], args["k"], args["v"], do)
             fd[idx] = (lp - lm) / (2 * h)
-        scale = max(1.0, float(np.abs(fd).max()))
-        np.testing.assert_allclose(grad, fd, rtol=0, atol=2e-7 * scale, err_msg=f"d{which}")
+        out.append(fd)
+    return out
+
+
+def _fd_tol(fd):
+    return 2e-7 * max(1.0, float(np.abs(fd).max()))
+
+
+@pytest.mark.parametrize("name", sorted(FD_CASES))
+def test_backward_matches_central_differences(oracle_mod, name):
+    """dL/dQ, dL/dK, dL/dV of L = sum(O * dO) by central differences of the forward."""
+    p = FD_CASES[name]
+    q, k, v, do = _inputs(p, seed=sum(map(ord, name)))
+    o, lse = oracle_mod.forward(p, q, k, v)
+    grads = oracle_mod.backward(p, q, k, v, o, do, lse)
+    fds = _central_differences(oracle_mod, p, q, k, v, do)
+    for grad, fd, which in zip(grads, fds, "qkv"):
+        np.testing.assert_allclose(grad, fd, rtol=0, atol=_fd_tol(fd), err_msg=f"d{which}")
+
+
+def test_finite_difference_pin_rejects_planted_mistakes(oracle_mod):
+    """The pin above has teeth: backward results with a planted mistake (made on
+    the CPU by feeding the oracle a wrong argument, or by altering its output)
+    miss the central differences by far more than the tolerance."""
+    import dataclasses
+    p = Problem(1, 2, 2, 6, 6, 4, 4, causal=True, window_left=3, scale=0.6)
+    q, k, v, do = _inputs(p, seed=11)
+    o, lse = oracle_mod.forward(p, q, k, v)
+    fds = _central_differences(oracle_mod, p, q, k, v, do)
+    good = oracle_mod.backward(p, q, k, v, o, do, lse)
+    wider = dataclasses.replace(p, window_left=4)
+    kq = oracle_mod.backward(p, k, q, v, o, do, lse)  # Q and K exchanged: S transposed
+    mutants = {
+        "dropped delta": oracle_mod.backward(p, q, k, v, np.zeros_like(o), do, lse),
+        "sign of dS": (-good[0], -good[1], good[2]),
+        "scale missing from dK": (good[0], good[1] / p.scale, good[2]),
+        "transposed scores": (kq[1], kq[0], kq[2]),
+        "window edge off by one": oracle_mod.backward(wider, q, k, v, o, do, lse),
+    }
+    for grad, fd in zip(good, fds):
+        assert np.abs(grad - fd).max() <= _fd_tol(fd)
+    for what, grads in mutants.items():
+        miss = max(np.abs(g - fd).max() / _fd_tol(fd) for g, fd in zip(grads, fds))
+        assert miss > 100, what
 
 
 @pytest.mark.parametrize("name", ["dense", "causal_br_long_q", "padded", "gqa", "window_causal"])
