@@ -122,6 +122,55 @@ def _check_bf16(name, t, shape, dtype=torch.bfloat16):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
 
 
+def _check_lens(B, seq_q_lens, seq_kv_lens):
+    for name, lens in (("seq_q_lens", seq_q_lens), ("seq_kv_lens", seq_kv_lens)):
+        if lens is not None and (lens.dtype != torch.int32 or not lens.is_cuda or lens.numel() != B
+                                 or not lens.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor of B elements")
+
+
+def _check_lse(lse, B, Hq, Sq):
+    if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous() \
+            or lse.numel() != B * Hq * Sq:
+        raise ValueError("lse must be a contiguous fp32 CUDA tensor with B*Hq*Sq elements")
+
+
+def _check_workspace(workspace) -> int:
+    if workspace is None:
+        return 0
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    return workspace.numel() * workspace.element_size()
+
+
+def _check_sink(sink, dsink, Hq):
+    """Validates the fp32 (Hq,) sink logits; returns dsink (allocated when None)."""
+    if sink.dtype != torch.float32 or not sink.is_cuda or not sink.is_contiguous() \
+            or sink.numel() != Hq:
+        raise ValueError("sink must be a contiguous fp32 CUDA tensor of Hq elements")
+    dsink = torch.empty_like(sink) if dsink is None else dsink
+    if dsink.dtype != torch.float32 or not dsink.is_cuda or not dsink.is_contiguous() \
+            or dsink.numel() != Hq:
+        raise ValueError("dsink must be a contiguous fp32 CUDA tensor of Hq elements")
+    return dsink
+
+
+def _check_same_device(ref: torch.Tensor, **tensors) -> None:
+    """Every tensor argument lives on ref's device (the library takes raw pointers
+    and launches on one device)."""
+    for name, t in tensors.items():
+        if t is not None and t.device != ref.device:
+            raise ValueError(f"{name} is on {t.device} but q is on {ref.device}: "
+                             "all tensors must be on one device")
+
+
+def _check_launch_device(ref: torch.Tensor) -> None:
+    """The library launches on the current CUDA device: it must be the tensors' one."""
+    if ref.device.index != torch.cuda.current_device():
+        raise ValueError(f"the tensors are on {ref.device} but the current device is "
+                         f"cuda:{torch.cuda.current_device()}: call under torch.cuda.device({ref.device})")
+
+
 # io element types of the C ABI (sdpa_dtype) for the typed entry points.
 _IO_CODES = {torch.bfloat16: 0, torch.float16: 2}
 
@@ -145,12 +194,12 @@ def sdpa_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
              stream: Optional[torch.cuda.Stream] = None):
     """dQ, dK, dV of scaled-dot-product attention (see include/sdpa_bwd.h).
 
-    q (B,Hq,Sq,Dqk), k (B,Hkv,Skv,Dqk), v (B,Hkv,Skv,Dv), o/do (B,Hq,Sq,Dv): bf16 CUDA,
-    contiguous. lse (B,Hq,Sq) fp32 natural-log forward statistic. Lengths: int32 (B,) CUDA.
+    q (B,Hq,Sq,Dqk), k (B,Hkv,Skv,Dqk), v (B,Hkv,Skv,Dv), o/do (B,Hq,Sq,Dv): bf16 or fp16
+    (one type for all) CUDA tensors on the current device, contiguous. lse (B,Hq,Sq) fp32 natural-log forward statistic. Lengths: int32 (B,) CUDA.
     Outputs are allocated when not given. Runs on ``stream`` (default: current stream).
     With ``sink`` (fp32 (Hq,) CUDA sink logits, already folded into ``lse`` by the
     forward) the call goes through sdpa_bwd_sink and returns (dq, dk, dv, dsink).
-    With ``bias`` ((1|B, Hq, Sq, Skv) bf16 or fp32 CUDA, contiguous: the additive
+    With ``bias`` ((1|B, Hq, Sq, Skv) bf16, fp16 or fp32 CUDA, contiguous: the additive
     bias that ``lse`` was computed with) the call goes through sdpa_bwd_bias and,
     unless ``bias_grad`` is False, appends the fp32 dBias (shaped like ``bias``) to
     the returned tuple (``dbias_dtype`` float32, or bfloat16 / float16 for the
@@ -168,24 +217,22 @@ def sdpa_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
     _check_bf16("v", v, (B, Hkv, Skv, Dv), io)
     _check_bf16("o", o, (B, Hq, Sq, Dv), io)
     _check_bf16("do", do, (B, Hq, Sq, Dv), io)
-    if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous() \
-            or lse.numel() != B * Hq * Sq:
-        raise ValueError("lse must be a contiguous fp32 CUDA tensor with B*Hq*Sq elements")
-    for name, lens in (("seq_q_lens", seq_q_lens), ("seq_kv_lens", seq_kv_lens)):
-        if lens is not None and (lens.dtype != torch.int32 or not lens.is_cuda or lens.numel() != B
-                                 or not lens.is_contiguous()):
-            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor of B elements")
+    _check_lse(lse, B, Hq, Sq)
+    _check_lens(B, seq_q_lens, seq_kv_lens)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     _check_bf16("dq", dq, q.shape, io)
     _check_bf16("dk", dk, k.shape, io)
     _check_bf16("dv", dv, v.shape, io)
-    ws_bytes = 0
-    if workspace is not None:
-        if not workspace.is_cuda or not workspace.is_contiguous():
-            raise ValueError("workspace must be a contiguous CUDA tensor")
-        ws_bytes = workspace.numel() * workspace.element_size()
+    ws_bytes = _check_workspace(workspace)
+    if sink is not None:
+        dsink = _check_sink(sink, dsink, Hq)
+    _check_same_device(q, k=k, v=v, o=o, do=do, lse=lse, seq_q_lens=seq_q_lens,
+                       seq_kv_lens=seq_kv_lens, dq=dq, dk=dk, dv=dv, workspace=workspace,
+                       sink=sink, dsink=dsink if sink is not None else None, bias=bias,
+                       dbias=dbias if bias is not None and bias_grad else None)
+    _check_launch_device(q)
     sc = 0.0 if scale is None else float(scale)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
             _ptr(dv), B, Hq, Hkv, Sq, Skv, Dqk, Dv, sc, int(causal), int(bottom_right),
@@ -193,8 +240,6 @@ def sdpa_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
             _ptr(seq_kv_lens), _ptr(workspace), ws_bytes)
     if io == torch.float16 or (bias is not None and bias_grad and dbias_dtype != torch.float32):
         # the general typed entry: fp16 io, or an io-type dBias (sink and bias optional)
-        if sink is not None:
-            dsink = torch.empty_like(sink) if dsink is None else dsink
         bias_dtype, bias_batch = 0, 0
         if bias is not None:
             bias_dtype = _check_bias(bias, B, Hq, Sq, Skv)
@@ -225,14 +270,6 @@ def sdpa_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
         if rc != 0:
             raise SdpaError(rc, "sdpa_bwd")
         return dq, dk, dv
-    if sink is not None:
-        if sink.dtype != torch.float32 or not sink.is_cuda or not sink.is_contiguous() \
-                or sink.numel() != Hq:
-            raise ValueError("sink must be a contiguous fp32 CUDA tensor of Hq elements")
-        dsink = torch.empty_like(sink) if dsink is None else dsink
-        if dsink.dtype != torch.float32 or not dsink.is_cuda or not dsink.is_contiguous() \
-                or dsink.numel() != Hq:
-            raise ValueError("dsink must be a contiguous fp32 CUDA tensor of Hq elements")
     if bias is None:
         rc = lib.sdpa_bwd_sink(*args, _ptr(sink), _ptr(dsink), _stream_handle(stream))
         if rc != 0:
@@ -277,7 +314,7 @@ def sdpa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: Option
              stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
     """O (bf16, (B,Hq,Sq,Dv)) and natural-log LSE (fp32, (B,Hq,Sq)) of the masked
     softmax attention (see include/sdpa_bwd.h); the inputs of sdpa_bwd. ``bias``
-    ((1|B, Hq, Sq, Skv) bf16 or fp32 CUDA, contiguous) is added to the scaled
+    ((1|B, Hq, Sq, Skv) bf16, fp16 or fp32 CUDA, contiguous) is added to the scaled
     scores (sdpa_fwd_bias)."""
     lib = load()
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
@@ -289,19 +326,17 @@ def sdpa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: Option
     _check_bf16("q", q, (B, Hq, Sq, Dqk), io)
     _check_bf16("k", k, (B, Hkv, Skv, Dqk), io)
     _check_bf16("v", v, (B, Hkv, Skv, Dv), io)
-    for name, lens in (("seq_q_lens", seq_q_lens), ("seq_kv_lens", seq_kv_lens)):
-        if lens is not None and (lens.dtype != torch.int32 or not lens.is_cuda or lens.numel() != B
-                                 or not lens.is_contiguous()):
-            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor of B elements")
+    _check_lens(B, seq_q_lens, seq_kv_lens)
     if sink is not None and (sink.dtype != torch.float32 or not sink.is_cuda
                              or not sink.is_contiguous() or sink.numel() != Hq):
         raise ValueError("sink must be a contiguous fp32 CUDA tensor of Hq elements")
     o = torch.empty((B, Hq, Sq, Dv), dtype=io, device=q.device) if o is None else o
     lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device) if lse is None else lse
     _check_bf16("o", o, (B, Hq, Sq, Dv), io)
-    if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous() \
-            or lse.numel() != B * Hq * Sq:
-        raise ValueError("lse must be a contiguous fp32 CUDA tensor with B*Hq*Sq elements")
+    _check_lse(lse, B, Hq, Sq)
+    _check_same_device(q, k=k, v=v, o=o, lse=lse, seq_q_lens=seq_q_lens, seq_kv_lens=seq_kv_lens,
+                       sink=sink, bias=bias)
+    _check_launch_device(q)
     sc = 0.0 if scale is None else float(scale)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Skv, Dqk, Dv, sc,
             int(causal), int(bottom_right), int(window_left), int(window_right),
@@ -330,6 +365,8 @@ def nvfp4_fake_quant(x: torch.Tensor, out: Optional[torch.Tensor] = None,
         raise ValueError("x must be a contiguous bf16 CUDA tensor")
     out = torch.empty_like(x) if out is None else out
     _check_bf16("out", out, x.shape)
+    _check_same_device(x, out=out)
+    _check_launch_device(x)
     rc = lib.sdpa_nvfp4_fake_quant(_ptr(x), _ptr(out), x.numel(), _stream_handle(stream))
     if rc != 0:
         raise SdpaError(rc, "sdpa_nvfp4_fake_quant")
@@ -355,19 +392,26 @@ def sdpa_bwd_nvfp4_qat(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o_hp: 
     """dQ, dK, dV of NVFP4 QAT attention (sdpa_bwd_nvfp4_qat): q, k, v unquantized,
     o_hp / lse from sdpa_fwd_nvfp4_qat. D = 128."""
     lib = load()
+    if not isinstance(q, torch.Tensor) or q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be (B, H, S, D) tensors")
     B, Hq, Sq, Dqk = q.shape
     Hkv, Skv, Dv = k.shape[1], k.shape[2], v.shape[3]
     for name, t, shape in (("q", q, (B, Hq, Sq, Dqk)), ("k", k, (B, Hkv, Skv, Dqk)),
                            ("v", v, (B, Hkv, Skv, Dv)), ("o_hp", o_hp, (B, Hq, Sq, Dv)),
                            ("do", do, (B, Hq, Sq, Dv))):
         _check_bf16(name, t, shape)
-    if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous() \
-            or lse.numel() != B * Hq * Sq:
-        raise ValueError("lse must be a contiguous fp32 CUDA tensor with B*Hq*Sq elements")
+    _check_lse(lse, B, Hq, Sq)
+    _check_lens(B, seq_q_lens, seq_kv_lens)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check_bf16("dq", dq, q.shape)
+    _check_bf16("dk", dk, k.shape)
+    _check_bf16("dv", dv, v.shape)
+    ws_bytes = _check_workspace(workspace)
+    _check_same_device(q, k=k, v=v, o_hp=o_hp, do=do, lse=lse, seq_q_lens=seq_q_lens,
+                       seq_kv_lens=seq_kv_lens, dq=dq, dk=dk, dv=dv, workspace=workspace)
+    _check_launch_device(q)
     rc = lib.sdpa_bwd_nvfp4_qat(_ptr(q), _ptr(k), _ptr(v), _ptr(o_hp), _ptr(do), _ptr(lse), _ptr(dq),
                                 _ptr(dk), _ptr(dv), B, Hq, Hkv, Sq, Skv, Dqk, Dv,
                                 0.0 if scale is None else float(scale), int(causal),

@@ -163,6 +163,31 @@ def test_python_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
         pkg.load()
 
 
+def test_python_binding_checks_one_device():
+    """Tensors on different devices are refused before any pointer is passed."""
+    import torch
+    import attention_backward_sdpa_gb300 as pkg
+    a = torch.zeros(4)
+    pkg._check_same_device(a, b=torch.zeros(4), c=None)
+    with pytest.raises(ValueError, match="one device"):
+        pkg._check_same_device(a, b=torch.zeros(4, device="meta"))
+
+
+def test_python_binding_rejects_cpu_inputs_everywhere():
+    import torch
+    import attention_backward_sdpa_gb300 as pkg
+    x = torch.zeros(1, 2, 128, 128, dtype=torch.bfloat16)
+    lse = torch.zeros(1, 2, 128)
+    with pytest.raises(ValueError):
+        pkg.sdpa_bwd_nvfp4_qat(x, x, x, x, x, lse)
+    with pytest.raises(ValueError):
+        pkg.sdpa_fwd(x, x, x)
+    with pytest.raises(ValueError):
+        pkg.nvfp4_fake_quant(x)
+    with pytest.raises(ValueError):
+        pkg._check_sink(torch.zeros(2), None, 2)
+
+
 def test_public_names_exist():
     import attention_backward_sdpa_gb300 as pkg
     assert [n for n in pkg.__all__ if not hasattr(pkg, n)] == []
