@@ -11,8 +11,15 @@
 // turn counters and the GQA partials) comes from the static array below.
 //
 // Costs and limits:
-//   - Every GPU that loads the library holds NOALLOC_SCRATCH_BYTES of device
-//     memory for this array until the process exits.
+//   - The array takes NOALLOC_SCRATCH_BYTES of device memory on each GPU where
+//     the code module holding it is loaded, until the process exits. Under
+//     CUDA's default lazy module loading that happens at the first call on
+//     that GPU (the address lookup below), and the chain's kernel modules load
+//     at their first launch; both need device memory. A caller whose framework
+//     later reserves the whole device pool should therefore make one small
+//     call on each GPU before the pool is reserved (or run with
+//     CUDA_MODULE_LOADING=EAGER, which loads every module, the array included,
+//     when the CUDA context is created).
 //   - A problem whose workspace (sdpa_bwd_workspace_size) exceeds the array is
 //     rejected with SDPA_ERR_WORKSPACE before anything is launched.
 //   - All calls on a device share the one array, which keeps the contents the

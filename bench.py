@@ -45,7 +45,7 @@ import workloads  # noqa: E402
 
 METRIC = "SDPA backward TFLOP/s (bf16, 1xGB300) and fraction of dense tensor peak"
 METRIC_FWD = "SDPA forward TFLOP/s (bf16, 1xGB300) and fraction of dense tensor peak"
-DEFAULT_WORKLOAD = "causal_mha"
+DEFAULT_WORKLOAD = "causal_gqa_det"
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -376,7 +376,7 @@ def cpu_baseline_leg(w, t, target_s=12.0):
 
 # ---------------------------------------------------------------- GPU leg
 # DRAM bytes per launch of the main kernel (dram__bytes_read.sum +
-# dram__bytes_write.sum from one ncu capture, profiles/sdpa_bwd_main_traffic.md),
+# dram__bytes_write.sum from one ncu capture of the same bench command),
 # valid only for the kernel sources they were taken on: the digest covers the
 # kernel's source files, and a changed kernel reports null. D_qk = 192 runs
 # sdpa_bwd_main_ds, every other head dim sdpa_bwd_main.

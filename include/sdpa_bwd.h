@@ -349,8 +349,13 @@ int sdpa_bwd_profile_read(float* ms, int* launches, int n);
  *
  * Same arguments and results as sdpa_bwd() without the workspace: the caller
  * still provides every input and output, and the chain's scratch memory comes
- * from a 16 MiB device array compiled into the library (held on every GPU that
- * loads the library until the process exits). It calls no allocator.
+ * from a 16 MiB device array compiled into the library. It calls no allocator.
+ *   - The array occupies 16 MiB on a GPU from the moment the library's code
+ *     module holding it is loaded there until the process exits. Under CUDA's
+ *     default lazy module loading that is the first call on that GPU, and the
+ *     kernels' modules load at their first launch; both take device memory. A
+ *     caller whose framework later reserves the whole device pool makes one
+ *     small call on each GPU first (or sets CUDA_MODULE_LOADING=EAGER).
  *   - Problems whose sdpa_bwd_workspace_size() exceeds 16 MiB (16777216 bytes)
  *     return SDPA_ERR_WORKSPACE before anything is launched.
  *   - All calls on a device share that array and it keeps what the last call

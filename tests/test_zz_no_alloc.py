@@ -2,10 +2,15 @@
 
 It serves callers that cannot allocate device memory where they run the
 backward (for example a plugin of a framework that owns the whole device
-memory pool). Its scratch is a fixed 16 MiB array inside the library, so these
-checks make two calls in a row on different problems (the array keeps the
-previous call's contents) and compare each with the workspace-taking
-sdpa_bwd on the same inputs, within the parity tolerance of the other tests.
+memory pool). Its scratch is a fixed 16 MiB array inside the library, shared
+by every call and keeping what the previous call left. So the check makes a
+series of calls in a row on different problems, one per dQ route that carves
+its scratch from the array (the fp32 accumulator of the reduction route, the
+ordered relay's counters, the stored dS tiles and the zero tile of the
+two-kernel route, the GQA partial sets), each after a larger call has left
+stale data in the array. Each result is compared with the fp64 oracle and with
+the workspace-taking sdpa_bwd on the same inputs, within the parity tolerance
+of the other tests; deterministic calls must equal sdpa_bwd bit for bit.
 This file is collected last so that a run stopping at the first failure has
 already run every other test.
 """
@@ -15,7 +20,7 @@ import pytest
 import torch
 
 import workloads
-from harness import assert_close, make_case, to_device
+from harness import assert_close, make_case, oracle_backward, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -44,33 +49,50 @@ def _call_noalloc(lib, w, d, outs):
                                 stream)
 
 
+# In call order. The first fills most of the array with accumulator values, so
+# every later call starts from another call's leftovers.
 CASES = [
-    W("noalloc_gqa", 1, 4, 2, 384, 384, 128, 128, causal=True, window_left=200, seed=31),
+    # reduction route (fp32 dQ accumulator), GQA with a sliding window
+    W("noalloc_gqa", 1, 8, 2, 1000, 1000, 128, 128, causal=True, window_left=300, seed=31),
+    # ordered relay (D 64, deterministic): turn counters and the accumulator
     W("noalloc_padded", 2, 2, 2, 300, 300, 64, 64, causal=True, bottom_right=True,
       padded=(100, 300), deterministic=True, seed=32),
+    # two-kernel route (D 128, deterministic): stored dS tiles, the zero tile,
+    # GQA partial sets
+    W("noalloc_det128", 1, 4, 2, 320, 320, 128, 128, causal=True, deterministic=True, seed=33),
+    # two-kernel route at D_qk 192 / D_v 128 (non-deterministic)
+    W("noalloc_mla", 1, 2, 2, 260, 260, 192, 128, causal=True, bottom_right=True, seed=34),
+    # the reduction route once more, after the dS calls
+    W("noalloc_dense", 1, 2, 1, 200, 330, 128, 128, seed=35),
 ]
 
 
-def test_noalloc_matches_sdpa_bwd_on_two_calls_in_a_row():
+def test_noalloc_matches_oracle_and_sdpa_bwd_on_calls_in_a_row():
     lib, pkg = _lib()
     for w in CASES:
         assert pkg.workspace_size(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.Dqk, w.Dv, w.deterministic) \
             <= LIMIT_BYTES
     cases = [make_case(w) for w in CASES]
     devs = [to_device(c) for c in cases]
-    for w, d in zip(CASES, devs):  # two calls in a row, different problems
-        outs = [torch.full_like(d["q"], float("nan")), torch.full_like(d["k"], float("nan")),
-                torch.full_like(d["v"], float("nan"))]
-        assert _call_noalloc(lib, w, d, outs) == 0
-        pkg.check_device_status()
-        ref = pkg.sdpa_bwd(d["q"], d["k"], d["v"], d["o"], d["do"], d["lse"],
-                           scale=w.resolved_scale, causal=w.causal, bottom_right=w.bottom_right,
-                           window_left=w.window_left, window_right=w.window_right,
-                           deterministic=w.deterministic, seq_q_lens=d["seq_q_lens"],
-                           seq_kv_lens=d["seq_kv_lens"])
-        torch.cuda.synchronize()
-        for name, g, r in zip(("dq", "dk", "dv"), outs, ref):
-            assert_close(name, g.double().cpu().numpy(), r.double().cpu().numpy())
+    for rep in range(2):  # the whole series twice: every call follows another
+        for w, c, d in zip(CASES, cases, devs):
+            outs = [torch.full_like(d["q"], float("nan")), torch.full_like(d["k"], float("nan")),
+                    torch.full_like(d["v"], float("nan"))]
+            assert _call_noalloc(lib, w, d, outs) == 0, w.name
+            pkg.check_device_status()
+            ref = pkg.sdpa_bwd(d["q"], d["k"], d["v"], d["o"], d["do"], d["lse"],
+                               scale=w.resolved_scale, causal=w.causal,
+                               bottom_right=w.bottom_right, window_left=w.window_left,
+                               window_right=w.window_right, deterministic=w.deterministic,
+                               seq_q_lens=d["seq_q_lens"], seq_kv_lens=d["seq_kv_lens"])
+            torch.cuda.synchronize()
+            exact = oracle_backward(c)
+            for name, g, r, e in zip(("dq", "dk", "dv"), outs, ref, exact):
+                g64 = g.double().cpu().numpy()
+                assert_close(f"{w.name} {name} vs oracle", g64, e)
+                assert_close(f"{w.name} {name} vs sdpa_bwd", g64, r.double().cpu().numpy())
+                if w.deterministic:
+                    assert torch.equal(g, r), f"{w.name} {name}: not bitwise equal to sdpa_bwd"
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
