@@ -76,6 +76,7 @@ __global__ void __launch_bounds__(256) sdpa_bwd_preprocess(const ChainParams p) 
     const __nv_bfloat16* o_base = p.o + (long long)bh * p.Sq * DV + sub * 8;
     const __nv_bfloat16* do_base = p.d_o + (long long)bh * p.Sq * DV + sub * 8;
     uint4 vo[PASSES], vd[PASSES];
+    float lv[PASSES];  // the rows' LSE, loaded with O and dO rather than after the sums
 #pragma unroll
     for (int u = 0; u < PASSES; ++u) {
       const int q = qt * BQ + u * RPP + rsub;
@@ -86,6 +87,7 @@ __global__ void __launch_bounds__(256) sdpa_bwd_preprocess(const ChainParams p) 
         vo[u] = make_uint4(0, 0, 0, 0);
         vd[u] = make_uint4(0, 0, 0, 0);
       }
+      lv[u] = (q < Lq && sub == 0) ? p.lse[(long long)bh * p.Sq + q] : 0.f;
     }
     float* qs = p.qstat + (long long)t * QSTAT_FLOATS;
     const float sink2 = p.dsink_part ? p.sink[bh % (unsigned)p.Hq] * LOG2E : 0.f;
@@ -104,7 +106,7 @@ __global__ void __launch_bounds__(256) sdpa_bwd_preprocess(const ChainParams p) 
       if (sub == 0) {
         float lse2 = INFINITY, delta = 0.f;
         if (q < Lq) {
-          const float l = p.lse[(long long)bh * p.Sq + q];
+          const float l = lv[u];
           lse2 = (l == -INFINITY) ? INFINITY : l * LOG2E;
           delta = dot;
         }

@@ -87,7 +87,7 @@ static_assert(128 * (2 * REGS_COMPUTE + REGS_DQ + REGS_CTRL) <= MAIN_THREADS * 1
 constexpr uint64_t WAIT_LIMIT_NS = 4000000000ull;  // 4 s: far above any legal wait
 
 enum : int {
-  BAR_KV = 0,
+  BAR_K = 0,            // the K tile has landed (G1, G5)
   BAR_QFULL = 1,        // + stage (up to 4)
   BAR_QEMPTY = 5,       // + stage (up to 4)
   BAR_SFULL = 9,        // + slot (2)
@@ -102,7 +102,8 @@ enum : int {
   BAR_DPREAD = 26,      // + slot, 128 arrivals: dP^T has been loaded into registers
   BAR_STAGEREADY = 28,  // + staging half (2), 128 arrivals: the half is written
   BAR_STAGEFREE = 30,   // + staging half (2): its bulk reduction has read it
-  NUM_BARS = 32
+  BAR_V = 32,           // the V tile has landed (G2)
+  NUM_BARS = 33
 };
 
 // NST Q/dO stages; the dQ staging buffer exists only on the dQ-reduction route
@@ -313,18 +314,12 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
     if (warp == 12) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && n > 0) {
-      mbar_arrive_expect_tx(&bars[BAR_KV], 2 * L::TILE_KV);
-      for (int blk = 0; blk < D / 64; ++blk) {
-        tma_load_3d(sK + blk * L::BLK_KV, &maps.k, &bars[BAR_KV], blk * 64, k0, b * p.Hkv + hk);
-        tma_load_3d(sV + blk * L::BLK_KV, &maps.v, &bars[BAR_KV], blk * 64, k0, b * p.Hkv + hk);
-      }
-      pdl_wait_prior_grid();  // row statistics come from the preprocess kernel
-      for (int t = 0; t < n; ++t) {
-        const int st = t % NSTAGE;
-        if (t >= NSTAGE && !mbar_wait(&bars[BAR_QEMPTY + st], ((t / NSTAGE) - 1) & 1, abort_flag,
-                                      WAIT_LIMIT_NS))
-          break;
-        const int hj = t / n1;
+      // K first, then the first tile's Q and dO, then V: G1 of the first tile
+      // needs only K and Q, so its score GEMM and softmax can run while V and
+      // dO are still landing. Q, dO, K and V are inputs of the chain; only the
+      // row statistics come from the preprocess kernel, so they alone wait for it.
+      auto load_q_do = [&](int t) {
+        const int st = t % NSTAGE, hj = t / n1;
         const int qt = qt_hi - (t - hj * n1), bh = bh0 + hj;
         uint64_t* full = &bars[BAR_QFULL + st];
         mbar_arrive_expect_tx(full, 2 * L::TILE_Q + QSTAT_FLOATS * 4);
@@ -332,8 +327,30 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
           tma_load_3d(sQ + st * L::TILE_Q + blk * L::BLK_Q, &maps.q, full, blk * 64, qt * BQ, bh);
           tma_load_3d(sDO + st * L::TILE_Q + blk * L::BLK_Q, &maps.d_o, full, blk * 64, qt * BQ, bh);
         }
+      };
+      auto load_qstat = [&](int t) {
+        const int st = t % NSTAGE, hj = t / n1;
+        const int qt = qt_hi - (t - hj * n1), bh = bh0 + hj;
         bulk_load(sQS + st * QSTAT_FLOATS,
-                  p.qstat + ((long long)bh * p.n_qt + qt) * QSTAT_FLOATS, QSTAT_FLOATS * 4, full);
+                  p.qstat + ((long long)bh * p.n_qt + qt) * QSTAT_FLOATS, QSTAT_FLOATS * 4,
+                  &bars[BAR_QFULL + st]);
+      };
+      mbar_arrive_expect_tx(&bars[BAR_K], L::TILE_KV);
+      for (int blk = 0; blk < D / 64; ++blk)
+        tma_load_3d(sK + blk * L::BLK_KV, &maps.k, &bars[BAR_K], blk * 64, k0, b * p.Hkv + hk);
+      load_q_do(0);
+      mbar_arrive_expect_tx(&bars[BAR_V], L::TILE_KV);
+      for (int blk = 0; blk < D / 64; ++blk)
+        tma_load_3d(sV + blk * L::BLK_KV, &maps.v, &bars[BAR_V], blk * 64, k0, b * p.Hkv + hk);
+      pdl_wait_prior_grid();  // row statistics come from the preprocess kernel
+      load_qstat(0);
+      for (int t = 1; t < n; ++t) {
+        const int st = t % NSTAGE;
+        if (t >= NSTAGE && !mbar_wait(&bars[BAR_QEMPTY + st], ((t / NSTAGE) - 1) & 1, abort_flag,
+                                      WAIT_LIMIT_NS))
+          break;
+        load_q_do(t);
+        load_qstat(t);
       }
     }
     } else if (warp == 13 || warp == 14) {
@@ -351,7 +368,8 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
       constexpr uint64_t T_MN_Q = sdesc_sw128_template(L::BLK_Q, 1024);    // MN-major, 64-row tiles
       constexpr uint64_t T_MN_KV = sdesc_sw128_template(L::BLK_KV, 1024);  // MN-major, 128-row tiles
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
-      bool ok = n > 0 && mbar_wait(&bars[BAR_KV], 0, abort_flag, WAIT_LIMIT_NS);
+      // Both issuers need K (G1, G5); G2 also needs V, waited for before its first use.
+      bool ok = n > 0 && mbar_wait(&bars[BAR_K], 0, abort_flag, WAIT_LIMIT_NS);
       if (warp == 13) {
         for (int t = 0; t < n && ok; ++t) {
           const int s = t & 1, st = t % NSTAGE, j = t >> 1;
@@ -383,6 +401,7 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
           if (!DS_OUT && t >= 2 &&
               !mbar_wait(&bars[BAR_DQEMPTY + s], (j - 1) & 1, abort_flag, WAIT_LIMIT_NS))
             break;
+          if (t == 0 && !mbar_wait(&bars[BAR_V], 0, abort_flag, WAIT_LIMIT_NS)) break;
           __syncwarp();
           tc_fence_after();
           if (elect_one()) {
@@ -574,7 +593,11 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
       if (!ok) break;
     }
     if (leader) {
-      bulk_wait_group0();
+      // The relay releases the last turn only once the reductions have landed;
+      // otherwise the CTA may leave as soon as they have read shared memory
+      // (the writes complete before the grid does).
+      if (p.deterministic) bulk_wait_group0();
+      else bulk_wait_group_read0();
       if (pending_counter != nullptr) {
         fence_proxy_async_global();
         st_release_gpu(pending_counter, pending_turn + 1);
