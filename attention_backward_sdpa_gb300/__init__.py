@@ -20,7 +20,7 @@ import torch
 from . import _build
 
 __all__ = ["sdpa_bwd", "sdpa_fwd", "workspace_size", "nvfp4_fake_quant", "sdpa_fwd_nvfp4_qat",
-           "sdpa_bwd_nvfp4_qat", "nvfp4_qat_workspace_size", "check_device_status",
+           "sdpa_bwd_nvfp4_qat", "nvfp4_qat_workspace_size", "check_device_status", "debug_relay",
            "profile_enable", "profile_read", "library_path", "load", "SdpaError", "KERNEL_NAMES"]
 
 KERNEL_NAMES = ("preprocess", "main", "dq")
@@ -78,10 +78,12 @@ def load(build_if_missing: bool = False):
     lib.sdpa_bwd_nvfp4_qat.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i,
                                        ctypes.c_float, i, i, i, i, vp, vp, vp, sz, vp]
     lib.sdpa_bwd_nvfp4_qat.restype = i
-    lib.sdpa_bwd_workspace_size.argtypes = [i, i, i, i, i, i, i, i]
+    lib.sdpa_bwd_workspace_size.argtypes = [i] * 13
     lib.sdpa_bwd_workspace_size.restype = sz
     lib.sdpa_status_string.argtypes = [i]
     lib.sdpa_status_string.restype = ctypes.c_char_p
+    lib.sdpa_bwd_debug_relay.argtypes = [ctypes.c_ulonglong, i]
+    lib.sdpa_bwd_debug_relay.restype = i
     lib.sdpa_bwd_check_device_status.argtypes = [vp]
     lib.sdpa_bwd_check_device_status.restype = i
     lib.sdpa_bwd_profile_enable.argtypes = [i]
@@ -109,8 +111,14 @@ def _stream_handle(stream: Optional[torch.cuda.Stream]):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def workspace_size(B, Hq, Hkv, Sq, Skv, Dqk, Dv, deterministic=False) -> int:
-    return int(load().sdpa_bwd_workspace_size(B, Hq, Hkv, Sq, Skv, Dqk, Dv, int(deterministic)))
+def workspace_size(B, Hq, Hkv, Sq, Skv, Dqk, Dv, deterministic=False, *, causal=False,
+                   bottom_right=False, window_left=-1, window_right=-1, padded=False) -> int:
+    """Workspace bytes of sdpa_bwd for this shape and mask (``padded``: length
+    arrays will be passed). The defaults (no mask) give the largest size for the
+    shape, which serves every mask."""
+    return int(load().sdpa_bwd_workspace_size(B, Hq, Hkv, Sq, Skv, Dqk, Dv, int(causal),
+                                              int(bottom_right), int(window_left),
+                                              int(window_right), int(deterministic), int(padded)))
 
 
 def _check_bf16(name, t, shape, dtype=torch.bfloat16):
@@ -425,6 +433,12 @@ def sdpa_bwd_nvfp4_qat(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o_hp: 
 
 def nvfp4_qat_workspace_size(B, Hq, Hkv, Sq, Skv, Dqk, Dv) -> int:
     return int(load().sdpa_bwd_nvfp4_qat_workspace_size(B, Hq, Hkv, Sq, Skv, Dqk, Dv))
+
+
+def debug_relay(wait_limit_ns: int = 0, turn_skew: int = 0) -> None:
+    """Sets the ordered relay's wait limit (0: the 4 s default) and turn skew (0:
+    normal use) for later calls; see sdpa_bwd_debug_relay in the header."""
+    load().sdpa_bwd_debug_relay(int(wait_limit_ns), int(turn_skew))
 
 
 def check_device_status(stream: Optional[torch.cuda.Stream] = None) -> None:

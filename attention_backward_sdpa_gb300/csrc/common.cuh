@@ -80,16 +80,31 @@ struct ChainParams {
   int dbias_red;
   int dbias_out;        // element type written: 0 fp32, 1 bf16, 2 fp16 (0 whenever dbias_red)
 
-  // Deterministic two-kernel route: the main kernel stores each bf16 dS^T tile
-  // (its swizzled shared-memory image, DS_TILE_BYTES) at
-  // ds_ws + ((bh * n_kt + kt) * n_qt + qt) * DS_TILE_BYTES, and the dQ kernel
-  // reads them back in ascending key-tile order. zero_tile is DS_TILE_BYTES of
-  // zeros standing in for tiles the main kernel never visits.
+  // Two-kernel route: the main kernel stores each bf16 dS^T tile (its swizzled
+  // shared-memory image, DS_TILE_BYTES) at ds_tile(p, bh, ...) below, and the
+  // dQ kernel reads them back in ascending key-tile order. zero_tile is
+  // DS_TILE_BYTES of zeros standing in for tiles the main kernel never visits.
+  // The tiles of one (batch, query head) are stored key tile by key tile, each
+  // key tile's band of query tiles contiguous (ds_tile below): with ds_band the
+  // band is the query tiles the key tile visits at the full lengths, which
+  // contains every range it visits under shorter lengths when the mask is
+  // top-left aligned or no length array is given; otherwise (a bottom-right mask
+  // with per-batch lengths moves the diagonal) the band is every query tile.
+  // ds_band_tiles is the band size summed over the key tiles.
   int ds_route;
+  int ds_band;
+  long long ds_band_tiles;
   uint8_t* ds_ws;
   uint8_t* zero_tile;
 
   int* status;          // per-device status word
+  // Ordered relay (deterministic mode, D_qk up to 128 but not 128): how long a
+  // key tile waits for its turn before it gives up and reports a timeout, and a
+  // skew added to every expected turn (0; a nonzero skew makes the first key
+  // tile of each query tile wait for a turn that no tile releases, which is how
+  // the bounded wait is tested).
+  unsigned long long relay_wait_ns;
+  int relay_turn_skew;
 };
 
 constexpr int DS_TILE_BYTES = BN * BQ * 2;  // one dS^T tile: 128 keys x 64 queries, bf16
@@ -114,6 +129,36 @@ __host__ __device__ inline void visited_query_tiles(int kt, int Lq, int Lk, int 
   if (q_min > q_max) return;
   qt_lo = (int)(q_min / BQ);
   qt_hi = (int)(q_max / BQ);
+}
+
+// Band of query tiles [lo, hi] of key tile kt in the dS workspace (see ChainParams).
+__host__ __device__ inline void ds_band_range(const ChainParams& p, int kt, int& lo, int& hi) {
+  if (!p.ds_band) {
+    lo = 0;
+    hi = p.n_qt - 1;
+    return;
+  }
+  visited_query_tiles(kt, p.Sq, p.Skv, p.causal, p.bottom_right, p.window_left, p.window_right, lo, hi);
+}
+
+// Index (in tiles, within one (batch, query head)) of the first tile of key
+// tile kt's band: the band sizes of key tiles 0 .. kt-1 summed.
+__host__ __device__ inline long long ds_band_prefix(const ChainParams& p, int kt) {
+  long long s = 0;
+  for (int k = 0; k < kt; ++k) {
+    int lo, hi;
+    ds_band_range(p, k, lo, hi);
+    if (hi >= lo) s += hi - lo + 1;
+  }
+  return s;
+}
+
+// Address of the stored dS^T tile (bh, kt, qt); `prefix` = ds_band_prefix(p, kt)
+// and `band_lo` the first query tile of kt's band (callers compute both once per key
+// tile). qt must lie in the band.
+__host__ __device__ inline uint8_t* ds_tile(const ChainParams& p, int bh, long long prefix, int band_lo,
+                                            int qt) {
+  return p.ds_ws + ((long long)bh * p.ds_band_tiles + prefix + (qt - band_lo)) * (long long)DS_TILE_BYTES;
 }
 
 // Forward pass (sdpa_fwd.cu): O and the natural-log LSE of the masked softmax.

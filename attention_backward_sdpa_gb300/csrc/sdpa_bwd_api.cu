@@ -37,34 +37,76 @@ int g_num_sms[kMaxDevices] = {};
 
 // Profiling state.
 bool g_profile = false;
+
+// Ordered-relay wait limit and turn skew (sdpa_bwd_debug_relay).
+constexpr unsigned long long kRelayWaitDefaultNs = 4000000000ull;
+unsigned long long g_relay_wait_ns = kRelayWaitDefaultNs;
+int g_relay_turn_skew = 0;
 float g_prof_ms[3] = {};
 int g_prof_n[3] = {};
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Two-kernel route (dS stored, dQ from a Q-stationary kernel): the
-// deterministic route for D_qk = 128 as on the pages (the relay serves
-// D_qk = 64), and the only route for D_qk = 192, whose dK accumulator leaves no
-// tensor memory for dQ in the main kernel.
-bool use_ds_route(int deterministic, int Dqk) { return Dqk == 192 || (deterministic && Dqk == 128); }
+// Routes of the chain:
+//   kTwoKernel main kernel with dS stored, then the Q-stationary dQ kernel:
+//              the deterministic route for D_qk = 128 as on the pages (the
+//              relay serves every other D_qk up to 128), and the only route
+//              for D_qk = 192,
+//              whose dK accumulator leaves no tensor memory for dQ in the main
+//              kernel.
+//   kReduce    main kernel with the fp32 dQ accumulator (the ordered relay
+//              when deterministic), then the convert.
+enum class Route { kReduce, kTwoKernel };
+
+Route choose_route(int deterministic, int Dqk) {
+  return (Dqk == 192 || (deterministic && Dqk == 128)) ? Route::kTwoKernel : Route::kReduce;
+}
+
+// The problem shape and mask as far as they size the workspace.
+struct Shape {
+  int B, Hq, Hkv, Sq, Skv, Dqk, Dv;
+  int causal, bottom_right, window_left, window_right;
+  int padded;  // per-batch length arrays are given
+};
+
+// Band mode of the dS workspace (ChainParams::ds_band) and the band size per
+// (batch, query head) in tiles.
+void ds_band_geometry(const Shape& sh, int& band, long long& tiles) {
+  ChainParams p{};
+  p.Sq = sh.Sq;
+  p.Skv = sh.Skv;
+  p.n_qt = ceil_div(sh.Sq, BQ);
+  p.n_kt = ceil_div(sh.Skv, BN);
+  p.causal = sh.causal ? 1 : 0;
+  p.bottom_right = sh.bottom_right ? 1 : 0;
+  p.window_left = sh.window_left < 0 ? -1 : sh.window_left;
+  p.window_right = (sh.causal && sh.window_right > 0) ? sh.window_right : -1;
+  p.ds_band = (sh.bottom_right && sh.padded) ? 0 : 1;
+  band = p.ds_band;
+  tiles = ds_band_prefix(p, p.n_kt);
+}
 
 struct Carve {
   size_t qstat, dq_accum, ds_ws, zero_tile, counters, dk_ws, dv_ws, dsink_part;
   size_t q_hat, k_hat, v_hat;  // NVFP4 QAT: the fake-quantized Q, K, V
+  int ds_band;
+  long long ds_band_tiles;
   size_t total;
 };
 
-Carve carve(int B, int Hq, int Hkv, int Sq, int Skv, int Dqk, int Dv, bool ds_route, bool qat = false) {
-  const size_t n_qt = (size_t)ceil_div(Sq, BQ), n_kt = (size_t)ceil_div(Skv, BN);
+Carve carve(const Shape& sh, Route route, bool qat = false) {
+  const int B = sh.B, Hq = sh.Hq, Hkv = sh.Hkv, Sq = sh.Sq, Skv = sh.Skv, Dqk = sh.Dqk, Dv = sh.Dv;
+  const size_t n_qt = (size_t)ceil_div(Sq, BQ);
   const size_t bh = (size_t)B * Hq;
   Carve c{};
   size_t off = 0;
   c.qstat = off;
   off = align256(off + bh * n_qt * QSTAT_FLOATS * sizeof(float));
-  if (ds_route) {
+  if (route != Route::kReduce) {
+    ds_band_geometry(sh, c.ds_band, c.ds_band_tiles);
     c.dq_accum = SIZE_MAX;
     c.ds_ws = off;
-    off = align256(off + bh * n_kt * n_qt * (size_t)DS_TILE_BYTES);
+    off = align256(off + bh * (size_t)c.ds_band_tiles * (size_t)DS_TILE_BYTES);
     c.zero_tile = off;
     off = align256(off + DS_TILE_BYTES);
   } else {
@@ -72,7 +114,7 @@ Carve carve(int B, int Hq, int Hkv, int Sq, int Skv, int Dqk, int Dv, bool ds_ro
     c.dq_accum = off;  // rows of 64 or 128 columns: the width of the main kernel that runs
     off = align256(off + bh * n_qt * BQ * (size_t)(Dqk <= 64 ? 64 : 128) * sizeof(float));
   }
-  c.counters = off;
+  c.counters = off;  // turn counters, then the work ticket
   off = align256(off + (bh * n_qt + 1) * sizeof(int));
   c.dsink_part = off;  // sink-token partials (one float per 64-row tile); used only by sdpa_bwd_sink
   off = align256(off + bh * n_qt * sizeof(float));
@@ -195,7 +237,7 @@ using namespace sdpa;
 
 extern "C" {
 
-int sdpa_bwd_version(void) { return 100; }
+int sdpa_bwd_version(void) { return 200; }
 
 const char* sdpa_status_string(int status) {
   switch (status) {
@@ -211,17 +253,21 @@ const char* sdpa_status_string(int status) {
 }
 
 size_t sdpa_bwd_workspace_size(int B, int H_q, int H_kv, int S_q, int S_kv, int D_qk, int D_v,
-                               int deterministic) {
+                               int causal, int bottom_right, int window_left, int window_right,
+                               int deterministic, int padded) {
   if (basic_checks(B, H_q, H_kv, S_q, S_kv, D_qk, D_v) != SDPA_OK) return 0;
   if (S_q == 0 || S_kv == 0) return 0;
-  return carve(B, H_q, H_kv, S_q, S_kv, D_qk, D_v, use_ds_route(deterministic, D_qk)).total;
+  const Shape sh{B, H_q, H_kv, S_q, S_kv, D_qk, D_v, causal, bottom_right, window_left, window_right,
+                 padded};
+  return carve(sh, choose_route(deterministic, D_qk)).total;
 }
 
 size_t sdpa_bwd_nvfp4_qat_workspace_size(int B, int H_q, int H_kv, int S_q, int S_kv, int D_qk,
                                          int D_v) {
   if (basic_checks(B, H_q, H_kv, S_q, S_kv, D_qk, D_v) != SDPA_OK) return 0;
   if (D_qk != 128 || D_v != 128 || S_q == 0 || S_kv == 0) return 0;
-  return carve(B, H_q, H_kv, S_q, S_kv, D_qk, D_v, false, true).total;
+  const Shape sh{B, H_q, H_kv, S_q, S_kv, D_qk, D_v, 0, 0, -1, -1, 0};
+  return carve(sh, Route::kReduce, true).total;
 }
 
 int sdpa_bwd_profile_enable(int on) {
@@ -241,6 +287,13 @@ int sdpa_bwd_profile_read(float* ms, int* launches, int n) {
     if (launches) launches[i] = g_prof_n[i];
   }
   return 3;
+}
+
+int sdpa_bwd_debug_relay(unsigned long long wait_limit_ns, int turn_skew) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_relay_wait_ns = wait_limit_ns == 0 ? kRelayWaitDefaultNs : wait_limit_ns;
+  g_relay_turn_skew = turn_skew;
+  return SDPA_OK;
 }
 
 int sdpa_bwd_check_device_status(void* stream) {
@@ -335,8 +388,11 @@ int run_chain(const void* q, const void* k, const void* v, const void* o, const 
     return SDPA_OK;
   }
 
-  const bool ds_route = use_ds_route(deterministic, D_qk);
-  const Carve cv = carve(B, H_q, H_kv, S_q, S_kv, D_qk, D_v, ds_route, qat);
+  const Route route = choose_route(deterministic, D_qk);
+  const bool ds_route = route != Route::kReduce;
+  const Shape sh{B, H_q, H_kv, S_q, S_kv, D_qk, D_v, causal, bottom_right, window_left, window_right,
+                 (seq_q_lens || seq_kv_lens) ? 1 : 0};
+  const Carve cv = carve(sh, route, qat);
   bool own_ws = false;
   if (workspace == nullptr) {
     if (cudaMallocAsync(&workspace, cv.total, stream) != cudaSuccess) return SDPA_ERR_CUDA;
@@ -379,6 +435,8 @@ int run_chain(const void* q, const void* k, const void* v, const void* o, const 
   p.deterministic = (deterministic && !ds_route) ? 1 : 0;
   p.f16 = f16 ? 1 : 0;
   p.ds_route = ds_route ? 1 : 0;
+  p.ds_band = cv.ds_band;
+  p.ds_band_tiles = cv.ds_band_tiles;
   p.seq_q_lens = seq_q_lens;
   p.seq_kv_lens = seq_kv_lens;
   p.o = static_cast<const __nv_bfloat16*>(o);
@@ -400,6 +458,11 @@ int run_chain(const void* q, const void* k, const void* v, const void* o, const 
   p.dk_ws = p.n_part > 1 ? reinterpret_cast<__nv_bfloat16*>(ws + cv.dk_ws) : nullptr;
   p.dv_ws = p.n_part > 1 ? reinterpret_cast<__nv_bfloat16*>(ws + cv.dv_ws) : nullptr;
   p.status = status;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    p.relay_wait_ns = g_relay_wait_ns;
+    p.relay_turn_skew = g_relay_turn_skew;
+  }
   p.sink = dsink ? sink : nullptr;
   p.dsink = dsink;
   p.dsink_part = dsink ? reinterpret_cast<float*>(ws + cv.dsink_part) : nullptr;

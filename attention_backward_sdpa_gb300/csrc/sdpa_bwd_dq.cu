@@ -179,6 +179,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         mbar_arrive(&ufull[r]);
         if (u >= n_units) break;
         const DqUnit w = dq_unit(p, u);
+        long long band_prefix = w.n > 0 ? ds_band_prefix(p, w.kv_first) : 0;
         for (int i = 0; i < w.n; ++i, ++step) {
           const int st = step % L::NDS;
           const int kt = w.kv_first + i;
@@ -189,14 +190,16 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
           mbar_arrive_expect_tx(&dsfull[st], L::TILE_DS);
           int lo, hi;
           visited_query_tiles(kt, w.Lq, w.Lk, p.causal, p.bottom_right, p.window_left, p.window_right, lo, hi);
+          // Without length arrays the band is the visited range itself.
+          int band_lo = lo, band_hi = hi;
+          if (p.seq_q_lens != nullptr || p.seq_kv_lens != nullptr) ds_band_range(p, kt, band_lo, band_hi);
           for (int half = 0; half < 2; ++half) {
             const int qt = w.qt0 + half;
             const bool stored = qt < p.n_qt && lo <= qt && qt <= hi;
-            const uint8_t* src =
-                stored ? p.ds_ws + (((long long)w.bh * p.n_kt + kt) * p.n_qt + qt) * (long long)DS_TILE_BYTES
-                       : p.zero_tile;
+            const uint8_t* src = stored ? ds_tile(p, w.bh, band_prefix, band_lo, qt) : p.zero_tile;
             bulk_load(stage + half * DS_TILE_BYTES, src, DS_TILE_BYTES, &dsfull[st]);
           }
+          if (band_hi >= band_lo) band_prefix += band_hi - band_lo + 1;
         }
       }
     loads_done:;

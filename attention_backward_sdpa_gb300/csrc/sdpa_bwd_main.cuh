@@ -475,12 +475,15 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
       // stores it to the workspace (the dQ kernel's input) and releases the
       // buffer when the copy has read it, so no compute warp waits on the copy.
       if (lane == 0) {
+        int band_lo, band_hi;
+        ds_band_range(p, kt, band_lo, band_hi);
+        const long long band_prefix = ds_band_prefix(p, kt);
         for (int t = 0; t < n; ++t) {
           const int s = t & 1, j = t >> 1;
           if (!mbar_wait(&bars[BAR_DSREADY + s], j & 1, abort_flag, WAIT_LIMIT_NS)) break;
           const int hj = t / n1;
           const int qt = qt_hi - (t - hj * n1), bh = bh0 + hj;
-          uint8_t* dst = p.ds_ws + (((long long)bh * p.n_kt + kt) * p.n_qt + qt) * (long long)DS_TILE_BYTES;
+          uint8_t* dst = ds_tile(p, bh, band_prefix, band_lo, qt);
           bulk_store(dst, sDS + s * L::TILE_DS, DS_TILE_BYTES);
           bulk_commit_group();
           bulk_wait_group_read0();
@@ -541,12 +544,14 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
         const int kv_lo = has_window ? (int)max(0ll, floor_div((long long)qt * BQ + diag -
                                                                    p.window_left, BN))
                                      : 0;
-        const int turn = kt - kv_lo;
+        const int turn = kt - kv_lo + p.relay_turn_skew;
         int* counter = p.counters + (long long)bh * p.n_qt + qt;
         const uint64_t t0 = globaltimer_ns();
         while (ld_acquire_gpu(counter) != turn) {
           __nanosleep(32);
-          if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+          if (globaltimer_ns() - t0 > p.relay_wait_ns) {
+            // Gives up on the turn (the adds may then come out of order) and
+            // reports it; the kernel still completes.
             set_main_status(p.status, STATUS_TIMEOUT);
             break;
           }

@@ -320,11 +320,14 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
     // workspace and releases the buffer when the copy has read it, so no
     // compute warp waits on the copy.
     if (lane == 0) {
+      int band_lo, band_hi;
+      ds_band_range(p, kt, band_lo, band_hi);
+      const long long band_prefix = ds_band_prefix(p, kt);
       for (int t = 0; t < n; ++t) {
         const int s = t & 1, j = t >> 1;
         if (!mbar_wait(&bars[BAR_DSREADY + s], j & 1, abort_flag, WAIT_LIMIT_NS)) break;
         const int qt = qt_hi - t;
-        uint8_t* dst = p.ds_ws + (((long long)bh * p.n_kt + kt) * p.n_qt + qt) * (long long)DS_TILE_BYTES;
+        uint8_t* dst = ds_tile(p, bh, band_prefix, band_lo, qt);
         bulk_store(dst, sDS + s * L::TILE_DS, DS_TILE_BYTES);
         bulk_commit_group();
         bulk_wait_group_read0();

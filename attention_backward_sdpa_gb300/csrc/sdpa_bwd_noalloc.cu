@@ -73,7 +73,9 @@ int sdpa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                      int S_q, int S_kv, int D_qk, int D_v, float scale, int causal,
                      int bottom_right, int window_left, int window_right, int deterministic,
                      const int32_t* seq_q_lens, const int32_t* seq_kv_lens, void* stream) {
-  const size_t need = sdpa_bwd_workspace_size(B, H_q, H_kv, S_q, S_kv, D_qk, D_v, deterministic);
+  const size_t need = sdpa_bwd_workspace_size(B, H_q, H_kv, S_q, S_kv, D_qk, D_v, causal, bottom_right,
+                                              window_left, window_right, deterministic,
+                                              (seq_q_lens || seq_kv_lens) ? 1 : 0);
   if (need > NOALLOC_SCRATCH_BYTES) return SDPA_ERR_WORKSPACE;
   void* scratch = nullptr;
   const int rc = scratch_address(&scratch);

@@ -393,13 +393,13 @@ MAIN_TRAFFIC = {
 }
 
 
-def main_kernel_name(w) -> str:
+def main_kernel_name(w, tag=None) -> str:
     return "sdpa_bwd_main_ds" if w.Dqk == 192 else "sdpa_bwd_main"
 
 
 def main_traffic(w, tag=None):
     csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "attention_backward_sdpa_gb300", "csrc")
-    blob = b"".join(open(os.path.join(csrc, f), "rb").read() for f in MAIN_SOURCES[main_kernel_name(w)])
+    blob = b"".join(open(os.path.join(csrc, f), "rb").read() for f in MAIN_SOURCES[main_kernel_name(w, tag)])
     key = w.name if tag is None else f"{w.name}/{tag}"
     return MAIN_TRAFFIC.get(hashlib.sha256(blob).hexdigest()[:16], {}).get(key)
 
@@ -438,7 +438,11 @@ def run_gpu(args, w, t, o, lse, rank, world, device):
     lk = None if t["seq_kv_lens"] is None else t["seq_kv_lens"].to(device)
     dq, dk, dv = torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"])
     ws = torch.empty(max(pkg.workspace_size(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.Dqk, w.Dv,
-                                            w.deterministic), 256), dtype=torch.uint8, device=device)
+                                            w.deterministic, causal=w.causal,
+                                            bottom_right=w.bottom_right, window_left=w.window_left,
+                                            window_right=w.window_right,
+                                            padded=w.padded is not None), 256),
+                     dtype=torch.uint8, device=device)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
     kw = dict(scale=w.resolved_scale, causal=w.causal, bottom_right=w.bottom_right,
@@ -535,7 +539,7 @@ def run_gpu(args, w, t, o, lse, rank, world, device):
     kernel_ms = {k: round(v[0] / max(v[1], 1), 5) for k, v in prof.items() if v[1]}
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
             "frac": achieved / peak_tf, "traffic": main_traffic(w, bias_tag(t)),
-            "kernel": main_kernel_name(w), "peak_kind": f"{peak_kind} bf16 burst",
+            "kernel": main_kernel_name(w, bias_tag(t)), "peak_kind": f"{peak_kind} bf16 burst",
             "kernel_gflop": main_flops / 1e9}
     if "bias" in t:
         # With a bias the main kernel streams the bias and the fp32 dBias: it is
@@ -544,7 +548,7 @@ def run_gpu(args, w, t, o, lse, rank, world, device):
         gbs = nbytes / (main_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": gbs, "peak": peak_hbm, "unit": "GB/s",
                 "frac": gbs / peak_hbm, "traffic": main_traffic(w, bias_tag(t)),
-                "kernel": main_kernel_name(w), "peak_kind": f"{peak_kind} HBM copy",
+                "kernel": main_kernel_name(w, bias_tag(t)), "peak_kind": f"{peak_kind} HBM copy",
                 "algorithmic_bytes": nbytes, "tensor_tflops": achieved,
                 "tensor_frac": achieved / peak_tf}
     return {
@@ -554,7 +558,9 @@ def run_gpu(args, w, t, o, lse, rank, world, device):
         "e2e": {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "clocks": clocks.summary(),
-        "gpu_launches": (4 if args.sink else 6 if t.get("qat") else 3) * args.steps,
+        # preprocess + main + dQ kernel (+ the three fake quantizations with QAT,
+        # + dsink with sink tokens)
+        "gpu_launches": (3 + (3 if t.get("qat") else 0) + (1 if args.sink else 0)) * args.steps,
     }
 
 

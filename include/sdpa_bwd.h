@@ -64,18 +64,24 @@ typedef enum {
 } sdpa_dtype;
 
 /*
- * Bytes of device workspace sdpa_bwd() needs for this problem (0 when none).
- * The workspace holds, each region 256-byte aligned: per-query-tile fp32 row
- * statistics (LSE * log2(e) and delta); the fp32 dQ accumulator (rows of 64
- * columns for D_qk up to 64, else 128), or on the deterministic two-kernel
- * route the 16-bit dS tiles; the deterministic-mode turn
- * counters and a work ticket; one fp32 sink-token partial per query tile
+ * Bytes of device workspace sdpa_bwd() (and sdpa_bwd_sink, sdpa_bwd_bias,
+ * sdpa_bwd_typed) needs for this problem and mask (0 when none). The mask
+ * arguments are those of the call (padded: 1 when seq_q_lens or seq_kv_lens
+ * will be given). The workspace holds, each region 256-byte aligned:
+ * per-query-tile fp32 row statistics (LSE * log2(e) and delta); either the
+ * fp32 dQ accumulator (rows of 64 columns for D_qk up to 64, else 128) or, on
+ * the routes that store dS (deterministic D_qk = 128, every D_qk = 192), the
+ * 16-bit dS tiles of the band of query tiles each 128-key tile visits (the
+ * whole rectangle when a bottom-right mask meets per-batch lengths) plus one
+ * zero tile; the deterministic-mode turn counters (one int per query tile)
+ * and a work ticket; one fp32 sink-token partial per query tile
  * (sdpa_bwd_sink); and, when H_kv < H_q, the per-query-head 16-bit dK/dV
  * partials of the GQA reduction. The size does not depend on the io type.
  * Returns 0 for arguments sdpa_bwd() would reject.
  */
 size_t sdpa_bwd_workspace_size(int B, int H_q, int H_kv, int S_q, int S_kv, int D_qk, int D_v,
-                               int deterministic);
+                               int causal, int bottom_right, int window_left, int window_right,
+                               int deterministic, int padded);
 
 /*
  * SDPA backward. Arguments:
@@ -98,11 +104,12 @@ size_t sdpa_bwd_workspace_size(int B, int H_q, int H_kv, int S_q, int S_kv, int 
  *   deterministic     1: repeated calls give bitwise-identical dQ. For D_qk =
  *                     128 the main kernel stores dS and a second kernel forms
  *                     dQ = scale * dS K over an ascending key walk (larger
- *                     workspace: 2 bytes per (query, key) position); for
- *                     other D_qk up to 128 the dQ partials of the KV tiles are
- *                     added in ascending KV-tile order. D_qk = 192 always takes the
- *                     stored-dS route, so its dQ is reproducible in both
- *                     modes. dK and dV are bitwise reproducible in both modes.
+ *                     workspace: 2 bytes per visited (query, key) position);
+ *                     for other D_qk up to 128 the dQ partials of the KV tiles
+ *                     are added in ascending KV-tile order. D_qk = 192 always
+ *                     takes the stored-dS route, so its dQ is reproducible in
+ *                     both modes. dK and dV are bitwise reproducible in both
+ *                     modes.
  *   seq_q_lens,       device int32 (B,) per-batch valid lengths, or NULL for
  *   seq_kv_lens       "the full S". Queries at or past seq_q_lens[b] and keys
  *                     at or past seq_kv_lens[b] are masked; their gradient
@@ -323,6 +330,21 @@ const char* sdpa_status_string(int status);
  * if the synchronization itself failed.
  */
 int sdpa_bwd_check_device_status(void* stream);
+
+/*
+ * Failure detection of the ordered relay (deterministic mode for D_qk other
+ * than 128 and 192; cuDNN frontend docs, "SDPA Backward (SM120)", section
+ * "Deterministic vs. non-deterministic dQ": the relay can stall if its
+ * ordering assumption fails). Each key tile waits for its turn on a query
+ * tile at most `wait_limit_ns` nanoseconds (0 restores the default, 4 s);
+ * then it adds out of order, the call's results are not reproducible, and the
+ * next sdpa_bwd_check_device_status() returns SDPA_ERR_TIMEOUT. `turn_skew`
+ * (0 in normal use) is added to every expected turn: a nonzero skew makes the
+ * first key tile of each query tile wait for a turn that no tile releases,
+ * which exercises the bounded wait without any fault. Process-wide; applies
+ * to calls made afterwards. Returns SDPA_OK.
+ */
+int sdpa_bwd_debug_relay(unsigned long long wait_limit_ns, int turn_skew);
 
 /*
  * Per-kernel timing for benchmarks. While enabled, sdpa_bwd() records CUDA

@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.sdpa_bwd_version() == 100
+    assert lib.sdpa_bwd_version() == 200
     assert lib.sdpa_status_string(OK) == b"ok"
     for code in range(1, 7):
         assert lib.sdpa_status_string(code) not in (b"ok", b"unknown status")
@@ -50,19 +50,53 @@ def _a256(x):
     return (x + 255) // 256 * 256
 
 
-def expected_workspace(B, Hq, Hkv, Sq, Skv, Dqk, Dv, det=0):
+def visited_query_tiles(kt, Lq, Lk, causal, br, wl, wr):
+    """64-row query tiles that 128-key tile kt visits (the kernels' loop bounds),
+    restated from the mask definitions: keys k <= q + diag + max(wr, 0) when causal,
+    k >= q + diag - wl with a left window, diag = Lk - Lq when bottom-right."""
+    k0 = kt * 128
+    if k0 >= Lk or Lq <= 0:
+        return 0, -1
+    diag = Lk - Lq if br else 0
+    k_last = min(k0 + 127, Lk - 1)
+    q_min, q_max = 0, Lq - 1
+    if causal:
+        q_min = max(0, k0 - diag - max(wr, 0))
+    if wl >= 0:
+        q_max = min(q_max, k_last - diag + wl)
+    if q_min > q_max:
+        return 0, -1
+    return q_min // 64, q_max // 64
+
+
+def band_tiles(Sq, Skv, causal, br, wl, wr, padded):
+    """dS tiles stored per (batch, query head): the query tiles each key tile visits at
+    the full lengths, or every query tile when a bottom-right mask meets per-batch lengths."""
+    n_qt, n_kt = -(-Sq // 64), -(-Skv // 128)
+    if br and padded:
+        return n_kt * n_qt
+    tot = 0
+    for kt in range(n_kt):
+        lo, hi = visited_query_tiles(kt, Sq, Skv, causal, br, wl, wr if causal else -1)
+        tot += max(0, hi - lo + 1)
+    return tot
+
+
+def route(det, Dqk):
+    return "two" if Dqk == 192 or (det and Dqk == 128) else "reduce"
+
+
+def carve_size(B, Hq, Hkv, Sq, Skv, Dqk, Dv, rt, causal=0, br=0, wl=-1, wr=-1, padded=0):
     """Documented layout: per-query-tile row statistics (2 x 64 fp32 per 64-row tile);
     then either the fp32 dQ accumulator over whole 64-row tiles (rows of max(D_qk, 64)
-    columns: D_qk up to 64 runs on the 64-column kernels, up to 128 on the 128-column
-    ones), or (deterministic,
-    D_qk = 128: two-kernel route) one 16 KiB bf16 dS^T tile per (128-key tile,
-    64-query tile) plus one zero tile; one int per query tile plus a ticket; one fp32
-    sink-token partial per query tile; and for GQA the bf16 dK/dV partials with H_q
-    heads. Every region 256-byte aligned."""
-    n_qt, n_kt = -(-Sq // 64), -(-Skv // 128)
+    columns) or, on the routes that store dS, one 16 KiB dS^T tile per (128-key tile,
+    64-query tile of its band) plus one zero tile; one int per query tile plus a ticket;
+    one fp32 sink-token partial per query tile; and for GQA on the routes that split a
+    group, the bf16 dK/dV partials with H_q heads. Every region 256-byte aligned."""
+    n_qt = -(-Sq // 64)
     total = _a256(B * Hq * n_qt * 128 * 4)
-    if (det and Dqk == 128) or Dqk == 192:
-        total += _a256(B * Hq * n_kt * n_qt * 16384) + _a256(16384)
+    if rt != "reduce":
+        total += _a256(B * Hq * band_tiles(Sq, Skv, causal, br, wl, wr, padded) * 16384) + _a256(16384)
     else:
         total += _a256(B * Hq * n_qt * 64 * (64 if Dqk <= 64 else 128) * 4)
     total += _a256((B * Hq * n_qt + 1) * 4)
@@ -72,21 +106,69 @@ def expected_workspace(B, Hq, Hkv, Sq, Skv, Dqk, Dv, det=0):
     return total
 
 
-@pytest.mark.parametrize("shape", [(1, 2, 2, 128, 128, 64, 64), (2, 16, 16, 2048, 2048, 128, 128),
-                                   (1, 32, 8, 4096, 4096, 128, 128), (3, 4, 1, 300, 177, 128, 128),
-                                   (1, 1, 1, 1, 1, 64, 64), (1, 16, 16, 4096, 4096, 192, 128),
-                                   (2, 4, 2, 300, 177, 192, 128), (2, 4, 2, 300, 177, 32, 32),
-                                   (1, 3, 1, 200, 130, 96, 96), (2, 2, 2, 65, 70, 8, 8)])
+def expected_workspace(B, Hq, Hkv, Sq, Skv, Dqk, Dv, det=0, causal=0, br=0, wl=-1, wr=-1, padded=0):
+    return carve_size(B, Hq, Hkv, Sq, Skv, Dqk, Dv, route(det, Dqk), causal=causal, br=br, wl=wl,
+                      wr=wr, padded=padded)
+
+
+def ws(lib, B, Hq, Hkv, Sq, Skv, Dqk, Dv, det=0, causal=0, br=0, wl=-1, wr=-1, padded=0):
+    return lib.sdpa_bwd_workspace_size(B, Hq, Hkv, Sq, Skv, Dqk, Dv, causal, br, wl, wr, det, padded)
+
+
+SHAPES = [(1, 2, 2, 128, 128, 64, 64), (2, 16, 16, 2048, 2048, 128, 128),
+          (1, 32, 8, 4096, 4096, 128, 128), (3, 4, 1, 300, 177, 128, 128),
+          (1, 1, 1, 1, 1, 64, 64), (1, 16, 16, 4096, 4096, 192, 128),
+          (2, 4, 2, 300, 177, 192, 128), (2, 4, 2, 300, 177, 32, 32),
+          (1, 3, 1, 200, 130, 96, 96), (2, 2, 2, 65, 70, 8, 8)]
+MASKS = [dict(), dict(causal=1), dict(causal=1, br=1), dict(causal=1, wl=1024),
+         dict(causal=1, wr=100, wl=50), dict(wl=70), dict(causal=1, padded=1),
+         dict(causal=1, br=1, padded=1)]
+
+
+@pytest.mark.parametrize("shape", SHAPES)
 def test_workspace_size_matches_layout(lib, shape):
     for det in (0, 1):
-        assert lib.sdpa_bwd_workspace_size(*shape, det) == expected_workspace(*shape, det=det)
+        for m in MASKS:
+            assert ws(lib, *shape, det=det, **m) == expected_workspace(*shape, det=det, **m), (det, m)
+
+
+def test_workspace_band_halves_causal_and_shrinks_windows(lib):
+    # causal: about half of the rectangle of dS tiles; a 1024-key window far less
+    full = ws(lib, 1, 32, 32, 4096, 4096, 128, 128, det=1)
+    causal = ws(lib, 1, 32, 32, 4096, 4096, 128, 128, det=1, causal=1)
+    assert 0.5 < causal / full < 0.53
+    assert ws(lib, 4, 16, 16, 4096, 4096, 128, 128, det=1, causal=1, wl=1024, padded=1) < \
+        0.3 * ws(lib, 4, 16, 16, 4096, 4096, 128, 128, det=1, padded=1)
+    # a bottom-right mask with per-batch lengths keeps the whole rectangle
+    assert ws(lib, 1, 2, 2, 512, 512, 128, 128, det=1, causal=1, br=1, padded=1) == \
+        ws(lib, 1, 2, 2, 512, 512, 128, 128, det=1)
+
+
+def test_band_model_against_brute_force():
+    """The band restated above against a brute-force scan of (query, key) pairs."""
+    for (Sq, Skv, causal, br, wl, wr) in [(300, 177, 1, 0, -1, -1), (177, 300, 1, 1, -1, -1),
+                                           (500, 500, 1, 0, 100, -1), (260, 380, 1, 1, 90, 30),
+                                           (200, 200, 0, 0, 33, -1)]:
+        diag = Skv - Sq if br else 0
+        for kt in range(-(-Skv // 128)):
+            tiles = set()
+            for q in range(Sq):
+                for k in range(kt * 128, min(kt * 128 + 128, Skv)):
+                    ok = (not causal or k <= q + diag + max(wr, 0)) and (wl < 0 or k >= q + diag - wl)
+                    if ok:
+                        tiles.add(q // 64)
+            lo, hi = visited_query_tiles(kt, Sq, Skv, causal, br, wl, wr)
+            if tiles:
+                assert (lo, hi) == (min(tiles), max(tiles))
+            else:
+                assert hi < lo
 
 
 def test_workspace_size_rejects(lib):
-    assert lib.sdpa_bwd_workspace_size(1, 3, 2, 128, 128, 128, 128, 0) == 0  # Hkv does not divide
-    assert lib.sdpa_bwd_workspace_size(1, 2, 2, 128, 128, 100, 100, 0) == 0  # head dim not served
-    assert lib.sdpa_bwd_workspace_size(0, 2, 2, 128, 128, 128, 128, 0) == 0
-    assert lib.sdpa_bwd_workspace_size(1, 2, 2, 0, 128, 128, 128, 0) == 0    # nothing to stage
+    assert ws(lib, 1, 3, 2, 128, 128, 128, 128) == 0  # Hkv does not divide
+    assert ws(lib, 1, 2, 2, 128, 128, 100, 100) == 0  # head dim not served
+    assert ws(lib, 0, 2, 2, 128, 128, 128, 128) == 0
+    assert ws(lib, 1, 2, 2, 0, 128, 128, 128) == 0    # nothing to stage
 
 
 FAKE = 0x10000  # never dereferenced: every call below fails validation first
@@ -281,9 +363,9 @@ def test_nvfp4_qat_argument_validation(lib):
     assert fq(ctypes.c_void_p(FAKE + 8), ctypes.c_void_p(FAKE), ctypes.c_longlong(16), None) == ALIGN
     assert fq(ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), ctypes.c_longlong(0), None) == OK
     # workspace: the plain chain's regions plus bf16 copies of Q, K and V
-    ws = lib.sdpa_bwd_nvfp4_qat_workspace_size(1, 2, 2, 128, 128, 128, 128)
-    base = lib.sdpa_bwd_workspace_size(1, 2, 2, 128, 128, 128, 128, 0)
-    assert ws == base + 3 * 2 * 128 * 128 * 2
+    qws = lib.sdpa_bwd_nvfp4_qat_workspace_size(1, 2, 2, 128, 128, 128, 128)
+    base = ws(lib, 1, 2, 2, 128, 128, 128, 128)
+    assert qws == base + 3 * 2 * 128 * 128 * 2
     assert lib.sdpa_bwd_nvfp4_qat_workspace_size(1, 2, 2, 128, 128, 64, 64) == 0
 
 

@@ -49,29 +49,31 @@ def _call_noalloc(lib, w, d, outs):
                                 stream)
 
 
-# In call order. The first fills most of the array with accumulator values, so
-# every later call starts from another call's leftovers.
+# In call order. The first fills half the array, so every later call starts
+# from another call's leftovers.
 CASES = [
     # reduction route (fp32 dQ accumulator), GQA with a sliding window
     W("noalloc_gqa", 1, 8, 2, 1000, 1000, 128, 128, causal=True, window_left=300, seed=31),
     # ordered relay (D 64, deterministic): turn counters and the accumulator
     W("noalloc_padded", 2, 2, 2, 300, 300, 64, 64, causal=True, bottom_right=True,
       padded=(100, 300), deterministic=True, seed=32),
-    # two-kernel route (D 128, deterministic): stored dS tiles, the zero tile,
-    # GQA partial sets
+    # two-kernel route (D 128, deterministic): the band of stored dS tiles, the
+    # zero tile, GQA partial sets
     W("noalloc_det128", 1, 4, 2, 320, 320, 128, 128, causal=True, deterministic=True, seed=33),
-    # two-kernel route at D_qk 192 / D_v 128 (non-deterministic)
-    W("noalloc_mla", 1, 2, 2, 260, 260, 192, 128, causal=True, bottom_right=True, seed=34),
-    # the reduction route once more, after the dS calls
-    W("noalloc_dense", 1, 2, 1, 200, 330, 128, 128, seed=35),
+    # two-kernel route at D_qk 192 / D_v 128: stored dS tiles, GQA partial sets
+    W("noalloc_mla", 1, 4, 2, 260, 260, 192, 128, causal=True, bottom_right=True, seed=34),
+    # the reduction route once more (D 64), after the dS calls
+    W("noalloc_dense", 1, 2, 1, 200, 330, 64, 64, seed=35),
 ]
 
 
 def test_noalloc_matches_oracle_and_sdpa_bwd_on_calls_in_a_row():
     lib, pkg = _lib()
     for w in CASES:
-        assert pkg.workspace_size(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.Dqk, w.Dv, w.deterministic) \
-            <= LIMIT_BYTES
+        assert pkg.workspace_size(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.Dqk, w.Dv, w.deterministic,
+                                  causal=w.causal, bottom_right=w.bottom_right,
+                                  window_left=w.window_left, window_right=w.window_right,
+                                  padded=w.padded is not None) <= LIMIT_BYTES
     cases = [make_case(w) for w in CASES]
     devs = [to_device(c) for c in cases]
     for rep in range(2):  # the whole series twice: every call follows another
