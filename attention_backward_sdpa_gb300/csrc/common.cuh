@@ -198,7 +198,8 @@ struct MainMaps {
 // Host launchers, one per kernel, defined beside their kernels. `pdl` launches
 // with programmatic stream serialization (the kernel waits on its predecessor
 // with griddepcontrol.wait before touching dependent data).
-cudaError_t launch_preprocess(const ChainParams& p, cudaStream_t s);
+cudaError_t launch_preprocess(const ChainParams& p, cudaStream_t s, int num_sms);
+cudaError_t preprocess_kernel_setup();  // per device: opt in to the preprocess's shared memory
 cudaError_t launch_main(const MainMaps& maps, const ChainParams& p, cudaStream_t s);
 cudaError_t launch_dq_convert(const ChainParams& p, cudaStream_t s);
 cudaError_t launch_dsink(const ChainParams& p, cudaStream_t s);

@@ -174,6 +174,7 @@ int device_state(int dev, int** status_out, int* sms_out) {
       if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return SDPA_ERR_CUDA;
       g_status_ptr[dev] = static_cast<int*>(p);
       if (main_kernel_setup() != cudaSuccess || main_ds_kernel_setup() != cudaSuccess ||
+          preprocess_kernel_setup() != cudaSuccess ||
           dq_kernel_setup() != cudaSuccess || fwd_kernel_setup() != cudaSuccess)
         return SDPA_ERR_CUDA;
     }
@@ -519,7 +520,7 @@ int run_chain(const void* q, const void* k, const void* v, const void* o, const 
     if (e == cudaSuccess) e = launch_nvfp4_fake_quant(k, ws + cv.k_hat, BHkv * S_kv * D_qk / 16, sms, stream);
     if (e == cudaSuccess) e = launch_nvfp4_fake_quant(v, ws + cv.v_hat, BHkv * S_kv * D_v / 16, sms, stream);
   }
-  if (e == cudaSuccess) e = launch_preprocess(p, stream);
+  if (e == cudaSuccess) e = launch_preprocess(p, stream, sms);
   prof.end(0);
   if (e == cudaSuccess) {
     prof.begin(1);

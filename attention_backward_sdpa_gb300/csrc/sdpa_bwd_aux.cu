@@ -44,21 +44,38 @@ __device__ void zero_shared_dbias_rows(const ChainParams& p, unsigned bh, int qt
 }
 
 // ---------------------------------------------------------------- preprocess
-// One 64-row query tile per CTA pass: TPR = DV/8 lanes per row (8 bf16 each),
-// 256 / TPR rows per pass, all loads of a tile issued before any reduction.
-// Index arithmetic is done once per tile in 32 bits (the host rejects tensors
-// of 2^31 elements or more).
-// TPR lanes share a row: D_v/8 of them load 8 values each (the rest, when D_v
-// is not a power-of-two multiple of 8, load nothing).
+// Persistent and TMA-staged: a CTA walks the 64-row query tiles t = blockIdx.x,
+// + gridDim.x, ... with PRE_STAGES tiles in flight. One thread issues each
+// tile's O and dO rows (the rows below the query length: contiguous, 16-byte
+// multiples) as two bulk copies into a shared-memory stage ring, and clears
+// the tile's dQ accumulator rows with bulk stores from a zeroed buffer; all
+// threads reduce the rows from shared memory. Two CTAs per SM keep about
+// 192 KB of loads in flight per SM (one short CTA per tile, reading into
+// registers, left half the HBM bandwidth idle).
+// TPR = DV/8 lanes per row (8 io elements each), 256 / TPR rows per pass;
+// lanes past D_v/8 (D_v not a power-of-two multiple of 8) read nothing.
+constexpr int PRE_THREADS = 256;
+constexpr int PRE_STAGES = 3;
+constexpr int PRE_TILE = BQ * 128 * 2;               // one 64-row io tile at D_v <= 128
+constexpr int PRE_ZERO = 16384;                      // zero source of the accumulator clear
+constexpr int PRE_OFF_O = 0;
+constexpr int PRE_OFF_DO = PRE_OFF_O + PRE_STAGES * PRE_TILE;
+constexpr int PRE_OFF_ZERO = PRE_OFF_DO + PRE_STAGES * PRE_TILE;
+constexpr int PRE_OFF_BAR = PRE_OFF_ZERO + PRE_ZERO;
+constexpr int PRE_BYTES = PRE_OFF_BAR + PRE_STAGES * 8;
+
 template <int TPR, bool F16>
-__global__ void __launch_bounds__(256) sdpa_bwd_preprocess(const ChainParams p) {
+__global__ void __launch_bounds__(PRE_THREADS, 2) sdpa_bwd_preprocess(const ChainParams p) {
   // The main kernel may start its prologue (barrier setup, TMEM allocation,
   // K/V loads) while this grid runs; it waits for completion before reading
   // anything written here.
   pdl_launch_dependents();
 
-  const int DV = p.Dv;                     // row width of O and dO
-  constexpr int RPP = 256 / TPR;           // rows per pass
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + PRE_OFF_BAR);
+  const uint8_t* zero = smem + PRE_OFF_ZERO;
+  const int DV = p.Dv;
+  constexpr int RPP = PRE_THREADS / TPR;   // rows per pass
   constexpr int PASSES = BQ / RPP;         // passes per 64-row tile
   constexpr float LOG2E = 1.4426950408889634f;
   const int lane = threadIdx.x & 31;
@@ -67,40 +84,89 @@ __global__ void __launch_bounds__(256) sdpa_bwd_preprocess(const ChainParams p) 
   const int rsub = threadIdx.x / TPR;
   const unsigned n_tiles = (unsigned)p.B * p.Hq * p.n_qt;
   __shared__ float sink_terms[BQ];  // per-row sink terms of the current tile
+  __shared__ int abort_flag;         // a stage wait that ran out (then results are invalid)
 
-  for (unsigned t = blockIdx.x; t < n_tiles; t += gridDim.x) {
-    const unsigned bh = t / (unsigned)p.n_qt;
-    const int qt = (int)(t - bh * (unsigned)p.n_qt);
-    int Lq, Lk;
+  for (int i = threadIdx.x; i < PRE_ZERO / 16; i += PRE_THREADS)
+    reinterpret_cast<uint4*>(smem + PRE_OFF_ZERO)[i] = make_uint4(0u, 0u, 0u, 0u);
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int st = 0; st < PRE_STAGES; ++st) mbar_init(&full[st], 1);
+    fence_mbar_init();
+  }
+  fence_proxy_async_smem();  // the zeros are read by bulk stores
+  __syncthreads();
+
+  // Query rows of tile t below the length, i.e. the rows the bulk copies fill.
+  auto live_rows = [&](unsigned t, unsigned& bh, int& qt, int& Lq) {
+    bh = t / (unsigned)p.n_qt;
+    qt = (int)(t - bh * (unsigned)p.n_qt);
+    int Lk;
     batch_lengths(p, (int)(bh / (unsigned)p.Hq), Lq, Lk);
-    const __nv_bfloat16* o_base = p.o + (long long)bh * p.Sq * DV + sub * 8;
-    const __nv_bfloat16* do_base = p.d_o + (long long)bh * p.Sq * DV + sub * 8;
-    uint4 vo[PASSES], vd[PASSES];
-    float lv[PASSES];  // the rows' LSE, loaded with O and dO rather than after the sums
+    return max(0, min(BQ, Lq - qt * BQ));
+  };
+  // Thread 0: the loads of this CTA's k-th tile into stage k % PRE_STAGES.
+  auto issue = [&](unsigned k) {
+    const unsigned t = blockIdx.x + k * gridDim.x;
+    if (t >= n_tiles) return;
+    unsigned bh;
+    int qt, Lq;
+    const int rows = live_rows(t, bh, qt, Lq);
+    uint64_t* bar = &full[k % PRE_STAGES];
+    if (rows == 0) {
+      mbar_arrive(bar);
+      return;
+    }
+    const uint32_t bytes = (uint32_t)rows * DV * 2;
+    const long long row0 = (long long)bh * p.Sq + (long long)qt * BQ;
+    mbar_arrive_expect_tx(bar, 2 * bytes);
+    bulk_load(smem + PRE_OFF_O + (k % PRE_STAGES) * PRE_TILE, p.o + row0 * DV, bytes, bar);
+    bulk_load(smem + PRE_OFF_DO + (k % PRE_STAGES) * PRE_TILE, p.d_o + row0 * DV, bytes, bar);
+  };
+  if (threadIdx.x == 0)
+    for (unsigned k = 0; k < PRE_STAGES; ++k) issue(k);
+
+  unsigned k = 0;
+  for (unsigned t = blockIdx.x; t < n_tiles; t += gridDim.x, ++k) {
+    unsigned bh;
+    int qt, Lq;
+    const int rows = live_rows(t, bh, qt, Lq);
+    // dQ-reduction route: clear this tile's accumulator rows below Lq (the
+    // convert kernel writes zeros for rows at or past Lq without reading them).
+    if (threadIdx.x == 0 && p.dq_accum && rows > 0) {
+      uint8_t* acc = reinterpret_cast<uint8_t*>(p.dq_accum + ((long long)bh * p.n_qt + qt) * BQ * p.dq_acc_cols);
+      const uint32_t total = (uint32_t)rows * p.dq_acc_cols * 4;
+      for (uint32_t off = 0; off < total; off += PRE_ZERO)
+        bulk_store(acc + off, zero, total - off < (uint32_t)PRE_ZERO ? total - off : (uint32_t)PRE_ZERO);
+      bulk_commit_group();
+    }
+    if (p.dbias_red) zero_shared_dbias_rows(p, bh, qt);
+    float lv[PASSES];  // the rows' LSE, requested before the wait for the stage
 #pragma unroll
     for (int u = 0; u < PASSES; ++u) {
       const int q = qt * BQ + u * RPP + rsub;
-      if (q < Lq && sub * 8 < DV) {
-        vo[u] = *reinterpret_cast<const uint4*>(o_base + (long long)q * DV);
-        vd[u] = *reinterpret_cast<const uint4*>(do_base + (long long)q * DV);
-      } else {
-        vo[u] = make_uint4(0, 0, 0, 0);
-        vd[u] = make_uint4(0, 0, 0, 0);
-      }
       lv[u] = (q < Lq && sub == 0) ? p.lse[(long long)bh * p.Sq + q] : 0.f;
     }
+    const int st = (int)(k % PRE_STAGES);
+    if (!mbar_wait(&full[st], (k / PRE_STAGES) & 1, &abort_flag, 4000000000ull)) {
+      atomicOr(p.status, STATUS_TIMEOUT);
+      break;  // every thread leaves (the flag is shared); nothing waits on this kernel's threads
+    }
+    const uint8_t* so = smem + PRE_OFF_O + st * PRE_TILE;
+    const uint8_t* sd = smem + PRE_OFF_DO + st * PRE_TILE;
     float* qs = p.qstat + (long long)t * QSTAT_FLOATS;
     const float sink2 = p.dsink_part ? p.sink[bh % (unsigned)p.Hq] * LOG2E : 0.f;
 #pragma unroll
     for (int u = 0; u < PASSES; ++u) {
       const int qi = u * RPP + rsub;
       const int q = qt * BQ + qi;
-      float fo[8], fd[8];
-      unpack8<F16>(vo[u], fo);
-      unpack8<F16>(vd[u], fd);
       float dot = 0.f;
+      if (qi < rows && sub * 8 < DV) {
+        float fo[8], fd[8];
+        unpack8<F16>(*reinterpret_cast<const uint4*>(so + (qi * DV + sub * 8) * 2), fo);
+        unpack8<F16>(*reinterpret_cast<const uint4*>(sd + (qi * DV + sub * 8) * 2), fd);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) dot = fmaf(fo[i], fd[i], dot);
+        for (int i = 0; i < 8; ++i) dot = fmaf(fo[i], fd[i], dot);
+      }
 #pragma unroll
       for (int sft = TPR / 2; sft > 0; sft >>= 1) dot += __shfl_xor_sync(group_mask, dot, sft, TPR);
       if (sub == 0) {
@@ -117,29 +183,22 @@ __global__ void __launch_bounds__(256) sdpa_bwd_preprocess(const ChainParams p) 
         if (p.dsink_part) sink_terms[qi] = exp2f(sink2 - lse2) * delta;
       }
     }
-    if (p.dsink_part) {
-      // The tile's 64 terms in ascending row order, by one thread: bitwise
-      // reproducible, and so is the fixed-order sum of the tiles (dsink kernel).
-      __syncthreads();
-      if (threadIdx.x == 0) {
+    // Every thread has read the stage (and the sink terms are written): the
+    // stage takes the tile PRE_STAGES ahead.
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      if (p.dsink_part) {
+        // The tile's 64 terms in ascending row order, by one thread: bitwise
+        // reproducible, and so is the fixed-order sum of the tiles (dsink kernel).
         float acc = 0.f;
         for (int i = 0; i < BQ; ++i) acc += sink_terms[i];
         p.dsink_part[t] = acc;
       }
-      __syncthreads();
+      issue(k + PRE_STAGES);
     }
-    if (p.dbias_red) zero_shared_dbias_rows(p, bh, qt);
-    // dQ-reduction route: clear this tile's accumulator rows below Lq (the
-    // convert kernel writes zeros for rows at or past Lq without reading them).
-    if (p.dq_accum) {
-      const int rows = min(BQ, Lq - qt * BQ);
-      if (rows > 0) {
-        float4* acc = reinterpret_cast<float4*>(p.dq_accum + ((long long)bh * p.n_qt + qt) * BQ * p.dq_acc_cols);
-        const int n4 = rows * p.dq_acc_cols / 4;
-        for (int i = threadIdx.x; i < n4; i += blockDim.x) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    }
+    if (p.dsink_part) __syncthreads();  // sink_terms is rewritten by the next tile
   }
+  if (threadIdx.x == 0) bulk_wait_group_read0();  // the zero buffer outlives its readers
 
   // Clear the stand-in zero dS tile (two-kernel route) and the counters (+ ticket).
   const long long nthreads = (long long)gridDim.x * blockDim.x;
@@ -247,18 +306,41 @@ cudaError_t launch_dsink(const ChainParams& p, cudaStream_t s) {
   return launch_kernel(sdpa_bwd_dsink, dim3((unsigned)p.Hq), dim3(DSINK_THREADS), 0, s, false, p);
 }
 
-// Both kernels take one 64-row query tile per CTA and leave the balancing of
+// The convert takes one 64-row query tile per CTA and leaves the balancing of
 // the tiles to the hardware dispatcher.
-template <bool F16>
-static cudaError_t launch_preprocess_io(const ChainParams& p, cudaStream_t s) {
-  const dim3 grid((unsigned)(p.B * p.Hq * p.n_qt));
-  if (p.Dv <= 32) return launch_kernel(sdpa_bwd_preprocess<4, F16>, grid, dim3(256), 0, s, false, p);
-  if (p.Dv <= 64) return launch_kernel(sdpa_bwd_preprocess<8, F16>, grid, dim3(256), 0, s, false, p);
-  return launch_kernel(sdpa_bwd_preprocess<16, F16>, grid, dim3(256), 0, s, false, p);
+// Persistent: two CTAs per SM (fewer when there are fewer tiles).
+template <int TPR, bool F16>
+static cudaError_t launch_preprocess_tpr(const ChainParams& p, cudaStream_t s, int num_sms) {
+  const long long tiles = (long long)p.B * p.Hq * p.n_qt;
+  const long long cap = 2ll * num_sms;
+  const dim3 grid((unsigned)(tiles < cap ? tiles : cap));
+  return launch_kernel(sdpa_bwd_preprocess<TPR, F16>, grid, dim3(PRE_THREADS), PRE_BYTES, s, false, p);
 }
 
-cudaError_t launch_preprocess(const ChainParams& p, cudaStream_t s) {
-  return p.f16 ? launch_preprocess_io<true>(p, s) : launch_preprocess_io<false>(p, s);
+template <bool F16>
+static cudaError_t launch_preprocess_io(const ChainParams& p, cudaStream_t s, int num_sms) {
+  if (p.Dv <= 32) return launch_preprocess_tpr<4, F16>(p, s, num_sms);
+  if (p.Dv <= 64) return launch_preprocess_tpr<8, F16>(p, s, num_sms);
+  return launch_preprocess_tpr<16, F16>(p, s, num_sms);
+}
+
+template <int TPR, bool F16>
+static cudaError_t set_pre_smem() {
+  return cudaFuncSetAttribute(sdpa_bwd_preprocess<TPR, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, PRE_BYTES);
+}
+
+cudaError_t preprocess_kernel_setup() {
+  cudaError_t e = set_pre_smem<4, false>();
+  if (e == cudaSuccess) e = set_pre_smem<8, false>();
+  if (e == cudaSuccess) e = set_pre_smem<16, false>();
+  if (e == cudaSuccess) e = set_pre_smem<4, true>();
+  if (e == cudaSuccess) e = set_pre_smem<8, true>();
+  if (e == cudaSuccess) e = set_pre_smem<16, true>();
+  return e;
+}
+
+cudaError_t launch_preprocess(const ChainParams& p, cudaStream_t s, int num_sms) {
+  return p.f16 ? launch_preprocess_io<true>(p, s, num_sms) : launch_preprocess_io<false>(p, s, num_sms);
 }
 
 template <bool F16>
