@@ -26,7 +26,7 @@ __all__ = ["sdpa_bwd", "sdpa_fwd", "workspace_size", "nvfp4_fake_quant", "sdpa_f
 KERNEL_NAMES = ("preprocess", "main", "dq")
 
 _STATUS = {0: "SDPA_OK", 1: "SDPA_ERR_INVALID", 2: "SDPA_ERR_UNSUPPORTED", 3: "SDPA_ERR_ALIGN",
-           4: "SDPA_ERR_WORKSPACE", 5: "SDPA_ERR_CUDA", 6: "SDPA_ERR_TIMEOUT"}
+           4: "SDPA_ERR_WORKSPACE", 5: "SDPA_ERR_CUDA", 6: "SDPA_ERR_TIMEOUT", 7: "SDPA_ERR_BOUNDS"}
 
 
 class SdpaError(RuntimeError):
@@ -39,7 +39,10 @@ _lib = None
 
 
 def library_path() -> str:
-    return _build.LIB
+    """The library this process loads: libsdpa_bwd.so, or the build named by the
+    SDPA_BWD_LIBRARY environment variable (for example the debug-bounds build,
+    libsdpa_bwd_debug.so, whose kernels check their global accesses)."""
+    return os.environ.get("SDPA_BWD_LIBRARY") or _build.LIB
 
 
 def load(build_if_missing: bool = False):

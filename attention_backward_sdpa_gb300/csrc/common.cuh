@@ -24,6 +24,7 @@ constexpr int QSTAT_FLOATS = 2 * BQ;
 // Device status bits (OR-ed into the per-device status word).
 constexpr int STATUS_TIMEOUT = 1;
 constexpr int STATUS_SMEM_ALIGN = 2;
+constexpr int STATUS_BOUNDS = 4;  // debug-bounds build: an access outside its region was skipped
 
 struct ChainParams {
   int B, Hq, Hkv, Sq, Skv, Dqk, Dv;
@@ -131,6 +132,39 @@ __host__ __device__ inline void visited_query_tiles(int kt, int Lq, int Lk, int 
   qt_hi = (int)(q_max / BQ);
 }
 
+// Debug-bounds build (compiled with -DSDPA_DEBUG_BOUNDS): the kernels check
+// every raw-pointer global access (bulk copies, reductions, counters, direct
+// stores) against the region it belongs to; an access outside it sets
+// STATUS_BOUNDS in the status word and is skipped, with no trap. In the normal
+// build the check is the constant true and compiles away.
+__device__ __forceinline__ bool in_bounds(int* status, const void* ptr, size_t bytes, const void* base,
+                                          size_t extent) {
+#ifdef SDPA_DEBUG_BOUNDS
+  const uintptr_t a = reinterpret_cast<uintptr_t>(ptr), b0 = reinterpret_cast<uintptr_t>(base);
+  if (base == nullptr || a < b0 || a + bytes > b0 + extent) {
+    atomicOr(status, STATUS_BOUNDS);
+    return false;
+  }
+#else
+  (void)status; (void)ptr; (void)bytes; (void)base; (void)extent;
+#endif
+  return true;
+}
+
+// Region sizes in bytes, from the parameters (for the debug-bounds checks).
+__host__ __device__ inline size_t qstat_bytes(const ChainParams& p) {
+  return (size_t)p.B * p.Hq * p.n_qt * QSTAT_FLOATS * sizeof(float);
+}
+__host__ __device__ inline size_t dq_accum_bytes(const ChainParams& p) {
+  return (size_t)p.B * p.Hq * p.n_qt * BQ * p.dq_acc_cols * sizeof(float);
+}
+__host__ __device__ inline size_t io_q_bytes(const ChainParams& p, int D) {  // (B, H_q, S_q, D) io tensor
+  return (size_t)p.B * p.Hq * p.Sq * D * 2;
+}
+__host__ __device__ inline size_t kv_out_bytes(const ChainParams& p, int D, bool partials) {  // dK / dV (or partial sets)
+  return (size_t)p.B * (partials ? p.Hq : p.Hkv) * p.Skv * D * 2;
+}
+
 // Band of query tiles [lo, hi] of key tile kt in the dS workspace (see ChainParams).
 __host__ __device__ inline void ds_band_range(const ChainParams& p, int kt, int& lo, int& hi) {
   if (!p.ds_band) {
@@ -151,6 +185,10 @@ __host__ __device__ inline long long ds_band_prefix(const ChainParams& p, int kt
     if (hi >= lo) s += hi - lo + 1;
   }
   return s;
+}
+
+__host__ __device__ inline size_t ds_ws_bytes(const ChainParams& p) {
+  return (size_t)p.B * p.Hq * p.ds_band_tiles * DS_TILE_BYTES;
 }
 
 // Address of the stored dS^T tile (bh, kt, qt); `prefix` = ds_band_prefix(p, kt)
@@ -311,6 +349,11 @@ __device__ inline void zero_group_share_of_empty_key_tiles(const ChainParams& p,
       const int rows = min(BN, p.Skv - k0);
       uint4* dk = reinterpret_cast<uint4*>((p.dk_ws ? p.dk_ws : p.dk) + (head * p.Skv + k0) * p.Dqk);
       uint4* dv = reinterpret_cast<uint4*>((p.dv_ws ? p.dv_ws : p.dv) + (head * p.Skv + k0) * p.Dv);
+      if (!in_bounds(p.status, dk, (size_t)rows * p.Dqk * 2, p.dk_ws ? p.dk_ws : p.dk,
+                     kv_out_bytes(p, p.Dqk, p.dk_ws != nullptr)) ||
+          !in_bounds(p.status, dv, (size_t)rows * p.Dv * 2, p.dv_ws ? p.dv_ws : p.dv,
+                     kv_out_bytes(p, p.Dv, p.dv_ws != nullptr)))
+        continue;
       for (int i = lane; i < rows * (p.Dqk / 8); i += 32) dk[i] = z;
       for (int i = lane; i < rows * (p.Dv / 8); i += 32) dv[i] = z;
     }
@@ -322,6 +365,11 @@ __device__ inline void zero_key_tile_rows(const ChainParams& p, long long head, 
   const uint4 z = make_uint4(0u, 0u, 0u, 0u);
   uint4* dk = reinterpret_cast<uint4*>((p.dk_ws ? p.dk_ws : p.dk) + (head * p.Skv + k0) * p.Dqk);
   uint4* dv = reinterpret_cast<uint4*>((p.dv_ws ? p.dv_ws : p.dv) + (head * p.Skv + k0) * p.Dv);
+  if (!in_bounds(p.status, dk, (size_t)rows * p.Dqk * 2, p.dk_ws ? p.dk_ws : p.dk,
+                 kv_out_bytes(p, p.Dqk, p.dk_ws != nullptr)) ||
+      !in_bounds(p.status, dv, (size_t)rows * p.Dv * 2, p.dv_ws ? p.dv_ws : p.dv,
+                 kv_out_bytes(p, p.Dv, p.dv_ws != nullptr)))
+    return;
   for (int i = threadIdx.x; i < rows * (p.Dqk / 8); i += blockDim.x) dk[i] = z;
   for (int i = threadIdx.x; i < rows * (p.Dv / 8); i += blockDim.x) dv[i] = z;
 }

@@ -53,6 +53,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Counts `bytes` of expected transactions as arrived without a copy: keeps a
+// barrier's phase consistent when a debug-bounds check skips a bulk load.
+__device__ __forceinline__ void mbar_complete_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
 // Waits for the phase with the given parity to complete. Bounded: gives up
 // (returns false) once *abort is set by another thread or after `limit_ns`
 // nanoseconds, setting *abort itself in the latter case.

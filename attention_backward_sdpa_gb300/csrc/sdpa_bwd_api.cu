@@ -11,6 +11,7 @@
 // predecessor's completion (griddepcontrol.wait) before touching its outputs.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <cmath>
 #include <cstdint>
@@ -197,15 +198,21 @@ bool make_bhsd_map(CUtensorMap* m, const void* base, int D, int S, long long BH,
                    dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// Records one event pair per launch while profiling is on; the pairs are
-// resolved once at the end of the call, so no synchronization sits between
-// launches (a busy stream keeps host launch latency out of the intervals).
+// NVTX range names of the chain's launches (seen by profilers and tracers;
+// a no-op without one attached).
+const char* const kRangeNames[3] = {"sdpa_bwd.preprocess", "sdpa_bwd.main", "sdpa_bwd.dq"};
+
+// Opens an NVTX range around each launch and, while profiling is on, records
+// one event pair per launch; the pairs are resolved once at the end of the
+// call, so no synchronization sits between launches (a busy stream keeps host
+// launch latency out of the intervals).
 struct ProfEvents {
   cudaEvent_t ev[3][2] = {};
   bool used[3] = {};
   cudaStream_t s;
   explicit ProfEvents(cudaStream_t s_) : s(s_) {}
   void begin(int slot) {
+    nvtxRangePushA(kRangeNames[slot]);
     if (!g_profile) return;
     cudaEventCreate(&ev[slot][0]);
     cudaEventCreate(&ev[slot][1]);
@@ -214,6 +221,7 @@ struct ProfEvents {
   }
   void end(int slot) {
     if (g_profile && used[slot]) cudaEventRecord(ev[slot][1], s);
+    nvtxRangePop();
   }
   ~ProfEvents() {
     for (int i = 0; i < 3; ++i) {
@@ -249,6 +257,7 @@ const char* sdpa_status_string(int status) {
     case SDPA_ERR_WORKSPACE: return "workspace too small";
     case SDPA_ERR_CUDA: return "CUDA runtime error";
     case SDPA_ERR_TIMEOUT: return "device-side wait timed out";
+    case SDPA_ERR_BOUNDS: return "debug-bounds build: an out-of-range access was skipped";
     default: return "unknown status";
   }
 }
@@ -310,7 +319,7 @@ int sdpa_bwd_check_device_status(void* stream) {
   if (v != 0) {
     const int zero = 0;
     cudaMemcpy(status, &zero, sizeof(int), cudaMemcpyHostToDevice);
-    return SDPA_ERR_TIMEOUT;
+    return (v & STATUS_BOUNDS) ? SDPA_ERR_BOUNDS : SDPA_ERR_TIMEOUT;
   }
   return SDPA_OK;
 }
@@ -533,7 +542,11 @@ int run_chain(const void* q, const void* k, const void* v, const void* o, const 
     e = ds_route ? launch_dq_from_ds(maps.k, p, stream, sms) : launch_dq_convert(p, stream);
     prof.end(2);
   }
-  if (e == cudaSuccess && dsink) e = launch_dsink(p, stream);
+  if (e == cudaSuccess && dsink) {
+    nvtxRangePushA("sdpa_bwd.dsink");
+    e = launch_dsink(p, stream);
+    nvtxRangePop();
+  }
   if (dbias_tmp) {
     if (e == cudaSuccess)
       e = launch_dbias_cast(dbias_tmp, ba.dbias, (long long)H_q * S_q * S_kv,
@@ -627,7 +640,10 @@ int run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
       !make_bhsd_map(&maps.v, vb, D_v, Skv_map, S_kv > 0 ? BHkv : BHq, 128, f16) ||
       !make_bhsd_map(&maps.o, o, D_v, S_q, BHq, 128, f16))
     return SDPA_ERR_CUDA;
-  return launch_fwd(maps, p, stream) == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+  nvtxRangePushA("sdpa_fwd");
+  const cudaError_t e = launch_fwd(maps, p, stream);
+  nvtxRangePop();
+  return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }
 
 }  // namespace

@@ -119,8 +119,13 @@ __global__ void __launch_bounds__(PRE_THREADS, 2) sdpa_bwd_preprocess(const Chai
     const uint32_t bytes = (uint32_t)rows * DV * 2;
     const long long row0 = (long long)bh * p.Sq + (long long)qt * BQ;
     mbar_arrive_expect_tx(bar, 2 * bytes);
-    bulk_load(smem + PRE_OFF_O + (k % PRE_STAGES) * PRE_TILE, p.o + row0 * DV, bytes, bar);
-    bulk_load(smem + PRE_OFF_DO + (k % PRE_STAGES) * PRE_TILE, p.d_o + row0 * DV, bytes, bar);
+    if (in_bounds(p.status, p.o + row0 * DV, bytes, p.o, io_q_bytes(p, DV)) &&
+        in_bounds(p.status, p.d_o + row0 * DV, bytes, p.d_o, io_q_bytes(p, DV)) && bytes <= PRE_TILE) {
+      bulk_load(smem + PRE_OFF_O + (k % PRE_STAGES) * PRE_TILE, p.o + row0 * DV, bytes, bar);
+      bulk_load(smem + PRE_OFF_DO + (k % PRE_STAGES) * PRE_TILE, p.d_o + row0 * DV, bytes, bar);
+    } else {
+      mbar_complete_tx(bar, 2 * bytes);
+    }
   };
   if (threadIdx.x == 0)
     for (unsigned k = 0; k < PRE_STAGES; ++k) issue(k);
@@ -135,8 +140,9 @@ __global__ void __launch_bounds__(PRE_THREADS, 2) sdpa_bwd_preprocess(const Chai
     if (threadIdx.x == 0 && p.dq_accum && rows > 0) {
       uint8_t* acc = reinterpret_cast<uint8_t*>(p.dq_accum + ((long long)bh * p.n_qt + qt) * BQ * p.dq_acc_cols);
       const uint32_t total = (uint32_t)rows * p.dq_acc_cols * 4;
-      for (uint32_t off = 0; off < total; off += PRE_ZERO)
-        bulk_store(acc + off, zero, total - off < (uint32_t)PRE_ZERO ? total - off : (uint32_t)PRE_ZERO);
+      if (in_bounds(p.status, acc, total, p.dq_accum, dq_accum_bytes(p)))
+        for (uint32_t off = 0; off < total; off += PRE_ZERO)
+          bulk_store(acc + off, zero, total - off < (uint32_t)PRE_ZERO ? total - off : (uint32_t)PRE_ZERO);
       bulk_commit_group();
     }
     if (p.dbias_red) zero_shared_dbias_rows(p, bh, qt);
@@ -154,6 +160,7 @@ __global__ void __launch_bounds__(PRE_THREADS, 2) sdpa_bwd_preprocess(const Chai
     const uint8_t* so = smem + PRE_OFF_O + st * PRE_TILE;
     const uint8_t* sd = smem + PRE_OFF_DO + st * PRE_TILE;
     float* qs = p.qstat + (long long)t * QSTAT_FLOATS;
+    const bool qs_ok = in_bounds(p.status, qs, QSTAT_FLOATS * 4, p.qstat, qstat_bytes(p));
     const float sink2 = p.dsink_part ? p.sink[bh % (unsigned)p.Hq] * LOG2E : 0.f;
 #pragma unroll
     for (int u = 0; u < PASSES; ++u) {
@@ -176,8 +183,10 @@ __global__ void __launch_bounds__(PRE_THREADS, 2) sdpa_bwd_preprocess(const Chai
           lse2 = (l == -INFINITY) ? INFINITY : l * LOG2E;
           delta = dot;
         }
-        qs[qi] = lse2;
-        qs[BQ + qi] = delta;
+        if (qs_ok) {
+          qs[qi] = lse2;
+          qs[BQ + qi] = delta;
+        }
         // Sink term of this row: exp(sink - LSE) * delta (0 for a row past the
         // length, whose delta is 0, or with LSE = -inf, whose lse2 is +inf).
         if (p.dsink_part) sink_terms[qi] = exp2f(sink2 - lse2) * delta;
@@ -235,6 +244,9 @@ __global__ void __launch_bounds__(256) sdpa_bwd_dq_convert(const ChainParams p) 
   const int live = max(0, min(rows, Lq - qt * BQ)); // rows holding accumulated values
   const float* src = p.dq_accum + ((long long)bh * p.n_qt + qt) * BQ * ACC;
   __nv_bfloat16* dst = p.dq + ((long long)bh * p.Sq + (long long)qt * BQ) * DQK;
+  if (!in_bounds(p.status, src, (size_t)BQ * ACC * 4, p.dq_accum, dq_accum_bytes(p)) ||
+      !in_bounds(p.status, dst, (size_t)rows * DQK * 2, p.dq, io_q_bytes(p, DQK)))
+    return;
   float4 a[MAX_ITEMS], c[MAX_ITEMS];
 #pragma unroll
   for (int u = 0; u < MAX_ITEMS; ++u) {

@@ -197,7 +197,11 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
             const int qt = w.qt0 + half;
             const bool stored = qt < p.n_qt && lo <= qt && qt <= hi;
             const uint8_t* src = stored ? ds_tile(p, w.bh, band_prefix, band_lo, qt) : p.zero_tile;
-            bulk_load(stage + half * DS_TILE_BYTES, src, DS_TILE_BYTES, &dsfull[st]);
+            if (stored ? in_bounds(p.status, src, DS_TILE_BYTES, p.ds_ws, ds_ws_bytes(p))
+                       : in_bounds(p.status, src, DS_TILE_BYTES, p.zero_tile, DS_TILE_BYTES))
+              bulk_load(stage + half * DS_TILE_BYTES, src, DS_TILE_BYTES, &dsfull[st]);
+            else
+              mbar_complete_tx(&dsfull[st], DS_TILE_BYTES);
           }
           if (band_hi >= band_lo) band_prefix += band_hi - band_lo + 1;
         }

@@ -331,9 +331,11 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
       auto load_qstat = [&](int t) {
         const int st = t % NSTAGE, hj = t / n1;
         const int qt = qt_hi - (t - hj * n1), bh = bh0 + hj;
-        bulk_load(sQS + st * QSTAT_FLOATS,
-                  p.qstat + ((long long)bh * p.n_qt + qt) * QSTAT_FLOATS, QSTAT_FLOATS * 4,
-                  &bars[BAR_QFULL + st]);
+        const float* src = p.qstat + ((long long)bh * p.n_qt + qt) * QSTAT_FLOATS;
+        if (in_bounds(p.status, src, QSTAT_FLOATS * 4, p.qstat, qstat_bytes(p)))
+          bulk_load(sQS + st * QSTAT_FLOATS, src, QSTAT_FLOATS * 4, &bars[BAR_QFULL + st]);
+        else
+          mbar_complete_tx(&bars[BAR_QFULL + st], QSTAT_FLOATS * 4);
       };
       mbar_arrive_expect_tx(&bars[BAR_K], L::TILE_KV);
       for (int blk = 0; blk < D / 64; ++blk)
@@ -484,7 +486,8 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
           const int hj = t / n1;
           const int qt = qt_hi - (t - hj * n1), bh = bh0 + hj;
           uint8_t* dst = ds_tile(p, bh, band_prefix, band_lo, qt);
-          bulk_store(dst, sDS + s * L::TILE_DS, DS_TILE_BYTES);
+          if (in_bounds(p.status, dst, DS_TILE_BYTES, p.ds_ws, ds_ws_bytes(p)))
+            bulk_store(dst, sDS + s * L::TILE_DS, DS_TILE_BYTES);
           bulk_commit_group();
           bulk_wait_group_read0();
           mbar_arrive(&bars[BAR_DSCOPIED + s]);
@@ -547,7 +550,10 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
         const int turn = kt - kv_lo + p.relay_turn_skew;
         int* counter = p.counters + (long long)bh * p.n_qt + qt;
         const uint64_t t0 = globaltimer_ns();
-        while (ld_acquire_gpu(counter) != turn) {
+        const bool counter_ok = in_bounds(p.status, counter, sizeof(int), p.counters,
+                                          (size_t)p.n_counters * sizeof(int));
+        if (!counter_ok) counter = p.counters;  // stays in range; the status word reports it
+        while (counter_ok && ld_acquire_gpu(counter) != turn) {
           __nanosleep(32);
           if (globaltimer_ns() - t0 > p.relay_wait_ns) {
             // Gives up on the turn (the adds may then come out of order) and
@@ -577,7 +583,8 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
         mbar_arrive(&bars[BAR_STAGEREADY + hf]);
         if (leader) {
           mbar_wait(&bars[BAR_STAGEREADY + hf], t & 1, abort_flag, WAIT_LIMIT_NS);
-          bulk_reduce_add_f32(dst + hf * 32 * D, stg, L::TILE_DQ / 2);
+          if (in_bounds(p.status, dst + hf * 32 * D, L::TILE_DQ / 2, p.dq_accum, dq_accum_bytes(p)))
+            bulk_reduce_add_f32(dst + hf * 32 * D, stg, L::TILE_DQ / 2);
           bulk_commit_group();
           // The previously issued half's reduction has read its buffer.
           if (t >= 1 || hf == 1) {

@@ -212,8 +212,11 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
         mbar_arrive_expect_tx(qfull, L::TILE_Q + QSTAT_FLOATS * 4);
         for (int blk = 0; blk < DQK / 64; ++blk)
           tma_load_3d(sQ + sq * L::TILE_Q + blk * L::BLK_Q, &maps.q, qfull, blk * 64, qt * BQ, bh);
-        bulk_load(sQS + sq * QSTAT_FLOATS, p.qstat + ((long long)bh * p.n_qt + qt) * QSTAT_FLOATS,
-                  QSTAT_FLOATS * 4, qfull);
+        const float* src = p.qstat + ((long long)bh * p.n_qt + qt) * QSTAT_FLOATS;
+        if (in_bounds(p.status, src, QSTAT_FLOATS * 4, p.qstat, qstat_bytes(p)))
+          bulk_load(sQS + sq * QSTAT_FLOATS, src, QSTAT_FLOATS * 4, qfull);
+        else
+          mbar_complete_tx(qfull, QSTAT_FLOATS * 4);
         if (t >= NDO &&
             !mbar_wait(&bars[BAR_DOEMPTY + sd], ((t / NDO) - 1) & 1, abort_flag, WAIT_LIMIT_NS))
           break;
@@ -328,7 +331,8 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
         if (!mbar_wait(&bars[BAR_DSREADY + s], j & 1, abort_flag, WAIT_LIMIT_NS)) break;
         const int qt = qt_hi - t;
         uint8_t* dst = ds_tile(p, bh, band_prefix, band_lo, qt);
-        bulk_store(dst, sDS + s * L::TILE_DS, DS_TILE_BYTES);
+        if (in_bounds(p.status, dst, DS_TILE_BYTES, p.ds_ws, ds_ws_bytes(p)))
+          bulk_store(dst, sDS + s * L::TILE_DS, DS_TILE_BYTES);
         bulk_commit_group();
         bulk_wait_group_read0();
         mbar_arrive(&bars[BAR_DSCOPIED + s]);

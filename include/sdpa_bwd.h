@@ -52,7 +52,11 @@ typedef enum {
   SDPA_ERR_ALIGN = 3,       /* a tensor pointer is not 16-byte aligned              */
   SDPA_ERR_WORKSPACE = 4,   /* workspace smaller than sdpa_bwd_workspace_size()     */
   SDPA_ERR_CUDA = 5,        /* a CUDA runtime call failed                           */
-  SDPA_ERR_TIMEOUT = 6      /* a device-side bounded wait ran out (reported later)  */
+  SDPA_ERR_TIMEOUT = 6,     /* a device-side bounded wait ran out (reported later)  */
+  SDPA_ERR_BOUNDS = 7       /* debug-bounds build only (libsdpa_bwd_debug.so, built
+                               with SDPA_DEBUG_BOUNDS): a kernel found a global
+                               access outside its region and skipped it (reported
+                               later, results invalid)                               */
 } sdpa_status;
 
 /* Element types: of an optional additive bias (BF16, F16 or F32) and of the
@@ -329,7 +333,7 @@ const char* sdpa_status_string(int status);
  * wait since the last check (its results are then invalid), or SDPA_ERR_CUDA
  * if the synchronization itself failed.
  */
-int sdpa_bwd_check_device_status(void* stream);
+int sdpa_bwd_check_device_status(void* stream);  /* SDPA_ERR_BOUNDS takes precedence */
 
 /*
  * Failure detection of the ordered relay (deterministic mode for D_qk other

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_version_and_status_strings(lib):
     assert lib.sdpa_bwd_version() == 200
     assert lib.sdpa_status_string(OK) == b"ok"
-    for code in range(1, 7):
+    for code in range(1, 8):
         assert lib.sdpa_status_string(code) not in (b"ok", b"unknown status")
     assert lib.sdpa_status_string(99) == b"unknown status"
 
