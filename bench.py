@@ -383,13 +383,13 @@ def cpu_baseline_leg(w, t, target_s=12.0):
 MAIN_SOURCES = {"sdpa_bwd_main": ("sdpa_bwd_main.cuh", "common.cuh", "ptx.cuh", "nvfp4.cuh", "bias.cuh"),
                 "sdpa_bwd_main_ds": ("sdpa_bwd_main_ds.cu", "common.cuh", "ptx.cuh", "bias.cuh")}
 MAIN_TRAFFIC = {
-    "128fcc156055751a": {"causal_mha": 114551296 + 31852544,
-                         "causal_gqa_det": 123352320 + 513683200,
-                         "swa_causal_padded": 247342336 + 186045952,
-                         "causal_mha/bias-B-f32": 468788992 + 584808704,
-                         "causal_mha/qat": 113423360 + 29674752},
-    "0ac47d748bd4a176": {"mla_br_causal": 131985152 + 263710976,
-                         "mla_br_causal/bias-B-bf16": 426161664 + 1331418368},
+    "ef56c54db91919ba": {"causal_gqa_det": 123785472 + 512181504,
+                         "causal_mha": 114017792 + 31246848,
+                         "swa_causal_padded": 246417920 + 186324992,
+                         "causal_mha/bias-B-f32": 468240384 + 583655680,
+                         "causal_mha/qat": 112624896 + 28589568},
+    "fea0e1085973a768": {"mla_br_causal": 132064000 + 263953920,
+                         "mla_br_causal/bias-B-bf16": 423545856 + 1330964736},
 }
 
 
