@@ -5,6 +5,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -162,6 +163,33 @@ def test_band_model_against_brute_force():
                 assert (lo, hi) == (min(tiles), max(tiles))
             else:
                 assert hi < lo
+
+
+def test_band_contains_every_shorter_batch_row():
+    """With per-batch lengths and a top-left mask (or no lengths at all) the stored band,
+    taken at the full lengths, contains the query tiles that each key tile visits for
+    any shorter batch row: the kernels index a stored tile by its offset inside the band."""
+    rng = np.random.default_rng(7)
+    for _ in range(60):
+        Sq, Skv = int(rng.integers(1, 700)), int(rng.integers(1, 700))
+        causal = int(rng.integers(0, 2))
+        wl = int(rng.integers(0, 300)) if rng.random() < 0.5 else -1
+        wr = int(rng.integers(0, 100)) if causal and rng.random() < 0.3 else -1
+        for kt in range(-(-Skv // 128)):
+            lo, hi = visited_query_tiles(kt, Sq, Skv, causal, 0, wl, wr)
+            for _ in range(8):
+                Lq, Lk = int(rng.integers(0, Sq + 1)), int(rng.integers(0, Skv + 1))
+                a, b = visited_query_tiles(kt, Lq, Lk, causal, 0, wl, wr)
+                if a <= b:
+                    assert lo <= a and b <= hi, (Sq, Skv, causal, wl, wr, kt, Lq, Lk)
+    # A bottom-right mask moves the visited range with the lengths, so the host stores
+    # the whole rectangle there: shorter rows leave the full-length band.
+    outside = 0
+    for kt in range(4):
+        lo, hi = visited_query_tiles(kt, 512, 512, 1, 1, -1, -1)
+        a, b = visited_query_tiles(kt, 200, 512, 1, 1, -1, -1)
+        outside += a <= b and not (lo <= a and b <= hi)
+    assert outside > 0
 
 
 def test_workspace_size_rejects(lib):
