@@ -52,15 +52,14 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 //   kTwoKernel main kernel with dS stored, then the Q-stationary dQ kernel:
 //              the deterministic route for D_qk = 128 as on the pages (the
 //              relay serves every other D_qk up to 128), and the only route
-//              for D_qk = 192,
-//              whose dK accumulator leaves no tensor memory for dQ in the main
-//              kernel.
+//              for D_qk = 192 and 256, whose dK accumulators leave no tensor
+//              memory for dQ in the main kernel.
 //   kReduce    main kernel with the fp32 dQ accumulator (the ordered relay
 //              when deterministic), then the convert.
 enum class Route { kReduce, kTwoKernel };
 
 Route choose_route(int deterministic, int Dqk) {
-  return (Dqk == 192 || (deterministic && Dqk == 128)) ? Route::kTwoKernel : Route::kReduce;
+  return (Dqk > 128 || (deterministic && Dqk == 128)) ? Route::kTwoKernel : Route::kReduce;
 }
 
 // The problem shape and mask as far as they size the workspace.
@@ -142,8 +141,10 @@ Carve carve(const Shape& sh, Route route, bool qat = false) {
 
 bool dims_supported(int Dqk, int Dv) {
   // D_qk = D_v, a multiple of 8 up to 128: the 64- or 128-column kernels, the
-  // columns past D zero-filled by TMA; and the MLA pair 192/128.
-  return (Dqk == Dv && Dqk % 8 == 0 && Dqk >= 8 && Dqk <= 128) || (Dqk == 192 && Dv == 128);
+  // columns past D zero-filled by TMA; the MLA pair 192/128; and 256/256 (the
+  // backward only: units that accumulate half of the dK/dV columns each).
+  return (Dqk == Dv && Dqk % 8 == 0 && Dqk >= 8 && Dqk <= 128) || (Dqk == 192 && Dv == 128) ||
+         (Dqk == 256 && Dv == 256);
 }
 
 int basic_checks(int B, int Hq, int Hkv, int Sq, int Skv, int Dqk, int Dv) {
@@ -423,7 +424,7 @@ int run_chain(const void* q, const void* k, const void* v, const void* o, const 
   // to reduce; below 1.5 units per SM the greedy dispatch of uneven (causal)
   // units loses more to imbalance than that saves.
   p.gsz = 1;
-  if (D_qk != 192) {
+  if (D_qk <= 128) {
     for (int c = p.G; c > 1; --c) {
       if (p.G % c == 0 && (long long)ceil_div(S_kv, BN) * B * H_kv * (p.G / c) * 2 >= 3ll * sms) {
         p.gsz = c;
@@ -533,7 +534,7 @@ int run_chain(const void* q, const void* k, const void* v, const void* o, const 
   prof.end(0);
   if (e == cudaSuccess) {
     prof.begin(1);
-    e = D_qk == 192 ? launch_main_ds(maps, p, stream)
+    e = D_qk > 128 ? launch_main_ds(maps, p, stream)
                     : (qat ? launch_main_qat(maps, p, stream) : launch_main(maps, p, stream));
     prof.end(1);
   }
@@ -583,6 +584,9 @@ int run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   int rc = basic_checks(B, H_q, H_kv, S_q, S_kv, D_qk, D_v);
   if (rc != SDPA_OK) return rc;
+  // The forward kernel keeps two S slots and two O halves in tensor memory,
+  // which leaves room for D_v up to 128 (and the MLA pair).
+  if (D_v > 128) return SDPA_ERR_UNSUPPORTED;
   if (!q || !k || !v || !o || !lse) return SDPA_ERR_INVALID;
   for (const void* ptr : {q, k, v, (const void*)o})
     if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return SDPA_ERR_ALIGN;

@@ -56,13 +56,18 @@ __device__ void zero_shared_dbias_rows(const ChainParams& p, unsigned bh, int qt
 // lanes past D_v/8 (D_v not a power-of-two multiple of 8) read nothing.
 constexpr int PRE_THREADS = 256;
 constexpr int PRE_STAGES = 3;
-constexpr int PRE_TILE = BQ * 128 * 2;               // one 64-row io tile at D_v <= 128
 constexpr int PRE_ZERO = 16384;                      // zero source of the accumulator clear
-constexpr int PRE_OFF_O = 0;
-constexpr int PRE_OFF_DO = PRE_OFF_O + PRE_STAGES * PRE_TILE;
-constexpr int PRE_OFF_ZERO = PRE_OFF_DO + PRE_STAGES * PRE_TILE;
-constexpr int PRE_OFF_BAR = PRE_OFF_ZERO + PRE_ZERO;
-constexpr int PRE_BYTES = PRE_OFF_BAR + PRE_STAGES * 8;
+template <int TPR>
+struct PreLayout {
+  static constexpr int TILE = BQ * TPR * 8 * 2;      // one 64-row io tile at D_v <= 8 * TPR
+  static constexpr int OFF_O = 0;
+  static constexpr int OFF_DO = OFF_O + PRE_STAGES * TILE;
+  static constexpr int OFF_ZERO = OFF_DO + PRE_STAGES * TILE;
+  static constexpr int OFF_BAR = OFF_ZERO + PRE_ZERO;
+  static constexpr int BYTES = OFF_BAR + PRE_STAGES * 8;
+  // Up to D_v = 128 two CTAs share an SM; at 256 one CTA takes 208 KiB.
+  static constexpr int CTAS_PER_SM = BYTES <= 113 * 1024 ? 2 : 1;
+};
 
 template <int TPR, bool F16>
 __global__ void __launch_bounds__(PRE_THREADS, 2) sdpa_bwd_preprocess(const ChainParams p) {
@@ -71,8 +76,11 @@ __global__ void __launch_bounds__(PRE_THREADS, 2) sdpa_bwd_preprocess(const Chai
   // anything written here.
   pdl_launch_dependents();
 
+  using PL = PreLayout<TPR>;
+  constexpr int PRE_TILE = PL::TILE;
+  constexpr int PRE_OFF_O = PL::OFF_O, PRE_OFF_DO = PL::OFF_DO, PRE_OFF_ZERO = PL::OFF_ZERO;
   extern __shared__ __align__(128) uint8_t smem[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + PRE_OFF_BAR);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + PL::OFF_BAR);
   const uint8_t* zero = smem + PRE_OFF_ZERO;
   const int DV = p.Dv;
   constexpr int RPP = PRE_THREADS / TPR;   // rows per pass
@@ -121,7 +129,10 @@ __global__ void __launch_bounds__(PRE_THREADS, 2) sdpa_bwd_preprocess(const Chai
     mbar_arrive_expect_tx(bar, 2 * bytes);
     if (in_bounds(p.status, p.o + row0 * DV, bytes, p.o, io_q_bytes(p, DV)) &&
         in_bounds(p.status, p.d_o + row0 * DV, bytes, p.d_o, io_q_bytes(p, DV)) && bytes <= PRE_TILE) {
-      bulk_load(smem + PRE_OFF_O + (k % PRE_STAGES) * PRE_TILE, p.o + row0 * DV, bytes, bar);
+      // O is read only here (dO is read again by the main kernel): on the
+      // reduction route it makes way for the dQ accumulator cleared below.
+      bulk_load_hint(smem + PRE_OFF_O + (k % PRE_STAGES) * PRE_TILE, p.o + row0 * DV, bytes, bar,
+                     p.dq_accum ? l2_evict_first() : l2_evict_normal());
       bulk_load(smem + PRE_OFF_DO + (k % PRE_STAGES) * PRE_TILE, p.d_o + row0 * DV, bytes, bar);
     } else {
       mbar_complete_tx(bar, 2 * bytes);
@@ -142,7 +153,8 @@ __global__ void __launch_bounds__(PRE_THREADS, 2) sdpa_bwd_preprocess(const Chai
       const uint32_t total = (uint32_t)rows * p.dq_acc_cols * 4;
       if (in_bounds(p.status, acc, total, p.dq_accum, dq_accum_bytes(p)))
         for (uint32_t off = 0; off < total; off += PRE_ZERO)
-          bulk_store(acc + off, zero, total - off < (uint32_t)PRE_ZERO ? total - off : (uint32_t)PRE_ZERO);
+          bulk_store_hint(acc + off, zero, total - off < (uint32_t)PRE_ZERO ? total - off : (uint32_t)PRE_ZERO,
+                          l2_evict_last());  // the main kernel's reductions follow
       bulk_commit_group();
     }
     if (p.dbias_red) zero_shared_dbias_rows(p, bh, qt);
@@ -324,30 +336,35 @@ cudaError_t launch_dsink(const ChainParams& p, cudaStream_t s) {
 template <int TPR, bool F16>
 static cudaError_t launch_preprocess_tpr(const ChainParams& p, cudaStream_t s, int num_sms) {
   const long long tiles = (long long)p.B * p.Hq * p.n_qt;
-  const long long cap = 2ll * num_sms;
+  const long long cap = (long long)PreLayout<TPR>::CTAS_PER_SM * num_sms;
   const dim3 grid((unsigned)(tiles < cap ? tiles : cap));
-  return launch_kernel(sdpa_bwd_preprocess<TPR, F16>, grid, dim3(PRE_THREADS), PRE_BYTES, s, false, p);
+  return launch_kernel(sdpa_bwd_preprocess<TPR, F16>, grid, dim3(PRE_THREADS), PreLayout<TPR>::BYTES, s,
+                       false, p);
 }
 
 template <bool F16>
 static cudaError_t launch_preprocess_io(const ChainParams& p, cudaStream_t s, int num_sms) {
   if (p.Dv <= 32) return launch_preprocess_tpr<4, F16>(p, s, num_sms);
   if (p.Dv <= 64) return launch_preprocess_tpr<8, F16>(p, s, num_sms);
-  return launch_preprocess_tpr<16, F16>(p, s, num_sms);
+  if (p.Dv <= 128) return launch_preprocess_tpr<16, F16>(p, s, num_sms);
+  return launch_preprocess_tpr<32, F16>(p, s, num_sms);
 }
 
 template <int TPR, bool F16>
 static cudaError_t set_pre_smem() {
-  return cudaFuncSetAttribute(sdpa_bwd_preprocess<TPR, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, PRE_BYTES);
+  return cudaFuncSetAttribute(sdpa_bwd_preprocess<TPR, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              PreLayout<TPR>::BYTES);
 }
 
 cudaError_t preprocess_kernel_setup() {
   cudaError_t e = set_pre_smem<4, false>();
   if (e == cudaSuccess) e = set_pre_smem<8, false>();
   if (e == cudaSuccess) e = set_pre_smem<16, false>();
+  if (e == cudaSuccess) e = set_pre_smem<32, false>();
   if (e == cudaSuccess) e = set_pre_smem<4, true>();
   if (e == cudaSuccess) e = set_pre_smem<8, true>();
   if (e == cudaSuccess) e = set_pre_smem<16, true>();
+  if (e == cudaSuccess) e = set_pre_smem<32, true>();
   return e;
 }
 

@@ -34,7 +34,7 @@ constexpr uint64_t DQ_WAIT_LIMIT_NS = 4000000000ull;
 // paces the kernel, can run further ahead.
 template <int D>
 struct DqLayout {
-  static constexpr int NK = (D <= 128) ? 3 : 2;         // K buffers
+  static constexpr int NK = (D <= 128) ? 3 : 2;         // K buffers (64 KiB each at D = 256)
   static constexpr int NDS = (D <= 128) ? 4 : 3;        // dS buffers
   static constexpr int TILE_K = BN * D * 2;             // [D/64 blocks][128 keys][128 B]
   static constexpr int TILE_DS = 2 * DS_TILE_BYTES;     // two dS^T tiles: [2][128 keys][64 q]
@@ -362,8 +362,10 @@ static cudaError_t set_dq_smem() {
 cudaError_t dq_kernel_setup() {
   cudaError_t e = set_dq_smem<128, false>();
   if (e == cudaSuccess) e = set_dq_smem<192, false>();
+  if (e == cudaSuccess) e = set_dq_smem<256, false>();
   if (e == cudaSuccess) e = set_dq_smem<128, true>();
   if (e == cudaSuccess) e = set_dq_smem<192, true>();
+  if (e == cudaSuccess) e = set_dq_smem<256, true>();
   return e;
 }
 
@@ -372,6 +374,9 @@ static cudaError_t launch_dq_variant(const CUtensorMap& k_map, const ChainParams
                                      dim3 grid) {
   if (p.Dqk == 192)
     return launch_kernel(sdpa_bwd_dq_from_ds<192, F16>, grid, dim3(DQ_THREADS), DqLayout<192>::BYTES, s,
+                         true, k_map, p);
+  if (p.Dqk == 256)
+    return launch_kernel(sdpa_bwd_dq_from_ds<256, F16>, grid, dim3(DQ_THREADS), DqLayout<256>::BYTES, s,
                          true, k_map, p);
   return launch_kernel(sdpa_bwd_dq_from_ds<128, F16>, grid, dim3(DQ_THREADS), DqLayout<128>::BYTES, s,
                        true, k_map, p);

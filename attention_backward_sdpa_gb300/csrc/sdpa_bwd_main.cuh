@@ -337,13 +337,20 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
         else
           mbar_complete_tx(&bars[BAR_QFULL + st], QSTAT_FLOATS * 4);
       };
+      // On the dQ-reduction route a K/V tile is read by this unit only, when
+      // its KV group is one unit; marking it evict-first keeps the fp32 dQ
+      // accumulator in L2 (the two-kernel route, whose dQ kernel reads K
+      // again, measured slightly slower with the hints and keeps the default).
+      const bool once = !DS_OUT && p.n_part == 1;
+      const uint64_t pol_k = once ? l2_evict_first() : l2_evict_normal();
+      const uint64_t pol_v = pol_k;
       mbar_arrive_expect_tx(&bars[BAR_K], L::TILE_KV);
       for (int blk = 0; blk < D / 64; ++blk)
-        tma_load_3d(sK + blk * L::BLK_KV, &maps.k, &bars[BAR_K], blk * 64, k0, b * p.Hkv + hk);
+        tma_load_3d_hint(sK + blk * L::BLK_KV, &maps.k, &bars[BAR_K], blk * 64, k0, b * p.Hkv + hk, pol_k);
       load_q_do(0);
       mbar_arrive_expect_tx(&bars[BAR_V], L::TILE_KV);
       for (int blk = 0; blk < D / 64; ++blk)
-        tma_load_3d(sV + blk * L::BLK_KV, &maps.v, &bars[BAR_V], blk * 64, k0, b * p.Hkv + hk);
+        tma_load_3d_hint(sV + blk * L::BLK_KV, &maps.v, &bars[BAR_V], blk * 64, k0, b * p.Hkv + hk, pol_v);
       pdl_wait_prior_grid();  // row statistics come from the preprocess kernel
       load_qstat(0);
       for (int t = 1; t < n; ++t) {
@@ -511,6 +518,7 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
     const bool has_rows = quarter * 32 < D;            // warp-uniform
     const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
     const bool leader = (warp == 8 && lane == 0);
+    const uint64_t pol_acc = l2_evict_last();  // the convert reads the accumulator next
     int* pending_counter = nullptr;  // deterministic mode: turn not yet released
     int pending_turn = 0;
     int* pending_next = nullptr;     // ... and the current tile's, once the next is issued
@@ -584,7 +592,7 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
         if (leader) {
           mbar_wait(&bars[BAR_STAGEREADY + hf], t & 1, abort_flag, WAIT_LIMIT_NS);
           if (in_bounds(p.status, dst + hf * 32 * D, L::TILE_DQ / 2, p.dq_accum, dq_accum_bytes(p)))
-            bulk_reduce_add_f32(dst + hf * 32 * D, stg, L::TILE_DQ / 2);
+            bulk_reduce_add_f32_hint(dst + hf * 32 * D, stg, L::TILE_DQ / 2, pol_acc);
           bulk_commit_group();
           // The previously issued half's reduction has read its buffer.
           if (t >= 1 || hf == 1) {
@@ -840,7 +848,11 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
     if (row == 0) {
       const long long head = out_head;
       const CUtensorMap* map = slot ? &maps.dk_out : &maps.dv_out;
-      for (int blk = 0; blk < D / 64; ++blk) tma_store_3d(map, stg + blk * L::BLK_KV, blk * 64, k0, (int)head);
+      // Final dK/dV rows are not read again (partial sets are, by the group
+      // reduction); the reduction route keeps its accumulator in L2 instead.
+      const uint64_t pol = (!DS_OUT && p.n_part == 1) ? l2_evict_first() : l2_evict_normal();
+      for (int blk = 0; blk < D / 64; ++blk)
+        tma_store_3d_hint(map, stg + blk * L::BLK_KV, blk * 64, k0, (int)head, pol);
       bulk_commit_group();
       bulk_wait_group_read0();  // the CTA may exit once the copies have read shared memory
     }

@@ -1,5 +1,6 @@
 // sdpa_bwd_main_ds.cu -- SDPA backward main kernel for head dims whose dK
-// accumulator leaves no tensor memory for dQ (MLA: D_qk = 192, D_v = 128).
+// accumulator leaves no tensor memory for dQ (MLA: D_qk = 192, D_v = 128; and
+// D_qk = D_v = 256).
 //
 // Same computation as sdpa_bwd_main.cu (cuDNN frontend docs, "SDPA Backward
 // (SM120)", "Main-kernel pipeline: KV-stationary, five chained GEMMs"; D_qk
@@ -15,6 +16,14 @@
 //   G4  dK  += dS^T Q
 // Tensor memory (512 columns): two 96-column slots at 96s, dV at [192,192+D_v),
 // dK at [192+D_v, 192+D_v+D_qk): 2*96 + 128 + 192 = 512 for MLA.
+//
+// D_qk = D_v = 256 (SPLIT = 2): dK and dV alone would need all 512 columns, so
+// a work unit accumulates one half of their columns, [128h, 128h+128), and the
+// two units of a key tile each compute S^T and dP^T over the full head dim
+// (G1 and G2 are done twice: 7 GEMMs per pair instead of 5). G3 and G4 read
+// the matching half of dO and Q. Unit h = 0 alone stores dS^T, writes dBias and
+// zeroes the rows of empty key tiles. Its shared memory holds K and V (64 KiB
+// each), the two dS^T buffers and one Q and one dO stage (32 KiB each).
 //
 // Warps: 0-3 even tiles (slot 0), 4-7 odd tiles (slot 1), 8 TMA producer,
 // 9 G1 issuer and tensor-memory owner, 10 G3/G4 issuer, 11 G2 issuer, 12 dS^T store,
@@ -59,7 +68,7 @@ enum : int {
   NUM_BARS = 30
 };
 
-template <int DQK, int DV>
+template <int DQK, int DV, int SPLIT = 1>
 struct Layout {
   static constexpr int BLK_KV = BN * 128;
   static constexpr int BLK_Q = BQ * 128;
@@ -68,13 +77,17 @@ struct Layout {
   static constexpr int TILE_Q = BQ * DQK * 2;
   static constexpr int TILE_DO = BQ * DV * 2;
   static constexpr int TILE_DS = BN * BQ * 2;
+  static constexpr int ACC_K = DQK / SPLIT, ACC_V = DV / SPLIT;  // accumulated columns
   static constexpr int FIXED = TILE_K + TILE_V + 2 * TILE_DS;
+  static constexpr bool fits(int nq, int ndo) {
+    return FIXED + nq * (TILE_Q + QSTAT_FLOATS * 4) + ndo * TILE_DO + NUM_BARS * 8 + 64 <= 232448;
+  }
   // Q (with the row statistics) is held from G1 to G4, the whole tile, while
   // dO is released by G3; so Q gets the deeper ring. Three Q stages cover the
   // ~2000-cycle load latency at the tensor pipe's tile rate, two would not.
-  static constexpr int NDO = 2;
-  static constexpr int NQ =
-      (FIXED + 3 * (TILE_Q + QSTAT_FLOATS * 4) + NDO * TILE_DO + NUM_BARS * 8 + 64 <= 232448) ? 3 : 2;
+  // At D = 256 one stage of each is all that fits.
+  static constexpr int NDO = fits(1, 2) ? 2 : 1;
+  static constexpr int NQ = fits(3, NDO) ? 3 : (fits(2, NDO) ? 2 : 1);
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + TILE_K;
   static constexpr int OFF_DS = OFF_V + TILE_V;
@@ -84,10 +97,11 @@ struct Layout {
   static constexpr int OFF_BAR = OFF_QS + NQ * QSTAT_FLOATS * 4;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int BYTES = OFF_MISC + 64;
-  static constexpr uint32_t COL_DV = 192, COL_DK = 192 + DV;
+  static constexpr uint32_t COL_DV = 192, COL_DK = 192 + ACC_V;
   __host__ __device__ static constexpr uint32_t col_s(int slot) { return 96u * slot; }
   __host__ __device__ static constexpr uint32_t col_p(int slot) { return 96u * slot + 64u; }
-  static_assert(COL_DK + DQK <= 512, "tensor memory budget");
+  static_assert(COL_DK + ACC_K <= 512, "tensor memory budget");
+  static_assert(ACC_K % 64 == 0 && ACC_V % 64 == 0, "whole 64-column blocks per unit");
   static_assert(BYTES <= 232448, "shared memory budget");
   static_assert(BYTES > 116 * 1024, "one CTA per SM");
   static_assert(TILE_Q % 1024 == 0 && TILE_DO % 1024 == 0 && TILE_K % 1024 == 0, "alignment");
@@ -99,11 +113,11 @@ struct Layout {
 // D_qk 64/128 kernel (bias.cuh): loads of the next tile's bias column issued
 // right after dS, dS' stored as dBias, and the dBias blocks no CTA computes
 // zeroed by an idle warp (or by an empty unit's whole CTA).
-template <int DQK, int DV, bool BIAS, bool F16 = false>
+template <int DQK, int DV, bool BIAS, bool F16 = false, int SPLIT = 1>
 __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
     sdpa_bwd_main_ds(const __grid_constant__ MainMaps maps, const ChainParams p) {
   using namespace ds_kernel;
-  using L = Layout<DQK, DV>;
+  using L = Layout<DQK, DV, SPLIT>;
   constexpr int NQ = L::NQ, NDO = L::NDO;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -126,12 +140,14 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
     // written by an idle warp of the head's other CTAs (or here, when the
     // batch row has no query or no key); leave before any setup.
     const int BH0 = p.B * p.Hq;
-    const int kt0 = blockIdx.x / BH0, bh0 = blockIdx.x % BH0, b0 = bh0 / p.Hq;
+    const int u0 = (int)blockIdx.x / SPLIT;
+    const int kt0 = u0 / BH0, bh0 = u0 % BH0, b0 = bh0 / p.Hq;
     int Lq0, Lk0, lo0, hi0;
     batch_lengths(p, b0, Lq0, Lk0);
     visited_query_tiles(kt0, Lq0, Lk0, p.causal, p.bottom_right, p.window_left, p.window_right, lo0,
                         hi0);
     if (hi0 < lo0) {
+      if (blockIdx.x % SPLIT != 0) return;  // the first half-unit writes the zeros
       // gsz = 1: the partial set of a query head is its bh index.
       if (!row_has_visible_pair(Lq0, Lk0))
         zero_key_tile_rows(p, p.dk_ws ? (long long)bh0 : (long long)b0 * p.Hkv + (bh0 % p.Hq) / p.G,
@@ -168,8 +184,10 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
   const uint32_t tmem = *tmem_slot;
 
   const int BH = p.B * p.Hq;
-  const int kt = blockIdx.x / BH;   // key tile major: the longest units first under causal masks
-  const int bh = blockIdx.x % BH;
+  const int half = (int)blockIdx.x % SPLIT;  // accumulated column half (SPLIT = 2)
+  const int unit = (int)blockIdx.x / SPLIT;
+  const int kt = unit / BH;   // key tile major: the longest units first under causal masks
+  const int bh = unit % BH;
   const int b = bh / p.Hq, h = bh % p.Hq, hk = h / p.G;
   const int k0 = kt * BN;
   int Lq, Lk;
@@ -184,8 +202,12 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
 
   constexpr uint32_t ID_G1 = idesc_io(128, BQ, false, false, F16);
   constexpr uint32_t ID_G2 = idesc_io(128, BQ, false, false, F16);
-  constexpr uint32_t ID_G3 = idesc_io(128, DV, false, true, F16);
-  constexpr uint32_t ID_G4 = idesc_io(128, DQK, false, true, F16);
+  constexpr uint32_t ID_G3 = idesc_io(128, L::ACC_V, false, true, F16);
+  constexpr uint32_t ID_G4 = idesc_io(128, L::ACC_K, false, true, F16);
+  // Byte offsets of this unit's column half in a dO and a Q stage.
+  const uint32_t off_dov = (uint32_t)(half * (L::ACC_V / 64) * L::BLK_Q);
+  const uint32_t off_qk = (uint32_t)(half * (L::ACC_K / 64) * L::BLK_Q);
+  const bool lead = half == 0;  // stores dS^T, writes dBias and the zero rows
   constexpr uint64_t T_KMAJ = sdesc_sw128_template(16, 1024);
   constexpr uint64_t T_MN_Q = sdesc_sw128_template(L::BLK_Q, 1024);
 
@@ -289,7 +311,7 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
         tc_fence_after();
         if (elect_one()) {
           // G3: dV[key, d] += sum_q P^T[key, q] dO[q, d]
-          const uint32_t aDO = smem_u32(sDO + sdu * L::TILE_DO);
+          const uint32_t aDO = smem_u32(sDO + sdu * L::TILE_DO) + off_dov;
 #pragma unroll
           for (int k = 0; k < BQ / 16; ++k)
             mma_ts(tmem + L::COL_DV, tmem + L::col_p(su) + 8 * k, sdesc_at(T_MN_Q, aDO + k * 2048),
@@ -303,7 +325,7 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
         tc_fence_after();
         if (elect_one()) {
           // G4: dK[key, d] += sum_q dS^T[key, q] Q[q, d]
-          const uint32_t aQ = smem_u32(sQ + squ * L::TILE_Q);
+          const uint32_t aQ = smem_u32(sQ + squ * L::TILE_Q) + off_qk;
           const uint32_t aDS = smem_u32(sDS + su * L::TILE_DS);
 #pragma unroll
           for (int k = 0; k < BQ / 16; ++k)
@@ -331,7 +353,7 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
         if (!mbar_wait(&bars[BAR_DSREADY + s], j & 1, abort_flag, WAIT_LIMIT_NS)) break;
         const int qt = qt_hi - t;
         uint8_t* dst = ds_tile(p, bh, band_prefix, band_lo, qt);
-        if (in_bounds(p.status, dst, DS_TILE_BYTES, p.ds_ws, ds_ws_bytes(p)))
+        if (lead && in_bounds(p.status, dst, DS_TILE_BYTES, p.ds_ws, ds_ws_bytes(p)))
           bulk_store(dst, sDS + s * L::TILE_DS, DS_TILE_BYTES);
         bulk_commit_group();
         bulk_wait_group_read0();
@@ -339,12 +361,12 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
       }
       bulk_wait_group_read0();
     }
-  } else if (warp == 13) {
+  } else if (warp == 13 && lead) {
     // This CTA's share of the head's empty key tiles (gsz = 1: the partial
     // set of a query head is its bh index).
     zero_group_share_of_empty_key_tiles(p, p.dk_ws ? (long long)bh : (long long)b * p.Hkv + hk,
                                                  kt, Lq, Lk, lane);
-  } else if (BIAS && warp == 14) {
+  } else if (BIAS && warp == 14 && lead) {
     // The dBias blocks of this key tile that no CTA computes.
     if (p.dbias != nullptr && !p.dbias_red) zero_unvisited_dbias_blocks(p, b, bh, 1, kt, qt_lo, qt_hi, lane, 32);
   }  // warp 15 (and 14 without a bias): idle members of the fourth warpgroup
@@ -474,7 +496,7 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
           const uint32_t w3 = pack_io2<F16>(ds[6], ds[7]);
           *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (row & 7)) << 4)) = make_uint4(w0, w1, w2, w3);
           if constexpr (BIAS) {
-            if (p.dbias != nullptr && key_in) {
+            if (p.dbias != nullptr && key_in && lead) {
               const long long off = (long long)b * p.dbias_bstride + bias_off + (long long)c * p.Skv;
               const int rows_in = min(8, p.Sq - q0 - c);
               if (p.dbias_red) {
@@ -523,12 +545,12 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
       tc_fence_after();
     }
     const bool warp_ok = __all_sync(0xffffffffu, ok);
-    const int D = slot ? DQK : DV;
+    const int D = slot ? L::ACC_K : L::ACC_V;  // this unit's columns
     const uint32_t col0 = slot ? L::COL_DK : L::COL_DV;
     const float mult = slot ? p.scale : 1.f;
     uint8_t* stg = slot ? sQ : sDO;
-    static_assert(L::NQ * L::TILE_Q >= DQK / 64 * L::BLK_KV &&
-                      L::NDO * L::TILE_DO >= DV / 64 * L::BLK_KV,
+    static_assert(L::NQ * L::TILE_Q >= L::ACC_K / 64 * L::BLK_KV &&
+                      L::NDO * L::TILE_DO >= L::ACC_V / 64 * L::BLK_KV,
                   "staging fits in the stage rings");
     for (int c32 = 0; c32 < D / 32; ++c32) {
       uint32_t r[32];
@@ -556,7 +578,8 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
     if (row == 0) {
       const long long head = p.dk_ws ? (long long)bh : (long long)b * p.Hkv + hk;
       const CUtensorMap* map = slot ? &maps.dk_out : &maps.dv_out;
-      for (int blk = 0; blk < D / 64; ++blk) tma_store_3d(map, stg + blk * L::BLK_KV, blk * 64, k0, (int)head);
+      for (int blk = 0; blk < D / 64; ++blk)
+        tma_store_3d(map, stg + blk * L::BLK_KV, (half * (D / 64) + blk) * 64, k0, (int)head);
       bulk_commit_group();
       bulk_wait_group_read0();  // the CTA may exit once the copies have read shared memory
     }
@@ -571,35 +594,47 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
   }
 }
 
-template <int DQK, int DV, bool BIAS, bool F16 = false>
+template <int DQK, int DV, bool BIAS, bool F16, int SPLIT>
 static cudaError_t set_ds_smem() {
-  return cudaFuncSetAttribute(sdpa_bwd_main_ds<DQK, DV, BIAS, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              ds_kernel::Layout<DQK, DV>::BYTES);
+  return cudaFuncSetAttribute(sdpa_bwd_main_ds<DQK, DV, BIAS, F16, SPLIT>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              ds_kernel::Layout<DQK, DV, SPLIT>::BYTES);
 }
 
-cudaError_t main_ds_kernel_setup() {
-  cudaError_t e = set_ds_smem<192, 128, false>();
-  if (e == cudaSuccess) e = set_ds_smem<192, 128, true>();
-  if (e == cudaSuccess) e = set_ds_smem<192, 128, false, true>();
-  if (e == cudaSuccess) e = set_ds_smem<192, 128, true, true>();
+template <int DQK, int DV, int SPLIT>
+static cudaError_t set_ds_smem_all() {
+  cudaError_t e = set_ds_smem<DQK, DV, false, false, SPLIT>();
+  if (e == cudaSuccess) e = set_ds_smem<DQK, DV, true, false, SPLIT>();
+  if (e == cudaSuccess) e = set_ds_smem<DQK, DV, false, true, SPLIT>();
+  if (e == cudaSuccess) e = set_ds_smem<DQK, DV, true, true, SPLIT>();
   return e;
 }
 
-cudaError_t launch_main_ds(const MainMaps& maps, const ChainParams& p, cudaStream_t s) {
-  const dim3 grid((unsigned)(p.n_kt * p.B * p.Hq));
+cudaError_t main_ds_kernel_setup() {
+  cudaError_t e = set_ds_smem_all<192, 128, 1>();
+  if (e == cudaSuccess) e = set_ds_smem_all<256, 256, 2>();
+  return e;
+}
+
+template <int DQK, int DV, int SPLIT>
+static cudaError_t launch_main_ds_dims(const MainMaps& maps, const ChainParams& p, cudaStream_t s) {
+  // SPLIT units per (key tile, query head), key tile major.
+  const dim3 grid((unsigned)(p.n_kt * p.B * p.Hq * SPLIT));
   const dim3 block(ds_kernel::THREADS);
-  if (p.Dqk != 192 || p.Dv != 128) return cudaErrorInvalidValue;
+  constexpr int bytes = ds_kernel::Layout<DQK, DV, SPLIT>::BYTES;
   if (p.bias != nullptr && p.f16)
-    return launch_kernel(sdpa_bwd_main_ds<192, 128, true, true>, grid, block,
-                         ds_kernel::Layout<192, 128>::BYTES, s, true, maps, p);
+    return launch_kernel(sdpa_bwd_main_ds<DQK, DV, true, true, SPLIT>, grid, block, bytes, s, true, maps, p);
   if (p.bias != nullptr)
-    return launch_kernel(sdpa_bwd_main_ds<192, 128, true>, grid, block,
-                         ds_kernel::Layout<192, 128>::BYTES, s, true, maps, p);
+    return launch_kernel(sdpa_bwd_main_ds<DQK, DV, true, false, SPLIT>, grid, block, bytes, s, true, maps, p);
   if (p.f16)
-    return launch_kernel(sdpa_bwd_main_ds<192, 128, false, true>, grid, block,
-                         ds_kernel::Layout<192, 128>::BYTES, s, true, maps, p);
-  return launch_kernel(sdpa_bwd_main_ds<192, 128, false>, grid, block, ds_kernel::Layout<192, 128>::BYTES,
-                       s, true, maps, p);
+    return launch_kernel(sdpa_bwd_main_ds<DQK, DV, false, true, SPLIT>, grid, block, bytes, s, true, maps, p);
+  return launch_kernel(sdpa_bwd_main_ds<DQK, DV, false, false, SPLIT>, grid, block, bytes, s, true, maps, p);
+}
+
+cudaError_t launch_main_ds(const MainMaps& maps, const ChainParams& p, cudaStream_t s) {
+  if (p.Dqk == 192 && p.Dv == 128) return launch_main_ds_dims<192, 128, 1>(maps, p, s);
+  if (p.Dqk == 256 && p.Dv == 256) return launch_main_ds_dims<256, 256, 2>(maps, p, s);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace sdpa

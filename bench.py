@@ -81,11 +81,12 @@ def fwd_flops_per_pair(w: workloads.Workload) -> int:
 
 
 def main_kernel_flops_per_pair(w: workloads.Workload) -> int:
-    """FLOPs the main kernel itself performs per visible pair: all five GEMMs, or
+    """Algorithmic FLOPs of the main kernel per visible pair: all five GEMMs, or
     four on the two-kernel route, where dQ = dS K runs in the separate dQ kernel
-    (the library takes that route for D_qk = 192, and for D_qk = 128 when
-    deterministic)."""
-    if w.Dqk == 192 or (w.deterministic and w.Dqk == 128):
+    (the library takes that route for D_qk = 192 and 256, and for D_qk = 128 when
+    deterministic). At D = 256 the kernel runs S and dP twice (once per half of
+    the dK/dV columns); only the algorithmic four are counted."""
+    if w.Dqk > 128 or (w.deterministic and w.Dqk == 128):
         return 2 * (2 * w.Dqk + 2 * w.Dv)
     return flops_per_pair(w)
 
@@ -378,8 +379,8 @@ def cpu_baseline_leg(w, t, target_s=12.0):
 # DRAM bytes per launch of the main kernel (dram__bytes_read.sum +
 # dram__bytes_write.sum from one ncu capture of the same bench command),
 # valid only for the kernel sources they were taken on: the digest covers the
-# kernel's source files, and a changed kernel reports null. D_qk = 192 runs
-# sdpa_bwd_main_ds, every other head dim sdpa_bwd_main.
+# kernel's source files, and a changed kernel reports null. D_qk = 192 and 256
+# run sdpa_bwd_main_ds, every other head dim sdpa_bwd_main.
 MAIN_SOURCES = {"sdpa_bwd_main": ("sdpa_bwd_main.cuh", "common.cuh", "ptx.cuh", "nvfp4.cuh", "bias.cuh"),
                 "sdpa_bwd_main_ds": ("sdpa_bwd_main_ds.cu", "common.cuh", "ptx.cuh", "bias.cuh")}
 MAIN_TRAFFIC = {
@@ -394,7 +395,7 @@ MAIN_TRAFFIC = {
 
 
 def main_kernel_name(w, tag=None) -> str:
-    return "sdpa_bwd_main_ds" if w.Dqk == 192 else "sdpa_bwd_main"
+    return "sdpa_bwd_main_ds" if w.Dqk > 128 else "sdpa_bwd_main"
 
 
 def main_traffic(w, tag=None):

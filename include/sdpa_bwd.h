@@ -74,7 +74,7 @@ typedef enum {
  * will be given). The workspace holds, each region 256-byte aligned:
  * per-query-tile fp32 row statistics (LSE * log2(e) and delta); either the
  * fp32 dQ accumulator (rows of 64 columns for D_qk up to 64, else 128) or, on
- * the routes that store dS (deterministic D_qk = 128, every D_qk = 192), the
+ * the routes that store dS (deterministic D_qk = 128, every D_qk = 192 or 256), the
  * 16-bit dS tiles of the band of query tiles each 128-key tile visits (the
  * whole rectangle when a bottom-right mask meets per-batch lengths) plus one
  * zero tile; the deterministic-mode turn counters (one int per query tile)
@@ -97,7 +97,10 @@ size_t sdpa_bwd_workspace_size(int B, int H_q, int H_kv, int S_q, int S_kv, int 
  *   D_qk, D_v         head dims; served: D_qk = D_v, any multiple of 8 from 8 to
  *                     128 (up to 64 on the 64-column kernels, above on the
  *                     128-column ones, the columns past D zero-filled by TMA),
- *                     and (192, 128).
+ *                     (192, 128), and (256, 256) (cuDNN frontend docs, "SDPA
+ *                     Backward (SM120)", "Head-size support and tile configs":
+ *                     two work units per key tile, each accumulating half of
+ *                     the dK/dV columns; dS stored as for 192).
  *   scale             softmax scale applied to Q K^T; <= 0 or NaN selects 1/sqrt(D_qk).
  *   causal            1: keep key k for query q only if k <= q + diag + max(window_right, 0).
  *   bottom_right      1: diag = L_kv - L_q (the actual lengths of the batch row);
@@ -110,9 +113,9 @@ size_t sdpa_bwd_workspace_size(int B, int H_q, int H_kv, int S_q, int S_kv, int 
  *                     dQ = scale * dS K over an ascending key walk (larger
  *                     workspace: 2 bytes per visited (query, key) position);
  *                     for other D_qk up to 128 the dQ partials of the KV tiles
- *                     are added in ascending KV-tile order. D_qk = 192 always
- *                     takes the stored-dS route, so its dQ is reproducible in
- *                     both modes. dK and dV are bitwise reproducible in both
+ *                     are added in ascending KV-tile order. D_qk = 192 and 256
+ *                     always take the stored-dS route, so their dQ is
+ *                     reproducible in both modes. dK and dV are bitwise reproducible in both
  *                     modes.
  *   seq_q_lens,       device int32 (B,) per-batch valid lengths, or NULL for
  *   seq_kv_lens       "the full S". Queries at or past seq_q_lens[b] and keys
@@ -200,6 +203,9 @@ int sdpa_bwd_bias(const void* q, const void* k, const void* v, const void* o, co
  * A row with no visible key (queries at or past seq_q_lens[b] included) gets
  * O = 0 and LSE = -inf, or LSE = sink[h] with a sink.
  * Arguments are those of sdpa_bwd() with:
+ *   D_qk, D_v  as sdpa_bwd() except (256, 256): SDPA_ERR_UNSUPPORTED (the
+ *          kernel's two score slots and two O halves fill tensor memory at
+ *          D_v = 128).
  *   o      device bf16 (B, H_q, S_q, D_v) output, 16-byte aligned.
  *   lse    device fp32 (B, H_q, S_q) output, 4-byte aligned.
  *   sink   device fp32 (H_q,) sink logits, or NULL.

@@ -29,6 +29,8 @@ SHAPES = [
       seed=87),                                                                       # partial dK/dV sets
     W("padded_br_det", 2, 2, 2, 190, 260, 128, 128, causal=True, bottom_right=True,
       padded=(1, 260), deterministic=True, seed=88),                                  # full-rectangle band
+    W("d256_gqa_window", 2, 4, 2, 140, 200, 256, 256, causal=True, window_left=60,
+      padded=(1, 140), seed=89),                                                      # D 256, half-column units
 ]
 
 assert pkg.library_path() == os.environ["SDPA_BWD_LIBRARY"]

@@ -84,7 +84,7 @@ def band_tiles(Sq, Skv, causal, br, wl, wr, padded):
 
 
 def route(det, Dqk):
-    return "two" if Dqk == 192 or (det and Dqk == 128) else "reduce"
+    return "two" if Dqk > 128 or (det and Dqk == 128) else "reduce"
 
 
 def carve_size(B, Hq, Hkv, Sq, Skv, Dqk, Dv, rt, causal=0, br=0, wl=-1, wr=-1, padded=0):
@@ -120,6 +120,7 @@ SHAPES = [(1, 2, 2, 128, 128, 64, 64), (2, 16, 16, 2048, 2048, 128, 128),
           (1, 32, 8, 4096, 4096, 128, 128), (3, 4, 1, 300, 177, 128, 128),
           (1, 1, 1, 1, 1, 64, 64), (1, 16, 16, 4096, 4096, 192, 128),
           (2, 4, 2, 300, 177, 192, 128), (2, 4, 2, 300, 177, 32, 32),
+          (2, 4, 2, 300, 177, 256, 256), (1, 8, 8, 4096, 4096, 256, 256),
           (1, 3, 1, 200, 130, 96, 96), (2, 2, 2, 65, 70, 8, 8)]
 MASKS = [dict(), dict(causal=1), dict(causal=1, br=1), dict(causal=1, wl=1024),
          dict(causal=1, wr=100, wl=50), dict(wl=70), dict(causal=1, padded=1),
@@ -218,8 +219,11 @@ def test_argument_validation(lib):
     assert call(lib, Dqk=136, Dv=136) == UNSUPPORTED   # past 128 (other than 192/128)
     assert call(lib, Dqk=128, Dv=64) == UNSUPPORTED
     assert call(lib, Dqk=32, Dv=64) == UNSUPPORTED
-    assert call(lib, Dqk=256, Dv=256) == UNSUPPORTED
+    assert call(lib, Dqk=256, Dv=128) == UNSUPPORTED
     assert call(lib, Dqk=192, Dv=192) == UNSUPPORTED
+    assert call(lib, Dqk=264, Dv=264) == UNSUPPORTED
+    # 256/256 is served: these pointer checks fail only after the head dims pass
+    assert call(lib, Dqk=256, Dv=256, ptrs=[FAKE] * 8 + [None]) == INVALID
     for i in range(9):
         ptrs = [FAKE] * 9
         ptrs[i] = None
@@ -317,6 +321,7 @@ def test_forward_argument_validation(lib):
     assert call_fwd(lib, B=0) == INVALID
     assert call_fwd(lib, Dqk=100, Dv=100) == UNSUPPORTED
     assert call_fwd(lib, Dqk=192, Dv=192) == UNSUPPORTED
+    assert call_fwd(lib, Dqk=256, Dv=256) == UNSUPPORTED  # the backward only
     for i in range(5):
         ptrs = [FAKE] * 5
         ptrs[i] = None

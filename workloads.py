@@ -64,6 +64,10 @@ WORKLOADS: Dict[str, Workload] = {
     # non-causal), for the QAT path; not one of the five above.
     "qat_dense": Workload("qat_dense", B=1, Hq=16, Hkv=16, Sq=4096, Skv=4096, Dqk=128, Dv=128,
                           seed=5),
+    # Head dim 256 (listed among the pages' head sizes), a causal shape of the
+    # same visible-pair count as the S = 4096 workloads above; not one of the five.
+    "d256_causal": Workload("d256_causal", B=1, Hq=16, Hkv=16, Sq=4096, Skv=4096, Dqk=256, Dv=256,
+                            causal=True, seed=6),
 }
 
 ORDER = ["tiny_dense", "causal_mha", "causal_gqa_det", "swa_causal_padded", "mla_br_causal"]
