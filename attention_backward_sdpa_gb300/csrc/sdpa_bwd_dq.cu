@@ -161,12 +161,17 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  pdl_wait_prior_grid();  // the dS tiles (and GQA partials) come from the main kernel
+  // The main kernel lets this grid launch while its last units run (once each
+  // of its CTAs has passed the wait for the preprocess, which clears the ticket
+  // and the zero tile): setup, unit claims and K loads proceed, and the roles
+  // that read the main kernel's output (dS tiles, GQA partial sets) wait for
+  // its completion first.
 
   if (warp == 4) {
     // ------------------------------------------------------------ dS loads, unit claims
     if (lane == 0) {
       int step = 0;
+      bool main_done = false;
       for (int e = 0;; ++e) {
         // The ticket was cleared by the preprocess kernel; on this route the
         // main kernel does not use it.
@@ -187,6 +192,10 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
               !mbar_wait(&dsempty[st], ((step / L::NDS) - 1) & 1, abort_flag, DQ_WAIT_LIMIT_NS))
             goto loads_done;
           uint8_t* stage = smem + L::OFF_DS + st * L::TILE_DS;
+          if (!main_done) {
+            pdl_wait_prior_grid();  // the dS tiles come from the main kernel
+            main_done = true;
+          }
           mbar_arrive_expect_tx(&dsfull[st], L::TILE_DS);
           int lo, hi;
           visited_query_tiles(kt, w.Lq, w.Lk, p.causal, p.bottom_right, p.window_left, p.window_right, lo, hi);
@@ -289,6 +298,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     // pieces left over when the CTA runs out of units are reduced at the end.
     const int n_pieces = (n_units + (int)gridDim.x - 1) / (int)gridDim.x;
     int unit_idx = 0;
+    pdl_wait_prior_grid();  // the GQA partial sets come from the main kernel
     const int row = warp * 32 + lane;          // query within the 128-row unit
     const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
     int done_units = 0;
@@ -344,6 +354,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       gqa_reduce_slice<F16>(p, blockIdx.x, gridDim.x, tid, 128, unit_idx, n_pieces);
   }
 
+  pdl_wait_prior_grid();  // this grid ends after the main kernel's
   tc_fence_before();
   __syncthreads();
   if (*abort_flag && tid == 0) atomicOr(p.status, STATUS_TIMEOUT);

@@ -280,6 +280,17 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int unit = *unit_slot;
+  if constexpr (DS_OUT) {
+    // The dQ kernel may become resident on the SMs this grid's finished units
+    // leave (its setup and first K loads need nothing from here; it waits for
+    // this grid before loading dS). Each thread releases it only after the
+    // preprocess has completed, which clears the dQ kernel's ticket and zero
+    // tile; the producer lane does so after issuing its first loads.
+    if (!(warp == 12 && lane == 0)) {
+      pdl_wait_prior_grid();
+      pdl_launch_dependents();
+    }
+  }
 
   // A unit is one key tile of one head group: gsz query heads of one KV head
   // (group gi = (b * Hkv + hk) * n_part + g covers query heads
@@ -352,6 +363,7 @@ __global__ void __launch_bounds__(MAIN_THREADS, 1)
       for (int blk = 0; blk < D / 64; ++blk)
         tma_load_3d_hint(sV + blk * L::BLK_KV, &maps.v, &bars[BAR_V], blk * 64, k0, b * p.Hkv + hk, pol_v);
       pdl_wait_prior_grid();  // row statistics come from the preprocess kernel
+      if constexpr (DS_OUT) pdl_launch_dependents();
       load_qstat(0);
       for (int t = 1; t < n; ++t) {
         const int st = t % NSTAGE;

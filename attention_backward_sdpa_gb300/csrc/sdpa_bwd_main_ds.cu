@@ -182,6 +182,14 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // The dQ kernel may become resident on the SMs this grid's finished units
+  // leave (it waits for this grid before loading dS). Each thread releases it
+  // only after the preprocess, which clears its ticket and zero tile, has
+  // completed; the producer lane does so after issuing the K/V loads.
+  if (!(warp == 8 && lane == 0)) {
+    pdl_wait_prior_grid();
+    pdl_launch_dependents();
+  }
 
   const int BH = p.B * p.Hq;
   const int half = (int)blockIdx.x % SPLIT;  // accumulated column half (SPLIT = 2)
@@ -222,6 +230,7 @@ __global__ void __launch_bounds__(ds_kernel::THREADS, 1)
       for (int blk = 0; blk < DV / 64; ++blk)
         tma_load_3d(sV + blk * L::BLK_KV, &maps.v, &bars[BAR_KV], blk * 64, k0, b * p.Hkv + hk);
       pdl_wait_prior_grid();
+      pdl_launch_dependents();
       // Q(t) waits for G4(t - NQ), dO(t) for G2 and G3 of tile t - NDO; G3(t - 2)
       // is issued after G4(t - 3), so issuing Q(t) first never delays dO(t).
       for (int t = 0; t < n; ++t) {
