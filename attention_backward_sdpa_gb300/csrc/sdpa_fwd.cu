@@ -30,8 +30,8 @@
 //
 // Warps: 0-7 two softmax warpgroups (a row's keys split between warps w and w+4,
 // which read the same tensor-memory lanes; one warp per SMSP did not hide the
-// instruction latencies), 8 the TMA producer (Q once, K/V stage ring), 9 the MMA
-// issuer and tensor-memory owner, 10-11 idle. Tensor memory: S/P slots at
+// instruction latencies), 8 the TMA producer (Q once, K/V stage ring), 9 the G1
+// issuer and tensor-memory owner, 10 the G2 issuer, 11 idle. Tensor memory: S/P slots at
 // [0,128) and [128,256), O_0 at [256, 256+D_v), O_1 at [384, 384+D_v).
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -229,18 +229,21 @@ __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
           tma_load_3d(sV + blk * L::BLK, &maps.v, full, blk * 64, k0, kvh);
       }
     }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    // Order: G1(0), then for j >= 1: G1(j), G2(j-1); finally G2(n-1). G1(j)
-    // reuses the slot of tile j-3, whose P G2(j-3) read; G2(j-1) needs P(j-1).
+  } else if (warp == 9 || warp == 10) {
+    // ------------------------------------------------------------ MMA issuers
+    // A tcgen05.mma costs its issuing thread on the order of 100 cycles, about
+    // what a 128-column MMA takes on the tensor core, so the 16 MMAs of a tile
+    // are issued by two warps: 9 the score GEMM G1, 10 the PV GEMM G2. G1(j)
+    // reuses the slot of tile j-2, whose P G2(j-2) read; G2(j) needs P(j).
     constexpr uint32_t ID_S = idesc_io(BM, BK, false, false, F16);  // S = Q K^T
     constexpr uint32_t ID_O = idesc_io(BM, DV, false, true, F16);   // O += P V
     constexpr uint64_t T_KMAJ = sdesc_sw128_template(16, 1024);
     constexpr uint64_t T_MN_V = sdesc_sw128_template(L::BLK, 1024);
-    bool ok = n > 0 && mbar_wait(&bars[BAR_QFULL], 0, abort_flag, WAIT_LIMIT_NS);
-    const uint32_t aQ = smem_u32(sQ);
-    for (int j = 0; j <= n && ok; ++j) {
-      if (j < n) {
+    bool ok = n > 0;
+    if (warp == 9) {
+      ok = ok && mbar_wait(&bars[BAR_QFULL], 0, abort_flag, WAIT_LIMIT_NS);
+      const uint32_t aQ = smem_u32(sQ);
+      for (int j = 0; j < n && ok; ++j) {
         const int st = j % NS, s = j % NSLOT;
         ok = mbar_wait(&bars[BAR_KVFULL + st], (j / NS) & 1, abort_flag, WAIT_LIMIT_NS);
         if (ok && j >= NSLOT)
@@ -259,9 +262,14 @@ __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
         }
         __syncwarp();
       }
-      if (j >= 1) {
-        const int u = j - 1, su = u % NSLOT, stu = u % NS;
-        if (!mbar_wait(&bars[BAR_PREADY + su], (u / NSLOT) & 1, abort_flag, WAIT_LIMIT_NS)) break;
+    } else {
+      for (int u = 0; u < n && ok; ++u) {
+        const int su = u % NSLOT, stu = u % NS;
+        // P(u) written implies S(u) computed, so V(u) has landed as well;
+        // waiting on the stage barrier too makes that explicit for this warp.
+        ok = mbar_wait(&bars[BAR_PREADY + su], (u / NSLOT) & 1, abort_flag, WAIT_LIMIT_NS) &&
+             mbar_wait(&bars[BAR_KVFULL + stu], (u / NS) & 1, abort_flag, WAIT_LIMIT_NS);
+        if (!ok) break;
         __syncwarp();
         tc_fence_after();
         if (elect_one()) {
