@@ -218,6 +218,7 @@ struct FwdParams {
   long long bias_bstride;
   int bias_vec;               // rows allow 16-byte loads (S_kv * size % 16 == 0, base aligned)
   float* lse;                 // (B, Hq, Sq) output
+  void* o;                    // (B, Hq, Sq, Dv) output (io type), also behind FwdMaps::o
   int* status;                // device status word
 };
 struct FwdMaps {

@@ -632,6 +632,7 @@ int run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
     p.bias_vec = ((long long)S_kv * esz) % 16 == 0 && reinterpret_cast<uintptr_t>(ba.bias) % 16 == 0;
   }
   p.lse = lse;
+  p.o = o;
   p.status = status;
   FwdMaps maps;
   const long long BHq = (long long)B * H_q, BHkv = (long long)B * H_kv;

@@ -185,6 +185,21 @@ __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
     }
   }
   const int n = kt_hi - kt_lo + 1;  // may be 0
+  if (n <= 0) {
+    // No row of this tile sees a key (every row past the query length, or a
+    // mask that leaves none): O = 0 and LSE = -inf, or the sink logit, written
+    // directly, without setting up barriers or tensor memory. Under padding
+    // most tiles of the shorter batch rows are of this kind.
+    const int rows = min(BM, p.Sq - q0);
+    const long long row0 = (long long)bh * p.Sq + q0;
+    uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + row0 * p.Dv);
+    const int n16 = rows * p.Dv / 8;
+    if (in_bounds(p.status, o, (size_t)n16 * 16, p.o, (size_t)p.B * p.Hq * p.Sq * p.Dv * 2))
+      for (int i = tid; i < n16; i += blockDim.x) o[i] = make_uint4(0u, 0u, 0u, 0u);
+    const float lse_empty = p.sink ? p.sink[h] : -INFINITY;
+    if (tid < rows) p.lse[row0 + tid] = lse_empty;
+    return;
+  }
 
   if (tid == 0) {
     *abort_flag = 0;
