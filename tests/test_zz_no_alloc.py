@@ -7,7 +7,7 @@ by every call and keeping what the previous call left. So the check makes a
 series of calls in a row on different problems, one per dQ route that carves
 its scratch from the array (the fp32 accumulator of the reduction route, the
 ordered relay's counters, the stored dS tiles and the zero tile of the
-two-kernel route, the GQA partial sets), each after a larger call has left
+two-kernel route at head dims 128, 192 and 256, the GQA partial sets), each after a larger call has left
 stale data in the array. Each result is compared with the fp64 oracle and with
 the workspace-taking sdpa_bwd on the same inputs, within the parity tolerance
 of the other tests; deterministic calls must equal sdpa_bwd bit for bit.
@@ -64,6 +64,8 @@ CASES = [
     W("noalloc_mla", 1, 4, 2, 260, 260, 192, 128, causal=True, bottom_right=True, seed=34),
     # the reduction route once more (D 64), after the dS calls
     W("noalloc_dense", 1, 2, 1, 200, 330, 64, 64, seed=35),
+    # head dim 256: stored dS tiles of the half-column units, GQA partial sets
+    W("noalloc_d256", 1, 4, 2, 200, 200, 256, 256, causal=True, window_left=90, seed=36),
 ]
 
 
