@@ -384,13 +384,14 @@ def cpu_baseline_leg(w, t, target_s=12.0):
 MAIN_SOURCES = {"sdpa_bwd_main": ("sdpa_bwd_main.cuh", "common.cuh", "ptx.cuh", "nvfp4.cuh", "bias.cuh"),
                 "sdpa_bwd_main_ds": ("sdpa_bwd_main_ds.cu", "common.cuh", "ptx.cuh", "bias.cuh")}
 MAIN_TRAFFIC = {
-    "ef56c54db91919ba": {"causal_gqa_det": 123785472 + 512181504,
-                         "causal_mha": 114017792 + 31246848,
-                         "swa_causal_padded": 246417920 + 186324992,
-                         "causal_mha/bias-B-f32": 468240384 + 583655680,
-                         "causal_mha/qat": 112624896 + 28589568},
-    "fea0e1085973a768": {"mla_br_causal": 132064000 + 263953920,
-                         "mla_br_causal/bias-B-bf16": 423545856 + 1330964736},
+    "d37336d80f5254fa": {"causal_gqa_det": 134370304 + 513630464,
+                         "causal_mha": 103112192 + 15115008,
+                         "swa_causal_padded": 228067840 + 158214912,
+                         "causal_mha/bias-B-f32": 456930816 + 540702464,
+                         "causal_mha/qat": 102860544 + 14223872},
+    "ffd89974697c001e": {"mla_br_causal": 132089088 + 263580416,
+                         "mla_br_causal/bias-B-bf16": 430743808 + 1331224064,
+                         "d256_causal": 302962176 + 301679616},
 }
 
 
