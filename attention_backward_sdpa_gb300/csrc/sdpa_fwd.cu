@@ -53,6 +53,11 @@ constexpr float RESCALE_THRESHOLD = 8.f;  // log2 units
 constexpr int NSLOT = 2;                  // S/P slots in tensor memory
 constexpr int FWD_SLOTS_HOST = 64;        // launch slots of the persistent form's tickets
 
+// Register split: launched with 168 per thread (384 threads), the control
+// warpgroup (warps 8-11) drops to 56 and the two softmax warpgroups grow to 224:
+// 128 x (56 + 224 + 224) = 64,512 = 384 x 168.
+constexpr uint32_t REGS_CTRL = 56, REGS_SOFTMAX = 224;
+static_assert(128 * (REGS_CTRL + 2 * REGS_SOFTMAX) <= THREADS * 168, "register split");
 constexpr int RING = 4;           // items published by the producer (persistent form)
 constexpr int RING_READERS = 10;  // warps that read them: 0-7, 9 and 10
 
@@ -266,127 +271,132 @@ __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
   // stage ring, the two S/P slots and their barrier phases run on across items;
   // ni counts the items with at least one key tile (the Q buffer's phases).
   // Items whose rows see no key are written by the softmax warps alone.
-  if (warp == 8) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+  if (warp >= 8) {
+    // Producer and MMA issuers need few registers; the softmax warpgroups get them.
+    regs_decrease<REGS_CTRL>();
+    if (warp == 8) {
+      // ------------------------------------------------------------ TMA producer
+      if (lane == 0) {
+        int g = 0, ni = 0;
+        bool ok = true;
+        auto load_kv = [&](const FwdItem& w, int j) -> bool {
+          const int st = g % NS;
+          if (g >= NS && !mbar_wait(&bars[BAR_KVEMPTY + st], ((g / NS) - 1) & 1, abort_flag, WAIT_LIMIT_NS))
+            return false;
+          const int k0 = (w.kt_lo + j) * BK;
+          uint8_t* sK = sKV + st * L::STAGE;
+          uint8_t* sV = sK + L::TILE_K;
+          uint64_t* full = &bars[BAR_KVFULL + st];
+          mbar_arrive_expect_tx(full, L::STAGE);
+          for (int blk = 0; blk < DQK / 64; ++blk) tma_load_3d(sK + blk * L::BLK, &maps.k, full, blk * 64, k0, w.kvh);
+          for (int blk = 0; blk < DV / 64; ++blk) tma_load_3d(sV + blk * L::BLK, &maps.v, full, blk * 64, k0, w.kvh);
+          ++g;
+          return true;
+        };
+        for (int e = 0; e < E_MAX && ok; ++e) {
+          int it;
+          if constexpr (PERSIST) {
+            // Take the next item and publish it to the other roles.
+            const int r = e % RING;
+            if (e >= RING && !mbar_wait(&bars[BAR_REMPTY + r], ((e / RING) - 1) & 1, abort_flag, WAIT_LIMIT_NS))
+              break;
+            it = atomicAdd(&g_fwd_ticket[ticket_slot], 1);
+            if (it >= n_items) it = -1;
+            ring[r] = it;
+            mbar_arrive(&bars[BAR_RFULL + r]);
+          } else {
+            it = e == 0 ? (int)blockIdx.x : -1;
+          }
+          if (it < 0) break;
+          const FwdItem w = fwd_item(p, it);
+          if (w.n <= 0) continue;
+          // The item's first key tiles only wait for stages that earlier items
+          // release, so they load before its Q, which waits for the previous
+          // item's last G1; later tiles wait for stages this item releases,
+          // which needs its Q first.
+          const int pre = w.n < NS ? w.n : NS;
+          for (int j = 0; j < pre && ok; ++j) ok = load_kv(w, j);
+          if (ok && ni >= 1) ok = mbar_wait(&bars[BAR_QEMPTY], (ni - 1) & 1, abort_flag, WAIT_LIMIT_NS);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&bars[BAR_QFULL], L::TILE_Q);
+          for (int blk = 0; blk < DQK / 64; ++blk)
+            tma_load_3d(sQ + blk * L::BLK, &maps.q, &bars[BAR_QFULL], blk * 64, w.q0, w.bh);
+          for (int j = pre; j < w.n && ok; ++j) ok = load_kv(w, j);
+          ++ni;
+        }
+      }
+    } else if (warp == 9 || warp == 10) {
+      // ------------------------------------------------------------ MMA issuers
+      // A tcgen05.mma costs its issuing thread on the order of 100 cycles, about
+      // what a 128-column MMA takes on the tensor core, so the 16 MMAs of a tile
+      // are issued by two warps: 9 the score GEMM G1, 10 the PV GEMM G2. G1 of
+      // tile g reuses the slot of tile g-2, whose P G2(g-2) read; G2(g) needs P(g).
+      constexpr uint32_t ID_S = idesc_io(BM, BK, false, false, F16);  // S = Q K^T
+      constexpr uint32_t ID_O = idesc_io(BM, DV, false, true, F16);   // O += P V
+      constexpr uint64_t T_KMAJ = sdesc_sw128_template(16, 1024);
+      constexpr uint64_t T_MN_V = sdesc_sw128_template(L::BLK, 1024);
       int g = 0, ni = 0;
       bool ok = true;
-      auto load_kv = [&](const FwdItem& w, int j) -> bool {
-        const int st = g % NS;
-        if (g >= NS && !mbar_wait(&bars[BAR_KVEMPTY + st], ((g / NS) - 1) & 1, abort_flag, WAIT_LIMIT_NS))
-          return false;
-        const int k0 = (w.kt_lo + j) * BK;
-        uint8_t* sK = sKV + st * L::STAGE;
-        uint8_t* sV = sK + L::TILE_K;
-        uint64_t* full = &bars[BAR_KVFULL + st];
-        mbar_arrive_expect_tx(full, L::STAGE);
-        for (int blk = 0; blk < DQK / 64; ++blk) tma_load_3d(sK + blk * L::BLK, &maps.k, full, blk * 64, k0, w.kvh);
-        for (int blk = 0; blk < DV / 64; ++blk) tma_load_3d(sV + blk * L::BLK, &maps.v, full, blk * 64, k0, w.kvh);
-        ++g;
-        return true;
-      };
+      const uint32_t aQ = smem_u32(sQ);
       for (int e = 0; e < E_MAX && ok; ++e) {
-        int it;
-        if constexpr (PERSIST) {
-          // Take the next item and publish it to the other roles.
-          const int r = e % RING;
-          if (e >= RING && !mbar_wait(&bars[BAR_REMPTY + r], ((e / RING) - 1) & 1, abort_flag, WAIT_LIMIT_NS))
-            break;
-          it = atomicAdd(&g_fwd_ticket[ticket_slot], 1);
-          if (it >= n_items) it = -1;
-          ring[r] = it;
-          mbar_arrive(&bars[BAR_RFULL + r]);
-        } else {
-          it = e == 0 ? (int)blockIdx.x : -1;
-        }
+        const int it = next_item(e);
         if (it < 0) break;
         const FwdItem w = fwd_item(p, it);
         if (w.n <= 0) continue;
-        // The item's first key tiles only wait for stages that earlier items
-        // release, so they load before its Q, which waits for the previous
-        // item's last G1; later tiles wait for stages this item releases,
-        // which needs its Q first.
-        const int pre = w.n < NS ? w.n : NS;
-        for (int j = 0; j < pre && ok; ++j) ok = load_kv(w, j);
-        if (ok && ni >= 1) ok = mbar_wait(&bars[BAR_QEMPTY], (ni - 1) & 1, abort_flag, WAIT_LIMIT_NS);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&bars[BAR_QFULL], L::TILE_Q);
-        for (int blk = 0; blk < DQK / 64; ++blk)
-          tma_load_3d(sQ + blk * L::BLK, &maps.q, &bars[BAR_QFULL], blk * 64, w.q0, w.bh);
-        for (int j = pre; j < w.n && ok; ++j) ok = load_kv(w, j);
+        if (warp == 9) {
+          ok = mbar_wait(&bars[BAR_QFULL], ni & 1, abort_flag, WAIT_LIMIT_NS);
+          for (int j = 0; j < w.n && ok; ++j, ++g) {
+            const int st = g % NS, s = g % NSLOT;
+            ok = mbar_wait(&bars[BAR_KVFULL + st], (g / NS) & 1, abort_flag, WAIT_LIMIT_NS);
+            if (ok && g >= NSLOT)
+              ok = mbar_wait(&bars[BAR_PVDONE + s], ((g - NSLOT) / NSLOT) & 1, abort_flag, WAIT_LIMIT_NS);
+            if (!ok) break;
+            __syncwarp();
+            tc_fence_after();
+            if (elect_one()) {
+              const uint32_t aK = smem_u32(sKV + st * L::STAGE);
+  #pragma unroll
+              for (int k = 0; k < DQK / 16; ++k) {
+                const uint32_t ko = (k >> 2) * L::BLK + (k & 3) * 32;
+                mma_ss(tmem + 128u * s, sdesc_at(T_KMAJ, aQ + ko), sdesc_at(T_KMAJ, aK + ko), ID_S, k > 0);
+              }
+              mma_commit(&bars[BAR_SFULL + s]);
+              // After the item's last G1 the Q buffer takes the next item's Q.
+              if (j == w.n - 1) mma_commit(&bars[BAR_QEMPTY]);
+            }
+            __syncwarp();
+          }
+        } else {
+          for (int u = 0; u < w.n && ok; ++u, ++g) {
+            const int su = g % NSLOT, stu = g % NS;
+            // P(g) written implies S(g) computed, so V(g) has landed as well;
+            // waiting on the stage barrier too makes that explicit for this warp.
+            // (The previous item's epilogue has read O before any P of this item
+            // is written: the same threads do both, in that order.)
+            ok = mbar_wait(&bars[BAR_PREADY + su], (g / NSLOT) & 1, abort_flag, WAIT_LIMIT_NS) &&
+                 mbar_wait(&bars[BAR_KVFULL + stu], (g / NS) & 1, abort_flag, WAIT_LIMIT_NS);
+            if (!ok) break;
+            __syncwarp();
+            tc_fence_after();
+            if (elect_one()) {
+              const uint32_t aV = smem_u32(sKV + stu * L::STAGE + L::TILE_K);
+              // O_h += P[:, keys of half h] V[keys of half h, :]; P of half h sits in
+              // the slot's columns [64 h, 64 h + 32).
+  #pragma unroll
+              for (int k = 0; k < BK / 16; ++k)
+                mma_ts(tmem + L::COL_O + 128u * (k >> 2), tmem + 128u * su + 64u * (k >> 2) + 8 * (k & 3),
+                       sdesc_at(T_MN_V, aV + k * 2048), ID_O, (u > 0 || (k & 3) > 0));
+              mma_commit(&bars[BAR_PVDONE + su]);
+              mma_commit(&bars[BAR_KVEMPTY + stu]);
+            }
+            __syncwarp();
+          }
+        }
         ++ni;
       }
     }
-  } else if (warp == 9 || warp == 10) {
-    // ------------------------------------------------------------ MMA issuers
-    // A tcgen05.mma costs its issuing thread on the order of 100 cycles, about
-    // what a 128-column MMA takes on the tensor core, so the 16 MMAs of a tile
-    // are issued by two warps: 9 the score GEMM G1, 10 the PV GEMM G2. G1 of
-    // tile g reuses the slot of tile g-2, whose P G2(g-2) read; G2(g) needs P(g).
-    constexpr uint32_t ID_S = idesc_io(BM, BK, false, false, F16);  // S = Q K^T
-    constexpr uint32_t ID_O = idesc_io(BM, DV, false, true, F16);   // O += P V
-    constexpr uint64_t T_KMAJ = sdesc_sw128_template(16, 1024);
-    constexpr uint64_t T_MN_V = sdesc_sw128_template(L::BLK, 1024);
-    int g = 0, ni = 0;
-    bool ok = true;
-    const uint32_t aQ = smem_u32(sQ);
-    for (int e = 0; e < E_MAX && ok; ++e) {
-      const int it = next_item(e);
-      if (it < 0) break;
-      const FwdItem w = fwd_item(p, it);
-      if (w.n <= 0) continue;
-      if (warp == 9) {
-        ok = mbar_wait(&bars[BAR_QFULL], ni & 1, abort_flag, WAIT_LIMIT_NS);
-        for (int j = 0; j < w.n && ok; ++j, ++g) {
-          const int st = g % NS, s = g % NSLOT;
-          ok = mbar_wait(&bars[BAR_KVFULL + st], (g / NS) & 1, abort_flag, WAIT_LIMIT_NS);
-          if (ok && g >= NSLOT)
-            ok = mbar_wait(&bars[BAR_PVDONE + s], ((g - NSLOT) / NSLOT) & 1, abort_flag, WAIT_LIMIT_NS);
-          if (!ok) break;
-          __syncwarp();
-          tc_fence_after();
-          if (elect_one()) {
-            const uint32_t aK = smem_u32(sKV + st * L::STAGE);
-#pragma unroll
-            for (int k = 0; k < DQK / 16; ++k) {
-              const uint32_t ko = (k >> 2) * L::BLK + (k & 3) * 32;
-              mma_ss(tmem + 128u * s, sdesc_at(T_KMAJ, aQ + ko), sdesc_at(T_KMAJ, aK + ko), ID_S, k > 0);
-            }
-            mma_commit(&bars[BAR_SFULL + s]);
-            // After the item's last G1 the Q buffer takes the next item's Q.
-            if (j == w.n - 1) mma_commit(&bars[BAR_QEMPTY]);
-          }
-          __syncwarp();
-        }
-      } else {
-        for (int u = 0; u < w.n && ok; ++u, ++g) {
-          const int su = g % NSLOT, stu = g % NS;
-          // P(g) written implies S(g) computed, so V(g) has landed as well;
-          // waiting on the stage barrier too makes that explicit for this warp.
-          // (The previous item's epilogue has read O before any P of this item
-          // is written: the same threads do both, in that order.)
-          ok = mbar_wait(&bars[BAR_PREADY + su], (g / NSLOT) & 1, abort_flag, WAIT_LIMIT_NS) &&
-               mbar_wait(&bars[BAR_KVFULL + stu], (g / NS) & 1, abort_flag, WAIT_LIMIT_NS);
-          if (!ok) break;
-          __syncwarp();
-          tc_fence_after();
-          if (elect_one()) {
-            const uint32_t aV = smem_u32(sKV + stu * L::STAGE + L::TILE_K);
-            // O_h += P[:, keys of half h] V[keys of half h, :]; P of half h sits in
-            // the slot's columns [64 h, 64 h + 32).
-#pragma unroll
-            for (int k = 0; k < BK / 16; ++k)
-              mma_ts(tmem + L::COL_O + 128u * (k >> 2), tmem + 128u * su + 64u * (k >> 2) + 8 * (k & 3),
-                     sdesc_at(T_MN_V, aV + k * 2048), ID_O, (u > 0 || (k & 3) > 0));
-            mma_commit(&bars[BAR_PVDONE + su]);
-            mma_commit(&bars[BAR_KVEMPTY + stu]);
-          }
-          __syncwarp();
-        }
-      }
-      ++ni;
-    }
-  } else if (warp < 8) {
+  } else {
+    regs_increase<REGS_SOFTMAX>();
     // ------------------------------------------------------------ softmax warpgroups
     // Warps w and w + 4 read the same tensor-memory lanes (w % 4): warpgroup
     // `half` takes keys [64 half, 64 half + 64) of each tile. Each half keeps a
@@ -676,9 +686,7 @@ __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
 
 template <int DQK, int DV, bool BIAS, bool F16>
 static cudaError_t set_fwd_smem() {
-  // Without a bias the persistent form runs; the biased one keeps one item per CTA
-  // (the item loop's state pushed its bias path into register spills).
-  return cudaFuncSetAttribute(sdpa_fwd_kernel<DQK, DV, BIAS, F16, !BIAS>,
+  return cudaFuncSetAttribute(sdpa_fwd_kernel<DQK, DV, BIAS, F16, true>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, fwd_kernel::Layout<DQK, DV>::BYTES);
 }
 
@@ -701,9 +709,9 @@ cudaError_t fwd_kernel_setup() {
 template <bool BIAS, bool F16>
 static cudaError_t launch_fwd_variant(const FwdMaps& maps, const FwdParams& p, cudaStream_t s, int sms,
                                       int slot) {
-  // Without a bias: persistent, one CTA per SM (more than half its shared memory
-  // each) taking items from the launch's ticket; with a bias one CTA per item.
-  constexpr bool PERSIST = !BIAS;
+  // Persistent: one CTA per SM (more than half its shared memory each) taking
+  // items from the launch's ticket.
+  constexpr bool PERSIST = true;
   const long long items = (long long)p.n_qt * p.B * p.Hq;
   const dim3 grid((unsigned)(PERSIST ? (items < sms ? items : sms) : items));
   const dim3 block(fwd_kernel::THREADS);
