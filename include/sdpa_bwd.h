@@ -209,8 +209,12 @@ int sdpa_bwd_bias(const void* q, const void* k, const void* v, const void* o, co
  *   o      device bf16 (B, H_q, S_q, D_v) output, 16-byte aligned.
  *   lse    device fp32 (B, H_q, S_q) output, 4-byte aligned.
  *   sink   device fp32 (H_q,) sink logits, or NULL.
- * No workspace. Returns SDPA_OK once the kernel is enqueued on `stream`, else an
- * error code (nothing enqueued); a device-side timeout is reported by
+ * No workspace. The kernel is persistent (one CTA per SM) and takes its work
+ * items from a counter in the library's device memory; the library hands out
+ * 64 such counters in turn, so more than 64 forward launches running at once on
+ * one device (on different streams) could share one and must not be issued.
+ * Returns SDPA_OK once the kernel is enqueued on `stream`, else an error code
+ * (nothing enqueued); a device-side timeout is reported by
  * sdpa_bwd_check_device_status().
  */
 int sdpa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
