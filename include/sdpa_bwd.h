@@ -212,7 +212,9 @@ int sdpa_bwd_bias(const void* q, const void* k, const void* v, const void* o, co
  * No workspace. The kernel is persistent (one CTA per SM) and takes its work
  * items from a counter in the library's device memory; the library hands out
  * 64 such counters in turn, so more than 64 forward launches running at once on
- * one device (on different streams) could share one and must not be issued.
+ * one device (on different streams) could share one and must not be issued; a
+ * CUDA graph that captured a forward launch reuses its counter on every replay,
+ * so two replays of that graph must not run at the same time.
  * Returns SDPA_OK once the kernel is enqueued on `stream`, else an error code
  * (nothing enqueued); a device-side timeout is reported by
  * sdpa_bwd_check_device_status().
