@@ -584,9 +584,8 @@ int run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   int rc = basic_checks(B, H_q, H_kv, S_q, S_kv, D_qk, D_v);
   if (rc != SDPA_OK) return rc;
-  // The forward kernel keeps two S slots and two O halves in tensor memory,
-  // which leaves room for D_v up to 128 (and the MLA pair).
-  if (D_v > 128) return SDPA_ERR_UNSUPPORTED;
+  // Every pair the backward serves: D_v up to 128 (and the MLA pair) on the
+  // kernel with two O halves in tensor memory, 256/256 on the one with a single O.
   if (!q || !k || !v || !o || !lse) return SDPA_ERR_INVALID;
   for (const void* ptr : {q, k, v, (const void*)o})
     if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return SDPA_ERR_ALIGN;

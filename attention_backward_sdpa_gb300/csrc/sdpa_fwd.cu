@@ -38,20 +38,18 @@
 
 #include <atomic>
 
-#include "common.cuh"
-#include "ptx.cuh"
+#include "sdpa_fwd.cuh"
 
 namespace sdpa {
 
 namespace fwd_kernel {
 
 constexpr int THREADS = 384;
-constexpr int BM = 128;  // query rows per CTA
-constexpr int BK = 128;  // keys per tile
-constexpr uint64_t WAIT_LIMIT_NS = 4000000000ull;
-constexpr float RESCALE_THRESHOLD = 8.f;  // log2 units
-constexpr int NSLOT = 2;                  // S/P slots in tensor memory
-constexpr int FWD_SLOTS_HOST = 64;        // launch slots of the persistent form's tickets
+using fwd_shared::BM;
+using fwd_shared::BK;
+using fwd_shared::WAIT_LIMIT_NS;
+using fwd_shared::RESCALE_THRESHOLD;
+constexpr int NSLOT = 2;  // S/P slots in tensor memory
 
 // Register split: launched with 168 per thread (384 threads), the control
 // warpgroup (warps 8-11) drops to 56 and the two softmax warpgroups grow to 224:
@@ -59,7 +57,7 @@ constexpr int FWD_SLOTS_HOST = 64;        // launch slots of the persistent form
 constexpr uint32_t REGS_CTRL = 56, REGS_SOFTMAX = 224;
 static_assert(128 * (REGS_CTRL + 2 * REGS_SOFTMAX) <= THREADS * 168, "register split");
 constexpr int RING = 4;           // items published by the producer (persistent form)
-constexpr int RING_READERS = 10;  // warps that read them: 0-7, 9 and 10
+constexpr int RING_READERS = 3;   // warps that read them: 0 (for warps 0-7), 9 and 10
 
 enum : int {
   BAR_QFULL = 0,                 // the item's Q tile landed
@@ -103,106 +101,12 @@ struct Layout {
 
 }  // namespace fwd_kernel
 
-// This row's bias for keys kb .. kb + 63 as 32-bit words: on the 16-byte path
-// 16-bit pairs (`packed`, 32 words) or fp32 values (64 words); otherwise fp32
-// values from scalar loads, 0 past S_kv.
-__device__ __forceinline__ void load_fwd_bias_row(const FwdParams& p, long long row_off, int kb, bool live,
-                                                  uint32_t (&raw)[64], bool& packed) {
-  const bool vec = p.bias_vec && kb + 64 <= p.Skv;  // uniform across the warp
-  packed = vec && !p.bias_fp32;
-  if (!live) {
-#pragma unroll
-    for (int i = 0; i < 64; ++i) raw[i] = 0u;
-    return;
-  }
-  if (vec) {
-    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const char*>(p.bias) +
-                                                      (row_off + kb) * (p.bias_fp32 ? 4 : 2));
-    if (p.bias_fp32) {
-#pragma unroll
-      for (int v = 0; v < 16; ++v) {
-        const uint4 x = __ldcs(src + v);
-        raw[4 * v] = x.x; raw[4 * v + 1] = x.y; raw[4 * v + 2] = x.z; raw[4 * v + 3] = x.w;
-      }
-    } else {
-#pragma unroll
-      for (int v = 0; v < 8; ++v) {
-        const uint4 x = __ldcs(src + v);
-        raw[4 * v] = x.x; raw[4 * v + 1] = x.y; raw[4 * v + 2] = x.z; raw[4 * v + 3] = x.w;
-      }
-#pragma unroll
-      for (int i = 32; i < 64; ++i) raw[i] = 0u;
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 64; ++i) {
-      float x = 0.f;
-      if (kb + i < p.Skv)
-        x = p.bias_fp32 ? __ldcs(static_cast<const float*>(p.bias) + row_off + kb + i)
-                        : bias16_to_f32(__ldcs(static_cast<const unsigned short*>(p.bias) + row_off + kb + i),
-                                        p.bias_f16 != 0);
-      raw[i] = __float_as_uint(x);
-    }
-  }
-}
-
-// One work item: 128 query rows (query tile qt, descending so that under a
-// causal mask the longest items come first) of one (batch, query head), and the
-// range [kt_lo, kt_lo + n) of 128-key tiles that any of its live rows sees.
-struct FwdItem {
-  int qt, bh, h, kvh, q0, Lq, Lk, kt_lo, n;
-  long long diag;
-};
-
-__device__ __forceinline__ FwdItem fwd_item(const FwdParams& p, int it) {
-  FwdItem w;
-  const int BH = p.B * p.Hq;
-  w.qt = p.n_qt - 1 - it / BH;
-  w.bh = it % BH;
-  const int b = w.bh / p.Hq;
-  w.h = w.bh % p.Hq;
-  w.kvh = b * p.Hkv + w.h / p.G;
-  w.q0 = w.qt * fwd_kernel::BM;
-  w.Lq = p.Sq;
-  w.Lk = p.Skv;
-  if (p.seq_q_lens) w.Lq = min(max(p.seq_q_lens[b], 0), p.Sq);
-  if (p.seq_kv_lens) w.Lk = min(max(p.seq_kv_lens[b], 0), p.Skv);
-  w.diag = p.bottom_right ? (long long)w.Lk - w.Lq : 0;
-  const long long Rp = p.window_right > 0 ? p.window_right : 0;
-  int kt_lo = 0, kt_hi = -1;
-  const long long q_last = min(w.q0 + fwd_kernel::BM, w.Lq) - 1;
-  if (w.q0 < w.Lq && w.Lk > 0) {
-    long long k_hi = w.Lk - 1, k_lo = 0;
-    if (p.causal) k_hi = min(k_hi, q_last + w.diag + Rp);
-    if (p.window_left >= 0) k_lo = max(0ll, (long long)w.q0 + w.diag - p.window_left);
-    if (k_lo <= k_hi) {
-      kt_lo = (int)(k_lo / fwd_kernel::BK);
-      kt_hi = (int)(k_hi / fwd_kernel::BK);
-    }
-  }
-  w.kt_lo = kt_lo;
-  w.n = kt_hi - kt_lo + 1;  // may be 0
-  return w;
-}
-
-// Named barrier over nthreads threads that also ORs a predicate over them.
-__device__ __forceinline__ bool named_bar_sync_or(uint32_t id, uint32_t nthreads, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\tbar.red.or.pred po, %2, %3, pi;\n\t"
-      "selp.u32 %0, 1, 0, po;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
-      : "memory");
-  return r != 0;
-}
-
 // Work tickets of the persistent forward (PERSIST), one counter pair per launch
 // slot: a CTA's producer takes items (longest first) from g_fwd_ticket[slot], and
 // the last CTA to finish puts both counters back to zero for the slot's next
 // launch. The host hands out the 64 slots in turn, so launches share a counter
 // only if 64 forward launches run on one device at once.
-constexpr int FWD_SLOTS = fwd_kernel::FWD_SLOTS_HOST;
+constexpr int FWD_SLOTS = fwd_shared::FWD_SLOTS;
 __device__ int g_fwd_ticket[FWD_SLOTS];
 __device__ int g_fwd_done[FWD_SLOTS];
 
@@ -229,20 +133,25 @@ __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
   volatile int* ring = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 16);  // [RING] items
+  volatile int* sitem = ring + RING;  // [2] the softmax warpgroups' current item, by parity
   const int n_items = p.n_qt * p.B * p.Hq;
   // Items a CTA walks at most: one without PERSIST, so that the compiler sees
   // a single pass and keeps no state across items.
   constexpr int E_MAX = PERSIST ? 0x7fffffff : 1;
-  // Item e of this CTA, for every role but the producer: from the ring the
-  // producer fills (PERSIST), else blockIdx.x then the end (-1).
+  // Item e of this CTA, for a whole warp: from the ring the producer fills
+  // (PERSIST; lane 0 waits, reads and releases the entry, and hands the item to
+  // the other lanes), else blockIdx.x then the end (-1).
   auto next_item = [&](int e) -> int {
     if constexpr (!PERSIST) return e == 0 ? (int)blockIdx.x : -1;
-    const int r = e % RING;
-    if (!mbar_wait(&bars[BAR_RFULL + r], (e / RING) & 1, abort_flag, WAIT_LIMIT_NS)) return -1;
-    const int it = ring[r];
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(&bars[BAR_REMPTY + r]);
-    return it;
+    int it = -1;
+    if ((threadIdx.x & 31) == 0) {
+      const int r = e % RING;
+      if (mbar_wait(&bars[BAR_RFULL + r], (e / RING) & 1, abort_flag, WAIT_LIMIT_NS)) {
+        it = ring[r];
+        mbar_arrive(&bars[BAR_REMPTY + r]);
+      }
+    }
+    return __shfl_sync(0xffffffffu, it, 0);
   };
 
   if (tid == 0) {
@@ -418,8 +327,28 @@ __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
     const size_t o_bytes = (size_t)p.B * p.Hq * p.Sq * p.Dv * 2;
     int g = 0;
     bool ok = true;
+    bool have_next = false;  // the item for this e was taken during the previous epilogue
     for (int e = 0; e < E_MAX && ok; ++e) {
-      const int it = next_item(e);
+      // Warp 0 takes the item for all eight warps, so that they never disagree
+      // on it (a wait that gives up can do so in one reader and not in another)
+      // and meet at the same named barriers: during the previous item's
+      // epilogue, whose barrier hands it over, else here with a barrier of its
+      // own. Double-buffered by parity: a slot is rewritten only after a later
+      // barrier that every reader of it has passed.
+      int it;
+      if constexpr (PERSIST) {
+        if (!have_next) {
+          if (warp == 0) {
+            const int t = next_item(e);
+            if (lane == 0) sitem[e & 1] = t;
+          }
+          named_bar_sync(3, 256);
+        }
+        have_next = false;
+        it = sitem[e & 1];
+      } else {
+        it = next_item(e);
+      }
       if (it < 0) break;
       const FwdItem w = fwd_item(p, it);
       const int q = w.q0 + row;
@@ -615,6 +544,14 @@ __global__ void __launch_bounds__(fwd_kernel::THREADS, 1)
       if (warp_ok) tc_fence_after();
       xch[half * 128 + row] = m;
       xch[256 + half * 128 + row] = l;
+      if constexpr (PERSIST) {
+        // The next item, handed to every softmax warp by the barrier below.
+        if (warp == 0) {
+          const int t = next_item(e + 1);
+          if (lane == 0) sitem[(e + 1) & 1] = t;
+        }
+        have_next = true;
+      }
       // Every softmax thread learns whether any of them gave up, so that all
       // leave the item loop together after this epilogue.
       const bool any_fail = named_bar_sync_or(1, 256, !warp_ok);
@@ -703,6 +640,7 @@ cudaError_t fwd_kernel_setup() {
   if (e == cudaSuccess) e = fwd_setup_variant<true, false>();
   if (e == cudaSuccess) e = fwd_setup_variant<false, true>();
   if (e == cudaSuccess) e = fwd_setup_variant<true, true>();
+  if (e == cudaSuccess) e = fwd_wide_setup();
   return e;
 }
 
@@ -731,11 +669,13 @@ static cudaError_t launch_fwd_variant(const FwdMaps& maps, const FwdParams& p, c
 
 cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, cudaStream_t s) {
   static std::atomic<unsigned> next_slot{0};
-  const int slot = (int)(next_slot.fetch_add(1, std::memory_order_relaxed) % fwd_kernel::FWD_SLOTS_HOST);
+  const int slot = (int)(next_slot.fetch_add(1, std::memory_order_relaxed) % fwd_shared::FWD_SLOTS);
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
     return cudaErrorInvalidValue;
+  // Head dim 256: the kernel with one shared O accumulator (sdpa_fwd_wide.cu).
+  if (p.Dqk == 256 && p.Dv == 256) return launch_fwd_wide(maps, p, s, sms, slot);
   if (p.bias)
     return p.f16 ? launch_fwd_variant<true, true>(maps, p, s, sms, slot)
                  : launch_fwd_variant<true, false>(maps, p, s, sms, slot);

@@ -1,0 +1,124 @@
+// sdpa_fwd.cuh -- what the two forward kernels share: the work-item decode of
+// the persistent schedule, the bias row loader, a named barrier that also ORs a
+// predicate, the constants of the schedule, and the launcher of the head-dim-256
+// kernel (sdpa_fwd_wide.cu), which launch_fwd (sdpa_fwd.cu) calls for D = 256.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace sdpa {
+
+namespace fwd_shared {
+constexpr int BM = 128;  // query rows per item
+constexpr int BK = 128;  // keys per tile
+constexpr uint64_t WAIT_LIMIT_NS = 4000000000ull;
+constexpr float RESCALE_THRESHOLD = 8.f;  // log2 units: P stays below 2^8 until a raise
+constexpr int FWD_SLOTS = 64;             // launch slots of the persistent tickets
+}  // namespace fwd_shared
+
+// This row's bias for keys kb .. kb + 63 as 32-bit words: on the 16-byte path
+// 16-bit pairs (`packed`, 32 words) or fp32 values (64 words); otherwise fp32
+// values from scalar loads, 0 past S_kv.
+__device__ __forceinline__ void load_fwd_bias_row(const FwdParams& p, long long row_off, int kb, bool live,
+                                                  uint32_t (&raw)[64], bool& packed) {
+  const bool vec = p.bias_vec && kb + 64 <= p.Skv;  // uniform across the warp
+  packed = vec && !p.bias_fp32;
+  if (!live) {
+#pragma unroll
+    for (int i = 0; i < 64; ++i) raw[i] = 0u;
+    return;
+  }
+  if (vec) {
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const char*>(p.bias) +
+                                                      (row_off + kb) * (p.bias_fp32 ? 4 : 2));
+    if (p.bias_fp32) {
+#pragma unroll
+      for (int v = 0; v < 16; ++v) {
+        const uint4 x = __ldcs(src + v);
+        raw[4 * v] = x.x; raw[4 * v + 1] = x.y; raw[4 * v + 2] = x.z; raw[4 * v + 3] = x.w;
+      }
+    } else {
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const uint4 x = __ldcs(src + v);
+        raw[4 * v] = x.x; raw[4 * v + 1] = x.y; raw[4 * v + 2] = x.z; raw[4 * v + 3] = x.w;
+      }
+#pragma unroll
+      for (int i = 32; i < 64; ++i) raw[i] = 0u;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+      float x = 0.f;
+      if (kb + i < p.Skv)
+        x = p.bias_fp32 ? __ldcs(static_cast<const float*>(p.bias) + row_off + kb + i)
+                        : bias16_to_f32(__ldcs(static_cast<const unsigned short*>(p.bias) + row_off + kb + i),
+                                        p.bias_f16 != 0);
+      raw[i] = __float_as_uint(x);
+    }
+  }
+}
+
+// One work item: 128 query rows (query tile qt, descending so that under a
+// causal mask the longest items come first) of one (batch, query head), and the
+// range [kt_lo, kt_lo + n) of 128-key tiles that any of its live rows sees.
+struct FwdItem {
+  int qt, bh, h, kvh, q0, Lq, Lk, kt_lo, n;
+  long long diag;
+};
+
+__device__ __forceinline__ FwdItem fwd_item(const FwdParams& p, int it) {
+  FwdItem w;
+  const int BH = p.B * p.Hq;
+  w.qt = p.n_qt - 1 - it / BH;
+  w.bh = it % BH;
+  const int b = w.bh / p.Hq;
+  w.h = w.bh % p.Hq;
+  w.kvh = b * p.Hkv + w.h / p.G;
+  w.q0 = w.qt * fwd_shared::BM;
+  w.Lq = p.Sq;
+  w.Lk = p.Skv;
+  if (p.seq_q_lens) w.Lq = min(max(p.seq_q_lens[b], 0), p.Sq);
+  if (p.seq_kv_lens) w.Lk = min(max(p.seq_kv_lens[b], 0), p.Skv);
+  w.diag = p.bottom_right ? (long long)w.Lk - w.Lq : 0;
+  const long long Rp = p.window_right > 0 ? p.window_right : 0;
+  int kt_lo = 0, kt_hi = -1;
+  const long long q_last = min(w.q0 + fwd_shared::BM, w.Lq) - 1;
+  if (w.q0 < w.Lq && w.Lk > 0) {
+    long long k_hi = w.Lk - 1, k_lo = 0;
+    if (p.causal) k_hi = min(k_hi, q_last + w.diag + Rp);
+    if (p.window_left >= 0) k_lo = max(0ll, (long long)w.q0 + w.diag - p.window_left);
+    if (k_lo <= k_hi) {
+      kt_lo = (int)(k_lo / fwd_shared::BK);
+      kt_hi = (int)(k_hi / fwd_shared::BK);
+    }
+  }
+  w.kt_lo = kt_lo;
+  w.n = kt_hi - kt_lo + 1;  // may be 0
+  return w;
+}
+
+// Named barrier over nthreads threads that also ORs a predicate over them.
+__device__ __forceinline__ bool named_bar_sync_or(uint32_t id, uint32_t nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\tbar.red.or.pred po, %2, %3, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+
+// The head-dim-256 forward (sdpa_fwd_wide.cu): persistent grid of `sms` CTAs
+// taking items from ticket slot `slot`; D_qk = D_v = 256 only.
+cudaError_t launch_fwd_wide(const FwdMaps& maps, const FwdParams& p, cudaStream_t s, int sms, int slot);
+cudaError_t fwd_wide_setup();
+
+}  // namespace sdpa

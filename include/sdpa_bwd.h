@@ -203,13 +203,13 @@ int sdpa_bwd_bias(const void* q, const void* k, const void* v, const void* o, co
  * A row with no visible key (queries at or past seq_q_lens[b] included) gets
  * O = 0 and LSE = -inf, or LSE = sink[h] with a sink.
  * Arguments are those of sdpa_bwd() with:
- *   D_qk, D_v  as sdpa_bwd() except (256, 256): SDPA_ERR_UNSUPPORTED (the
- *          kernel's two score slots and two O halves fill tensor memory at
- *          D_v = 128).
+ *   D_qk, D_v  as sdpa_bwd(). (256, 256) runs on a kernel of its own, with one
+ *          O accumulator whose softmax reference the two halves of each row's
+ *          keys agree on every key tile; the others keep an O per half.
  *   o      device bf16 (B, H_q, S_q, D_v) output, 16-byte aligned.
  *   lse    device fp32 (B, H_q, S_q) output, 4-byte aligned.
  *   sink   device fp32 (H_q,) sink logits, or NULL.
- * No workspace. The kernel is persistent (one CTA per SM) and takes its work
+ * No workspace. The kernels are persistent (one CTA per SM) and take their work
  * items from a counter in the library's device memory; the library hands out
  * 64 such counters in turn, so more than 64 forward launches running at once on
  * one device (on different streams) could share one and must not be issued; a

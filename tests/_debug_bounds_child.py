@@ -1,7 +1,8 @@
-"""Child process of test_debug_bounds.py: runs shapes on every dQ route through
-the debug-bounds library (selected by SDPA_BWD_LIBRARY before the binding
-loads it), checks that no kernel reported an out-of-range access and that the
-gradients match the fp64 oracle. Not collected by pytest on its own."""
+"""Child process of test_debug_bounds.py: runs shapes on every dQ route and
+both forward kernels through the debug-bounds library (selected by
+SDPA_BWD_LIBRARY before the binding loads it), checks that no kernel reported
+an out-of-range access and that the gradients, O and LSE match the fp64 oracle.
+Not collected by pytest on its own."""
 import os
 import sys
 
@@ -13,7 +14,8 @@ import torch  # noqa: E402
 
 import attention_backward_sdpa_gb300 as pkg  # noqa: E402
 import workloads  # noqa: E402
-from harness import assert_close, gpu_backward, make_case, oracle_backward  # noqa: E402
+from harness import assert_close, gpu_backward, make_case, oracle_backward, to_device  # noqa: E402
+from test_parity_gpu import _check_fwd, _gpu_fwd  # noqa: E402
 
 W = workloads.Workload
 SHAPES = [
@@ -40,5 +42,7 @@ for w in SHAPES:
     torch.cuda.synchronize()
     for name, g, r in zip(("dq", "dk", "dv"), res, oracle_backward(case)):
         assert_close(f"{w.name} {name}", g.double().cpu().numpy(), r)
+    o, lse = _gpu_fwd(case, to_device(case))  # checks the status word too
+    _check_fwd(case, o, lse)
     print("ok", w.name, flush=True)
 print("DEBUG_BOUNDS_OK", len(SHAPES))

@@ -321,7 +321,9 @@ def test_forward_argument_validation(lib):
     assert call_fwd(lib, B=0) == INVALID
     assert call_fwd(lib, Dqk=100, Dv=100) == UNSUPPORTED
     assert call_fwd(lib, Dqk=192, Dv=192) == UNSUPPORTED
-    assert call_fwd(lib, Dqk=256, Dv=256) == UNSUPPORTED  # the backward only
+    assert call_fwd(lib, Dqk=256, Dv=128) == UNSUPPORTED
+    # 256/256 is served: the null LSE pointer fails only after the head dims pass
+    assert call_fwd(lib, Dqk=256, Dv=256, ptrs=[FAKE] * 4 + [None]) == INVALID
     for i in range(5):
         ptrs = [FAKE] * 5
         ptrs[i] = None

@@ -9,6 +9,10 @@ The cases cover both causal alignments with S_q != S_kv, GQA partial sets, a
 left window with per-batch lengths, a right band, fp16 io, a bias with its
 dBias, a sink with dsink, a full-size shape on sampled rows, and bitwise
 reproducibility. Every output element is compared (NaN-poisoned before the call).
+The forward at this size runs on its own kernel (one O accumulator shared by
+the two softmax warpgroups, which agree on each row's reference every tile); it
+is checked on the same cases, with sinks, biases, fp16 io, the full-size shape
+and a forward-then-backward step.
 """
 import numpy as np
 import pytest
@@ -97,11 +101,55 @@ def test_d256_full_size_sampled():
     _sampled_check(make_case(workloads.WORKLOADS["d256_causal"]))
 
 
-def test_d256_forward_is_refused():
-    """The forward kernel serves D_v up to 128: at 256 the call is refused."""
-    import attention_backward_sdpa_gb300 as pkg
-    case = make_case(CASES["d256_dense_gqa"])
+@pytest.mark.parametrize("name", sorted(CASES))
+@pytest.mark.parametrize("sink", [False, True])
+def test_d256_forward_parity(name, sink):
+    from test_parity_gpu import _check_fwd, _gpu_fwd
+    case = make_case(CASES[name], sink=sink)
+    o, lse = _gpu_fwd(case, to_device(case))
+    _check_fwd(case, o, lse)
+
+
+@pytest.mark.parametrize("kind,dtype", [("B", torch.bfloat16), ("1", torch.float32), ("B", torch.float16)])
+def test_d256_forward_bias_parity(kind, dtype):
+    from test_parity_gpu import _check_fwd, _gpu_fwd
+    w = CASES["d256_dense_gqa"] if kind == "1" else CASES["d256_padded_window"]
+    case = make_case(w, bias=(1 if kind == "1" else w.B, dtype))
+    o, lse = _gpu_fwd(case, to_device(case))
+    _check_fwd(case, o, lse)
+
+
+@pytest.mark.parametrize("name", ["d256_br_causal_long_kv", "d256_padded_window"])
+def test_d256_forward_f16_parity(name):
+    from test_parity_gpu import _check_fwd, _gpu_fwd
+    case = make_case(CASES[name], io=torch.float16)
+    o, lse = _gpu_fwd(case, to_device(case))
+    assert o.dtype == torch.float16
+    _check_fwd(case, o, lse)
+
+
+def test_d256_forward_full_size_sampled_and_bitwise():
+    """The benchmark's head-dim-256 shape: sampled rows against the oracle, and
+    the same bits on a second call (each item's rows come from one CTA)."""
+    from test_parity_gpu import _check_fwd, _gpu_fwd
+    w = workloads.WORKLOADS["d256_causal"]
+    case = make_case(w)
     d = to_device(case)
-    with pytest.raises(pkg.SdpaError) as err:
-        pkg.sdpa_fwd(d["q"], d["k"], d["v"])
-    assert err.value.code == 2  # SDPA_ERR_UNSUPPORTED
+    o, lse = _gpu_fwd(case, d)
+    rng = np.random.default_rng(w.seed + 7)
+    rows = np.unique(rng.integers(0, w.B * w.Hq * w.Sq, 4096))
+    _check_fwd(case, o, lse, rows)
+    o2, lse2 = _gpu_fwd(case, d)
+    assert torch.equal(o.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(lse, lse2)
+
+
+def test_d256_forward_then_backward():
+    """A training step at head dim 256: the GPU forward's O/LSE into the GPU
+    backward, against the oracle backward of the same O/LSE."""
+    from test_parity_gpu import _gpu_fwd
+    case = make_case(CASES["d256_padded_window"])
+    d = to_device(case)
+    o, lse = _gpu_fwd(case, d)
+    case["o"], case["lse"] = o.cpu(), lse.cpu()
+    _compare(case, gpu_backward(case))
