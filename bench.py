@@ -323,24 +323,29 @@ def run_gpu_fwd(args, w, t, rank, world, device):
         torch.cuda.synchronize(device)
         barrier(world)
         total_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
+        # End to end with host buffers (as in run_gpu): Q, K, V (+ bias) in, O and
+        # LSE out every step; E2E_IN_FLIGHT steps in flight, and one at a time.
         host_in = {k: v.cpu().pin_memory() for k, v in d.items()}
-        host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (o, lse)]
         h2d = sum(x.numel() * x.element_size() for x in host_in.values())
-        d2h = sum(x.numel() * x.element_size() for x in host_out)
+        d2h = sum(x.numel() * x.element_size() for x in (o, lse))
         e2e_steps = max(3, min(args.steps, 50))
-        torch.cuda.synchronize(device)
-        t0 = time.perf_counter()
-        for _ in range(e2e_steps):
-            for k, v in host_in.items():
-                d[k].copy_(v, non_blocking=True)
-            step()
-            for hh, x in zip(host_out, (o, lse)):
-                hh.copy_(x, non_blocking=True)
-            torch.cuda.synchronize(device)
-        e2e_s = (time.perf_counter() - t0) / e2e_steps
+
+        def new_slot():
+            dd = {k: torch.empty_like(v) for k, v in d.items()}
+            kws = dict(kw, o=torch.empty_like(o), lse=torch.empty_like(lse))
+            if "bias" in dd:
+                kws["bias"] = dd["bias"]
+            return {"d": dd, "outs": [kws["o"], kws["lse"]],
+                    "run": lambda: pkg.sdpa_fwd(dd["q"], dd["k"], dd["v"], **kws)}
+
+        slot0 = {"d": d, "outs": [o, lse], "run": step}
+        e2e_serial_s = e2e_time(device, host_in, [slot0], e2e_steps)
+        e2e_s = e2e_time(device, host_in, [slot0] + [new_slot() for _ in range(E2E_IN_FLIGHT - 1)],
+                         e2e_steps)
     pkg.check_device_status()
     ms_step = max_over_ranks(total_ms / args.steps, world, device)
     e2e_s = max_over_ranks(e2e_s, world, device)
+    e2e_serial_s = max_over_ranks(e2e_serial_s, world, device)
     peak_tf, peak_hbm, peak_kind = peaks()
     achieved = flops / (ms_step * 1e-3) / 1e12
     return {
@@ -351,7 +356,9 @@ def run_gpu_fwd(args, w, t, rank, world, device):
                      "peak_kind": f"{peak_kind} bf16 burst", "kernel_gflop": flops / 1e9},
         "kernel_ms": {"fwd": round(ms_step, 5)},
         "e2e": {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps_in_flight": E2E_IN_FLIGHT,
+                "serial_value": world * flops / e2e_serial_s / 1e12},
         "clocks": clocks.summary(),
         "gpu_launches": args.steps,
     }
@@ -431,6 +438,35 @@ def peaks():
     return 1900.0, 6800.0, "fallback"
 
 
+E2E_IN_FLIGHT = 2  # steps in flight in the end-to-end measurement
+
+
+def e2e_time(device, host_in, slots, n_steps):
+    """Wall-clock seconds per step over n_steps steps through the public API with
+    host buffers. Every step copies the inputs from pinned host memory into its
+    slot's device buffers, runs the step and copies the outputs back into pinned
+    host memory. Step i uses slot i % len(slots), each slot on a stream of its
+    own with its own buffers and workspace, so with two slots one step's copies
+    overlap the other's kernels (and the link carries both directions at once),
+    as a training loop that stages its next batch does; with one slot the steps
+    run one after another."""
+    streams = [torch.cuda.Stream(device) for _ in slots]
+    outs_h = [[torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in sl["outs"]] for sl in slots]
+    torch.cuda.synchronize(device)
+    t0 = time.perf_counter()
+    for i in range(n_steps):
+        j = i % len(slots)
+        sl = slots[j]
+        with torch.cuda.stream(streams[j]):
+            for k, v in host_in.items():
+                sl["d"][k].copy_(v, non_blocking=True)
+            sl["run"]()
+            for h, x in zip(outs_h[j], sl["outs"]):
+                h.copy_(x, non_blocking=True)
+    torch.cuda.synchronize(device)
+    return (time.perf_counter() - t0) / n_steps
+
+
 def run_gpu(args, w, t, o, lse, rank, world, device):
     import attention_backward_sdpa_gb300 as pkg
     pkg.load()
@@ -463,24 +499,39 @@ def run_gpu(args, w, t, o, lse, rank, world, device):
         kw["dbias"] = torch.empty(tuple(t["bias"].shape), dtype=t["dbias_dtype"], device=device)
         outs.append(kw["dbias"])
 
-    def call_kw():
-        return dict(kw, bias=d["bias"]) if "bias" in d else kw
-
     qat_ws = None
     if t.get("qat"):
         qat_ws = torch.empty(max(pkg.nvfp4_qat_workspace_size(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.Dqk,
                                                               w.Dv), 256), dtype=torch.uint8,
                              device=device)
 
-    def step():
-        if qat_ws is not None:
-            pkg.sdpa_bwd_nvfp4_qat(d["q"], d["k"], d["v"], d["o"], d["do"], d["lse"],
+    def run_with(dd, kws, qws):
+        if qws is not None:
+            pkg.sdpa_bwd_nvfp4_qat(dd["q"], dd["k"], dd["v"], dd["o"], dd["do"], dd["lse"],
                                    scale=w.resolved_scale, causal=w.causal,
                                    bottom_right=w.bottom_right, window_left=w.window_left,
                                    window_right=w.window_right, seq_q_lens=lq, seq_kv_lens=lk,
-                                   dq=dq, dk=dk, dv=dv, workspace=qat_ws)
+                                   dq=kws["dq"], dk=kws["dk"], dv=kws["dv"], workspace=qws)
             return
-        pkg.sdpa_bwd(d["q"], d["k"], d["v"], d["o"], d["do"], d["lse"], **call_kw())
+        pkg.sdpa_bwd(dd["q"], dd["k"], dd["v"], dd["o"], dd["do"], dd["lse"],
+                     **(dict(kws, bias=dd["bias"]) if "bias" in dd else kws))
+
+    def step():
+        run_with(d, kw, qat_ws)
+
+    def new_slot():
+        """A second set of device inputs, outputs and workspace for the e2e loop."""
+        dd = {k: torch.empty_like(v) for k, v in d.items()}
+        kws = dict(kw, dq=torch.empty_like(dq), dk=torch.empty_like(dk), dv=torch.empty_like(dv),
+                   workspace=torch.empty_like(ws))
+        outs_s = [kws["dq"], kws["dk"], kws["dv"]]
+        if args.sink:
+            kws["dsink"] = torch.empty_like(kw["dsink"])
+        if "bias" in d:
+            kws["dbias"] = torch.empty_like(kw["dbias"])
+            outs_s.append(kws["dbias"])
+        qws = torch.empty_like(qat_ws) if qat_ws is not None else None
+        return {"d": dd, "outs": outs_s, "run": lambda: run_with(dd, kws, qws)}
 
     def timed_loop(n, profile=False):
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
@@ -516,25 +567,20 @@ def run_gpu(args, w, t, o, lse, rank, world, device):
         # (a second pass: the events between launches disable the PDL overlap).
         _, prof = timed_loop(args.steps, profile=True)
         # End to end through the public API with host buffers: pinned host -> device
-        # copies of the inputs and a device -> host read of dQ/dK/dV every step.
+        # copies of the inputs and a device -> host read of dQ/dK/dV (+ dBias)
+        # every step; E2E_IN_FLIGHT steps in flight, and one at a time.
         host_in = {k: v.cpu().pin_memory() for k, v in d.items()}
-        host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in outs]
         h2d = sum(x.numel() * x.element_size() for x in host_in.values())
-        d2h = sum(x.numel() * x.element_size() for x in host_out)
+        d2h = sum(x.numel() * x.element_size() for x in outs)
         e2e_steps = max(3, min(args.steps, 50))
-        torch.cuda.synchronize(device)
-        t0 = time.perf_counter()
-        for _ in range(e2e_steps):
-            for k, v in host_in.items():
-                d[k].copy_(v, non_blocking=True)
-            step()
-            for h, x in zip(host_out, outs):
-                h.copy_(x, non_blocking=True)
-            torch.cuda.synchronize(device)
-        e2e_s = (time.perf_counter() - t0) / e2e_steps
+        slot0 = {"d": d, "outs": outs, "run": step}
+        e2e_serial_s = e2e_time(device, host_in, [slot0], e2e_steps)
+        e2e_s = e2e_time(device, host_in, [slot0] + [new_slot() for _ in range(E2E_IN_FLIGHT - 1)],
+                         e2e_steps)
     pkg.check_device_status()
     ms_step = max_over_ranks(total_ms / args.steps, world, device)
     e2e_s = max_over_ranks(e2e_s, world, device)
+    e2e_serial_s = max_over_ranks(e2e_serial_s, world, device)
     peak_tf, peak_hbm, peak_kind = peaks()
     main_ms = prof["main"][0] / max(prof["main"][1], 1)
     achieved = main_flops / (main_ms * 1e-3) / 1e12
@@ -559,7 +605,9 @@ def run_gpu(args, w, t, o, lse, rank, world, device):
         "roofline": roof,
         "kernel_ms": kernel_ms,
         "e2e": {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps_in_flight": E2E_IN_FLIGHT,
+                "serial_value": world * flops / e2e_serial_s / 1e12},
         "clocks": clocks.summary(),
         # preprocess + main + dQ kernel (+ the three fake quantizations with QAT,
         # + dsink with sink tokens)
