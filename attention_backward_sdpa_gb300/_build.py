@@ -29,7 +29,7 @@ SOURCES = ["sdpa_bwd_api.cu", "sdpa_bwd_main.cu", "sdpa_bwd_main_bias.cu", "sdpa
            "sdpa_bwd_main_f16.cu",
            "sdpa_bwd_main_ds.cu",
            "sdpa_bwd_aux.cu",
-           "sdpa_bwd_dq.cu", "sdpa_bwd_noalloc.cu", "sdpa_fwd.cu", "sdpa_fwd_wide.cu"]
+           "sdpa_bwd_dq.cu", "sdpa_bwd_noalloc.cu", "sdpa_fwd.cu", "sdpa_fwd_shared.cu", "sdpa_fwd_wide.cu"]
 HEADERS = ["common.cuh", "gqa.cuh", "ptx.cuh", "tmap.h", "sdpa_bwd_main.cuh", "nvfp4.cuh", "bias.cuh", "sdpa_fwd.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -631,7 +631,6 @@ template <bool BIAS, bool F16>
 static cudaError_t fwd_setup_variant() {
   cudaError_t e = set_fwd_smem<64, 64, BIAS, F16>();
   if (e == cudaSuccess) e = set_fwd_smem<128, 128, BIAS, F16>();
-  if (e == cudaSuccess) e = set_fwd_smem<192, 128, BIAS, F16>();
   return e;
 }
 
@@ -640,6 +639,7 @@ cudaError_t fwd_kernel_setup() {
   if (e == cudaSuccess) e = fwd_setup_variant<true, false>();
   if (e == cudaSuccess) e = fwd_setup_variant<false, true>();
   if (e == cudaSuccess) e = fwd_setup_variant<true, true>();
+  if (e == cudaSuccess) e = fwd_shared_setup();
   if (e == cudaSuccess) e = fwd_wide_setup();
   return e;
 }
@@ -661,9 +661,6 @@ static cudaError_t launch_fwd_variant(const FwdMaps& maps, const FwdParams& p, c
   if (p.Dqk <= 128 && p.Dv == p.Dqk)
     return launch_kernel(sdpa_fwd_kernel<128, 128, BIAS, F16, PERSIST>, grid, block,
                          fwd_kernel::Layout<128, 128>::BYTES, s, false, maps, p, slot);
-  if (p.Dqk == 192 && p.Dv == 128)
-    return launch_kernel(sdpa_fwd_kernel<192, 128, BIAS, F16, PERSIST>, grid, block,
-                         fwd_kernel::Layout<192, 128>::BYTES, s, false, maps, p, slot);
   return cudaErrorInvalidValue;
 }
 
@@ -674,7 +671,10 @@ cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, cudaStream_t s) 
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
     return cudaErrorInvalidValue;
-  // Head dim 256: the kernel with one shared O accumulator (sdpa_fwd_wide.cu).
+  // The MLA pair: one O shared by the softmax warpgroups and three score slots
+  // (sdpa_fwd_shared.cu). Head dim 256: one shared O, single K and V buffers
+  // (sdpa_fwd_wide.cu).
+  if (p.Dqk == 192 && p.Dv == 128) return launch_fwd_shared(maps, p, s, sms, slot);
   if (p.Dqk == 256 && p.Dv == 256) return launch_fwd_wide(maps, p, s, sms, slot);
   if (p.bias)
     return p.f16 ? launch_fwd_variant<true, true>(maps, p, s, sms, slot)

@@ -1,7 +1,7 @@
-// sdpa_fwd.cuh -- what the two forward kernels share: the work-item decode of
+// sdpa_fwd.cuh -- what the three forward kernels share: the work-item decode of
 // the persistent schedule, the bias row loader, a named barrier that also ORs a
-// predicate, the constants of the schedule, and the launcher of the head-dim-256
-// kernel (sdpa_fwd_wide.cu), which launch_fwd (sdpa_fwd.cu) calls for D = 256.
+// predicate, the constants of the schedule, and the launchers of the other two
+// forward kernels, which launch_fwd (sdpa_fwd.cu) calls by head dims.
 #pragma once
 
 #include <cuda.h>
@@ -116,8 +116,11 @@ __device__ __forceinline__ bool named_bar_sync_or(uint32_t id, uint32_t nthreads
 }
 
 
-// The head-dim-256 forward (sdpa_fwd_wide.cu): persistent grid of `sms` CTAs
-// taking items from ticket slot `slot`; D_qk = D_v = 256 only.
+// The other forward kernels, each a persistent grid of `sms` CTAs taking items
+// from ticket slot `slot`: the shared-O kernel for the MLA pair (D_qk = 192,
+// D_v = 128; sdpa_fwd_shared.cu) and the head-dim-256 kernel (sdpa_fwd_wide.cu).
+cudaError_t launch_fwd_shared(const FwdMaps& maps, const FwdParams& p, cudaStream_t s, int sms, int slot);
+cudaError_t fwd_shared_setup();
 cudaError_t launch_fwd_wide(const FwdMaps& maps, const FwdParams& p, cudaStream_t s, int sms, int slot);
 cudaError_t fwd_wide_setup();
 

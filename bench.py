@@ -352,7 +352,8 @@ def run_gpu_fwd(args, w, t, rank, world, device):
         "value": world * achieved, "ms_per_step": ms_step, "flops": flops,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
                      "frac": achieved / peak_tf, "traffic": None,
-                     "kernel": "sdpa_fwd_wide_kernel" if w.Dqk == 256 else "sdpa_fwd_kernel",
+                     "kernel": {256: "sdpa_fwd_wide_kernel", 192: "sdpa_fwd_shared_kernel"}.get(
+                         w.Dqk, "sdpa_fwd_kernel"),
                      "peak_kind": f"{peak_kind} bf16 burst", "kernel_gflop": flops / 1e9},
         "kernel_ms": {"fwd": round(ms_step, 5)},
         "e2e": {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s",
