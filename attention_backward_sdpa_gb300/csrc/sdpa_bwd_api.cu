@@ -641,7 +641,8 @@ int run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
   const void* vb = S_kv > 0 ? v : q;
   if (!make_bhsd_map(&maps.q, q, D_qk, S_q, BHq, 128, f16) ||
       !make_bhsd_map(&maps.k, kb, D_qk, Skv_map, S_kv > 0 ? BHkv : BHq, 128, f16) ||
-      !make_bhsd_map(&maps.v, vb, D_v, Skv_map, S_kv > 0 ? BHkv : BHq, 128, f16) ||
+      // (the head-dim-256 kernel loads V in 32-key row groups)
+      !make_bhsd_map(&maps.v, vb, D_v, Skv_map, S_kv > 0 ? BHkv : BHq, D_v == 256 ? 32 : 128, f16) ||
       !make_bhsd_map(&maps.o, o, D_v, S_q, BHq, 128, f16))
     return SDPA_ERR_CUDA;
   nvtxRangePushA("sdpa_fwd");

@@ -20,10 +20,13 @@
 //   - P packed into the slot's first 64 columns (warpgroup h at [32 h, 32 h + 32)),
 //     written after the exchange, when both have read their scores;
 //   - shared memory holds Q (64 KB), one K tile and one V tile (64 KB each), 192
-//     KB in all. Two producers: warp 8 loads Q and K(j + 1) as soon as G1(j)
-//     has read K(j); warp 11 loads V(j + 1) as soon as G2(j) has read V(j). In
-//     steady state the tensor pipe alternates G1(j + 1) and G2(j), each 1024
-//     tensor cycles, and each covers the load the other one waits for.
+//     KB in all, moved in 16 KB pieces with a barrier pair each: K by 64-column
+//     block, V by 32-key row group. Two producers: warp 8 loads Q and each
+//     piece of K(j + 1) as soon as G1(j)'s MMAs over that piece have completed;
+//     warp 11 does the same for V(j + 1) after G2(j). Several pieces are then in
+//     flight at once: with whole tiles (one load in flight per buffer) the
+//     loads' latency paced the kernel at about 4,950 cycles a tile against
+//     2,048 of tensor work.
 //   Per key tile j (slot s = j % 2):
 //     G1  S_s = Q K_j^T                        (16 MMAs 128x128x16, warp 9)
 //         P = exp2(S scale log2e [+ bias log2e] - m) -> bf16 pairs in slot s
@@ -51,22 +54,30 @@ constexpr int TILE = 128 * D * 2;      // a Q, K or V tile (64 KB)
 constexpr uint32_t COL_O = 256;        // O accumulator columns [256, 512)
 constexpr int RING = 4;                // items published by the ticket taker
 constexpr int RING_READERS = 4;        // warps 0 (for the softmax warpgroups), 9, 10 and 11
-// Register split as in sdpa_fwd.cu: launched at 168 per thread, the control
-// warpgroup drops to 56 and the softmax warpgroups grow to 224.
-constexpr uint32_t REGS_CTRL = 56, REGS_SOFTMAX = 224;
+// Register split: launched at 168 per thread, the control warpgroup drops to 72
+// (the per-piece issue loops spilled at 56) and the softmax warpgroups grow to
+// 216: 128 x (72 + 216 + 216) = 64,512 = 384 x 168.
+constexpr uint32_t REGS_CTRL = 72, REGS_SOFTMAX = 216;
 static_assert(128 * (REGS_CTRL + 2 * REGS_SOFTMAX) <= THREADS * 168, "register split");
 
+// K and V move in pieces of 16 KB, each with a barrier pair of its own: K(j)
+// by 64-column block (G1's MMAs walk the head dim, four MMAs per block), V(j)
+// by 32-key row group (G2's MMAs walk the keys, two MMAs per group). A piece is
+// replaced as soon as the MMAs that read it have completed, so the next tile's
+// first pieces load while the current GEMM still reads the last ones.
+constexpr int NPIECE = 4;
+constexpr int PIECE = TILE / NPIECE;
 enum : int {
   BAR_QFULL = 0,   // the item's Q landed
   BAR_QEMPTY = 1,  // the item's last G1 completed: Q may be replaced
-  BAR_KFULL = 2,   // K(j) landed
-  BAR_KEMPTY = 3,  // G1(j) completed: K may be replaced
-  BAR_VFULL = 4,   // V(j) landed
-  BAR_VEMPTY = 5,  // G2(j) completed: V may be replaced
-  BAR_SFULL = 6,   // + slot: S in tensor memory
-  BAR_PREADY = 8,  // + slot, 256 arrivals: P written (both warpgroups)
-  BAR_PVDONE = 10, // + slot: G2 of the slot's tile completed
-  BAR_RFULL = 12,  // + ring entry: an item published
+  BAR_KFULL = 2,   // + block: K(j)'s 64-column block landed
+  BAR_KEMPTY = 6,  // + block: G1(j)'s MMAs over the block completed
+  BAR_VFULL = 10,  // + row group: V(j)'s 32 keys landed
+  BAR_VEMPTY = 14, // + row group: G2(j)'s MMAs over those keys completed
+  BAR_SFULL = 18,  // + slot: S in tensor memory
+  BAR_PREADY = 20, // + slot, 256 arrivals: P written (both warpgroups)
+  BAR_PVDONE = 22, // + slot: G2 of the slot's tile completed
+  BAR_RFULL = 24,  // + ring entry: an item published
   BAR_REMPTY = BAR_RFULL + RING,  // + ring entry, RING_READERS arrivals
   NUM_BARS = BAR_REMPTY + RING
 };
@@ -166,9 +177,16 @@ __global__ void __launch_bounds__(fwd_wide::THREADS, 1)
         const FwdItem w = fwd_item(p, it);
         if (w.n <= 0) continue;
         for (int j = 0; j < w.n && ok; ++j, ++g) {
-          // K(g) replaces K(g - 1) once G1(g - 1) has read it; on an item's
-          // first tile that G1 was the previous item's last, which frees Q too.
-          if (g >= 1) ok = mbar_wait(&bars[BAR_KEMPTY], (g - 1) & 1, abort_flag, WAIT_LIMIT_NS);
+          // Block b of K(g) replaces that of K(g - 1) once G1(g - 1)'s MMAs over
+          // it have completed. On an item's first tile that G1 was the previous
+          // item's last, whose completion also frees Q.
+          const int k0 = (w.kt_lo + j) * BK;
+          for (int b = 0; b < NPIECE && ok; ++b) {
+            if (g >= 1) ok = mbar_wait(&bars[BAR_KEMPTY + b], (g - 1) & 1, abort_flag, WAIT_LIMIT_NS);
+            if (!ok) break;
+            mbar_arrive_expect_tx(&bars[BAR_KFULL + b], PIECE);
+            tma_load_3d(sK + b * BLK, &maps.k, &bars[BAR_KFULL + b], b * 64, k0, w.kvh);
+          }
           if (ok && j == 0) {
             if (ni >= 1) ok = mbar_wait(&bars[BAR_QEMPTY], (ni - 1) & 1, abort_flag, WAIT_LIMIT_NS);
             if (ok) {
@@ -177,11 +195,6 @@ __global__ void __launch_bounds__(fwd_wide::THREADS, 1)
                 tma_load_3d(sQ + blk * BLK, &maps.q, &bars[BAR_QFULL], blk * 64, w.q0, w.bh);
             }
           }
-          if (!ok) break;
-          const int k0 = (w.kt_lo + j) * BK;
-          mbar_arrive_expect_tx(&bars[BAR_KFULL], TILE);
-          for (int blk = 0; blk < D / 64; ++blk)
-            tma_load_3d(sK + blk * BLK, &maps.k, &bars[BAR_KFULL], blk * 64, k0, w.kvh);
         }
         ++ni;
       }
@@ -194,12 +207,18 @@ __global__ void __launch_bounds__(fwd_wide::THREADS, 1)
         if (it < 0) break;
         const FwdItem w = fwd_item(p, it);
         for (int j = 0; j < w.n && ok; ++j, ++g) {
-          if (g >= 1) ok = mbar_wait(&bars[BAR_VEMPTY], (g - 1) & 1, abort_flag, WAIT_LIMIT_NS);
-          if (!ok) break;
+          // Keys 32 r .. 32 r + 31 of V(g) replace those of V(g - 1) once G2(g - 1)'s
+          // MMAs over them have completed: four 32-row boxes, one per 64-column
+          // block (the V map's boxes are 32 rows high).
           const int k0 = (w.kt_lo + j) * BK;
-          mbar_arrive_expect_tx(&bars[BAR_VFULL], TILE);
-          for (int blk = 0; blk < D / 64; ++blk)
-            tma_load_3d(sV + blk * BLK, &maps.v, &bars[BAR_VFULL], blk * 64, k0, w.kvh);
+          for (int r = 0; r < NPIECE && ok; ++r) {
+            if (g >= 1) ok = mbar_wait(&bars[BAR_VEMPTY + r], (g - 1) & 1, abort_flag, WAIT_LIMIT_NS);
+            if (!ok) break;
+            mbar_arrive_expect_tx(&bars[BAR_VFULL + r], PIECE);
+            for (int blk = 0; blk < D / 64; ++blk)
+              tma_load_3d(sV + blk * BLK + r * 32 * 128, &maps.v, &bars[BAR_VFULL + r], blk * 64, k0 + 32 * r,
+                          w.kvh);
+          }
         }
       }
     } else if (warp == 9 && lane == 0) {
@@ -217,18 +236,22 @@ __global__ void __launch_bounds__(fwd_wide::THREADS, 1)
         ok = mbar_wait(&bars[BAR_QFULL], ni & 1, abort_flag, WAIT_LIMIT_NS);
         for (int j = 0; j < w.n && ok; ++j, ++g) {
           const int s = g & 1;
-          ok = mbar_wait(&bars[BAR_KFULL], g & 1, abort_flag, WAIT_LIMIT_NS);
           // The slot held P(g - 2) until G2(g - 2) read it.
-          if (ok && g >= 2) ok = mbar_wait(&bars[BAR_PVDONE + s], ((g - 2) >> 1) & 1, abort_flag, WAIT_LIMIT_NS);
-          if (!ok) break;
-          tc_fence_after();
+          if (g >= 2) ok = mbar_wait(&bars[BAR_PVDONE + s], ((g - 2) >> 1) & 1, abort_flag, WAIT_LIMIT_NS);
+          for (int b = 0; b < NPIECE && ok; ++b) {
+            ok = mbar_wait(&bars[BAR_KFULL + b], g & 1, abort_flag, WAIT_LIMIT_NS);
+            if (!ok) break;
+            tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t ko = (k >> 2) * BLK + (k & 3) * 32;
-            mma_ss(tmem + 128u * s, sdesc_at(T_KMAJ, aQ + ko), sdesc_at(T_KMAJ, aK + ko), ID_S, k > 0);
+            for (int kk = 0; kk < 4; ++kk) {
+              const int k = 4 * b + kk;
+              const uint32_t ko = b * BLK + kk * 32;
+              mma_ss(tmem + 128u * s, sdesc_at(T_KMAJ, aQ + ko), sdesc_at(T_KMAJ, aK + ko), ID_S, k > 0);
+            }
+            mma_commit(&bars[BAR_KEMPTY + b]);
           }
+          if (!ok) break;
           mma_commit(&bars[BAR_SFULL + s]);
-          mma_commit(&bars[BAR_KEMPTY]);
           if (j == w.n - 1) mma_commit(&bars[BAR_QEMPTY]);
         }
         ++ni;
@@ -248,17 +271,23 @@ __global__ void __launch_bounds__(fwd_wide::THREADS, 1)
           const int s = g & 1;
           // (The previous item's epilogue has read O before any P of this item
           // is written: the same threads do both, in that order.)
-          ok = mbar_wait(&bars[BAR_PREADY + s], (g >> 1) & 1, abort_flag, WAIT_LIMIT_NS) &&
-               mbar_wait(&bars[BAR_VFULL], g & 1, abort_flag, WAIT_LIMIT_NS);
-          if (!ok) break;
-          tc_fence_after();
-          // Keys 16 k .. 16 k + 15 of P sit in the slot's columns [8 k, 8 k + 8).
+          ok = mbar_wait(&bars[BAR_PREADY + s], (g >> 1) & 1, abort_flag, WAIT_LIMIT_NS);
+          // Keys 16 k .. 16 k + 15 of P sit in the slot's columns [8 k, 8 k + 8);
+          // row group r of V holds keys 32 r .. 32 r + 31 (MMAs 2 r and 2 r + 1).
+          for (int r = 0; r < NPIECE && ok; ++r) {
+            ok = mbar_wait(&bars[BAR_VFULL + r], g & 1, abort_flag, WAIT_LIMIT_NS);
+            if (!ok) break;
+            tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)
-            mma_ts(tmem + COL_O, tmem + 128u * s + 8u * k, sdesc_at(T_MN_V, aV + k * 2048), ID_O,
-                   (u > 0 || k > 0) ? 1u : 0u);
+            for (int kk = 0; kk < 2; ++kk) {
+              const int k = 2 * r + kk;
+              mma_ts(tmem + COL_O, tmem + 128u * s + 8u * k, sdesc_at(T_MN_V, aV + k * 2048), ID_O,
+                     (u > 0 || k > 0) ? 1u : 0u);
+            }
+            mma_commit(&bars[BAR_VEMPTY + r]);
+          }
+          if (!ok) break;
           mma_commit(&bars[BAR_PVDONE + s]);
-          mma_commit(&bars[BAR_VEMPTY]);
         }
       }
     }
