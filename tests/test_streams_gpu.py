@@ -21,6 +21,7 @@ CASES = [
     W("streams_det", 2, 4, 2, 300, 300, 128, 128, causal=True, deterministic=True, seed=120),
     W("streams_reduction", 2, 4, 4, 333, 333, 64, 64, causal=True, window_left=100, seed=121),
     W("streams_d256", 1, 4, 2, 260, 260, 256, 256, causal=True, bottom_right=True, seed=122),
+    W("streams_mla", 1, 4, 2, 300, 280, 192, 128, causal=True, window_left=120, seed=123),
 ]
 
 
@@ -54,8 +55,9 @@ def test_backward_calls_on_two_streams(w):
                 assert torch.equal(g.view(torch.int16), a.view(torch.int16)), name
 
 
-@pytest.mark.parametrize("w", [CASES[0], CASES[2]], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [CASES[0], CASES[2], CASES[3]], ids=lambda w: w.name)
 def test_forward_calls_on_two_streams(w):
+    """One case per forward kernel (each takes tickets from counters of its own)."""
     import attention_backward_sdpa_gb300 as pkg
     from test_parity_gpu import _check_fwd
     case = make_case(w)
