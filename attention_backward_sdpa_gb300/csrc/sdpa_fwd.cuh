@@ -103,6 +103,14 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdParams& p, int it) {
   return w;
 }
 
+// One 32-byte global store of two 16-byte halves (the address 32-byte aligned):
+// a thread writes a whole 32-byte sector of its O row at once.
+__device__ __forceinline__ void st_global_32b(void* ptr, const uint4& a, const uint4& b) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(a.x), "r"(a.y),
+               "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+               : "memory");
+}
+
 // Named barrier over nthreads threads that also ORs a predicate over them.
 __device__ __forceinline__ bool named_bar_sync_or(uint32_t id, uint32_t nthreads, bool pred) {
   uint32_t r;
