@@ -308,6 +308,9 @@ __global__ void __launch_bounds__(fwd_wide::THREADS, 1)
     const float cs = BIAS ? 1.f : c;
     uint16_t* const o_base = static_cast<uint16_t*>(p.o);
     const size_t o_bytes = (size_t)p.B * p.Hq * p.Sq * D * 2;
+    // O rows go out in 32-byte stores when every 16-column piece is 32-byte
+    // aligned (the base 32-byte aligned, D_v a multiple of 16), else 16-byte ones.
+    const bool o_sector = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0 && (p.Dv & 15) == 0;
     int g = 0;
     bool ok = true;
     bool have_next = false;  // the item for this e was taken during the previous epilogue
@@ -547,14 +550,25 @@ __global__ void __launch_bounds__(fwd_wide::THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = 0u;
         }
+        uint4 wv[4];
 #pragma unroll
         for (int v8 = 0; v8 < 4; ++v8) {
-          uint4 wv;
-          wv.x = pack_io2<F16>(__uint_as_float(o[v8 * 8 + 0]) * inv_l, __uint_as_float(o[v8 * 8 + 1]) * inv_l);
-          wv.y = pack_io2<F16>(__uint_as_float(o[v8 * 8 + 2]) * inv_l, __uint_as_float(o[v8 * 8 + 3]) * inv_l);
-          wv.z = pack_io2<F16>(__uint_as_float(o[v8 * 8 + 4]) * inv_l, __uint_as_float(o[v8 * 8 + 5]) * inv_l);
-          wv.w = pack_io2<F16>(__uint_as_float(o[v8 * 8 + 6]) * inv_l, __uint_as_float(o[v8 * 8 + 7]) * inv_l);
-          if (row_ok) *reinterpret_cast<uint4*>(orow_ptr + cbase + v8 * 8) = wv;
+          wv[v8].x = pack_io2<F16>(__uint_as_float(o[v8 * 8 + 0]) * inv_l, __uint_as_float(o[v8 * 8 + 1]) * inv_l);
+          wv[v8].y = pack_io2<F16>(__uint_as_float(o[v8 * 8 + 2]) * inv_l, __uint_as_float(o[v8 * 8 + 3]) * inv_l);
+          wv[v8].z = pack_io2<F16>(__uint_as_float(o[v8 * 8 + 4]) * inv_l, __uint_as_float(o[v8 * 8 + 5]) * inv_l);
+          wv[v8].w = pack_io2<F16>(__uint_as_float(o[v8 * 8 + 6]) * inv_l, __uint_as_float(o[v8 * 8 + 7]) * inv_l);
+        }
+        if (o_sector) {
+          // Whole 32-byte sectors: 16-column pieces, each inside the row.
+#pragma unroll
+          for (int v16 = 0; v16 < 2; ++v16)
+            if (row_ok && cbase + v16 * 16 < p.Dv) st_global_32b(orow_ptr + cbase + v16 * 16, wv[2 * v16], wv[2 * v16 + 1]);
+        } else {
+#pragma unroll
+          for (int v8 = 0; v8 < 4; ++v8) {
+            const int cc = cbase + v8 * 8;  // column of this 16-byte piece
+            if (row_ok && cc < p.Dv) *reinterpret_cast<uint4*>(orow_ptr + cc) = wv[v8];
+          }
         }
       }
       tc_fence_before();
