@@ -21,6 +21,14 @@ constexpr float RESCALE_THRESHOLD = 8.f;  // log2 units: P stays below 2^8 until
 constexpr int FWD_SLOTS = 64;             // launch slots of the persistent tickets
 }  // namespace fwd_shared
 
+// One 32-byte streaming load (the address 32-byte aligned) into r[at .. at + 7].
+__device__ __forceinline__ void ld_global_cs_32b(const void* ptr, uint32_t (&r)[64], int at) {
+  asm volatile("ld.global.cs.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[at]), "=r"(r[at + 1]), "=r"(r[at + 2]), "=r"(r[at + 3]), "=r"(r[at + 4]),
+                 "=r"(r[at + 5]), "=r"(r[at + 6]), "=r"(r[at + 7])
+               : "l"(ptr));
+}
+
 // This row's bias for keys kb .. kb + 63 as 32-bit words: on the 16-byte path
 // 16-bit pairs (`packed`, 32 words) or fp32 values (64 words); otherwise fp32
 // values from scalar loads, 0 past S_kv.
@@ -33,9 +41,24 @@ __device__ __forceinline__ void load_fwd_bias_row(const FwdParams& p, long long 
     for (int i = 0; i < 64; ++i) raw[i] = 0u;
     return;
   }
-  if (vec) {
-    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const char*>(p.bias) +
-                                                      (row_off + kb) * (p.bias_fp32 ? 4 : 2));
+  const int esz = p.bias_fp32 ? 4 : 2;
+  // 32-byte loads (a thread reads whole 32-byte sectors of its row) when every
+  // row segment is 32-byte aligned: the base, and rows whose byte length is a
+  // multiple of 32 (kb is a multiple of 64 keys). Uniform across the launch.
+  const bool v32 = vec && (reinterpret_cast<uintptr_t>(p.bias) & 31u) == 0 && ((long long)p.Skv * esz) % 32 == 0;
+  if (v32) {
+    const char* src = static_cast<const char*>(p.bias) + (row_off + kb) * esz;
+    if (p.bias_fp32) {
+#pragma unroll
+      for (int v = 0; v < 8; ++v) ld_global_cs_32b(src + 32 * v, raw, 8 * v);
+    } else {
+#pragma unroll
+      for (int v = 0; v < 4; ++v) ld_global_cs_32b(src + 32 * v, raw, 8 * v);
+#pragma unroll
+      for (int i = 32; i < 64; ++i) raw[i] = 0u;
+    }
+  } else if (vec) {
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const char*>(p.bias) + (row_off + kb) * esz);
     if (p.bias_fp32) {
 #pragma unroll
       for (int v = 0; v < 16; ++v) {
