@@ -26,6 +26,13 @@
 
 namespace sdpa {
 
+// One 32-byte store of two 16-byte halves (the address 32-byte aligned).
+__device__ __forceinline__ void dq_store_32b(void* ptr, const uint4& a, const uint4& b) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(a.x), "r"(a.y),
+               "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+               : "memory");
+}
+
 constexpr int DQ_THREADS = 224;
 constexpr uint64_t DQ_WAIT_LIMIT_NS = 4000000000ull;
 
@@ -300,6 +307,9 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     int unit_idx = 0;
     pdl_wait_prior_grid();  // the GQA partial sets come from the main kernel
     const int row = warp * 32 + lane;          // query within the 128-row unit
+    // A thread writes its own dQ row: in 32-byte stores (whole sectors) when dQ's
+    // base is 32-byte aligned (its rows, D x 2 bytes, then are too), else 16-byte.
+    const bool dq_sector = (reinterpret_cast<uintptr_t>(p.dq) & 31u) == 0;
     const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
     int done_units = 0;
     bool ok = true;
@@ -333,14 +343,20 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
           for (int i = 0; i < 32; ++i) r[i] = 0u;
         }
         if (q < p.Sq) {
+          uint4 o[4];
 #pragma unroll
           for (int v8 = 0; v8 < 4; ++v8) {
-            uint4 o;
-            o.x = pack_io2<F16>(__uint_as_float(r[v8 * 8 + 0]) * p.scale, __uint_as_float(r[v8 * 8 + 1]) * p.scale);
-            o.y = pack_io2<F16>(__uint_as_float(r[v8 * 8 + 2]) * p.scale, __uint_as_float(r[v8 * 8 + 3]) * p.scale);
-            o.z = pack_io2<F16>(__uint_as_float(r[v8 * 8 + 4]) * p.scale, __uint_as_float(r[v8 * 8 + 5]) * p.scale);
-            o.w = pack_io2<F16>(__uint_as_float(r[v8 * 8 + 6]) * p.scale, __uint_as_float(r[v8 * 8 + 7]) * p.scale);
-            *reinterpret_cast<uint4*>(out + c32 * 32 + v8 * 8) = o;
+            o[v8].x = pack_io2<F16>(__uint_as_float(r[v8 * 8 + 0]) * p.scale, __uint_as_float(r[v8 * 8 + 1]) * p.scale);
+            o[v8].y = pack_io2<F16>(__uint_as_float(r[v8 * 8 + 2]) * p.scale, __uint_as_float(r[v8 * 8 + 3]) * p.scale);
+            o[v8].z = pack_io2<F16>(__uint_as_float(r[v8 * 8 + 4]) * p.scale, __uint_as_float(r[v8 * 8 + 5]) * p.scale);
+            o[v8].w = pack_io2<F16>(__uint_as_float(r[v8 * 8 + 6]) * p.scale, __uint_as_float(r[v8 * 8 + 7]) * p.scale);
+          }
+          if (dq_sector) {
+            dq_store_32b(out + c32 * 32, o[0], o[1]);
+            dq_store_32b(out + c32 * 32 + 16, o[2], o[3]);
+          } else {
+#pragma unroll
+            for (int v8 = 0; v8 < 4; ++v8) *reinterpret_cast<uint4*>(out + c32 * 32 + v8 * 8) = o[v8];
           }
         }
       }
