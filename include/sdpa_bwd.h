@@ -203,9 +203,11 @@ int sdpa_bwd_bias(const void* q, const void* k, const void* v, const void* o, co
  * A row with no visible key (queries at or past seq_q_lens[b] included) gets
  * O = 0 and LSE = -inf, or LSE = sink[h] with a sink.
  * Arguments are those of sdpa_bwd() with:
- *   D_qk, D_v  as sdpa_bwd(). (256, 256) runs on a kernel of its own, with one
- *          O accumulator whose softmax reference the two halves of each row's
- *          keys agree on every key tile; the others keep an O per half.
+ *   D_qk, D_v  as sdpa_bwd(). D_qk = D_v up to 128 run on a kernel that keeps an
+ *          O accumulator per half of each row's keys; (192, 128) and (256, 256)
+ *          on kernels with one O whose softmax reference the two halves agree
+ *          on every key tile (three score slots at 192/128; K and V in 16 KB
+ *          pieces at 256).
  *   o      device bf16 (B, H_q, S_q, D_v) output, 16-byte aligned.
  *   lse    device fp32 (B, H_q, S_q) output, 4-byte aligned.
  *   sink   device fp32 (H_q,) sink logits, or NULL.
