@@ -87,6 +87,37 @@ __device__ __forceinline__ void load_fwd_bias_row(const FwdParams& p, long long 
   }
 }
 
+// A thread's 64 scores of a tile rewritten as x = s * c + bias * log2e, the bias
+// widened from 16-bit pairs (`packed`; fp16 when p.bias_f16, else bf16) or taken
+// as fp32 words. One loop per element form (the choice is uniform across the
+// warp), so that widening an element is a fixed instruction or two: a
+// per-element choice between the bf16 and the fp16 widening cost the biased
+// forward about a third of its speed.
+__device__ __forceinline__ void add_bias_row(const FwdParams& p, float c, const uint32_t (&braw)[64], bool packed,
+                                             uint32_t (&sr)[2][32]) {
+  constexpr float LOG2E_F = 1.4426950408889634f;
+  if (packed && p.bias_f16) {
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+      const uint32_t wd = braw[i >> 1];
+      const float bv = __half2float(__ushort_as_half((unsigned short)((i & 1) ? (wd >> 16) : (wd & 0xFFFFu))));
+      sr[i >> 5][i & 31] = __float_as_uint(fmaf(__uint_as_float(sr[i >> 5][i & 31]), c, bv * LOG2E_F));
+    }
+  } else if (packed) {
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+      const uint32_t wd = braw[i >> 1];
+      const float bv = __uint_as_float((i & 1) ? (wd & 0xFFFF0000u) : (wd << 16));
+      sr[i >> 5][i & 31] = __float_as_uint(fmaf(__uint_as_float(sr[i >> 5][i & 31]), c, bv * LOG2E_F));
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 64; ++i)
+      sr[i >> 5][i & 31] =
+          __float_as_uint(fmaf(__uint_as_float(sr[i >> 5][i & 31]), c, __uint_as_float(braw[i]) * LOG2E_F));
+  }
+}
+
 // One work item: 128 query rows (query tile qt, descending so that under a
 // causal mask the longest items come first) of one (batch, query head), and the
 // range [kt_lo, kt_lo + n) of 128-key tiles that any of its live rows sees.

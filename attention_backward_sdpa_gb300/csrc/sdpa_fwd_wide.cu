@@ -382,30 +382,7 @@ __global__ void __launch_bounds__(fwd_wide::THREADS, 1)
           tmem_ld32(t_lane + 128u * s + i0 + 32, sr[1]);
           tmem_ld_wait(sr[0]);
           tmem_ld_wait(sr[1]);
-          if constexpr (BIAS) {
-            // One loop per bias element form (uniform across the warp).
-            constexpr float LOG2E_F = 1.4426950408889634f;
-            if (bpacked && p.bias_f16) {
-#pragma unroll
-              for (int i = 0; i < 64; ++i) {
-                const uint32_t wd = braw[i >> 1];
-                const float bv = __half2float(__ushort_as_half((unsigned short)((i & 1) ? (wd >> 16) : (wd & 0xFFFFu))));
-                sr[i >> 5][i & 31] = __float_as_uint(fmaf(__uint_as_float(sr[i >> 5][i & 31]), c, bv * LOG2E_F));
-              }
-            } else if (bpacked) {
-#pragma unroll
-              for (int i = 0; i < 64; ++i) {
-                const uint32_t wd = braw[i >> 1];
-                const float bv = __uint_as_float((i & 1) ? (wd & 0xFFFF0000u) : (wd << 16));
-                sr[i >> 5][i & 31] = __float_as_uint(fmaf(__uint_as_float(sr[i >> 5][i & 31]), c, bv * LOG2E_F));
-              }
-            } else {
-#pragma unroll
-              for (int i = 0; i < 64; ++i)
-                sr[i >> 5][i & 31] = __float_as_uint(
-                    fmaf(__uint_as_float(sr[i >> 5][i & 31]), c, __uint_as_float(braw[i]) * LOG2E_F));
-            }
-          }
+          if constexpr (BIAS) add_bias_row(p, c, braw, bpacked, sr);
           // Visible keys of this row within the tile: [v_lo, v_hi] relative to k0.
           if (live) {
             v_hi = (int)min((long long)BK - 1, min((long long)w.Lk - 1, k_vis_hi) - k0);
