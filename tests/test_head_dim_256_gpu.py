@@ -119,6 +119,16 @@ def test_d256_forward_bias_parity(kind, dtype):
     _check_fwd(case, o, lse)
 
 
+def test_d256_forward_f16_io_with_bias():
+    """fp16 io and an fp16 bias: the one forward variant the cases above leave out."""
+    from test_parity_gpu import _check_fwd, _gpu_fwd
+    w = CASES["d256_dense_gqa"]
+    case = make_case(w, bias=(w.B, torch.float16), io=torch.float16)
+    o, lse = _gpu_fwd(case, to_device(case))
+    assert o.dtype == torch.float16
+    _check_fwd(case, o, lse)
+
+
 @pytest.mark.parametrize("name", ["d256_br_causal_long_kv", "d256_padded_window"])
 def test_d256_forward_f16_parity(name):
     from test_parity_gpu import _check_fwd, _gpu_fwd
